@@ -1,0 +1,250 @@
+"""CPU oracle for the NVFP4 hot path (numpy front end over liboracle.so).
+
+TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and
+bench.py's CPU-baseline / reference legs may import this package.  It shares
+no code with the CUDA path (nvfp4_block_scaled_30_b300), and neither imports
+the other.  Every function follows a passage of the pages named in
+nvfp4_oracle.c; the readings taken where the pages are silent are listed
+there and in the design doc.
+
+Layouts: activations/weights are BF16 bit patterns (uint16) [rows, K];
+codes are uint8 [rows, K/2] with the even element in the low nibble; scales
+are E4M3 bytes [rows, K/16] row-major; the second-level scale is one float32
+(per-tensor mode) or binary16 bits [rows, K/256] (macro mode).
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_LIB = None
+
+_u8 = np.ctypeslib.ndpointer(np.uint8, flags="C_CONTIGUOUS")
+_u16 = np.ctypeslib.ndpointer(np.uint16, flags="C_CONTIGUOUS")
+_i32 = np.ctypeslib.ndpointer(np.int32, flags="C_CONTIGUOUS")
+_i64 = np.ctypeslib.ndpointer(np.int64, flags="C_CONTIGUOUS")
+_f32 = np.ctypeslib.ndpointer(np.float32, flags="C_CONTIGUOUS")
+_f64 = np.ctypeslib.ndpointer(np.float64, flags="C_CONTIGUOUS")
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+_VP = ctypes.c_void_p
+
+ORC_OK, ORC_ERR_ARG, ORC_ERR_NONFINITE = 0, 1, 3
+
+
+class OracleError(ValueError):
+    pass
+
+
+def lib():
+    global _LIB
+    if _LIB is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        L.orc_e2m1_value.restype = ctypes.c_double
+        L.orc_e2m1_value.argtypes = [ctypes.c_uint32]
+        L.orc_e2m1_encode.restype = ctypes.c_uint32
+        L.orc_e2m1_encode.argtypes = [ctypes.c_float]
+        L.orc_e4m3_value.restype = ctypes.c_double
+        L.orc_e4m3_value.argtypes = [ctypes.c_uint32]
+        L.orc_e4m3_encode.restype = ctypes.c_uint32
+        L.orc_e4m3_encode.argtypes = [ctypes.c_float]
+        L.orc_fp16_value.restype = ctypes.c_double
+        L.orc_fp16_value.argtypes = [ctypes.c_uint32]
+        L.orc_fp16_encode.restype = ctypes.c_uint32
+        L.orc_fp16_encode.argtypes = [ctypes.c_float]
+        L.orc_bf16_value.restype = ctypes.c_float
+        L.orc_bf16_value.argtypes = [ctypes.c_uint32]
+        L.orc_nvfp4_encode.restype = ctypes.c_int
+        L.orc_nvfp4_encode.argtypes = [_u16, _I64, _I64, _I64, _u8, _u8, _f32]
+        L.orc_nvfp4_encode_macro.restype = ctypes.c_int
+        L.orc_nvfp4_encode_macro.argtypes = [_u16, _I64, _I64, _I64, _u8, _u8, _u16]
+        L.orc_fp8_token_encode.restype = ctypes.c_int
+        L.orc_fp8_token_encode.argtypes = [_u16, _I64, _I64, _I64, _u8, _f32]
+        L.orc_nvfp4_dequant.restype = None
+        L.orc_nvfp4_dequant.argtypes = [_u8, _u8, _F, _I64, _I64, _f64]
+        L.orc_nvfp4_dequant_macro.restype = None
+        L.orc_nvfp4_dequant_macro.argtypes = [_u8, _u8, _u16, _I64, _I64, _f64]
+        L.orc_gemm_w4a4.restype = None
+        L.orc_gemm_w4a4.argtypes = [_u8, _u8, _F, _u8, _u8, _F, _I64, _I64, _I64,
+                                    _VP, _I64, _f64]
+        L.orc_gemm_w4a4_macro.restype = None
+        L.orc_gemm_w4a4_macro.argtypes = [_u8, _u8, _u16, _u8, _u8, _u16, _I64, _I64,
+                                          _I64, _VP, _I64, _f64]
+        L.orc_gemm_w4a8.restype = None
+        L.orc_gemm_w4a8.argtypes = [_u8, _f32, _u8, _u8, _F, _I64, _I64, _I64, _VP,
+                                    _I64, _f64]
+        L.orc_gemm_grouped_w4a4.restype = None
+        L.orc_gemm_grouped_w4a4.argtypes = [_u8, _u8, _F, _VP, _i64, _I64, _u8, _u8,
+                                            _f32, _I64, _I64, _f64]
+        _LIB = L
+    return _LIB
+
+
+def _c(a, dt):
+    return np.ascontiguousarray(a, dtype=dt)
+
+
+def _check(rc):
+    if rc == ORC_ERR_NONFINITE:
+        raise OracleError("non-finite input")
+    if rc != ORC_OK:
+        raise OracleError(f"invalid argument (status {rc})")
+
+
+# ---- element formats --------------------------------------------------------
+
+def e2m1_value(code):
+    return lib().orc_e2m1_value(int(code))
+
+
+def e2m1_encode(q):
+    return lib().orc_e2m1_encode(float(q))
+
+
+def e4m3_value(code):
+    return lib().orc_e4m3_value(int(code))
+
+
+def e4m3_encode(u):
+    return lib().orc_e4m3_encode(float(u))
+
+
+def fp16_value(h):
+    return lib().orc_fp16_value(int(h))
+
+
+def fp16_encode(v):
+    return lib().orc_fp16_encode(float(v))
+
+
+def bf16_value(b):
+    return lib().orc_bf16_value(int(b))
+
+
+# ---- encoders -----------------------------------------------------------------
+
+def nvfp4_encode(x_bf16):
+    """Per-tensor NVFP4 encode of a BF16-bit array [R, K].
+
+    Returns (codes uint8 [R, K/2], scales uint8 [R, K/16], s_g float32)."""
+    x = _c(x_bf16, np.uint16)
+    R, K = x.shape
+    codes = np.zeros((R, K // 2), np.uint8)
+    scales = np.zeros((R, K // 16), np.uint8)
+    sg = np.zeros(1, np.float32)
+    _check(lib().orc_nvfp4_encode(x, R, K, K, codes, scales, sg))
+    return codes, scales, np.float32(sg[0])
+
+
+def nvfp4_encode_macro(x_bf16):
+    """Macro-mode NVFP4 encode: returns (codes, scales, macro fp16 bits [R, K/256])."""
+    x = _c(x_bf16, np.uint16)
+    R, K = x.shape
+    codes = np.zeros((R, K // 2), np.uint8)
+    scales = np.zeros((R, K // 16), np.uint8)
+    macro = np.zeros((R, max(K // 256, 0)), np.uint16)
+    _check(lib().orc_nvfp4_encode_macro(x, R, K, K, codes, scales, macro))
+    return codes, scales, macro
+
+
+def fp8_token_encode(x_bf16):
+    """Per-token FP8 encode: returns (E4M3 bytes [R, K], s_t float32 [R])."""
+    x = _c(x_bf16, np.uint16)
+    R, K = x.shape
+    a = np.zeros((R, K), np.uint8)
+    st = np.zeros(R, np.float32)
+    _check(lib().orc_fp8_token_encode(x, R, K, K, a, st))
+    return a, st
+
+
+def nvfp4_dequant(codes, scales, s_g):
+    codes, scales = _c(codes, np.uint8), _c(scales, np.uint8)
+    R, K = codes.shape[0], codes.shape[1] * 2
+    out = np.zeros((R, K), np.float64)
+    lib().orc_nvfp4_dequant(codes, scales, float(s_g), R, K, out)
+    return out
+
+
+def nvfp4_dequant_macro(codes, scales, macro):
+    codes, scales, macro = _c(codes, np.uint8), _c(scales, np.uint8), _c(macro, np.uint16)
+    R, K = codes.shape[0], codes.shape[1] * 2
+    out = np.zeros((R, K), np.float64)
+    lib().orc_nvfp4_dequant_macro(codes, scales, macro, R, K, out)
+    return out
+
+
+# ---- contractions -------------------------------------------------------------
+
+def _rows(rows, M):
+    if rows is None:
+        return None, M
+    r = _c(rows, np.int64)
+    if r.size and (r.min() < 0 or r.max() >= M):
+        raise OracleError("row index out of range")
+    return r, r.size
+
+
+def gemm_w4a4(a, w, rows=None):
+    """a, w: (codes, scales, s_g) tuples.  Returns float64 Y [len(rows) or M, N]."""
+    ac, as_, asg = _c(a[0], np.uint8), _c(a[1], np.uint8), float(a[2])
+    wc, ws, wsg = _c(w[0], np.uint8), _c(w[1], np.uint8), float(w[2])
+    M, N, K = ac.shape[0], wc.shape[0], ac.shape[1] * 2
+    if wc.shape[1] * 2 != K:
+        raise OracleError("K mismatch")
+    r, nr = _rows(rows, M)
+    Y = np.zeros((nr, N), np.float64)
+    lib().orc_gemm_w4a4(ac, as_, asg, wc, ws, wsg, M, N, K,
+                        None if r is None else r.ctypes.data, nr, Y)
+    return Y
+
+
+def gemm_w4a4_macro(a, w, rows=None):
+    """a, w: (codes, scales, macro) tuples in macro mode."""
+    ac, as_, am = _c(a[0], np.uint8), _c(a[1], np.uint8), _c(a[2], np.uint16)
+    wc, ws, wm = _c(w[0], np.uint8), _c(w[1], np.uint8), _c(w[2], np.uint16)
+    M, N, K = ac.shape[0], wc.shape[0], ac.shape[1] * 2
+    r, nr = _rows(rows, M)
+    Y = np.zeros((nr, N), np.float64)
+    lib().orc_gemm_w4a4_macro(ac, as_, am, wc, ws, wm, M, N, K,
+                              None if r is None else r.ctypes.data, nr, Y)
+    return Y
+
+
+def gemm_w4a8(a_fp8, s_t, w, rows=None):
+    a, st = _c(a_fp8, np.uint8), _c(s_t, np.float32)
+    wc, ws, wsg = _c(w[0], np.uint8), _c(w[1], np.uint8), float(w[2])
+    M, K, N = a.shape[0], a.shape[1], wc.shape[0]
+    r, nr = _rows(rows, M)
+    Y = np.zeros((nr, N), np.float64)
+    lib().orc_gemm_w4a8(a, st, wc, ws, wsg, M, N, K,
+                        None if r is None else r.ctypes.data, nr, Y)
+    return Y
+
+
+def gemm_grouped_w4a4(a, row_idx, offsets, w_codes, w_scales, w_sg):
+    """a: (codes, scales, s_g); row_idx int32 [T] or None; offsets int64 [E+1];
+    w_codes uint8 [E, N, K/2]; w_scales uint8 [E, N, K/16]; w_sg float32 [E]."""
+    ac, as_, asg = _c(a[0], np.uint8), _c(a[1], np.uint8), float(a[2])
+    off = _c(offsets, np.int64)
+    wc, ws, wsg = _c(w_codes, np.uint8), _c(w_scales, np.uint8), _c(w_sg, np.float32)
+    E, N, K = wc.shape[0], wc.shape[1], wc.shape[2] * 2
+    T = int(off[-1])
+    ridx = None
+    if row_idx is not None:
+        ridx = _c(row_idx, np.int32)
+        if ridx.size != T or (T and (ridx.min() < 0 or ridx.max() >= ac.shape[0])):
+            raise OracleError("bad row_idx")
+    elif T > ac.shape[0]:
+        raise OracleError("offsets exceed activation rows")
+    Y = np.zeros((T, N), np.float64)
+    lib().orc_gemm_grouped_w4a4(ac, as_, asg, None if ridx is None else ridx.ctypes.data,
+                                off, E, wc, ws, wsg, N, K, Y)
+    return Y
+
+
+def threads():
+    """OpenMP threads the oracle's parallel loops use."""
+    return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))

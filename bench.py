@@ -1,0 +1,476 @@
+#!/usr/bin/env python
+"""Benchmark of the NVFP4 W4A4 inference-GEMM hot path on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode|prefill|policy|moe] [--no-extras]
+
+Prints ONE JSON line.  The headline workload is the decode-shape MLP up
+projection (X [8, 8192] BF16 against NVFP4 weights [28672, 8192]); a step
+quantises the BF16 activations (global amax + block encode) and runs the
+block-scaled FP4 GEMM, i.e. one pass of the whole W4A4 path.  The metric is
+the memory-bound one, GB/s of algorithmic bytes, with the GEMM kernel's
+roofline fraction against the measured HBM bandwidth.  The prefill shape
+(TFLOP/s against the FP4 tensor peak), the per-layer-policy stack and the
+MoE grouped GEMM are measured in the same run under "workloads".
+
+Inputs are seeded synthetic data (synth/); weights rotate over 4 copies
+(528 MB > the 126 MB L2) so every step streams them from HBM.  Multi-GPU
+runs (torchrun) are independent replicas: each rank runs the same workload
+on its own GPU and `value` sums them (weak scaling).
+
+--impl reference times the CPU oracle (oracle/, test infrastructure) on a
+bounded sample of the same workload on this machine's host cores.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25     # dense tensor-core ratio of B300
+FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6400.0, 1800.0
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1400.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks sampler
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={','.join(self.FIELDS)}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        sm, mx, reasons = [], [], set()
+        for t, line in self.lines:
+            if not (t0 - 0.15 <= t <= t1 + 0.15):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(self.NAMES, parts[2:]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU workloads
+class Ctx:
+    def __init__(self, torch, nv, dev):
+        self.torch, self.nv, self.dev = torch, nv, dev
+
+    def bf16(self, bits):
+        t = self.torch
+        return t.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(self.dev).view(t.bfloat16)
+
+    def quantized_weights(self, bits, copies=1):
+        t, nv = self.torch, self.nv
+        w = nv.quantize(self.bf16(bits))
+        out = [w]
+        for _ in range(copies - 1):
+            out.append(nv.NVFP4Tensor(w.codes.clone(), w.scales.clone(), w.second.clone(), w.rows, w.K))
+        t.cuda.synchronize()
+        return out
+
+    def time(self, fn, steps, warmup):
+        """Mean ms per call of fn(i) over `steps` calls after `warmup` calls,
+        CUDA events on the current stream."""
+        t = self.torch
+        for i in range(warmup):
+            fn(i)
+        t.cuda.synchronize()
+        s, e = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+        s.record()
+        for i in range(steps):
+            fn(warmup + i)
+        e.record()
+        t.cuda.synchronize()
+        return s.elapsed_time(e) / steps
+
+
+def nvfp4_bytes(rows, K):
+    return rows * K // 2 + rows * K // 16
+
+
+def workload_decode(c, M, steps, warmup, rot=4, with_e2e=False, peaks_=None):
+    t, nv = c.torch, c.nv
+    N, K = 28672, 8192
+    ws = synth.weights(2, 1, N, K)
+    W = c.quantized_weights(ws, copies=rot)
+    del ws
+    xb = synth.activations(2, 0, M, K, 0.005, 100.0)
+    x = c.bf16(xb)
+    y = t.empty((M, N), dtype=t.bfloat16, device=c.dev)
+    work = nv.Workspace(nv.workspace_size(nv.OP_GEMM, M, N, K))
+    a_q = nv.quantize(x, ws=work)
+
+    # algorithmic bytes: W (codes + scales), X read, quantised X write + read, Y write
+    w_bytes = nvfp4_bytes(N, K)
+    step_bytes = w_bytes + M * K * 2 + 2 * nvfp4_bytes(M, K) + M * N * 2
+    gemm_bytes = w_bytes + nvfp4_bytes(M, K) + M * N * 2
+
+    def step(i):
+        nv.gemm(W[i % rot], x=x, y=y, ws=work)
+
+    def gemm_only(i):
+        nv.gemm(W[i % rot], a_q=a_q, y=y, ws=work)
+
+    ms = c.time(step, steps, warmup)
+    gms = c.time(gemm_only, steps, warmup)
+    st = work.status()
+    res = {"ms": ms, "gemm_ms": gms, "step_bytes": step_bytes, "gemm_bytes": gemm_bytes,
+           "value": step_bytes / (ms * 1e-3) / 1e9, "launches_per_step": 3, "device_status": st}
+    if with_e2e:
+        hx = t.from_numpy(xb.view(np.int16)).pin_memory()
+        hy = t.empty((M, N), dtype=t.int16).pin_memory()
+        xd = t.empty((M, K), dtype=t.int16, device=c.dev)
+
+        def e2e(i):
+            xd.copy_(hx, non_blocking=True)
+            nv.gemm(W[i % rot], x=xd.view(t.bfloat16), y=y, ws=work)
+            hy.copy_(y.view(t.int16), non_blocking=True)
+
+        ems = c.time(e2e, steps, warmup)
+        res["e2e"] = {"value": step_bytes / (ems * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ems,
+                      "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": M * N * 2}
+    del W
+    return res
+
+
+def workload_prefill(c, N, steps, warmup, rot=2):
+    t, nv = c.torch, c.nv
+    M, K = 4096, 8192
+    W = c.quantized_weights(synth.weights(3, 1, N, K), copies=rot)
+    x = c.bf16(synth.activations(3, 0, M, K, 0.005, 100.0))
+    y = t.empty((M, N), dtype=t.bfloat16, device=c.dev)
+    work = nv.Workspace(nv.workspace_size(nv.OP_GEMM, M, N, K))
+    a_q = nv.quantize(x, ws=work)
+    flops = 2.0 * M * N * K
+
+    def step(i):
+        nv.gemm(W[i % rot], x=x, y=y, ws=work)
+
+    def gemm_only(i):
+        nv.gemm(W[i % rot], a_q=a_q, y=y, ws=work)
+
+    ms = c.time(step, steps, warmup)
+    gms = c.time(gemm_only, steps, warmup)
+    qbytes = M * K * 2 + nvfp4_bytes(M, K)
+
+    def quant_only(i):
+        nv.quantize(x, out=a_q, ws=work)
+
+    qms = c.time(quant_only, steps, warmup)
+    st = work.status()
+    del W
+    return {"ms": ms, "gemm_ms": gms, "flops": flops, "value": flops / (ms * 1e-3) / 1e12,
+            "gemm_tflops": flops / (gms * 1e-3) / 1e12, "quant_ms": qms, "quant_bytes": qbytes,
+            "quant_gbs": qbytes / (qms * 1e-3) / 1e9, "device_status": st}
+
+
+def workload_policy(c, steps, warmup, policy):
+    t, nv = c.torch, c.nv
+    cfg = synth.CONFIGS[4]
+    M, N, K, L = cfg["M"], cfg["N"], cfg["K"], cfg["layers"]
+    Ws = [c.quantized_weights(synth.weights(4, 100 + i, N, K))[0] for i in range(L)]
+    flags = synth.sensitive_flags(L, cfg["n_sensitive"])
+    x = c.bf16(synth.activations(4, 0, M, K, cfg["outlier_frac"], cfg["outlier_factor"]))
+    ys = [t.empty((M, N), dtype=t.bfloat16, device=c.dev) for _ in range(2)]
+    work = nv.Workspace(nv.workspace_size(nv.OP_GEMM, M, N, K))
+
+    def step(i):
+        cur = x
+        for li in range(L):
+            out = ys[li % 2]
+            nv.gemm(Ws[li], x=cur, y=out, policy=policy, sensitive=int(flags[li]), ws=work)
+            cur = out
+
+    ms = c.time(step, steps, warmup)
+    flops = 2.0 * M * N * K * L
+    routes = [nv.policy_route(policy, int(f)) for f in flags]
+    return {"ms": ms, "flops": flops, "value": flops / (ms * 1e-3) / 1e12, "routes": routes,
+            "device_status": work.status()}
+
+
+def workload_moe(c, steps, warmup):
+    t, nv = c.torch, c.nv
+    cfg = synth.CONFIGS[5]
+    T, H, E, I = cfg["T"], cfg["H"], cfg["E"], cfg["inter"]
+    row_idx, offsets, counts, _ = synth.moe_routing()
+    R = int(offsets[-1])
+
+    def stacked(N, K, tid):
+        parts = [c.quantized_weights(synth.weights(5, tid * 1000 + e, N, K))[0] for e in range(E)]
+        return nv.NVFP4Tensor(t.cat([p.codes for p in parts]), t.cat([p.scales for p in parts]),
+                              t.cat([p.second for p in parts]), E * N, K)
+
+    w_up, w_dn = stacked(I, H, 1), stacked(H, I, 2)
+    x = c.bf16(synth.activations(5, 0, T, H, cfg["outlier_frac"], cfg["outlier_factor"]))
+    xd = c.bf16(synth.activations(5, 2, R, I, cfg["outlier_frac"], cfg["outlier_factor"]))
+    off = t.from_numpy(offsets).to(c.dev)
+    ridx = t.from_numpy(row_idx).to(c.dev)
+    y_up = t.empty((R, I), dtype=t.bfloat16, device=c.dev)
+    y_dn = t.empty((R, H), dtype=t.bfloat16, device=c.dev)
+    work = nv.Workspace(nv.workspace_size(nv.OP_QUANTIZE, R, 0, max(H, I)))
+    a_up = nv.quantize(x, ws=work)
+    a_dn = nv.quantize(xd, ws=work)
+
+    def step(i):
+        nv.quantize(x, out=a_up, ws=work)
+        nv.grouped_gemm(a_up, off, w_up, I, R, row_idx=ridx, y=y_up, ws=work)
+        nv.quantize(xd, out=a_dn, ws=work)
+        nv.grouped_gemm(a_dn, off, w_dn, H, R, y=y_dn, ws=work)
+
+    ms = c.time(step, steps, warmup)
+    wbytes = 2 * E * nvfp4_bytes(I, H)
+    step_bytes = (wbytes + T * H * 2 + 2 * nvfp4_bytes(T, H) + R * I * 2          # up
+                  + R * I * 2 + 2 * nvfp4_bytes(R, I) + R * H * 2)                 # down
+    flops = 2.0 * R * I * H * 2
+    return {"ms": ms, "bytes": step_bytes, "value": step_bytes / (ms * 1e-3) / 1e9,
+            "tflops": flops / (ms * 1e-3) / 1e12, "counts_min": int(counts.min()),
+            "counts_max": int(counts.max()), "device_status": work.status()}
+
+
+# ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
+def oracle_decode_sample(M=8, n_rows=2048, reps=1):
+    """The oracle's decode step (encode X, dequantise-and-contract in FP64)
+    on the first n_rows of the 28672 weight rows; weights encoded by the
+    oracle itself beforehand (offline, untimed).  Returns (GB/s, seconds, bytes)."""
+    import oracle
+    K = 8192
+    wb = synth.weights(2, 1, 28672, K)[:n_rows]
+    wq = oracle.nvfp4_encode(wb)
+    xb = synth.activations(2, 0, M, K, 0.005, 100.0)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        aq = oracle.nvfp4_encode(xb)
+        oracle.gemm_w4a4(aq, wq)
+    dt = (time.perf_counter() - t0) / reps
+    nbytes = nvfp4_bytes(n_rows, K) + M * K * 2 + 2 * nvfp4_bytes(M, K) + M * n_rows * 2
+    return nbytes / dt / 1e9, dt, nbytes
+
+
+def cpu_cores():
+    try:
+        import oracle
+        return oracle.threads()
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["decode", "prefill", "policy", "moe"], default="decode")
+    ap.add_argument("--no-extras", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    hbm, bf16, bf16_sus, peak_src = peaks()
+    fp4_peak = bf16 * NOMINAL_FP4_OVER_BF16
+    metric = "NVFP4 W4A4 GEMM TFLOPS & % dense FP4 peak (prefill); GB/s & % HBM (decode)"
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        n_rows = 2048
+        rates = []
+        for _ in range(args.warmup):
+            oracle_decode_sample(n_rows=n_rows)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            r, dt, nb = oracle_decode_sample(n_rows=n_rows)
+            rates.append(r)
+        total = time.perf_counter() - t0
+        v = float(np.mean(rates))
+        cores = cpu_cores()
+        line = {"impl": "reference", "metric": metric, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / max(args.steps, 1),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic",
+                "config": {"workload": "decode_mlp_up M=8 N=28672 K=8192 (sample: first 2048 weight rows)"},
+                "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                 "sample": f"decode step on {n_rows} of 28672 weight rows per step"},
+                "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    import torch
+    import nvfp4_block_scaled_30_b300 as nv
+    nv.lib()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (there is no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    c = Ctx(torch, nv, dev)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.4)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    barrier()
+    t_start = time.time()
+    if args.workload == "decode":
+        r = workload_decode(c, 8, args.steps, args.warmup, with_e2e=True)
+        unit, value_rank = "GB/s", r["value"]
+    elif args.workload == "prefill":
+        r = workload_prefill(c, 28672, args.steps, args.warmup)
+        unit, value_rank = "TFLOP/s", r["value"]
+    elif args.workload == "policy":
+        r = workload_policy(c, args.steps, args.warmup, nv.POLICY_AUTO)
+        unit, value_rank = "TFLOP/s", r["value"]
+    else:
+        r = workload_moe(c, args.steps, args.warmup)
+        unit, value_rank = "GB/s", r["value"]
+    barrier()
+    t_end = time.time()
+    ms = r["ms"]
+    if dist is not None:
+        tm = torch.tensor([ms], device=dev)
+        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+        ms = float(tm.item())
+    value = value_rank * r["ms"] / ms * world   # units of all ranks over the slowest rank's time
+
+    clocks = sampler.summary(t_start, t_end)
+
+    extras = {}
+    if not args.no_extras and rank == 0:
+        es = max(20, min(args.steps, 200))
+        for M in (1, 16):
+            d = workload_decode(c, M, es, args.warmup)
+            extras[f"decode_m{M}"] = {"value": d["value"], "unit": "GB/s", "ms": d["ms"],
+                                      "gemm_gbs": d["gemm_bytes"] / (d["gemm_ms"] * 1e-3) / 1e9,
+                                      "gemm_frac_hbm": d["gemm_bytes"] / (d["gemm_ms"] * 1e-3) / 1e9 / hbm}
+        if args.workload != "prefill":
+            for N in (8192, 28672):
+                p = workload_prefill(c, N, min(es, 50), args.warmup)
+                extras[f"prefill_n{N}"] = {"value": p["value"], "unit": "TFLOP/s", "ms": p["ms"],
+                                           "gemm_tflops": p["gemm_tflops"],
+                                           "gemm_frac_fp4": p["gemm_tflops"] / fp4_peak,
+                                           "quant_gbs": p["quant_gbs"], "quant_frac_hbm": p["quant_gbs"] / hbm}
+        for pol, name in ((nv.POLICY_AUTO, "auto"), (nv.POLICY_Q4, "q4"), (nv.POLICY_Q8, "q8")):
+            q = workload_policy(c, min(es, 20), 2, pol)
+            extras[f"policy_stack_{name}"] = {"value": q["value"], "unit": "TFLOP/s", "ms": q["ms"],
+                                              "routes": q["routes"]}
+        mo = workload_moe(c, min(es, 50), 2)
+        extras["moe_grouped"] = {"value": mo["value"], "unit": "GB/s", "ms": mo["ms"], "tflops": mo["tflops"],
+                                 "frac_hbm": mo["value"] / hbm, "counts": [mo["counts_min"], mo["counts_max"]]}
+
+    cpu = None
+    if rank == 0 and world == 1:
+        v, dt, nb = oracle_decode_sample()
+        cpu = {"value": v, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": "decode step (encode X, FP64 contraction) on 2048 of 28672 weight rows"}
+
+    if args.workload == "decode":
+        ach = r["gemm_bytes"] / (r["gemm_ms"] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "traffic": None, "kernel": "w4a4_kernel<16> (stream-K, operands swapped)",
+                "peak_source": f"{peak_src} hbm_gbs"}
+        cfg = {"workload": "decode_mlp_up: X[8,8192] bf16 -> NVFP4, W NVFP4[28672,8192], Y bf16",
+               "global_batch": 8, "l2": "4 rotating weight copies (528 MB > 126 MB L2)"}
+    elif args.workload == "prefill":
+        ach = r["gemm_tflops"]
+        roof = {"bound": "tensor", "achieved": ach, "peak": fp4_peak, "unit": "TFLOP/s", "frac": ach / fp4_peak,
+                "traffic": None, "kernel": "w4a4_kernel<256>",
+                "peak_source": f"{peak_src} bf16_tflops x {NOMINAL_FP4_OVER_BF16:g} (nominal FP4/BF16)"}
+        cfg = {"workload": "prefill_proj: X[4096,8192], W NVFP4[28672,8192]", "global_batch": 4096,
+               "l2": "inputs larger than L2 (X 67 MB + 2 rotating W copies of 132 MB)"}
+    elif args.workload == "policy":
+        roof = None
+        cfg = {"workload": "policy_stack AUTO: 8 x [2048,4096]x[4096,4096]^T, 2 W4A8 layers", "global_batch": 2048}
+    else:
+        roof = None
+        cfg = {"workload": "moe_grouped: 2048 tokens, 128 experts top-8, up [768,2048] + down [2048,768]",
+               "global_batch": 2048}
+
+    if rank == 0:
+        line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "fp4 (e2m1 x e4m3-scaled, fp32 accumulate)", "data": "synthetic",
+                "config": cfg, "gpu_launches": r.get("launches_per_step", 0) * args.steps,
+                "clocks": clocks, "device_status": r.get("device_status")}
+        if roof is not None:
+            line["roofline"] = roof
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        if "e2e" in r:
+            line["e2e"] = r["e2e"]
+        if extras:
+            line["workloads"] = extras
+        print(json.dumps(line))
+    sampler.stop()
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

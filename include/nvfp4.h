@@ -1,0 +1,237 @@
+/*
+ * nvfp4.h: C ABI of libnvfp4, the NVFP4 inference-GEMM hot path for
+ * B300 (sm_103a).
+ *
+ * The operations follow these pages (cited by title and section):
+ *  [TRT] "NVIDIA Ships TensorRT-LLM 0.16: Native FP4 Quantization for
+ *        Blackwell B200", section "The Mathematical Breakthrough of
+ *        Microscopic FP4 Scaling": E2M1 elements (1 sign, 2 exponent,
+ *        1 mantissa bit); item 2 "Two-Level Block Scaling" (one FP8 scale per
+ *        16 consecutive elements; an FP16 macro-scale per 16 micro-vectors);
+ *        item 3 "Hardware-Fused Dequantization" (tensor cores apply the
+ *        scales before the dot products).
+ *  [LCP] "llama.cpp Put Precision Policy Inside the Model. That Matters More
+ *        Than W4A4": section "One model can need more than one precision"
+ *        (native W4A4 path; W4A8 for marked tensors; dense and MoE) and
+ *        section "Local inference is becoming a policy engine" (q4 forces
+ *        W4A4, q8 forces W4A8, auto follows per-tensor metadata).
+ *  [ADA] "AdaLLM Breakthrough: First NVFP4-Only Inference Engine for RTX 4090
+ *        Unveiled": fail fast, no silent fallback to a slower precision.
+ *
+ * Conventions shared by every entry point:
+ *  - All data pointers are DEVICE pointers owned by the caller.  The library
+ *    allocates no memory on these paths; scratch lives in a caller-provided
+ *    workspace (see nvfp4_workspace_size / nvfp4_workspace_init).
+ *  - Every call is asynchronous and stream-ordered on `stream` (a
+ *    cudaStream_t; NULL is the legacy default stream).
+ *  - Argument checks run on the host before anything is enqueued; a call
+ *    that returns an error has enqueued no work ("fail fast", [ADA]).
+ *  - Errors found on the device (non-finite input, a bounded wait that gave
+ *    up) are OR-ed into a sticky status word in the workspace; read it with
+ *    nvfp4_device_status.  There is no CPU or lower-precision fallback.
+ *  - The entry points are not re-entrant on one workspace: two calls that
+ *    overlap on the GPU must use different workspaces.
+ */
+#ifndef NVFP4_H
+#define NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *nvfp4_stream_t; /* same type as cudaStream_t */
+
+typedef enum nvfp4_status {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID_ARG = 1,       /* null pointer, bad enum, bad stride or alignment */
+    NVFP4_ERR_UNSUPPORTED_SHAPE = 2, /* K, N or M outside what the kernels take */
+    NVFP4_ERR_NONFINITE_INPUT = 3,   /* device: an input element was Inf or NaN */
+    NVFP4_ERR_TIMEOUT = 4,           /* device: a bounded wait inside a kernel gave up */
+    NVFP4_ERR_CUDA = 5,              /* a CUDA runtime or driver call failed */
+    NVFP4_ERR_WORKSPACE = 6,         /* workspace missing, misaligned or too small */
+    NVFP4_ERR_UNSUPPORTED = 7        /* valid request the library does not implement */
+} nvfp4_status;
+
+/* Per-call precision policy, [LCP] "Local inference is becoming a policy
+ * engine": Q4 forces W4A4, Q8 forces W4A8, AUTO follows the layer's
+ * `sensitive` flag (W4A8 when set, W4A4 otherwise). */
+typedef enum nvfp4_policy {
+    NVFP4_POLICY_AUTO = 0,
+    NVFP4_POLICY_Q4 = 1,
+    NVFP4_POLICY_Q8 = 2
+} nvfp4_policy;
+
+/* Second-level scale, [TRT] item 2.  TENSOR_FP32: one float per tensor,
+ * amax / (6 * 448).  MACRO_FP16: one binary16 per 256 consecutive elements of
+ * a row (16 micro-blocks), FP16(amax_256 / 2688), saturating at 65504. */
+typedef enum nvfp4_scale_mode {
+    NVFP4_SCALE_TENSOR_FP32 = 0,
+    NVFP4_SCALE_MACRO_FP16 = 1
+} nvfp4_scale_mode;
+
+/* Layout of the E4M3 micro-scale bytes.
+ *  ROW_MAJOR: byte [r][b] at r * (K/16) + b.
+ *  MMA_TILED: the layout the tensor cores read.  Rows are padded to a
+ *    multiple of 128 (padding bytes are written as 0) and K to a multiple
+ *    of 64.  Scale b of row r lives in the 512-byte atom
+ *    (r / 128) * (K/64) + (b / 4), at byte (r % 32) * 16 + ((r % 128) / 32) * 4
+ *    + (b % 4) of that atom. */
+typedef enum nvfp4_scale_layout {
+    NVFP4_LAYOUT_ROW_MAJOR = 0,
+    NVFP4_LAYOUT_MMA_TILED = 1
+} nvfp4_scale_layout;
+
+typedef enum nvfp4_out_dtype {
+    NVFP4_OUT_BF16 = 0, /* round to nearest even */
+    NVFP4_OUT_FP32 = 1
+} nvfp4_out_dtype;
+
+/* An NVFP4 tensor [rows, K] (activations [M, K] or weights [N, K]).
+ *  codes : uint8 [rows][K/2]; element 2j in the low nibble of byte j, 2j+1
+ *          in the high nibble; each nibble is an E2M1 code (bit 3 = sign).
+ *          16-byte aligned.
+ *  scales: E4M3 bytes, `layout` as above, 16-byte aligned.
+ *  second: TENSOR_FP32 -> float[1] (for the stacked expert weights of
+ *          nvfp4_grouped_gemm, float[E]); MACRO_FP16 -> binary16 [rows][K/256].
+ *  Dequantised value: E2M1(code) * E4M3(scale) * second. */
+typedef struct nvfp4_tensor {
+    void *codes;
+    void *scales;
+    void *second;
+    int64_t rows;
+    int64_t K;
+    int32_t mode;   /* nvfp4_scale_mode */
+    int32_t layout; /* nvfp4_scale_layout */
+} nvfp4_tensor;
+
+/* Operation ids for nvfp4_workspace_size. */
+typedef enum nvfp4_op {
+    NVFP4_OP_QUANTIZE = 0,     /* M = rows, K */
+    NVFP4_OP_QUANTIZE_FP8 = 1, /* M = rows, K */
+    NVFP4_OP_GEMM = 2,         /* M, N, K; covers both routes and on-the-fly quantisation */
+    NVFP4_OP_W4A8_GEMM = 3,    /* M, N, K */
+    NVFP4_OP_GROUPED_GEMM = 4  /* M = total routed rows, N, K, E experts */
+} nvfp4_op;
+
+/* ---- sizing and workspace ------------------------------------------------ */
+
+/* Bytes of the E4M3 scale buffer of a [rows, K] tensor in `layout`.
+ * Errors: INVALID_ARG for a null `bytes`, negative sizes or a bad layout;
+ * UNSUPPORTED_SHAPE when K % 16 != 0 (row-major) or K % 64 != 0 (tiled). */
+nvfp4_status nvfp4_scale_bytes(int64_t rows, int64_t K, int32_t layout, size_t *bytes);
+
+/* Workspace bytes an operation needs.  Unused sizes may be 0.  The result
+ * includes a 256-byte header that holds the sticky device status word. */
+nvfp4_status nvfp4_workspace_size(int32_t op, int64_t M, int64_t N, int64_t K, int32_t E,
+                                  size_t *bytes);
+
+/* Zeroes a workspace (status word and the stream-K accumulator, which the
+ * GEMM kernels leave zeroed after every call) on `stream`.  Call once after
+ * allocating it, and again after a TIMEOUT status (an aborted kernel may leave
+ * partial sums behind).  The status word stays sticky between calls.
+ * `ws` must be 256-byte aligned. */
+nvfp4_status nvfp4_workspace_init(void *ws, size_t ws_bytes, nvfp4_stream_t stream);
+
+/* Waits for `stream`, then reads and clears the workspace's device status
+ * word into *device_status (a nvfp4_status: OK, NONFINITE_INPUT or TIMEOUT;
+ * NONFINITE wins when both bits are set).  The only synchronising call. */
+nvfp4_status nvfp4_device_status(void *ws, nvfp4_stream_t stream, int32_t *device_status);
+
+/* Route the policy selects for one layer: returns 4 (W4A4), 8 (W4A8) or -1
+ * for an unknown policy.  Host only; nvfp4_gemm uses exactly this rule.
+ * [LCP] "Local inference is becoming a policy engine". */
+int32_t nvfp4_policy_route(int32_t policy, int32_t sensitive);
+
+/* ---- the hot path ---------------------------------------------------------- */
+
+/* NVFP4 quantisation of BF16 x [rows, K] (row stride ldx elements) into
+ * `out` (caller sets out->mode and out->layout and provides the buffers;
+ * out->rows and out->K must equal rows and K).  [TRT] item 2; encode order,
+ * in IEEE binary32:
+ *   s = amax(tensor) / 2688  (or per 256-group FP16 macro-scale)
+ *   per 16-block: e = E4M3_rne_sat((amax_b / 6) / s), d = e * s,
+ *   r = 1 / d (0 when d == 0, at most FLT_MAX), code = E2M1_rne_sat(x * r).
+ * K % 16 == 0 (row-major scales), % 64 (tiled), % 256 (macro).  x must be
+ * 16-byte aligned, ldx % 8 == 0.  Non-finite input sets NONFINITE_INPUT in
+ * the device status; its outputs are then unspecified. */
+nvfp4_status nvfp4_quantize(const void *x_bf16, int64_t rows, int64_t K, int64_t ldx,
+                            nvfp4_tensor *out, void *ws, size_t ws_bytes, nvfp4_stream_t stream);
+
+/* Per-token FP8 quantisation for the W4A8 route ([LCP] "One model can need
+ * more than one precision"): per row, s_t = amax_row / 448 and
+ * a = E4M3_rne_sat(x * (1 / s_t)).  a_fp8 is uint8 [rows][K] (dense),
+ * s_t float[rows].  K % 16 == 0, x 16-byte aligned, ldx % 8 == 0. */
+nvfp4_status nvfp4_quantize_fp8(const void *x_bf16, int64_t rows, int64_t K, int64_t ldx,
+                                void *a_fp8, float *s_t, void *ws, size_t ws_bytes,
+                                nvfp4_stream_t stream);
+
+/* One layer Y[M, N] = X[M, K] * W[N, K]^T under the precision policy.
+ *  Give exactly one of x_bf16 (BF16 [M, K], row stride ldx; quantised on the
+ *  fly into the workspace by the route's quantiser) or a_q (pre-quantised
+ *  NVFP4 activations, tiled scales; W4A4 route only).
+ *  w: NVFP4 weights [N, K], MMA_TILED scales, TENSOR_FP32 or MACRO_FP16.
+ *  Route = nvfp4_policy_route(policy, sensitive):
+ *    W4A4: Y = s_a * s_w * sum_k E2M1(a)E4M3(ea) * E2M1(w)E4M3(ew)  ([TRT] item 3,
+ *          [LCP] native W4A4), or per-256-group macro-scales in MACRO mode;
+ *    W4A8: Y = s_t[m] * s_w * sum_k E4M3(a) * E2M1(w)E4M3(ew)   ([LCP]).
+ *  y: [M, N] with row stride ldy elements, y_dtype BF16 or FP32, 16-byte
+ *  aligned.  K % 64 == 0 (% 256 in macro mode).  W4A8 needs x_bf16 and
+ *  TENSOR_FP32 weights.  Returns UNSUPPORTED_SHAPE for shapes the kernels do
+ *  not take, UNSUPPORTED for W4A8 with pre-quantised activations. */
+nvfp4_status nvfp4_gemm(const void *x_bf16, int64_t ldx, const nvfp4_tensor *a_q,
+                        const nvfp4_tensor *w, void *y, int64_t ldy, int32_t y_dtype, int64_t M,
+                        int32_t policy, int32_t sensitive, void *ws, size_t ws_bytes,
+                        nvfp4_stream_t stream);
+
+/* W4A8 contraction from pre-quantised FP8 activations:
+ * Y[m, n] = s_t[m] * s_w * sum_k E4M3(a[m, k]) * E2M1(w[n, k]) * E4M3(ew[n, k/16]).
+ * a_fp8 uint8 [M][K] dense, s_t float[M]; w TENSOR_FP32, MMA_TILED. */
+nvfp4_status nvfp4_w4a8_gemm(const void *a_fp8, const float *s_t, const nvfp4_tensor *w,
+                             void *y, int64_t ldy, int32_t y_dtype, int64_t M, void *ws,
+                             size_t ws_bytes, nvfp4_stream_t stream);
+
+/* Grouped (mixture-of-experts) W4A4, [LCP] (MoE operations):
+ *  a: NVFP4 activations [T_a, K], TENSOR_FP32, MMA_TILED, quantised once.
+ *  expert_offsets: device int64[E+1], non-decreasing, offsets[0] == 0,
+ *    offsets[E] <= total_rows; expert e owns output rows
+ *    offsets[e] .. offsets[e+1]-1.
+ *  row_idx: device int32[total_rows] giving the activation row of each
+ *    output row (values in [0, T_a)), or NULL for row j reading row j.
+ *  w: the E experts' weights stacked as one NVFP4 tensor [E*N, K]
+ *    (rows e*N .. e*N+N-1 belong to expert e), TENSOR_FP32 with
+ *    second = float[E] (one tensor scale per expert), MMA_TILED, N % 128 == 0.
+ *  y: [total_rows, N] with row stride ldy; rows past offsets[E] untouched.
+ *  Y[j, n] = s_a * s_w[e] * sum_k a[row(j), k] * w[e*N + n, k].
+ *  policy/sensitive: the layer's policy and sensitive flag as for nvfp4_gemm;
+ *  only the W4A4 route is implemented here, so a request that resolves to
+ *  W4A8 returns UNSUPPORTED.  Offsets are read on the device (no
+ *  host synchronisation); invalid offsets give unspecified rows. */
+nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor *a, const int32_t *row_idx,
+                                const int64_t *expert_offsets, int32_t E, const nvfp4_tensor *w,
+                                int64_t N, void *y, int64_t ldy, int32_t y_dtype,
+                                int64_t total_rows, int32_t policy, int32_t sensitive,
+                                void *ws, size_t ws_bytes, nvfp4_stream_t stream);
+
+/* ---- diagnostics ----------------------------------------------------------- */
+
+/* Runs the kernels' own element conversions on n floats: out_e2m1[i] is the
+ * E2M1 code of in[i] (round to nearest even, saturating at 6, sign kept) and
+ * out_e4m3[i] the E4M3 code (round to nearest even, saturating at 448).
+ * Used to check the device conversions exhaustively against the oracle. */
+nvfp4_status nvfp4_probe_convert(const float *in, int64_t n, uint8_t *out_e2m1, uint8_t *out_e4m3,
+                                 nvfp4_stream_t stream);
+
+/* Number of streaming multiprocessors of the current device (0 on error). */
+int32_t nvfp4_sm_count(void);
+
+/* Library version string. */
+const char *nvfp4_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_H */

@@ -1,0 +1,271 @@
+"""Python binding of libnvfp4 (the NVFP4 W4A4 / W4A8 inference-GEMM hot path
+for B300, sm_103a).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels behind the C ABI declared in include/nvfp4.h.  PyTorch supplies
+device memory and the current CUDA stream.  If libnvfp4.so is missing or a
+call fails, the functions raise; there is no fallback implementation.
+"""
+import ctypes
+import dataclasses
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libnvfp4.so")
+
+# ---- enums (include/nvfp4.h) -----------------------------------------------------
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_NONFINITE_INPUT, ERR_TIMEOUT, ERR_CUDA, \
+    ERR_WORKSPACE, ERR_UNSUPPORTED = range(8)
+STATUS_NAMES = {OK: "OK", ERR_INVALID_ARG: "INVALID_ARG", ERR_UNSUPPORTED_SHAPE: "UNSUPPORTED_SHAPE",
+                ERR_NONFINITE_INPUT: "NONFINITE_INPUT", ERR_TIMEOUT: "TIMEOUT", ERR_CUDA: "CUDA",
+                ERR_WORKSPACE: "WORKSPACE", ERR_UNSUPPORTED: "UNSUPPORTED"}
+POLICY_AUTO, POLICY_Q4, POLICY_Q8 = 0, 1, 2
+SCALE_TENSOR_FP32, SCALE_MACRO_FP16 = 0, 1
+LAYOUT_ROW_MAJOR, LAYOUT_MMA_TILED = 0, 1
+OUT_BF16, OUT_FP32 = 0, 1
+OP_QUANTIZE, OP_QUANTIZE_FP8, OP_GEMM, OP_W4A8_GEMM, OP_GROUPED_GEMM = range(5)
+
+EXPORTED = ["nvfp4_scale_bytes", "nvfp4_workspace_size", "nvfp4_workspace_init", "nvfp4_device_status",
+            "nvfp4_policy_route", "nvfp4_quantize", "nvfp4_quantize_fp8", "nvfp4_gemm", "nvfp4_w4a8_gemm",
+            "nvfp4_grouped_gemm", "nvfp4_probe_convert", "nvfp4_sm_count", "nvfp4_version"]
+
+
+class NVFP4Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+class TensorDesc(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("second", ctypes.c_void_p),
+                ("rows", ctypes.c_int64), ("K", ctypes.c_int64), ("mode", ctypes.c_int32),
+                ("layout", ctypes.c_int32)]
+
+
+_LIB = None
+_I64, _I32, _VP, _SZ = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t
+_PT = ctypes.POINTER(TensorDesc)
+
+
+def lib():
+    """Load libnvfp4.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libnvfp4.so not built ({LIB_PATH}); run "
+                               "python -m nvfp4_block_scaled_30_b300.build")
+        L = ctypes.CDLL(LIB_PATH)
+        sig = {
+            "nvfp4_scale_bytes": (_I32, [_I64, _I64, _I32, ctypes.POINTER(_SZ)]),
+            "nvfp4_workspace_size": (_I32, [_I32, _I64, _I64, _I64, _I32, ctypes.POINTER(_SZ)]),
+            "nvfp4_workspace_init": (_I32, [_VP, _SZ, _VP]),
+            "nvfp4_device_status": (_I32, [_VP, _VP, ctypes.POINTER(_I32)]),
+            "nvfp4_policy_route": (_I32, [_I32, _I32]),
+            "nvfp4_quantize": (_I32, [_VP, _I64, _I64, _I64, _PT, _VP, _SZ, _VP]),
+            "nvfp4_quantize_fp8": (_I32, [_VP, _I64, _I64, _I64, _VP, _VP, _VP, _SZ, _VP]),
+            "nvfp4_gemm": (_I32, [_VP, _I64, _PT, _PT, _VP, _I64, _I32, _I64, _I32, _I32, _VP, _SZ, _VP]),
+            "nvfp4_w4a8_gemm": (_I32, [_VP, _VP, _PT, _VP, _I64, _I32, _I64, _VP, _SZ, _VP]),
+            "nvfp4_grouped_gemm": (_I32, [_PT, _VP, _VP, _I32, _PT, _I64, _VP, _I64, _I32, _I64, _I32, _I32,
+                                          _VP, _SZ, _VP]),
+            "nvfp4_probe_convert": (_I32, [_VP, _I64, _VP, _VP, _VP]),
+            "nvfp4_sm_count": (_I32, []),
+            "nvfp4_version": (ctypes.c_char_p, []),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise NVFP4Error(status, where)
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+# ---- tensors and workspaces ----------------------------------------------------------
+
+@dataclasses.dataclass
+class NVFP4Tensor:
+    """Device NVFP4 tensor [rows, K]: packed E2M1 codes uint8 [rows, K/2],
+    E4M3 scale bytes (row-major [rows, K/16] or MMA-tiled), and the second
+    level (float32 [1] or [E] tensor scale, or binary16 [rows, K/256] macro)."""
+    codes: torch.Tensor
+    scales: torch.Tensor
+    second: torch.Tensor
+    rows: int
+    K: int
+    mode: int = SCALE_TENSOR_FP32
+    layout: int = LAYOUT_MMA_TILED
+
+    def desc(self) -> TensorDesc:
+        return TensorDesc(self.codes.data_ptr(), self.scales.data_ptr(), self.second.data_ptr(),
+                          self.rows, self.K, self.mode, self.layout)
+
+
+def scale_bytes(rows: int, K: int, layout: int = LAYOUT_MMA_TILED) -> int:
+    n = _SZ(0)
+    _check(lib().nvfp4_scale_bytes(rows, K, layout, ctypes.byref(n)), "nvfp4_scale_bytes")
+    return n.value
+
+
+def workspace_size(op: int, M: int = 0, N: int = 0, K: int = 0, E: int = 0) -> int:
+    n = _SZ(0)
+    _check(lib().nvfp4_workspace_size(op, M, N, K, E, ctypes.byref(n)), "nvfp4_workspace_size")
+    return n.value
+
+
+class Workspace:
+    """Caller-owned device scratch (holds the sticky device status word)."""
+
+    def __init__(self, nbytes: int, device="cuda", stream=None):
+        self.buf = torch.empty(max(nbytes, 256) + 256, dtype=torch.uint8, device=device)
+        off = (-self.buf.data_ptr()) % 256
+        self.ptr = self.buf.data_ptr() + off
+        self.nbytes = self.buf.numel() - off
+        _check(lib().nvfp4_workspace_init(self.ptr, self.nbytes, _stream(stream)), "nvfp4_workspace_init")
+
+    def ensure(self, nbytes: int, stream=None) -> "Workspace":
+        return self if nbytes <= self.nbytes else Workspace(nbytes, self.buf.device, stream)
+
+    def status(self, stream=None) -> int:
+        out = _I32(0)
+        _check(lib().nvfp4_device_status(self.ptr, _stream(stream), ctypes.byref(out)), "nvfp4_device_status")
+        return out.value
+
+
+def _ws(ws: Optional[Workspace], need: int, device) -> Workspace:
+    if ws is None:
+        return Workspace(need, device)
+    if ws.nbytes < need:
+        raise NVFP4Error(ERR_WORKSPACE, f"workspace of {ws.nbytes} bytes < {need}")
+    return ws
+
+
+def empty_nvfp4(rows: int, K: int, mode: int = SCALE_TENSOR_FP32, layout: int = LAYOUT_MMA_TILED,
+                device="cuda", n_second: int = 1) -> NVFP4Tensor:
+    codes = torch.empty((rows, K // 2), dtype=torch.uint8, device=device)
+    scales = torch.empty(scale_bytes(rows, K, layout), dtype=torch.uint8, device=device)
+    if mode == SCALE_TENSOR_FP32:
+        second = torch.empty(n_second, dtype=torch.float32, device=device)
+    else:
+        second = torch.empty((rows, K // 256), dtype=torch.int16, device=device)
+    return NVFP4Tensor(codes, scales, second, rows, K, mode, layout)
+
+
+# ---- the hot path ----------------------------------------------------------------------
+
+def policy_route(policy: int, sensitive: int) -> int:
+    return lib().nvfp4_policy_route(policy, int(bool(sensitive)))
+
+
+def quantize(x: torch.Tensor, mode: int = SCALE_TENSOR_FP32, layout: int = LAYOUT_MMA_TILED,
+             out: Optional[NVFP4Tensor] = None, ws: Optional[Workspace] = None, stream=None) -> NVFP4Tensor:
+    """nvfp4_quantize of a BF16 [rows, K] tensor (row stride x.stride(0))."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, K = x.shape
+    if out is None:
+        out = empty_nvfp4(rows, K, mode, layout, x.device)
+    ws = _ws(ws, workspace_size(OP_QUANTIZE, rows, 0, K), x.device)
+    d = out.desc()
+    _check(lib().nvfp4_quantize(_ptr(x), rows, K, x.stride(0), ctypes.byref(d), ws.ptr, ws.nbytes,
+                                _stream(stream)), "nvfp4_quantize")
+    return out
+
+
+def quantize_fp8(x: torch.Tensor, ws: Optional[Workspace] = None, stream=None):
+    """nvfp4_quantize_fp8: returns (E4M3 bytes uint8 [rows, K], s_t float32 [rows])."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, K = x.shape
+    a = torch.empty((rows, K), dtype=torch.uint8, device=x.device)
+    st = torch.empty(rows, dtype=torch.float32, device=x.device)
+    ws = _ws(ws, workspace_size(OP_QUANTIZE_FP8, rows, 0, K), x.device)
+    _check(lib().nvfp4_quantize_fp8(_ptr(x), rows, K, x.stride(0), _ptr(a), _ptr(st), ws.ptr, ws.nbytes,
+                                    _stream(stream)), "nvfp4_quantize_fp8")
+    return a, st
+
+
+def _out(y, M, N, out_dtype, device):
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32,
+                        device=device)
+    assert y.stride(1) == 1
+    return y
+
+
+def gemm(w: NVFP4Tensor, x: Optional[torch.Tensor] = None, a_q: Optional[NVFP4Tensor] = None,
+         out_dtype: int = OUT_BF16, policy: int = POLICY_AUTO, sensitive: int = 0,
+         y: Optional[torch.Tensor] = None, ws: Optional[Workspace] = None, stream=None) -> torch.Tensor:
+    """nvfp4_gemm: Y = X W^T for one layer under the precision policy."""
+    N, K = w.rows, w.K
+    M = x.shape[0] if x is not None else a_q.rows
+    device = w.codes.device
+    y = _out(y, M, N, out_dtype, device)
+    if M == 0:
+        return y
+    ws = _ws(ws, workspace_size(OP_GEMM, M, N, K), device)
+    wd = w.desc()
+    ad = a_q.desc() if a_q is not None else None
+    _check(lib().nvfp4_gemm(_ptr(x), x.stride(0) if x is not None else 0,
+                            ctypes.byref(ad) if ad is not None else None, ctypes.byref(wd), _ptr(y),
+                            y.stride(0), out_dtype, M, policy, int(bool(sensitive)), ws.ptr, ws.nbytes,
+                            _stream(stream)), "nvfp4_gemm")
+    return y
+
+
+def w4a8_gemm(a_fp8: torch.Tensor, s_t: torch.Tensor, w: NVFP4Tensor, out_dtype: int = OUT_BF16,
+              y: Optional[torch.Tensor] = None, ws: Optional[Workspace] = None, stream=None) -> torch.Tensor:
+    M = a_fp8.shape[0]
+    y = _out(y, M, w.rows, out_dtype, a_fp8.device)
+    if M == 0:
+        return y
+    ws = _ws(ws, workspace_size(OP_W4A8_GEMM, M, w.rows, w.K), a_fp8.device)
+    wd = w.desc()
+    _check(lib().nvfp4_w4a8_gemm(_ptr(a_fp8), _ptr(s_t), ctypes.byref(wd), _ptr(y), y.stride(0), out_dtype, M,
+                                 ws.ptr, ws.nbytes, _stream(stream)), "nvfp4_w4a8_gemm")
+    return y
+
+
+def grouped_gemm(a: NVFP4Tensor, offsets: torch.Tensor, w: NVFP4Tensor, N: int, total_rows: int,
+                 row_idx: Optional[torch.Tensor] = None, out_dtype: int = OUT_BF16,
+                 policy: int = POLICY_AUTO, sensitive: int = 0, y: Optional[torch.Tensor] = None,
+                 ws: Optional[Workspace] = None, stream=None) -> torch.Tensor:
+    """nvfp4_grouped_gemm over E = offsets.numel() - 1 experts stacked in w."""
+    assert offsets.dtype == torch.int64 and (row_idx is None or row_idx.dtype == torch.int32)
+    E = offsets.numel() - 1
+    y = _out(y, total_rows, N, out_dtype, a.codes.device)
+    if total_rows == 0:
+        return y
+    ws = _ws(ws, workspace_size(OP_GROUPED_GEMM, total_rows, N, a.K, E), a.codes.device)
+    ad, wd = a.desc(), w.desc()
+    _check(lib().nvfp4_grouped_gemm(ctypes.byref(ad), _ptr(row_idx), _ptr(offsets), E, ctypes.byref(wd), N,
+                                    _ptr(y), y.stride(0), out_dtype, total_rows, policy, int(bool(sensitive)),
+                                    ws.ptr, ws.nbytes, _stream(stream)), "nvfp4_grouped_gemm")
+    return y
+
+
+def probe_convert(v: torch.Tensor, stream=None):
+    """The kernels' own E2M1 / E4M3 conversions applied to float32 values."""
+    assert v.dtype == torch.float32 and v.is_contiguous()
+    o2 = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
+    o3 = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
+    _check(lib().nvfp4_probe_convert(_ptr(v), v.numel(), _ptr(o2), _ptr(o3), _stream(stream)),
+           "nvfp4_probe_convert")
+    return o2, o3
+
+
+def version() -> str:
+    return lib().nvfp4_version().decode()

@@ -1,0 +1,540 @@
+// C ABI of libnvfp4: argument checks, workspace layout, precision-policy
+// routing and launch configuration.  Declarations and contracts are in
+// include/nvfp4.h.  Every check runs before any work is enqueued, so an
+// error return means nothing was launched ("fail fast, no silent fallback",
+// "AdaLLM Breakthrough: First NVFP4-Only Inference Engine for RTX 4090
+// Unveiled").
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <cudaTypedefs.h>
+#include <mutex>
+
+#include "internal.h"
+
+namespace nv4 {
+
+static constexpr uint64_t DEFAULT_TIMEOUT_NS = 2000000000ull; // bounded waits: 2 s
+static constexpr int64_t MAX_DIM = (int64_t)1 << 30;
+
+int device_sm_count()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 148;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+CUresult make_tmap_2d_u8(CUtensorMap *map, const void *base, uint64_t inner_bytes, uint64_t rows,
+                         uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return CUDA_ERROR_NOT_FOUND;
+    cuuint64_t dims[2] = {inner_bytes, rows};
+    cuuint64_t strides[1] = {row_pitch_bytes};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// ---- workspace layout ------------------------------------------------------------
+
+struct WsLayout {
+    size_t amax = 0;      // partial maxima of the first quantiser pass
+    size_t a_codes = 0;   // on-the-fly NVFP4 activations
+    size_t a_scales = 0;
+    size_t a_second = 0;  // float (tensor mode) or binary16 [M][K/256] (macro)
+    size_t a_fp8 = 0;     // on-the-fly FP8 activations (W4A8 route)
+    size_t a_st = 0;
+    size_t acc = 0;       // stream-K FP32 accumulator [M][N], kept zero between calls
+    size_t tile_cnt = 0;  // stream-K per-tile stage counters, kept zero between calls
+    size_t total = 0;
+};
+
+static constexpr int64_t SPLITK_MAX_M = 128;
+
+static WsLayout ws_layout(int op, int64_t M, int64_t N, int64_t K)
+{
+    WsLayout L;
+    size_t off = WS_HEADER;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off = align_up(off + bytes, 256);
+        return o;
+    };
+    L.amax = take(WS_AMAX_BYTES);
+    if (op == NVFP4_OP_GEMM) {
+        const int64_t mpad = ceil_div(M, 128) * 128;
+        const int64_t kpad = ceil_div(K, 64) * 64;
+        L.a_codes = take((size_t)(M * (K / 2)));
+        L.a_scales = take((size_t)(mpad * (kpad / 16)));
+        L.a_second = take(std::max<size_t>(16, (size_t)(M * (K / 256) * 2)));
+        L.a_fp8 = take((size_t)(M * K));
+        L.a_st = take((size_t)(M * 4));
+    }
+    if (op == NVFP4_OP_GEMM && M <= SPLITK_MAX_M) {
+        L.acc = take((size_t)(M * N * 4));
+        L.tile_cnt = take((size_t)(ceil_div(M, 16) * ceil_div(N, 16) * 4));
+    }
+    L.total = off;
+    return L;
+}
+
+static uint32_t *status_word(void *ws) { return static_cast<uint32_t *>(ws); }
+
+static uint8_t *ws_at(void *ws, size_t off) { return static_cast<uint8_t *>(ws) + off; }
+
+static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+static nvfp4_status check_ws(void *ws, size_t ws_bytes, size_t need)
+{
+    if (!ws || !aligned(ws, 256) || ws_bytes < need)
+        return NVFP4_ERR_WORKSPACE;
+    return NVFP4_OK;
+}
+
+static nvfp4_status check_tensor(const nvfp4_tensor *t, bool need_tiled)
+{
+    if (!t || !t->second || (t->rows > 0 && (!t->codes || !t->scales)))
+        return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(t->codes, 16) || !aligned(t->scales, 16) || !aligned(t->second, 4))
+        return NVFP4_ERR_INVALID_ARG;
+    if (t->mode != NVFP4_SCALE_TENSOR_FP32 && t->mode != NVFP4_SCALE_MACRO_FP16)
+        return NVFP4_ERR_INVALID_ARG;
+    if (t->layout != NVFP4_LAYOUT_ROW_MAJOR && t->layout != NVFP4_LAYOUT_MMA_TILED)
+        return NVFP4_ERR_INVALID_ARG;
+    if (need_tiled && t->layout != NVFP4_LAYOUT_MMA_TILED)
+        return NVFP4_ERR_INVALID_ARG;
+    if (t->rows < 0 || t->K <= 0 || t->rows > MAX_DIM || t->K > MAX_DIM)
+        return NVFP4_ERR_INVALID_ARG;
+    if (t->K % 16 != 0 || (t->layout == NVFP4_LAYOUT_MMA_TILED && t->K % 64 != 0) ||
+        (t->mode == NVFP4_SCALE_MACRO_FP16 && t->K % 256 != 0))
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    return NVFP4_OK;
+}
+
+static nvfp4_status from_cuda(cudaError_t e)
+{
+    if (e == cudaSuccess)
+        return NVFP4_OK;
+    return e == cudaErrorNotSupported ? NVFP4_ERR_UNSUPPORTED : NVFP4_ERR_CUDA;
+}
+
+// Stream-K pays off when whole tiles fill the SMs poorly (wave efficiency
+// below 90%) and there are enough K stages to spread.
+static bool use_streamk(int64_t tiles, int64_t kstages, int sms)
+{
+    const double eff = (double)tiles / (double)(ceil_div(tiles, sms) * sms);
+    return eff < 0.9 && tiles * kstages >= 2 * (int64_t)sms;
+}
+
+// W4A4 dense product of NVFP4 activations `a` ([M, K], tiled scales, tensor
+// mode) and weights `w` ([N, K]) into y.  M <= 64 swaps the operands so the
+// weights fill the 128-row MMA side (decode shapes).
+static nvfp4_status run_w4a4_dense(const uint8_t *a_codes, const uint8_t *a_scales, const float *a_second,
+                                   int64_t M, const nvfp4_tensor *w, void *y, int64_t ldy, int y_dtype, void *ws,
+                                   const WsLayout &L, cudaStream_t stream)
+{
+    const int64_t N = w->rows, K = w->K;
+    DenseGemmArgs g{};
+    const bool swap = M <= 64;
+    if (swap) {
+        g.a_codes = static_cast<const uint8_t *>(w->codes);
+        g.a_scales = static_cast<const uint8_t *>(w->scales);
+        g.a_second = static_cast<const float *>(w->second);
+        g.a_rows = N;
+        g.b_codes = a_codes;
+        g.b_scales = a_scales;
+        g.b_second = a_second;
+        g.b_rows = M;
+    } else {
+        g.a_codes = a_codes;
+        g.a_scales = a_scales;
+        g.a_second = a_second;
+        g.a_rows = M;
+        g.b_codes = static_cast<const uint8_t *>(w->codes);
+        g.b_scales = static_cast<const uint8_t *>(w->scales);
+        g.b_second = static_cast<const float *>(w->second);
+        g.b_rows = N;
+    }
+    g.K = K;
+    g.status = status_word(ws);
+    g.timeout_ns = DEFAULT_TIMEOUT_NS;
+    const int bn = w4a4_dense_bn(g.b_rows);
+    const int64_t tiles = ceil_div(g.a_rows, 128) * ceil_div(g.b_rows, bn);
+    const bool sk = L.acc != 0 && use_streamk(tiles, ceil_div(K / 64, 4), device_sm_count());
+    g.streamk = sk;
+    if (!sk) {
+        g.out = y;
+        g.out_dtype = y_dtype;
+        g.ld_i = swap ? 1 : ldy;
+        g.ld_j = swap ? ldy : 1;
+        return from_cuda(launch_w4a4_dense(g, stream));
+    }
+    // stream-K: partial tiles meet in the workspace accumulator; the kernel
+    // writes y itself and leaves the accumulator and counters zeroed
+    g.out = y;
+    g.out_dtype = y_dtype;
+    g.ld_i = swap ? 1 : ldy;
+    g.ld_j = swap ? ldy : 1;
+    g.acc = reinterpret_cast<float *>(ws_at(ws, L.acc));
+    g.acc_ld_i = swap ? 1 : N;
+    g.acc_ld_j = swap ? N : 1;
+    g.tile_cnt = reinterpret_cast<uint32_t *>(ws_at(ws, L.tile_cnt));
+    return from_cuda(launch_w4a4_dense(g, stream));
+}
+
+} // namespace nv4
+
+using namespace nv4;
+
+extern "C" {
+
+const char *nvfp4_version(void) { return "nvfp4-b300 0.1 (sm_103a)"; }
+
+int32_t nvfp4_sm_count(void)
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+int32_t nvfp4_policy_route(int32_t policy, int32_t sensitive)
+{
+    switch (policy) {
+    case NVFP4_POLICY_AUTO: return sensitive ? 8 : 4;
+    case NVFP4_POLICY_Q4: return 4;
+    case NVFP4_POLICY_Q8: return 8;
+    default: return -1;
+    }
+}
+
+nvfp4_status nvfp4_scale_bytes(int64_t rows, int64_t K, int32_t layout, size_t *bytes)
+{
+    if (!bytes || rows < 0 || K < 0 || rows > MAX_DIM || K > MAX_DIM)
+        return NVFP4_ERR_INVALID_ARG;
+    if (layout == NVFP4_LAYOUT_ROW_MAJOR) {
+        if (K % 16 != 0)
+            return NVFP4_ERR_UNSUPPORTED_SHAPE;
+        *bytes = (size_t)rows * (size_t)(K / 16);
+        return NVFP4_OK;
+    }
+    if (layout == NVFP4_LAYOUT_MMA_TILED) {
+        if (K % 64 != 0)
+            return NVFP4_ERR_UNSUPPORTED_SHAPE;
+        *bytes = (size_t)ceil_div(rows, 128) * 128 * (size_t)(K / 16);
+        return NVFP4_OK;
+    }
+    return NVFP4_ERR_INVALID_ARG;
+}
+
+nvfp4_status nvfp4_workspace_size(int32_t op, int64_t M, int64_t N, int64_t K, int32_t E, size_t *bytes)
+{
+    if (!bytes || M < 0 || N < 0 || K < 0 || E < 0 || M > MAX_DIM || N > MAX_DIM || K > MAX_DIM)
+        return NVFP4_ERR_INVALID_ARG;
+    if (op < NVFP4_OP_QUANTIZE || op > NVFP4_OP_GROUPED_GEMM)
+        return NVFP4_ERR_INVALID_ARG;
+    *bytes = ws_layout(op, M, N, K).total;
+    return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_workspace_init(void *ws, size_t ws_bytes, nvfp4_stream_t stream)
+{
+    if (!ws || !aligned(ws, 256) || ws_bytes < WS_HEADER)
+        return NVFP4_ERR_WORKSPACE;
+    return from_cuda(cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream));
+}
+
+nvfp4_status nvfp4_device_status(void *ws, nvfp4_stream_t stream, int32_t *device_status)
+{
+    if (!ws || !device_status || !aligned(ws, 256))
+        return NVFP4_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    uint32_t w = 0;
+    if (cudaMemcpy(&w, ws, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    if (cudaMemset(ws, 0, 4) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    *device_status = (w & ST_NONFINITE) ? NVFP4_ERR_NONFINITE_INPUT : (w & ST_TIMEOUT) ? NVFP4_ERR_TIMEOUT : NVFP4_OK;
+    return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_quantize(const void *x_bf16, int64_t rows, int64_t K, int64_t ldx, nvfp4_tensor *out, void *ws,
+                            size_t ws_bytes, nvfp4_stream_t stream)
+{
+    nvfp4_status st = check_tensor(out, false);
+    if (st != NVFP4_OK)
+        return st;
+    if (rows < 0 || out->rows != rows || out->K != K || ldx < K || ldx % 8 != 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (rows > 0 && (!x_bf16 || !aligned(x_bf16, 16)))
+        return NVFP4_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(NVFP4_OP_QUANTIZE, rows, 0, K);
+    if ((st = check_ws(ws, ws_bytes, L.total)) != NVFP4_OK)
+        return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (rows == 0) {
+        if (out->mode == NVFP4_SCALE_TENSOR_FP32)
+            return from_cuda(cudaMemsetAsync(out->second, 0, 4, s));
+        return NVFP4_OK;
+    }
+    return from_cuda(launch_nvfp4_quantize(static_cast<const uint16_t *>(x_bf16), rows, K, ldx,
+                                           static_cast<uint8_t *>(out->codes), static_cast<uint8_t *>(out->scales),
+                                           out->second, out->mode, out->layout,
+                                           reinterpret_cast<uint32_t *>(ws_at(ws, L.amax)), status_word(ws), s));
+}
+
+nvfp4_status nvfp4_quantize_fp8(const void *x_bf16, int64_t rows, int64_t K, int64_t ldx, void *a_fp8, float *s_t,
+                                void *ws, size_t ws_bytes, nvfp4_stream_t stream)
+{
+    if (rows < 0 || K <= 0 || rows > MAX_DIM || K > MAX_DIM || ldx < K || ldx % 8 != 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (K % 16 != 0)
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (rows > 0 && (!x_bf16 || !aligned(x_bf16, 16) || !a_fp8 || !aligned(a_fp8, 16) || !s_t))
+        return NVFP4_ERR_INVALID_ARG;
+    nvfp4_status st = check_ws(ws, ws_bytes, ws_layout(NVFP4_OP_QUANTIZE_FP8, rows, 0, K).total);
+    if (st != NVFP4_OK)
+        return st;
+    return from_cuda(launch_fp8_quantize(static_cast<const uint16_t *>(x_bf16), rows, K, ldx,
+                                         static_cast<uint8_t *>(a_fp8), s_t, status_word(ws), (cudaStream_t)stream));
+}
+
+static nvfp4_status check_out(const void *y, int64_t ldy, int32_t y_dtype, int64_t N)
+{
+    if (y_dtype != NVFP4_OUT_BF16 && y_dtype != NVFP4_OUT_FP32)
+        return NVFP4_ERR_INVALID_ARG;
+    if (!y || !aligned(y, 16) || ldy < N)
+        return NVFP4_ERR_INVALID_ARG;
+    return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_w4a8_gemm(const void *a_fp8, const float *s_t, const nvfp4_tensor *w, void *y, int64_t ldy,
+                             int32_t y_dtype, int64_t M, void *ws, size_t ws_bytes, nvfp4_stream_t stream)
+{
+    nvfp4_status st = check_tensor(w, true);
+    if (st != NVFP4_OK)
+        return st;
+    if (w->mode != NVFP4_SCALE_TENSOR_FP32)
+        return NVFP4_ERR_UNSUPPORTED;
+    if (M < 0 || M > MAX_DIM || (M > 0 && (!a_fp8 || !aligned(a_fp8, 16) || !s_t)))
+        return NVFP4_ERR_INVALID_ARG;
+    if ((st = check_out(y, ldy, y_dtype, w->rows)) != NVFP4_OK)
+        return st;
+    const WsLayout L = ws_layout(NVFP4_OP_W4A8_GEMM, M, w->rows, w->K);
+    if ((st = check_ws(ws, ws_bytes, L.total)) != NVFP4_OK)
+        return st;
+    if (M == 0 || w->rows == 0)
+        return NVFP4_OK;
+    W4A8GemmArgs g{};
+    g.a_fp8 = static_cast<const uint8_t *>(a_fp8);
+    g.s_t = s_t;
+    g.M = M;
+    g.w_codes = static_cast<const uint8_t *>(w->codes);
+    g.w_scales = static_cast<const uint8_t *>(w->scales);
+    g.w_second = static_cast<const float *>(w->second);
+    g.N = w->rows;
+    g.K = w->K;
+    g.out = y;
+    g.ldy = ldy;
+    g.out_dtype = y_dtype;
+    g.status = status_word(ws);
+    g.timeout_ns = DEFAULT_TIMEOUT_NS;
+    return from_cuda(launch_w4a8(g, (cudaStream_t)stream));
+}
+
+nvfp4_status nvfp4_gemm(const void *x_bf16, int64_t ldx, const nvfp4_tensor *a_q, const nvfp4_tensor *w, void *y,
+                        int64_t ldy, int32_t y_dtype, int64_t M, int32_t policy, int32_t sensitive, void *ws,
+                        size_t ws_bytes, nvfp4_stream_t stream)
+{
+    const int32_t route = nvfp4_policy_route(policy, sensitive);
+    if (route < 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if ((x_bf16 == nullptr) == (a_q == nullptr))
+        return NVFP4_ERR_INVALID_ARG;
+    nvfp4_status st = check_tensor(w, true);
+    if (st != NVFP4_OK)
+        return st;
+    const int64_t N = w->rows, K = w->K;
+    if (M < 0 || M > MAX_DIM)
+        return NVFP4_ERR_INVALID_ARG;
+    if ((st = check_out(y, ldy, y_dtype, N)) != NVFP4_OK)
+        return st;
+    if (x_bf16) {
+        if (ldx < K || ldx % 8 != 0 || (M > 0 && !aligned(x_bf16, 16)))
+            return NVFP4_ERR_INVALID_ARG;
+    } else {
+        if ((st = check_tensor(a_q, true)) != NVFP4_OK)
+            return st;
+        if (a_q->rows != M || a_q->K != K || a_q->mode != w->mode)
+            return NVFP4_ERR_INVALID_ARG;
+        if (route == 8)
+            return NVFP4_ERR_UNSUPPORTED; // W4A8 needs the BF16 activations
+    }
+    const WsLayout L = ws_layout(NVFP4_OP_GEMM, M, N, K);
+    if ((st = check_ws(ws, ws_bytes, L.total)) != NVFP4_OK)
+        return st;
+    if (route == 8 && w->mode != NVFP4_SCALE_TENSOR_FP32)
+        return NVFP4_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0)
+        return NVFP4_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+
+    if (route == 8) {
+        uint8_t *a8 = ws_at(ws, L.a_fp8);
+        float *st_ = reinterpret_cast<float *>(ws_at(ws, L.a_st));
+        cudaError_t e = launch_fp8_quantize(static_cast<const uint16_t *>(x_bf16), M, K, ldx, a8, st_,
+                                            status_word(ws), s);
+        if (e != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        W4A8GemmArgs g{};
+        g.a_fp8 = a8;
+        g.s_t = st_;
+        g.M = M;
+        g.w_codes = static_cast<const uint8_t *>(w->codes);
+        g.w_scales = static_cast<const uint8_t *>(w->scales);
+        g.w_second = static_cast<const float *>(w->second);
+        g.N = N;
+        g.K = K;
+        g.out = y;
+        g.ldy = ldy;
+        g.out_dtype = y_dtype;
+        g.status = status_word(ws);
+        g.timeout_ns = DEFAULT_TIMEOUT_NS;
+        return from_cuda(launch_w4a8(g, s));
+    }
+
+    const uint8_t *ac, *as;
+    const void *asec;
+    if (x_bf16) {
+        uint8_t *c = ws_at(ws, L.a_codes), *sc = ws_at(ws, L.a_scales);
+        void *sec = ws_at(ws, L.a_second);
+        cudaError_t e = launch_nvfp4_quantize(static_cast<const uint16_t *>(x_bf16), M, K, ldx, c, sc, sec, w->mode,
+                                              NVFP4_LAYOUT_MMA_TILED, reinterpret_cast<uint32_t *>(ws_at(ws, L.amax)),
+                                              status_word(ws), s);
+        if (e != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        ac = c;
+        as = sc;
+        asec = sec;
+    } else {
+        ac = static_cast<const uint8_t *>(a_q->codes);
+        as = static_cast<const uint8_t *>(a_q->scales);
+        asec = a_q->second;
+    }
+    if (w->mode == NVFP4_SCALE_MACRO_FP16) {
+        MacroGemmArgs g{};
+        g.a_codes = ac;
+        g.a_scales = as;
+        g.a_macro = static_cast<const uint16_t *>(asec);
+        g.M = M;
+        g.w_codes = static_cast<const uint8_t *>(w->codes);
+        g.w_scales = static_cast<const uint8_t *>(w->scales);
+        g.w_macro = static_cast<const uint16_t *>(w->second);
+        g.N = N;
+        g.K = K;
+        g.out = y;
+        g.ldy = ldy;
+        g.out_dtype = y_dtype;
+        g.status = status_word(ws);
+        g.timeout_ns = DEFAULT_TIMEOUT_NS;
+        return from_cuda(launch_w4a4_macro(g, s));
+    }
+    return run_w4a4_dense(ac, as, static_cast<const float *>(asec), M, w, y, ldy, y_dtype, ws, L, s);
+}
+
+nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor *a, const int32_t *row_idx, const int64_t *expert_offsets,
+                                int32_t E, const nvfp4_tensor *w, int64_t N, void *y, int64_t ldy, int32_t y_dtype,
+                                int64_t total_rows, int32_t policy, int32_t sensitive, void *ws,
+                                size_t ws_bytes, nvfp4_stream_t stream)
+{
+    const int32_t route = nvfp4_policy_route(policy, sensitive);
+    if (route < 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (route == 8)
+        return NVFP4_ERR_UNSUPPORTED; // grouped W4A8 is not implemented
+    nvfp4_status st = check_tensor(a, true);
+    if (st != NVFP4_OK)
+        return st;
+    if ((st = check_tensor(w, true)) != NVFP4_OK)
+        return st;
+    if (a->mode != NVFP4_SCALE_TENSOR_FP32 || w->mode != NVFP4_SCALE_TENSOR_FP32)
+        return NVFP4_ERR_UNSUPPORTED;
+    if (E <= 0 || E > 1024 || !expert_offsets || !aligned(expert_offsets, 8))
+        return NVFP4_ERR_INVALID_ARG;
+    if (N <= 0 || N % 128 != 0)
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (w->rows != (int64_t)E * N || w->K != a->K)
+        return NVFP4_ERR_INVALID_ARG;
+    if (total_rows < 0 || total_rows > MAX_DIM)
+        return NVFP4_ERR_INVALID_ARG;
+    if (row_idx == nullptr && total_rows > a->rows)
+        return NVFP4_ERR_INVALID_ARG;
+    if (row_idx != nullptr && !aligned(row_idx, 4))
+        return NVFP4_ERR_INVALID_ARG;
+    if ((st = check_out(y, ldy, y_dtype, N)) != NVFP4_OK)
+        return st;
+    if ((st = check_ws(ws, ws_bytes, ws_layout(NVFP4_OP_GROUPED_GEMM, total_rows, N, a->K).total)) != NVFP4_OK)
+        return st;
+    if (total_rows == 0)
+        return NVFP4_OK;
+    GroupedGemmArgs g{};
+    g.a_codes = static_cast<const uint8_t *>(a->codes);
+    g.a_scales = static_cast<const uint8_t *>(a->scales);
+    g.a_second = static_cast<const float *>(a->second);
+    g.a_rows = a->rows;
+    g.row_idx = row_idx;
+    g.offsets = expert_offsets;
+    g.E = E;
+    g.w_codes = static_cast<const uint8_t *>(w->codes);
+    g.w_scales = static_cast<const uint8_t *>(w->scales);
+    g.w_second = static_cast<const float *>(w->second);
+    g.N = N;
+    g.K = a->K;
+    g.out = y;
+    g.ldy = ldy;
+    g.out_dtype = y_dtype;
+    g.total_rows = total_rows;
+    g.status = status_word(ws);
+    g.timeout_ns = DEFAULT_TIMEOUT_NS;
+    return from_cuda(launch_w4a4_grouped(g, (cudaStream_t)stream));
+}
+
+nvfp4_status nvfp4_probe_convert(const float *in, int64_t n, uint8_t *out_e2m1, uint8_t *out_e4m3,
+                                 nvfp4_stream_t stream)
+{
+    if (n < 0 || (n > 0 && (!in || !out_e2m1 || !out_e4m3)))
+        return NVFP4_ERR_INVALID_ARG;
+    return from_cuda(launch_probe_convert(in, n, out_e2m1, out_e4m3, (cudaStream_t)stream));
+}
+
+} // extern "C"

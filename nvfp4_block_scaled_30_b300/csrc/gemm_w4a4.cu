@@ -1,0 +1,786 @@
+// W4A4 block-scaled GEMM on 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// Computes D[i][j] = alpha * sum_k A[i][k] * B[j][k] where A and B are NVFP4
+// (E2M1 codes with one UE4M3 scale per 16 elements of K), the contraction
+// that "NVIDIA Ships TensorRT-LLM 0.16: Native FP4 Quantization for Blackwell
+// B200", section "The Mathematical Breakthrough of Microscopic FP4 Scaling",
+// item 3 "Hardware-Fused Dequantization" describes: the tensor cores take the
+// FP4 codes and the micro-scales directly and apply the scales before the
+// dot products.  alpha is the product of the two FP32 second-level scales.
+// The grouped variant serves the mixture-of-experts operations of "llama.cpp
+// Put Precision Policy Inside the Model. That Matters More Than W4A4",
+// section "One model can need more than one precision".
+//
+// Design (one CTA per SM, persistent, warp-specialised, 192 threads):
+//   warp 0      TMA producer: A/B code tiles (128-byte rows = 256 FP4, 128-byte
+//               swizzle) and the 512-byte scale atoms into a STAGES-deep ring.
+//   warp 1      allocates TMEM; lane 0 issues tcgen05.cp (scales smem->TMEM)
+//               and tcgen05.mma kind::mxf4nvf4 (M=128, N=BN, K=64 each, 4 per
+//               stage), then tcgen05.commit to release the stage.
+//   warps 2..5  epilogue: tcgen05.ld of the FP32 accumulator, alpha scale,
+//               BF16/FP32 store (or FP32 red.add for split-K).
+// Accumulators are double-buffered in TMEM when BN <= 128 so the epilogue of
+// one tile overlaps the mainloop of the next.  Every mbarrier wait is bounded;
+// on timeout the CTA records NVFP4 TIMEOUT in the status word, drains its
+// in-flight copies and MMAs, frees TMEM and exits.
+#include <algorithm>
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace nv4 {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int STAGE_K_BYTES = 128; // per row and stage: 256 FP4 elements
+constexpr int GROUP_M = 8;         // tile rasterisation band for L2 reuse
+constexpr int EPI_WARPS = 4;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int MAX_EXPERTS = 1024;
+
+template <int BN>
+struct Cfg {
+    static constexpr int NB = BN >= 128 ? BN / 128 : 1; // 128-row scale atoms per B tile
+    static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr int ACC_BUFS = BN == 256 ? 1 : 2;
+    static constexpr int A_BYTES = BM * STAGE_K_BYTES;
+    static constexpr int B_BYTES = BN * STAGE_K_BYTES;
+    static constexpr int SFA_BYTES = 4 * 512;
+    static constexpr int SFB_BYTES = NB * 4 * 512;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    static constexpr int SF_COLS = 16 + 16 * NB; // TMEM columns of scales per stage
+    static constexpr int SF_BASE = ACC_BUFS * BN;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+    static_assert(SF_BASE + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
+    static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+};
+
+struct Params {
+    CUtensorMap tmap_a;  // MMA operand A codes [a_rows][K/2] (unused for indexed grouped rows)
+    CUtensorMap tmap_b;  // MMA operand B codes
+    const uint8_t *a_codes; // indexed grouped rows are copied from here with cp.async
+    const uint8_t *sfa;  // tiled scales of A (row-padded to 128)
+    const uint8_t *sfb;  // tiled scales of B
+    const float *a_second;
+    const float *b_second; // [1] dense, [E] grouped
+    void *out;
+    int64_t ld_i, ld_j;
+    float *acc;              // stream-K: FP32 partial sums, acc[i*acc_ld_i + j*acc_ld_j], zero between calls
+    int64_t acc_ld_i, acc_ld_j;
+    uint32_t *tile_cnt;      // stream-K: K stages summed so far per tile, zero between calls
+    int64_t a_rows, b_rows; // valid extents (b_rows = N per expert in grouped mode)
+    int32_t m_tiles, n_tiles, k64, kstages, streamk;
+    int32_t out_dtype, vec_ok;
+    int32_t b_row_tiles;    // 128-row scale atoms available in B (total)
+    // grouped mode
+    const int64_t *offsets;
+    const int32_t *row_idx;
+    int32_t E;
+    int64_t total_rows;      // rows of the index list / output (offsets are clamped to it)
+    uint32_t *status;
+    uint64_t timeout_ns;
+};
+
+struct Tile {
+    int tile, tile_m, tile_n, kst0, kst1;
+    int expert;            // grouped
+    int64_t row0, row_end; // grouped: first output row of the tile, end of the expert's rows
+};
+
+__device__ __forceinline__ void decode_dense(const Params &p, int tile, Tile &t)
+{
+    const int band = GROUP_M * p.n_tiles;
+    const int bid = tile / band;
+    const int first_m = bid * GROUP_M;
+    const int gsize = min(p.m_tiles - first_m, GROUP_M);
+    const int rr = tile - bid * band;
+    t.tile = tile;
+    t.tile_m = first_m + rr % gsize;
+    t.tile_n = rr / gsize;
+    t.kst0 = 0;
+    t.kst1 = p.kstages;
+    t.expert = 0;
+    t.row0 = 0;
+    t.row_end = 0;
+}
+
+// Expert e's output rows [lo, hi), with the device offsets clamped to
+// [0, total_rows] and made non-decreasing so a malformed list cannot address
+// memory outside the index list or the output.
+__device__ __forceinline__ void expert_rows(const Params &p, int e, int64_t &lo, int64_t &hi)
+{
+    lo = min(max(p.offsets[e], (int64_t)0), p.total_rows);
+    hi = min(max(p.offsets[e + 1], lo), p.total_rows);
+}
+
+// Grouped: prefix[e] = number of 128-row tiles of experts 0..e-1.
+__device__ __forceinline__ void decode_grouped(const Params &p, const int *prefix, int item, Tile &t)
+{
+    const int tile_idx = item / p.n_tiles;
+    int lo = 0, hi = p.E; // find e with prefix[e] <= tile_idx < prefix[e+1]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= tile_idx)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    const int e = lo;
+    const int mt_e = prefix[e + 1] - prefix[e];
+    const int local = item - prefix[e] * p.n_tiles;
+    t.tile = item;
+    t.expert = e;
+    t.tile_n = local / mt_e;
+    const int mt = local - t.tile_n * mt_e;
+    t.tile_m = mt;
+    int64_t r_lo, r_hi;
+    expert_rows(p, e, r_lo, r_hi);
+    t.row0 = r_lo + (int64_t)mt * BM;
+    t.row_end = r_hi;
+    t.kst0 = 0;
+    t.kst1 = p.kstages;
+}
+
+// The sequence of work segments of one CTA, identical for all its roles.
+// Static mode: whole tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+// Stream-K mode: the contiguous range [b*T/G, (b+1)*T/G) of the flattened
+// (tile, K-stage) space, cut at tile boundaries; partial tiles are summed
+// by FP32 red.add in the epilogue.
+struct WorkIter {
+    int64_t g, g_end;
+    int item;
+};
+
+__device__ __forceinline__ void work_begin(const Params &p, int total_items, WorkIter &w)
+{
+    if (p.streamk) {
+        const int64_t T = (int64_t)total_items * p.kstages;
+        w.g = (int64_t)blockIdx.x * T / gridDim.x;
+        w.g_end = (int64_t)(blockIdx.x + 1) * T / gridDim.x;
+    }
+    w.item = blockIdx.x;
+}
+
+template <bool GROUPED>
+__device__ __forceinline__ bool work_next(const Params &p, const int *prefix, int total_items, WorkIter &w, Tile &t)
+{
+    if (!GROUPED && p.streamk) {
+        if (w.g >= w.g_end)
+            return false;
+        const int tile = (int)(w.g / p.kstages);
+        const int k0 = (int)(w.g - (int64_t)tile * p.kstages);
+        const int64_t rem = w.g_end - w.g;
+        const int k1 = rem < (int64_t)(p.kstages - k0) ? k0 + (int)rem : p.kstages;
+        decode_dense(p, tile, t);
+        t.kst0 = k0;
+        t.kst1 = k1;
+        w.g += k1 - k0;
+        return true;
+    }
+    if (w.item >= total_items)
+        return false;
+    if (GROUPED)
+        decode_grouped(p, prefix, w.item, t);
+    else
+        decode_dense(p, w.item, t);
+    w.item += gridDim.x;
+    return true;
+}
+
+// Named barrier 1 across the four epilogue warps only.
+__device__ __forceinline__ void epi_bar_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * EPI_WARPS) : "memory");
+}
+
+// Named barrier 1 across the epilogue warps returning the AND of `pred`, so
+// every epilogue warp takes the same exit decision.
+__device__ __forceinline__ bool epi_bar_all(bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.and.pred po, 1, %2, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "n"(32 * EPI_WARPS)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void record_timeout(const Params &p, volatile int *abort_flag)
+{
+    *abort_flag = 1;
+    atomicOr(p.status, ST_TIMEOUT);
+}
+
+template <int BN>
+__device__ __forceinline__ void store_chunk(const Params &p, const uint32_t (&v)[32], int nv, int64_t i, int64_t j0,
+                                            float alpha, int64_t i_end, int64_t j_end, bool partial)
+{
+    if (i >= i_end)
+        return;
+    if (partial) {
+        for (int c = 0; c < nv; ++c) {
+            const int64_t j = j0 + c;
+            if (j < j_end)
+                atomicAdd(p.acc + i * p.acc_ld_i + j * p.acc_ld_j, alpha * __uint_as_float(v[c]));
+        }
+        return;
+    }
+    if (p.ld_j == 1 && p.vec_ok && j0 + nv <= j_end) {
+        if (p.out_dtype == NVFP4_OUT_BF16) {
+            uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + i * p.ld_i + j0);
+            for (int c = 0; c < nv; c += 8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    __nv_bfloat162 h = __floats2bfloat162_rn(alpha * __uint_as_float(v[c + 2 * q]),
+                                                             alpha * __uint_as_float(v[c + 2 * q + 1]));
+                    w[q] = *reinterpret_cast<uint32_t *>(&h);
+                }
+                o[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        } else {
+            float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + i * p.ld_i + j0);
+            for (int c = 0; c < nv; c += 4)
+                o[c / 4] = make_float4(alpha * __uint_as_float(v[c]), alpha * __uint_as_float(v[c + 1]),
+                                       alpha * __uint_as_float(v[c + 2]), alpha * __uint_as_float(v[c + 3]));
+        }
+        return;
+    }
+    for (int c = 0; c < nv; ++c) {
+        const int64_t j = j0 + c;
+        if (j >= j_end)
+            break;
+        const float y = alpha * __uint_as_float(v[c]);
+        const int64_t off = i * p.ld_i + j * p.ld_j;
+        if (p.out_dtype == NVFP4_OUT_BF16)
+            static_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(y);
+        else
+            static_cast<float *>(p.out)[off] = y;
+    }
+}
+
+template <int BN, bool GROUPED>
+__global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant__ Params p)
+{
+    using C = Cfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE_BYTES);
+    uint64_t *empty = full + C::STAGES;
+    uint64_t *acc_full = empty + C::STAGES;
+    uint64_t *acc_empty = acc_full + C::ACC_BUFS;
+    uint64_t *drain = acc_empty + C::ACC_BUFS;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *last_flag = abort_flag + 1;
+    __shared__ int prefix[GROUPED ? MAX_EXPERTS + 1 : 1];
+    __shared__ int total_items_s;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    constexpr unsigned FULLMASK = 0xFFFFFFFFu;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], GROUPED ? 2 : 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < C::ACC_BUFS; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], EPI_WARPS);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (GROUPED) {
+        if (warp == 2) {
+            // tiles per expert, prefix-summed by one warp: lane l owns a
+            // contiguous run of experts; a shuffle scan joins the runs
+            const int per = (p.E + 31) / 32;
+            const int e0 = min(lane * per, p.E), e1 = min(e0 + per, p.E);
+            int run = 0;
+            for (int e = e0; e < e1; ++e) {
+                int64_t lo, hi;
+                expert_rows(p, e, lo, hi);
+                run += (int)((hi - lo + BM - 1) / BM);
+            }
+            int incl = run;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(FULLMASK, incl, o);
+                if (lane >= o)
+                    incl += v;
+            }
+            int acc = incl - run;
+            if (lane == 0)
+                prefix[0] = 0;
+            for (int e = e0; e < e1; ++e) {
+                int64_t lo, hi;
+                expert_rows(p, e, lo, hi);
+                acc += (int)((hi - lo + BM - 1) / BM);
+                prefix[e + 1] = acc;
+            }
+            if (lane == 31)
+                total_items_s = incl * p.n_tiles;
+        }
+    } else if (threadIdx.x == 0) {
+        total_items_s = p.m_tiles * p.n_tiles;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int total_items = total_items_s;
+    const uint32_t idesc = idesc_mxf4nvf4(BN);
+    const bool indexed = GROUPED && p.row_idx != nullptr;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued = 0;
+        bool ok = true;
+        WorkIter wi;
+        work_begin(p, total_items, wi);
+        Tile t;
+        while (ok && work_next<GROUPED>(p, prefix, total_items, wi, t)) {
+            // grouped: source activation row of tile rows lane + 32q
+            int src_row[4] = {0, 0, 0, 0};
+            bool row_ok[4] = {false, false, false, false};
+            if (GROUPED) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int64_t g = t.row0 + lane + 32 * q;
+                    row_ok[q] = g < t.row_end;
+                    int r = row_ok[q] ? (indexed ? p.row_idx[g] : (int)g) : 0;
+                    if (r < 0 || r >= p.a_rows) { // out-of-range index: read row 0, result unspecified
+                        r = 0;
+                    }
+                    src_row[q] = r;
+                }
+            }
+            for (int kb = t.kst0; kb < t.kst1; ++kb) {
+                const bool got = mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag);
+                if (!__all_sync(FULLMASK, got)) {
+                    if (lane == 0)
+                        record_timeout(p, abort_flag);
+                    ok = false;
+                    break;
+                }
+                const int nk = min(4, p.k64 - 4 * kb);
+                uint8_t *sA = smem + stage * C::STAGE_BYTES;
+                uint8_t *sB = sA + C::A_BYTES;
+                uint8_t *sSFA = sB + C::B_BYTES;
+                uint8_t *sSFB = sSFA + C::SFA_BYTES;
+                const int brow0 = GROUPED ? t.expert * (int)p.b_rows + t.tile_n * BN : t.tile_n * BN;
+                const int bt0 = BN >= 128 ? brow0 / 128 : 0;
+                int nb_loaded = 0;
+#pragma unroll
+                for (int h = 0; h < C::NB; ++h)
+                    nb_loaded += (bt0 + h < p.b_row_tiles) ? 1 : 0;
+                uint32_t bytes = C::B_BYTES + nb_loaded * nk * 512;
+                if (!indexed)
+                    bytes += C::A_BYTES;
+                if (!GROUPED)
+                    bytes += nk * 512;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&full[stage], bytes);
+                    if (!indexed) {
+                        const int arow = GROUPED ? (int)t.row0 : t.tile_m * BM;
+                        tma_load_2d(sA, &p.tmap_a, kb * STAGE_K_BYTES, arow, &full[stage]);
+                    }
+                    tma_load_2d(sB, &p.tmap_b, kb * STAGE_K_BYTES, brow0, &full[stage]);
+                    if (!GROUPED)
+                        bulk_load(sSFA, p.sfa + ((size_t)t.tile_m * p.k64 + 4 * kb) * 512, nk * 512, &full[stage]);
+#pragma unroll
+                    for (int h = 0; h < C::NB; ++h)
+                        if (bt0 + h < p.b_row_tiles)
+                            bulk_load(sSFB + h * 2048, p.sfb + ((size_t)(bt0 + h) * p.k64 + 4 * kb) * 512, nk * 512,
+                                      &full[stage]);
+                }
+                if (GROUPED) {
+                    if (indexed) {
+                        // gathered code rows: 16-byte cp.async with the 128-byte
+                        // swizzle (chunk c of row r lands in chunk c ^ (r & 7))
+                        const int row_bytes = p.k64 * 32;
+                        const int kbytes = min(STAGE_K_BYTES, row_bytes - kb * STAGE_K_BYTES);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int r = lane + 32 * q;
+                            const uint8_t *src = p.a_codes + (size_t)src_row[q] * row_bytes + kb * STAGE_K_BYTES;
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                const int n = row_ok[q] ? max(0, min(16, kbytes - c * 16)) : 0;
+                                cp_async_16(sA + r * STAGE_K_BYTES + ((c ^ (r & 7)) << 4), n ? src + c * 16 : src, n);
+                            }
+                        }
+                    }
+                    // activation scales of the tile's rows: 4 bytes per row and 64-K chunk
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int r = src_row[q];
+                        const size_t base =
+                            ((size_t)(r >> 7) * p.k64 + 4 * kb) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            uint32_t v = 0;
+                            if (row_ok[q] && kk < nk)
+                                v = __ldg(reinterpret_cast<const uint32_t *>(p.sfa + base + kk * 512));
+                            *reinterpret_cast<uint32_t *>(sSFA + kk * 512 + lane * 16 + q * 4) = v;
+                        }
+                    }
+                    if (indexed)
+                        cp_async_wait_all();
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&full[stage]);
+                }
+                ++issued;
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        // drain: wait (bounded) until every copy this warp issued has landed
+        if (lane == 0) {
+            const int n = min(issued, C::STAGES);
+            int s = stage;
+            uint32_t ph = phase;
+            for (int q = 0; q < n; ++q) {
+                if (--s < 0) {
+                    s = C::STAGES - 1;
+                    ph ^= 1u;
+                }
+                mbar_wait(&full[s], ph, p.timeout_ns, nullptr);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            WorkIter wi;
+            work_begin(p, total_items, wi);
+            Tile t;
+            while (ok && work_next<GROUPED>(p, prefix, total_items, wi, t)) {
+                if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
+                    record_timeout(p, abort_flag);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + acc * BN;
+                uint32_t accumulate = 0;
+                for (int kb = t.kst0; kb < t.kst1; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag)) {
+                        record_timeout(p, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int nk = min(4, p.k64 - 4 * kb);
+                    const uint8_t *sA = smem + stage * C::STAGE_BYTES;
+                    const uint8_t *sB = sA + C::A_BYTES;
+                    const uint8_t *sSFA = sB + C::B_BYTES;
+                    const uint8_t *sSFB = sSFA + C::SFA_BYTES;
+                    const uint32_t sf_col = tmem + C::SF_BASE + stage * C::SF_COLS;
+                    for (int kk = 0; kk < nk; ++kk) {
+                        tc_cp_32x128b_warpx4(sf_col + kk * 4, sdesc_sf(smem_u32(sSFA + kk * 512)));
+#pragma unroll
+                        for (int h = 0; h < C::NB; ++h)
+                            tc_cp_32x128b_warpx4(sf_col + 16 + kk * 4 * C::NB + h * 4,
+                                                 sdesc_sf(smem_u32(sSFB + h * 2048 + kk * 512)));
+                    }
+                    const uint64_t adesc = sdesc_sw128(smem_u32(sA));
+                    const uint64_t bdesc = sdesc_sw128(smem_u32(sB));
+                    for (int kk = 0; kk < nk; ++kk) {
+                        // +32 bytes (64 FP4) inside the swizzled 128-byte row
+                        mma_mxf4nvf4(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
+                                     sf_col + kk * 4, sf_col + 16 + kk * 4 * C::NB, accumulate);
+                        accumulate = 1;
+                    }
+                    tc_commit(&empty[stage]);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                tc_commit(&acc_full[acc]);
+                if (++acc == C::ACC_BUFS) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            // every MMA and copy of this thread completes before TMEM is freed
+            tc_commit(drain);
+            mbar_wait(drain, 0, p.timeout_ns, nullptr);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3; // the TMEM lane quarter this warp may access
+        const int row_in_tile = q * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        const float a_s = *p.a_second;
+        WorkIter wi;
+        work_begin(p, total_items, wi);
+        Tile t;
+        while (work_next<GROUPED>(p, prefix, total_items, wi, t)) {
+            const bool got = mbar_wait(&acc_full[acc], acc_phase, p.timeout_ns, abort_flag);
+            if (!epi_bar_all(got)) {
+                if (threadIdx.x == 64)
+                    record_timeout(p, abort_flag);
+                break;
+            }
+            tc_fence_after();
+            const float alpha = a_s * p.b_second[GROUPED ? t.expert : 0];
+            int64_t i, i_end;
+            if (GROUPED) {
+                i = t.row0 + row_in_tile;
+                i_end = t.row_end;
+            } else {
+                i = (int64_t)t.tile_m * BM + row_in_tile;
+                i_end = p.a_rows;
+            }
+            const int64_t j_base = (int64_t)t.tile_n * BN;
+            const int64_t j_end = p.b_rows;
+            const bool partial = !GROUPED && p.streamk && !(t.kst0 == 0 && t.kst1 == p.kstages);
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
+            if (BN % 32 == 0) {
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    uint32_t v[32];
+                    tc_ld_32x32b_x32(tbase + c0, v);
+                    tc_wait_ld();
+                    store_chunk<BN>(p, v, 32, i, j_base + c0, alpha, i_end, j_end, partial);
+                }
+            } else {
+                for (int c0 = 0; c0 < BN; c0 += 16) {
+                    uint32_t v16[16];
+                    tc_ld_32x32b_x16(tbase + c0, v16);
+                    tc_wait_ld();
+                    uint32_t v[32];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        v[c] = v16[c];
+                    store_chunk<BN>(p, v, 16, i, j_base + c0, alpha, i_end, j_end, partial);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&acc_empty[acc]);
+            if (++acc == C::ACC_BUFS) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+            if (partial) {
+                // the CTA whose stages complete the tile converts it and
+                // leaves the accumulator and the counter at zero again
+                epi_bar_sync();
+                if (threadIdx.x == 64) {
+                    __threadfence();
+                    const uint32_t add = (uint32_t)(t.kst1 - t.kst0);
+                    const uint32_t old = atomicAdd(p.tile_cnt + t.tile, add);
+                    *last_flag = (old + add == (uint32_t)p.kstages) ? 1 : 0;
+                }
+                epi_bar_sync();
+                if (*last_flag) {
+                    __threadfence();
+                    if (i < i_end) {
+                        for (int c = 0; c < BN; ++c) {
+                            const int64_t j = j_base + c;
+                            if (j >= j_end)
+                                break;
+                            float *a = p.acc + i * p.acc_ld_i + j * p.acc_ld_j;
+                            const float y = __ldcg(a);
+                            __stcg(a, 0.0f);
+                            const int64_t off = i * p.ld_i + j * p.ld_j;
+                            if (p.out_dtype == NVFP4_OUT_BF16)
+                                static_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(y);
+                            else
+                                static_cast<float *>(p.out)[off] = y;
+                        }
+                    }
+                    if (threadIdx.x == 64)
+                        p.tile_cnt[t.tile] = 0;
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int BN, bool GROUPED>
+cudaError_t launch(const Params &p, int total_items, cudaStream_t stream)
+{
+    using C = Cfg<BN>;
+    auto kern = w4a4_kernel<BN, GROUPED>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess)
+        return e;
+    const int grid = std::max(1, std::min(total_items, device_sm_count()));
+    kern<<<grid, THREADS, C::SMEM_BYTES, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t dispatch(int bn, bool grouped, const Params &p, int total_items, cudaStream_t stream)
+{
+    if (grouped) {
+        switch (bn) {
+        case 128: return launch<128, true>(p, total_items, stream);
+        case 256: return launch<256, true>(p, total_items, stream);
+        default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (bn) {
+    case 16: return launch<16, false>(p, total_items, stream);
+    case 32: return launch<32, false>(p, total_items, stream);
+    case 64: return launch<64, false>(p, total_items, stream);
+    case 128: return launch<128, false>(p, total_items, stream);
+    case 256: return launch<256, false>(p, total_items, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+} // namespace
+
+// N-side tile width: a narrow N side (<= 64 rows, e.g. decode activations after
+// the operands are swapped) takes one tile of the smallest MMA N that covers it.
+int w4a4_dense_bn(int64_t b_rows)
+{
+    if (b_rows <= 16)
+        return 16;
+    if (b_rows <= 32)
+        return 32;
+    if (b_rows <= 64)
+        return 64;
+    if (b_rows <= 128 || (b_rows % 256 != 0 && b_rows < 1024))
+        return 128;
+    return 256;
+}
+
+cudaError_t launch_w4a4_dense(const DenseGemmArgs &g, cudaStream_t stream)
+{
+    Params p{};
+    const int64_t k64 = g.K / 64;
+    const int sms = device_sm_count();
+    const int bn = w4a4_dense_bn(g.b_rows);
+    const int64_t m_tiles = ceil_div(g.a_rows, BM);
+    const int64_t n_tiles = ceil_div(g.b_rows, bn);
+    const int64_t kstages = ceil_div(k64, 4);
+    p.m_tiles = (int)m_tiles;
+    p.n_tiles = (int)n_tiles;
+    p.k64 = (int)k64;
+    p.kstages = (int)kstages;
+    p.streamk = g.streamk ? 1 : 0;
+    CUresult r = make_tmap_2d_u8(&p.tmap_a, g.a_codes, (uint64_t)(g.K / 2), (uint64_t)g.a_rows,
+                                 (uint64_t)(g.K / 2), STAGE_K_BYTES, BM, true);
+    if (r != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    r = make_tmap_2d_u8(&p.tmap_b, g.b_codes, (uint64_t)(g.K / 2), (uint64_t)g.b_rows, (uint64_t)(g.K / 2),
+                        STAGE_K_BYTES, (uint32_t)bn, true);
+    if (r != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    p.a_codes = g.a_codes;
+    p.sfa = g.a_scales;
+    p.sfb = g.b_scales;
+    p.a_second = g.a_second;
+    p.b_second = g.b_second;
+    p.out = g.out;
+    p.ld_i = g.ld_i;
+    p.ld_j = g.ld_j;
+    p.a_rows = g.a_rows;
+    p.b_rows = g.b_rows;
+    p.out_dtype = g.out_dtype;
+    p.acc = g.acc;
+    p.acc_ld_i = g.acc_ld_i;
+    p.acc_ld_j = g.acc_ld_j;
+    p.tile_cnt = g.tile_cnt;
+    const int esz = g.out_dtype == NVFP4_OUT_BF16 ? 2 : 4;
+    p.vec_ok = (g.ld_j == 1 && (g.ld_i * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(g.out) % 16) == 0) ? 1 : 0;
+    p.b_row_tiles = (int)ceil_div(g.b_rows, 128);
+    p.offsets = nullptr;
+    p.row_idx = nullptr;
+    p.E = 0;
+    p.status = g.status;
+    p.timeout_ns = g.timeout_ns;
+    const int tiles = p.m_tiles * p.n_tiles;
+    // stream-K: one CTA per SM over all (tile, stage) units
+    const int grid_units = g.streamk ? (int)std::min<int64_t>((int64_t)tiles * kstages, sms) : tiles;
+    return dispatch(bn, false, p, grid_units, stream);
+}
+
+cudaError_t launch_w4a4_grouped(const GroupedGemmArgs &g, cudaStream_t stream)
+{
+    Params p{};
+    const int64_t k64 = g.K / 64;
+    const int bn = (g.N % 256 == 0) ? 256 : 128;
+    p.m_tiles = 0;
+    p.n_tiles = (int)(g.N / bn);
+    p.k64 = (int)k64;
+    p.kstages = (int)ceil_div(k64, 4);
+    p.streamk = 0;
+    CUresult r = make_tmap_2d_u8(&p.tmap_a, g.a_codes, (uint64_t)(g.K / 2), (uint64_t)g.a_rows,
+                                 (uint64_t)(g.K / 2), STAGE_K_BYTES, BM, true);
+    if (r != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    r = make_tmap_2d_u8(&p.tmap_b, g.w_codes, (uint64_t)(g.K / 2), (uint64_t)(g.E * g.N), (uint64_t)(g.K / 2),
+                        STAGE_K_BYTES, (uint32_t)bn, true);
+    if (r != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    p.a_codes = g.a_codes;
+    p.sfa = g.a_scales;
+    p.sfb = g.w_scales;
+    p.a_second = g.a_second;
+    p.b_second = g.w_second;
+    p.out = g.out;
+    p.ld_i = g.ldy;
+    p.ld_j = 1;
+    p.a_rows = g.a_rows;
+    p.b_rows = g.N;
+    p.out_dtype = g.out_dtype;
+    const int esz = g.out_dtype == NVFP4_OUT_BF16 ? 2 : 4;
+    p.vec_ok = ((g.ldy * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(g.out) % 16) == 0) ? 1 : 0;
+    p.b_row_tiles = (int)ceil_div(g.E * g.N, 128);
+    p.offsets = g.offsets;
+    p.row_idx = g.row_idx;
+    p.E = g.E;
+    p.total_rows = g.total_rows;
+    p.status = g.status;
+    p.timeout_ns = g.timeout_ns;
+    // upper bound of items: every expert's rows in tiles of 128, plus one partial tile per expert
+    const int64_t max_tiles = ceil_div(g.total_rows, BM) + g.E;
+    const int total = (int)std::min<int64_t>(max_tiles * p.n_tiles, 1 << 30);
+    return dispatch(bn, true, p, total, stream);
+}
+
+} // namespace nv4

@@ -1,0 +1,428 @@
+// W4A8 GEMM: FP8 (E4M3, per-token FP32 scale) activations x NVFP4 weights, the
+// route "llama.cpp Put Precision Policy Inside the Model. That Matters More
+// Than W4A4", section "One model can need more than one precision", gives the
+// layers its metadata marks as sensitive.
+//
+//   Y[m][n] = s_t[m] * s_w * sum_k E4M3(a[m][k]) * E2M1(w[n][k]) * E4M3(ew[n][k/16])
+//
+// Exactness: an E4M3 value and an E2M1 x E4M3 product (at most 6 significant
+// bits, magnitudes 2^-10 .. 2688) are both exact in FP16, so converter warps
+// expand both operands to FP16 in shared memory and tcgen05.mma kind::f16
+// (FP16 x FP16 -> FP32) contracts them; no requantisation of the weights.
+// The block-scaled FP8 MMA kinds use power-of-two scales per 32 elements and
+// cannot carry the weights' E4M3 scales per 16 elements exactly.
+//
+// Pipeline (persistent, one CTA per SM, 320 threads):
+//   warp 0      TMA: raw FP8 A tile [128 x 64 B], raw FP4 W tile [BN x 32 B]
+//               and the W scale atom(s) per 64-element K step (raw ring)
+//   warp 1      TMEM alloc; lane 0 issues 4 x tcgen05.mma (K = 16) per step
+//   warps 2..5  converters: raw ring -> FP16 tiles (128-byte swizzled rows)
+//   warps 6..9  epilogue: TMEM -> registers, * s_t[m] * s_w, BF16/FP32 store
+#include <algorithm>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace nv4 {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int KSTEP = 64;       // K elements per pipeline step
+constexpr int RAW_STAGES = 4;
+constexpr int CONV_STAGES = 3;
+constexpr int ACC_BUFS = 2;
+constexpr int CONV_WARPS = 4;
+constexpr int EPI_WARPS = 4;
+constexpr int THREADS = 64 + 32 * (CONV_WARPS + EPI_WARPS);
+constexpr int RAW_A = BM * KSTEP;           // 8192 B of FP8
+constexpr int RAW_W = BN * KSTEP / 2;       // 4096 B of FP4 codes
+constexpr int RAW_S = (BN / 128) * 512;     // scale atom(s)
+constexpr int RAW_BYTES = RAW_A + RAW_W + RAW_S + 512; // keep 1024-aligned stages
+constexpr int CONV_A = BM * 128;            // FP16 rows of 128 bytes
+constexpr int CONV_B = BN * 128;
+constexpr int CONV_BYTES = CONV_A + CONV_B;
+constexpr int TMEM_COLS = 256;
+constexpr int SMEM_BYTES = CONV_STAGES * CONV_BYTES + RAW_STAGES * RAW_BYTES + 256 + 1024;
+static_assert(RAW_BYTES % 1024 == 0 && CONV_BYTES % 1024 == 0, "alignment");
+static_assert(SMEM_BYTES <= 232448, "shared memory");
+static_assert(ACC_BUFS * BN <= TMEM_COLS, "TMEM");
+
+struct Params {
+    CUtensorMap tmap_a; // FP8 [M][K]
+    CUtensorMap tmap_w; // FP4 codes [N][K/2]
+    const uint8_t *w_scales;
+    const float *s_t;
+    const float *w_second;
+    void *out;
+    int64_t ldy, M, N;
+    int32_t m_tiles, n_tiles, ksteps, k64_total, out_dtype, vec_ok;
+    uint32_t *status;
+    uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ void decode(const Params &p, int item, int &tm, int &tn)
+{
+    constexpr int G = 8;
+    const int band = G * p.n_tiles;
+    const int bid = item / band;
+    const int first = bid * G;
+    const int gs = min(p.m_tiles - first, G);
+    const int r = item - bid * band;
+    tm = first + r % gs;
+    tn = r / gs;
+}
+
+__device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t two_bytes)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)two_bytes));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t f16x2_from_e2m1x2(uint32_t byte)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(r) : "r"(byte));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b)
+{
+    __half2 r = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+
+__device__ __forceinline__ void timeout(const Params &p, volatile int *abort_flag)
+{
+    *abort_flag = 1;
+    atomicOr(p.status, ST_TIMEOUT);
+}
+
+__global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant__ Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *conv = smem;
+    uint8_t *raw = smem + CONV_STAGES * CONV_BYTES;
+    uint64_t *raw_full = reinterpret_cast<uint64_t *>(raw + RAW_STAGES * RAW_BYTES);
+    uint64_t *raw_empty = raw_full + RAW_STAGES;
+    uint64_t *conv_full = raw_empty + RAW_STAGES;
+    uint64_t *conv_empty = conv_full + CONV_STAGES;
+    uint64_t *acc_full = conv_empty + CONV_STAGES;
+    uint64_t *acc_empty = acc_full + ACC_BUFS;
+    uint64_t *drain = acc_empty + ACC_BUFS;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr unsigned FULLMASK = 0xFFFFFFFFu;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < RAW_STAGES; ++s) {
+            mbar_init(&raw_full[s], 1);
+            mbar_init(&raw_empty[s], CONV_WARPS);
+        }
+        for (int s = 0; s < CONV_STAGES; ++s) {
+            mbar_init(&conv_full[s], CONV_WARPS);
+            mbar_init(&conv_empty[s], 1);
+        }
+        for (int b = 0; b < ACC_BUFS; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], EPI_WARPS);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int total = p.m_tiles * p.n_tiles;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        int st = 0, issued = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        if (lane == 0) {
+            for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+                int tm, tn;
+                decode(p, item, tm, tn);
+                for (int ks = 0; ks < p.ksteps; ++ks) {
+                    if (!mbar_wait(&raw_empty[st], ph ^ 1u, p.timeout_ns, abort_flag)) {
+                        timeout(p, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *r = raw + st * RAW_BYTES;
+                    mbar_arrive_expect_tx(&raw_full[st], RAW_A + RAW_W + RAW_S);
+                    tma_load_2d(r, &p.tmap_a, ks * KSTEP, tm * BM, &raw_full[st]);
+                    tma_load_2d(r + RAW_A, &p.tmap_w, ks * (KSTEP / 2), tn * BN, &raw_full[st]);
+                    bulk_load(r + RAW_A + RAW_W, p.w_scales + ((size_t)tn * p.k64_total + ks) * 512, RAW_S,
+                              &raw_full[st]);
+                    ++issued;
+                    if (++st == RAW_STAGES) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            const int n = min(issued, RAW_STAGES);
+            for (int q = 0; q < n; ++q) {
+                if (--st < 0) {
+                    st = RAW_STAGES - 1;
+                    ph ^= 1u;
+                }
+                mbar_wait(&raw_full[st], ph, p.timeout_ns, nullptr);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16(BN);
+            int cs = 0, acc = 0;
+            uint32_t cph = 0, aph = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+                if (!mbar_wait(&acc_empty[acc], aph ^ 1u, p.timeout_ns, abort_flag)) {
+                    timeout(p, abort_flag);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + acc * BN;
+                uint32_t accumulate = 0;
+                for (int ks = 0; ks < p.ksteps; ++ks) {
+                    if (!mbar_wait(&conv_full[cs], cph, p.timeout_ns, abort_flag)) {
+                        timeout(p, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t *cA = conv + cs * CONV_BYTES;
+                    const uint64_t ad = sdesc_sw128(smem_u32(cA));
+                    const uint64_t bd = sdesc_sw128(smem_u32(cA + CONV_A));
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) { // 16 FP16 = 32 bytes per MMA
+                        mma_f16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, accumulate);
+                        accumulate = 1;
+                    }
+                    tc_commit(&conv_empty[cs]);
+                    if (++cs == CONV_STAGES) {
+                        cs = 0;
+                        cph ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                tc_commit(&acc_full[acc]);
+                if (++acc == ACC_BUFS) {
+                    acc = 0;
+                    aph ^= 1u;
+                }
+            }
+            tc_commit(drain);
+            mbar_wait(drain, 0, p.timeout_ns, nullptr);
+        }
+        __syncwarp();
+    } else if (warp < 2 + CONV_WARPS) {
+        // ------------------------------------------------------------ converters
+        const int t = threadIdx.x - 64; // 0..127: tile row
+        int rs = 0, cs = 0;
+        uint32_t rph = 0, cph = 0;
+        for (int item = blockIdx.x; item < total; item += gridDim.x) {
+            bool ok = true;
+            for (int ks = 0; ks < p.ksteps; ++ks) {
+                const bool g1 = mbar_wait(&raw_full[rs], rph, p.timeout_ns, abort_flag);
+                const bool g2 = g1 && mbar_wait(&conv_empty[cs], cph ^ 1u, p.timeout_ns, abort_flag);
+                if (!__all_sync(FULLMASK, g2)) {
+                    if (lane == 0)
+                        timeout(p, abort_flag);
+                    ok = false;
+                    break;
+                }
+                const uint8_t *r = raw + rs * RAW_BYTES;
+                uint8_t *cA = conv + cs * CONV_BYTES;
+                uint8_t *cB = cA + CONV_A;
+                // A row t: 64 FP8 -> 64 FP16 (8 chunks of 16 bytes, swizzled)
+                {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(r + t * KSTEP);
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const uint4 v = src[h]; // 16 FP8 -> 2 output chunks
+                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                        uint32_t o[8];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            o[2 * q] = f16x2_from_e4m3x2(w[q] & 0xFFFFu);
+                            o[2 * q + 1] = f16x2_from_e4m3x2(w[q] >> 16);
+                        }
+                        const int c0 = 2 * h, c1 = 2 * h + 1;
+                        *reinterpret_cast<uint4 *>(cA + t * 128 + ((c0 ^ (t & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                        *reinterpret_cast<uint4 *>(cA + t * 128 + ((c1 ^ (t & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                }
+                // W row t: 32 code bytes (64 E2M1) x 4 E4M3 scales -> 64 FP16
+                {
+                    const uint8_t *wr = r + RAW_A + t * (KSTEP / 2);
+                    const uint32_t sc = *reinterpret_cast<const uint32_t *>(r + RAW_A + RAW_W + (t & 31) * 16 +
+                                                                           ((t & 127) >> 5) * 4);
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) { // 16-element block b uses scale byte b
+                        const uint32_t s2 = f16x2_from_e4m3x2(((sc >> (8 * b)) & 0xFFu) * 0x0101u);
+                        const uint2 v = *reinterpret_cast<const uint2 *>(wr + b * 8);
+                        const uint32_t w[2] = {v.x, v.y};
+                        uint32_t o[8];
+#pragma unroll
+                        for (int q = 0; q < 2; ++q)
+#pragma unroll
+                            for (int y = 0; y < 4; ++y)
+                                o[4 * q + y] = hmul2_u32(f16x2_from_e2m1x2((w[q] >> (8 * y)) & 0xFFu), s2);
+                        const int c0 = 2 * b, c1 = 2 * b + 1;
+                        *reinterpret_cast<uint4 *>(cB + t * 128 + ((c0 ^ (t & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                        *reinterpret_cast<uint4 *>(cB + t * 128 + ((c1 ^ (t & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&conv_full[cs]);
+                    mbar_arrive(&raw_empty[rs]);
+                }
+                if (++rs == RAW_STAGES) {
+                    rs = 0;
+                    rph ^= 1u;
+                }
+                if (++cs == CONV_STAGES) {
+                    cs = 0;
+                    cph ^= 1u;
+                }
+            }
+            if (!ok)
+                break;
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        int acc = 0;
+        uint32_t aph = 0;
+        const float sw = *p.w_second;
+        for (int item = blockIdx.x; item < total; item += gridDim.x) {
+            int tm, tn;
+            decode(p, item, tm, tn);
+            const bool got = mbar_wait(&acc_full[acc], aph, p.timeout_ns, abort_flag);
+            if (!__all_sync(FULLMASK, got)) {
+                if (lane == 0)
+                    timeout(p, abort_flag);
+                break;
+            }
+            tc_fence_after();
+            const int64_t i = (int64_t)tm * BM + row;
+            const float alpha = i < p.M ? p.s_t[i] * sw : 0.0f;
+            const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t v[32];
+                tc_ld_32x32b_x32(tb + c0, v);
+                tc_wait_ld();
+                if (i < p.M) {
+                    const int64_t j0 = (int64_t)tn * BN + c0;
+                    if (p.vec_ok && j0 + 32 <= p.N) {
+                        if (p.out_dtype == NVFP4_OUT_BF16) {
+                            uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + i * p.ldy + j0);
+#pragma unroll
+                            for (int c = 0; c < 32; c += 8) {
+                                uint32_t w[4];
+#pragma unroll
+                                for (int z = 0; z < 4; ++z) {
+                                    __nv_bfloat162 h = __floats2bfloat162_rn(alpha * __uint_as_float(v[c + 2 * z]),
+                                                                             alpha * __uint_as_float(v[c + 2 * z + 1]));
+                                    w[z] = *reinterpret_cast<uint32_t *>(&h);
+                                }
+                                o[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
+                            }
+                        } else {
+                            float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + i * p.ldy + j0);
+#pragma unroll
+                            for (int c = 0; c < 32; c += 4)
+                                o[c / 4] = make_float4(alpha * __uint_as_float(v[c]), alpha * __uint_as_float(v[c + 1]),
+                                                       alpha * __uint_as_float(v[c + 2]), alpha * __uint_as_float(v[c + 3]));
+                        }
+                    } else {
+                        for (int c = 0; c < 32 && j0 + c < p.N; ++c) {
+                            const float y = alpha * __uint_as_float(v[c]);
+                            if (p.out_dtype == NVFP4_OUT_BF16)
+                                static_cast<__nv_bfloat16 *>(p.out)[i * p.ldy + j0 + c] = __float2bfloat16_rn(y);
+                            else
+                                static_cast<float *>(p.out)[i * p.ldy + j0 + c] = y;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&acc_empty[acc]);
+            if (++acc == ACC_BUFS) {
+                acc = 0;
+                aph ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+} // namespace
+
+cudaError_t launch_w4a8(const W4A8GemmArgs &g, cudaStream_t stream)
+{
+    if (g.K % KSTEP != 0)
+        return cudaErrorInvalidValue;
+    Params p{};
+    CUresult r = make_tmap_2d_u8(&p.tmap_a, g.a_fp8, (uint64_t)g.K, (uint64_t)g.M, (uint64_t)g.K, KSTEP, BM, false);
+    if (r != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    r = make_tmap_2d_u8(&p.tmap_w, g.w_codes, (uint64_t)(g.K / 2), (uint64_t)g.N, (uint64_t)(g.K / 2), KSTEP / 2, BN,
+                        false);
+    if (r != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    p.w_scales = g.w_scales;
+    p.s_t = g.s_t;
+    p.w_second = g.w_second;
+    p.out = g.out;
+    p.ldy = g.ldy;
+    p.M = g.M;
+    p.N = g.N;
+    p.m_tiles = (int)ceil_div(g.M, BM);
+    p.n_tiles = (int)ceil_div(g.N, BN);
+    p.ksteps = (int)(g.K / KSTEP);
+    p.k64_total = (int)(g.K / 64);
+    p.out_dtype = g.out_dtype;
+    const int esz = g.out_dtype == NVFP4_OUT_BF16 ? 2 : 4;
+    p.vec_ok = ((g.ldy * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(g.out) % 16) == 0) ? 1 : 0;
+    p.status = g.status;
+    p.timeout_ns = g.timeout_ns;
+    cudaError_t e = cudaFuncSetAttribute(w4a8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess)
+        return e;
+    const int total = p.m_tiles * p.n_tiles;
+    const int grid = std::max(1, std::min(total, device_sm_count()));
+    w4a8_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(p);
+    return cudaGetLastError();
+}
+
+} // namespace nv4

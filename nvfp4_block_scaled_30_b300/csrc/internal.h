@@ -1,0 +1,122 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/nvfp4.h"
+
+namespace nv4 {
+
+// Workspace header: the first 256 bytes; word 0 is the sticky device status.
+constexpr size_t WS_HEADER = 256;
+constexpr uint32_t ST_NONFINITE = 1u;
+constexpr uint32_t ST_TIMEOUT = 2u;
+// Partial maxima written by the first quantiser pass (one word per CTA).
+constexpr int AMAX_MAX_CTAS = 1024;
+constexpr size_t WS_AMAX_BYTES = AMAX_MAX_CTAS * sizeof(uint32_t);
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int device_sm_count();
+
+// ---- quantisers (quantize.cu) ------------------------------------------------
+cudaError_t launch_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx, uint8_t *codes,
+                                  uint8_t *scales, void *second, int mode, int layout, uint32_t *amax_partial,
+                                  uint32_t *status, cudaStream_t stream);
+cudaError_t launch_fp8_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx, uint8_t *a, float *s_t,
+                                uint32_t *status, cudaStream_t stream);
+cudaError_t launch_probe_convert(const float *in, int64_t n, uint8_t *o2, uint8_t *o3, cudaStream_t stream);
+cudaError_t launch_finalize_bf16(const float *acc, int64_t rows, int64_t cols, int64_t ld_acc, uint16_t *y,
+                                 int64_t ldy, cudaStream_t stream);
+
+// ---- GEMMs (gemm.cu) -----------------------------------------------------------
+struct DenseGemmArgs {
+    // MMA operand A (M side, tiles of 128 rows) and B (N side).
+    const uint8_t *a_codes;
+    const uint8_t *a_scales; // tiled
+    const float *a_second;
+    int64_t a_rows;
+    const uint8_t *b_codes;
+    const uint8_t *b_scales; // tiled
+    const float *b_second;
+    int64_t b_rows;
+    int64_t K;
+    // output element (i, j) of the accumulator tile goes to out[i*ld_i + j*ld_j]
+    void *out;
+    int64_t ld_i, ld_j;
+    int out_dtype;           // 0 bf16, 1 fp32
+    // stream-K (spread K stages evenly over the SMs): partial tiles are summed
+    // into acc (FP32, index i*acc_ld_i + j*acc_ld_j) with per-tile stage
+    // counters; both are zero between calls and left zero by the kernel.
+    bool streamk;
+    float *acc;
+    int64_t acc_ld_i, acc_ld_j;
+    uint32_t *tile_cnt;
+    uint32_t *status;
+    uint64_t timeout_ns;
+};
+cudaError_t launch_w4a4_dense(const DenseGemmArgs &g, cudaStream_t stream);
+int w4a4_dense_bn(int64_t b_rows);
+
+struct GroupedGemmArgs {
+    const uint8_t *a_codes;
+    const uint8_t *a_scales; // tiled, rows padded to 128
+    const float *a_second;
+    int64_t a_rows;
+    const int32_t *row_idx;  // may be null
+    const int64_t *offsets;  // device [E+1]
+    int E;
+    const uint8_t *w_codes;  // [E*N][K/2]
+    const uint8_t *w_scales; // tiled over E*N rows
+    const float *w_second;   // [E]
+    int64_t N, K;
+    void *out;
+    int64_t ldy;
+    int out_dtype;
+    int64_t total_rows;
+    uint32_t *status;
+    uint64_t timeout_ns;
+};
+cudaError_t launch_w4a4_grouped(const GroupedGemmArgs &g, cudaStream_t stream);
+
+struct W4A8GemmArgs {
+    const uint8_t *a_fp8;    // [M][K]
+    const float *s_t;        // [M]
+    int64_t M;
+    const uint8_t *w_codes;  // [N][K/2]
+    const uint8_t *w_scales; // tiled
+    const float *w_second;
+    int64_t N, K;
+    void *out;
+    int64_t ldy;
+    int out_dtype;
+    uint32_t *status;
+    uint64_t timeout_ns;
+};
+cudaError_t launch_w4a8(const W4A8GemmArgs &g, cudaStream_t stream);
+
+struct MacroGemmArgs {
+    const uint8_t *a_codes;
+    const uint8_t *a_scales;  // tiled
+    const uint16_t *a_macro;  // [M][K/256] binary16
+    int64_t M;
+    const uint8_t *w_codes;
+    const uint8_t *w_scales;  // tiled
+    const uint16_t *w_macro;  // [N][K/256]
+    int64_t N, K;
+    void *out;
+    int64_t ldy;
+    int out_dtype;
+    uint32_t *status;
+    uint64_t timeout_ns;
+};
+cudaError_t launch_w4a4_macro(const MacroGemmArgs &g, cudaStream_t stream);
+
+// Tensor-map creation through the driver entry point (no libcuda link).
+CUresult make_tmap_2d_u8(CUtensorMap *map, const void *base, uint64_t inner_bytes, uint64_t rows,
+                         uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128);
+
+} // namespace nv4

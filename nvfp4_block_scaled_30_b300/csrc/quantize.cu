@@ -1,0 +1,354 @@
+// Quantisers on the NVFP4 hot path.
+//
+// NVFP4 encode follows "NVIDIA Ships TensorRT-LLM 0.16: Native FP4
+// Quantization for Blackwell B200", section "The Mathematical Breakthrough of
+// Microscopic FP4 Scaling", item 2 "Two-Level Block Scaling": one E4M3 scale
+// per 16 consecutive elements and a second level that is either one FP32
+// tensor scale (amax / (6 * 448)) or one FP16 macro-scale per 16 micro-vectors
+// (256 elements).  Per-token FP8 encode serves the W4A8 route of "llama.cpp
+// Put Precision Policy Inside the Model. That Matters More Than W4A4",
+// section "One model can need more than one precision".
+//
+// All encode arithmetic is IEEE binary32 with explicit round-to-nearest
+// intrinsics, in this order per 16-element block:
+//   t = amax_b / 6, u = t / s, e = E4M3(u) (0 when s == 0), d = e * s,
+//   r = 1 / d (0 when d == 0, at most FLT_MAX), code = E2M1(x * r).
+//
+// Memory: each thread owns 8 consecutive BF16 values (one 16-byte load);
+// a lane pair owns one 16-element block (absmax by one shfl.xor); the pair
+// writes 8 packed code bytes (one 32-bit store each) and one scale byte.
+#include <cfloat>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace nv4 {
+
+namespace {
+
+constexpr int QT = 256; // threads per quantiser CTA
+constexpr unsigned FULL = 0xFFFFFFFFu;
+
+__device__ __forceinline__ void bf16x8(const uint16_t *p, float (&f)[8])
+{
+    uint4 v = __ldg(reinterpret_cast<const uint4 *>(p));
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t *red)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = max(v, __shfl_xor_sync(FULL, v, o));
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0)
+        red[w] = v;
+    __syncthreads();
+    uint32_t r = 0;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i)
+        r = max(r, red[i]);
+    __syncthreads();
+    return r;
+}
+
+// Reciprocal of a dequantisation step: 0 for 0, clamped to the largest float.
+__device__ __forceinline__ float recip_step(float d)
+{
+    return d == 0.0f ? 0.0f : fminf(__frcp_rn(d), FLT_MAX);
+}
+
+// E4M3 scale code of a block with absolute maximum amax_b under second-level s.
+__device__ __forceinline__ uint32_t block_scale_code(float amax_b, float s)
+{
+    if (s == 0.0f)
+        return 0u;
+    float t = __fdiv_rn(amax_b, 6.0f);
+    float u = __fdiv_rn(t, s);
+    return e4m3(u);
+}
+
+// 8 values times r -> 4 packed E2M1 bytes (element 0 in the lowest nibble).
+__device__ __forceinline__ uint32_t pack8(const float (&f)[8], float r)
+{
+    uint32_t p = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        p |= e2m1x2(__fmul_rn(f[2 * i], r), __fmul_rn(f[2 * i + 1], r)) << (8 * i);
+    return p;
+}
+
+__device__ __forceinline__ size_t scale_offset(int64_t row, int64_t blk, int64_t K, bool tiled)
+{
+    if (!tiled)
+        return (size_t)(row * (K / 16) + blk);
+    int64_t r = row & 127;
+    return (size_t)(((row >> 7) * (K / 64) + (blk >> 2)) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (blk & 3));
+}
+
+// Pass 1: per-CTA maximum of |x| (as BF16 magnitude bits) and a non-finite flag.
+__global__ void __launch_bounds__(QT) amax_partial_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t K,
+                                                          int64_t ldx, uint32_t *__restrict__ partial,
+                                                          uint32_t *__restrict__ status)
+{
+    __shared__ uint32_t red[QT / 32];
+    const int64_t cpr = K / 8;
+    uint32_t m = 0, bad = 0;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const uint16_t *xr = x + row * ldx;
+        for (int64_t j = threadIdx.x; j < cpr; j += QT) {
+            uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr + j * 8));
+            uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t lo = w[i] & 0x7FFFu, hi = (w[i] >> 16) & 0x7FFFu;
+                bad |= (lo >= 0x7F80u) | (hi >= 0x7F80u);
+                m = max(m, max(lo, hi));
+            }
+        }
+    }
+    bad = __any_sync(FULL, bad);
+    uint32_t bm = block_max_u32(m, red);
+    if (threadIdx.x == 0) {
+        partial[blockIdx.x] = bm;
+        if (bad)
+            atomicOr(status, ST_NONFINITE);
+    }
+    if (bad && (threadIdx.x & 31) == 0)
+        atomicOr(status, ST_NONFINITE);
+}
+
+// Pass 2, tensor-scale mode.  Every CTA reduces the partial maxima itself,
+// so no extra launch or host synchronisation is needed.  Rows rows..rows_pad
+// (tiled layout padding) get zero scales.
+template <bool TILED>
+__global__ void __launch_bounds__(QT) nvfp4_encode_kernel(const uint16_t *__restrict__ x, int64_t rows,
+                                                          int64_t rows_pad, int64_t K, int64_t ldx,
+                                                          uint8_t *__restrict__ codes, uint8_t *__restrict__ scales,
+                                                          float *__restrict__ sg_out,
+                                                          const uint32_t *__restrict__ partial, int n_partial)
+{
+    __shared__ uint32_t red[QT / 32];
+    uint32_t m = 0;
+    for (int i = threadIdx.x; i < n_partial; i += QT)
+        m = max(m, partial[i]);
+    const float amax = __uint_as_float(block_max_u32(m, red) << 16);
+    const float sg = __fdiv_rn(amax, 2688.0f);
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        *sg_out = sg;
+
+    const int64_t cpr = K / 8;
+    for (int64_t row = blockIdx.x; row < rows_pad; row += gridDim.x) {
+        const bool real_row = row < rows;
+        for (int64_t j0 = 0; j0 < cpr; j0 += QT) {
+            const int64_t j = j0 + threadIdx.x;
+            const bool valid = j < cpr;
+            const bool real = valid && real_row;
+            float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            if (real)
+                bf16x8(x + row * ldx + j * 8, f);
+            float am = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                am = fmaxf(am, fabsf(f[i]));
+            const float amb = fmaxf(am, __shfl_xor_sync(FULL, am, 1));
+            const uint32_t e = real ? block_scale_code(amb, sg) : 0u;
+            const float r = recip_step(__fmul_rn(e4m3_value(e), sg));
+            if (real)
+                *reinterpret_cast<uint32_t *>(codes + row * (K / 2) + j * 4) = pack8(f, r);
+            if (valid && (threadIdx.x & 1) == 0)
+                scales[scale_offset(row, j >> 1, K, TILED)] = (uint8_t)e;
+        }
+    }
+}
+
+// Macro mode: one warp covers 32 chunks = 256 elements = one macro group (K is
+// a multiple of 256 and the chunk loop advances in whole CTAs of 8 warps).
+template <bool TILED>
+__global__ void __launch_bounds__(QT) nvfp4_encode_macro_kernel(const uint16_t *__restrict__ x, int64_t rows,
+                                                                int64_t rows_pad, int64_t K, int64_t ldx,
+                                                                uint8_t *__restrict__ codes,
+                                                                uint8_t *__restrict__ scales,
+                                                                uint16_t *__restrict__ macro,
+                                                                uint32_t *__restrict__ status)
+{
+    const int64_t cpr = K / 8;
+    uint32_t bad = 0;
+    for (int64_t row = blockIdx.x; row < rows_pad; row += gridDim.x) {
+        const bool real_row = row < rows;
+        for (int64_t j0 = 0; j0 < cpr; j0 += QT) {
+            const int64_t j = j0 + threadIdx.x;
+            const bool valid = j < cpr;
+            const bool real = valid && real_row;
+            float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            if (real) {
+                bf16x8(x + row * ldx + j * 8, f);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    bad |= (__float_as_uint(f[i]) & 0x7F800000u) == 0x7F800000u;
+            }
+            float am = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                am = fmaxf(am, fabsf(f[i]));
+            const float amb = fmaxf(am, __shfl_xor_sync(FULL, am, 1));
+            float ag = amb;
+#pragma unroll
+            for (int o = 2; o < 32; o <<= 1)
+                ag = fmaxf(ag, __shfl_xor_sync(FULL, ag, o));
+            float q = __fdiv_rn(ag, 2688.0f);
+            q = fminf(q, 65504.0f);
+            const __half h = __float2half_rn(q);
+            const float S = __half2float(h);
+            const uint32_t e = real ? block_scale_code(amb, S) : 0u;
+            const float r = recip_step(__fmul_rn(e4m3_value(e), S));
+            if (real) {
+                *reinterpret_cast<uint32_t *>(codes + row * (K / 2) + j * 4) = pack8(f, r);
+                if ((threadIdx.x & 31) == 0)
+                    macro[row * (K / 256) + (j >> 5)] = __half_as_ushort(h);
+            }
+            if (valid && (threadIdx.x & 1) == 0)
+                scales[scale_offset(row, j >> 1, K, TILED)] = (uint8_t)e;
+        }
+    }
+    if (__any_sync(FULL, bad) && (threadIdx.x & 31) == 0)
+        atomicOr(status, ST_NONFINITE);
+}
+
+__device__ __forceinline__ uint32_t e4m3_signed(float v)
+{
+    return (e4m3(v) & 0x7Fu) | ((__float_as_uint(v) >> 31) << 7);
+}
+
+// Per-token FP8: one CTA per row (grid-stride); pass 1 finds the row maximum,
+// pass 2 (re-reading the row from L1/L2) encodes 8 elements per thread.
+__global__ void __launch_bounds__(QT) fp8_token_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t K,
+                                                       int64_t ldx, uint8_t *__restrict__ a,
+                                                       float *__restrict__ s_t, uint32_t *__restrict__ status)
+{
+    __shared__ uint32_t red[QT / 32];
+    const int64_t cpr = K / 8;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const uint16_t *xr = x + row * ldx;
+        uint32_t m = 0, bad = 0;
+        for (int64_t j = threadIdx.x; j < cpr; j += QT) {
+            uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr + j * 8));
+            uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t lo = w[i] & 0x7FFFu, hi = (w[i] >> 16) & 0x7FFFu;
+                bad |= (lo >= 0x7F80u) | (hi >= 0x7F80u);
+                m = max(m, max(lo, hi));
+            }
+        }
+        if (__any_sync(FULL, bad) && (threadIdx.x & 31) == 0)
+            atomicOr(status, ST_NONFINITE);
+        const float amax = __uint_as_float(block_max_u32(m, red) << 16);
+        const float s = __fdiv_rn(amax, 448.0f);
+        const float r = recip_step(s);
+        if (threadIdx.x == 0)
+            s_t[row] = s;
+        for (int64_t j = threadIdx.x; j < cpr; j += QT) {
+            float f[8];
+            bf16x8(xr + j * 8, f);
+            uint32_t lo = 0, hi = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                lo |= e4m3_signed(__fmul_rn(f[i], r)) << (8 * i);
+                hi |= e4m3_signed(__fmul_rn(f[4 + i], r)) << (8 * i);
+            }
+            *reinterpret_cast<uint2 *>(a + row * K + j * 8) = make_uint2(lo, hi);
+        }
+    }
+}
+
+__global__ void probe_convert_kernel(const float *__restrict__ in, int64_t n, uint8_t *__restrict__ o2,
+                                     uint8_t *__restrict__ o3)
+{
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const float v = in[i];
+        o2[i] = (uint8_t)(e2m1x2(v, 0.0f) & 0xFu);
+        o3[i] = (uint8_t)e4m3_signed(v);
+    }
+}
+
+// Split-K epilogue for BF16 outputs: y = bf16_rn(acc).
+__global__ void finalize_bf16_kernel(const float *__restrict__ acc, int64_t rows, int64_t cols, int64_t ld_acc,
+                                     uint16_t *__restrict__ y, int64_t ldy)
+{
+    const int64_t total = rows * cols;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / cols, c = i - r * cols;
+        y[r * ldy + c] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[r * ld_acc + c]));
+    }
+}
+
+} // namespace
+
+cudaError_t launch_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx, uint8_t *codes,
+                                  uint8_t *scales, void *second, int mode, int layout, uint32_t *amax_partial,
+                                  uint32_t *status, cudaStream_t stream)
+{
+    const bool tiled = layout == NVFP4_LAYOUT_MMA_TILED;
+    const int64_t rows_pad = tiled ? ceil_div(rows, 128) * 128 : rows;
+    const int sms = device_sm_count();
+    if (rows_pad == 0)
+        return cudaSuccess;
+    const int grid2 = (int)std::min<int64_t>(rows_pad, (int64_t)sms * 8);
+    if (mode == NVFP4_SCALE_TENSOR_FP32) {
+        const int grid1 = (int)std::min<int64_t>(std::max<int64_t>(rows, 1), std::min(AMAX_MAX_CTAS, sms * 4));
+        amax_partial_kernel<<<grid1, QT, 0, stream>>>(x, rows, K, ldx, amax_partial, status);
+        if (tiled)
+            nvfp4_encode_kernel<true><<<grid2, QT, 0, stream>>>(x, rows, rows_pad, K, ldx, codes, scales,
+                                                                  static_cast<float *>(second), amax_partial, grid1);
+        else
+            nvfp4_encode_kernel<false><<<grid2, QT, 0, stream>>>(x, rows, rows_pad, K, ldx, codes, scales,
+                                                                   static_cast<float *>(second), amax_partial, grid1);
+    } else {
+        if (tiled)
+            nvfp4_encode_macro_kernel<true><<<grid2, QT, 0, stream>>>(x, rows, rows_pad, K, ldx, codes, scales,
+                                                                        static_cast<uint16_t *>(second), status);
+        else
+            nvfp4_encode_macro_kernel<false><<<grid2, QT, 0, stream>>>(x, rows, rows_pad, K, ldx, codes, scales,
+                                                                         static_cast<uint16_t *>(second), status);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx, uint8_t *a, float *s_t,
+                                uint32_t *status, cudaStream_t stream)
+{
+    if (rows == 0)
+        return cudaSuccess;
+    const int grid = (int)std::min<int64_t>(rows, (int64_t)device_sm_count() * 8);
+    fp8_token_kernel<<<grid, QT, 0, stream>>>(x, rows, K, ldx, a, s_t, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_probe_convert(const float *in, int64_t n, uint8_t *o2, uint8_t *o3, cudaStream_t stream)
+{
+    if (n == 0)
+        return cudaSuccess;
+    const int grid = (int)std::min<int64_t>(ceil_div(n, 256), (int64_t)device_sm_count() * 16);
+    probe_convert_kernel<<<grid, 256, 0, stream>>>(in, n, o2, o3);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_finalize_bf16(const float *acc, int64_t rows, int64_t cols, int64_t ld_acc, uint16_t *y,
+                                 int64_t ldy, cudaStream_t stream)
+{
+    const int64_t total = rows * cols;
+    if (total == 0)
+        return cudaSuccess;
+    const int grid = (int)std::min<int64_t>(ceil_div(total, 256), (int64_t)device_sm_count() * 8);
+    finalize_bf16_kernel<<<grid, 256, 0, stream>>>(acc, rows, cols, ld_acc, y, ldy);
+    return cudaGetLastError();
+}
+
+} // namespace nv4

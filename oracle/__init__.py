@@ -57,6 +57,10 @@ def lib():
         L.orc_fp16_encode.argtypes = [ctypes.c_float]
         L.orc_bf16_value.restype = ctypes.c_float
         L.orc_bf16_value.argtypes = [ctypes.c_uint32]
+        L.orc_e2m1_encode_array.restype = None
+        L.orc_e2m1_encode_array.argtypes = [_f32, _I64, _u8]
+        L.orc_e4m3_encode_array.restype = None
+        L.orc_e4m3_encode_array.argtypes = [_f32, _I64, _u8]
         L.orc_nvfp4_encode.restype = ctypes.c_int
         L.orc_nvfp4_encode.argtypes = [_u16, _I64, _I64, _I64, _u8, _u8, _f32]
         L.orc_nvfp4_encode_macro.restype = ctypes.c_int
@@ -110,6 +114,20 @@ def e4m3_value(code):
 
 def e4m3_encode(u):
     return lib().orc_e4m3_encode(float(u))
+
+
+def e2m1_encode_array(v):
+    v = _c(v, np.float32).ravel()
+    out = np.empty(v.size, np.uint8)
+    lib().orc_e2m1_encode_array(v, v.size, out)
+    return out
+
+
+def e4m3_encode_array(v):
+    v = _c(v, np.float32).ravel()
+    out = np.empty(v.size, np.uint8)
+    lib().orc_e4m3_encode_array(v, v.size, out)
+    return out
 
 
 def fp16_value(h):

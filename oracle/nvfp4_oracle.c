@@ -108,24 +108,44 @@ __attribute__((constructor)) static void fill_e4m3_table(void)
         E4M3_POS[c] = orc_e4m3_value(c);
 }
 
-/* Nearest finite E4M3 value by exhaustive search over the 127 non-negative
- * codes, ties to the even code, saturating at 448. */
+/* Nearest finite E4M3 value, ties to the even code, saturating at 448.  The
+ * non-negative codes increase with their value, so a bisection over the
+ * table finds the two neighbours of |u|; the nearer one wins. */
 uint32_t orc_e4m3_encode(float u)
 {
     uint32_t sign = signbit(u) ? 0x80u : 0u;
     double a = fabs((double)u);
-    uint32_t best = 0;
-    double bestd = INFINITY;
     if (a >= 448.0)
         return sign | 0x7Eu;
-    for (uint32_t c = 0; c <= 0x7Eu; ++c) {
-        double dd = fabs(a - E4M3_POS[c]);
-        if (dd < bestd || (dd == bestd && (c & 1u) == 0)) {
-            best = c;
-            bestd = dd;
-        }
+    uint32_t lo = 0, hi = 0x7Eu;
+    while (hi - lo > 1u) { /* invariant: E4M3_POS[lo] <= a < E4M3_POS[hi] */
+        uint32_t mid = (lo + hi) / 2u;
+        if (E4M3_POS[mid] <= a)
+            lo = mid;
+        else
+            hi = mid;
     }
-    return sign | best;
+    double dl = a - E4M3_POS[lo], dh = E4M3_POS[hi] - a;
+    if (dl < dh)
+        return sign | lo;
+    if (dh < dl)
+        return sign | hi;
+    return sign | ((lo & 1u) ? hi : lo);
+}
+
+/* Element-wise encoders over arrays (same functions, OpenMP over i). */
+void orc_e2m1_encode_array(const float *in, int64_t n, uint8_t *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = (uint8_t)orc_e2m1_encode(in[i]);
+}
+
+void orc_e4m3_encode_array(const float *in, int64_t n, uint8_t *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = (uint8_t)orc_e4m3_encode(in[i]);
 }
 
 /* IEEE binary16: sign bit 15, exponent bits 14..10 (bias 15), mantissa 9..0. */

@@ -1,0 +1,32 @@
+"""Test helpers: layout permutations of the ABI's tiled scale format, the
+GEMM tolerance of the benchmark spec, and host/device moves.  No quantisation or
+contraction arithmetic lives here."""
+import numpy as np
+
+
+def tile_scales(rowmajor: np.ndarray, rows: int, K: int) -> np.ndarray:
+    """Row-major E4M3 scale bytes [rows, K/16] -> MMA-tiled bytes (rows padded
+    to 128 with zeros): byte (r % 32) * 16 + ((r % 128) // 32) * 4 + b % 4 of
+    atom (r // 128) * (K/64) + b // 4."""
+    rt = -(-rows // 128)
+    pad = np.zeros((rt * 128, K // 16), np.uint8)
+    pad[:rows] = rowmajor
+    t = pad.reshape(rt, 4, 32, K // 64, 4)            # [rt][sub][lane][kc][j]
+    return np.ascontiguousarray(t.transpose(0, 3, 2, 1, 4)).reshape(-1)
+
+
+def untile_scales(tiled: np.ndarray, rows: int, K: int) -> np.ndarray:
+    t = np.asarray(tiled, np.uint8).reshape(-1, K // 64, 32, 4, 4)   # [rt][kc][lane][sub][j]
+    return np.ascontiguousarray(t.transpose(0, 3, 2, 1, 4)).reshape(-1, K // 16)[:rows]
+
+
+def row_tolerance_ok(y_gpu: np.ndarray, y_ref: np.ndarray, rel: float = 1e-3):
+    """Per output row m: max_n |Y_gpu - Y_ref| <= rel * ||Y_ref[m, :]||_2
+    (zero rows must be exactly zero).  Returns (ok, worst ratio)."""
+    y_gpu = np.asarray(y_gpu, np.float64)
+    y_ref = np.asarray(y_ref, np.float64)
+    err = np.abs(y_gpu - y_ref).max(axis=1)
+    norm = np.sqrt((y_ref ** 2).sum(axis=1))
+    zero = norm == 0
+    ratio = np.where(zero, np.where(err == 0, 0.0, np.inf), err / np.where(zero, 1, norm))
+    return bool((ratio <= rel).all()), float(ratio.max(initial=0.0))

@@ -1,0 +1,170 @@
+"""W4A4 block-scaled GEMM on the tensor cores against the oracle.
+
+Exact cases (FP32 output; every partial sum is exactly representable):
+all 16x16 E2M1 code pairs, every non-negative E4M3 scale, one-hot rows.
+Tolerance cases: max_n |Y - Y_ref| <= 1e-3 * ||Y_ref[m, :]||_2 per row
+against the FP64 oracle, on configuration 1 in full, the decode shapes
+(M = 1, 8, 16 against the 28672 x 8192 weights) in full, the prefill shapes
+on sampled rows, and ragged shapes that exercise M/N/K tails and split-K."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_common import dev_bf16, host, nv, nvfp4_device, quantize_gpu, y_np
+from helpers import row_tolerance_ok
+
+pytestmark = pytest.mark.gpu
+
+ONE = 0x38
+C = synth.CONFIGS
+
+
+def pack(codes):
+    codes = np.asarray(codes, np.uint8)
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+
+
+def gemm_q(a, w, out_dtype=nv.OUT_FP32):
+    y = nv.gemm(w, a_q=a, out_dtype=out_dtype)
+    return y_np(y)
+
+
+@pytest.mark.parametrize("M", [16, 128])
+def test_all_code_pairs_exact(M):
+    # A row i: code (i + k) % 16 for k < 16, W row j: (j + 3k) % 16; K = 64 with
+    # zeros past k = 16; unit scales and tensor scales.  M = 16 runs the
+    # swapped (decode) orientation, M = 128 the direct one.
+    K = 64
+    ca = np.zeros((M, K), np.uint8)
+    cw = np.zeros((16, K), np.uint8)
+    for i in range(M):
+        ca[i, :16] = [(i + k) % 16 for k in range(16)]
+    for j in range(16):
+        cw[j, :16] = [(j + 3 * k) % 16 for k in range(16)]
+    sa = np.full((M, K // 16), ONE, np.uint8)
+    sw = np.full((16, K // 16), ONE, np.uint8)
+    a = nvfp4_device(pack(ca), sa, 1.0, M, K)
+    w = nvfp4_device(pack(cw), sw, 1.0, 16, K)
+    Y = gemm_q(a, w)
+    ref = oracle.gemm_w4a4((pack(ca), sa, 1.0), (pack(cw), sw, 1.0))
+    np.testing.assert_array_equal(Y, ref)
+
+
+def test_every_e4m3_scale_exact():
+    # only block 1 (k = 16..31) of the weights is non-zero, so every output is
+    # one scaled block sum: E4M3(m % 127) * E4M3(n) * sum_k a*w, exact in FP32
+    rng = np.random.default_rng(21)
+    K = 64
+    ca = rng.integers(0, 16, size=(128, K)).astype(np.uint8)
+    cw = np.zeros((127, K), np.uint8)
+    cw[:, 16:32] = rng.integers(0, 16, size=(127, 16))
+    sa = np.full((128, 4), ONE, np.uint8)
+    sw = np.full((127, 4), ONE, np.uint8)
+    sw[:, 1] = np.arange(127)
+    sa[:, 1] = (np.arange(128) % 127).astype(np.uint8)
+    a = nvfp4_device(pack(ca), sa, 1.0, 128, K)
+    w = nvfp4_device(pack(cw), sw, 1.0, 127, K)
+    Y = gemm_q(a, w)
+    ref = oracle.gemm_w4a4((pack(ca), sa, 1.0), (pack(cw), sw, 1.0))
+    np.testing.assert_array_equal(Y, ref)
+
+
+def test_one_hot_rows_read_out_weights():
+    rng = np.random.default_rng(22)
+    N, K = 256, 256
+    cw = rng.integers(0, 16, size=(N, K)).astype(np.uint8)
+    sw = rng.integers(0x20, 0x50, size=(N, K // 16)).astype(np.uint8)
+    A = np.zeros((K, K), np.uint8)
+    A[np.arange(K), np.arange(K)] = 2
+    sa = np.full((K, K // 16), ONE, np.uint8)
+    a = nvfp4_device(pack(A), sa, 0.125, K, K)
+    w = nvfp4_device(pack(cw), sw, 0.75, N, K)
+    Y = gemm_q(a, w)
+    ref = oracle.gemm_w4a4((pack(A), sa, 0.125), (pack(cw), sw, 0.75))
+    np.testing.assert_array_equal(Y, ref)
+
+
+def _layer(cfg, M, N, K, xtid=0, wtid=1):
+    c = C[cfg]
+    xb = synth.activations(cfg, xtid, M, K, c["outlier_frac"], c["outlier_factor"])
+    wb = synth.weights(cfg, wtid, N, K)
+    return xb, wb
+
+
+def _check(y, ref, what):
+    ok, worst = row_tolerance_ok(y, ref)
+    assert ok, f"{what}: worst row error ratio {worst:.3e} > 1e-3"
+
+
+@pytest.mark.parametrize("out_dtype", [nv.OUT_BF16, nv.OUT_FP32])
+def test_config1_full(out_dtype):
+    xb, wb = _layer(1, 128, 256, 512)
+    w, wc, ws, wg = quantize_gpu(wb)
+    oc, os_, og = oracle.nvfp4_encode(wb)
+    np.testing.assert_array_equal(wc, oc)
+    np.testing.assert_array_equal(ws, os_)
+    y = nv.gemm(w, x=dev_bf16(xb), out_dtype=out_dtype)  # quantises X on the fly
+    ref = oracle.gemm_w4a4(oracle.nvfp4_encode(xb), (oc, os_, og))
+    _check(y_np(y), ref, "config 1")
+    # the pre-quantised activation path gives the same numbers
+    a, *_ = quantize_gpu(xb)
+    y2 = nv.gemm(w, a_q=a, out_dtype=out_dtype)
+    np.testing.assert_array_equal(y_np(y2), y_np(y))
+
+
+@pytest.fixture(scope="module")
+def w_28672():
+    wb = synth.weights(2, 1, 28672, 8192)
+    w, wc, ws, wg = quantize_gpu(wb)
+    return w, (wc, ws, wg[0])
+
+
+@pytest.mark.parametrize("M", [1, 8, 16])
+def test_decode_full(w_28672, M):
+    w, wq = w_28672
+    xb = synth.activations(2, 0, M, 8192, 0.005, 100.0)
+    y = nv.gemm(w, x=dev_bf16(xb))
+    ref = oracle.gemm_w4a4(oracle.nvfp4_encode(xb), wq)
+    _check(y_np(y), ref, f"decode M={M}")
+
+
+@pytest.mark.parametrize("N", [8192, 28672])
+def test_prefill_sampled_rows(w_28672, N):
+    if N == 28672:
+        w, wq = w_28672
+    else:
+        wb = synth.weights(3, 1, 8192, 8192)
+        w, wc, ws, wg = quantize_gpu(wb)
+        wq = (wc, ws, wg[0])
+    xb = synth.activations(3, 0, 4096, 8192, 0.005, 100.0)
+    y = y_np(nv.gemm(w, x=dev_bf16(xb)))
+    rows = np.concatenate([[0, 4095], np.random.default_rng(N).choice(np.arange(1, 4095), 14, replace=False)])
+    ref = oracle.gemm_w4a4(oracle.nvfp4_encode(xb), wq, rows=rows)
+    _check(y[rows], ref, f"prefill N={N}")
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 384, 320), (129, 136, 64), (1, 130, 128), (64, 4096, 1024),
+                                   (300, 1000, 256), (8, 1024, 8192), (33, 512, 2048), (2048, 256, 576)])
+@pytest.mark.parametrize("out_dtype", [nv.OUT_BF16, nv.OUT_FP32])
+def test_ragged_shapes(M, N, K, out_dtype):
+    xb = synth.activations(9, 10, M, K, 0.01, 50.0)
+    wb = synth.weights(9, 11, N, K)
+    w, wc, ws, wg = quantize_gpu(wb)
+    y = nv.gemm(w, x=dev_bf16(xb), out_dtype=out_dtype)
+    ref = oracle.gemm_w4a4(oracle.nvfp4_encode(xb), (wc, ws, wg[0]))
+    _check(y_np(y), ref, f"{M}x{N}x{K}")
+
+
+def test_output_row_stride_and_empty():
+    xb, wb = _layer(1, 40, 256, 512)
+    w, wc, ws, wg = quantize_gpu(wb)
+    big = torch.full((40, 300), 7.0, dtype=torch.bfloat16, device="cuda")
+    nv.gemm(w, x=dev_bf16(xb), y=big[:, :256])
+    ref = oracle.gemm_w4a4(oracle.nvfp4_encode(xb), (wc, ws, wg[0]))
+    full = y_np(big)
+    _check(full[:, :256], ref, "strided output")
+    assert (full[:, 256:] == 7.0).all()
+    y = nv.gemm(w, x=torch.zeros((0, 512), dtype=torch.bfloat16, device="cuda"))
+    assert y.shape == (0, 256)

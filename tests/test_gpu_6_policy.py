@@ -1,0 +1,47 @@
+"""Per-layer precision policy over the 8-layer [2048, 4096] -> [4096] stack:
+AUTO routes the two seeded sensitive layers through W4A8 and the rest
+through W4A4; Q4 and Q8 force one route.  Each layer's output is checked
+against the oracle fed the GPU's previous BF16 output (sampled rows)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_common import dev_bf16, host, nv, quantize_gpu, y_np
+from helpers import row_tolerance_ok
+
+pytestmark = pytest.mark.gpu
+
+C4 = synth.CONFIGS[4]
+
+
+@pytest.fixture(scope="module")
+def stack():
+    layers = []
+    for i in range(C4["layers"]):
+        wb = synth.weights(4, 100 + i, C4["N"], C4["K"])
+        t, c, s, g = quantize_gpu(wb)
+        layers.append((t, (c, s, g[0])))
+    return layers
+
+
+@pytest.mark.parametrize("policy", [nv.POLICY_AUTO, nv.POLICY_Q4, nv.POLICY_Q8])
+def test_policy_stack(stack, policy):
+    flags = synth.sensitive_flags(C4["layers"], C4["n_sensitive"])
+    assert flags.sum() == 2
+    x = synth.activations(4, 0, C4["M"], C4["K"], C4["outlier_frac"], C4["outlier_factor"])
+    rows = np.concatenate([[0, C4["M"] - 1], np.random.default_rng(4).choice(C4["M"], 14, replace=False)])
+    xd = dev_bf16(x)
+    for i, (w, wq) in enumerate(stack):
+        route = nv.policy_route(policy, int(flags[i]))
+        y = nv.gemm(w, x=xd, policy=policy, sensitive=int(flags[i]))
+        xh = host(xd.view(torch.int16)).view(np.uint16)
+        if route == 4:
+            ref = oracle.gemm_w4a4(oracle.nvfp4_encode(xh), wq, rows=rows)
+        else:
+            a8, st = oracle.fp8_token_encode(xh)
+            ref = oracle.gemm_w4a8(a8, st, wq, rows=rows)
+        ok, worst = row_tolerance_ok(y_np(y)[rows], ref)
+        assert ok, f"layer {i} route {route}: {worst}"
+        xd = y

@@ -215,6 +215,35 @@ nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor *a, const int32_t *row_idx,
                                 int64_t total_rows, int32_t policy, int32_t sensitive,
                                 void *ws, size_t ws_bytes, nvfp4_stream_t stream);
 
+/* ---- no-allocation variant --------------------------------------------------- */
+
+/* W4A4 product Y[M, N] = A[M, K] * W[N, K]^T of pre-quantised NVFP4
+ * activations a_q (TENSOR_FP32, MMA_TILED) and weights w, for callers that
+ * cannot allocate device memory at call time: a host framework that owns all
+ * device memory through its own pool and forbids cudaMalloc, a plugin without
+ * allocation rights, or a serving loop that must never reach the allocator.
+ * The pages have no counterpart to this entry point; it is the nvfp4_gemm
+ * W4A4 kernel with its scratch moved into the library.
+ *  - Takes no workspace and allocates nothing (no cudaMalloc, no cudaFree, no
+ *    allocating library call).  Its scratch (status word, stream-K FP32
+ *    accumulator and per-tile counters) is a fixed 4 MiB array inside the
+ *    library, which every GPU that loads the library holds until exit.
+ *  - A shape whose scratch would exceed 4 MiB (narrow shapes that use
+ *    stream-K, needing about 4*M*N bytes) is rejected with
+ *    NVFP4_ERR_WORKSPACE before anything is enqueued.
+ *  - The first call on a device looks up the array's device address for that
+ *    device (with that device current); make that first call before any
+ *    stream capture.
+ *  - Every call shares the one array and zeroes the part it uses on `stream`
+ *    before the kernel runs; calls that overlap on the GPU (other streams,
+ *    other threads) race on it and must be serialised by the caller.
+ *  - Device-side status (a bounded wait that ran out) is kept in that array
+ *    and not reported; use nvfp4_gemm with a workspace to read it.
+ *  y: [M, N] with row stride ldy, y_dtype BF16 or FP32, 16-byte aligned.
+ *  Other errors as nvfp4_gemm. */
+nvfp4_status nvfp4_gemm_w4a4_noalloc(const nvfp4_tensor *a_q, const nvfp4_tensor *w, void *y, int64_t ldy,
+                                     int32_t y_dtype, nvfp4_stream_t stream);
+
 /* ---- diagnostics ----------------------------------------------------------- */
 
 /* Runs the kernels' own element conversions on n floats: out_e2m1[i] is the

@@ -30,7 +30,8 @@ OP_QUANTIZE, OP_QUANTIZE_FP8, OP_GEMM, OP_W4A8_GEMM, OP_GROUPED_GEMM = range(5)
 
 EXPORTED = ["nvfp4_scale_bytes", "nvfp4_workspace_size", "nvfp4_workspace_init", "nvfp4_device_status",
             "nvfp4_policy_route", "nvfp4_quantize", "nvfp4_quantize_fp8", "nvfp4_gemm", "nvfp4_w4a8_gemm",
-            "nvfp4_grouped_gemm", "nvfp4_probe_convert", "nvfp4_sm_count", "nvfp4_version"]
+            "nvfp4_grouped_gemm", "nvfp4_probe_convert", "nvfp4_sm_count", "nvfp4_version",
+            "nvfp4_gemm_w4a4_noalloc"]
 
 
 class NVFP4Error(RuntimeError):
@@ -71,6 +72,7 @@ def lib():
             "nvfp4_grouped_gemm": (_I32, [_PT, _VP, _VP, _I32, _PT, _I64, _VP, _I64, _I32, _I64, _I32, _I32,
                                           _VP, _SZ, _VP]),
             "nvfp4_probe_convert": (_I32, [_VP, _I64, _VP, _VP, _VP]),
+            "nvfp4_gemm_w4a4_noalloc": (_I32, [_PT, _PT, _VP, _I64, _I32, _VP]),
             "nvfp4_sm_count": (_I32, []),
             "nvfp4_version": (ctypes.c_char_p, []),
         }
@@ -254,6 +256,17 @@ def grouped_gemm(a: NVFP4Tensor, offsets: torch.Tensor, w: NVFP4Tensor, N: int, 
     _check(lib().nvfp4_grouped_gemm(ctypes.byref(ad), _ptr(row_idx), _ptr(offsets), E, ctypes.byref(wd), N,
                                     _ptr(y), y.stride(0), out_dtype, total_rows, policy, int(bool(sensitive)),
                                     ws.ptr, ws.nbytes, _stream(stream)), "nvfp4_grouped_gemm")
+    return y
+
+
+def gemm_w4a4_noalloc(a_q: NVFP4Tensor, w: NVFP4Tensor, y: torch.Tensor, out_dtype: int = OUT_BF16,
+                      stream=None) -> torch.Tensor:
+    """nvfp4_gemm_w4a4_noalloc: the W4A4 product for callers that cannot
+    allocate; takes no workspace (its scratch is a fixed array inside the
+    library, shared by all calls).  y must be provided by the caller."""
+    ad, wd = a_q.desc(), w.desc()
+    _check(lib().nvfp4_gemm_w4a4_noalloc(ctypes.byref(ad), ctypes.byref(wd), _ptr(y), y.stride(0), out_dtype,
+                                         _stream(stream)), "nvfp4_gemm_w4a4_noalloc")
     return y
 
 

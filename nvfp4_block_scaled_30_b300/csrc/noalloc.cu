@@ -1,0 +1,148 @@
+// nvfp4_gemm_w4a4_noalloc: the W4A4 GEMM for callers that cannot allocate.
+//
+// Some callers have no way to obtain device memory at the point of the call:
+// a host framework that owns every byte of device memory through its own
+// pool and forbids direct cudaMalloc, a plugin running inside another
+// runtime without allocation rights, or a latency-critical serving loop that
+// must never reach the allocator.  nvfp4_gemm needs a caller-allocated
+// workspace for its stream-K partial sums; this entry point instead keeps
+// that scratch in a fixed array inside the library (see the header for the
+// contract).  It allocates nothing: no cudaMalloc, no cudaFree, no
+// allocating library routine.
+#include <mutex>
+
+#include "internal.h"
+
+namespace nv4 {
+
+namespace {
+
+// Scratch of the no-allocation entry point: every GPU that loads the library
+// holds these bytes until the process exits.  Layout: [0, 256) status word,
+// then the stream-K FP32 accumulator, then the per-tile counters.
+constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(4) << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+constexpr uint64_t NOALLOC_TIMEOUT_NS = 2000000000ull;
+
+std::mutex g_mu;
+void *g_scratch_addr[64] = {nullptr};
+
+// Device address of the scratch array on the current device.  The symbol's
+// host-side name is only a stand-in; the address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+cudaError_t scratch_address(void **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess)
+            return e;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return cudaSuccess;
+}
+
+bool valid_tensor(const nvfp4_tensor *t)
+{
+    auto al = [](const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; };
+    return t && t->second && t->rows >= 0 && t->K > 0 && t->K % 64 == 0 &&
+           t->mode == NVFP4_SCALE_TENSOR_FP32 && t->layout == NVFP4_LAYOUT_MMA_TILED &&
+           (t->rows == 0 || (t->codes && t->scales && al(t->codes, 16) && al(t->scales, 16))) &&
+           al(t->second, 4);
+}
+
+} // namespace
+
+} // namespace nv4
+
+using namespace nv4;
+
+extern "C" nvfp4_status nvfp4_gemm_w4a4_noalloc(const nvfp4_tensor *a_q, const nvfp4_tensor *w, void *y,
+                                                 int64_t ldy, int32_t y_dtype, nvfp4_stream_t stream)
+{
+    if (!valid_tensor(a_q) || !valid_tensor(w) || a_q->K != w->K)
+        return NVFP4_ERR_INVALID_ARG;
+    if (y_dtype != NVFP4_OUT_BF16 && y_dtype != NVFP4_OUT_FP32)
+        return NVFP4_ERR_INVALID_ARG;
+    const int64_t M = a_q->rows, N = w->rows, K = w->K;
+    if (M > ((int64_t)1 << 30) || N > ((int64_t)1 << 30))
+        return NVFP4_ERR_INVALID_ARG;
+    if (M == 0 || N == 0)
+        return NVFP4_OK;
+    if (!y || (reinterpret_cast<uintptr_t>(y) % 16) != 0 || ldy < N)
+        return NVFP4_ERR_INVALID_ARG;
+
+    // the same launch shape nvfp4_gemm picks: operands swapped for M <= 64,
+    // stream-K when whole tiles fill the SMs poorly
+    DenseGemmArgs g{};
+    const bool swap = M <= 64;
+    if (swap) {
+        g.a_codes = static_cast<const uint8_t *>(w->codes);
+        g.a_scales = static_cast<const uint8_t *>(w->scales);
+        g.a_second = static_cast<const float *>(w->second);
+        g.a_rows = N;
+        g.b_codes = static_cast<const uint8_t *>(a_q->codes);
+        g.b_scales = static_cast<const uint8_t *>(a_q->scales);
+        g.b_second = static_cast<const float *>(a_q->second);
+        g.b_rows = M;
+    } else {
+        g.a_codes = static_cast<const uint8_t *>(a_q->codes);
+        g.a_scales = static_cast<const uint8_t *>(a_q->scales);
+        g.a_second = static_cast<const float *>(a_q->second);
+        g.a_rows = M;
+        g.b_codes = static_cast<const uint8_t *>(w->codes);
+        g.b_scales = static_cast<const uint8_t *>(w->scales);
+        g.b_second = static_cast<const float *>(w->second);
+        g.b_rows = N;
+    }
+    g.K = K;
+    const int sms = device_sm_count();
+    const int bn = w4a4_dense_bn(g.b_rows);
+    const int64_t tiles = ceil_div(g.a_rows, 128) * ceil_div(g.b_rows, bn);
+    const int64_t kstages = ceil_div(K / 64, 4);
+    const double eff = (double)tiles / (double)(ceil_div(tiles, sms) * sms);
+    const bool streamk = M <= 128 && eff < 0.9 && tiles * kstages >= 2 * (int64_t)sms;
+
+    // scratch needed by this call; larger requests are rejected
+    const size_t acc_bytes = streamk ? align_up((size_t)(M * N * 4), 256) : 0;
+    const size_t cnt_bytes = streamk ? align_up((size_t)(tiles * 4), 256) : 0;
+    const size_t need = WS_HEADER + acc_bytes + cnt_bytes;
+    if (need > NOALLOC_SCRATCH_BYTES)
+        return NVFP4_ERR_WORKSPACE;
+
+    void *scratch = nullptr;
+    if (scratch_address(&scratch) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    // the array keeps the previous call's contents: zero the status word,
+    // the accumulator and the counters this call relies on
+    if (cudaMemsetAsync(scratch, 0, need, s) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    uint8_t *base = static_cast<uint8_t *>(scratch);
+    g.status = reinterpret_cast<uint32_t *>(base);
+    g.timeout_ns = NOALLOC_TIMEOUT_NS;
+    g.out = y;
+    g.out_dtype = y_dtype;
+    g.ld_i = swap ? 1 : ldy;
+    g.ld_j = swap ? ldy : 1;
+    g.streamk = streamk;
+    if (streamk) {
+        g.acc = reinterpret_cast<float *>(base + WS_HEADER);
+        g.acc_ld_i = swap ? 1 : N;
+        g.acc_ld_j = swap ? N : 1;
+        g.tile_cnt = reinterpret_cast<uint32_t *>(base + WS_HEADER + acc_bytes);
+    }
+    const cudaError_t e = launch_w4a4_dense(g, s);
+    if (e == cudaSuccess)
+        return NVFP4_OK;
+    return e == cudaErrorNotSupported ? NVFP4_ERR_UNSUPPORTED : NVFP4_ERR_CUDA;
+}

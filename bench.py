@@ -216,7 +216,7 @@ def workload_prefill(c, N, steps, warmup, rot=2):
     qms = c.time(quant_only, steps, warmup)
     st = work.status()
     del W
-    return {"ms": ms, "gemm_ms": gms, "flops": flops, "value": flops / (ms * 1e-3) / 1e12,
+    return {"ms": ms, "gemm_ms": gms, "flops": flops, "value": flops / (ms * 1e-3) / 1e12, "launches_per_step": 3,
             "gemm_tflops": flops / (gms * 1e-3) / 1e12, "quant_ms": qms, "quant_bytes": qbytes,
             "quant_gbs": qbytes / (qms * 1e-3) / 1e9, "device_status": st}
 
@@ -242,7 +242,7 @@ def workload_policy(c, steps, warmup, policy):
     flops = 2.0 * M * N * K * L
     routes = [nv.policy_route(policy, int(f)) for f in flags]
     return {"ms": ms, "flops": flops, "value": flops / (ms * 1e-3) / 1e12, "routes": routes,
-            "device_status": work.status()}
+            "launches_per_step": sum(3 if r == 4 else 2 for r in routes), "device_status": work.status()}
 
 
 def workload_moe(c, steps, warmup):
@@ -279,7 +279,7 @@ def workload_moe(c, steps, warmup):
     step_bytes = (wbytes + T * H * 2 + 2 * nvfp4_bytes(T, H) + R * I * 2          # up
                   + R * I * 2 + 2 * nvfp4_bytes(R, I) + R * H * 2)                 # down
     flops = 2.0 * R * I * H * 2
-    return {"ms": ms, "bytes": step_bytes, "value": step_bytes / (ms * 1e-3) / 1e9,
+    return {"ms": ms, "bytes": step_bytes, "value": step_bytes / (ms * 1e-3) / 1e9, "launches_per_step": 6,
             "tflops": flops / (ms * 1e-3) / 1e12, "counts_min": int(counts.min()),
             "counts_max": int(counts.max()), "device_status": work.status()}
 
@@ -320,6 +320,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["decode", "prefill", "policy", "moe"], default="decode")
     ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle leg (profiling runs)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -424,7 +425,7 @@ def main():
                                  "frac_hbm": mo["value"] / hbm, "counts": [mo["counts_min"], mo["counts_max"]]}
 
     cpu = None
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, dt, nb = oracle_decode_sample()
         cpu = {"value": v, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
                "sample": "decode step (encode X, FP64 contraction) on 2048 of 28672 weight rows"}

@@ -154,34 +154,21 @@ static bool use_streamk(int64_t tiles, int64_t kstages, int sms)
 }
 
 // W4A4 dense product of NVFP4 activations `a` ([M, K], tiled scales, tensor
-// mode) and weights `w` ([N, K]) into y.  M <= 64 swaps the operands so the
-// weights fill the 128-row MMA side (decode shapes).
+// mode) and weights `w` ([N, K]) into y.
 static nvfp4_status run_w4a4_dense(const uint8_t *a_codes, const uint8_t *a_scales, const float *a_second,
                                    int64_t M, const nvfp4_tensor *w, void *y, int64_t ldy, int y_dtype, void *ws,
                                    const WsLayout &L, cudaStream_t stream)
 {
     const int64_t N = w->rows, K = w->K;
     DenseGemmArgs g{};
-    const bool swap = M <= 64;
-    if (swap) {
-        g.a_codes = static_cast<const uint8_t *>(w->codes);
-        g.a_scales = static_cast<const uint8_t *>(w->scales);
-        g.a_second = static_cast<const float *>(w->second);
-        g.a_rows = N;
-        g.b_codes = a_codes;
-        g.b_scales = a_scales;
-        g.b_second = a_second;
-        g.b_rows = M;
-    } else {
-        g.a_codes = a_codes;
-        g.a_scales = a_scales;
-        g.a_second = a_second;
-        g.a_rows = M;
-        g.b_codes = static_cast<const uint8_t *>(w->codes);
-        g.b_scales = static_cast<const uint8_t *>(w->scales);
-        g.b_second = static_cast<const float *>(w->second);
-        g.b_rows = N;
-    }
+    g.a_codes = a_codes;
+    g.a_scales = a_scales;
+    g.a_second = a_second;
+    g.a_rows = M;
+    g.b_codes = static_cast<const uint8_t *>(w->codes);
+    g.b_scales = static_cast<const uint8_t *>(w->scales);
+    g.b_second = static_cast<const float *>(w->second);
+    g.b_rows = N;
     g.K = K;
     g.status = status_word(ws);
     g.timeout_ns = DEFAULT_TIMEOUT_NS;
@@ -192,19 +179,19 @@ static nvfp4_status run_w4a4_dense(const uint8_t *a_codes, const uint8_t *a_scal
     if (!sk) {
         g.out = y;
         g.out_dtype = y_dtype;
-        g.ld_i = swap ? 1 : ldy;
-        g.ld_j = swap ? ldy : 1;
+        g.ld_i = ldy;
+        g.ld_j = 1;
         return from_cuda(launch_w4a4_dense(g, stream));
     }
     // stream-K: partial tiles meet in the workspace accumulator; the kernel
     // writes y itself and leaves the accumulator and counters zeroed
     g.out = y;
     g.out_dtype = y_dtype;
-    g.ld_i = swap ? 1 : ldy;
-    g.ld_j = swap ? ldy : 1;
+    g.ld_i = ldy;
+    g.ld_j = 1;
     g.acc = reinterpret_cast<float *>(ws_at(ws, L.acc));
-    g.acc_ld_i = swap ? 1 : N;
-    g.acc_ld_j = swap ? N : 1;
+    g.acc_ld_i = N;
+    g.acc_ld_j = 1;
     g.tile_cnt = reinterpret_cast<uint32_t *>(ws_at(ws, L.tile_cnt));
     return from_cuda(launch_w4a4_dense(g, stream));
 }

@@ -1,8 +1,347 @@
-// Placeholder for the FP16 macro-scale contraction (see launch_w4a4_macro).
+// W4A4 GEMM with FP16 macro-scales, the second scaling level of "NVIDIA Ships
+// TensorRT-LLM 0.16: Native FP4 Quantization for Blackwell B200", section
+// "The Mathematical Breakthrough of Microscopic FP4 Scaling", item 2
+// "Two-Level Block Scaling": 16 consecutive micro-vectors (256 elements of
+// a row) share one FP16 macro-scale.  With macro-scales the product is
+//
+//   Y[m][n] = sum_g S_A[m][g] * S_W[n][g] * P_g[m][n],
+//   P_g[m][n] = sum_{k in group g} E2M1(a)E4M3(ea) * E2M1(w)E4M3(ew),
+//
+// so the macro-scales cannot be folded into one epilogue factor.  One
+// pipeline stage covers exactly one group (256 elements of K): the tensor
+// cores compute P_g into one of two TMEM buffers (tcgen05.mma kind::mxf4nvf4,
+// 4 x K=64) while eight epilogue warps rescale the previous P_{g-1} by
+// S_A * S_W and accumulate it in registers (FP32).
+//
+// Roles (one CTA per SM, persistent, 320 threads): warp 0 TMA producer,
+// warp 1 TMEM allocation + MMA issue, warps 2..9 epilogue (warp w covers TMEM
+// lane quarter w % 4 and columns 64 * ((w - 2) / 4) .. +63 of the 128-wide tile).
+#include <algorithm>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace nv4 {
 
-cudaError_t launch_w4a4_macro(const MacroGemmArgs &, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 128;               // B tiles start on a 128-row scale atom
+constexpr int STAGE_K_BYTES = 128; // 256 FP4 = one macro group
+constexpr int STAGES = 5;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int A_BYTES = BM * STAGE_K_BYTES;
+constexpr int B_BYTES = BN * STAGE_K_BYTES;
+constexpr int SFA_BYTES = 2048;
+constexpr int SFB_BYTES = 2048;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+constexpr int SF_COLS = 32;            // 16 (A) + 16 (B) TMEM columns per stage
+constexpr int P_BUFS = 2;
+constexpr int SF_BASE = P_BUFS * BN;
+constexpr int TMEM_COLS = 512;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + 1024;
+static_assert(SF_BASE + STAGES * SF_COLS <= TMEM_COLS, "TMEM");
+static_assert(STAGE_BYTES % 1024 == 0, "alignment");
+static_assert(SMEM_BYTES <= 232448, "shared memory");
+
+struct Params {
+    CUtensorMap tmap_a;
+    CUtensorMap tmap_b;
+    const uint8_t *sfa;
+    const uint8_t *sfb;
+    const uint16_t *a_macro; // [M][K/256]
+    const uint16_t *w_macro; // [N][K/256]
+    void *out;
+    int64_t ldy, M, N;
+    int32_t m_tiles, n_tiles, k64, groups, out_dtype, vec_ok;
+    uint32_t *status;
+    uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ void tile_of(const Params &p, int item, int &tm, int &tn)
+{
+    constexpr int G = 8;
+    const int band = G * p.n_tiles;
+    const int bid = item / band;
+    const int first = bid * G;
+    const int gs = min(p.m_tiles - first, G);
+    const int r = item - bid * band;
+    tm = first + r % gs;
+    tn = r / gs;
+}
+
+__device__ __forceinline__ void timeout(const Params &p, volatile int *abort_flag)
+{
+    *abort_flag = 1;
+    atomicOr(p.status, ST_TIMEOUT);
+}
+
+__global__ void __launch_bounds__(THREADS, 1) macro_kernel(const __grid_constant__ Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    uint64_t *empty = full + STAGES;
+    uint64_t *pfull = empty + STAGES;
+    uint64_t *pempty = pfull + P_BUFS;
+    uint64_t *drain = pempty + P_BUFS;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < P_BUFS; ++b) {
+            mbar_init(&pfull[b], 1);
+            mbar_init(&pempty[b], EPI_WARPS);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int total = p.m_tiles * p.n_tiles;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int st = 0, issued = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+                int tm, tn;
+                tile_of(p, item, tm, tn);
+                for (int g = 0; g < p.groups; ++g) {
+                    if (!mbar_wait(&empty[st], ph ^ 1u, p.timeout_ns, abort_flag)) {
+                        timeout(p, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *sA = smem + st * STAGE_BYTES;
+                    uint8_t *sB = sA + A_BYTES;
+                    mbar_arrive_expect_tx(&full[st], A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES);
+                    tma_load_2d(sA, &p.tmap_a, g * STAGE_K_BYTES, tm * BM, &full[st]);
+                    tma_load_2d(sB, &p.tmap_b, g * STAGE_K_BYTES, tn * BN, &full[st]);
+                    bulk_load(sB + B_BYTES, p.sfa + ((size_t)tm * p.k64 + 4 * g) * 512, SFA_BYTES, &full[st]);
+                    bulk_load(sB + B_BYTES + SFA_BYTES, p.sfb + ((size_t)tn * p.k64 + 4 * g) * 512, SFB_BYTES,
+                              &full[st]);
+                    ++issued;
+                    if (++st == STAGES) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            const int n = min(issued, STAGES);
+            for (int q = 0; q < n; ++q) {
+                if (--st < 0) {
+                    st = STAGES - 1;
+                    ph ^= 1u;
+                }
+                mbar_wait(&full[st], ph, p.timeout_ns, nullptr);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_mxf4nvf4(BN);
+            int st = 0, pb = 0;
+            uint32_t ph = 0, pph = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+                int tm, tn;
+                tile_of(p, item, tm, tn);
+                for (int g = 0; g < p.groups; ++g) {
+                    if (!mbar_wait(&pempty[pb], pph ^ 1u, p.timeout_ns, abort_flag) ||
+                        !mbar_wait(&full[st], ph, p.timeout_ns, abort_flag)) {
+                        timeout(p, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t *sA = smem + st * STAGE_BYTES;
+                    const uint8_t *sB = sA + A_BYTES;
+                    const uint8_t *sSFA = sB + B_BYTES;
+                    const uint8_t *sSFB = sSFA + SFA_BYTES;
+                    const uint32_t sf = tmem + SF_BASE + st * SF_COLS;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        tc_cp_32x128b_warpx4(sf + kk * 4, sdesc_sf(smem_u32(sSFA + kk * 512)));
+                        tc_cp_32x128b_warpx4(sf + 16 + kk * 4, sdesc_sf(smem_u32(sSFB + kk * 512)));
+                    }
+                    const uint64_t ad = sdesc_sw128(smem_u32(sA)), bd = sdesc_sw128(smem_u32(sB));
+                    const uint32_t d = tmem + pb * BN;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_mxf4nvf4(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, sf + kk * 4,
+                                     sf + 16 + kk * 4, kk > 0 ? 1u : 0u);
+                    tc_commit(&empty[st]);
+                    tc_commit(&pfull[pb]);
+                    if (++st == STAGES) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                    if (++pb == P_BUFS) {
+                        pb = 0;
+                        pph ^= 1u;
+                    }
+                }
+            }
+            tc_commit(drain);
+            mbar_wait(drain, 0, p.timeout_ns, nullptr);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int row = q * 32 + lane;
+        int pb = 0;
+        uint32_t pph = 0;
+        for (int item = blockIdx.x; item < total; item += gridDim.x) {
+            int tm, tn;
+            tile_of(p, item, tm, tn);
+            const int64_t i = (int64_t)tm * BM + row;
+            const int64_t j0 = (int64_t)tn * BN + half * 64;
+            float acc[64];
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+                acc[c] = 0.0f;
+            bool ok = true;
+            for (int g = 0; g < p.groups; ++g) {
+                const bool got = mbar_wait(&pfull[pb], pph, p.timeout_ns, abort_flag);
+                if (!__all_sync(0xFFFFFFFFu, got)) {
+                    if (lane == 0)
+                        timeout(p, abort_flag);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float sa = i < p.M ? __half2float(__ushort_as_half(p.a_macro[i * p.groups + g])) : 0.0f;
+                const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + pb * BN + half * 64;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    uint32_t v[32];
+                    tc_ld_32x32b_x32(ta + h2 * 32, v);
+                    tc_wait_ld();
+                    if (h2 == 1) {
+                        // both halves are in registers: the buffer can take the next group
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(&pempty[pb]);
+                    }
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const int64_t j = j0 + h2 * 32 + c;
+                        const float sw =
+                            j < p.N ? __half2float(__ushort_as_half(__ldg(p.w_macro + j * p.groups + g))) : 0.0f;
+                        acc[h2 * 32 + c] = fmaf(sa * sw, __uint_as_float(v[c]), acc[h2 * 32 + c]);
+                    }
+                }
+                if (++pb == P_BUFS) {
+                    pb = 0;
+                    pph ^= 1u;
+                }
+            }
+            if (!ok)
+                break;
+            if (i < p.M) {
+                if (p.vec_ok && j0 + 64 <= p.N) {
+                    if (p.out_dtype == NVFP4_OUT_BF16) {
+                        uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + i * p.ldy + j0);
+#pragma unroll
+                        for (int c = 0; c < 64; c += 8) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int z = 0; z < 4; ++z) {
+                                __nv_bfloat162 h = __floats2bfloat162_rn(acc[c + 2 * z], acc[c + 2 * z + 1]);
+                                w[z] = *reinterpret_cast<uint32_t *>(&h);
+                            }
+                            o[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    } else {
+                        float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + i * p.ldy + j0);
+#pragma unroll
+                        for (int c = 0; c < 64; c += 4)
+                            o[c / 4] = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) {
+                        if (j0 + c < p.N) {
+                            if (p.out_dtype == NVFP4_OUT_BF16)
+                                static_cast<__nv_bfloat16 *>(p.out)[i * p.ldy + j0 + c] = __float2bfloat16_rn(acc[c]);
+                            else
+                                static_cast<float *>(p.out)[i * p.ldy + j0 + c] = acc[c];
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+} // namespace
+
+cudaError_t launch_w4a4_macro(const MacroGemmArgs &g, cudaStream_t stream)
+{
+    if (g.K % 256 != 0)
+        return cudaErrorInvalidValue;
+    Params p{};
+    CUresult r = make_tmap_2d_u8(&p.tmap_a, g.a_codes, (uint64_t)(g.K / 2), (uint64_t)g.M, (uint64_t)(g.K / 2),
+                                 STAGE_K_BYTES, BM, true);
+    if (r != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    r = make_tmap_2d_u8(&p.tmap_b, g.w_codes, (uint64_t)(g.K / 2), (uint64_t)g.N, (uint64_t)(g.K / 2), STAGE_K_BYTES,
+                        BN, true);
+    if (r != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    p.sfa = g.a_scales;
+    p.sfb = g.w_scales;
+    p.a_macro = g.a_macro;
+    p.w_macro = g.w_macro;
+    p.out = g.out;
+    p.ldy = g.ldy;
+    p.M = g.M;
+    p.N = g.N;
+    p.m_tiles = (int)ceil_div(g.M, BM);
+    p.n_tiles = (int)ceil_div(g.N, BN);
+    p.k64 = (int)(g.K / 64);
+    p.groups = (int)(g.K / 256);
+    p.out_dtype = g.out_dtype;
+    const int esz = g.out_dtype == NVFP4_OUT_BF16 ? 2 : 4;
+    p.vec_ok = ((g.ldy * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(g.out) % 16) == 0) ? 1 : 0;
+    p.status = g.status;
+    p.timeout_ns = g.timeout_ns;
+    cudaError_t e = cudaFuncSetAttribute(macro_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess)
+        return e;
+    const int total = p.m_tiles * p.n_tiles;
+    const int grid = std::max(1, std::min(total, device_sm_count()));
+    macro_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(p);
+    return cudaGetLastError();
+}
 
 } // namespace nv4

@@ -11,18 +11,25 @@
 // Put Precision Policy Inside the Model. That Matters More Than W4A4",
 // section "One model can need more than one precision".
 //
-// Design (one CTA per SM, persistent, warp-specialised, 192 threads):
-//   warp 0      TMA producer: A/B code tiles (128-byte rows = 256 FP4, 128-byte
-//               swizzle) and the 512-byte scale atoms into a STAGES-deep ring.
-//   warp 1      allocates TMEM; lane 0 issues tcgen05.cp (scales smem->TMEM)
-//               and tcgen05.mma kind::mxf4nvf4 (M=128, N=BN, K=64 each, 4 per
-//               stage), then tcgen05.commit to release the stage.
-//   warps 2..5  epilogue: tcgen05.ld of the FP32 accumulator, alpha scale,
-//               BF16/FP32 store (or FP32 red.add for split-K).
-// Accumulators are double-buffered in TMEM when BN <= 128 so the epilogue of
-// one tile overlaps the mainloop of the next.  Every mbarrier wait is bounded;
-// on timeout the CTA records NVFP4 TIMEOUT in the status word, drains its
-// in-flight copies and MMAs, frees TMEM and exits.
+// Design (one CTA per SM, persistent, warp-specialised, 352 threads):
+//   warp 0      producer: A/B code tiles by TMA (128-byte rows = 256 FP4,
+//               128-byte swizzle) and the compact 512-byte scale atoms by bulk
+//               copies, into a STAGES-deep ring.
+//   warp 1      allocates TMEM; lane 0 issues tcgen05.mma kind::mxf4nvf4
+//               (M = 128, N = BN, K = 64; 4 per stage) and tcgen05.commit.
+//   warp 2      scale warp: rewrites each stage's atoms into the 128x256b copy
+//               layout and moves them to TMEM with tcgen05.cp (4 KB per copy,
+//               two 64-element K chunks of one 128-row group each), off the
+//               MMA thread.  Each TMEM lane quarter of the tensor core reads
+//               scales from its own 32 lanes (row m of A: lane m, column
+//               address + m / 32; B: all rows in every quarter), so each atom
+//               row is written once per quarter.
+//   warps 3-10  epilogue: tcgen05.ld of the FP32 accumulator into registers,
+//               release of the accumulator, then alpha scale and BF16/FP32
+//               stores (or FP32 red.add of stream-K partial tiles).
+// Every mbarrier wait is bounded; on timeout the CTA records NVFP4 TIMEOUT in
+// the status word, drains its in-flight copies and MMAs, frees TMEM and
+// exits (epilogue warps decide together through a barrier reduction).
 #include <algorithm>
 #include <cuda_bf16.h>
 
@@ -35,34 +42,43 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int STAGE_K_BYTES = 128; // per row and stage: 256 FP4 elements
-constexpr int GROUP_M = 8;         // tile rasterisation band for L2 reuse
-constexpr int EPI_WARPS = 4;
-constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int EPI_WARPS = 8;
+constexpr int EPI_FIRST_WARP = 3;
+constexpr int THREADS = 32 * (EPI_FIRST_WARP + EPI_WARPS);
 constexpr int MAX_EXPERTS = 1024;
+constexpr int CP_SRC_BYTES = 4096;  // one 128x256b copy source: 128 rows x 32 B
+constexpr int KCORE_BYTES = 2048;   // one K-core of it: 128 rows x 16 B
 
 template <int BN>
 struct Cfg {
-    static constexpr int NB = BN >= 128 ? BN / 128 : 1; // 128-row scale atoms per B tile
-    static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+    static_assert(BN == 128 || BN == 256, "N tile");
+    static constexpr int NB = BN / 128;                 // 128-row scale groups per B tile
+    static constexpr int STAGES = BN == 256 ? 3 : 5;
     static constexpr int ACC_BUFS = BN == 256 ? 1 : 2;
     static constexpr int A_BYTES = BM * STAGE_K_BYTES;
     static constexpr int B_BYTES = BN * STAGE_K_BYTES;
-    static constexpr int SFA_BYTES = 4 * 512;
+    static constexpr int SFA_BYTES = 4 * 512;           // compact atoms as loaded
     static constexpr int SFB_BYTES = NB * 4 * 512;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-    static constexpr int SF_COLS = 16 + 16 * NB; // TMEM columns of scales per stage
+    // copy sources of one stage: A: 2 (chunk pairs); B: 2 (NB = 1, chunk
+    // pairs) or 4 (NB = 2, one chunk with both 128-row groups per copy)
+    static constexpr int CPS_A = 2;
+    static constexpr int CPS_B = NB == 1 ? 2 : 4;
+    static constexpr int STG_BYTES = (CPS_A + CPS_B) * CP_SRC_BYTES;
+    static constexpr int STG_SLOTS = 2;
+    static constexpr int SF_COLS = 16 + 16 * NB;        // TMEM scale columns per stage
     static constexpr int SF_BASE = ACC_BUFS * BN;
     static constexpr int TMEM_COLS = 512;
-    static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+    static constexpr int BAR_BYTES = 512;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STG_SLOTS * STG_BYTES + BAR_BYTES + 1024;
+    static constexpr int EPI_COLS = BN / 2;              // accumulator columns per epilogue warp
     static_assert(SF_BASE + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
-    static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
-    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+    static_assert(STAGE_BYTES % 1024 == 0 && STG_BYTES % 1024 == 0, "alignment");
+    static_assert(SMEM_BYTES + 4 * (MAX_EXPERTS + 2) <= 232448, "shared memory budget");
 };
 
 struct Params {
-    CUtensorMap tmap_a;  // MMA operand A codes [a_rows][K/2] (unused for indexed grouped rows)
+    CUtensorMap tmap_a;  // MMA operand A codes [a_rows][K/2]
     CUtensorMap tmap_b;  // MMA operand B codes
     const uint8_t *a_codes; // indexed grouped rows are copied from here with cp.async
     const uint8_t *sfa;  // tiled scales of A (row-padded to 128)
@@ -75,7 +91,7 @@ struct Params {
     int64_t acc_ld_i, acc_ld_j;
     uint32_t *tile_cnt;      // stream-K: K stages summed so far per tile, zero between calls
     int64_t a_rows, b_rows; // valid extents (b_rows = N per expert in grouped mode)
-    int32_t m_tiles, n_tiles, k64, kstages, streamk;
+    int32_t m_tiles, n_tiles, k64, kstages, streamk, group_m;
     int32_t out_dtype, vec_ok;
     int32_t b_row_tiles;    // 128-row scale atoms available in B (total)
     // grouped mode
@@ -93,12 +109,15 @@ struct Tile {
     int64_t row0, row_end; // grouped: first output row of the tile, end of the expert's rows
 };
 
+// Tiles in bands of group_m M-tiles, M fastest inside a band, so CTAs running
+// at the same time share weight tiles (L2) and, when the band holds every
+// M-tile, each weight tile comes from HBM once.
 __device__ __forceinline__ void decode_dense(const Params &p, int tile, Tile &t)
 {
-    const int band = GROUP_M * p.n_tiles;
+    const int band = p.group_m * p.n_tiles;
     const int bid = tile / band;
-    const int first_m = bid * GROUP_M;
-    const int gsize = min(p.m_tiles - first_m, GROUP_M);
+    const int first_m = bid * p.group_m;
+    const int gsize = min(p.m_tiles - first_m, p.group_m);
     const int rr = tile - bid * band;
     t.tile = tile;
     t.tile_m = first_m + rr % gsize;
@@ -193,7 +212,7 @@ __device__ __forceinline__ bool work_next(const Params &p, const int *prefix, in
     return true;
 }
 
-// Named barrier 1 across the four epilogue warps only.
+// Named barrier 1 across the epilogue warps.
 __device__ __forceinline__ void epi_bar_sync()
 {
     asm volatile("bar.sync 1, %0;" ::"n"(32 * EPI_WARPS) : "memory");
@@ -221,24 +240,67 @@ __device__ __forceinline__ void record_timeout(const Params &p, volatile int *ab
     atomicOr(p.status, ST_TIMEOUT);
 }
 
+// 128x256b copy: 128 TMEM lanes x 8 columns from a source of two 2 KB K-cores
+// (K-core c holds bytes 16c..16c+15 of every row; row m at (m/8)*128 + (m%8)*16).
+__device__ __forceinline__ void tc_cp_128x256b(uint32_t taddr, uint32_t src)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((src >> 4) & 0x3FFFu);
+    d |= (uint64_t)(KCORE_BYTES >> 4) << 16; // leading byte offset: K-core 0 -> 1
+    d |= (uint64_t)(128u >> 4) << 32;        // stride byte offset: 8-row groups
+    d |= (uint64_t)1u << 46;
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
+}
+
+// Scale warp, lane l: copy one compact atom (32 rows x 16 B; row l holds the
+// 4 scales of rows l, l+32, l+64, l+96 in words 0..3) into a K-core of a copy
+// source, once per TMEM lane quarter (rows l, 32+l, 64+l, 96+l).  Each lane
+// quarter of the tensor core reads scales from its own 32 TMEM lanes: for
+// the B operand every quarter needs every row's scales, and for A row m the
+// word m/32 of lane m holds them.
+__device__ __forceinline__ void spread_atom(const uint8_t *atom, uint8_t *kcore, int lane)
+{
+    const uint4 v = *reinterpret_cast<const uint4 *>(atom + lane * 16);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int m = 32 * q + lane;
+        *reinterpret_cast<uint4 *>(kcore + (m >> 3) * 128 + (m & 7) * 16) = v;
+    }
+}
+
+__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d)
+{
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
 template <int BN>
-__device__ __forceinline__ void store_chunk(const Params &p, const uint32_t (&v)[32], int nv, int64_t i, int64_t j0,
+__device__ __forceinline__ void store_chunk(const Params &p, const uint32_t (&v)[32], int64_t i, int64_t j0,
                                             float alpha, int64_t i_end, int64_t j_end, bool partial)
 {
     if (i >= i_end)
         return;
     if (partial) {
-        for (int c = 0; c < nv; ++c) {
-            const int64_t j = j0 + c;
-            if (j < j_end)
-                atomicAdd(p.acc + i * p.acc_ld_i + j * p.acc_ld_j, alpha * __uint_as_float(v[c]));
+        float *a = p.acc + i * p.acc_ld_i + j0 * p.acc_ld_j;
+        if (p.acc_ld_j == 1 && (p.acc_ld_i & 3) == 0 && j0 + 32 <= j_end) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 4)
+                red_add_v4(a + c, alpha * __uint_as_float(v[c]), alpha * __uint_as_float(v[c + 1]),
+                           alpha * __uint_as_float(v[c + 2]), alpha * __uint_as_float(v[c + 3]));
+            return;
+        }
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+            if (j0 + c < j_end)
+                atomicAdd(a + c * p.acc_ld_j, alpha * __uint_as_float(v[c]));
         }
         return;
     }
-    if (p.ld_j == 1 && p.vec_ok && j0 + nv <= j_end) {
+    if (p.ld_j == 1 && p.vec_ok && j0 + 32 <= j_end) {
         if (p.out_dtype == NVFP4_OUT_BF16) {
             uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + i * p.ld_i + j0);
-            for (int c = 0; c < nv; c += 8) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 8) {
                 uint32_t w[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -250,22 +312,24 @@ __device__ __forceinline__ void store_chunk(const Params &p, const uint32_t (&v)
             }
         } else {
             float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + i * p.ld_i + j0);
-            for (int c = 0; c < nv; c += 4)
+#pragma unroll
+            for (int c = 0; c < 32; c += 4)
                 o[c / 4] = make_float4(alpha * __uint_as_float(v[c]), alpha * __uint_as_float(v[c + 1]),
                                        alpha * __uint_as_float(v[c + 2]), alpha * __uint_as_float(v[c + 3]));
         }
         return;
     }
-    for (int c = 0; c < nv; ++c) {
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
         const int64_t j = j0 + c;
-        if (j >= j_end)
-            break;
-        const float y = alpha * __uint_as_float(v[c]);
-        const int64_t off = i * p.ld_i + j * p.ld_j;
-        if (p.out_dtype == NVFP4_OUT_BF16)
-            static_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(y);
-        else
-            static_cast<float *>(p.out)[off] = y;
+        if (j < j_end) {
+            const float y = alpha * __uint_as_float(v[c]);
+            const int64_t off = i * p.ld_i + j * p.ld_j;
+            if (p.out_dtype == NVFP4_OUT_BF16)
+                static_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(y);
+            else
+                static_cast<float *>(p.out)[off] = y;
+        }
     }
 }
 
@@ -275,9 +339,12 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
     using C = Cfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE_BYTES);
+    uint8_t *stg = smem + C::STAGES * C::STAGE_BYTES; // scale copy sources, STG_SLOTS slots
+    uint64_t *full = reinterpret_cast<uint64_t *>(stg + C::STG_SLOTS * C::STG_BYTES);
     uint64_t *empty = full + C::STAGES;
-    uint64_t *acc_full = empty + C::STAGES;
+    uint64_t *sf_ready = empty + C::STAGES;
+    uint64_t *stg_done = sf_ready + C::STAGES;
+    uint64_t *acc_full = stg_done + C::STG_SLOTS;
     uint64_t *acc_empty = acc_full + C::ACC_BUFS;
     uint64_t *drain = acc_empty + C::ACC_BUFS;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
@@ -294,7 +361,10 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&full[s], GROUPED ? 2 : 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&sf_ready[s], 1);
         }
+        for (int b = 0; b < C::STG_SLOTS; ++b)
+            mbar_init(&stg_done[b], 1);
         for (int b = 0; b < C::ACC_BUFS; ++b) {
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], EPI_WARPS);
@@ -346,7 +416,6 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int total_items = total_items_s;
-    const uint32_t idesc = idesc_mxf4nvf4(BN);
     const bool indexed = GROUPED && p.row_idx != nullptr;
 
     if (warp == 0) {
@@ -368,9 +437,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                     const int64_t g = t.row0 + lane + 32 * q;
                     row_ok[q] = g < t.row_end;
                     int r = row_ok[q] ? (indexed ? p.row_idx[g] : (int)g) : 0;
-                    if (r < 0 || r >= p.a_rows) { // out-of-range index: read row 0, result unspecified
+                    if (r < 0 || r >= p.a_rows) // out-of-range index: read row 0, result unspecified
                         r = 0;
-                    }
                     src_row[q] = r;
                 }
             }
@@ -388,7 +456,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                 uint8_t *sSFA = sB + C::B_BYTES;
                 uint8_t *sSFB = sSFA + C::SFA_BYTES;
                 const int brow0 = GROUPED ? t.expert * (int)p.b_rows + t.tile_n * BN : t.tile_n * BN;
-                const int bt0 = BN >= 128 ? brow0 / 128 : 0;
+                const int bt0 = brow0 / 128;
                 int nb_loaded = 0;
 #pragma unroll
                 for (int h = 0; h < C::NB; ++h)
@@ -475,6 +543,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
+            const uint32_t idesc = idesc_mxf4nvf4(BN);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -492,7 +561,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                 const uint32_t d_tmem = tmem + acc * BN;
                 uint32_t accumulate = 0;
                 for (int kb = t.kst0; kb < t.kst1; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag)) {
+                    if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag) ||
+                        !mbar_wait(&sf_ready[stage], phase, p.timeout_ns, abort_flag)) {
                         record_timeout(p, abort_flag);
                         ok = false;
                         break;
@@ -501,22 +571,16 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                     const int nk = min(4, p.k64 - 4 * kb);
                     const uint8_t *sA = smem + stage * C::STAGE_BYTES;
                     const uint8_t *sB = sA + C::A_BYTES;
-                    const uint8_t *sSFA = sB + C::B_BYTES;
-                    const uint8_t *sSFB = sSFA + C::SFA_BYTES;
                     const uint32_t sf_col = tmem + C::SF_BASE + stage * C::SF_COLS;
-                    for (int kk = 0; kk < nk; ++kk) {
-                        tc_cp_32x128b_warpx4(sf_col + kk * 4, sdesc_sf(smem_u32(sSFA + kk * 512)));
-#pragma unroll
-                        for (int h = 0; h < C::NB; ++h)
-                            tc_cp_32x128b_warpx4(sf_col + 16 + kk * 4 * C::NB + h * 4,
-                                                 sdesc_sf(smem_u32(sSFB + h * 2048 + kk * 512)));
-                    }
                     const uint64_t adesc = sdesc_sw128(smem_u32(sA));
                     const uint64_t bdesc = sdesc_sw128(smem_u32(sB));
                     for (int kk = 0; kk < nk; ++kk) {
+                        const uint32_t sfa = sf_col + 8 * (kk >> 1) + 4 * (kk & 1);
+                        const uint32_t sfb = C::NB == 1 ? sf_col + 16 + 8 * (kk >> 1) + 4 * (kk & 1)
+                                                        : sf_col + 16 + 8 * kk;
                         // +32 bytes (64 FP4) inside the swizzled 128-byte row
-                        mma_mxf4nvf4(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
-                                     sf_col + kk * 4, sf_col + 16 + kk * 4 * C::NB, accumulate);
+                        mma_mxf4nvf4(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc, sfa,
+                                     sfb, accumulate);
                         accumulate = 1;
                     }
                     tc_commit(&empty[stage]);
@@ -533,14 +597,90 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                     acc_phase ^= 1u;
                 }
             }
-            // every MMA and copy of this thread completes before TMEM is freed
+            // every MMA of this thread completes before TMEM is freed
             tc_commit(drain);
             mbar_wait(drain, 0, p.timeout_ns, nullptr);
         }
         __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ scale warp
+        int stage = 0;
+        uint32_t phase = 0;
+        int slot = 0;
+        int slot_uses[C::STG_SLOTS] = {0};
+        bool ok = true;
+        WorkIter wi;
+        work_begin(p, total_items, wi);
+        Tile t;
+        while (ok && work_next<GROUPED>(p, prefix, total_items, wi, t)) {
+            for (int kb = t.kst0; kb < t.kst1; ++kb) {
+                bool got = mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag);
+                if (got && slot_uses[slot] > 0)
+                    got = mbar_wait(&stg_done[slot], (uint32_t)((slot_uses[slot] - 1) & 1), p.timeout_ns,
+                                    abort_flag);
+                if (!__all_sync(FULLMASK, got)) {
+                    if (lane == 0)
+                        record_timeout(p, abort_flag);
+                    ok = false;
+                    break;
+                }
+                const int nk = min(4, p.k64 - 4 * kb);
+                const uint8_t *sSFA = smem + stage * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
+                const uint8_t *sSFB = sSFA + C::SFA_BYTES;
+                uint8_t *src = stg + slot * C::STG_BYTES;
+                // A: source (kk / 2), K-core (kk % 2)
+                for (int kk = 0; kk < nk; ++kk)
+                    spread_atom(sSFA + kk * 512, src + (kk >> 1) * CP_SRC_BYTES + (kk & 1) * KCORE_BYTES, lane);
+                uint8_t *srcb = src + C::CPS_A * CP_SRC_BYTES;
+                if (C::NB == 1) {
+                    for (int kk = 0; kk < nk; ++kk)
+                        spread_atom(sSFB + kk * 512, srcb + (kk >> 1) * CP_SRC_BYTES + (kk & 1) * KCORE_BYTES, lane);
+                } else {
+                    // B: source kk, K-core h = 128-row group h (rows 0-127 / 128-255)
+                    for (int kk = 0; kk < nk; ++kk)
+#pragma unroll
+                        for (int h = 0; h < C::NB; ++h)
+                            spread_atom(sSFB + h * 2048 + kk * 512, srcb + kk * CP_SRC_BYTES + h * KCORE_BYTES, lane);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t sf_col = tmem + C::SF_BASE + stage * C::SF_COLS;
+                    const int npairs = (nk + 1) >> 1;
+                    for (int q = 0; q < npairs; ++q)
+                        tc_cp_128x256b(sf_col + 8 * q, smem_u32(src + q * CP_SRC_BYTES));
+                    if (C::NB == 1) {
+                        for (int q = 0; q < npairs; ++q)
+                            tc_cp_128x256b(sf_col + 16 + 8 * q, smem_u32(srcb + q * CP_SRC_BYTES));
+                    } else {
+                        for (int kk = 0; kk < nk; ++kk)
+                            tc_cp_128x256b(sf_col + 16 + 8 * kk, smem_u32(srcb + kk * CP_SRC_BYTES));
+                    }
+                    tc_commit(&sf_ready[stage]);
+                    tc_commit(&stg_done[slot]);
+                }
+                __syncwarp();
+                ++slot_uses[slot];
+                if (++slot == C::STG_SLOTS)
+                    slot = 0;
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        // the copies this warp issued complete before TMEM is freed
+        if (lane == 0) {
+            for (int b = 0; b < C::STG_SLOTS; ++b)
+                if (slot_uses[b] > 0)
+                    mbar_wait(&stg_done[b], (uint32_t)((slot_uses[b] - 1) & 1), p.timeout_ns, nullptr);
+        }
+        __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        const int q = warp & 3; // the TMEM lane quarter this warp may access
+        const int ew = warp - EPI_FIRST_WARP;    // 0..7
+        const int q = warp & 3;                  // the TMEM lane quarter this warp may access
+        const int cbase = (ew >> 2) * C::EPI_COLS;
         const int row_in_tile = q * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -551,11 +691,28 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
         while (work_next<GROUPED>(p, prefix, total_items, wi, t)) {
             const bool got = mbar_wait(&acc_full[acc], acc_phase, p.timeout_ns, abort_flag);
             if (!epi_bar_all(got)) {
-                if (threadIdx.x == 64)
+                if (threadIdx.x == 32 * EPI_FIRST_WARP)
                     record_timeout(p, abort_flag);
                 break;
             }
             tc_fence_after();
+            // the whole accumulator slice of this warp into registers, then
+            // the accumulator goes back to the MMA warp
+            constexpr int NCH = C::EPI_COLS / 32;
+            uint32_t v[NCH][32];
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + cbase;
+#pragma unroll
+            for (int c = 0; c < NCH; ++c)
+                tc_ld_32x32b_x32(tbase + c * 32, v[c]);
+            tc_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&acc_empty[acc]);
+            if (++acc == C::ACC_BUFS) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
             const float alpha = a_s * p.b_second[GROUPED ? t.expert : 0];
             int64_t i, i_end;
             if (GROUPED) {
@@ -565,42 +722,17 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                 i = (int64_t)t.tile_m * BM + row_in_tile;
                 i_end = p.a_rows;
             }
-            const int64_t j_base = (int64_t)t.tile_n * BN;
+            const int64_t j_base = (int64_t)t.tile_n * BN + cbase;
             const int64_t j_end = p.b_rows;
             const bool partial = !GROUPED && p.streamk && !(t.kst0 == 0 && t.kst1 == p.kstages);
-            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
-            if (BN % 32 == 0) {
-                for (int c0 = 0; c0 < BN; c0 += 32) {
-                    uint32_t v[32];
-                    tc_ld_32x32b_x32(tbase + c0, v);
-                    tc_wait_ld();
-                    store_chunk<BN>(p, v, 32, i, j_base + c0, alpha, i_end, j_end, partial);
-                }
-            } else {
-                for (int c0 = 0; c0 < BN; c0 += 16) {
-                    uint32_t v16[16];
-                    tc_ld_32x32b_x16(tbase + c0, v16);
-                    tc_wait_ld();
-                    uint32_t v[32];
 #pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        v[c] = v16[c];
-                    store_chunk<BN>(p, v, 16, i, j_base + c0, alpha, i_end, j_end, partial);
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&acc_empty[acc]);
-            if (++acc == C::ACC_BUFS) {
-                acc = 0;
-                acc_phase ^= 1u;
-            }
+            for (int c = 0; c < NCH; ++c)
+                store_chunk<BN>(p, v[c], i, j_base + c * 32, alpha, i_end, j_end, partial);
             if (partial) {
                 // the CTA whose stages complete the tile converts it and
                 // leaves the accumulator and the counter at zero again
                 epi_bar_sync();
-                if (threadIdx.x == 64) {
+                if (threadIdx.x == 32 * EPI_FIRST_WARP) {
                     __threadfence();
                     const uint32_t add = (uint32_t)(t.kst1 - t.kst0);
                     const uint32_t old = atomicAdd(p.tile_cnt + t.tile, add);
@@ -608,23 +740,43 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                 }
                 epi_bar_sync();
                 if (*last_flag) {
+                    // column-parallel pass over the tile's valid rows: consecutive
+                    // threads take consecutive columns (coalesced), 4 loads in flight
                     __threadfence();
-                    if (i < i_end) {
-                        for (int c = 0; c < BN; ++c) {
-                            const int64_t j = j_base + c;
-                            if (j >= j_end)
-                                break;
-                            float *a = p.acc + i * p.acc_ld_i + j * p.acc_ld_j;
-                            const float y = __ldcg(a);
-                            __stcg(a, 0.0f);
-                            const int64_t off = i * p.ld_i + j * p.ld_j;
+                    const int et = threadIdx.x - 32 * EPI_FIRST_WARP;
+                    const int64_t r0 = (int64_t)t.tile_m * BM;
+                    const int rows = (int)(p.a_rows - r0 < BM ? p.a_rows - r0 : BM);
+                    const int64_t c0 = (int64_t)t.tile_n * BN;
+                    const int cols = (int)(p.b_rows - c0 < BN ? p.b_rows - c0 : BN);
+                    const int total = rows * BN;
+                    for (int base = et; base < total; base += 4 * 32 * EPI_WARPS) {
+                        float y[4];
+                        int64_t ai[4];
+                        bool ok4[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int idx = base + u * 32 * EPI_WARPS;
+                            const int r = idx / BN, c = idx - (idx / BN) * BN;
+                            ok4[u] = idx < total && c < cols;
+                            ai[u] = (r0 + r) * p.acc_ld_i + (c0 + c) * p.acc_ld_j;
+                            y[u] = ok4[u] ? __ldcg(p.acc + ai[u]) : 0.0f;
+                        }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            if (!ok4[u])
+                                continue;
+                            const int idx = base + u * 32 * EPI_WARPS;
+                            const int r = idx / BN, c = idx - (idx / BN) * BN;
+                            __stcg(p.acc + ai[u], 0.0f);
+                            const int64_t off = (r0 + r) * p.ld_i + (c0 + c) * p.ld_j;
                             if (p.out_dtype == NVFP4_OUT_BF16)
-                                static_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(y);
+                                static_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(y[u]);
                             else
-                                static_cast<float *>(p.out)[off] = y;
+                                static_cast<float *>(p.out)[off] = y[u];
                         }
                     }
-                    if (threadIdx.x == 64)
+                    epi_bar_sync();
+                    if (threadIdx.x == 32 * EPI_FIRST_WARP)
                         p.tile_cnt[t.tile] = 0;
                 }
             }
@@ -640,49 +792,42 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
 }
 
 template <int BN, bool GROUPED>
-cudaError_t launch(const Params &p, int total_items, cudaStream_t stream)
+cudaError_t launch(const Params &p, int grid_units, cudaStream_t stream)
 {
     using C = Cfg<BN>;
     auto kern = w4a4_kernel<BN, GROUPED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess)
         return e;
-    const int grid = std::max(1, std::min(total_items, device_sm_count()));
+    const int grid = std::max(1, std::min(grid_units, device_sm_count()));
     kern<<<grid, THREADS, C::SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t dispatch(int bn, bool grouped, const Params &p, int total_items, cudaStream_t stream)
+cudaError_t dispatch(int bn, bool grouped, const Params &p, int grid_units, cudaStream_t stream)
 {
-    if (grouped) {
-        switch (bn) {
-        case 128: return launch<128, true>(p, total_items, stream);
-        case 256: return launch<256, true>(p, total_items, stream);
-        default: return cudaErrorInvalidValue;
-        }
-    }
-    switch (bn) {
-    case 16: return launch<16, false>(p, total_items, stream);
-    case 32: return launch<32, false>(p, total_items, stream);
-    case 64: return launch<64, false>(p, total_items, stream);
-    case 128: return launch<128, false>(p, total_items, stream);
-    case 256: return launch<256, false>(p, total_items, stream);
-    default: return cudaErrorInvalidValue;
-    }
+    if (grouped)
+        return bn == 256 ? launch<256, true>(p, grid_units, stream) : launch<128, true>(p, grid_units, stream);
+    return bn == 256 ? launch<256, false>(p, grid_units, stream) : launch<128, false>(p, grid_units, stream);
+}
+
+// Band of M-tiles that run together: every M-tile when the quantised
+// activations fit comfortably in L2 (each weight tile then streams from HBM
+// once), else 8.
+int group_m_for(int64_t m_tiles, int64_t K)
+{
+    const int64_t a_bytes = m_tiles * 128 * (K / 2 + K / 16);
+    if (a_bytes <= ((int64_t)48 << 20))
+        return (int)std::max<int64_t>(1, m_tiles);
+    return (int)std::min<int64_t>(8, m_tiles);
 }
 
 } // namespace
 
-// N-side tile width: a narrow N side (<= 64 rows, e.g. decode activations after
-// the operands are swapped) takes one tile of the smallest MMA N that covers it.
+// N-side tile width: 256 when N fills it (every weight tile starts on a scale
+// atom), 128 for narrow N.
 int w4a4_dense_bn(int64_t b_rows)
 {
-    if (b_rows <= 16)
-        return 16;
-    if (b_rows <= 32)
-        return 32;
-    if (b_rows <= 64)
-        return 64;
     if (b_rows <= 128 || (b_rows % 256 != 0 && b_rows < 1024))
         return 128;
     return 256;
@@ -701,6 +846,7 @@ cudaError_t launch_w4a4_dense(const DenseGemmArgs &g, cudaStream_t stream)
     p.n_tiles = (int)n_tiles;
     p.k64 = (int)k64;
     p.kstages = (int)kstages;
+    p.group_m = group_m_for(m_tiles, g.K);
     p.streamk = g.streamk ? 1 : 0;
     CUresult r = make_tmap_2d_u8(&p.tmap_a, g.a_codes, (uint64_t)(g.K / 2), (uint64_t)g.a_rows,
                                  (uint64_t)(g.K / 2), STAGE_K_BYTES, BM, true);
@@ -749,6 +895,7 @@ cudaError_t launch_w4a4_grouped(const GroupedGemmArgs &g, cudaStream_t stream)
     p.k64 = (int)k64;
     p.kstages = (int)ceil_div(k64, 4);
     p.streamk = 0;
+    p.group_m = 1;
     CUresult r = make_tmap_2d_u8(&p.tmap_a, g.a_codes, (uint64_t)(g.K / 2), (uint64_t)g.a_rows,
                                  (uint64_t)(g.K / 2), STAGE_K_BYTES, BM, true);
     if (r != CUDA_SUCCESS)

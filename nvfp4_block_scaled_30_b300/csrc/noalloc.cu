@@ -81,29 +81,17 @@ extern "C" nvfp4_status nvfp4_gemm_w4a4_noalloc(const nvfp4_tensor *a_q, const n
     if (!y || (reinterpret_cast<uintptr_t>(y) % 16) != 0 || ldy < N)
         return NVFP4_ERR_INVALID_ARG;
 
-    // the same launch shape nvfp4_gemm picks: operands swapped for M <= 64,
-    // stream-K when whole tiles fill the SMs poorly
+    // the same launch shape nvfp4_gemm picks: stream-K when whole tiles fill
+    // the SMs poorly
     DenseGemmArgs g{};
-    const bool swap = M <= 64;
-    if (swap) {
-        g.a_codes = static_cast<const uint8_t *>(w->codes);
-        g.a_scales = static_cast<const uint8_t *>(w->scales);
-        g.a_second = static_cast<const float *>(w->second);
-        g.a_rows = N;
-        g.b_codes = static_cast<const uint8_t *>(a_q->codes);
-        g.b_scales = static_cast<const uint8_t *>(a_q->scales);
-        g.b_second = static_cast<const float *>(a_q->second);
-        g.b_rows = M;
-    } else {
-        g.a_codes = static_cast<const uint8_t *>(a_q->codes);
-        g.a_scales = static_cast<const uint8_t *>(a_q->scales);
-        g.a_second = static_cast<const float *>(a_q->second);
-        g.a_rows = M;
-        g.b_codes = static_cast<const uint8_t *>(w->codes);
-        g.b_scales = static_cast<const uint8_t *>(w->scales);
-        g.b_second = static_cast<const float *>(w->second);
-        g.b_rows = N;
-    }
+    g.a_codes = static_cast<const uint8_t *>(a_q->codes);
+    g.a_scales = static_cast<const uint8_t *>(a_q->scales);
+    g.a_second = static_cast<const float *>(a_q->second);
+    g.a_rows = M;
+    g.b_codes = static_cast<const uint8_t *>(w->codes);
+    g.b_scales = static_cast<const uint8_t *>(w->scales);
+    g.b_second = static_cast<const float *>(w->second);
+    g.b_rows = N;
     g.K = K;
     const int sms = device_sm_count();
     const int bn = w4a4_dense_bn(g.b_rows);
@@ -132,13 +120,13 @@ extern "C" nvfp4_status nvfp4_gemm_w4a4_noalloc(const nvfp4_tensor *a_q, const n
     g.timeout_ns = NOALLOC_TIMEOUT_NS;
     g.out = y;
     g.out_dtype = y_dtype;
-    g.ld_i = swap ? 1 : ldy;
-    g.ld_j = swap ? ldy : 1;
+    g.ld_i = ldy;
+    g.ld_j = 1;
     g.streamk = streamk;
     if (streamk) {
         g.acc = reinterpret_cast<float *>(base + WS_HEADER);
-        g.acc_ld_i = swap ? 1 : N;
-        g.acc_ld_j = swap ? N : 1;
+        g.acc_ld_i = N;
+        g.acc_ld_j = 1;
         g.tile_cnt = reinterpret_cast<uint32_t *>(base + WS_HEADER + acc_bytes);
     }
     const cudaError_t e = launch_w4a4_dense(g, s);

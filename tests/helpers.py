@@ -20,12 +20,25 @@ def untile_scales(tiled: np.ndarray, rows: int, K: int) -> np.ndarray:
     return np.ascontiguousarray(t.transpose(0, 3, 2, 1, 4)).reshape(-1, K // 16)[:rows]
 
 
-def row_tolerance_ok(y_gpu: np.ndarray, y_ref: np.ndarray, rel: float = 1e-3):
+def bf16_half_ulp(y: np.ndarray) -> np.ndarray:
+    """Half the BF16 spacing at |y| (the largest error of rounding y to BF16)."""
+    a = np.abs(np.asarray(y, np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, np.exp2(e - 8), 0.0)
+
+
+def row_tolerance_ok(y_gpu: np.ndarray, y_ref: np.ndarray, rel: float = 1e-3, out_bf16: bool = False):
     """Per output row m: max_n |Y_gpu - Y_ref| <= rel * ||Y_ref[m, :]||_2
-    (zero rows must be exactly zero).  Returns (ok, worst ratio)."""
+    (zero rows must be exactly zero).  For BF16 outputs each element may in
+    addition carry the rounding of Y_ref to BF16 (half a BF16 ulp), since the
+    output format alone cannot hold a dominant element of a row to 1e-3 of the
+    row norm.  Returns (ok, worst ratio)."""
     y_gpu = np.asarray(y_gpu, np.float64)
     y_ref = np.asarray(y_ref, np.float64)
-    err = np.abs(y_gpu - y_ref).max(axis=1)
+    diff = np.abs(y_gpu - y_ref)
+    if out_bf16:
+        diff = np.maximum(diff - bf16_half_ulp(y_ref), 0.0)
+    err = diff.max(axis=1)
     norm = np.sqrt((y_ref ** 2).sum(axis=1))
     zero = norm == 0
     ratio = np.where(zero, np.where(err == 0, 0.0, np.inf), err / np.where(zero, 1, norm))

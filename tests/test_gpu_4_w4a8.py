@@ -64,7 +64,7 @@ def test_w4a8_route_against_oracle(M, N, K):
     a8, st = oracle.fp8_token_encode(xb)
     rows = np.arange(M) if M <= 300 else np.concatenate([[0, M - 1], np.random.default_rng(M).choice(M, 30, replace=False)])
     ref = oracle.gemm_w4a8(a8, st, (wc, ws, wg[0]), rows=rows)
-    ok, worst = row_tolerance_ok(y_np(y)[rows], ref)
+    ok, worst = row_tolerance_ok(y_np(y)[rows], ref, out_bf16=True)
     assert ok, worst
     # the separately exposed pieces give the same result
     a_dev, st_dev = nv.quantize_fp8(dev_bf16(xb))

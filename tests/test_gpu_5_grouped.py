@@ -42,7 +42,7 @@ def check_experts(y, a_q, row_idx, offsets, wc, ws, wg, experts):
             continue
         rows = row_idx[lo:hi].astype(np.int64) if row_idx is not None else np.arange(lo, hi)
         ref = oracle.gemm_w4a4(a_q, (wc[e], ws[e], wg[e]), rows=rows)
-        ok, worst = row_tolerance_ok(y[lo:hi], ref)
+        ok, worst = row_tolerance_ok(y[lo:hi], ref, out_bf16=True)
         assert ok, f"expert {e}: {worst}"
 
 

@@ -14,7 +14,9 @@
 // Design (one CTA per SM, persistent, warp-specialised, 352 threads):
 //   warp 0      producer: A/B code tiles by TMA (128-byte rows = 256 FP4,
 //               128-byte swizzle) and the compact 512-byte scale atoms by bulk
-//               copies, into a STAGES-deep ring.
+//               copies, into a STAGES-deep ring; each copy of a stage is
+//               issued by its own lane (one thread's copies are served in
+//               order, different threads' copies in parallel).
 //   warp 1      allocates TMEM; lane 0 issues tcgen05.mma kind::mxf4nvf4
 //               (M = 128, N = BN, K = 64; 4 per stage) and tcgen05.commit.
 //   warp 2      scale warp: rewrites each stage's atoms into the 128x256b copy
@@ -94,6 +96,8 @@ struct Params {
     int32_t m_tiles, n_tiles, k64, kstages, streamk, group_m;
     int32_t out_dtype, vec_ok;
     int32_t b_row_tiles;    // 128-row scale atoms available in B (total)
+    int32_t pf_dist;        // L2 prefetch distance in stages (0: none)
+    int32_t a_box_rows;     // rows of A one stage loads (128, or M rounded up to 16 when M < 128)
     // grouped mode
     const int64_t *offsets;
     const int32_t *row_idx;
@@ -252,15 +256,14 @@ __device__ __forceinline__ void tc_cp_128x256b(uint32_t taddr, uint32_t src)
     asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
 }
 
-// Scale warp, lane l: copy one compact atom (32 rows x 16 B; row l holds the
-// 4 scales of rows l, l+32, l+64, l+96 in words 0..3) into a K-core of a copy
-// source, once per TMEM lane quarter (rows l, 32+l, 64+l, 96+l).  Each lane
+// Scale warp, lane l: write row l of one compact atom (32 rows x 16 B; row l
+// holds the 4 scales of rows l, l+32, l+64, l+96 in words 0..3) into a K-core
+// of a copy source, once per TMEM lane quarter (rows l, 32+l, 64+l, 96+l).  Each lane
 // quarter of the tensor core reads scales from its own 32 TMEM lanes: for
 // the B operand every quarter needs every row's scales, and for A row m the
 // word m/32 of lane m holds them.
-__device__ __forceinline__ void spread_atom(const uint8_t *atom, uint8_t *kcore, int lane)
+__device__ __forceinline__ void spread_atom(const uint4 v, uint8_t *kcore, int lane)
 {
-    const uint4 v = *reinterpret_cast<const uint4 *>(atom + lane * 16);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const int m = 32 * q + lane;
@@ -343,7 +346,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
     uint64_t *full = reinterpret_cast<uint64_t *>(stg + C::STG_SLOTS * C::STG_BYTES);
     uint64_t *empty = full + C::STAGES;
     uint64_t *sf_ready = empty + C::STAGES;
-    uint64_t *stg_done = sf_ready + C::STAGES;
+    uint64_t *sf_full = sf_ready + C::STAGES;
+    uint64_t *stg_done = sf_full + C::STAGES;
     uint64_t *acc_full = stg_done + C::STG_SLOTS;
     uint64_t *acc_empty = acc_full + C::ACC_BUFS;
     uint64_t *drain = acc_empty + C::ACC_BUFS;
@@ -357,9 +361,14 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
     const int lane = threadIdx.x & 31;
     constexpr unsigned FULLMASK = 0xFFFFFFFFu;
 
+    const bool indexed = GROUPED && p.row_idx != nullptr;
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(&full[s], GROUPED ? 2 : 1);
+            // codes: the copies, plus the gather's arrival for indexed rows;
+            // scales: the copies, plus the producer's arrival after it wrote
+            // the gathered activation scales (grouped)
+            mbar_init(&full[s], indexed ? 2 : 1);
+            mbar_init(&sf_full[s], GROUPED ? 2 : 1);
             mbar_init(&empty[s], 1);
             mbar_init(&sf_ready[s], 1);
         }
@@ -416,7 +425,6 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int total_items = total_items_s;
-    const bool indexed = GROUPED && p.row_idx != nullptr;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -427,6 +435,23 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
         WorkIter wi;
         work_begin(p, total_items, wi);
         Tile t;
+        // L2 prefetch cursor, pf_dist stages ahead of the loads along this
+        // CTA's own work sequence: the tiles a stage reads are often first
+        // touched by several CTAs at once, and a prefetch issued earlier
+        // turns their HBM latency into an L2 hit without holding shared memory
+        WorkIter pw;
+        work_begin(p, total_items, pw);
+        Tile pt;
+        bool pf_live = work_next<GROUPED>(p, prefix, total_items, pw, pt);
+        int pkb = pf_live ? pt.kst0 : 0;
+        auto pf_advance = [&]() {
+            if (pf_live && ++pkb >= pt.kst1) {
+                pf_live = work_next<GROUPED>(p, prefix, total_items, pw, pt);
+                pkb = pf_live ? pt.kst0 : 0;
+            }
+        };
+        for (int i = 0; i < p.pf_dist; ++i)
+            pf_advance();
         while (ok && work_next<GROUPED>(p, prefix, total_items, wi, t)) {
             // grouped: source activation row of tile rows lane + 32q
             int src_row[4] = {0, 0, 0, 0};
@@ -461,26 +486,50 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
 #pragma unroll
                 for (int h = 0; h < C::NB; ++h)
                     nb_loaded += (bt0 + h < p.b_row_tiles) ? 1 : 0;
-                uint32_t bytes = C::B_BYTES + nb_loaded * nk * 512;
-                if (!indexed)
-                    bytes += C::A_BYTES;
-                if (!GROUPED)
-                    bytes += nk * 512;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&full[stage], bytes);
-                    if (!indexed) {
-                        const int arow = GROUPED ? (int)t.row0 : t.tile_m * BM;
-                        tma_load_2d(sA, &p.tmap_a, kb * STAGE_K_BYTES, arow, &full[stage]);
-                    }
-                    tma_load_2d(sB, &p.tmap_b, kb * STAGE_K_BYTES, brow0, &full[stage]);
-                    if (!GROUPED)
-                        bulk_load(sSFA, p.sfa + ((size_t)t.tile_m * p.k64 + 4 * kb) * 512, nk * 512, &full[stage]);
-#pragma unroll
-                    for (int h = 0; h < C::NB; ++h)
-                        if (bt0 + h < p.b_row_tiles)
-                            bulk_load(sSFB + h * 2048, p.sfb + ((size_t)(bt0 + h) * p.k64 + 4 * kb) * 512, nk * 512,
-                                      &full[stage]);
+                // codes and scales land on separate barriers, so the scale
+                // warp starts on a stage's (small) scale copies while its
+                // codes are still in flight
+                const uint32_t code_bytes = C::B_BYTES + (indexed ? 0u : (uint32_t)p.a_box_rows * STAGE_K_BYTES);
+                const uint32_t sf_bytes = (nb_loaded + (GROUPED ? 0 : 1)) * nk * 512;
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&full[stage], code_bytes);
+                else if (lane == 1)
+                    mbar_arrive_expect_tx(&sf_full[stage], sf_bytes);
+                __syncwarp();
+                // One copy per lane: copies issued by one thread are served
+                // one after another, copies from different threads overlap.
+                // Lanes 8r..8r+4 serve stages r, r+4, ... so each thread has
+                // at most one copy of four consecutive stages outstanding.
+                // op 0: A codes, 1: B codes, 2: A scales, 3..3+NB-1: B scales
+                const int op = lane - 8 * (issued & 3);
+                if (op == 1 || (op == 0 && !indexed)) {
+                    const int arow = GROUPED ? (int)t.row0 : t.tile_m * BM;
+                    tma_load_2d(op == 0 ? sA : sB, op == 0 ? &p.tmap_a : &p.tmap_b, kb * STAGE_K_BYTES,
+                                op == 0 ? arow : brow0, &full[stage]);
+                } else if ((op == 2 && !GROUPED) || (op >= 3 && op < 3 + C::NB && bt0 + op - 3 < p.b_row_tiles)) {
+                    const uint8_t *src = op == 2 ? p.sfa + ((size_t)t.tile_m * p.k64 + 4 * kb) * 512
+                                                 : p.sfb + ((size_t)(bt0 + op - 3) * p.k64 + 4 * kb) * 512;
+                    bulk_load(op == 2 ? sSFA : sSFB + (op - 3) * 2048, src, nk * 512, &sf_full[stage]);
                 }
+                if (pf_live && p.pf_dist > 0) {
+                    // ops 5, 6, 7: L2 prefetch of stage pkb of tile pt
+                    const int pnk = min(4, p.k64 - 4 * pkb);
+                    if (op == 5 && !indexed) {
+                        tma_prefetch_2d(&p.tmap_a, pkb * STAGE_K_BYTES, GROUPED ? (int)pt.row0 : pt.tile_m * BM);
+                        if (!GROUPED)
+                            bulk_prefetch_l2(p.sfa + ((size_t)pt.tile_m * p.k64 + 4 * pkb) * 512, pnk * 512);
+                    } else if (op == 6) {
+                        tma_prefetch_2d(&p.tmap_b, pkb * STAGE_K_BYTES,
+                                        GROUPED ? pt.expert * (int)p.b_rows + pt.tile_n * BN : pt.tile_n * BN);
+                    } else if (op == 7) {
+                        const int pbt0 = (GROUPED ? pt.expert * (int)p.b_rows + pt.tile_n * BN : pt.tile_n * BN) / 128;
+#pragma unroll
+                        for (int h = 0; h < C::NB; ++h)
+                            if (pbt0 + h < p.b_row_tiles)
+                                bulk_prefetch_l2(p.sfb + ((size_t)(pbt0 + h) * p.k64 + 4 * pkb) * 512, pnk * 512);
+                    }
+                }
+                pf_advance();
                 if (GROUPED) {
                     if (indexed) {
                         // gathered code rows: 16-byte cp.async with the 128-byte
@@ -512,12 +561,17 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                             *reinterpret_cast<uint32_t *>(sSFA + kk * 512 + lane * 16 + q * 4) = v;
                         }
                     }
-                    if (indexed)
-                        cp_async_wait_all();
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0)
-                        mbar_arrive(&full[stage]);
+                        mbar_arrive(&sf_full[stage]);
+                    if (indexed) {
+                        cp_async_wait_all();
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(&full[stage]);
+                    }
                 }
                 ++issued;
                 if (++stage == C::STAGES) {
@@ -537,6 +591,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                     ph ^= 1u;
                 }
                 mbar_wait(&full[s], ph, p.timeout_ns, nullptr);
+                mbar_wait(&sf_full[s], ph, p.timeout_ns, nullptr);
             }
         }
         __syncwarp();
@@ -614,7 +669,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
         Tile t;
         while (ok && work_next<GROUPED>(p, prefix, total_items, wi, t)) {
             for (int kb = t.kst0; kb < t.kst1; ++kb) {
-                bool got = mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag);
+                bool got = mbar_wait(&sf_full[stage], phase, p.timeout_ns, abort_flag);
                 if (got && slot_uses[slot] > 0)
                     got = mbar_wait(&stg_done[slot], (uint32_t)((slot_uses[slot] - 1) & 1), p.timeout_ns,
                                     abort_flag);
@@ -628,19 +683,30 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                 const uint8_t *sSFA = smem + stage * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
                 const uint8_t *sSFB = sSFA + C::SFA_BYTES;
                 uint8_t *src = stg + slot * C::STG_BYTES;
-                // A: source (kk / 2), K-core (kk % 2)
-                for (int kk = 0; kk < nk; ++kk)
-                    spread_atom(sSFA + kk * 512, src + (kk >> 1) * CP_SRC_BYTES + (kk & 1) * KCORE_BYTES, lane);
+                // every atom of the stage is read before any is written, so
+                // the shared-memory loads overlap; atoms past nk (a K tail)
+                // hold stale bytes that no copy or MMA uses
+                uint4 va[4], vb[4 * C::NB];
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    va[kk] = *reinterpret_cast<const uint4 *>(sSFA + kk * 512 + lane * 16);
+#pragma unroll
+                    for (int h = 0; h < C::NB; ++h)
+                        vb[kk * C::NB + h] = *reinterpret_cast<const uint4 *>(sSFB + h * 2048 + kk * 512 + lane * 16);
+                }
                 uint8_t *srcb = src + C::CPS_A * CP_SRC_BYTES;
-                if (C::NB == 1) {
-                    for (int kk = 0; kk < nk; ++kk)
-                        spread_atom(sSFB + kk * 512, srcb + (kk >> 1) * CP_SRC_BYTES + (kk & 1) * KCORE_BYTES, lane);
-                } else {
-                    // B: source kk, K-core h = 128-row group h (rows 0-127 / 128-255)
-                    for (int kk = 0; kk < nk; ++kk)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    // A: source kk / 2, K-core kk % 2
+                    spread_atom(va[kk], src + (kk >> 1) * CP_SRC_BYTES + (kk & 1) * KCORE_BYTES, lane);
+                    if (C::NB == 1) {
+                        spread_atom(vb[kk], srcb + (kk >> 1) * CP_SRC_BYTES + (kk & 1) * KCORE_BYTES, lane);
+                    } else {
+                        // B: source kk, K-core h = 128-row group h (rows 0-127 / 128-255)
 #pragma unroll
                         for (int h = 0; h < C::NB; ++h)
-                            spread_atom(sSFB + h * 2048 + kk * 512, srcb + kk * CP_SRC_BYTES + h * KCORE_BYTES, lane);
+                            spread_atom(vb[kk * C::NB + h], srcb + kk * CP_SRC_BYTES + h * KCORE_BYTES, lane);
+                    }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -822,6 +888,15 @@ int group_m_for(int64_t m_tiles, int64_t K)
     return (int)std::min<int64_t>(8, m_tiles);
 }
 
+// L2 prefetch distance in stages.  Measured on B300 (decode 8x28672x8192
+// and prefill 4096x8192x8192): prefetching 3 to 10 stages ahead was neutral
+// to 5% slower, since the copies themselves, not HBM latency, bound a
+// stage; the cursor stays for shapes where it pays, off by default.
+int pf_dist_for(int /*bn*/)
+{
+    return 0;
+}
+
 } // namespace
 
 // N-side tile width: 256 when N fills it (every weight tile starts on a scale
@@ -848,8 +923,12 @@ cudaError_t launch_w4a4_dense(const DenseGemmArgs &g, cudaStream_t stream)
     p.kstages = (int)kstages;
     p.group_m = group_m_for(m_tiles, g.K);
     p.streamk = g.streamk ? 1 : 0;
+    // a single M-tile of fewer than 128 rows loads only its rows (rounded
+    // up to 16); the MMA still reads 128 rows, and the rows past the box
+    // only feed output rows that are never stored
+    p.a_box_rows = g.a_rows < BM ? (int)ceil_div(g.a_rows, 16) * 16 : BM;
     CUresult r = make_tmap_2d_u8(&p.tmap_a, g.a_codes, (uint64_t)(g.K / 2), (uint64_t)g.a_rows,
-                                 (uint64_t)(g.K / 2), STAGE_K_BYTES, BM, true);
+                                 (uint64_t)(g.K / 2), STAGE_K_BYTES, (uint32_t)p.a_box_rows, true);
     if (r != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     r = make_tmap_2d_u8(&p.tmap_b, g.b_codes, (uint64_t)(g.K / 2), (uint64_t)g.b_rows, (uint64_t)(g.K / 2),
@@ -879,6 +958,7 @@ cudaError_t launch_w4a4_dense(const DenseGemmArgs &g, cudaStream_t stream)
     p.E = 0;
     p.status = g.status;
     p.timeout_ns = g.timeout_ns;
+    p.pf_dist = pf_dist_for(bn);
     const int tiles = p.m_tiles * p.n_tiles;
     // stream-K: one CTA per SM over all (tile, stage) units
     const int grid_units = g.streamk ? (int)std::min<int64_t>((int64_t)tiles * kstages, sms) : tiles;
@@ -896,6 +976,7 @@ cudaError_t launch_w4a4_grouped(const GroupedGemmArgs &g, cudaStream_t stream)
     p.kstages = (int)ceil_div(k64, 4);
     p.streamk = 0;
     p.group_m = 1;
+    p.a_box_rows = BM;
     CUresult r = make_tmap_2d_u8(&p.tmap_a, g.a_codes, (uint64_t)(g.K / 2), (uint64_t)g.a_rows,
                                  (uint64_t)(g.K / 2), STAGE_K_BYTES, BM, true);
     if (r != CUDA_SUCCESS)
@@ -924,6 +1005,7 @@ cudaError_t launch_w4a4_grouped(const GroupedGemmArgs &g, cudaStream_t stream)
     p.total_rows = g.total_rows;
     p.status = g.status;
     p.timeout_ns = g.timeout_ns;
+    p.pf_dist = pf_dist_for(bn);
     // upper bound of items: every expert's rows in tiles of 128, plus one partial tile per expert
     const int64_t max_tiles = ceil_div(g.total_rows, BM) + g.E;
     const int total = (int)std::min<int64_t>(max_tiles * p.n_tiles, 1 << 30);

@@ -29,6 +29,10 @@
 //   warps 3-10  epilogue: tcgen05.ld of the FP32 accumulator into registers,
 //               release of the accumulator, then alpha scale and BF16/FP32
 //               stores (or FP32 red.add of stream-K partial tiles).
+// The dense launch is a programmatic dependent launch: set-up, tensor-map
+// fetch and the first weight stages' L2 prefetch overlap the previous grid
+// (normally the activation quantiser); every access to memory the previous
+// grid touches comes after griddepcontrol.wait.
 // Every mbarrier wait is bounded; on timeout the CTA records NVFP4 TIMEOUT in
 // the status word, drains its in-flight copies and MMAs, frees TMEM and
 // exits (epilogue warps decide together through a barrier reduction).
@@ -388,6 +392,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
     }
     if (GROUPED) {
         if (warp == 2) {
+            pdl_wait(); // the expert offsets may come from the previous grid
             // tiles per expert, prefix-summed by one warp: lane l owns a
             // contiguous run of experts; a shuffle scan joins the runs
             const int per = (p.E + 31) / 32;
@@ -444,6 +449,24 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
         Tile pt;
         bool pf_live = work_next<GROUPED>(p, prefix, total_items, pw, pt);
         int pkb = pf_live ? pt.kst0 : 0;
+        // before waiting for the previous grid (programmatic dependent
+        // launch): fetch the tensor maps and start the first weight stages
+        // towards L2 (weights do not depend on the previous grid)
+        if (lane == 0) {
+            prefetch_tmap(&p.tmap_a);
+            prefetch_tmap(&p.tmap_b);
+        }
+        if (pf_live && lane < C::STAGES && pt.kst0 + lane < pt.kst1) {
+            const int kq = pt.kst0 + lane;
+            const int brow = GROUPED ? pt.expert * (int)p.b_rows + pt.tile_n * BN : pt.tile_n * BN;
+            tma_prefetch_2d(&p.tmap_b, kq * STAGE_K_BYTES, brow);
+#pragma unroll
+            for (int h = 0; h < C::NB; ++h)
+                if (brow / 128 + h < p.b_row_tiles)
+                    bulk_prefetch_l2(p.sfb + ((size_t)(brow / 128 + h) * p.k64 + 4 * kq) * 512,
+                                     min(4, p.k64 - 4 * kq) * 512);
+        }
+        pdl_wait();
         auto pf_advance = [&]() {
             if (pf_live && ++pkb >= pt.kst1) {
                 pf_live = work_next<GROUPED>(p, prefix, total_items, pw, pt);
@@ -597,6 +620,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        pdl_wait(); // bounded waits below start after the previous grid
         if (lane == 0) {
             const uint32_t idesc = idesc_mxf4nvf4(BN);
             int stage = 0;
@@ -659,6 +683,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
         __syncwarp();
     } else if (warp == 2) {
         // ------------------------------------------------------------ scale warp
+        pdl_wait(); // bounded waits below start after the previous grid
         int stage = 0;
         uint32_t phase = 0;
         int slot = 0;
@@ -750,6 +775,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
         const int row_in_tile = q * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
+        pdl_wait(); // activation scale, output and workspace follow the previous grid
         const float a_s = *p.a_second;
         WorkIter wi;
         work_begin(p, total_items, wi);
@@ -866,6 +892,8 @@ cudaError_t launch(const Params &p, int grid_units, cudaStream_t stream)
     if (e != cudaSuccess)
         return e;
     const int grid = std::max(1, std::min(grid_units, device_sm_count()));
+    if (!GROUPED)
+        return launch_pdl(kern, grid, THREADS, C::SMEM_BYTES, stream, p);
     kern<<<grid, THREADS, C::SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
 }

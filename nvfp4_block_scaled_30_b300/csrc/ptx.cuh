@@ -108,6 +108,26 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// Programmatic dependent launch.  pdl_wait blocks until the grids this one
+// depends on have completed and their memory is visible (no-op when the
+// launch carried no programmatic dependency); pdl_trigger lets the next
+// grid in the stream start launching.
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Fetch a tensor map (kernel parameter) into the descriptor cache.
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 // L2 prefetch of one tile of a 2-D tensor map (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int32_t x, int32_t y)
 {

@@ -14,9 +14,10 @@
 //   t = amax_b / 6, u = t / s, e = E4M3(u) (0 when s == 0), d = e * s,
 //   r = 1 / d (0 when d == 0, at most FLT_MAX), code = E2M1(x * r).
 //
-// Memory: each thread owns 8 consecutive BF16 values (one 16-byte load);
-// a lane pair owns one 16-element block (absmax by one shfl.xor); the pair
-// writes 8 packed code bytes (one 32-bit store each) and one scale byte.
+// Memory: each thread owns 8 consecutive BF16 values per 16-byte load and
+// keeps several loads in flight; a lane pair owns one 16-element block
+// (absmax by one shfl.xor); the pair writes 8 packed code bytes (one 32-bit
+// store each) and one scale byte.
 #include <cfloat>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -92,22 +93,43 @@ __device__ __forceinline__ size_t scale_offset(int64_t row, int64_t blk, int64_t
     return (size_t)(((row >> 7) * (K / 64) + (blk >> 2)) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (blk & 3));
 }
 
-// Pass 1: per-CTA maximum of |x| (as BF16 magnitude bits) and a non-finite flag.
+// Loads in flight per thread in the streaming passes.
+constexpr int QU = 4;
+
+// Pass 1: per-CTA maximum of |x| (as BF16 magnitude bits) and a non-finite
+// flag.  The rows x K/8 chunks of 8 values are one flat index space, so small
+// row counts still spread over many CTAs; each thread keeps QU 16-byte loads
+// in flight.
 __global__ void __launch_bounds__(QT) amax_partial_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t K,
                                                           int64_t ldx, uint32_t *__restrict__ partial,
                                                           uint32_t *__restrict__ status)
 {
     __shared__ uint32_t red[QT / 32];
+    // launched as a programmatic dependent: wait for the previous grid (it
+    // may still read the buffers this pass and the next one write)
+    pdl_wait();
+    pdl_trigger();
     const int64_t cpr = K / 8;
+    const int64_t total = rows * cpr;
+    const int64_t stride = (int64_t)gridDim.x * QT * QU;
     uint32_t m = 0, bad = 0;
-    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
-        const uint16_t *xr = x + row * ldx;
-        for (int64_t j = threadIdx.x; j < cpr; j += QT) {
-            uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr + j * 8));
-            uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    for (int64_t base = (int64_t)blockIdx.x * QT * QU + threadIdx.x; base < total; base += stride) {
+        uint4 v[QU];
+#pragma unroll
+        for (int u = 0; u < QU; ++u) {
+            const int64_t idx = base + (int64_t)u * QT;
+            v[u] = make_uint4(0, 0, 0, 0);
+            if (idx < total) {
+                const int64_t row = idx / cpr, j = idx - row * cpr;
+                v[u] = __ldg(reinterpret_cast<const uint4 *>(x + row * ldx + j * 8));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < QU; ++u) {
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                uint32_t lo = w[i] & 0x7FFFu, hi = (w[i] >> 16) & 0x7FFFu;
+                const uint32_t lo = w[i] & 0x7FFFu, hi = (w[i] >> 16) & 0x7FFFu;
                 bad |= (lo >= 0x7F80u) | (hi >= 0x7F80u);
                 m = max(m, max(lo, hi));
             }
@@ -115,18 +137,17 @@ __global__ void __launch_bounds__(QT) amax_partial_kernel(const uint16_t *__rest
     }
     bad = __any_sync(FULL, bad);
     uint32_t bm = block_max_u32(m, red);
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0)
         partial[blockIdx.x] = bm;
-        if (bad)
-            atomicOr(status, ST_NONFINITE);
-    }
     if (bad && (threadIdx.x & 31) == 0)
         atomicOr(status, ST_NONFINITE);
 }
 
 // Pass 2, tensor-scale mode.  Every CTA reduces the partial maxima itself,
-// so no extra launch or host synchronisation is needed.  Rows rows..rows_pad
-// (tiled layout padding) get zero scales.
+// so no extra launch or host synchronisation is needed.  The real rows' chunks
+// form one flat index space (a lane pair = one 16-element block, never split
+// across rows since K/8 is even); the padding rows rows..rows_pad of the tiled
+// layout only get zero scales, written by a separate loop.
 template <bool TILED>
 __global__ void __launch_bounds__(QT) nvfp4_encode_kernel(const uint16_t *__restrict__ x, int64_t rows,
                                                           int64_t rows_pad, int64_t K, int64_t ldx,
@@ -135,6 +156,8 @@ __global__ void __launch_bounds__(QT) nvfp4_encode_kernel(const uint16_t *__rest
                                                           const uint32_t *__restrict__ partial, int n_partial)
 {
     __shared__ uint32_t red[QT / 32];
+    pdl_wait(); // the partial maxima of pass 1
+    pdl_trigger();
     uint32_t m = 0;
     for (int i = threadIdx.x; i < n_partial; i += QT)
         m = max(m, partial[i]);
@@ -144,26 +167,50 @@ __global__ void __launch_bounds__(QT) nvfp4_encode_kernel(const uint16_t *__rest
         *sg_out = sg;
 
     const int64_t cpr = K / 8;
-    for (int64_t row = blockIdx.x; row < rows_pad; row += gridDim.x) {
-        const bool real_row = row < rows;
-        for (int64_t j0 = 0; j0 < cpr; j0 += QT) {
-            const int64_t j = j0 + threadIdx.x;
-            const bool valid = j < cpr;
-            const bool real = valid && real_row;
-            float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            if (real)
-                bf16x8(x + row * ldx + j * 8, f);
+    const int64_t total = rows * cpr;
+    const int64_t stride = (int64_t)gridDim.x * QT * QU;
+    // the trip count follows the warp's first index, so every lane of a warp
+    // runs the same iterations (the pair shuffle needs the whole warp)
+    for (int64_t base = (int64_t)blockIdx.x * QT * QU + threadIdx.x; base - (threadIdx.x & 31) < total;
+         base += stride) {
+        float f[QU][8];
+#pragma unroll
+        for (int u = 0; u < QU; ++u) {
+            const int64_t idx = base + (int64_t)u * QT;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                f[u][i] = 0.0f;
+            if (idx < total) {
+                const int64_t row = idx / cpr, j = idx - row * cpr;
+                bf16x8(x + row * ldx + j * 8, f[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < QU; ++u) {
+            const int64_t idx = base + (int64_t)u * QT;
+            const bool real = idx < total;
             float am = 0.0f;
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                am = fmaxf(am, fabsf(f[i]));
+                am = fmaxf(am, fabsf(f[u][i]));
             const float amb = fmaxf(am, __shfl_xor_sync(FULL, am, 1));
             const uint32_t e = real ? block_scale_code(amb, sg) : 0u;
             const float r = recip_step(__fmul_rn(e4m3_value(e), sg));
-            if (real)
-                *reinterpret_cast<uint32_t *>(codes + row * (K / 2) + j * 4) = pack8(f, r);
-            if (valid && (threadIdx.x & 1) == 0)
-                scales[scale_offset(row, j >> 1, K, TILED)] = (uint8_t)e;
+            if (real) {
+                const int64_t row = idx / cpr, j = idx - row * cpr;
+                *reinterpret_cast<uint32_t *>(codes + row * (K / 2) + j * 4) = pack8(f[u], r);
+                if ((threadIdx.x & 1) == 0)
+                    scales[scale_offset(row, j >> 1, K, TILED)] = (uint8_t)e;
+            }
+        }
+    }
+    if (TILED) {
+        // one 32-bit word = one padding row's 4 scales of a 64-element chunk
+        const int64_t k64 = K / 64;
+        const int64_t pad = (rows_pad - rows) * k64;
+        for (int64_t i = (int64_t)blockIdx.x * QT + threadIdx.x; i < pad; i += (int64_t)gridDim.x * QT) {
+            const int64_t row = rows + i / k64;
+            *reinterpret_cast<uint32_t *>(scales + scale_offset(row, (i - (i / k64) * k64) * 4, K, true)) = 0u;
         }
     }
 }
@@ -302,14 +349,28 @@ cudaError_t launch_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K, in
         return cudaSuccess;
     const int grid2 = (int)std::min<int64_t>(rows_pad, (int64_t)sms * 8);
     if (mode == NVFP4_SCALE_TENSOR_FP32) {
-        const int grid1 = (int)std::min<int64_t>(std::max<int64_t>(rows, 1), std::min(AMAX_MAX_CTAS, sms * 4));
-        amax_partial_kernel<<<grid1, QT, 0, stream>>>(x, rows, K, ldx, amax_partial, status);
+        // flat passes: enough CTAs for one sweep of QU loads per thread, at
+        // most a few waves
+        const int64_t chunks = std::max<int64_t>(rows * (K / 8), 1);
+        const int64_t per_cta = (int64_t)QT * QU;
+        const int grid1 = (int)std::min<int64_t>(ceil_div(chunks, per_cta), std::min(AMAX_MAX_CTAS, sms * 4));
+        const int64_t pad_words = tiled ? (rows_pad - rows) * (K / 64) : 0;
+        const int grid_e = (int)std::max<int64_t>(
+            1, std::min<int64_t>(std::max(ceil_div(chunks, per_cta), ceil_div(pad_words, (int64_t)QT * 8)),
+                                 (int64_t)sms * 8));
+        cudaError_t e = launch_pdl(amax_partial_kernel, grid1, QT, 0, stream, x, rows, K, ldx, amax_partial, status);
+        if (e != cudaSuccess)
+            return e;
+        float *sg = static_cast<float *>(second);
+        const uint32_t *part = amax_partial;
         if (tiled)
-            nvfp4_encode_kernel<true><<<grid2, QT, 0, stream>>>(x, rows, rows_pad, K, ldx, codes, scales,
-                                                                  static_cast<float *>(second), amax_partial, grid1);
+            e = launch_pdl(nvfp4_encode_kernel<true>, grid_e, QT, 0, stream, x, rows, rows_pad, K, ldx, codes, scales,
+                           sg, part, grid1);
         else
-            nvfp4_encode_kernel<false><<<grid2, QT, 0, stream>>>(x, rows, rows_pad, K, ldx, codes, scales,
-                                                                   static_cast<float *>(second), amax_partial, grid1);
+            e = launch_pdl(nvfp4_encode_kernel<false>, grid_e, QT, 0, stream, x, rows, rows_pad, K, ldx, codes,
+                           scales, sg, part, grid1);
+        if (e != cudaSuccess)
+            return e;
     } else {
         if (tiled)
             nvfp4_encode_macro_kernel<true><<<grid2, QT, 0, stream>>>(x, rows, rows_pad, K, ldx, codes, scales,

@@ -19,13 +19,15 @@
 //               order, different threads' copies in parallel).
 //   warp 1      allocates TMEM; lane 0 issues tcgen05.mma kind::mxf4nvf4
 //               (M = 128, N = BN, K = 64; 4 per stage) and tcgen05.commit.
-//   warp 2      scale warp: rewrites each stage's atoms into the 128x256b copy
-//               layout and moves them to TMEM with tcgen05.cp (4 KB per copy,
-//               two 64-element K chunks of one 128-row group each), off the
-//               MMA thread.  Each TMEM lane quarter of the tensor core reads
-//               scales from its own 32 lanes (row m of A: lane m, column
-//               address + m / 32; B: all rows in every quarter), so each atom
-//               row is written once per quarter.
+//   warp 2      scale warp: moves each stage's compact scale atoms from the
+//               ring to TMEM with tcgen05.cp.32x128b.warpx4 (the copy engine
+//               replicates every 32-row atom into all four TMEM lane
+//               quarters, which is what each quarter of the tensor core
+//               reads: row m of A at lane m, column address + m / 32; B in
+//               every quarter), off the MMA thread.  Measured on B300 this
+//               beats rebuilding replicated copy sources in shared memory
+//               with the threads: shared-memory bandwidth, not the copy
+//               engine, limits a stage.
 //   warps 3-10  epilogue: tcgen05.ld of the FP32 accumulator into registers,
 //               release of the accumulator, then alpha scale and BF16/FP32
 //               stores (or FP32 red.add of stream-K partial tiles).
@@ -52,34 +54,26 @@ constexpr int EPI_WARPS = 8;
 constexpr int EPI_FIRST_WARP = 3;
 constexpr int THREADS = 32 * (EPI_FIRST_WARP + EPI_WARPS);
 constexpr int MAX_EXPERTS = 1024;
-constexpr int CP_SRC_BYTES = 4096;  // one 128x256b copy source: 128 rows x 32 B
-constexpr int KCORE_BYTES = 2048;   // one K-core of it: 128 rows x 16 B
 
 template <int BN>
 struct Cfg {
     static_assert(BN == 128 || BN == 256, "N tile");
     static constexpr int NB = BN / 128;                 // 128-row scale groups per B tile
-    static constexpr int STAGES = BN == 256 ? 3 : 5;
+    static constexpr int STAGES = BN == 256 ? 4 : 6;
     static constexpr int ACC_BUFS = BN == 256 ? 1 : 2;
     static constexpr int A_BYTES = BM * STAGE_K_BYTES;
     static constexpr int B_BYTES = BN * STAGE_K_BYTES;
     static constexpr int SFA_BYTES = 4 * 512;           // compact atoms as loaded
     static constexpr int SFB_BYTES = NB * 4 * 512;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-    // copy sources of one stage: A: 2 (chunk pairs); B: 2 (NB = 1, chunk
-    // pairs) or 4 (NB = 2, one chunk with both 128-row groups per copy)
-    static constexpr int CPS_A = 2;
-    static constexpr int CPS_B = NB == 1 ? 2 : 4;
-    static constexpr int STG_BYTES = (CPS_A + CPS_B) * CP_SRC_BYTES;
-    static constexpr int STG_SLOTS = 2;
     static constexpr int SF_COLS = 16 + 16 * NB;        // TMEM scale columns per stage
     static constexpr int SF_BASE = ACC_BUFS * BN;
     static constexpr int TMEM_COLS = 512;
     static constexpr int BAR_BYTES = 512;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STG_SLOTS * STG_BYTES + BAR_BYTES + 1024;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
     static constexpr int EPI_COLS = BN / 2;              // accumulator columns per epilogue warp
     static_assert(SF_BASE + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
-    static_assert(STAGE_BYTES % 1024 == 0 && STG_BYTES % 1024 == 0, "alignment");
+    static_assert(STAGE_BYTES % 1024 == 0, "alignment");
     static_assert(SMEM_BYTES + 4 * (MAX_EXPERTS + 2) <= 232448, "shared memory budget");
 };
 
@@ -248,33 +242,6 @@ __device__ __forceinline__ void record_timeout(const Params &p, volatile int *ab
     atomicOr(p.status, ST_TIMEOUT);
 }
 
-// 128x256b copy: 128 TMEM lanes x 8 columns from a source of two 2 KB K-cores
-// (K-core c holds bytes 16c..16c+15 of every row; row m at (m/8)*128 + (m%8)*16).
-__device__ __forceinline__ void tc_cp_128x256b(uint32_t taddr, uint32_t src)
-{
-    uint64_t d = 0;
-    d |= (uint64_t)((src >> 4) & 0x3FFFu);
-    d |= (uint64_t)(KCORE_BYTES >> 4) << 16; // leading byte offset: K-core 0 -> 1
-    d |= (uint64_t)(128u >> 4) << 32;        // stride byte offset: 8-row groups
-    d |= (uint64_t)1u << 46;
-    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
-}
-
-// Scale warp, lane l: write row l of one compact atom (32 rows x 16 B; row l
-// holds the 4 scales of rows l, l+32, l+64, l+96 in words 0..3) into a K-core
-// of a copy source, once per TMEM lane quarter (rows l, 32+l, 64+l, 96+l).  Each lane
-// quarter of the tensor core reads scales from its own 32 TMEM lanes: for
-// the B operand every quarter needs every row's scales, and for A row m the
-// word m/32 of lane m holds them.
-__device__ __forceinline__ void spread_atom(const uint4 v, uint8_t *kcore, int lane)
-{
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int m = 32 * q + lane;
-        *reinterpret_cast<uint4 *>(kcore + (m >> 3) * 128 + (m & 7) * 16) = v;
-    }
-}
-
 __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d)
 {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
@@ -346,13 +313,11 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
     using C = Cfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *stg = smem + C::STAGES * C::STAGE_BYTES; // scale copy sources, STG_SLOTS slots
-    uint64_t *full = reinterpret_cast<uint64_t *>(stg + C::STG_SLOTS * C::STG_BYTES);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE_BYTES);
     uint64_t *empty = full + C::STAGES;
     uint64_t *sf_ready = empty + C::STAGES;
     uint64_t *sf_full = sf_ready + C::STAGES;
-    uint64_t *stg_done = sf_full + C::STAGES;
-    uint64_t *acc_full = stg_done + C::STG_SLOTS;
+    uint64_t *acc_full = sf_full + C::STAGES;
     uint64_t *acc_empty = acc_full + C::ACC_BUFS;
     uint64_t *drain = acc_empty + C::ACC_BUFS;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
@@ -376,8 +341,6 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
             mbar_init(&empty[s], 1);
             mbar_init(&sf_ready[s], 1);
         }
-        for (int b = 0; b < C::STG_SLOTS; ++b)
-            mbar_init(&stg_done[b], 1);
         for (int b = 0; b < C::ACC_BUFS; ++b) {
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], EPI_WARPS);
@@ -654,9 +617,10 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                     const uint64_t adesc = sdesc_sw128(smem_u32(sA));
                     const uint64_t bdesc = sdesc_sw128(smem_u32(sB));
                     for (int kk = 0; kk < nk; ++kk) {
-                        const uint32_t sfa = sf_col + 8 * (kk >> 1) + 4 * (kk & 1);
-                        const uint32_t sfb = C::NB == 1 ? sf_col + 16 + 8 * (kk >> 1) + 4 * (kk & 1)
-                                                        : sf_col + 16 + 8 * kk;
+                        // A atom kk: 4 columns at 4 kk; B atom (kk, h): 4 columns
+                        // at 16 + 4 kk (one 128-row group) or 16 + 8 kk + 4 h
+                        const uint32_t sfa = sf_col + 4 * kk;
+                        const uint32_t sfb = sf_col + 16 + (C::NB == 1 ? 4 * kk : 8 * kk);
                         // +32 bytes (64 FP4) inside the swizzled 128-byte row
                         mma_mxf4nvf4(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc, sfa,
                                      sfb, accumulate);
@@ -686,74 +650,42 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
         pdl_wait(); // bounded waits below start after the previous grid
         int stage = 0;
         uint32_t phase = 0;
-        int slot = 0;
-        int slot_uses[C::STG_SLOTS] = {0};
+        int issued = 0;
         bool ok = true;
         WorkIter wi;
         work_begin(p, total_items, wi);
         Tile t;
         while (ok && work_next<GROUPED>(p, prefix, total_items, wi, t)) {
             for (int kb = t.kst0; kb < t.kst1; ++kb) {
-                bool got = mbar_wait(&sf_full[stage], phase, p.timeout_ns, abort_flag);
-                if (got && slot_uses[slot] > 0)
-                    got = mbar_wait(&stg_done[slot], (uint32_t)((slot_uses[slot] - 1) & 1), p.timeout_ns,
-                                    abort_flag);
+                const bool got = mbar_wait(&sf_full[stage], phase, p.timeout_ns, abort_flag);
                 if (!__all_sync(FULLMASK, got)) {
                     if (lane == 0)
                         record_timeout(p, abort_flag);
                     ok = false;
                     break;
                 }
-                const int nk = min(4, p.k64 - 4 * kb);
-                const uint8_t *sSFA = smem + stage * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
-                const uint8_t *sSFB = sSFA + C::SFA_BYTES;
-                uint8_t *src = stg + slot * C::STG_BYTES;
-                // every atom of the stage is read before any is written, so
-                // the shared-memory loads overlap; atoms past nk (a K tail)
-                // hold stale bytes that no copy or MMA uses
-                uint4 va[4], vb[4 * C::NB];
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    va[kk] = *reinterpret_cast<const uint4 *>(sSFA + kk * 512 + lane * 16);
-#pragma unroll
-                    for (int h = 0; h < C::NB; ++h)
-                        vb[kk * C::NB + h] = *reinterpret_cast<const uint4 *>(sSFB + h * 2048 + kk * 512 + lane * 16);
-                }
-                uint8_t *srcb = src + C::CPS_A * CP_SRC_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    // A: source kk / 2, K-core kk % 2
-                    spread_atom(va[kk], src + (kk >> 1) * CP_SRC_BYTES + (kk & 1) * KCORE_BYTES, lane);
-                    if (C::NB == 1) {
-                        spread_atom(vb[kk], srcb + (kk >> 1) * CP_SRC_BYTES + (kk & 1) * KCORE_BYTES, lane);
-                    } else {
-                        // B: source kk, K-core h = 128-row group h (rows 0-127 / 128-255)
-#pragma unroll
-                        for (int h = 0; h < C::NB; ++h)
-                            spread_atom(vb[kk * C::NB + h], srcb + kk * CP_SRC_BYTES + h * KCORE_BYTES, lane);
-                    }
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
                 if (lane == 0) {
+                    // atoms of B row groups past the weight rows hold stale
+                    // bytes; they only feed output columns that are never stored
+                    const int nk = min(4, p.k64 - 4 * kb);
+                    const uint8_t *sSFA = smem + stage * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
+                    const uint8_t *sSFB = sSFA + C::SFA_BYTES;
                     const uint32_t sf_col = tmem + C::SF_BASE + stage * C::SF_COLS;
-                    const int npairs = (nk + 1) >> 1;
-                    for (int q = 0; q < npairs; ++q)
-                        tc_cp_128x256b(sf_col + 8 * q, smem_u32(src + q * CP_SRC_BYTES));
-                    if (C::NB == 1) {
-                        for (int q = 0; q < npairs; ++q)
-                            tc_cp_128x256b(sf_col + 16 + 8 * q, smem_u32(srcb + q * CP_SRC_BYTES));
-                    } else {
-                        for (int kk = 0; kk < nk; ++kk)
-                            tc_cp_128x256b(sf_col + 16 + 8 * kk, smem_u32(srcb + kk * CP_SRC_BYTES));
+                    for (int kk = 0; kk < nk; ++kk) {
+                        tc_cp_32x128b_warpx4(sf_col + 4 * kk, sdesc_sf(smem_u32(sSFA + kk * 512)));
+                        if (C::NB == 1) {
+                            tc_cp_32x128b_warpx4(sf_col + 16 + 4 * kk, sdesc_sf(smem_u32(sSFB + kk * 512)));
+                        } else {
+#pragma unroll
+                            for (int h = 0; h < C::NB; ++h)
+                                tc_cp_32x128b_warpx4(sf_col + 16 + 8 * kk + 4 * h,
+                                                     sdesc_sf(smem_u32(sSFB + h * 2048 + kk * 512)));
+                        }
                     }
                     tc_commit(&sf_ready[stage]);
-                    tc_commit(&stg_done[slot]);
                 }
                 __syncwarp();
-                ++slot_uses[slot];
-                if (++slot == C::STG_SLOTS)
-                    slot = 0;
+                ++issued;
                 if (++stage == C::STAGES) {
                     stage = 0;
                     phase ^= 1u;
@@ -762,9 +694,16 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
         }
         // the copies this warp issued complete before TMEM is freed
         if (lane == 0) {
-            for (int b = 0; b < C::STG_SLOTS; ++b)
-                if (slot_uses[b] > 0)
-                    mbar_wait(&stg_done[b], (uint32_t)((slot_uses[b] - 1) & 1), p.timeout_ns, nullptr);
+            const int n = min(issued, C::STAGES);
+            int s_ = stage;
+            uint32_t ph = phase;
+            for (int q = 0; q < n; ++q) {
+                if (--s_ < 0) {
+                    s_ = C::STAGES - 1;
+                    ph ^= 1u;
+                }
+                mbar_wait(&sf_ready[s_], ph, p.timeout_ns, nullptr);
+            }
         }
         __syncwarp();
     } else {

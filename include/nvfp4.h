@@ -128,10 +128,10 @@ nvfp4_status nvfp4_scale_bytes(int64_t rows, int64_t K, int32_t layout, size_t *
 nvfp4_status nvfp4_workspace_size(int32_t op, int64_t M, int64_t N, int64_t K, int32_t E,
                                   size_t *bytes);
 
-/* Zeroes a workspace (status word and the stream-K accumulator, which the
+/* Zeroes a workspace (status word and the stream-K ready flags, which the
  * GEMM kernels leave zeroed after every call) on `stream`.  Call once after
  * allocating it, and again after a TIMEOUT status (an aborted kernel may leave
- * partial sums behind).  The status word stays sticky between calls.
+ * flags raised).  The status word stays sticky between calls.
  * `ws` must be 256-byte aligned. */
 nvfp4_status nvfp4_workspace_init(void *ws, size_t ws_bytes, nvfp4_stream_t stream);
 
@@ -226,11 +226,11 @@ nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor *a, const int32_t *row_idx,
  * W4A4 kernel with its scratch moved into the library.
  *  - Takes no workspace and allocates nothing (no cudaMalloc, no cudaFree, no
  *    allocating library call).  Its scratch (status word, stream-K FP32
- *    accumulator and per-tile counters) is a fixed 4 MiB array inside the
+ *    partial tiles and ready flags) is a fixed 4 MiB array inside the
  *    library, which every GPU that loads the library holds until exit.
- *  - A shape whose scratch would exceed 4 MiB (narrow shapes that use
- *    stream-K, needing about 4*M*N bytes) is rejected with
- *    NVFP4_ERR_WORKSPACE before anything is enqueued.
+ *  - A shape whose scratch would exceed 4 MiB (M <= 128 shapes that use
+ *    stream-K need about 1 KiB * M per SM for their partial tiles) is
+ *    rejected with NVFP4_ERR_WORKSPACE before anything is enqueued.
  *  - The first call on a device looks up the array's device address for that
  *    device (with that device current); make that first call before any
  *    stream capture.

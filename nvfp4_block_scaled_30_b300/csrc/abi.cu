@@ -71,8 +71,8 @@ struct WsLayout {
     size_t a_second = 0;  // float (tensor mode) or binary16 [M][K/256] (macro)
     size_t a_fp8 = 0;     // on-the-fly FP8 activations (W4A8 route)
     size_t a_st = 0;
-    size_t acc = 0;       // stream-K FP32 accumulator [M][N], kept zero between calls
-    size_t tile_cnt = 0;  // stream-K per-tile stage counters, kept zero between calls
+    size_t sk_slots = 0;  // stream-K FP32 partial tiles, one per CTA
+    size_t sk_flags = 0;  // stream-K ready flags, one per CTA, kept zero between calls
     size_t total = 0;
 };
 
@@ -98,8 +98,11 @@ static WsLayout ws_layout(int op, int64_t M, int64_t N, int64_t K)
         L.a_st = take((size_t)(M * 4));
     }
     if (op == NVFP4_OP_GEMM && M <= SPLITK_MAX_M) {
-        L.acc = take((size_t)(M * N * 4));
-        L.tile_cnt = take((size_t)(ceil_div(M, 16) * ceil_div(N, 16) * 4));
+        const StreamKPlan pl = w4a4_streamk_plan(M, N, K, device_sm_count());
+        if (pl.used) {
+            L.sk_slots = take(pl.slot_bytes);
+            L.sk_flags = take(pl.flag_bytes);
+        }
     }
     L.total = off;
     return L;
@@ -147,12 +150,6 @@ static nvfp4_status from_cuda(cudaError_t e)
 
 // Stream-K pays off when whole tiles fill the SMs poorly (wave efficiency
 // below 90%) and there are enough K stages to spread.
-static bool use_streamk(int64_t tiles, int64_t kstages, int sms)
-{
-    const double eff = (double)tiles / (double)(ceil_div(tiles, sms) * sms);
-    return eff < 0.9 && tiles * kstages >= 2 * (int64_t)sms;
-}
-
 // W4A4 dense product of NVFP4 activations `a` ([M, K], tiled scales, tensor
 // mode) and weights `w` ([N, K]) into y.
 static nvfp4_status run_w4a4_dense(const uint8_t *a_codes, const uint8_t *a_scales, const float *a_second,
@@ -172,27 +169,19 @@ static nvfp4_status run_w4a4_dense(const uint8_t *a_codes, const uint8_t *a_scal
     g.K = K;
     g.status = status_word(ws);
     g.timeout_ns = DEFAULT_TIMEOUT_NS;
-    const int bn = w4a4_dense_bn(g.b_rows);
-    const int64_t tiles = ceil_div(g.a_rows, 128) * ceil_div(g.b_rows, bn);
-    const bool sk = L.acc != 0 && use_streamk(tiles, ceil_div(K / 64, 4), device_sm_count());
-    g.streamk = sk;
-    if (!sk) {
-        g.out = y;
-        g.out_dtype = y_dtype;
-        g.ld_i = ldy;
-        g.ld_j = 1;
-        return from_cuda(launch_w4a4_dense(g, stream));
-    }
-    // stream-K: partial tiles meet in the workspace accumulator; the kernel
-    // writes y itself and leaves the accumulator and counters zeroed
     g.out = y;
     g.out_dtype = y_dtype;
     g.ld_i = ldy;
     g.ld_j = 1;
-    g.acc = reinterpret_cast<float *>(ws_at(ws, L.acc));
-    g.acc_ld_i = N;
-    g.acc_ld_j = 1;
-    g.tile_cnt = reinterpret_cast<uint32_t *>(ws_at(ws, L.tile_cnt));
+    // stream-K when the plan (the same one that sized the workspace) says
+    // so: partial tiles meet in the workspace slots; the kernel writes y
+    // itself and leaves the flags zeroed
+    g.streamk = L.sk_slots != 0;
+    if (g.streamk) {
+        g.slots = reinterpret_cast<float *>(ws_at(ws, L.sk_slots));
+        g.flags = reinterpret_cast<uint32_t *>(ws_at(ws, L.sk_flags));
+    }
+    (void)N;
     return from_cuda(launch_w4a4_dense(g, stream));
 }
 

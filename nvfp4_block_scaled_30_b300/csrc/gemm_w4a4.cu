@@ -30,7 +30,12 @@
 //               engine, limits a stage.
 //   warps 3-10  epilogue: tcgen05.ld of the FP32 accumulator into registers,
 //               release of the accumulator, then alpha scale and BF16/FP32
-//               stores (or FP32 red.add of stream-K partial tiles).
+//               stores.  Stream-K partial tiles: a CTA whose range starts
+//               inside a tile parks its FP32 partial in its own workspace
+//               slot and raises its flag; the CTA holding the tile's first
+//               K stages (normally the last to finish it) adds the slots of
+//               the flagged contributors to its registers and stores the
+//               tile.
 // The dense launch is a programmatic dependent launch: set-up, tensor-map
 // fetch and the first weight stages' L2 prefetch overlap the previous grid
 // (normally the activation quantiser); every access to memory the previous
@@ -87,14 +92,13 @@ struct Params {
     const float *b_second; // [1] dense, [E] grouped
     void *out;
     int64_t ld_i, ld_j;
-    float *acc;              // stream-K: FP32 partial sums, acc[i*acc_ld_i + j*acc_ld_j], zero between calls
-    int64_t acc_ld_i, acc_ld_j;
-    uint32_t *tile_cnt;      // stream-K: K stages summed so far per tile, zero between calls
+    float *slots;            // stream-K: one FP32 partial tile [a_rows][BN] per CTA
+    uint32_t *flags;         // stream-K: one ready flag per CTA, zero between calls
     int64_t a_rows, b_rows; // valid extents (b_rows = N per expert in grouped mode)
+    int64_t slot_stride;    // stream-K: floats per partial slot (a_rows * BN)
     int32_t m_tiles, n_tiles, k64, kstages, streamk, group_m;
     int32_t out_dtype, vec_ok;
     int32_t b_row_tiles;    // 128-row scale atoms available in B (total)
-    int32_t pf_dist;        // L2 prefetch distance in stages (0: none)
     int32_t a_box_rows;     // rows of A one stage loads (128, or M rounded up to 16 when M < 128)
     // grouped mode
     const int64_t *offsets;
@@ -171,8 +175,8 @@ __device__ __forceinline__ void decode_grouped(const Params &p, const int *prefi
 // The sequence of work segments of one CTA, identical for all its roles.
 // Static mode: whole tiles blockIdx.x, blockIdx.x + gridDim.x, ...
 // Stream-K mode: the contiguous range [b*T/G, (b+1)*T/G) of the flattened
-// (tile, K-stage) space, cut at tile boundaries; partial tiles are summed
-// by FP32 red.add in the epilogue.
+// (tile, K-stage) space, cut at tile boundaries.  A CTA's range starts
+// inside at most one tile (its first), so one partial slot per CTA suffices.
 struct WorkIter {
     int64_t g, g_end;
     int item;
@@ -242,34 +246,36 @@ __device__ __forceinline__ void record_timeout(const Params &p, volatile int *ab
     atomicOr(p.status, ST_TIMEOUT);
 }
 
-__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d)
+__device__ __forceinline__ void st_release_gpu(uint32_t *addr, uint32_t v)
 {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *addr)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+    return v;
+}
+
+// Bounded wait for another CTA's ready flag (true once it reads non-zero).
+__device__ __forceinline__ bool wait_flag(const uint32_t *f, uint64_t timeout_ns, const volatile int *abort_flag)
+{
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire_gpu(f) == 0u) {
+        if (*abort_flag || globaltimer_ns() - t0 > timeout_ns)
+            return false;
+        __nanosleep(64);
+    }
+    return true;
 }
 
 template <int BN>
 __device__ __forceinline__ void store_chunk(const Params &p, const uint32_t (&v)[32], int64_t i, int64_t j0,
-                                            float alpha, int64_t i_end, int64_t j_end, bool partial)
+                                            float alpha, int64_t i_end, int64_t j_end)
 {
     if (i >= i_end)
         return;
-    if (partial) {
-        float *a = p.acc + i * p.acc_ld_i + j0 * p.acc_ld_j;
-        if (p.acc_ld_j == 1 && (p.acc_ld_i & 3) == 0 && j0 + 32 <= j_end) {
-#pragma unroll
-            for (int c = 0; c < 32; c += 4)
-                red_add_v4(a + c, alpha * __uint_as_float(v[c]), alpha * __uint_as_float(v[c + 1]),
-                           alpha * __uint_as_float(v[c + 2]), alpha * __uint_as_float(v[c + 3]));
-            return;
-        }
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-            if (j0 + c < j_end)
-                atomicAdd(a + c * p.acc_ld_j, alpha * __uint_as_float(v[c]));
-        }
-        return;
-    }
     if (p.ld_j == 1 && p.vec_ok && j0 + 32 <= j_end) {
         if (p.out_dtype == NVFP4_OUT_BF16) {
             uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + i * p.ld_i + j0);
@@ -322,7 +328,6 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
     uint64_t *drain = acc_empty + C::ACC_BUFS;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    volatile int *last_flag = abort_flag + 1;
     __shared__ int prefix[GROUPED ? MAX_EXPERTS + 1 : 1];
     __shared__ int total_items_s;
 
@@ -403,15 +408,6 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
         WorkIter wi;
         work_begin(p, total_items, wi);
         Tile t;
-        // L2 prefetch cursor, pf_dist stages ahead of the loads along this
-        // CTA's own work sequence: the tiles a stage reads are often first
-        // touched by several CTAs at once, and a prefetch issued earlier
-        // turns their HBM latency into an L2 hit without holding shared memory
-        WorkIter pw;
-        work_begin(p, total_items, pw);
-        Tile pt;
-        bool pf_live = work_next<GROUPED>(p, prefix, total_items, pw, pt);
-        int pkb = pf_live ? pt.kst0 : 0;
         // before waiting for the previous grid (programmatic dependent
         // launch): fetch the tensor maps and start the first weight stages
         // towards L2 (weights do not depend on the previous grid)
@@ -419,7 +415,10 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
             prefetch_tmap(&p.tmap_a);
             prefetch_tmap(&p.tmap_b);
         }
-        if (pf_live && lane < C::STAGES && pt.kst0 + lane < pt.kst1) {
+        WorkIter pw;
+        work_begin(p, total_items, pw);
+        Tile pt;
+        if (work_next<GROUPED>(p, prefix, total_items, pw, pt) && lane < C::STAGES && pt.kst0 + lane < pt.kst1) {
             const int kq = pt.kst0 + lane;
             const int brow = GROUPED ? pt.expert * (int)p.b_rows + pt.tile_n * BN : pt.tile_n * BN;
             tma_prefetch_2d(&p.tmap_b, kq * STAGE_K_BYTES, brow);
@@ -430,14 +429,6 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                                      min(4, p.k64 - 4 * kq) * 512);
         }
         pdl_wait();
-        auto pf_advance = [&]() {
-            if (pf_live && ++pkb >= pt.kst1) {
-                pf_live = work_next<GROUPED>(p, prefix, total_items, pw, pt);
-                pkb = pf_live ? pt.kst0 : 0;
-            }
-        };
-        for (int i = 0; i < p.pf_dist; ++i)
-            pf_advance();
         while (ok && work_next<GROUPED>(p, prefix, total_items, wi, t)) {
             // grouped: source activation row of tile rows lane + 32q
             int src_row[4] = {0, 0, 0, 0};
@@ -497,25 +488,6 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                                                  : p.sfb + ((size_t)(bt0 + op - 3) * p.k64 + 4 * kb) * 512;
                     bulk_load(op == 2 ? sSFA : sSFB + (op - 3) * 2048, src, nk * 512, &sf_full[stage]);
                 }
-                if (pf_live && p.pf_dist > 0) {
-                    // ops 5, 6, 7: L2 prefetch of stage pkb of tile pt
-                    const int pnk = min(4, p.k64 - 4 * pkb);
-                    if (op == 5 && !indexed) {
-                        tma_prefetch_2d(&p.tmap_a, pkb * STAGE_K_BYTES, GROUPED ? (int)pt.row0 : pt.tile_m * BM);
-                        if (!GROUPED)
-                            bulk_prefetch_l2(p.sfa + ((size_t)pt.tile_m * p.k64 + 4 * pkb) * 512, pnk * 512);
-                    } else if (op == 6) {
-                        tma_prefetch_2d(&p.tmap_b, pkb * STAGE_K_BYTES,
-                                        GROUPED ? pt.expert * (int)p.b_rows + pt.tile_n * BN : pt.tile_n * BN);
-                    } else if (op == 7) {
-                        const int pbt0 = (GROUPED ? pt.expert * (int)p.b_rows + pt.tile_n * BN : pt.tile_n * BN) / 128;
-#pragma unroll
-                        for (int h = 0; h < C::NB; ++h)
-                            if (pbt0 + h < p.b_row_tiles)
-                                bulk_prefetch_l2(p.sfb + ((size_t)(pbt0 + h) * p.k64 + 4 * pkb) * 512, pnk * 512);
-                    }
-                }
-                pf_advance();
                 if (GROUPED) {
                     if (indexed) {
                         // gathered code rows: 16-byte cp.async with the 128-byte
@@ -566,6 +538,9 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                 }
             }
         }
+        // every load is issued: the next grid in the stream may start its
+        // set-up (it waits for this grid's completion before touching memory)
+        pdl_trigger();
         // drain: wait (bounded) until every copy this warp issued has landed
         if (lane == 0) {
             const int n = min(issued, C::STAGES);
@@ -756,61 +731,142 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
             const int64_t j_base = (int64_t)t.tile_n * BN + cbase;
             const int64_t j_end = p.b_rows;
             const bool partial = !GROUPED && p.streamk && !(t.kst0 == 0 && t.kst1 == p.kstages);
+            if (partial && t.kst0 != 0) {
+                // contributor: this is the CTA's first tile and its range
+                // starts inside it; park the raw partial and raise the flag
+                float *slot = p.slots + (size_t)blockIdx.x * p.slot_stride + (size_t)row_in_tile * BN + cbase;
+                if (i < i_end) {
 #pragma unroll
-            for (int c = 0; c < NCH; ++c)
-                store_chunk<BN>(p, v[c], i, j_base + c * 32, alpha, i_end, j_end, partial);
-            if (partial) {
-                // the CTA whose stages complete the tile converts it and
-                // leaves the accumulator and the counter at zero again
+                    for (int c = 0; c < NCH; ++c)
+#pragma unroll
+                        for (int u = 0; u < 32; u += 4)
+                            __stcg(reinterpret_cast<float4 *>(slot + c * 32 + u),
+                                   make_float4(__uint_as_float(v[c][u]), __uint_as_float(v[c][u + 1]),
+                                               __uint_as_float(v[c][u + 2]), __uint_as_float(v[c][u + 3])));
+                }
                 epi_bar_sync();
                 if (threadIdx.x == 32 * EPI_FIRST_WARP) {
                     __threadfence();
-                    const uint32_t add = (uint32_t)(t.kst1 - t.kst0);
-                    const uint32_t old = atomicAdd(p.tile_cnt + t.tile, add);
-                    *last_flag = (old + add == (uint32_t)p.kstages) ? 1 : 0;
+                    st_release_gpu(p.flags + blockIdx.x, 1u);
                 }
-                epi_bar_sync();
-                if (*last_flag) {
-                    // column-parallel pass over the tile's valid rows: consecutive
-                    // threads take consecutive columns (coalesced), 4 loads in flight
-                    __threadfence();
-                    const int et = threadIdx.x - 32 * EPI_FIRST_WARP;
-                    const int64_t r0 = (int64_t)t.tile_m * BM;
-                    const int rows = (int)(p.a_rows - r0 < BM ? p.a_rows - r0 : BM);
-                    const int64_t c0 = (int64_t)t.tile_n * BN;
-                    const int cols = (int)(p.b_rows - c0 < BN ? p.b_rows - c0 : BN);
-                    const int total = rows * BN;
-                    for (int base = et; base < total; base += 4 * 32 * EPI_WARPS) {
-                        float y[4];
-                        int64_t ai[4];
-                        bool ok4[4];
+                continue;
+            }
+            if (partial) {
+                // owner: it holds the tile's first K stages, and since its
+                // range ends inside the tile this is its last work item: every
+                // load and MMA of the CTA has completed, so the ring's shared
+                // memory is free.  The accumulator goes there (row stride
+                // BN + 4 floats), then all epilogue threads add the partials
+                // of the CTAs after this one whose ranges start inside the tile
+                // (they wait on nothing, so the bounded wait is normally
+                // already satisfied) and store the tile, coalesced.
+                constexpr int RS = BN + 4;
+                float *tile_s = reinterpret_cast<float *>(smem);
+                fence_proxy_async_smem(); // the ring was last written by TMA
+                if (i < i_end) {
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int idx = base + u * 32 * EPI_WARPS;
-                            const int r = idx / BN, c = idx - (idx / BN) * BN;
-                            ok4[u] = idx < total && c < cols;
-                            ai[u] = (r0 + r) * p.acc_ld_i + (c0 + c) * p.acc_ld_j;
-                            y[u] = ok4[u] ? __ldcg(p.acc + ai[u]) : 0.0f;
+                    for (int c = 0; c < NCH; ++c)
+#pragma unroll
+                        for (int u = 0; u < 32; u += 4)
+                            *reinterpret_cast<float4 *>(tile_s + row_in_tile * RS + cbase + c * 32 + u) =
+                                make_float4(__uint_as_float(v[c][u]), __uint_as_float(v[c][u + 1]),
+                                            __uint_as_float(v[c][u + 2]), __uint_as_float(v[c][u + 3]));
+                }
+                const int64_t T = (int64_t)total_items * p.kstages;
+                const int64_t tile_end = (int64_t)(t.tile + 1) * p.kstages;
+                int n_contrib = 0;
+                while (blockIdx.x + 1 + n_contrib < (int)gridDim.x &&
+                       (int64_t)(blockIdx.x + 1 + n_contrib) * T / gridDim.x < tile_end)
+                    ++n_contrib;
+                bool got = true;
+                if (threadIdx.x == 32 * EPI_FIRST_WARP)
+                    for (int c = 1; c <= n_contrib && got; ++c)
+                        got = wait_flag(p.flags + blockIdx.x + c, p.timeout_ns, abort_flag);
+                if (!epi_bar_all(got)) {
+                    if (threadIdx.x == 32 * EPI_FIRST_WARP)
+                        record_timeout(p, abort_flag);
+                    break;
+                }
+                const int et = threadIdx.x - 32 * EPI_FIRST_WARP;
+                const int rows = (int)(i_end < BM ? i_end : BM); // one M-tile: rows 0..a_rows-1
+                const int64_t c0 = (int64_t)t.tile_n * BN;
+                const int cols = (int)(j_end - c0 < BN ? j_end - c0 : BN);
+                // 4 consecutive columns per thread and position; UB positions
+                // per round with all their slot loads in flight together
+                constexpr int UB = 8;
+                constexpr int STEP = 4 * 32 * EPI_WARPS;
+                const int total4 = rows * BN;
+                for (int base = et * 4; base < total4; base += UB * STEP) {
+                    float4 acc4[UB];
+#pragma unroll
+                    for (int u = 0; u < UB; ++u) {
+                        const int e4 = base + u * STEP;
+                        const int r = e4 / BN, cc = e4 - r * BN;
+                        acc4[u] = e4 < total4 ? *reinterpret_cast<const float4 *>(tile_s + r * RS + cc)
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                    for (int c = 1; c <= n_contrib; ++c) {
+                        const float *slot = p.slots + (size_t)(blockIdx.x + c) * p.slot_stride;
+                        float4 w4[UB];
+#pragma unroll
+                        for (int u = 0; u < UB; ++u) {
+                            const int e4 = base + u * STEP;
+                            w4[u] = e4 < total4 ? __ldcg(reinterpret_cast<const float4 *>(slot + e4))
+                                                : make_float4(0.f, 0.f, 0.f, 0.f);
                         }
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            if (!ok4[u])
-                                continue;
-                            const int idx = base + u * 32 * EPI_WARPS;
-                            const int r = idx / BN, c = idx - (idx / BN) * BN;
-                            __stcg(p.acc + ai[u], 0.0f);
-                            const int64_t off = (r0 + r) * p.ld_i + (c0 + c) * p.ld_j;
-                            if (p.out_dtype == NVFP4_OUT_BF16)
-                                static_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(y[u]);
-                            else
-                                static_cast<float *>(p.out)[off] = y[u];
+                        for (int u = 0; u < UB; ++u) {
+                            acc4[u].x += w4[u].x;
+                            acc4[u].y += w4[u].y;
+                            acc4[u].z += w4[u].z;
+                            acc4[u].w += w4[u].w;
                         }
                     }
-                    epi_bar_sync();
-                    if (threadIdx.x == 32 * EPI_FIRST_WARP)
-                        p.tile_cnt[t.tile] = 0;
+#pragma unroll
+                    for (int u = 0; u < UB; ++u) {
+                        const int e4 = base + u * STEP;
+                        if (e4 >= total4)
+                            continue;
+                        const int r = e4 / BN, cc = e4 - r * BN;
+                        const float y4[4] = {alpha * acc4[u].x, alpha * acc4[u].y, alpha * acc4[u].z,
+                                             alpha * acc4[u].w};
+                        const int64_t row = r;
+                        if (p.vec_ok && cc + 4 <= cols) {
+                            if (p.out_dtype == NVFP4_OUT_BF16) {
+                                __nv_bfloat162 h0 = __floats2bfloat162_rn(y4[0], y4[1]);
+                                __nv_bfloat162 h1 = __floats2bfloat162_rn(y4[2], y4[3]);
+                                const uint2 w2 = make_uint2(*reinterpret_cast<uint32_t *>(&h0),
+                                                            *reinterpret_cast<uint32_t *>(&h1));
+                                *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.out) + row * p.ld_i + c0 +
+                                                           cc) = w2;
+                            } else {
+                                *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + row * p.ld_i + c0 + cc) =
+                                    make_float4(y4[0], y4[1], y4[2], y4[3]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                if (cc + q4 < cols) {
+                                    const int64_t off = row * p.ld_i + (c0 + cc + q4) * p.ld_j;
+                                    if (p.out_dtype == NVFP4_OUT_BF16)
+                                        static_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(y4[q4]);
+                                    else
+                                        static_cast<float *>(p.out)[off] = y4[q4];
+                                }
+                            }
+                        }
+                    }
                 }
+                // every thread has read the slots: clear the flags for the next call
+                epi_bar_sync();
+                if (threadIdx.x == 32 * EPI_FIRST_WARP)
+                    for (int c = 1; c <= n_contrib; ++c)
+                        p.flags[blockIdx.x + c] = 0u;
+                continue;
             }
+#pragma unroll
+            for (int c = 0; c < NCH; ++c)
+                store_chunk<BN>(p, v[c], i, j_base + c * 32, alpha, i_end, j_end);
         }
     }
 
@@ -855,15 +911,6 @@ int group_m_for(int64_t m_tiles, int64_t K)
     return (int)std::min<int64_t>(8, m_tiles);
 }
 
-// L2 prefetch distance in stages.  Measured on B300 (decode 8x28672x8192
-// and prefill 4096x8192x8192): prefetching 3 to 10 stages ahead was neutral
-// to 5% slower, since the copies themselves, not HBM latency, bound a
-// stage; the cursor stays for shapes where it pays, off by default.
-int pf_dist_for(int /*bn*/)
-{
-    return 0;
-}
-
 } // namespace
 
 // N-side tile width: 256 when N fills it (every weight tile starts on a scale
@@ -873,6 +920,25 @@ int w4a4_dense_bn(int64_t b_rows)
     if (b_rows <= 128 || (b_rows % 256 != 0 && b_rows < 1024))
         return 128;
     return 256;
+}
+
+StreamKPlan w4a4_streamk_plan(int64_t M, int64_t N, int64_t K, int sms)
+{
+    StreamKPlan pl;
+    if (M <= 0 || M > BM || N <= 0 || K <= 0 || sms <= 0)
+        return pl;
+    const int bn = w4a4_dense_bn(N);
+    const int64_t tiles = ceil_div(N, bn);
+    const int64_t kstages = ceil_div(ceil_div(K, 64), 4);
+    // whole tiles fill the SMs poorly and there is enough K to share
+    const double eff = (double)tiles / (double)(ceil_div(tiles, sms) * sms);
+    if (!(eff < 0.9 && tiles * kstages >= 2 * (int64_t)sms))
+        return pl;
+    pl.used = true;
+    pl.grid = (int)std::min<int64_t>(tiles * kstages, sms);
+    pl.slot_bytes = align_up((size_t)pl.grid * (size_t)M * (size_t)bn * 4, 256);
+    pl.flag_bytes = align_up((size_t)pl.grid * 4, 256);
+    return pl;
 }
 
 cudaError_t launch_w4a4_dense(const DenseGemmArgs &g, cudaStream_t stream)
@@ -913,10 +979,9 @@ cudaError_t launch_w4a4_dense(const DenseGemmArgs &g, cudaStream_t stream)
     p.a_rows = g.a_rows;
     p.b_rows = g.b_rows;
     p.out_dtype = g.out_dtype;
-    p.acc = g.acc;
-    p.acc_ld_i = g.acc_ld_i;
-    p.acc_ld_j = g.acc_ld_j;
-    p.tile_cnt = g.tile_cnt;
+    p.slots = g.slots;
+    p.flags = g.flags;
+    p.slot_stride = g.a_rows * bn;
     const int esz = g.out_dtype == NVFP4_OUT_BF16 ? 2 : 4;
     p.vec_ok = (g.ld_j == 1 && (g.ld_i * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(g.out) % 16) == 0) ? 1 : 0;
     p.b_row_tiles = (int)ceil_div(g.b_rows, 128);
@@ -925,7 +990,6 @@ cudaError_t launch_w4a4_dense(const DenseGemmArgs &g, cudaStream_t stream)
     p.E = 0;
     p.status = g.status;
     p.timeout_ns = g.timeout_ns;
-    p.pf_dist = pf_dist_for(bn);
     const int tiles = p.m_tiles * p.n_tiles;
     // stream-K: one CTA per SM over all (tile, stage) units
     const int grid_units = g.streamk ? (int)std::min<int64_t>((int64_t)tiles * kstages, sms) : tiles;
@@ -972,7 +1036,6 @@ cudaError_t launch_w4a4_grouped(const GroupedGemmArgs &g, cudaStream_t stream)
     p.total_rows = g.total_rows;
     p.status = g.status;
     p.timeout_ns = g.timeout_ns;
-    p.pf_dist = pf_dist_for(bn);
     // upper bound of items: every expert's rows in tiles of 128, plus one partial tile per expert
     const int64_t max_tiles = ceil_div(g.total_rows, BM) + g.E;
     const int total = (int)std::min<int64_t>(max_tiles * p.n_tiles, 1 << 30);

@@ -69,18 +69,27 @@ struct DenseGemmArgs {
     void *out;
     int64_t ld_i, ld_j;
     int out_dtype;           // 0 bf16, 1 fp32
-    // stream-K (spread K stages evenly over the SMs): partial tiles are summed
-    // into acc (FP32, index i*acc_ld_i + j*acc_ld_j) with per-tile stage
-    // counters; both are zero between calls and left zero by the kernel.
+    // stream-K (spread K stages evenly over the SMs, only when a_rows <= 128):
+    // slots holds one FP32 partial tile [a_rows][N tile] per CTA of the grid
+    // (streamk_slot_floats each) and flags one word per CTA; the flags are
+    // zero between calls and left zero by the kernel.
     bool streamk;
-    float *acc;
-    int64_t acc_ld_i, acc_ld_j;
-    uint32_t *tile_cnt;
+    float *slots;
+    uint32_t *flags;
     uint32_t *status;
     uint64_t timeout_ns;
 };
 cudaError_t launch_w4a4_dense(const DenseGemmArgs &g, cudaStream_t stream);
 int w4a4_dense_bn(int64_t b_rows);
+// Stream-K launch shape of the dense W4A4 GEMM: whether it is used, the grid
+// size, and the workspace it needs (partial slots, then flags).
+struct StreamKPlan {
+    bool used = false;
+    int grid = 0;
+    size_t slot_bytes = 0; // all slots, 256-aligned
+    size_t flag_bytes = 0; // all flags, 256-aligned
+};
+StreamKPlan w4a4_streamk_plan(int64_t M, int64_t N, int64_t K, int sms);
 
 struct GroupedGemmArgs {
     const uint8_t *a_codes;

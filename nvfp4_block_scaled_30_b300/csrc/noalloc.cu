@@ -19,7 +19,7 @@ namespace {
 
 // Scratch of the no-allocation entry point: every GPU that loads the library
 // holds these bytes until the process exits.  Layout: [0, 256) status word,
-// then the stream-K FP32 accumulator, then the per-tile counters.
+// then the stream-K partial slots (one FP32 tile per CTA), then the flags.
 constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(4) << 20;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 
@@ -93,17 +93,10 @@ extern "C" nvfp4_status nvfp4_gemm_w4a4_noalloc(const nvfp4_tensor *a_q, const n
     g.b_second = static_cast<const float *>(w->second);
     g.b_rows = N;
     g.K = K;
-    const int sms = device_sm_count();
-    const int bn = w4a4_dense_bn(g.b_rows);
-    const int64_t tiles = ceil_div(g.a_rows, 128) * ceil_div(g.b_rows, bn);
-    const int64_t kstages = ceil_div(K / 64, 4);
-    const double eff = (double)tiles / (double)(ceil_div(tiles, sms) * sms);
-    const bool streamk = M <= 128 && eff < 0.9 && tiles * kstages >= 2 * (int64_t)sms;
+    const StreamKPlan pl = w4a4_streamk_plan(M, N, K, device_sm_count());
 
     // scratch needed by this call; larger requests are rejected
-    const size_t acc_bytes = streamk ? align_up((size_t)(M * N * 4), 256) : 0;
-    const size_t cnt_bytes = streamk ? align_up((size_t)(tiles * 4), 256) : 0;
-    const size_t need = WS_HEADER + acc_bytes + cnt_bytes;
+    const size_t need = WS_HEADER + (pl.used ? pl.slot_bytes + pl.flag_bytes : 0);
     if (need > NOALLOC_SCRATCH_BYTES)
         return NVFP4_ERR_WORKSPACE;
 
@@ -111,23 +104,24 @@ extern "C" nvfp4_status nvfp4_gemm_w4a4_noalloc(const nvfp4_tensor *a_q, const n
     if (scratch_address(&scratch) != cudaSuccess)
         return NVFP4_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
-    // the array keeps the previous call's contents: zero the status word,
-    // the accumulator and the counters this call relies on
-    if (cudaMemsetAsync(scratch, 0, need, s) != cudaSuccess)
-        return NVFP4_ERR_CUDA;
+    // the array keeps the previous call's contents: zero the status word and
+    // the stream-K flags this call relies on (the partial slots are always
+    // written before they are read)
     uint8_t *base = static_cast<uint8_t *>(scratch);
+    if (cudaMemsetAsync(base, 0, WS_HEADER, s) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    if (pl.used && cudaMemsetAsync(base + WS_HEADER + pl.slot_bytes, 0, pl.flag_bytes, s) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
     g.status = reinterpret_cast<uint32_t *>(base);
     g.timeout_ns = NOALLOC_TIMEOUT_NS;
     g.out = y;
     g.out_dtype = y_dtype;
     g.ld_i = ldy;
     g.ld_j = 1;
-    g.streamk = streamk;
-    if (streamk) {
-        g.acc = reinterpret_cast<float *>(base + WS_HEADER);
-        g.acc_ld_i = N;
-        g.acc_ld_j = 1;
-        g.tile_cnt = reinterpret_cast<uint32_t *>(base + WS_HEADER + acc_bytes);
+    g.streamk = pl.used;
+    if (pl.used) {
+        g.slots = reinterpret_cast<float *>(base + WS_HEADER);
+        g.flags = reinterpret_cast<uint32_t *>(base + WS_HEADER + pl.slot_bytes);
     }
     const cudaError_t e = launch_w4a4_dense(g, s);
     if (e == cudaSuccess)

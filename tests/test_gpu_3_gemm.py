@@ -168,3 +168,31 @@ def test_output_row_stride_and_empty():
     assert (full[:, 256:] == 7.0).all()
     y = nv.gemm(w, x=torch.zeros((0, 512), dtype=torch.bfloat16, device="cuda"))
     assert y.shape == (0, 256)
+
+
+# Shapes that run stream-K (M <= 128 and whole N tiles fill the SMs poorly):
+# about 10 CTAs per tile (8, 4096, 8192), a ragged last N tile
+# (16, 2944, 8192), the 128-wide N tile (8, 896, 16384) and M = 33.  The
+# same call twice must give identical bits (flags cleared, slots reused).
+@pytest.mark.parametrize("M,N,K", [(8, 4096, 8192), (16, 2944, 8192), (8, 896, 16384), (33, 4096, 8192)])
+def test_streamk_shapes(M, N, K):
+    xb = synth.activations(9, 40, M, K, 0.01, 50.0)
+    wb = synth.weights(9, 41, N, K)
+    w, wc, ws, wg = quantize_gpu(wb)
+    work = nv.Workspace(nv.workspace_size(nv.OP_GEMM, M, N, K))
+    x = dev_bf16(xb)
+    y1 = y_np(nv.gemm(w, x=x, ws=work, out_dtype=nv.OUT_FP32))
+    y2 = y_np(nv.gemm(w, x=x, ws=work, out_dtype=nv.OUT_FP32))
+    assert work.status() == nv.OK
+    np.testing.assert_array_equal(y1, y2)
+    ref = oracle.gemm_w4a4(oracle.nvfp4_encode(xb), (wc, ws, wg[0]))
+    _check(y1, ref, f"stream-K {M}x{N}x{K}", False)
+
+
+def test_streamk_m128_sampled_rows(w_28672):
+    w, wq = w_28672
+    xb = synth.activations(2, 5, 128, 8192, 0.005, 100.0)
+    y = y_np(nv.gemm(w, x=dev_bf16(xb)))
+    rows = np.array([0, 1, 31, 32, 63, 64, 100, 127])
+    ref = oracle.gemm_w4a4(oracle.nvfp4_encode(xb), wq, rows=rows)
+    _check(y[rows], ref, "stream-K M=128")

@@ -41,7 +41,8 @@ def test_noalloc_matches_workspace_entry_point_twice(M, N, K):
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
-    # a narrow shape whose stream-K accumulator (4*M*N bytes) exceeds 4 MiB
+    # a narrow stream-K shape whose partial tiles (64 rows x 256 columns of
+    # FP32 per SM) exceed 4 MiB
     a_q, w = _operands(64, 28672, 2048, 50)
     y = torch.empty((64, 28672), dtype=torch.bfloat16, device="cuda")
     ad, wd = a_q.desc(), w.desc()

@@ -14,7 +14,9 @@ roofline fraction against the measured HBM bandwidth.  The prefill shape
 MoE grouped GEMM are measured in the same run under "workloads".
 
 Inputs are seeded synthetic data (synth/); weights rotate over 4 copies
-(528 MB > the 126 MB L2) so every step streams them from HBM.  Multi-GPU
+(528 MB > the 126 MB L2) so every step streams them from HBM.  Device-side
+numbers (value, roofline) time a CUDA-graph replay of the K steps with CUDA
+events on the launching stream; e2e times plain API calls with host copies.  Multi-GPU
 runs (torchrun) are independent replicas: each rank runs the same workload
 on its own GPU and `value` sums them (weak scaling).
 
@@ -39,6 +41,11 @@ import synth  # noqa: E402
 
 NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25     # dense tensor-core ratio of B300
 FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6400.0, 1800.0
+
+# DRAM bytes (read + write) per launch of the roofline kernel, from one ncu
+# capture of the current kernel (profiles/ holds the capture and command);
+# None until a capture of the current kernel exists.
+TRAFFIC = {"decode": None, "prefill": None}
 
 
 def peaks():
@@ -125,14 +132,29 @@ class Ctx:
         t.cuda.synchronize()
         return out
 
-    def time(self, fn, steps, warmup):
+    def time(self, fn, steps, warmup, graph=True):
         """Mean ms per call of fn(i) over `steps` calls after `warmup` calls,
-        CUDA events on the current stream."""
+        CUDA events on the stream the calls are launched on.  With graph=True
+        the `steps` calls are captured once into a CUDA graph and one replay
+        is timed (the launch path a serving loop uses: no host gaps between
+        kernels); graph=False times the calls as issued from Python."""
         t = self.torch
         for i in range(warmup):
             fn(i)
         t.cuda.synchronize()
         s, e = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+        if graph:
+            g = t.cuda.CUDAGraph()
+            with t.cuda.graph(g, capture_error_mode="relaxed"):
+                for i in range(steps):
+                    fn(warmup + i)
+            g.replay()  # one untimed replay
+            t.cuda.synchronize()
+            s.record()
+            g.replay()
+            e.record()
+            t.cuda.synchronize()
+            return s.elapsed_time(e) / steps
         s.record()
         for i in range(steps):
             fn(warmup + i)
@@ -183,7 +205,7 @@ def workload_decode(c, M, steps, warmup, rot=4, with_e2e=False, peaks_=None):
             nv.gemm(W[i % rot], x=xd.view(t.bfloat16), y=y, ws=work)
             hy.copy_(y.view(t.int16), non_blocking=True)
 
-        ems = c.time(e2e, steps, warmup)
+        ems = c.time(e2e, steps, warmup, graph=False)
         res["e2e"] = {"value": step_bytes / (ems * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ems,
                       "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": M * N * 2}
     del W
@@ -433,14 +455,14 @@ def main():
     if args.workload == "decode":
         ach = r["gemm_bytes"] / (r["gemm_ms"] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-                "traffic": None, "kernel": "w4a4_kernel<16> (stream-K, operands swapped)",
+                "traffic": TRAFFIC.get("decode"), "kernel": "w4a4_kernel<256,false> (stream-K over 148 CTAs)",
                 "peak_source": f"{peak_src} hbm_gbs"}
         cfg = {"workload": "decode_mlp_up: X[8,8192] bf16 -> NVFP4, W NVFP4[28672,8192], Y bf16",
                "global_batch": 8, "l2": "4 rotating weight copies (528 MB > 126 MB L2)"}
     elif args.workload == "prefill":
         ach = r["gemm_tflops"]
         roof = {"bound": "tensor", "achieved": ach, "peak": fp4_peak, "unit": "TFLOP/s", "frac": ach / fp4_peak,
-                "traffic": None, "kernel": "w4a4_kernel<256>",
+                "traffic": TRAFFIC.get("prefill"), "kernel": "w4a4_kernel<256,false>",
                 "peak_source": f"{peak_src} bf16_tflops x {NOMINAL_FP4_OVER_BF16:g} (nominal FP4/BF16)"}
         cfg = {"workload": "prefill_proj: X[4096,8192], W NVFP4[28672,8192]", "global_batch": 4096,
                "l2": "inputs larger than L2 (X 67 MB + 2 rotating W copies of 132 MB)"}

@@ -930,9 +930,13 @@ StreamKPlan w4a4_streamk_plan(int64_t M, int64_t N, int64_t K, int sms)
     const int bn = w4a4_dense_bn(N);
     const int64_t tiles = ceil_div(N, bn);
     const int64_t kstages = ceil_div(ceil_div(K, 64), 4);
-    // whole tiles fill the SMs poorly and there is enough K to share
-    const double eff = (double)tiles / (double)(ceil_div(tiles, sms) * sms);
-    if (!(eff < 0.9 && tiles * kstages >= 2 * (int64_t)sms))
+    // M <= 128 is bound by streaming the weights.  Measured on B300 (M = 8 to
+    // 128, K = 8192): 112 whole tiles of N = 28672 already keep HBM busy and
+    // beat stream-K at every M (its partial reduction only adds a tail),
+    // while 16 tiles (N = 4096) leave most SMs idle and stream-K is 1.5x
+    // faster.  So stream-K only when the tiles cover under 60% of the SMs
+    // and there is enough K to share.
+    if (!(tiles * 10 < 6 * (int64_t)sms && tiles * kstages >= 2 * (int64_t)sms))
         return pl;
     pl.used = true;
     pl.grid = (int)std::min<int64_t>(tiles * kstages, sms);

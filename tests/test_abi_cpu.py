@@ -61,8 +61,8 @@ def test_workspace_size(nv):
     q = nv.workspace_size(nv.OP_QUANTIZE, 4096, 0, 8192)
     g = nv.workspace_size(nv.OP_GEMM, 4096, 8192, 8192)
     assert q >= 256 + 4096 and g > 4096 * 4096  # on-the-fly codes fit
-    small = nv.workspace_size(nv.OP_GEMM, 16, 28672, 8192)
-    # stream-K: one FP32 partial tile (16 rows x 256 columns) per SM
+    small = nv.workspace_size(nv.OP_GEMM, 16, 4096, 8192)
+    # stream-K (16 N tiles): one FP32 partial tile (16 rows x 256 columns) per SM
     assert small >= 148 * 16 * 256 * 4
 
 

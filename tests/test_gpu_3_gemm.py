@@ -189,10 +189,11 @@ def test_streamk_shapes(M, N, K):
     _check(y1, ref, f"stream-K {M}x{N}x{K}", False)
 
 
-def test_streamk_m128_sampled_rows(w_28672):
-    w, wq = w_28672
+def test_streamk_m128_sampled_rows():
+    wb = synth.weights(9, 43, 4096, 8192)
+    w, wc, ws, wg = quantize_gpu(wb)
     xb = synth.activations(2, 5, 128, 8192, 0.005, 100.0)
     y = y_np(nv.gemm(w, x=dev_bf16(xb)))
     rows = np.array([0, 1, 31, 32, 63, 64, 100, 127])
-    ref = oracle.gemm_w4a4(oracle.nvfp4_encode(xb), wq, rows=rows)
+    ref = oracle.gemm_w4a4(oracle.nvfp4_encode(xb), (wc, ws, wg[0]), rows=rows)
     _check(y[rows], ref, "stream-K M=128")

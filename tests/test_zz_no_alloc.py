@@ -26,7 +26,7 @@ def _operands(M, N, K, seed):
     return a_q, w
 
 
-@pytest.mark.parametrize("M,N,K", [(8, 4096, 8192), (16, 28672, 8192), (200, 512, 1024)])
+@pytest.mark.parametrize("M,N,K", [(8, 4096, 8192), (16, 2944, 8192), (16, 28672, 8192), (200, 512, 1024)])
 def test_noalloc_matches_workspace_entry_point_twice(M, N, K):
     a_q, w = _operands(M, N, K, 40)
     y_ref = y_np(nv.gemm(w, a_q=a_q, out_dtype=nv.OUT_FP32))
@@ -41,10 +41,10 @@ def test_noalloc_matches_workspace_entry_point_twice(M, N, K):
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
-    # a narrow stream-K shape whose partial tiles (64 rows x 256 columns of
-    # FP32 per SM) exceed 4 MiB
-    a_q, w = _operands(64, 28672, 2048, 50)
-    y = torch.empty((64, 28672), dtype=torch.bfloat16, device="cuda")
+    # a narrow stream-K shape (16 N tiles) whose partial tiles (128 rows x
+    # 256 columns of FP32 per SM) exceed 4 MiB
+    a_q, w = _operands(128, 4096, 8192, 50)
+    y = torch.empty((128, 4096), dtype=torch.bfloat16, device="cuda")
     ad, wd = a_q.desc(), w.desc()
     st = nv.lib().nvfp4_gemm_w4a4_noalloc(ctypes.byref(ad), ctypes.byref(wd), y.data_ptr(), y.stride(0),
                                           nv.OUT_BF16, torch.cuda.current_stream().cuda_stream)

@@ -122,6 +122,30 @@ __device__ __forceinline__ void pdl_trigger()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Thread-block cluster: this CTA's rank, a full cluster barrier (every
+// thread of every CTA; release/acquire on shared::cluster), and a 32-bit
+// load from the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_dsmem_u32(const void *local, uint32_t rank)
+{
+    uint32_t remote, v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+    return v;
+}
+
 // Fetch a tensor map (kernel parameter) into the descriptor cache.
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
 {

@@ -17,7 +17,9 @@
 // Memory: each thread owns 8 consecutive BF16 values per 16-byte load and
 // keeps several loads in flight; a lane pair owns one 16-element block
 // (absmax by one shfl.xor); the pair writes 8 packed code bytes (one 32-bit
-// store each) and one scale byte.
+// store each) and one scale byte.  Activations of up to 262144 values take a
+// single-launch path on one thread-block cluster (amax exchanged through
+// distributed shared memory); larger tensors take two streaming passes.
 #include <cfloat>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -96,10 +98,80 @@ __device__ __forceinline__ size_t scale_offset(int64_t row, int64_t blk, int64_t
 // Loads in flight per thread in the streaming passes.
 constexpr int QU = 4;
 
+// Position (row, chunk) in a rows x cpr grid of 8-value chunks, advanced by
+// a fixed flat step without dividing: step = q * cpr + r with r < cpr.
+struct Cursor {
+    int64_t row, j;
+};
+
+__device__ __forceinline__ void cursor_advance(Cursor &c, int64_t q, int64_t r, int64_t cpr)
+{
+    c.j += r;
+    c.row += q;
+    if (c.j >= cpr) {
+        c.j -= cpr;
+        ++c.row;
+    }
+}
+
+__device__ __forceinline__ void bf16x8_of(const uint4 v, float (&f)[8])
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+__device__ __forceinline__ void absmax_bits(const uint4 v, uint32_t &m, uint32_t &bad)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = w[i] & 0x7FFFu, hi = (w[i] >> 16) & 0x7FFFu;
+        bad |= (lo >= 0x7F80u) | (hi >= 0x7F80u);
+        m = max(m, max(lo, hi));
+    }
+}
+
+// Zero scales of the tiled layout's padding rows rows..rows_pad: one 32-bit
+// word = one row's 4 scales of a 64-element chunk.
+__device__ __forceinline__ void zero_pad_scales(uint8_t *scales, int64_t rows, int64_t rows_pad, int64_t K,
+                                                int64_t first, int64_t stride)
+{
+    const int64_t k64 = K / 64;
+    const int64_t pad = (rows_pad - rows) * k64;
+    for (int64_t i = first; i < pad; i += stride) {
+        const int64_t row = rows + i / k64;
+        *reinterpret_cast<uint32_t *>(scales + scale_offset(row, (i - (i / k64) * k64) * 4, K, true)) = 0u;
+    }
+}
+
+// One 16-element block (a lane pair, both lanes live) of tensor-scale encode:
+// codes and scale of chunk (row, j) of f under second-level scale sg.
+template <bool TILED>
+__device__ __forceinline__ void encode_chunk(const float (&f)[8], bool real, int64_t row, int64_t j, int64_t K,
+                                             float sg, uint8_t *codes, uint8_t *scales)
+{
+    float am = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        am = fmaxf(am, fabsf(f[i]));
+    const float amb = fmaxf(am, __shfl_xor_sync(FULL, am, 1));
+    const uint32_t e = real ? block_scale_code(amb, sg) : 0u;
+    const float r = recip_step(__fmul_rn(e4m3_value(e), sg));
+    if (real) {
+        *reinterpret_cast<uint32_t *>(codes + row * (K / 2) + j * 4) = pack8(f, r);
+        if ((threadIdx.x & 1) == 0)
+            scales[scale_offset(row, j >> 1, K, TILED)] = (uint8_t)e;
+    }
+}
+
 // Pass 1: per-CTA maximum of |x| (as BF16 magnitude bits) and a non-finite
 // flag.  The rows x K/8 chunks of 8 values are one flat index space, so small
 // row counts still spread over many CTAs; each thread keeps QU 16-byte loads
-// in flight.
+// in flight and walks the index space with a cursor (no division per chunk).
 __global__ void __launch_bounds__(QT) amax_partial_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t K,
                                                           int64_t ldx, uint32_t *__restrict__ partial,
                                                           uint32_t *__restrict__ status)
@@ -111,29 +183,25 @@ __global__ void __launch_bounds__(QT) amax_partial_kernel(const uint16_t *__rest
     pdl_trigger();
     const int64_t cpr = K / 8;
     const int64_t total = rows * cpr;
+    const int64_t base0 = (int64_t)blockIdx.x * QT * QU + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * QT * QU;
+    Cursor cur{base0 / cpr, base0 % cpr};
+    const int64_t qs = QT / cpr, rs = QT % cpr, qi = stride / cpr, ri = stride % cpr;
     uint32_t m = 0, bad = 0;
-    for (int64_t base = (int64_t)blockIdx.x * QT * QU + threadIdx.x; base < total; base += stride) {
+    for (int64_t base = base0; base < total; base += stride) {
         uint4 v[QU];
+        Cursor c = cur;
 #pragma unroll
         for (int u = 0; u < QU; ++u) {
-            const int64_t idx = base + (int64_t)u * QT;
             v[u] = make_uint4(0, 0, 0, 0);
-            if (idx < total) {
-                const int64_t row = idx / cpr, j = idx - row * cpr;
-                v[u] = __ldg(reinterpret_cast<const uint4 *>(x + row * ldx + j * 8));
-            }
+            if (base + (int64_t)u * QT < total)
+                v[u] = __ldg(reinterpret_cast<const uint4 *>(x + c.row * ldx + c.j * 8));
+            cursor_advance(c, qs, rs, cpr);
         }
 #pragma unroll
-        for (int u = 0; u < QU; ++u) {
-            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t lo = w[i] & 0x7FFFu, hi = (w[i] >> 16) & 0x7FFFu;
-                bad |= (lo >= 0x7F80u) | (hi >= 0x7F80u);
-                m = max(m, max(lo, hi));
-            }
-        }
+        for (int u = 0; u < QU; ++u)
+            absmax_bits(v[u], m, bad);
+        cursor_advance(cur, qi, ri, cpr);
     }
     bad = __any_sync(FULL, bad);
     uint32_t bm = block_max_u32(m, red);
@@ -168,51 +236,106 @@ __global__ void __launch_bounds__(QT) nvfp4_encode_kernel(const uint16_t *__rest
 
     const int64_t cpr = K / 8;
     const int64_t total = rows * cpr;
+    const int64_t base0 = (int64_t)blockIdx.x * QT * QU + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * QT * QU;
+    Cursor cur{base0 / cpr, base0 % cpr};
+    const int64_t qs = QT / cpr, rs = QT % cpr, qi = stride / cpr, ri = stride % cpr;
     // the trip count follows the warp's first index, so every lane of a warp
     // runs the same iterations (the pair shuffle needs the whole warp)
-    for (int64_t base = (int64_t)blockIdx.x * QT * QU + threadIdx.x; base - (threadIdx.x & 31) < total;
-         base += stride) {
+    for (int64_t base = base0; base - (threadIdx.x & 31) < total; base += stride) {
         float f[QU][8];
+        Cursor c[QU];
+        c[0] = cur;
 #pragma unroll
         for (int u = 0; u < QU; ++u) {
-            const int64_t idx = base + (int64_t)u * QT;
+            if (u > 0) {
+                c[u] = c[u - 1];
+                cursor_advance(c[u], qs, rs, cpr);
+            }
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 f[u][i] = 0.0f;
-            if (idx < total) {
-                const int64_t row = idx / cpr, j = idx - row * cpr;
-                bf16x8(x + row * ldx + j * 8, f[u]);
-            }
+            if (base + (int64_t)u * QT < total)
+                bf16x8(x + c[u].row * ldx + c[u].j * 8, f[u]);
         }
 #pragma unroll
-        for (int u = 0; u < QU; ++u) {
-            const int64_t idx = base + (int64_t)u * QT;
-            const bool real = idx < total;
-            float am = 0.0f;
+        for (int u = 0; u < QU; ++u)
+            encode_chunk<TILED>(f[u], base + (int64_t)u * QT < total, c[u].row, c[u].j, K, sg, codes, scales);
+        cursor_advance(cur, qi, ri, cpr);
+    }
+    if (TILED)
+        zero_pad_scales(scales, rows, rows_pad, K, (int64_t)blockIdx.x * QT + threadIdx.x, (int64_t)gridDim.x * QT);
+}
+
+// Small activations (decode): one kernel on one thread-block cluster of FC
+// CTAs.  Each thread holds up to FQ chunks of x in registers; the CTAs reduce
+// their absolute maxima, exchange them through distributed shared memory
+// (one cluster barrier before and one after), and encode from the registers,
+// so x is read once and there is no second launch.
+constexpr int FC = 8;    // CTAs per cluster
+constexpr int FT = 512;  // threads per CTA
+constexpr int FQ = 8;    // chunks per thread
+constexpr int64_t FUSED_MAX_CHUNKS = (int64_t)FC * FT * FQ;
+
+template <bool TILED>
+__global__ void __launch_bounds__(FT) nvfp4_encode_small_kernel(const uint16_t *__restrict__ x, int64_t rows,
+                                                                int64_t rows_pad, int64_t K, int64_t ldx,
+                                                                uint8_t *__restrict__ codes,
+                                                                uint8_t *__restrict__ scales,
+                                                                float *__restrict__ sg_out,
+                                                                uint32_t *__restrict__ status)
+{
+    __shared__ uint32_t red[FT / 32];
+    __shared__ uint32_t cta_max, all_max;
+    pdl_wait(); // x may come from the previous grid
+    pdl_trigger();
+    const uint32_t rank = cluster_ctarank();
+    const int64_t cpr = K / 8;
+    const int64_t total = rows * cpr;
+    const int64_t first = (int64_t)rank * FT + threadIdx.x;
+    constexpr int64_t STEP = (int64_t)FC * FT;
+    uint4 v[FQ];
+    uint32_t m = 0, bad = 0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                am = fmaxf(am, fabsf(f[u][i]));
-            const float amb = fmaxf(am, __shfl_xor_sync(FULL, am, 1));
-            const uint32_t e = real ? block_scale_code(amb, sg) : 0u;
-            const float r = recip_step(__fmul_rn(e4m3_value(e), sg));
-            if (real) {
-                const int64_t row = idx / cpr, j = idx - row * cpr;
-                *reinterpret_cast<uint32_t *>(codes + row * (K / 2) + j * 4) = pack8(f[u], r);
-                if ((threadIdx.x & 1) == 0)
-                    scales[scale_offset(row, j >> 1, K, TILED)] = (uint8_t)e;
-            }
+    for (int k = 0; k < FQ; ++k) {
+        const int64_t idx = first + k * STEP;
+        v[k] = make_uint4(0, 0, 0, 0);
+        if (idx < total) {
+            const int64_t row = idx / cpr, j = idx - row * cpr;
+            v[k] = __ldg(reinterpret_cast<const uint4 *>(x + row * ldx + j * 8));
         }
+        absmax_bits(v[k], m, bad);
     }
-    if (TILED) {
-        // one 32-bit word = one padding row's 4 scales of a 64-element chunk
-        const int64_t k64 = K / 64;
-        const int64_t pad = (rows_pad - rows) * k64;
-        for (int64_t i = (int64_t)blockIdx.x * QT + threadIdx.x; i < pad; i += (int64_t)gridDim.x * QT) {
-            const int64_t row = rows + i / k64;
-            *reinterpret_cast<uint32_t *>(scales + scale_offset(row, (i - (i / k64) * k64) * 4, K, true)) = 0u;
-        }
+    if (__any_sync(FULL, bad) && (threadIdx.x & 31) == 0)
+        atomicOr(status, ST_NONFINITE);
+    const uint32_t bm = block_max_u32(m, red);
+    if (threadIdx.x == 0)
+        cta_max = bm;
+    cluster_sync_all();
+    if (threadIdx.x < 32) {
+        uint32_t g = threadIdx.x < FC ? ld_dsmem_u32(&cta_max, threadIdx.x) : 0u;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            g = max(g, __shfl_xor_sync(FULL, g, o));
+        if (threadIdx.x == 0)
+            all_max = g;
     }
+    cluster_sync_all(); // no CTA reads another's shared memory after this
+    const float amax = __uint_as_float(all_max << 16);
+    const float sg = __fdiv_rn(amax, 2688.0f);
+    if (rank == 0 && threadIdx.x == 0)
+        *sg_out = sg;
+#pragma unroll
+    for (int k = 0; k < FQ; ++k) {
+        const int64_t idx = first + k * STEP;
+        const bool real = idx < total;
+        const int64_t row = real ? idx / cpr : 0, j = real ? idx - row * cpr : 0;
+        float f[8];
+        bf16x8_of(v[k], f);
+        encode_chunk<TILED>(f, real, row, j, K, sg, codes, scales);
+    }
+    if (TILED)
+        zero_pad_scales(scales, rows, rows_pad, K, first, STEP);
 }
 
 // Macro mode: one warp covers 32 chunks = 256 elements = one macro group (K is
@@ -348,6 +471,28 @@ cudaError_t launch_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K, in
     if (rows_pad == 0)
         return cudaSuccess;
     const int grid2 = (int)std::min<int64_t>(rows_pad, (int64_t)sms * 8);
+    if (mode == NVFP4_SCALE_TENSOR_FP32 && rows * (K / 8) <= FUSED_MAX_CHUNKS) {
+        // small activations: one cluster, one launch
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(FC);
+        cfg.blockDim = dim3(FT);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = FC;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        float *sg = static_cast<float *>(second);
+        if (tiled)
+            return cudaLaunchKernelEx(&cfg, nvfp4_encode_small_kernel<true>, x, rows, rows_pad, K, ldx, codes, scales,
+                                      sg, status);
+        return cudaLaunchKernelEx(&cfg, nvfp4_encode_small_kernel<false>, x, rows, rows_pad, K, ldx, codes, scales, sg,
+                                  status);
+    }
     if (mode == NVFP4_SCALE_TENSOR_FP32) {
         // flat passes: enough CTAs for one sweep of QU loads per thread, at
         // most a few waves

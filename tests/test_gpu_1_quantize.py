@@ -155,3 +155,21 @@ def test_fp8_edge_cases():
         oa, ost = oracle.fp8_token_encode(bits)
         np.testing.assert_array_equal(host(st).view(np.uint32), ost.view(np.uint32), err_msg=name)
         np.testing.assert_array_equal(host(a), oa, err_msg=name)
+
+
+# Around the single-launch (one cluster, at most 32768 chunks of 8 values)
+# and two-pass paths, and two-pass shapes whose rows are shorter than a
+# CTA's stride (the index cursor wraps rows) or not a divisor of it.
+@pytest.mark.parametrize("shape", [(32, 8192), (33, 8192), (4, 16384), (5000, 64), (300, 1088), (7, 4160),
+                                   (4097, 128)])
+def test_path_boundaries_bit_exact(shape):
+    M, K = shape
+    assert_same(synth.activations(9, 70 + M, M, K, 0.01, 50.0))
+
+
+def test_nonfinite_input_two_pass_path():
+    bits = synth.activations(9, 6, 64, 8192, 0.0, 1.0)   # 65536 chunks: two passes
+    bits[63, 8191] = 0x7F80  # +inf in the very last element
+    ws = nv.Workspace(nv.workspace_size(nv.OP_QUANTIZE, 64, 0, 8192))
+    nv.quantize(dev_bf16(bits), ws=ws)
+    assert ws.status() == nv.ERR_NONFINITE_INPUT

@@ -154,7 +154,7 @@ static nvfp4_status from_cuda(cudaError_t e)
 // mode) and weights `w` ([N, K]) into y.
 static nvfp4_status run_w4a4_dense(const uint8_t *a_codes, const uint8_t *a_scales, const float *a_second,
                                    int64_t M, const nvfp4_tensor *w, void *y, int64_t ldy, int y_dtype, void *ws,
-                                   const WsLayout &L, cudaStream_t stream)
+                                   const WsLayout &L, bool after_quantiser, cudaStream_t stream)
 {
     const int64_t N = w->rows, K = w->K;
     DenseGemmArgs g{};
@@ -176,6 +176,7 @@ static nvfp4_status run_w4a4_dense(const uint8_t *a_codes, const uint8_t *a_scal
     // stream-K when the plan (the same one that sized the workspace) says
     // so: partial tiles meet in the workspace slots; the kernel writes y
     // itself and leaves the flags zeroed
+    g.b_early = after_quantiser;
     g.streamk = L.sk_slots != 0;
     if (g.streamk) {
         g.slots = reinterpret_cast<float *>(ws_at(ws, L.sk_slots));
@@ -416,7 +417,7 @@ nvfp4_status nvfp4_gemm(const void *x_bf16, int64_t ldx, const nvfp4_tensor *a_q
         void *sec = ws_at(ws, L.a_second);
         cudaError_t e = launch_nvfp4_quantize(static_cast<const uint16_t *>(x_bf16), M, K, ldx, c, sc, sec, w->mode,
                                               NVFP4_LAYOUT_MMA_TILED, reinterpret_cast<uint32_t *>(ws_at(ws, L.amax)),
-                                              status_word(ws), s);
+                                              status_word(ws), s, false);
         if (e != cudaSuccess)
             return NVFP4_ERR_CUDA;
         ac = c;
@@ -445,7 +446,8 @@ nvfp4_status nvfp4_gemm(const void *x_bf16, int64_t ldx, const nvfp4_tensor *a_q
         g.timeout_ns = DEFAULT_TIMEOUT_NS;
         return from_cuda(launch_w4a4_macro(g, s));
     }
-    return run_w4a4_dense(ac, as, static_cast<const float *>(asec), M, w, y, ldy, y_dtype, ws, L, s);
+    return run_w4a4_dense(ac, as, static_cast<const float *>(asec), M, w, y, ldy, y_dtype, ws, L, x_bf16 != nullptr,
+                          s);
 }
 
 nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor *a, const int32_t *row_idx, const int64_t *expert_offsets,

@@ -100,6 +100,7 @@ struct Params {
     int32_t out_dtype, vec_ok;
     int32_t b_row_tiles;    // 128-row scale atoms available in B (total)
     int32_t a_box_rows;     // rows of A one stage loads (128, or M rounded up to 16 when M < 128)
+    int32_t b_early;        // issue the first stages' B copies before waiting for the previous grid
     // grouped mode
     const int64_t *offsets;
     const int32_t *row_idx;
@@ -408,25 +409,65 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
         WorkIter wi;
         work_begin(p, total_items, wi);
         Tile t;
-        // before waiting for the previous grid (programmatic dependent
-        // launch): fetch the tensor maps and start the first weight stages
-        // towards L2 (weights do not depend on the previous grid)
+        // Copies of one stage (one per lane: copies issued by one thread
+        // are served one after another, copies from different threads
+        // overlap; lanes 8r..8r+4 serve stages r, r+4, ... so each thread has
+        // at most one copy of four consecutive stages outstanding).
+        // op 0: A codes, 1: B codes, 2: A scales, 3..3+NB-1: B scales.  Codes
+        // and scales land on separate barriers, so the scale warp starts on a
+        // stage's (small) scale copies while its codes are still in flight.
+        auto issue = [&](const Tile &tt, int kb, int st, int idx, bool expect, bool part_b, bool part_a) {
+            const int nk = min(4, p.k64 - 4 * kb);
+            uint8_t *sA = smem + st * C::STAGE_BYTES;
+            uint8_t *sB = sA + C::A_BYTES;
+            uint8_t *sSFA = sB + C::B_BYTES;
+            uint8_t *sSFB = sSFA + C::SFA_BYTES;
+            const int brow0 = GROUPED ? tt.expert * (int)p.b_rows + tt.tile_n * BN : tt.tile_n * BN;
+            const int bt0 = brow0 / 128;
+            if (expect) {
+                int nb_loaded = 0;
+#pragma unroll
+                for (int h = 0; h < C::NB; ++h)
+                    nb_loaded += (bt0 + h < p.b_row_tiles) ? 1 : 0;
+                const uint32_t code_bytes =
+                    C::B_BYTES + (indexed ? 0u : (uint32_t)p.a_box_rows * STAGE_K_BYTES);
+                const uint32_t sf_bytes = (nb_loaded + (GROUPED ? 0 : 1)) * nk * 512;
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&full[st], code_bytes);
+                else if (lane == 1)
+                    mbar_arrive_expect_tx(&sf_full[st], sf_bytes);
+                __syncwarp();
+            }
+            const int op = lane - 8 * (idx & 3);
+            if ((op == 1 && part_b) || (op == 0 && !indexed && part_a)) {
+                const int arow = GROUPED ? (int)tt.row0 : tt.tile_m * BM;
+                tma_load_2d(op == 0 ? sA : sB, op == 0 ? &p.tmap_a : &p.tmap_b, kb * STAGE_K_BYTES,
+                            op == 0 ? arow : brow0, &full[st]);
+            } else if ((op == 2 && !GROUPED && part_a) ||
+                       (op >= 3 && op < 3 + C::NB && bt0 + op - 3 < p.b_row_tiles && part_b)) {
+                const uint8_t *src = op == 2 ? p.sfa + ((size_t)tt.tile_m * p.k64 + 4 * kb) * 512
+                                             : p.sfb + ((size_t)(bt0 + op - 3) * p.k64 + 4 * kb) * 512;
+                bulk_load(op == 2 ? sSFA : sSFB + (op - 3) * 2048, src, nk * 512, &sf_full[st]);
+            }
+        };
+        // Before waiting for the previous grid (programmatic dependent
+        // launch): fetch the tensor maps.  When the previous grid is the
+        // activation quantiser of the same call (it signals only after its
+        // own wait, so every grid before it has completed and the weights
+        // are final), the weight copies of the first ring stages go out now
+        // as well; their activation copies follow the wait.
         if (lane == 0) {
             prefetch_tmap(&p.tmap_a);
             prefetch_tmap(&p.tmap_b);
         }
-        WorkIter pw;
-        work_begin(p, total_items, pw);
-        Tile pt;
-        if (work_next<GROUPED>(p, prefix, total_items, pw, pt) && lane < C::STAGES && pt.kst0 + lane < pt.kst1) {
-            const int kq = pt.kst0 + lane;
-            const int brow = GROUPED ? pt.expert * (int)p.b_rows + pt.tile_n * BN : pt.tile_n * BN;
-            tma_prefetch_2d(&p.tmap_b, kq * STAGE_K_BYTES, brow);
-#pragma unroll
-            for (int h = 0; h < C::NB; ++h)
-                if (brow / 128 + h < p.b_row_tiles)
-                    bulk_prefetch_l2(p.sfb + ((size_t)(brow / 128 + h) * p.k64 + 4 * kq) * 512,
-                                     min(4, p.k64 - 4 * kq) * 512);
+        int n_early = 0;
+        if (!GROUPED && p.b_early) {
+            WorkIter pw;
+            work_begin(p, total_items, pw);
+            Tile pt;
+            while (n_early < C::STAGES && work_next<GROUPED>(p, prefix, total_items, pw, pt))
+                for (int kb = pt.kst0; kb < pt.kst1 && n_early < C::STAGES; ++kb, ++n_early)
+                    issue(pt, kb, n_early, n_early, true, true, false);
         }
         pdl_wait();
         while (ok && work_next<GROUPED>(p, prefix, total_items, wi, t)) {
@@ -452,42 +493,13 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                     ok = false;
                     break;
                 }
+                // stages issued early (ring slots still fresh) already have
+                // their barriers armed and weight copies in flight
+                const bool early = issued < n_early;
+                issue(t, kb, stage, issued, !early, !early, true);
                 const int nk = min(4, p.k64 - 4 * kb);
                 uint8_t *sA = smem + stage * C::STAGE_BYTES;
-                uint8_t *sB = sA + C::A_BYTES;
-                uint8_t *sSFA = sB + C::B_BYTES;
-                uint8_t *sSFB = sSFA + C::SFA_BYTES;
-                const int brow0 = GROUPED ? t.expert * (int)p.b_rows + t.tile_n * BN : t.tile_n * BN;
-                const int bt0 = brow0 / 128;
-                int nb_loaded = 0;
-#pragma unroll
-                for (int h = 0; h < C::NB; ++h)
-                    nb_loaded += (bt0 + h < p.b_row_tiles) ? 1 : 0;
-                // codes and scales land on separate barriers, so the scale
-                // warp starts on a stage's (small) scale copies while its
-                // codes are still in flight
-                const uint32_t code_bytes = C::B_BYTES + (indexed ? 0u : (uint32_t)p.a_box_rows * STAGE_K_BYTES);
-                const uint32_t sf_bytes = (nb_loaded + (GROUPED ? 0 : 1)) * nk * 512;
-                if (lane == 0)
-                    mbar_arrive_expect_tx(&full[stage], code_bytes);
-                else if (lane == 1)
-                    mbar_arrive_expect_tx(&sf_full[stage], sf_bytes);
-                __syncwarp();
-                // One copy per lane: copies issued by one thread are served
-                // one after another, copies from different threads overlap.
-                // Lanes 8r..8r+4 serve stages r, r+4, ... so each thread has
-                // at most one copy of four consecutive stages outstanding.
-                // op 0: A codes, 1: B codes, 2: A scales, 3..3+NB-1: B scales
-                const int op = lane - 8 * (issued & 3);
-                if (op == 1 || (op == 0 && !indexed)) {
-                    const int arow = GROUPED ? (int)t.row0 : t.tile_m * BM;
-                    tma_load_2d(op == 0 ? sA : sB, op == 0 ? &p.tmap_a : &p.tmap_b, kb * STAGE_K_BYTES,
-                                op == 0 ? arow : brow0, &full[stage]);
-                } else if ((op == 2 && !GROUPED) || (op >= 3 && op < 3 + C::NB && bt0 + op - 3 < p.b_row_tiles)) {
-                    const uint8_t *src = op == 2 ? p.sfa + ((size_t)t.tile_m * p.k64 + 4 * kb) * 512
-                                                 : p.sfb + ((size_t)(bt0 + op - 3) * p.k64 + 4 * kb) * 512;
-                    bulk_load(op == 2 ? sSFA : sSFB + (op - 3) * 2048, src, nk * 512, &sf_full[stage]);
-                }
+                uint8_t *sSFA = sA + C::A_BYTES + C::B_BYTES;
                 if (GROUPED) {
                     if (indexed) {
                         // gathered code rows: 16-byte cp.async with the 128-byte
@@ -983,6 +995,7 @@ cudaError_t launch_w4a4_dense(const DenseGemmArgs &g, cudaStream_t stream)
     p.a_rows = g.a_rows;
     p.b_rows = g.b_rows;
     p.out_dtype = g.out_dtype;
+    p.b_early = g.b_early ? 1 : 0;
     p.slots = g.slots;
     p.flags = g.flags;
     p.slot_stride = g.a_rows * bn;

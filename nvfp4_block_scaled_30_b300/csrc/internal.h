@@ -44,9 +44,12 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), int grid, int block, size_t smem,
 }
 
 // ---- quantisers (quantize.cu) ------------------------------------------------
+// zero_pad: also zero the scales of the tiled layout's padding rows (the
+// public quantiser promises them; the GEMM never reads them into stored
+// output, and its workspace keeps them zero from initialisation).
 cudaError_t launch_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx, uint8_t *codes,
                                   uint8_t *scales, void *second, int mode, int layout, uint32_t *amax_partial,
-                                  uint32_t *status, cudaStream_t stream);
+                                  uint32_t *status, cudaStream_t stream, bool zero_pad = true);
 cudaError_t launch_fp8_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx, uint8_t *a, float *s_t,
                                 uint32_t *status, cudaStream_t stream);
 cudaError_t launch_probe_convert(const float *in, int64_t n, uint8_t *o2, uint8_t *o3, cudaStream_t stream);
@@ -76,6 +79,9 @@ struct DenseGemmArgs {
     bool streamk;
     float *slots;
     uint32_t *flags;
+    // the previous grid in the stream is this call's activation quantiser:
+    // the first stages' weight copies may start before waiting for it
+    bool b_early;
     uint32_t *status;
     uint64_t timeout_ns;
 };

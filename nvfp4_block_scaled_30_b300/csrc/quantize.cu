@@ -140,11 +140,15 @@ __device__ __forceinline__ void absmax_bits(const uint4 v, uint32_t &m, uint32_t
 __device__ __forceinline__ void zero_pad_scales(uint8_t *scales, int64_t rows, int64_t rows_pad, int64_t K,
                                                 int64_t first, int64_t stride)
 {
-    const int64_t k64 = K / 64;
-    const int64_t pad = (rows_pad - rows) * k64;
-    for (int64_t i = first; i < pad; i += stride) {
-        const int64_t row = rows + i / k64;
-        *reinterpret_cast<uint32_t *>(scales + scale_offset(row, (i - (i / k64) * k64) * 4, K, true)) = 0u;
+    // fewer than 128 padding rows: 32-bit index arithmetic suffices
+    const uint32_t k64 = (uint32_t)(K / 64);
+    const uint32_t pad = (uint32_t)(rows_pad - rows) * k64;
+    const int64_t tile0 = rows >> 7; // the padding rows all lie in the last 128-row tile
+    for (int64_t i = first; i < (int64_t)pad; i += stride) {
+        const uint32_t q = (uint32_t)i / k64, c = (uint32_t)i - q * k64;
+        const uint32_t r = (uint32_t)(rows & 127) + q;
+        const size_t off = ((size_t)tile0 * k64 + c) * 512 + (r & 31) * 16 + (r >> 5) * 4;
+        *reinterpret_cast<uint32_t *>(scales + off) = 0u;
     }
 }
 
@@ -221,7 +225,8 @@ __global__ void __launch_bounds__(QT) nvfp4_encode_kernel(const uint16_t *__rest
                                                           int64_t rows_pad, int64_t K, int64_t ldx,
                                                           uint8_t *__restrict__ codes, uint8_t *__restrict__ scales,
                                                           float *__restrict__ sg_out,
-                                                          const uint32_t *__restrict__ partial, int n_partial)
+                                                          const uint32_t *__restrict__ partial, int n_partial,
+                                                          int zero_pad)
 {
     __shared__ uint32_t red[QT / 32];
     pdl_wait(); // the partial maxima of pass 1
@@ -263,15 +268,15 @@ __global__ void __launch_bounds__(QT) nvfp4_encode_kernel(const uint16_t *__rest
             encode_chunk<TILED>(f[u], base + (int64_t)u * QT < total, c[u].row, c[u].j, K, sg, codes, scales);
         cursor_advance(cur, qi, ri, cpr);
     }
-    if (TILED)
+    if (TILED && zero_pad)
         zero_pad_scales(scales, rows, rows_pad, K, (int64_t)blockIdx.x * QT + threadIdx.x, (int64_t)gridDim.x * QT);
 }
 
 // Small activations (decode): one kernel on one thread-block cluster of FC
-// CTAs.  Each thread holds up to FQ chunks of x in registers; the CTAs reduce
-// their absolute maxima, exchange them through distributed shared memory
-// (one cluster barrier before and one after), and encode from the registers,
-// so x is read once and there is no second launch.
+// CTAs.  Each thread holds up to FQ chunks of x in registers (a warp stops at
+// its last real chunk); every CTA pushes its absolute maximum into all CTAs'
+// shared memory, one cluster barrier publishes them, and each CTA encodes
+// from its registers, so x is read once and there is no second launch.
 constexpr int FC = 8;    // CTAs per cluster
 constexpr int FT = 512;  // threads per CTA
 constexpr int FQ = 8;    // chunks per thread
@@ -283,58 +288,73 @@ __global__ void __launch_bounds__(FT) nvfp4_encode_small_kernel(const uint16_t *
                                                                 uint8_t *__restrict__ codes,
                                                                 uint8_t *__restrict__ scales,
                                                                 float *__restrict__ sg_out,
-                                                                uint32_t *__restrict__ status)
+                                                                uint32_t *__restrict__ status, int zero_pad)
 {
     __shared__ uint32_t red[FT / 32];
-    __shared__ uint32_t cta_max, all_max;
+    __shared__ uint32_t cta_max[FC];
+    // this CTA is running: peers may write its shared memory once they have
+    // waited on this phase
+    cluster_arrive_relaxed();
     pdl_wait(); // x may come from the previous grid
     pdl_trigger();
     const uint32_t rank = cluster_ctarank();
-    const int64_t cpr = K / 8;
-    const int64_t total = rows * cpr;
-    const int64_t first = (int64_t)rank * FT + threadIdx.x;
-    constexpr int64_t STEP = (int64_t)FC * FT;
+    const int cpr = (int)(K / 8);
+    const int total = (int)(rows * (K / 8)); // at most FUSED_MAX_CHUNKS
+    const int first = (int)rank * FT + (int)threadIdx.x;
+    const int wfirst = first - (int)(threadIdx.x & 31);
+    constexpr int STEP = FC * FT;
     uint4 v[FQ];
     uint32_t m = 0, bad = 0;
 #pragma unroll
     for (int k = 0; k < FQ; ++k) {
-        const int64_t idx = first + k * STEP;
         v[k] = make_uint4(0, 0, 0, 0);
+        const int idx = first + k * STEP;
         if (idx < total) {
-            const int64_t row = idx / cpr, j = idx - row * cpr;
-            v[k] = __ldg(reinterpret_cast<const uint4 *>(x + row * ldx + j * 8));
+            const int row = idx / cpr, j = idx - row * cpr;
+            v[k] = __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)row * ldx + j * 8));
         }
-        absmax_bits(v[k], m, bad);
     }
+#pragma unroll
+    for (int k = 0; k < FQ; ++k)
+        absmax_bits(v[k], m, bad);
     if (__any_sync(FULL, bad) && (threadIdx.x & 31) == 0)
         atomicOr(status, ST_NONFINITE);
-    const uint32_t bm = block_max_u32(m, red);
-    if (threadIdx.x == 0)
-        cta_max = bm;
-    cluster_sync_all();
-    if (threadIdx.x < 32) {
-        uint32_t g = threadIdx.x < FC ? ld_dsmem_u32(&cta_max, threadIdx.x) : 0u;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            g = max(g, __shfl_xor_sync(FULL, g, o));
-        if (threadIdx.x == 0)
-            all_max = g;
+    for (int o = 16; o > 0; o >>= 1)
+        m = max(m, __shfl_xor_sync(FULL, m, o));
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    cluster_wait(); // every CTA of the cluster is running
+    if (threadIdx.x < FC) {
+        // this CTA's maximum into slot `rank` of every CTA of the cluster
+        uint32_t bb = red[0];
+#pragma unroll
+        for (int w = 1; w < FT / 32; ++w)
+            bb = max(bb, red[w]);
+        st_dsmem_u32(&cta_max[rank], threadIdx.x, bb);
     }
-    cluster_sync_all(); // no CTA reads another's shared memory after this
-    const float amax = __uint_as_float(all_max << 16);
+    cluster_sync_all(); // all maxima are in every CTA; no remote access follows
+    uint32_t g = 0;
+#pragma unroll
+    for (int c = 0; c < FC; ++c)
+        g = max(g, cta_max[c]);
+    const float amax = __uint_as_float(g << 16);
     const float sg = __fdiv_rn(amax, 2688.0f);
     if (rank == 0 && threadIdx.x == 0)
         *sg_out = sg;
 #pragma unroll
     for (int k = 0; k < FQ; ++k) {
-        const int64_t idx = first + k * STEP;
+        if (wfirst + k * STEP >= total) // warp-uniform: nothing left for this warp
+            break;
+        const int idx = first + k * STEP;
         const bool real = idx < total;
-        const int64_t row = real ? idx / cpr : 0, j = real ? idx - row * cpr : 0;
+        const int row = real ? idx / cpr : 0, j = real ? idx - row * cpr : 0;
         float f[8];
         bf16x8_of(v[k], f);
         encode_chunk<TILED>(f, real, row, j, K, sg, codes, scales);
     }
-    if (TILED)
+    if (TILED && zero_pad)
         zero_pad_scales(scales, rows, rows_pad, K, first, STEP);
 }
 
@@ -463,8 +483,9 @@ __global__ void finalize_bf16_kernel(const float *__restrict__ acc, int64_t rows
 
 cudaError_t launch_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx, uint8_t *codes,
                                   uint8_t *scales, void *second, int mode, int layout, uint32_t *amax_partial,
-                                  uint32_t *status, cudaStream_t stream)
+                                  uint32_t *status, cudaStream_t stream, bool zero_pad)
 {
+    const int zp = zero_pad ? 1 : 0;
     const bool tiled = layout == NVFP4_LAYOUT_MMA_TILED;
     const int64_t rows_pad = tiled ? ceil_div(rows, 128) * 128 : rows;
     const int sms = device_sm_count();
@@ -489,9 +510,9 @@ cudaError_t launch_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K, in
         float *sg = static_cast<float *>(second);
         if (tiled)
             return cudaLaunchKernelEx(&cfg, nvfp4_encode_small_kernel<true>, x, rows, rows_pad, K, ldx, codes, scales,
-                                      sg, status);
+                                      sg, status, zp);
         return cudaLaunchKernelEx(&cfg, nvfp4_encode_small_kernel<false>, x, rows, rows_pad, K, ldx, codes, scales, sg,
-                                  status);
+                                  status, zp);
     }
     if (mode == NVFP4_SCALE_TENSOR_FP32) {
         // flat passes: enough CTAs for one sweep of QU loads per thread, at
@@ -510,10 +531,10 @@ cudaError_t launch_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K, in
         const uint32_t *part = amax_partial;
         if (tiled)
             e = launch_pdl(nvfp4_encode_kernel<true>, grid_e, QT, 0, stream, x, rows, rows_pad, K, ldx, codes, scales,
-                           sg, part, grid1);
+                           sg, part, grid1, zp);
         else
             e = launch_pdl(nvfp4_encode_kernel<false>, grid_e, QT, 0, stream, x, rows, rows_pad, K, ldx, codes,
-                           scales, sg, part, grid1);
+                           scales, sg, part, grid1, zp);
         if (e != cudaSuccess)
             return e;
     } else {

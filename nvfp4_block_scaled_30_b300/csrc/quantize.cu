@@ -172,6 +172,54 @@ __device__ __forceinline__ void encode_chunk(const float (&f)[8], bool real, int
     }
 }
 
+// Blocks in flight per thread in the two-pass encode.
+constexpr int QB = 2;
+
+// Two IEEE round-to-nearest products at once (bit-identical to two
+// __fmul_rn).
+__device__ __forceinline__ void mul2_rn(float a0, float a1, float r, float &p0, float &p1)
+{
+    uint64_t a = (uint64_t)__float_as_uint(a0) | ((uint64_t)__float_as_uint(a1) << 32);
+    const uint64_t rr = (uint64_t)__float_as_uint(r) | ((uint64_t)__float_as_uint(r) << 32);
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(rr));
+    p0 = __uint_as_float((uint32_t)d);
+    p1 = __uint_as_float((uint32_t)(d >> 32));
+}
+
+// One whole 16-element block (16 BF16 values in lo, hi) by one thread: the
+// block maximum from the magnitude bits (exact, equal to the float maximum
+// of finite values), the same scale and code arithmetic as encode_chunk, and
+// one 8-byte code store plus one scale byte.
+template <bool TILED>
+__device__ __forceinline__ void encode_block16(const uint4 lo, const uint4 hi, int64_t row, int64_t blk, int64_t K,
+                                               float sg, uint8_t *codes, uint8_t *scales)
+{
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    uint32_t m2 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        m2 = __vmaxu2(m2, w[i] & 0x7FFF7FFFu);
+    const float amb = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
+    const uint32_t e = block_scale_code(amb, sg);
+    const float r = recip_step(__fmul_rn(e4m3_value(e), sg));
+    uint32_t pk[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t p = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t ww = w[4 * h + i];
+            float q0, q1;
+            mul2_rn(__uint_as_float(ww << 16), __uint_as_float(ww & 0xFFFF0000u), r, q0, q1);
+            p |= e2m1x2(q0, q1) << (8 * i);
+        }
+        pk[h] = p;
+    }
+    *reinterpret_cast<uint2 *>(codes + row * (K / 2) + blk * 8) = make_uint2(pk[0], pk[1]);
+    scales[scale_offset(row, blk, K, TILED)] = (uint8_t)e;
+}
+
 // Pass 1: per-CTA maximum of |x| (as BF16 magnitude bits) and a non-finite
 // flag.  The rows x K/8 chunks of 8 values are one flat index space, so small
 // row counts still spread over many CTAs; each thread keeps QU 16-byte loads
@@ -191,7 +239,7 @@ __global__ void __launch_bounds__(QT) amax_partial_kernel(const uint16_t *__rest
     const int64_t stride = (int64_t)gridDim.x * QT * QU;
     Cursor cur{base0 / cpr, base0 % cpr};
     const int64_t qs = QT / cpr, rs = QT % cpr, qi = stride / cpr, ri = stride % cpr;
-    uint32_t m = 0, bad = 0;
+    uint32_t m2 = 0, bad = 0; // m2: two 16-bit magnitude maxima
     for (int64_t base = base0; base < total; base += stride) {
         uint4 v[QU];
         Cursor c = cur;
@@ -203,11 +251,17 @@ __global__ void __launch_bounds__(QT) amax_partial_kernel(const uint16_t *__rest
             cursor_advance(c, qs, rs, cpr);
         }
 #pragma unroll
-        for (int u = 0; u < QU; ++u)
-            absmax_bits(v[u], m, bad);
+        for (int u = 0; u < QU; ++u) {
+            m2 = __vmaxu2(m2, v[u].x & 0x7FFF7FFFu);
+            m2 = __vmaxu2(m2, v[u].y & 0x7FFF7FFFu);
+            m2 = __vmaxu2(m2, v[u].z & 0x7FFF7FFFu);
+            m2 = __vmaxu2(m2, v[u].w & 0x7FFF7FFFu);
+        }
         cursor_advance(cur, qi, ri, cpr);
     }
-    bad = __any_sync(FULL, bad);
+    const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+    // a non-finite value has the largest magnitude bits (>= 0x7F80)
+    bad = __any_sync(FULL, m >= 0x7F80u);
     uint32_t bm = block_max_u32(m, red);
     if (threadIdx.x == 0)
         partial[blockIdx.x] = bm;
@@ -239,34 +293,38 @@ __global__ void __launch_bounds__(QT) nvfp4_encode_kernel(const uint16_t *__rest
     if (blockIdx.x == 0 && threadIdx.x == 0)
         *sg_out = sg;
 
-    const int64_t cpr = K / 8;
-    const int64_t total = rows * cpr;
-    const int64_t base0 = (int64_t)blockIdx.x * QT * QU + threadIdx.x;
-    const int64_t stride = (int64_t)gridDim.x * QT * QU;
-    Cursor cur{base0 / cpr, base0 % cpr};
-    const int64_t qs = QT / cpr, rs = QT % cpr, qi = stride / cpr, ri = stride % cpr;
-    // the trip count follows the warp's first index, so every lane of a warp
-    // runs the same iterations (the pair shuffle needs the whole warp)
-    for (int64_t base = base0; base - (threadIdx.x & 31) < total; base += stride) {
-        float f[QU][8];
-        Cursor c[QU];
+    // one thread per 16-element block (two 16-byte loads), QB blocks in
+    // flight per thread; blocks of all real rows form one flat index space
+    const int64_t bpr = K / 16;
+    const int64_t total = rows * bpr;
+    const int64_t base0 = (int64_t)blockIdx.x * QT * QB + threadIdx.x;
+    const int64_t stride = (int64_t)gridDim.x * QT * QB;
+    Cursor cur{base0 / bpr, base0 % bpr};
+    const int64_t qs = QT / bpr, rs = QT % bpr, qi = stride / bpr, ri = stride % bpr;
+    for (int64_t base = base0; base < total; base += stride) {
+        uint4 v[QB][2];
+        Cursor c[QB];
         c[0] = cur;
 #pragma unroll
-        for (int u = 0; u < QU; ++u) {
+        for (int u = 0; u < QB; ++u) {
             if (u > 0) {
                 c[u] = c[u - 1];
-                cursor_advance(c[u], qs, rs, cpr);
+                cursor_advance(c[u], qs, rs, bpr);
             }
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                f[u][i] = 0.0f;
-            if (base + (int64_t)u * QT < total)
-                bf16x8(x + c[u].row * ldx + c[u].j * 8, f[u]);
+            v[u][0] = v[u][1] = make_uint4(0, 0, 0, 0);
+            if (base + (int64_t)u * QT < total) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(x + c[u].row * ldx + c[u].j * 16);
+                v[u][0] = __ldg(src);
+                v[u][1] = __ldg(src + 1);
+            }
         }
 #pragma unroll
-        for (int u = 0; u < QU; ++u)
-            encode_chunk<TILED>(f[u], base + (int64_t)u * QT < total, c[u].row, c[u].j, K, sg, codes, scales);
-        cursor_advance(cur, qi, ri, cpr);
+        for (int u = 0; u < QB; ++u) {
+            if (base + (int64_t)u * QT >= total)
+                continue;
+            encode_block16<TILED>(v[u][0], v[u][1], c[u].row, c[u].j, K, sg, codes, scales);
+        }
+        cursor_advance(cur, qi, ri, bpr);
     }
     if (TILED && zero_pad)
         zero_pad_scales(scales, rows, rows_pad, K, (int64_t)blockIdx.x * QT + threadIdx.x, (int64_t)gridDim.x * QT);
@@ -521,8 +579,9 @@ cudaError_t launch_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K, in
         const int64_t per_cta = (int64_t)QT * QU;
         const int grid1 = (int)std::min<int64_t>(ceil_div(chunks, per_cta), std::min(AMAX_MAX_CTAS, sms * 4));
         const int64_t pad_words = tiled ? (rows_pad - rows) * (K / 64) : 0;
+        const int64_t blocks = std::max<int64_t>(rows * (K / 16), 1);
         const int grid_e = (int)std::max<int64_t>(
-            1, std::min<int64_t>(std::max(ceil_div(chunks, per_cta), ceil_div(pad_words, (int64_t)QT * 8)),
+            1, std::min<int64_t>(std::max(ceil_div(blocks, (int64_t)QT * QB), ceil_div(pad_words, (int64_t)QT * 8)),
                                  (int64_t)sms * 8));
         cudaError_t e = launch_pdl(amax_partial_kernel, grid1, QT, 0, stream, x, rows, K, ldx, amax_partial, status);
         if (e != cudaSuccess)

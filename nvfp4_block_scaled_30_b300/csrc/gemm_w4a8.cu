@@ -12,12 +12,17 @@
 // The block-scaled FP8 MMA kinds use power-of-two scales per 32 elements and
 // cannot carry the weights' E4M3 scales per 16 elements exactly.
 //
-// Pipeline (persistent, one CTA per SM, 320 threads):
-//   warp 0      TMA: raw FP8 A tile [128 x 64 B], raw FP4 W tile [BN x 32 B]
-//               and the W scale atom(s) per 64-element K step (raw ring)
-//   warp 1      TMEM alloc; lane 0 issues 4 x tcgen05.mma (K = 16) per step
-//   warps 2..5  converters: raw ring -> FP16 tiles (128-byte swizzled rows)
-//   warps 6..9  epilogue: TMEM -> registers, * s_t[m] * s_w, BF16/FP32 store
+// Pipeline (persistent, one CTA per SM, 576 threads, tile 128 x 256):
+//   warp 0      TMA: raw FP8 A tile [128 x 64 B], raw FP4 W tile [256 x 32 B]
+//               and the W scale atoms per 64-element K step (raw ring); each
+//               copy of a step from its own lane (one thread's copies are
+//               served one after another, different threads' in parallel)
+//   warp 1      TMEM alloc (two 256-column accumulators); lane 0 issues
+//               4 x tcgen05.mma kind::f16 (M 128, N 256, K 16) per step
+//   warps 2..9  converters: raw ring -> FP16 tiles (128-byte swizzled rows);
+//               thread t expands half of A row t % 128 and W row t
+//   warps 10..17 epilogue: TMEM -> registers 32 columns at a time,
+//               * s_t[m] * s_w, BF16/FP32 store
 #include <algorithm>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -30,22 +35,25 @@ namespace nv4 {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 128;
+constexpr int BN = 256;
+constexpr int NG = BN / 128;    // 128-row scale groups per W tile
 constexpr int KSTEP = 64;       // K elements per pipeline step
 constexpr int RAW_STAGES = 4;
 constexpr int CONV_STAGES = 3;
 constexpr int ACC_BUFS = 2;
-constexpr int CONV_WARPS = 4;
-constexpr int EPI_WARPS = 4;
+constexpr int CONV_WARPS = 8;
+constexpr int EPI_WARPS = 8;
+constexpr int EPI_FIRST_WARP = 2 + CONV_WARPS;
 constexpr int THREADS = 64 + 32 * (CONV_WARPS + EPI_WARPS);
 constexpr int RAW_A = BM * KSTEP;           // 8192 B of FP8
-constexpr int RAW_W = BN * KSTEP / 2;       // 4096 B of FP4 codes
-constexpr int RAW_S = (BN / 128) * 512;     // scale atom(s)
-constexpr int RAW_BYTES = RAW_A + RAW_W + RAW_S + 512; // keep 1024-aligned stages
+constexpr int RAW_W = BN * KSTEP / 2;       // 8192 B of FP4 codes
+constexpr int RAW_S = NG * 512;             // scale atoms
+constexpr int RAW_BYTES = RAW_A + RAW_W + RAW_S;
 constexpr int CONV_A = BM * 128;            // FP16 rows of 128 bytes
 constexpr int CONV_B = BN * 128;
 constexpr int CONV_BYTES = CONV_A + CONV_B;
-constexpr int TMEM_COLS = 256;
+constexpr int TMEM_COLS = 512;
+static_assert(CONV_WARPS * 32 == 2 * BM && CONV_WARPS * 32 == BN, "converter thread mapping");
 constexpr int SMEM_BYTES = CONV_STAGES * CONV_BYTES + RAW_STAGES * RAW_BYTES + 256 + 1024;
 static_assert(RAW_BYTES % 1024 == 0 && CONV_BYTES % 1024 == 0, "alignment");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -59,7 +67,7 @@ struct Params {
     const float *w_second;
     void *out;
     int64_t ldy, M, N;
-    int32_t m_tiles, n_tiles, ksteps, k64_total, out_dtype, vec_ok;
+    int32_t m_tiles, n_tiles, ksteps, k64_total, out_dtype, vec_ok, w_groups;
     uint32_t *status;
     uint64_t timeout_ns;
 };
@@ -152,29 +160,43 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
         int st = 0, issued = 0;
         uint32_t ph = 0;
         bool ok = true;
-        if (lane == 0) {
-            for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-                int tm, tn;
-                decode(p, item, tm, tn);
-                for (int ks = 0; ks < p.ksteps; ++ks) {
-                    if (!mbar_wait(&raw_empty[st], ph ^ 1u, p.timeout_ns, abort_flag)) {
+        for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+            int tm, tn;
+            decode(p, item, tm, tn);
+            const int g0 = tn * NG; // first 128-row scale group of the W tile
+            int ng = 0;
+#pragma unroll
+            for (int h = 0; h < NG; ++h)
+                ng += (g0 + h < p.w_groups) ? 1 : 0;
+            for (int ks = 0; ks < p.ksteps; ++ks) {
+                const bool got = mbar_wait(&raw_empty[st], ph ^ 1u, p.timeout_ns, abort_flag);
+                if (!__all_sync(FULLMASK, got)) {
+                    if (lane == 0)
                         timeout(p, abort_flag);
-                        ok = false;
-                        break;
-                    }
-                    uint8_t *r = raw + st * RAW_BYTES;
-                    mbar_arrive_expect_tx(&raw_full[st], RAW_A + RAW_W + RAW_S);
+                    ok = false;
+                    break;
+                }
+                uint8_t *r = raw + st * RAW_BYTES;
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&raw_full[st], RAW_A + RAW_W + ng * 512);
+                __syncwarp();
+                // op 0: A, 1: W codes, 2..2+NG-1: W scale atoms; lanes 8r.. serve steps r, r+4, ...
+                const int op = lane - 8 * (issued & 3);
+                if (op == 0)
                     tma_load_2d(r, &p.tmap_a, ks * KSTEP, tm * BM, &raw_full[st]);
+                else if (op == 1)
                     tma_load_2d(r + RAW_A, &p.tmap_w, ks * (KSTEP / 2), tn * BN, &raw_full[st]);
-                    bulk_load(r + RAW_A + RAW_W, p.w_scales + ((size_t)tn * p.k64_total + ks) * 512, RAW_S,
-                              &raw_full[st]);
-                    ++issued;
-                    if (++st == RAW_STAGES) {
-                        st = 0;
-                        ph ^= 1u;
-                    }
+                else if (op >= 2 && op < 2 + NG && g0 + op - 2 < p.w_groups)
+                    bulk_load(r + RAW_A + RAW_W + (op - 2) * 512,
+                              p.w_scales + ((size_t)(g0 + op - 2) * p.k64_total + ks) * 512, 512, &raw_full[st]);
+                ++issued;
+                if (++st == RAW_STAGES) {
+                    st = 0;
+                    ph ^= 1u;
                 }
             }
+        }
+        if (lane == 0) {
             const int n = min(issued, RAW_STAGES);
             for (int q = 0; q < n; ++q) {
                 if (--st < 0) {
@@ -235,7 +257,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
         __syncwarp();
     } else if (warp < 2 + CONV_WARPS) {
         // ------------------------------------------------------------ converters
-        const int t = threadIdx.x - 64; // 0..127: tile row
+        const int t = threadIdx.x - 64; // 0..255
         int rs = 0, cs = 0;
         uint32_t rph = 0, cph = 0;
         for (int item = blockIdx.x; item < total; item += gridDim.x) {
@@ -252,11 +274,12 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
                 const uint8_t *r = raw + rs * RAW_BYTES;
                 uint8_t *cA = conv + cs * CONV_BYTES;
                 uint8_t *cB = cA + CONV_A;
-                // A row t: 64 FP8 -> 64 FP16 (8 chunks of 16 bytes, swizzled)
+                // A row ar, half ah: 32 FP8 -> 32 FP16 = chunks 4 ah .. 4 ah + 3 (swizzled)
                 {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(r + t * KSTEP);
+                    const int ar = t & (BM - 1), ah = t >> 7;
+                    const uint4 *src = reinterpret_cast<const uint4 *>(r + ar * KSTEP + ah * 32);
 #pragma unroll
-                    for (int h = 0; h < 4; ++h) {
+                    for (int h = 0; h < 2; ++h) {
                         const uint4 v = src[h]; // 16 FP8 -> 2 output chunks
                         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
                         uint32_t o[8];
@@ -265,16 +288,16 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
                             o[2 * q] = f16x2_from_e4m3x2(w[q] & 0xFFFFu);
                             o[2 * q + 1] = f16x2_from_e4m3x2(w[q] >> 16);
                         }
-                        const int c0 = 2 * h, c1 = 2 * h + 1;
-                        *reinterpret_cast<uint4 *>(cA + t * 128 + ((c0 ^ (t & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-                        *reinterpret_cast<uint4 *>(cA + t * 128 + ((c1 ^ (t & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+                        const int c0 = 4 * ah + 2 * h, c1 = c0 + 1;
+                        *reinterpret_cast<uint4 *>(cA + ar * 128 + ((c0 ^ (ar & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                        *reinterpret_cast<uint4 *>(cA + ar * 128 + ((c1 ^ (ar & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
                     }
                 }
                 // W row t: 32 code bytes (64 E2M1) x 4 E4M3 scales -> 64 FP16
                 {
                     const uint8_t *wr = r + RAW_A + t * (KSTEP / 2);
-                    const uint32_t sc = *reinterpret_cast<const uint32_t *>(r + RAW_A + RAW_W + (t & 31) * 16 +
-                                                                           ((t & 127) >> 5) * 4);
+                    const uint32_t sc = *reinterpret_cast<const uint32_t *>(
+                        r + RAW_A + RAW_W + (t >> 7) * 512 + (t & 31) * 16 + ((t & 127) >> 5) * 4);
 #pragma unroll
                     for (int b = 0; b < 4; ++b) { // 16-element block b uses scale byte b
                         const uint32_t s2 = f16x2_from_e4m3x2(((sc >> (8 * b)) & 0xFFu) * 0x0101u);
@@ -311,7 +334,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;
+        const int q = warp & 3;                     // the TMEM lane quarter this warp may access
+        const int chalf = (warp - EPI_FIRST_WARP) >> 2; // which 128 accumulator columns
         const int row = q * 32 + lane;
         int acc = 0;
         uint32_t aph = 0;
@@ -329,7 +353,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
             const int64_t i = (int64_t)tm * BM + row;
             const float alpha = i < p.M ? p.s_t[i] * sw : 0.0f;
             const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
-            for (int c0 = 0; c0 < BN; c0 += 32) {
+            for (int c0 = chalf * (BN / 2); c0 < (chalf + 1) * (BN / 2); c0 += 32) {
                 uint32_t v[32];
                 tc_ld_32x32b_x32(tb + c0, v);
                 tc_wait_ld();
@@ -411,6 +435,7 @@ cudaError_t launch_w4a8(const W4A8GemmArgs &g, cudaStream_t stream)
     p.n_tiles = (int)ceil_div(g.N, BN);
     p.ksteps = (int)(g.K / KSTEP);
     p.k64_total = (int)(g.K / 64);
+    p.w_groups = (int)ceil_div(g.N, 128);
     p.out_dtype = g.out_dtype;
     const int esz = g.out_dtype == NVFP4_OUT_BF16 ? 2 : 4;
     p.vec_ok = ((g.ldy * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(g.out) % 16) == 0) ? 1 : 0;

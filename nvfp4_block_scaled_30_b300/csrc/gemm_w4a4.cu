@@ -219,6 +219,40 @@ __device__ __forceinline__ bool work_next(const Params &p, const int *prefix, in
     return true;
 }
 
+// The same sequence for roles that need only the number of K stages of each
+// work item (the MMA and scale warps): grouped items always run every K
+// stage, so their expert rows (global offsets) are not loaded.
+template <bool GROUPED>
+__device__ __forceinline__ bool work_next_light(const Params &p, const int *prefix, int total_items, WorkIter &w,
+                                                Tile &t)
+{
+    if (!GROUPED)
+        return work_next<false>(p, prefix, total_items, w, t);
+    if (w.item >= total_items)
+        return false;
+    t.tile = w.item;
+    t.kst0 = 0;
+    t.kst1 = p.kstages;
+    w.item += gridDim.x;
+    return true;
+}
+
+// Grouped: source activation row of tile rows lane + 32q (row 0 for rows past
+// the expert or out-of-range indices, whose results are unspecified).
+__device__ __forceinline__ void tile_rows(const Params &p, bool indexed, const Tile &t, int lane, int (&src_row)[4],
+                                          bool (&row_ok)[4])
+{
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int64_t g = t.row0 + lane + 32 * q;
+        row_ok[q] = g < t.row_end;
+        int r = row_ok[q] ? (indexed ? p.row_idx[g] : (int)g) : 0;
+        if (r < 0 || r >= p.a_rows)
+            r = 0;
+        src_row[q] = r;
+    }
+}
+
 // Named barrier 1 across the epilogue warps.
 __device__ __forceinline__ void epi_bar_sync()
 {
@@ -339,11 +373,11 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
     const bool indexed = GROUPED && p.row_idx != nullptr;
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            // codes: the copies, plus the gather's arrival for indexed rows;
-            // scales: the copies, plus the producer's arrival after it wrote
-            // the gathered activation scales (grouped)
-            mbar_init(&full[s], indexed ? 2 : 1);
-            mbar_init(&sf_full[s], GROUPED ? 2 : 1);
+            // codes: the bulk copies (one arrival), plus one cp.async
+            // arrival per producer lane for gathered rows; scales likewise
+            // (grouped: the activation scales are gathered by cp.async)
+            mbar_init(&full[s], indexed ? 33 : 1);
+            mbar_init(&sf_full[s], GROUPED ? 33 : 1);
             mbar_init(&empty[s], 1);
             mbar_init(&sf_ready[s], 1);
         }
@@ -470,21 +504,23 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                     issue(pt, kb, n_early, n_early, true, true, false);
         }
         pdl_wait();
-        while (ok && work_next<GROUPED>(p, prefix, total_items, wi, t)) {
-            // grouped: source activation row of tile rows lane + 32q
-            int src_row[4] = {0, 0, 0, 0};
-            bool row_ok[4] = {false, false, false, false};
-            if (GROUPED) {
+        // grouped items are decoded one ahead (expert offsets, then the row
+        // indices once the offsets have arrived) so their global loads
+        // overlap the current item's copies
+        Tile t_next;
+        bool have_next = work_next<GROUPED>(p, prefix, total_items, wi, t_next);
+        int src_row[4] = {0, 0, 0, 0}, next_row[4] = {0, 0, 0, 0};
+        bool row_ok[4] = {false, false, false, false}, next_ok[4] = {false, false, false, false};
+        if (GROUPED && have_next)
+            tile_rows(p, indexed, t_next, lane, next_row, next_ok);
+        while (ok && have_next) {
+            t = t_next;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int64_t g = t.row0 + lane + 32 * q;
-                    row_ok[q] = g < t.row_end;
-                    int r = row_ok[q] ? (indexed ? p.row_idx[g] : (int)g) : 0;
-                    if (r < 0 || r >= p.a_rows) // out-of-range index: read row 0, result unspecified
-                        r = 0;
-                    src_row[q] = r;
-                }
+            for (int q = 0; q < 4; ++q) {
+                src_row[q] = next_row[q];
+                row_ok[q] = next_ok[q];
             }
+            have_next = work_next<GROUPED>(p, prefix, total_items, wi, t_next);
             for (int kb = t.kst0; kb < t.kst1; ++kb) {
                 const bool got = mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag);
                 if (!__all_sync(FULLMASK, got)) {
@@ -517,7 +553,9 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                             }
                         }
                     }
-                    // activation scales of the tile's rows: 4 bytes per row and 64-K chunk
+                    // activation scales of the tile's rows: 4 bytes per row and
+                    // 64-K chunk, gathered asynchronously (zero for rows past
+                    // the expert and chunks past K)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int r = src_row[q];
@@ -525,23 +563,16 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                             ((size_t)(r >> 7) * p.k64 + 4 * kb) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
-                            uint32_t v = 0;
-                            if (row_ok[q] && kk < nk)
-                                v = __ldg(reinterpret_cast<const uint32_t *>(p.sfa + base + kk * 512));
-                            *reinterpret_cast<uint32_t *>(sSFA + kk * 512 + lane * 16 + q * 4) = v;
+                            const bool live = row_ok[q] && kk < nk;
+                            cp_async_4(sSFA + kk * 512 + lane * 16 + q * 4, p.sfa + (live ? base + kk * 512 : 0),
+                                       live ? 4u : 0u);
                         }
                     }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&sf_full[stage]);
-                    if (indexed) {
-                        cp_async_wait_all();
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive(&full[stage]);
-                    }
+                    // each lane's gathers complete the stage's barriers on
+                    // their own; the consumers fence before the tensor core reads
+                    cp_async_arrive_noinc(&sf_full[stage]);
+                    if (indexed)
+                        cp_async_arrive_noinc(&full[stage]);
                 }
                 ++issued;
                 if (++stage == C::STAGES) {
@@ -549,6 +580,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                     phase ^= 1u;
                 }
             }
+            if (GROUPED && have_next)
+                tile_rows(p, indexed, t_next, lane, next_row, next_ok);
         }
         // every load is issued: the next grid in the stream may start its
         // set-up (it waits for this grid's completion before touching memory)
@@ -581,7 +614,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
             WorkIter wi;
             work_begin(p, total_items, wi);
             Tile t;
-            while (ok && work_next<GROUPED>(p, prefix, total_items, wi, t)) {
+            while (ok && work_next_light<GROUPED>(p, prefix, total_items, wi, t)) {
                 if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
                     record_timeout(p, abort_flag);
                     break;
@@ -596,6 +629,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                         ok = false;
                         break;
                     }
+                    if (indexed) // gathered code rows were written by cp.async
+                        fence_proxy_async_smem();
                     tc_fence_after();
                     const int nk = min(4, p.k64 - 4 * kb);
                     const uint8_t *sA = smem + stage * C::STAGE_BYTES;
@@ -642,7 +677,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
         WorkIter wi;
         work_begin(p, total_items, wi);
         Tile t;
-        while (ok && work_next<GROUPED>(p, prefix, total_items, wi, t)) {
+        while (ok && work_next_light<GROUPED>(p, prefix, total_items, wi, t)) {
             for (int kb = t.kst0; kb < t.kst1; ++kb) {
                 const bool got = mbar_wait(&sf_full[stage], phase, p.timeout_ns, abort_flag);
                 if (!__all_sync(FULLMASK, got)) {
@@ -651,6 +686,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                     ok = false;
                     break;
                 }
+                if (GROUPED) // gathered activation scales were written by cp.async
+                    fence_proxy_async_smem();
                 if (lane == 0) {
                     // atoms of B row groups past the weight rows hold stale
                     // bytes; they only feed output columns that are never stored

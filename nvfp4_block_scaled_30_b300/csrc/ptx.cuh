@@ -91,6 +91,20 @@ __device__ __forceinline__ void cp_async_16(void *dst, const void *src, uint32_t
                  : "memory");
 }
 
+// 4-byte cp.async (src_bytes 0 or 4; 0 zero-fills the destination).
+__device__ __forceinline__ void cp_async_4(void *dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+// Arrive on *bar (without raising its expected count) once every cp.async
+// this thread issued so far has landed.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_wait_all()
 {
     asm volatile("cp.async.wait_all;" ::: "memory");

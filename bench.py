@@ -115,6 +115,24 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ---------------------------------------------------------------- multi-rank (replicas)
+def max_over_ranks(ms, dist, device):
+    """The slowest rank's time: every rank contributes its own ms (MAX
+    all-reduce); a single process returns its own."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(value_rank, ms_rank, ms_max, world):
+    """Whole-job throughput of `world` replicas doing the same work: the
+    units all ranks processed over the slowest rank's time."""
+    return value_rank * ms_rank / ms_max * world
+
+
 # ---------------------------------------------------------------- GPU workloads
 class Ctx:
     def __init__(self, torch, nv, dev):
@@ -415,12 +433,8 @@ def main():
         unit, value_rank = "GB/s", r["value"]
     barrier()
     t_end = time.time()
-    ms = r["ms"]
-    if dist is not None:
-        tm = torch.tensor([ms], device=dev)
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-        ms = float(tm.item())
-    value = value_rank * r["ms"] / ms * world   # units of all ranks over the slowest rank's time
+    ms = max_over_ranks(r["ms"], dist, dev)
+    value = job_value(value_rank, r["ms"], ms, world)
 
     clocks = sampler.summary(t_start, t_end)
 

@@ -187,15 +187,14 @@ __device__ __forceinline__ void mul2_rn(float a0, float a1, float r, float &p0, 
     p1 = __uint_as_float((uint32_t)(d >> 32));
 }
 
-// One whole 16-element block (16 BF16 values in lo, hi) by one thread: the
+// One whole 16-element block (16 BF16 values in 8 words) by one thread: the
 // block maximum from the magnitude bits (exact, equal to the float maximum
 // of finite values), the same scale and code arithmetic as encode_chunk, and
 // one 8-byte code store plus one scale byte.
 template <bool TILED>
-__device__ __forceinline__ void encode_block16(const uint4 lo, const uint4 hi, int64_t row, int64_t blk, int64_t K,
-                                               float sg, uint8_t *codes, uint8_t *scales)
+__device__ __forceinline__ void encode_block16(const uint32_t (&w)[8], int64_t row, int64_t blk, int64_t K, float sg,
+                                               uint8_t *codes, uint8_t *scales)
 {
-    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
     uint32_t m2 = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -220,10 +219,38 @@ __device__ __forceinline__ void encode_block16(const uint4 lo, const uint4 hi, i
     scales[scale_offset(row, blk, K, TILED)] = (uint8_t)e;
 }
 
+// One 16-value block (32 bytes) of x.  With V8 the block is 32-byte aligned
+// and comes in one 256-bit load; KEEP asks L2 to keep it (the amax pass:
+// the encode pass reads x again) and !KEEP marks its last use.  Without V8
+// two 16-byte loads.
+template <bool V8, bool KEEP>
+__device__ __forceinline__ void load_block16(const uint16_t *p, uint32_t (&w)[8])
+{
+    if (V8) {
+        if (KEEP)
+            asm volatile("ld.global.nc.L1::no_allocate.L2::evict_last.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+                           "=r"(w[7])
+                         : "l"(p));
+        else
+            asm volatile("ld.global.nc.L1::no_allocate.L2::evict_first.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+                           "=r"(w[7])
+                         : "l"(p));
+    } else {
+        const uint4 a = __ldg(reinterpret_cast<const uint4 *>(p));
+        const uint4 b = __ldg(reinterpret_cast<const uint4 *>(p) + 1);
+        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+        w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    }
+}
+
 // Pass 1: per-CTA maximum of |x| (as BF16 magnitude bits) and a non-finite
-// flag.  The rows x K/8 chunks of 8 values are one flat index space, so small
-// row counts still spread over many CTAs; each thread keeps QU 16-byte loads
-// in flight and walks the index space with a cursor (no division per chunk).
+// flag.  The rows x K/16 blocks of 16 values are one flat index space, so
+// small row counts still spread over many CTAs; each thread keeps QU block
+// loads in flight and walks the index space with a cursor (no division per
+// block).  Loads ask L2 to keep x for the encode pass.
+template <bool V8>
 __global__ void __launch_bounds__(QT) amax_partial_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t K,
                                                           int64_t ldx, uint32_t *__restrict__ partial,
                                                           uint32_t *__restrict__ status)
@@ -233,31 +260,31 @@ __global__ void __launch_bounds__(QT) amax_partial_kernel(const uint16_t *__rest
     // may still read the buffers this pass and the next one write)
     pdl_wait();
     pdl_trigger();
-    const int64_t cpr = K / 8;
-    const int64_t total = rows * cpr;
+    const int64_t bpr = K / 16;
+    const int64_t total = rows * bpr;
     const int64_t base0 = (int64_t)blockIdx.x * QT * QU + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * QT * QU;
-    Cursor cur{base0 / cpr, base0 % cpr};
-    const int64_t qs = QT / cpr, rs = QT % cpr, qi = stride / cpr, ri = stride % cpr;
+    Cursor cur{base0 / bpr, base0 % bpr};
+    const int64_t qs = QT / bpr, rs = QT % bpr, qi = stride / bpr, ri = stride % bpr;
     uint32_t m2 = 0, bad = 0; // m2: two 16-bit magnitude maxima
     for (int64_t base = base0; base < total; base += stride) {
-        uint4 v[QU];
+        uint32_t w[QU][8];
         Cursor c = cur;
 #pragma unroll
         for (int u = 0; u < QU; ++u) {
-            v[u] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                w[u][i] = 0u;
             if (base + (int64_t)u * QT < total)
-                v[u] = __ldg(reinterpret_cast<const uint4 *>(x + c.row * ldx + c.j * 8));
-            cursor_advance(c, qs, rs, cpr);
+                load_block16<V8, true>(x + c.row * ldx + c.j * 16, w[u]);
+            cursor_advance(c, qs, rs, bpr);
         }
 #pragma unroll
-        for (int u = 0; u < QU; ++u) {
-            m2 = __vmaxu2(m2, v[u].x & 0x7FFF7FFFu);
-            m2 = __vmaxu2(m2, v[u].y & 0x7FFF7FFFu);
-            m2 = __vmaxu2(m2, v[u].z & 0x7FFF7FFFu);
-            m2 = __vmaxu2(m2, v[u].w & 0x7FFF7FFFu);
-        }
-        cursor_advance(cur, qi, ri, cpr);
+        for (int u = 0; u < QU; ++u)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                m2 = __vmaxu2(m2, w[u][i] & 0x7FFF7FFFu);
+        cursor_advance(cur, qi, ri, bpr);
     }
     const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
     // a non-finite value has the largest magnitude bits (>= 0x7F80)
@@ -274,7 +301,7 @@ __global__ void __launch_bounds__(QT) amax_partial_kernel(const uint16_t *__rest
 // form one flat index space (a lane pair = one 16-element block, never split
 // across rows since K/8 is even); the padding rows rows..rows_pad of the tiled
 // layout only get zero scales, written by a separate loop.
-template <bool TILED>
+template <bool TILED, bool V8>
 __global__ void __launch_bounds__(QT) nvfp4_encode_kernel(const uint16_t *__restrict__ x, int64_t rows,
                                                           int64_t rows_pad, int64_t K, int64_t ldx,
                                                           uint8_t *__restrict__ codes, uint8_t *__restrict__ scales,
@@ -302,7 +329,7 @@ __global__ void __launch_bounds__(QT) nvfp4_encode_kernel(const uint16_t *__rest
     Cursor cur{base0 / bpr, base0 % bpr};
     const int64_t qs = QT / bpr, rs = QT % bpr, qi = stride / bpr, ri = stride % bpr;
     for (int64_t base = base0; base < total; base += stride) {
-        uint4 v[QB][2];
+        uint32_t v[QB][8];
         Cursor c[QB];
         c[0] = cur;
 #pragma unroll
@@ -311,18 +338,17 @@ __global__ void __launch_bounds__(QT) nvfp4_encode_kernel(const uint16_t *__rest
                 c[u] = c[u - 1];
                 cursor_advance(c[u], qs, rs, bpr);
             }
-            v[u][0] = v[u][1] = make_uint4(0, 0, 0, 0);
-            if (base + (int64_t)u * QT < total) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(x + c[u].row * ldx + c[u].j * 16);
-                v[u][0] = __ldg(src);
-                v[u][1] = __ldg(src + 1);
-            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                v[u][i] = 0u;
+            if (base + (int64_t)u * QT < total)
+                load_block16<V8, false>(x + c[u].row * ldx + c[u].j * 16, v[u]);
         }
 #pragma unroll
         for (int u = 0; u < QB; ++u) {
             if (base + (int64_t)u * QT >= total)
                 continue;
-            encode_block16<TILED>(v[u][0], v[u][1], c[u].row, c[u].j, K, sg, codes, scales);
+            encode_block16<TILED>(v[u], c[u].row, c[u].j, K, sg, codes, scales);
         }
         cursor_advance(cur, qi, ri, bpr);
     }
@@ -575,25 +601,34 @@ cudaError_t launch_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K, in
     if (mode == NVFP4_SCALE_TENSOR_FP32) {
         // flat passes: enough CTAs for one sweep of QU loads per thread, at
         // most a few waves
-        const int64_t chunks = std::max<int64_t>(rows * (K / 8), 1);
+        const int64_t blocks1 = std::max<int64_t>(rows * (K / 16), 1);
         const int64_t per_cta = (int64_t)QT * QU;
-        const int grid1 = (int)std::min<int64_t>(ceil_div(chunks, per_cta), std::min(AMAX_MAX_CTAS, sms * 4));
+        const int grid1 = (int)std::min<int64_t>(ceil_div(blocks1, per_cta), std::min(AMAX_MAX_CTAS, sms * 4));
         const int64_t pad_words = tiled ? (rows_pad - rows) * (K / 64) : 0;
         const int64_t blocks = std::max<int64_t>(rows * (K / 16), 1);
         const int grid_e = (int)std::max<int64_t>(
             1, std::min<int64_t>(std::max(ceil_div(blocks, (int64_t)QT * QB), ceil_div(pad_words, (int64_t)QT * 8)),
                                  (int64_t)sms * 8));
-        cudaError_t e = launch_pdl(amax_partial_kernel, grid1, QT, 0, stream, x, rows, K, ldx, amax_partial, status);
+        // 32-byte block loads when x and its row stride allow them
+        const bool v8 = (reinterpret_cast<uintptr_t>(x) % 32) == 0 && (ldx % 16) == 0;
+        cudaError_t e = v8 ? launch_pdl(amax_partial_kernel<true>, grid1, QT, 0, stream, x, rows, K, ldx,
+                                        amax_partial, status)
+                           : launch_pdl(amax_partial_kernel<false>, grid1, QT, 0, stream, x, rows, K, ldx,
+                                        amax_partial, status);
         if (e != cudaSuccess)
             return e;
         float *sg = static_cast<float *>(second);
         const uint32_t *part = amax_partial;
         if (tiled)
-            e = launch_pdl(nvfp4_encode_kernel<true>, grid_e, QT, 0, stream, x, rows, rows_pad, K, ldx, codes, scales,
-                           sg, part, grid1, zp);
+            e = v8 ? launch_pdl(nvfp4_encode_kernel<true, true>, grid_e, QT, 0, stream, x, rows, rows_pad, K, ldx,
+                                codes, scales, sg, part, grid1, zp)
+                   : launch_pdl(nvfp4_encode_kernel<true, false>, grid_e, QT, 0, stream, x, rows, rows_pad, K, ldx,
+                                codes, scales, sg, part, grid1, zp);
         else
-            e = launch_pdl(nvfp4_encode_kernel<false>, grid_e, QT, 0, stream, x, rows, rows_pad, K, ldx, codes,
-                           scales, sg, part, grid1, zp);
+            e = v8 ? launch_pdl(nvfp4_encode_kernel<false, true>, grid_e, QT, 0, stream, x, rows, rows_pad, K, ldx,
+                                codes, scales, sg, part, grid1, zp)
+                   : launch_pdl(nvfp4_encode_kernel<false, false>, grid_e, QT, 0, stream, x, rows, rows_pad, K, ldx,
+                                codes, scales, sg, part, grid1, zp);
         if (e != cudaSuccess)
             return e;
     } else {

@@ -173,3 +173,21 @@ def test_nonfinite_input_two_pass_path():
     ws = nv.Workspace(nv.workspace_size(nv.OP_QUANTIZE, 64, 0, 8192))
     nv.quantize(dev_bf16(bits), ws=ws)
     assert ws.status() == nv.ERR_NONFINITE_INPUT
+
+
+# The two-pass path loads 32-byte blocks when x and its row stride are 32-byte
+# aligned and falls back to 16-byte loads otherwise: a 16-byte start offset
+# and a row stride of 520 elements take the fallback.
+@pytest.mark.parametrize("offset,pitch", [(8, 8200), (0, 8200), (8, 8192 + 16)])
+def test_two_pass_alignment_fallback_bit_exact(offset, pitch):
+    M, K = 64, 8192                      # 65536 chunks: two passes
+    bits = synth.activations(9, 80 + offset, M, K, 0.01, 50.0)
+    wide = np.zeros((M, pitch), np.uint16)
+    wide[:, offset:offset + K] = bits
+    x = dev_bf16(wide)[:, offset:offset + K]
+    t = nv.quantize(x)
+    oc, os_, og = oracle.nvfp4_encode(bits)
+    np.testing.assert_array_equal(host(t.codes), oc)
+    from helpers import untile_scales
+    np.testing.assert_array_equal(untile_scales(host(t.scales), 128, K)[:M], os_)
+    assert host(t.second)[0] == og

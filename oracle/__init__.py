@@ -65,6 +65,8 @@ def lib():
         L.orc_nvfp4_encode.argtypes = [_u16, _I64, _I64, _I64, _u8, _u8, _f32]
         L.orc_nvfp4_encode_macro.restype = ctypes.c_int
         L.orc_nvfp4_encode_macro.argtypes = [_u16, _I64, _I64, _I64, _u8, _u8, _u16]
+        L.orc_nvfp4_encode_f32_scaled.restype = ctypes.c_int
+        L.orc_nvfp4_encode_f32_scaled.argtypes = [_f32, _I64, _I64, _I64, ctypes.c_float, _u8, _u8]
         L.orc_fp8_token_encode.restype = ctypes.c_int
         L.orc_fp8_token_encode.argtypes = [_u16, _I64, _I64, _I64, _u8, _f32]
         L.orc_nvfp4_dequant.restype = None
@@ -155,6 +157,17 @@ def nvfp4_encode(x_bf16):
     sg = np.zeros(1, np.float32)
     _check(lib().orc_nvfp4_encode(x, R, K, K, codes, scales, sg))
     return codes, scales, np.float32(sg[0])
+
+
+def nvfp4_encode_f32_scaled(x_f32, s_g):
+    """Per-tensor NVFP4 encode of binary32 values [R, K] under a GIVEN tensor
+    scale s_g (no amax pass).  Returns (codes [R, K/2], scales [R, K/16])."""
+    x = _c(x_f32, np.float32)
+    R, K = x.shape
+    codes = np.zeros((R, K // 2), np.uint8)
+    scales = np.zeros((R, K // 16), np.uint8)
+    _check(lib().orc_nvfp4_encode_f32_scaled(x, R, K, K, np.float32(s_g), codes, scales))
+    return codes, scales
 
 
 def nvfp4_encode_macro(x_bf16):

@@ -269,6 +269,53 @@ int orc_nvfp4_encode(const uint16_t *x, int64_t R, int64_t K, int64_t ld,
     return ORC_OK;
 }
 
+/* The same block encode for binary32 inputs (a GEMM output, say). */
+static uint32_t encode_block_f32(const float *x, float s, uint8_t *out8)
+{
+    float amax_b = 0.0f;
+    for (int i = 0; i < 16; ++i) {
+        float a = fabsf(x[i]);
+        if (a > amax_b)
+            amax_b = a;
+    }
+    uint32_t e = 0;
+    if (s != 0.0f) {
+        float t = amax_b / 6.0f;
+        float u = t / s;
+        e = orc_e4m3_encode(u);
+    }
+    float d = (float)orc_e4m3_value(e) * s;
+    float r = recip_step(d);
+    for (int i = 0; i < 16; i += 2) {
+        uint32_t c0 = orc_e2m1_encode(x[i] * r);
+        uint32_t c1 = orc_e2m1_encode(x[i + 1] * r);
+        out8[i / 2] = (uint8_t)(c0 | (c1 << 4));
+    }
+    return e;
+}
+
+/* Per-tensor mode with a GIVEN second-level scale s_g (a calibrated or
+ * previous-step tensor scale instead of this tensor's amax / 2688), on
+ * binary32 inputs x [R][ld].  The block steps are those of
+ * orc_nvfp4_encode; values beyond 6 * 448 * s_g saturate (E4M3 at 448, E2M1
+ * at 6).  [TRT] item 2; the fused next-layer quantiser reading. */
+int orc_nvfp4_encode_f32_scaled(const float *x, int64_t R, int64_t K, int64_t ld, float s_g,
+                                uint8_t *codes, uint8_t *scales)
+{
+    if (R < 0 || K < 0 || K % 16 != 0 || ld < K || !(s_g >= 0.0f) || isinf(s_g))
+        return ORC_ERR_ARG;
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t k = 0; k < K; ++k)
+            if (!isfinite(x[r * ld + k]))
+                return ORC_ERR_NONFINITE;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t b = 0; b < K / 16; ++b)
+            scales[r * (K / 16) + b] = (uint8_t)encode_block_f32(
+                x + r * ld + b * 16, s_g, codes + r * (K / 2) + b * 8);
+    return ORC_OK;
+}
+
 /* Macro mode: every 256 consecutive elements of a row (16 micro-blocks) share
  * an FP16 macro-scale S = FP16(amax_256 / 2688) that replaces the tensor
  * scale.  [TRT] item 2.  macro [R][K/256] holds binary16 bits. */

@@ -202,3 +202,45 @@ def test_fp8_token_power_of_two_rows_round_trip(orc):
     a, st = orc.fp8_token_encode(bf16(x))
     assert np.array_equal(st, np.exp2(p).astype(np.float32))
     assert np.array_equal(a, codes | sign)
+
+
+# ---- encode of binary32 values under a given tensor scale -------------------
+# (the fused next-layer quantiser: the scale comes from calibration or a
+# previous step instead of this tensor's amax)
+
+def test_f32_scaled_equals_tensor_mode_when_scale_is_amax_over_2688(orc):
+    for cfg, tid in [(1, 0), (2, 0), (9, 5)]:
+        bits = synth.activations(cfg, tid, 24, 512, 0.01, 50.0)
+        c, s, sg = orc.nvfp4_encode(bits)
+        x = synth.bf16_to_f32(bits)
+        c2, s2 = orc.nvfp4_encode_f32_scaled(x, sg)
+        np.testing.assert_array_equal(c2, c)
+        np.testing.assert_array_equal(s2, s)
+
+
+def test_f32_scaled_saturates_when_the_scale_is_too_small(orc):
+    # a constant block v with v / (6 s) = 1000 > 448: scale code 448 (0x7E)
+    # and codes E2M1(v / (448 s)) = E2M1(13.4) -> 6 (0x7, sign kept)
+    s = 1.0 / 2688.0
+    v = 1000.0 * 6.0 * s
+    x = np.full((2, 32), v, np.float32)
+    x[1] = -v
+    c, sc = orc.nvfp4_encode_f32_scaled(x, s)
+    assert (sc == 0x7E).all()
+    assert (c[0] == 0x77).all() and (c[1] == 0xFF).all()
+
+
+def test_f32_scaled_zero_scale_gives_zero_codes_with_sign(orc):
+    x = np.array([[0.5, -0.5] * 8], np.float32)
+    c, sc = orc.nvfp4_encode_f32_scaled(x, 0.0)
+    assert (sc == 0).all()
+    assert (c == 0x80).all()            # even elements +0, odd elements -0
+
+
+def test_f32_scaled_rejects_nonfinite_and_bad_scales(orc):
+    x = np.zeros((1, 16), np.float32)
+    x[0, 3] = np.inf
+    with pytest.raises(orc.OracleError):
+        orc.nvfp4_encode_f32_scaled(x, 1.0)
+    with pytest.raises(orc.OracleError):
+        orc.nvfp4_encode_f32_scaled(np.zeros((1, 16), np.float32), -1.0)

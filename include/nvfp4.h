@@ -186,6 +186,31 @@ nvfp4_status nvfp4_gemm(const void *x_bf16, int64_t ldx, const nvfp4_tensor *a_q
                         int32_t policy, int32_t sensitive, void *ws, size_t ws_bytes,
                         nvfp4_stream_t stream);
 
+/* One W4A4 layer whose output is the next layer's NVFP4 activations: the
+ * next layer's quantiser fused into this GEMM's epilogue, so Y never reaches
+ * HBM in BF16 or FP32.  [TRT] item 2 defines the encode; the tensor scale
+ * cannot be amax(Y)/2688 of this very output (Y is not complete while it is
+ * being encoded), so it is a static one fixed beforehand by calibration, or
+ * the previous step's, in the spirit of the calibration step [TRT]
+ * describes.
+ *  x_bf16/ldx or a_q: the activations, exactly as for nvfp4_gemm (W4A4 route,
+ *  TENSOR_FP32 only).  w: TENSOR_FP32 weights [N, K], MMA_TILED.
+ *  y_q: caller-owned output tensor: rows == M, K == N (so N % 64 == 0),
+ *  mode TENSOR_FP32, layout MMA_TILED; y_q->second is a device float[1]
+ *  holding the tensor scale s_y (read, not written).
+ *  Each 16-element block of y = fl32(s_a * s_w) * acc (the FP32 output of
+ *  nvfp4_gemm) is encoded with the nvfp4_quantize rule under s_y; blocks
+ *  whose magnitude exceeds 6 * 448 * s_y saturate.  Scales of the padding
+ *  rows of the last 128-row tile are written as 0.
+ *  y_amax: NULL, or a device float updated to max(*y_amax, max|y|) (the
+ *  amax from which a later call's s_y = amax / 2688 can be taken);
+ *  initialise it to 0.  Must not alias y_q.
+ *  Workspace: nvfp4_workspace_size(NVFP4_OP_GEMM, M, N, K).
+ *  Errors: as nvfp4_gemm; UNSUPPORTED for MACRO_FP16 weights. */
+nvfp4_status nvfp4_gemm_nvfp4_out(const void *x_bf16, int64_t ldx, const nvfp4_tensor *a_q,
+                                  const nvfp4_tensor *w, nvfp4_tensor *y_q, float *y_amax, int64_t M,
+                                  void *ws, size_t ws_bytes, nvfp4_stream_t stream);
+
 /* W4A8 contraction from pre-quantised FP8 activations:
  * Y[m, n] = s_t[m] * s_w * sum_k E4M3(a[m, k]) * E2M1(w[n, k]) * E4M3(ew[n, k/16]).
  * a_fp8 uint8 [M][K] dense, s_t float[M]; w TENSOR_FP32, MMA_TILED. */

@@ -31,7 +31,7 @@ OP_QUANTIZE, OP_QUANTIZE_FP8, OP_GEMM, OP_W4A8_GEMM, OP_GROUPED_GEMM = range(5)
 EXPORTED = ["nvfp4_scale_bytes", "nvfp4_workspace_size", "nvfp4_workspace_init", "nvfp4_device_status",
             "nvfp4_policy_route", "nvfp4_quantize", "nvfp4_quantize_fp8", "nvfp4_gemm", "nvfp4_w4a8_gemm",
             "nvfp4_grouped_gemm", "nvfp4_probe_convert", "nvfp4_sm_count", "nvfp4_version",
-            "nvfp4_gemm_w4a4_noalloc"]
+            "nvfp4_gemm_w4a4_noalloc", "nvfp4_gemm_nvfp4_out"]
 
 
 class NVFP4Error(RuntimeError):
@@ -73,6 +73,7 @@ def lib():
                                           _VP, _SZ, _VP]),
             "nvfp4_probe_convert": (_I32, [_VP, _I64, _VP, _VP, _VP]),
             "nvfp4_gemm_w4a4_noalloc": (_I32, [_PT, _PT, _VP, _I64, _I32, _VP]),
+            "nvfp4_gemm_nvfp4_out": (_I32, [_VP, _I64, _PT, _PT, _PT, _VP, _I64, _VP, _SZ, _VP]),
             "nvfp4_sm_count": (_I32, []),
             "nvfp4_version": (ctypes.c_char_p, []),
         }
@@ -226,6 +227,33 @@ def gemm(w: NVFP4Tensor, x: Optional[torch.Tensor] = None, a_q: Optional[NVFP4Te
                             y.stride(0), out_dtype, M, policy, int(bool(sensitive)), ws.ptr, ws.nbytes,
                             _stream(stream)), "nvfp4_gemm")
     return y
+
+
+def gemm_nvfp4_out(w: NVFP4Tensor, s_y: torch.Tensor, x: Optional[torch.Tensor] = None,
+                   a_q: Optional[NVFP4Tensor] = None, y_amax: Optional[torch.Tensor] = None,
+                   out: Optional[NVFP4Tensor] = None, ws: Optional[Workspace] = None,
+                   stream=None) -> NVFP4Tensor:
+    """nvfp4_gemm_nvfp4_out: the W4A4 product encoded straight to NVFP4 under
+    the device tensor scale s_y (float32 [1]); y_amax (float32 [1], optional)
+    accumulates max|Y|."""
+    N, K = w.rows, w.K
+    M = x.shape[0] if x is not None else a_q.rows
+    device = w.codes.device
+    assert s_y.dtype == torch.float32 and s_y.numel() == 1 and s_y.device == device
+    assert y_amax is None or (y_amax.dtype == torch.float32 and y_amax.device == device)
+    if out is None:
+        out = empty_nvfp4(M, N, SCALE_TENSOR_FP32, LAYOUT_MMA_TILED, device)
+    out.second = s_y
+    if M == 0:
+        return out
+    ws = _ws(ws, workspace_size(OP_GEMM, M, N, K), device)
+    wd, yd = w.desc(), out.desc()
+    ad = a_q.desc() if a_q is not None else None
+    _check(lib().nvfp4_gemm_nvfp4_out(_ptr(x), x.stride(0) if x is not None else 0,
+                                      ctypes.byref(ad) if ad is not None else None, ctypes.byref(wd),
+                                      ctypes.byref(yd), _ptr(y_amax), M, ws.ptr, ws.nbytes, _stream(stream)),
+           "nvfp4_gemm_nvfp4_out")
+    return out
 
 
 def w4a8_gemm(a_fp8: torch.Tensor, s_t: torch.Tensor, w: NVFP4Tensor, out_dtype: int = OUT_BF16,

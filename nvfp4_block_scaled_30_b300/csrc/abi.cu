@@ -152,9 +152,12 @@ static nvfp4_status from_cuda(cudaError_t e)
 // below 90%) and there are enough K stages to spread.
 // W4A4 dense product of NVFP4 activations `a` ([M, K], tiled scales, tensor
 // mode) and weights `w` ([N, K]) into y.
+// With yq set, the output is NVFP4 (codes, tiled scales) under the device
+// tensor scale yq->second instead of y; stream-K is then not used.
 static nvfp4_status run_w4a4_dense(const uint8_t *a_codes, const uint8_t *a_scales, const float *a_second,
                                    int64_t M, const nvfp4_tensor *w, void *y, int64_t ldy, int y_dtype, void *ws,
-                                   const WsLayout &L, bool after_quantiser, cudaStream_t stream)
+                                   const WsLayout &L, bool after_quantiser, cudaStream_t stream,
+                                   const nvfp4_tensor *yq = nullptr, float *y_amax = nullptr)
 {
     const int64_t N = w->rows, K = w->K;
     DenseGemmArgs g{};
@@ -177,6 +180,13 @@ static nvfp4_status run_w4a4_dense(const uint8_t *a_codes, const uint8_t *a_scal
     // so: partial tiles meet in the workspace slots; the kernel writes y
     // itself and leaves the flags zeroed
     g.b_early = after_quantiser;
+    if (yq) {
+        g.yq_codes = static_cast<uint8_t *>(yq->codes);
+        g.yq_scales = static_cast<uint8_t *>(yq->scales);
+        g.yq_scale = static_cast<const float *>(yq->second);
+        g.yq_amax = reinterpret_cast<uint32_t *>(y_amax);
+        return from_cuda(launch_w4a4_dense(g, stream));
+    }
     g.streamk = L.sk_slots != 0;
     if (g.streamk) {
         g.slots = reinterpret_cast<float *>(ws_at(ws, L.sk_slots));
@@ -448,6 +458,62 @@ nvfp4_status nvfp4_gemm(const void *x_bf16, int64_t ldx, const nvfp4_tensor *a_q
     }
     return run_w4a4_dense(ac, as, static_cast<const float *>(asec), M, w, y, ldy, y_dtype, ws, L, x_bf16 != nullptr,
                           s);
+}
+
+nvfp4_status nvfp4_gemm_nvfp4_out(const void *x_bf16, int64_t ldx, const nvfp4_tensor *a_q, const nvfp4_tensor *w,
+                                  nvfp4_tensor *y_q, float *y_amax, int64_t M, void *ws, size_t ws_bytes,
+                                  nvfp4_stream_t stream)
+{
+    if ((x_bf16 == nullptr) == (a_q == nullptr))
+        return NVFP4_ERR_INVALID_ARG;
+    nvfp4_status st = check_tensor(w, true);
+    if (st != NVFP4_OK)
+        return st;
+    if (w->mode != NVFP4_SCALE_TENSOR_FP32)
+        return NVFP4_ERR_UNSUPPORTED;
+    const int64_t N = w->rows, K = w->K;
+    if (M < 0 || M > MAX_DIM || (y_amax && !aligned(y_amax, 4)))
+        return NVFP4_ERR_INVALID_ARG;
+    if ((st = check_tensor(y_q, true)) != NVFP4_OK)
+        return st;
+    if (y_q->mode != NVFP4_SCALE_TENSOR_FP32 || y_q->rows != M || y_q->K != N)
+        return NVFP4_ERR_INVALID_ARG;
+    if (x_bf16) {
+        if (ldx < K || ldx % 8 != 0 || (M > 0 && !aligned(x_bf16, 16)))
+            return NVFP4_ERR_INVALID_ARG;
+    } else {
+        if ((st = check_tensor(a_q, true)) != NVFP4_OK)
+            return st;
+        if (a_q->rows != M || a_q->K != K || a_q->mode != NVFP4_SCALE_TENSOR_FP32)
+            return NVFP4_ERR_INVALID_ARG;
+    }
+    const WsLayout L = ws_layout(NVFP4_OP_GEMM, M, N, K);
+    if ((st = check_ws(ws, ws_bytes, L.total)) != NVFP4_OK)
+        return st;
+    if (M == 0 || N == 0)
+        return NVFP4_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    const uint8_t *ac, *as;
+    const void *asec;
+    if (x_bf16) {
+        uint8_t *c = ws_at(ws, L.a_codes), *sc = ws_at(ws, L.a_scales);
+        void *sec = ws_at(ws, L.a_second);
+        cudaError_t e = launch_nvfp4_quantize(static_cast<const uint16_t *>(x_bf16), M, K, ldx, c, sc, sec,
+                                              NVFP4_SCALE_TENSOR_FP32, NVFP4_LAYOUT_MMA_TILED,
+                                              reinterpret_cast<uint32_t *>(ws_at(ws, L.amax)), status_word(ws), s,
+                                              false);
+        if (e != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        ac = c;
+        as = sc;
+        asec = sec;
+    } else {
+        ac = static_cast<const uint8_t *>(a_q->codes);
+        as = static_cast<const uint8_t *>(a_q->scales);
+        asec = a_q->second;
+    }
+    return run_w4a4_dense(ac, as, static_cast<const float *>(asec), M, w, nullptr, 0, NVFP4_OUT_FP32, ws, L,
+                          x_bf16 != nullptr, s, y_q, y_amax);
 }
 
 nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor *a, const int32_t *row_idx, const int64_t *expert_offsets,

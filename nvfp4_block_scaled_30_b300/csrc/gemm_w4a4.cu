@@ -101,6 +101,14 @@ struct Params {
     int32_t b_row_tiles;    // 128-row scale atoms available in B (total)
     int32_t a_box_rows;     // rows of A one stage loads (128, or M rounded up to 16 when M < 128)
     int32_t b_early;        // issue the first stages' B copies before waiting for the previous grid
+    // NVFP4 output (the next layer's quantiser fused into the epilogue):
+    // codes [a_rows][b_rows/2], MMA-tiled scales, under the given tensor
+    // scale; the largest |Y| is max-reduced into yq_amax when it is set
+    int32_t out_q;
+    uint8_t *yq_codes;
+    uint8_t *yq_scales;
+    const float *yq_scale;
+    uint32_t *yq_amax;
     // grouped mode
     const int64_t *offsets;
     const int32_t *row_idx;
@@ -346,6 +354,42 @@ __device__ __forceinline__ void store_chunk(const Params &p, const uint32_t (&v)
                 static_cast<float *>(p.out)[off] = y;
         }
     }
+}
+
+// NVFP4 store of 32 consecutive outputs of row i (two 16-element blocks):
+// y = alpha * acc exactly as the FP32 output path computes it, then the block
+// encode of the quantisers under the given tensor scale s: 8 code bytes and
+// one MMA-tiled scale byte per block.  Returns the largest |y| of the chunk.
+__device__ __forceinline__ float store_chunk_q(const Params &p, const uint32_t (&v)[32], int64_t i, int64_t j0,
+                                               float alpha, float s)
+{
+    const int64_t n = p.b_rows; // the output's K (a multiple of 64)
+    float m = 0.0f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        // y is formed twice (for the block maximum, then for the codes)
+        // rather than held: the accumulator slice already fills the registers
+        float amb = 0.0f;
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+            amb = fmaxf(amb, fabsf(__fmul_rn(alpha, __uint_as_float(v[16 * h + t]))));
+        const uint32_t e = block_scale_code(amb, s);
+        const float r = recip_step(__fmul_rn(e4m3_value(e), s));
+        uint32_t pk[2] = {0u, 0u};
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const float y0 = __fmul_rn(alpha, __uint_as_float(v[16 * h + 2 * t]));
+            const float y1 = __fmul_rn(alpha, __uint_as_float(v[16 * h + 2 * t + 1]));
+            pk[t >> 2] |= e2m1x2(__fmul_rn(y0, r), __fmul_rn(y1, r)) << (8 * (t & 3));
+        }
+        const int64_t j = j0 + 16 * h;
+        *reinterpret_cast<uint2 *>(p.yq_codes + i * (n / 2) + j / 2) = make_uint2(pk[0], pk[1]);
+        const int64_t blk = j / 16, r7 = i & 127;
+        p.yq_scales[((i >> 7) * (n / 64) + (blk >> 2)) * 512 + (r7 & 31) * 16 + (r7 >> 5) * 4 + (blk & 3)] =
+            (uint8_t)e;
+        m = fmaxf(m, amb);
+    }
+    return m;
 }
 
 template <int BN, bool GROUPED>
@@ -751,9 +795,54 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                 break;
             }
             tc_fence_after();
+            constexpr int NCH = C::EPI_COLS / 32;
+            if (!GROUPED && p.out_q) {
+                // NVFP4 output (whole tiles only; N is a multiple of 64): one
+                // 32-column chunk at a time straight from TMEM, the
+                // accumulator goes back to the MMA warp after the last one
+                const int64_t i = (int64_t)t.tile_m * BM + row_in_tile;
+                const int64_t j_base = (int64_t)t.tile_n * BN + cbase;
+                const float alpha = a_s * p.b_second[0];
+                const float s = *p.yq_scale;
+                const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + cbase;
+                float m = 0.0f;
+#pragma unroll 1
+                for (int c = 0; c < NCH; ++c) {
+                    uint32_t v1[32];
+                    tc_ld_32x32b_x32(tbase + c * 32, v1);
+                    tc_wait_ld();
+                    const int64_t j = j_base + c * 32;
+                    if (j < p.b_rows) {
+                        if (i < p.a_rows) {
+                            m = fmaxf(m, store_chunk_q(p, v1, i, j, alpha, s));
+                        } else {
+                            // padding rows of the last M tile: zero scales,
+                            // as the quantisers leave them
+                            const int64_t r7 = i & 127, kb = p.b_rows / 64;
+                            uint8_t *sc = p.yq_scales + ((i >> 7) * kb + (j >> 6)) * 512 + (r7 & 31) * 16 +
+                                          (r7 >> 5) * 4 + ((j >> 4) & 3);
+                            sc[0] = 0;
+                            sc[1] = 0;
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&acc_empty[acc]);
+                if (++acc == C::ACC_BUFS) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    m = fmaxf(m, __shfl_xor_sync(FULLMASK, m, o));
+                if (p.yq_amax != nullptr && lane == 0)
+                    atomicMax(p.yq_amax, __float_as_uint(m)); // |y| >= 0: bit order = value order
+                continue;
+            }
             // the whole accumulator slice of this warp into registers, then
             // the accumulator goes back to the MMA warp
-            constexpr int NCH = C::EPI_COLS / 32;
             uint32_t v[NCH][32];
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + cbase;
 #pragma unroll
@@ -1033,6 +1122,11 @@ cudaError_t launch_w4a4_dense(const DenseGemmArgs &g, cudaStream_t stream)
     p.b_rows = g.b_rows;
     p.out_dtype = g.out_dtype;
     p.b_early = g.b_early ? 1 : 0;
+    p.out_q = g.yq_codes != nullptr ? 1 : 0;
+    p.yq_codes = g.yq_codes;
+    p.yq_scales = g.yq_scales;
+    p.yq_scale = g.yq_scale;
+    p.yq_amax = g.yq_amax;
     p.slots = g.slots;
     p.flags = g.flags;
     p.slot_stride = g.a_rows * bn;

@@ -82,6 +82,14 @@ struct DenseGemmArgs {
     // the previous grid in the stream is this call's activation quantiser:
     // the first stages' weight copies may start before waiting for it
     bool b_early;
+    // NVFP4 output instead of out (whole tiles only, b_rows % 64 == 0):
+    // codes [a_rows][b_rows/2], MMA-tiled scales, encoded under the device
+    // tensor scale *yq_scale; the largest |Y| (float bits) is max-reduced
+    // into *yq_amax when yq_amax is set
+    uint8_t *yq_codes;
+    uint8_t *yq_scales;
+    const float *yq_scale;
+    uint32_t *yq_amax;
     uint32_t *status;
     uint64_t timeout_ns;
 };

@@ -397,4 +397,23 @@ __device__ __forceinline__ float e4m3_value(uint32_t c)
     return __uint_as_float(((ex + 120u) << 23) | (m << 20));
 }
 
+// NVFP4 block encode arithmetic shared by the quantisers and the GEMM
+// epilogue that quantises its output (binary32, explicit round-to-nearest):
+// the E4M3 scale code of a block whose absolute maximum is amax_b under the
+// second-level scale s, and the reciprocal of a dequantisation step (0 for
+// 0, at most the largest float).
+__device__ __forceinline__ uint32_t block_scale_code(float amax_b, float s)
+{
+    if (s == 0.0f)
+        return 0u;
+    const float t = __fdiv_rn(amax_b, 6.0f);
+    const float u = __fdiv_rn(t, s);
+    return e4m3(u);
+}
+
+__device__ __forceinline__ float recip_step(float d)
+{
+    return d == 0.0f ? 0.0f : fminf(__frcp_rn(d), 3.402823466e+38f);
+}
+
 } // namespace nv4

@@ -61,21 +61,7 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t *red)
     return r;
 }
 
-// Reciprocal of a dequantisation step: 0 for 0, clamped to the largest float.
-__device__ __forceinline__ float recip_step(float d)
-{
-    return d == 0.0f ? 0.0f : fminf(__frcp_rn(d), FLT_MAX);
-}
 
-// E4M3 scale code of a block with absolute maximum amax_b under second-level s.
-__device__ __forceinline__ uint32_t block_scale_code(float amax_b, float s)
-{
-    if (s == 0.0f)
-        return 0u;
-    float t = __fdiv_rn(amax_b, 6.0f);
-    float u = __fdiv_rn(t, s);
-    return e4m3(u);
-}
 
 // 8 values times r -> 4 packed E2M1 bytes (element 0 in the lowest nibble).
 __device__ __forceinline__ uint32_t pack8(const float (&f)[8], float r)

@@ -286,6 +286,48 @@ def workload_policy(c, steps, warmup, policy):
             "launches_per_step": sum(3 if r == 4 else 2 for r in routes), "device_status": work.status()}
 
 
+def workload_fused_stack(c, steps, warmup):
+    """The all-W4A4 policy stack with every layer but the last writing the
+    next layer's NVFP4 activations from its epilogue (nvfp4_gemm_nvfp4_out):
+    layer 0 quantises the BF16 input on the fly, the last layer writes BF16.
+    Static per-layer output scales s_l = amax_l / 2688, calibrated once
+    before timing, layer by layer, from the amax the fused epilogue reports."""
+    t, nv = c.torch, c.nv
+    cfg = synth.CONFIGS[4]
+    M, N, K, L = cfg["M"], cfg["N"], cfg["K"], cfg["layers"]
+    Ws = [c.quantized_weights(synth.weights(4, 100 + i, N, K))[0] for i in range(L)]
+    x = c.bf16(synth.activations(4, 0, M, K, cfg["outlier_frac"], cfg["outlier_factor"]))
+    work = nv.Workspace(nv.workspace_size(nv.OP_GEMM, M, N, K))
+    scales = [t.ones(1, dtype=t.float32, device=c.dev) for _ in range(L - 1)]
+    acts = [nv.empty_nvfp4(M, N, device=c.dev) for _ in range(2)]
+    y = t.empty((M, N), dtype=t.bfloat16, device=c.dev)
+    amax = t.zeros(1, dtype=t.float32, device=c.dev)
+
+    def layer(li, y_amax=None):
+        a_in = None if li == 0 else acts[(li - 1) % 2]
+        if li == L - 1:
+            nv.gemm(Ws[li], a_q=a_in, y=y, policy=nv.POLICY_Q4, ws=work)
+        else:
+            nv.gemm_nvfp4_out(Ws[li], scales[li], x=x if li == 0 else None, a_q=a_in, y_amax=y_amax,
+                              out=acts[li % 2], ws=work)
+
+    for li in range(L - 1):             # calibration
+        amax.zero_()
+        layer(li, amax)
+        scales[li].copy_(amax / 2688.0)
+        layer(li)
+    t.cuda.synchronize()
+
+    def step(i):
+        for li in range(L):
+            layer(li)
+
+    ms = c.time(step, steps, warmup)
+    flops = 2.0 * M * N * K * L
+    return {"ms": ms, "flops": flops, "value": flops / (ms * 1e-3) / 1e12, "launches_per_step": L + 2,
+            "device_status": work.status()}
+
+
 def workload_moe(c, steps, warmup):
     t, nv = c.torch, c.nv
     cfg = synth.CONFIGS[5]
@@ -457,6 +499,8 @@ def main():
             q = workload_policy(c, min(es, 20), 2, pol)
             extras[f"policy_stack_{name}"] = {"value": q["value"], "unit": "TFLOP/s", "ms": q["ms"],
                                               "routes": q["routes"]}
+        fq = workload_fused_stack(c, min(es, 20), 2)
+        extras["policy_stack_q4_fused"] = {"value": fq["value"], "unit": "TFLOP/s", "ms": fq["ms"]}
         mo = workload_moe(c, min(es, 50), 2)
         extras["moe_grouped"] = {"value": mo["value"], "unit": "GB/s", "ms": mo["ms"], "tflops": mo["tflops"],
                                  "frac_hbm": mo["value"] / hbm, "counts": [mo["counts_min"], mo["counts_max"]]}

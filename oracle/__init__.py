@@ -276,6 +276,58 @@ def gemm_grouped_w4a4(a, row_idx, offsets, w_codes, w_scales, w_sg):
     return Y
 
 
+# ---- mixture-of-experts feed-forward around the grouped contraction ------------
+#
+# The pages name MoE models (Qwen3 MoE variants) and MoE operations on the
+# NVFP4/W4A8 paths ("llama.cpp Put Precision Policy Inside the Model",
+# section "One model can need more than one precision"; "AdaLLM
+# Breakthrough", model list) but print no expert formula.  Reading taken:
+# the experts of those models are SwiGLU feed-forward blocks
+#   h = SiLU(x W_gate^T) * (x W_up^T),   y_e(x) = h W_down^T,
+# and a token's output is the gate-weighted sum of its routed experts'
+# outputs, y(t) = sum_k g_k(t) y_{e_k(t)}(x_t).  Both products are the grouped
+# W4A4 contraction above; the element-wise steps run in FP64.
+
+def silu(x):
+    """SiLU(x) = x * sigmoid(x) = x / (1 + exp(-x)) in FP64."""
+    x = np.asarray(x, np.float64)
+    with np.errstate(over="ignore"):
+        return x / (1.0 + np.exp(-x))
+
+
+def moe_up_swiglu(a, row_idx, offsets, gate, up, w_sg):
+    """SwiGLU expert up projection of the routed rows.
+
+    a: (codes, scales, s_g) activations; row_idx int32 [R] (activation row of
+    routed row j) or None; offsets int64 [E+1]; gate, up: (codes uint8
+    [E, I, K/2], scales uint8 [E, I, K/16]) of each expert's gate and up
+    weights, quantised together under the tensor scale w_sg[e].
+    Returns h float64 [R, I] = SiLU(G) * U with G, U the grouped products."""
+    G = gemm_grouped_w4a4(a, row_idx, offsets, gate[0], gate[1], w_sg)
+    U = gemm_grouped_w4a4(a, row_idx, offsets, up[0], up[1], w_sg)
+    return silu(G) * U
+
+
+def moe_down_combine(h, offsets, w_codes, w_scales, w_sg, token_idx, gate_w, T, y0=None):
+    """Expert down projection and gate-weighted combine.
+
+    h: (codes, scales, s_g) of the routed rows [R, I]; offsets int64 [E+1];
+    w_codes/w_scales/w_sg: the experts' down weights as for
+    gemm_grouped_w4a4; token_idx int32 [R] (token of routed row j); gate_w
+    float32 [R] (routing weight of routed row j); T tokens.
+    Returns y float64 [T, N]: y0 (or zeros) plus, for every routed row j,
+    gate_w[j] * (h[j] W_e(j)^T) added to row token_idx[j]."""
+    D = gemm_grouped_w4a4(h, None, offsets, w_codes, w_scales, w_sg)
+    R = D.shape[0]
+    tok = _c(token_idx, np.int32)[:R].astype(np.int64)
+    g = _c(gate_w, np.float32)[:R].astype(np.float64)
+    if R and (tok.min() < 0 or tok.max() >= T):
+        raise OracleError("token index out of range")
+    y = np.zeros((T, D.shape[1]), np.float64) if y0 is None else np.array(y0, np.float64, copy=True)
+    np.add.at(y, tok, g[:, None] * D)
+    return y
+
+
 def threads():
     """OpenMP threads the oracle's parallel loops use."""
     return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))

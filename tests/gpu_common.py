@@ -4,6 +4,7 @@ import numpy as np
 import torch
 
 import nvfp4_block_scaled_30_b300 as nv
+import oracle
 from helpers import tile_scales, untile_scales
 
 
@@ -29,6 +30,24 @@ def quantize_gpu(bits: np.ndarray, mode=nv.SCALE_TENSOR_FP32, layout=nv.LAYOUT_M
     if mode == nv.SCALE_MACRO_FP16:
         second = second.view(np.uint16)
     return t, codes, scales, second
+
+
+def quantize_pinned(bits: np.ndarray, mode=nv.SCALE_TENSOR_FP32, ws=None):
+    """GPU NVFP4 encode (MMA-tiled scales) of BF16 bits, checked bit for bit
+    against the oracle's encode of the same bits.  Returns the device tensor
+    and the ORACLE's (codes, row-major scales, second), so that every
+    reference a test computes from them starts from oracle values only."""
+    t, codes, scales, second = quantize_gpu(bits, mode, nv.LAYOUT_MMA_TILED, ws)
+    if mode == nv.SCALE_TENSOR_FP32:
+        oc, os_, og = oracle.nvfp4_encode(bits)
+        osec = np.array([og], np.float32)
+        assert second.view(np.uint32)[0] == osec.view(np.uint32)[0], "tensor scale differs from the oracle's"
+    else:
+        oc, os_, osec = oracle.nvfp4_encode_macro(bits)
+        np.testing.assert_array_equal(second, osec)
+    np.testing.assert_array_equal(codes, oc)
+    np.testing.assert_array_equal(scales, os_)
+    return t, oc, os_, osec
 
 
 def nvfp4_device(codes: np.ndarray, scales_rm: np.ndarray, second, rows: int, K: int,

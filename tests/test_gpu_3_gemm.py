@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import synth
-from gpu_common import dev_bf16, host, nv, nvfp4_device, quantize_gpu, y_np
+from gpu_common import dev_bf16, host, nv, nvfp4_device, quantize_pinned, y_np
 from helpers import row_tolerance_ok
 
 pytestmark = pytest.mark.gpu
@@ -101,7 +101,7 @@ def _check(y, ref, what, bf16=True):
 @pytest.mark.parametrize("out_dtype", [nv.OUT_BF16, nv.OUT_FP32])
 def test_config1_full(out_dtype):
     xb, wb = _layer(1, 128, 256, 512)
-    w, wc, ws, wg = quantize_gpu(wb)
+    w, wc, ws, wg = quantize_pinned(wb)
     oc, os_, og = oracle.nvfp4_encode(wb)
     np.testing.assert_array_equal(wc, oc)
     np.testing.assert_array_equal(ws, os_)
@@ -109,7 +109,7 @@ def test_config1_full(out_dtype):
     ref = oracle.gemm_w4a4(oracle.nvfp4_encode(xb), (oc, os_, og))
     _check(y_np(y), ref, "config 1", out_dtype == nv.OUT_BF16)
     # the pre-quantised activation path gives the same numbers
-    a, *_ = quantize_gpu(xb)
+    a, *_ = quantize_pinned(xb)
     y2 = nv.gemm(w, a_q=a, out_dtype=out_dtype)
     np.testing.assert_array_equal(y_np(y2), y_np(y))
 
@@ -117,7 +117,7 @@ def test_config1_full(out_dtype):
 @pytest.fixture(scope="module")
 def w_28672():
     wb = synth.weights(2, 1, 28672, 8192)
-    w, wc, ws, wg = quantize_gpu(wb)
+    w, wc, ws, wg = quantize_pinned(wb)
     return w, (wc, ws, wg[0])
 
 
@@ -136,7 +136,7 @@ def test_prefill_sampled_rows(w_28672, N):
         w, wq = w_28672
     else:
         wb = synth.weights(3, 1, 8192, 8192)
-        w, wc, ws, wg = quantize_gpu(wb)
+        w, wc, ws, wg = quantize_pinned(wb)
         wq = (wc, ws, wg[0])
     xb = synth.activations(3, 0, 4096, 8192, 0.005, 100.0)
     y = y_np(nv.gemm(w, x=dev_bf16(xb)))
@@ -151,7 +151,7 @@ def test_prefill_sampled_rows(w_28672, N):
 def test_ragged_shapes(M, N, K, out_dtype):
     xb = synth.activations(9, 10, M, K, 0.01, 50.0)
     wb = synth.weights(9, 11, N, K)
-    w, wc, ws, wg = quantize_gpu(wb)
+    w, wc, ws, wg = quantize_pinned(wb)
     y = nv.gemm(w, x=dev_bf16(xb), out_dtype=out_dtype)
     ref = oracle.gemm_w4a4(oracle.nvfp4_encode(xb), (wc, ws, wg[0]))
     _check(y_np(y), ref, f"{M}x{N}x{K}", out_dtype == nv.OUT_BF16)
@@ -159,7 +159,7 @@ def test_ragged_shapes(M, N, K, out_dtype):
 
 def test_output_row_stride_and_empty():
     xb, wb = _layer(1, 40, 256, 512)
-    w, wc, ws, wg = quantize_gpu(wb)
+    w, wc, ws, wg = quantize_pinned(wb)
     big = torch.full((40, 300), 7.0, dtype=torch.bfloat16, device="cuda")
     nv.gemm(w, x=dev_bf16(xb), y=big[:, :256])
     ref = oracle.gemm_w4a4(oracle.nvfp4_encode(xb), (wc, ws, wg[0]))
@@ -178,7 +178,7 @@ def test_output_row_stride_and_empty():
 def test_streamk_shapes(M, N, K):
     xb = synth.activations(9, 40, M, K, 0.01, 50.0)
     wb = synth.weights(9, 41, N, K)
-    w, wc, ws, wg = quantize_gpu(wb)
+    w, wc, ws, wg = quantize_pinned(wb)
     work = nv.Workspace(nv.workspace_size(nv.OP_GEMM, M, N, K))
     x = dev_bf16(xb)
     y1 = y_np(nv.gemm(w, x=x, ws=work, out_dtype=nv.OUT_FP32))
@@ -191,7 +191,7 @@ def test_streamk_shapes(M, N, K):
 
 def test_streamk_m128_sampled_rows():
     wb = synth.weights(9, 43, 4096, 8192)
-    w, wc, ws, wg = quantize_gpu(wb)
+    w, wc, ws, wg = quantize_pinned(wb)
     xb = synth.activations(2, 5, 128, 8192, 0.005, 100.0)
     y = y_np(nv.gemm(w, x=dev_bf16(xb)))
     rows = np.array([0, 1, 31, 32, 63, 64, 100, 127])

@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import synth
-from gpu_common import dev_bf16, host, nv, nvfp4_device, quantize_gpu, y_np
+from gpu_common import dev_bf16, host, nv, nvfp4_device, quantize_pinned, y_np
 from helpers import row_tolerance_ok
 
 pytestmark = pytest.mark.gpu
@@ -59,7 +59,7 @@ def test_all_fp8_codes_times_all_weight_codes_exact():
 def test_w4a8_route_against_oracle(M, N, K):
     xb = synth.activations(4, 20, M, K, 0.01, 50.0)
     wb = synth.weights(4, 21, N, K)
-    w, wc, ws, wg = quantize_gpu(wb)
+    w, wc, ws, wg = quantize_pinned(wb)
     y = nv.gemm(w, x=dev_bf16(xb), policy=nv.POLICY_Q8)   # per-token FP8 quantiser + W4A8 GEMM
     a8, st = oracle.fp8_token_encode(xb)
     rows = np.arange(M) if M <= 300 else np.concatenate([[0, M - 1], np.random.default_rng(M).choice(M, 30, replace=False)])

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import synth
-from gpu_common import dev_bf16, host, nv, quantize_gpu, y_np
+from gpu_common import dev_bf16, host, nv, quantize_pinned, y_np
 from helpers import row_tolerance_ok
 
 pytestmark = pytest.mark.gpu
@@ -24,7 +24,7 @@ def stacked_weights(E, N, K, tid):
     dev_codes, dev_scales = [], []
     for e in range(E):
         wb = synth.weights(5, tid * 1000 + e, N, K)
-        t, c, s, g = quantize_gpu(wb)
+        t, c, s, g = quantize_pinned(wb)
         codes.append(c)
         scales.append(s)
         sgs.append(g[0])
@@ -55,7 +55,7 @@ def test_moe_up_projection(up_weights):
     w, wc, ws, wg = up_weights
     row_idx, offsets, counts, _ = synth.moe_routing()
     xb = synth.activations(5, 0, C5["T"], C5["H"], C5["outlier_frac"], C5["outlier_factor"])
-    a, ac, as_, ag = quantize_gpu(xb)
+    a, ac, as_, ag = quantize_pinned(xb)
     T = int(offsets[-1])
     y = nv.grouped_gemm(a, torch.from_numpy(offsets).cuda(), w, C5["inter"], T,
                         row_idx=torch.from_numpy(row_idx).cuda())
@@ -71,7 +71,7 @@ def test_moe_down_projection():
     row_idx, offsets, counts, _ = synth.moe_routing()
     T = int(offsets[-1])
     xb = synth.activations(5, 2, T, K, C5["outlier_frac"], C5["outlier_factor"])
-    a, ac, as_, ag = quantize_gpu(xb)
+    a, ac, as_, ag = quantize_pinned(xb)
     y = nv.grouped_gemm(a, torch.from_numpy(offsets).cuda(), w, N, T)
     yn = y_np(y)
     order = np.argsort(counts)
@@ -85,7 +85,7 @@ def test_small_full_with_empty_experts(indexed):
     counts = np.array([0, 37, 0, 1, 130, 0])
     w, wc, ws, wg = stacked_weights(E, N, K, 3)
     xb = synth.activations(9, 30, T if indexed else int(counts.sum()), K, 0.01, 50.0)
-    a, ac, as_, ag = quantize_gpu(xb)
+    a, ac, as_, ag = quantize_pinned(xb)
     if indexed:
         row_idx, offsets = synth.moe_routing_from_counts(np.minimum(counts, T), T)
     else:
@@ -104,7 +104,7 @@ def test_heavy_zipf_routing(up_weights):
     row_idx, offsets, counts, _ = synth.moe_routing(literal=True)
     assert counts.max() > 1000
     xb = synth.activations(5, 0, C5["T"], C5["H"], C5["outlier_frac"], C5["outlier_factor"])
-    a, ac, as_, ag = quantize_gpu(xb)
+    a, ac, as_, ag = quantize_pinned(xb)
     y = nv.grouped_gemm(a, torch.from_numpy(offsets).cuda(), w, C5["inter"], int(offsets[-1]),
                         row_idx=torch.from_numpy(row_idx).cuda())
     e_big = int(np.argmax(counts))

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 import synth
-from gpu_common import dev_bf16, host, nv, quantize_gpu, y_np
+from gpu_common import dev_bf16, host, nv, quantize_pinned, y_np
 from helpers import row_tolerance_ok
 
 pytestmark = pytest.mark.gpu
@@ -21,7 +21,7 @@ def stack():
     layers = []
     for i in range(C4["layers"]):
         wb = synth.weights(4, 100 + i, C4["N"], C4["K"])
-        t, c, s, g = quantize_gpu(wb)
+        t, c, s, g = quantize_pinned(wb)
         layers.append((t, (c, s, g[0])))
     return layers
 

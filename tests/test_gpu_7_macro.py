@@ -8,7 +8,7 @@ import torch
 
 import oracle
 import synth
-from gpu_common import dev_bf16, host, nv, quantize_gpu, y_np
+from gpu_common import dev_bf16, host, nv, quantize_pinned, y_np
 from helpers import row_tolerance_ok
 
 pytestmark = pytest.mark.gpu
@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 def _macro_case(M, N, K, xcfg=1, seed=60):
     xb = synth.activations(9, seed, M, K, 0.01, 50.0)
     wb = synth.weights(9, seed + 1, N, K)
-    w, wc, ws, wm = quantize_gpu(wb, mode=nv.SCALE_MACRO_FP16)
+    w, wc, ws, wm = quantize_pinned(wb, mode=nv.SCALE_MACRO_FP16)
     ow = oracle.nvfp4_encode_macro(wb)
     np.testing.assert_array_equal(wc, ow[0])
     np.testing.assert_array_equal(ws, ow[1])
@@ -34,7 +34,7 @@ def test_macro_gemm_against_oracle(M, N, K, out_dtype):
     ok, worst = row_tolerance_ok(y_np(y), ref, out_bf16=out_dtype == nv.OUT_BF16)
     assert ok, f"{M}x{N}x{K}: {worst}"
     # pre-quantised activations give the same result
-    a, *_ = quantize_gpu(xb, mode=nv.SCALE_MACRO_FP16)
+    a, *_ = quantize_pinned(xb, mode=nv.SCALE_MACRO_FP16)
     y2 = nv.gemm(w, a_q=a, out_dtype=out_dtype)
     np.testing.assert_array_equal(y_np(y2), y_np(y))
 
@@ -54,8 +54,8 @@ def test_equal_macro_scales_reduce_to_tensor_scale_path():
     M, N, K = 128, 256, 512
     xb = synth.activations(9, 64, M, K, 0.01, 50.0)
     wb = synth.weights(9, 65, N, K)
-    a, *_ = quantize_gpu(xb)
-    w, *_ = quantize_gpu(wb)
+    a, *_ = quantize_pinned(xb)
+    w, *_ = quantize_pinned(wb)
     y_t = y_np(nv.gemm(w, a_q=a, out_dtype=nv.OUT_FP32))
     a_s, w_s = float(host(a.second)[0]), float(host(w.second)[0])
     # force exact power-of-two tensor scales so FP16 holds them exactly

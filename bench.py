@@ -367,6 +367,57 @@ def workload_moe(c, steps, warmup):
             "counts_max": int(counts.max()), "device_status": work.status()}
 
 
+def workload_moe_ffn(c, steps, warmup):
+    """The mixture-of-experts feed-forward block with every fusion: the BF16
+    tokens quantised once, the grouped up projection gathering token rows and
+    applying SwiGLU in its epilogue, written as NVFP4 under a calibrated
+    static scale, then the grouped down projection adding each routed row,
+    times its routing weight, into its token's FP32 output row."""
+    t, nv = c.torch, c.nv
+    cfg = synth.CONFIGS[5]
+    T, H, E, I = cfg["T"], cfg["H"], cfg["E"], cfg["inter"]
+    row_idx, offsets, counts, logits = synth.moe_routing()
+    R = int(offsets[-1])
+    gate_w = synth.moe_gate_weights(logits, row_idx, offsets, cfg["topk"])
+
+    def stacked(N, K, tid):
+        parts = [c.quantized_weights(synth.weights(5, tid * 1000 + e, N, K))[0] for e in range(E)]
+        return nv.NVFP4Tensor(t.cat([p.codes for p in parts]), t.cat([p.scales for p in parts]),
+                              t.cat([p.second for p in parts]), E * N, K)
+
+    # random-init weights: the gate/up interleave is a row permutation of
+    # i.i.d. rows, so drawing the stacked [2I, H] block directly is the same
+    w_gu, w_dn = stacked(2 * I, H, 6), stacked(H, I, 7)
+    x = c.bf16(synth.activations(5, 0, T, H, cfg["outlier_frac"], cfg["outlier_factor"]))
+    off = t.from_numpy(offsets).to(c.dev)
+    ridx = t.from_numpy(row_idx).to(c.dev)
+    gw = t.from_numpy(gate_w).to(c.dev)
+    y = t.zeros((T, H), dtype=t.float32, device=c.dev)
+    work = nv.Workspace(max(nv.workspace_size(nv.OP_QUANTIZE, T, 0, H),
+                            nv.workspace_size(nv.OP_GROUPED_GEMM, R, 2 * I, H, E)))
+    a = nv.quantize(x, ws=work)
+    s_h = t.ones(1, dtype=t.float32, device=c.dev)
+    amax = t.zeros(1, dtype=t.float32, device=c.dev)
+    h_q = nv.empty_nvfp4(R, I, device=c.dev)
+    nv.moe_up_swiglu(a, off, w_gu, I, R, row_idx=ridx, s_h=s_h, h_amax=amax, h_q=h_q, ws=work)
+    s_h.copy_(amax / 2688.0)                 # calibration
+    t.cuda.synchronize()
+
+    def step(i):
+        nv.quantize(x, out=a, ws=work)
+        nv.moe_up_swiglu(a, off, w_gu, I, R, row_idx=ridx, s_h=s_h, h_q=h_q, ws=work)
+        y.zero_()
+        nv.moe_down_combine(h_q, off, w_dn, H, ridx, gw, y, ws=work)
+
+    ms = c.time(step, steps, warmup)
+    wbytes = E * (nvfp4_bytes(2 * I, H) + nvfp4_bytes(H, I))
+    step_bytes = (wbytes + T * H * 2 + 2 * nvfp4_bytes(T, H) + 2 * nvfp4_bytes(R, I)  # x, a, h
+                  + 2 * T * H * 4)                                                    # y zero + combine
+    flops = 6.0 * R * H * I
+    return {"ms": ms, "bytes": step_bytes, "value": step_bytes / (ms * 1e-3) / 1e9, "launches_per_step": 5,
+            "tflops": flops / (ms * 1e-3) / 1e12, "device_status": work.status()}
+
+
 # ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
 def oracle_decode_sample(M=8, n_rows=2048, reps=1):
     """The oracle's decode step (encode X, dequantise-and-contract in FP64)
@@ -501,6 +552,9 @@ def main():
                                               "routes": q["routes"]}
         fq = workload_fused_stack(c, min(es, 20), 2)
         extras["policy_stack_q4_fused"] = {"value": fq["value"], "unit": "TFLOP/s", "ms": fq["ms"]}
+        mf = workload_moe_ffn(c, min(es, 50), 2)
+        extras["moe_ffn_fused"] = {"value": mf["value"], "unit": "GB/s", "ms": mf["ms"], "tflops": mf["tflops"],
+                                   "frac_hbm": mf["value"] / hbm}
         mo = workload_moe(c, min(es, 50), 2)
         extras["moe_grouped"] = {"value": mo["value"], "unit": "GB/s", "ms": mo["ms"], "tflops": mo["tflops"],
                                  "frac_hbm": mo["value"] / hbm, "counts": [mo["counts_min"], mo["counts_max"]]}

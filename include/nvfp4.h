@@ -240,6 +240,56 @@ nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor *a, const int32_t *row_idx,
                                 int64_t total_rows, int32_t policy, int32_t sensitive,
                                 void *ws, size_t ws_bytes, nvfp4_stream_t stream);
 
+/* ---- mixture-of-experts feed-forward: fused epilogues of the grouped GEMM ----
+ * The pages run MoE models (Qwen3 MoE) through the NVFP4 path ([LCP], MoE
+ * operations; [ADA], model list) without printing the expert formula; the
+ * reading taken is the SwiGLU expert of those models,
+ *   h = SiLU(x W_gate^T) * (x W_up^T),  SiLU(v) = v / (1 + exp(-v)),
+ *   y(t) = sum over the routed rows j of token t of g_j * (h_j W_down^T),
+ * with both products the grouped W4A4 contraction of nvfp4_grouped_gemm
+ * (same a / row_idx / expert_offsets / E / total_rows conventions; W4A4
+ * route, TENSOR_FP32 only). */
+
+/* Up projection with the SwiGLU fused into the epilogue.
+ *  w_gate_up: the E experts' gate and up weights [I, K] each, stacked as one
+ *    NVFP4 tensor [E * 2I, K] (one tensor scale per expert, second =
+ *    float[E], MMA_TILED) in which expert e's rows e*2I + 256b + r hold gate
+ *    row 128b + r for r < 128 and up row 128b + r - 128 for r >= 128 (gate
+ *    and up interleaved in 128-row blocks).  I % 128 == 0.
+ *  Output, exactly one of:
+ *    h [total_rows, I] BF16/FP32 (h_dtype), row stride ldh elements with
+ *      ldh * element size % 16 == 0, 16-byte aligned;
+ *    h_q: NVFP4 [total_rows, I] (rows == total_rows, K == I, TENSOR_FP32,
+ *      MMA_TILED) encoded as nvfp4_gemm_nvfp4_out does under the given
+ *      device tensor scale h_q->second, with h_amax (optional) updated to
+ *      max(*h_amax, max|h|); padding-row scales are zeroed.  Ready to be the
+ *      `h` of nvfp4_moe_down_combine.
+ *  Row j of the output is routed row j (expert e owns offsets[e] ..
+ *  offsets[e+1]-1); rows past offsets[E] are untouched. */
+nvfp4_status nvfp4_moe_up_swiglu(const nvfp4_tensor *a, const int32_t *row_idx,
+                                 const int64_t *expert_offsets, int32_t E,
+                                 const nvfp4_tensor *w_gate_up, int64_t I, void *h, int64_t ldh,
+                                 int32_t h_dtype, nvfp4_tensor *h_q, float *h_amax,
+                                 int64_t total_rows, void *ws, size_t ws_bytes,
+                                 nvfp4_stream_t stream);
+
+/* Down projection with the gate-weighted combine fused into the epilogue:
+ *   y[token_idx[j], :] += gate_w[j] * (h[j, :] W_{e(j)}^T)
+ * for every routed row j < offsets[E], e(j) the expert owning row j.
+ *  h: NVFP4 routed rows [total_rows, I] (TENSOR_FP32, MMA_TILED), read in
+ *    order (no index list).  w_down: [E * N, I] stacked, N % 128 == 0.
+ *  token_idx: device int32[total_rows], values in [0, T) (rows with other
+ *    values add nothing); gate_w: device float[total_rows].
+ *  y: FP32 [T, N], row stride ldy (ldy % 4 == 0, 16-byte aligned), holding
+ *    the value to add to (zeros, or the residual stream).  The additions are
+ *    atomic and their order is unspecified, so the last bits of y may vary
+ *    from run to run. */
+nvfp4_status nvfp4_moe_down_combine(const nvfp4_tensor *h, const int64_t *expert_offsets, int32_t E,
+                                    const nvfp4_tensor *w_down, int64_t N,
+                                    const int32_t *token_idx, const float *gate_w, float *y,
+                                    int64_t ldy, int64_t T, int64_t total_rows, void *ws,
+                                    size_t ws_bytes, nvfp4_stream_t stream);
+
 /* ---- no-allocation variant --------------------------------------------------- */
 
 /* W4A4 product Y[M, N] = A[M, K] * W[N, K]^T of pre-quantised NVFP4

@@ -31,7 +31,8 @@ OP_QUANTIZE, OP_QUANTIZE_FP8, OP_GEMM, OP_W4A8_GEMM, OP_GROUPED_GEMM = range(5)
 EXPORTED = ["nvfp4_scale_bytes", "nvfp4_workspace_size", "nvfp4_workspace_init", "nvfp4_device_status",
             "nvfp4_policy_route", "nvfp4_quantize", "nvfp4_quantize_fp8", "nvfp4_gemm", "nvfp4_w4a8_gemm",
             "nvfp4_grouped_gemm", "nvfp4_probe_convert", "nvfp4_sm_count", "nvfp4_version",
-            "nvfp4_gemm_w4a4_noalloc", "nvfp4_gemm_nvfp4_out"]
+            "nvfp4_gemm_w4a4_noalloc", "nvfp4_gemm_nvfp4_out", "nvfp4_moe_up_swiglu",
+            "nvfp4_moe_down_combine"]
 
 
 class NVFP4Error(RuntimeError):
@@ -74,6 +75,10 @@ def lib():
             "nvfp4_probe_convert": (_I32, [_VP, _I64, _VP, _VP, _VP]),
             "nvfp4_gemm_w4a4_noalloc": (_I32, [_PT, _PT, _VP, _I64, _I32, _VP]),
             "nvfp4_gemm_nvfp4_out": (_I32, [_VP, _I64, _PT, _PT, _PT, _VP, _I64, _VP, _SZ, _VP]),
+            "nvfp4_moe_up_swiglu": (_I32, [_PT, _VP, _VP, _I32, _PT, _I64, _VP, _I64, _I32, _PT, _VP, _I64,
+                                           _VP, _SZ, _VP]),
+            "nvfp4_moe_down_combine": (_I32, [_PT, _VP, _I32, _PT, _I64, _VP, _VP, _VP, _I64, _I64, _I64,
+                                              _VP, _SZ, _VP]),
             "nvfp4_sm_count": (_I32, []),
             "nvfp4_version": (ctypes.c_char_p, []),
         }
@@ -310,3 +315,53 @@ def probe_convert(v: torch.Tensor, stream=None):
 
 def version() -> str:
     return lib().nvfp4_version().decode()
+
+
+def moe_up_swiglu(a: NVFP4Tensor, offsets: torch.Tensor, w_gate_up: NVFP4Tensor, I: int, total_rows: int,
+                  row_idx: Optional[torch.Tensor] = None, out_dtype: int = OUT_BF16,
+                  h: Optional[torch.Tensor] = None, s_h: Optional[torch.Tensor] = None,
+                  h_amax: Optional[torch.Tensor] = None, h_q: Optional[NVFP4Tensor] = None,
+                  ws: Optional[Workspace] = None, stream=None):
+    """nvfp4_moe_up_swiglu: SiLU(gate) * up of the routed rows.  With s_h
+    (float32 [1] device tensor scale) the output is NVFP4 (returned as an
+    NVFP4Tensor); otherwise a BF16/FP32 [total_rows, I] tensor."""
+    assert offsets.dtype == torch.int64 and (row_idx is None or row_idx.dtype == torch.int32)
+    E = offsets.numel() - 1
+    dev = a.codes.device
+    hd = None
+    if s_h is not None:
+        if h_q is None:
+            h_q = empty_nvfp4(total_rows, I, device=dev)
+        h_q.second = s_h
+        result = h_q
+    else:
+        h = _out(h, total_rows, I, out_dtype, dev)
+        result = h
+    if total_rows == 0:
+        return result
+    ws = _ws(ws, workspace_size(OP_GROUPED_GEMM, total_rows, 2 * I, a.K, E), dev)
+    ad, wd = a.desc(), w_gate_up.desc()
+    if s_h is not None:
+        hd = h_q.desc()
+    _check(lib().nvfp4_moe_up_swiglu(ctypes.byref(ad), _ptr(row_idx), _ptr(offsets), E, ctypes.byref(wd), I,
+                                     _ptr(h), h.stride(0) if h is not None else 0, out_dtype,
+                                     ctypes.byref(hd) if hd is not None else None, _ptr(h_amax), total_rows,
+                                     ws.ptr, ws.nbytes, _stream(stream)), "nvfp4_moe_up_swiglu")
+    return result
+
+
+def moe_down_combine(h: NVFP4Tensor, offsets: torch.Tensor, w_down: NVFP4Tensor, N: int,
+                     token_idx: torch.Tensor, gate_w: torch.Tensor, y: torch.Tensor,
+                     ws: Optional[Workspace] = None, stream=None) -> torch.Tensor:
+    """nvfp4_moe_down_combine: y[token_idx[j]] += gate_w[j] * (h[j] W_e^T) into
+    the FP32 [T, N] tensor y (which holds zeros or the residual)."""
+    assert offsets.dtype == torch.int64 and token_idx.dtype == torch.int32 and gate_w.dtype == torch.float32
+    assert y.dtype == torch.float32 and y.stride(1) == 1
+    E = offsets.numel() - 1
+    R = h.rows
+    ws = _ws(ws, workspace_size(OP_GROUPED_GEMM, R, N, h.K, E), h.codes.device)
+    hd, wd = h.desc(), w_down.desc()
+    _check(lib().nvfp4_moe_down_combine(ctypes.byref(hd), _ptr(offsets), E, ctypes.byref(wd), N,
+                                        _ptr(token_idx), _ptr(gate_w), _ptr(y), y.stride(0), y.shape[0], R,
+                                        ws.ptr, ws.nbytes, _stream(stream)), "nvfp4_moe_down_combine")
+    return y

@@ -516,16 +516,13 @@ nvfp4_status nvfp4_gemm_nvfp4_out(const void *x_bf16, int64_t ldx, const nvfp4_t
                           x_bf16 != nullptr, s, y_q, y_amax);
 }
 
-nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor *a, const int32_t *row_idx, const int64_t *expert_offsets,
-                                int32_t E, const nvfp4_tensor *w, int64_t N, void *y, int64_t ldy, int32_t y_dtype,
-                                int64_t total_rows, int32_t policy, int32_t sensitive, void *ws,
-                                size_t ws_bytes, nvfp4_stream_t stream)
+// Checks shared by the grouped entry points (activations, stacked weights of
+// E experts with n_rows rows each, offsets, index list) and the argument
+// block they fill.
+static nvfp4_status grouped_args(const nvfp4_tensor *a, const int32_t *row_idx, const int64_t *expert_offsets,
+                                 int32_t E, const nvfp4_tensor *w, int64_t n_rows, int64_t total_rows, void *ws,
+                                 size_t ws_bytes, GroupedGemmArgs &g)
 {
-    const int32_t route = nvfp4_policy_route(policy, sensitive);
-    if (route < 0)
-        return NVFP4_ERR_INVALID_ARG;
-    if (route == 8)
-        return NVFP4_ERR_UNSUPPORTED; // grouped W4A8 is not implemented
     nvfp4_status st = check_tensor(a, true);
     if (st != NVFP4_OK)
         return st;
@@ -535,9 +532,9 @@ nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor *a, const int32_t *row_idx, c
         return NVFP4_ERR_UNSUPPORTED;
     if (E <= 0 || E > 1024 || !expert_offsets || !aligned(expert_offsets, 8))
         return NVFP4_ERR_INVALID_ARG;
-    if (N <= 0 || N % 128 != 0)
+    if (n_rows <= 0 || n_rows % 128 != 0)
         return NVFP4_ERR_UNSUPPORTED_SHAPE;
-    if (w->rows != (int64_t)E * N || w->K != a->K)
+    if (w->rows != (int64_t)E * n_rows || w->K != a->K)
         return NVFP4_ERR_INVALID_ARG;
     if (total_rows < 0 || total_rows > MAX_DIM)
         return NVFP4_ERR_INVALID_ARG;
@@ -545,13 +542,9 @@ nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor *a, const int32_t *row_idx, c
         return NVFP4_ERR_INVALID_ARG;
     if (row_idx != nullptr && !aligned(row_idx, 4))
         return NVFP4_ERR_INVALID_ARG;
-    if ((st = check_out(y, ldy, y_dtype, N)) != NVFP4_OK)
+    if ((st = check_ws(ws, ws_bytes, ws_layout(NVFP4_OP_GROUPED_GEMM, total_rows, n_rows, a->K).total)) != NVFP4_OK)
         return st;
-    if ((st = check_ws(ws, ws_bytes, ws_layout(NVFP4_OP_GROUPED_GEMM, total_rows, N, a->K).total)) != NVFP4_OK)
-        return st;
-    if (total_rows == 0)
-        return NVFP4_OK;
-    GroupedGemmArgs g{};
+    g = GroupedGemmArgs{};
     g.a_codes = static_cast<const uint8_t *>(a->codes);
     g.a_scales = static_cast<const uint8_t *>(a->scales);
     g.a_second = static_cast<const float *>(a->second);
@@ -562,14 +555,112 @@ nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor *a, const int32_t *row_idx, c
     g.w_codes = static_cast<const uint8_t *>(w->codes);
     g.w_scales = static_cast<const uint8_t *>(w->scales);
     g.w_second = static_cast<const float *>(w->second);
-    g.N = N;
+    g.N = n_rows;
     g.K = a->K;
-    g.out = y;
-    g.ldy = ldy;
-    g.out_dtype = y_dtype;
     g.total_rows = total_rows;
     g.status = status_word(ws);
     g.timeout_ns = DEFAULT_TIMEOUT_NS;
+    g.epi = EPI_PLAIN;
+    return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor *a, const int32_t *row_idx, const int64_t *expert_offsets,
+                                int32_t E, const nvfp4_tensor *w, int64_t N, void *y, int64_t ldy, int32_t y_dtype,
+                                int64_t total_rows, int32_t policy, int32_t sensitive, void *ws,
+                                size_t ws_bytes, nvfp4_stream_t stream)
+{
+    const int32_t route = nvfp4_policy_route(policy, sensitive);
+    if (route < 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (route == 8)
+        return NVFP4_ERR_UNSUPPORTED; // grouped W4A8 is not implemented
+    GroupedGemmArgs g;
+    nvfp4_status st = grouped_args(a, row_idx, expert_offsets, E, w, N, total_rows, ws, ws_bytes, g);
+    if (st != NVFP4_OK)
+        return st;
+    if ((st = check_out(y, ldy, y_dtype, N)) != NVFP4_OK)
+        return st;
+    if (total_rows == 0)
+        return NVFP4_OK;
+    g.out = y;
+    g.ldy = ldy;
+    g.out_dtype = y_dtype;
+    return from_cuda(launch_w4a4_grouped(g, (cudaStream_t)stream));
+}
+
+nvfp4_status nvfp4_moe_up_swiglu(const nvfp4_tensor *a, const int32_t *row_idx, const int64_t *expert_offsets,
+                                 int32_t E, const nvfp4_tensor *w_gate_up, int64_t I, void *h, int64_t ldh,
+                                 int32_t h_dtype, nvfp4_tensor *h_q, float *h_amax, int64_t total_rows, void *ws,
+                                 size_t ws_bytes, nvfp4_stream_t stream)
+{
+    if ((h == nullptr) == (h_q == nullptr) || I <= 0 || I % 128 != 0)
+        return I > 0 && I % 128 != 0 ? NVFP4_ERR_UNSUPPORTED_SHAPE : NVFP4_ERR_INVALID_ARG;
+    GroupedGemmArgs g;
+    nvfp4_status st = grouped_args(a, row_idx, expert_offsets, E, w_gate_up, 2 * I, total_rows, ws, ws_bytes, g);
+    if (st != NVFP4_OK)
+        return st;
+    if (h) {
+        if ((st = check_out(h, ldh, h_dtype, I)) != NVFP4_OK)
+            return st;
+        if ((ldh * (h_dtype == NVFP4_OUT_BF16 ? 2 : 4)) % 16 != 0)
+            return NVFP4_ERR_INVALID_ARG;
+    } else {
+        if ((st = check_tensor(h_q, true)) != NVFP4_OK)
+            return st;
+        if (h_q->mode != NVFP4_SCALE_TENSOR_FP32 || h_q->rows != total_rows || h_q->K != I)
+            return NVFP4_ERR_INVALID_ARG;
+        if (h_amax && !aligned(h_amax, 4))
+            return NVFP4_ERR_INVALID_ARG;
+    }
+    if (total_rows == 0)
+        return NVFP4_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    g.epi = EPI_SWIGLU;
+    if (h) {
+        g.out = h;
+        g.ldy = ldh;
+        g.out_dtype = h_dtype;
+    } else {
+        g.yq_codes = static_cast<uint8_t *>(h_q->codes);
+        g.yq_scales = static_cast<uint8_t *>(h_q->scales);
+        g.yq_scale = static_cast<const float *>(h_q->second);
+        g.yq_amax = reinterpret_cast<uint32_t *>(h_amax);
+        g.out_dtype = NVFP4_OUT_FP32;
+        if (total_rows % 128 != 0) {
+            // the last 128-row scale tile holds padding rows: zero it, the
+            // kernel then writes the rows that exist
+            const size_t atom_row = (size_t)(I / 64) * 512;
+            if (cudaMemsetAsync(g.yq_scales + (size_t)(total_rows / 128) * atom_row, 0, atom_row, s) != cudaSuccess)
+                return NVFP4_ERR_CUDA;
+        }
+    }
+    return from_cuda(launch_w4a4_grouped(g, s));
+}
+
+nvfp4_status nvfp4_moe_down_combine(const nvfp4_tensor *h, const int64_t *expert_offsets, int32_t E,
+                                    const nvfp4_tensor *w_down, int64_t N, const int32_t *token_idx,
+                                    const float *gate_w, float *y, int64_t ldy, int64_t T, int64_t total_rows,
+                                    void *ws, size_t ws_bytes, nvfp4_stream_t stream)
+{
+    GroupedGemmArgs g;
+    nvfp4_status st = grouped_args(h, nullptr, expert_offsets, E, w_down, N, total_rows, ws, ws_bytes, g);
+    if (st != NVFP4_OK)
+        return st;
+    if (T < 0 || T > MAX_DIM || !token_idx || !gate_w || !aligned(token_idx, 4) || !aligned(gate_w, 4))
+        return NVFP4_ERR_INVALID_ARG;
+    if ((st = check_out(y, ldy, NVFP4_OUT_FP32, N)) != NVFP4_OK)
+        return st;
+    if (ldy % 4 != 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (total_rows == 0 || T == 0)
+        return NVFP4_OK;
+    g.epi = EPI_COMBINE;
+    g.out = y;
+    g.ldy = ldy;
+    g.out_dtype = NVFP4_OUT_FP32;
+    g.comb_idx = token_idx;
+    g.comb_w = gate_w;
+    g.comb_rows = T;
     return from_cuda(launch_w4a4_grouped(g, (cudaStream_t)stream));
 }
 

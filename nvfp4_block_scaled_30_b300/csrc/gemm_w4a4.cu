@@ -105,11 +105,16 @@ struct Params {
     // codes [a_rows][b_rows/2], MMA-tiled scales, under the given tensor
     // scale; the largest |Y| is max-reduced into yq_amax when it is set
     int32_t out_q;
+    int64_t yq_n;            // columns of the NVFP4 output
     uint8_t *yq_codes;
     uint8_t *yq_scales;
     const float *yq_scale;
     uint32_t *yq_amax;
     // grouped mode
+    int32_t epi;             // EPI_PLAIN, EPI_SWIGLU or EPI_COMBINE
+    const int32_t *comb_idx; // combine: token of each routed row
+    const float *comb_w;     // combine: routing weight of each routed row
+    int64_t comb_rows;       // combine: token rows of the output
     const int64_t *offsets;
     const int32_t *row_idx;
     int32_t E;
@@ -356,32 +361,28 @@ __device__ __forceinline__ void store_chunk(const Params &p, const uint32_t (&v)
     }
 }
 
-// NVFP4 store of 32 consecutive outputs of row i (two 16-element blocks):
-// y = alpha * acc exactly as the FP32 output path computes it, then the block
-// encode of the quantisers under the given tensor scale s: 8 code bytes and
-// one MMA-tiled scale byte per block.  Returns the largest |y| of the chunk.
-__device__ __forceinline__ float store_chunk_q(const Params &p, const uint32_t (&v)[32], int64_t i, int64_t j0,
-                                               float alpha, float s)
+// NVFP4 store of the 32 consecutive outputs y of row i starting at column
+// j0 (two 16-element blocks): the block encode of the quantisers under the
+// given tensor scale s, 8 code bytes and one MMA-tiled scale byte per block,
+// into an output of p.yq_n columns.  Returns the largest |y|.
+__device__ __forceinline__ float encode_store_q(const Params &p, const float (&y)[32], int64_t i, int64_t j0,
+                                                float s)
 {
-    const int64_t n = p.b_rows; // the output's K (a multiple of 64)
+    const int64_t n = p.yq_n; // a multiple of 64
     float m = 0.0f;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        // y is formed twice (for the block maximum, then for the codes)
-        // rather than held: the accumulator slice already fills the registers
         float amb = 0.0f;
 #pragma unroll
         for (int t = 0; t < 16; ++t)
-            amb = fmaxf(amb, fabsf(__fmul_rn(alpha, __uint_as_float(v[16 * h + t]))));
+            amb = fmaxf(amb, fabsf(y[16 * h + t]));
         const uint32_t e = block_scale_code(amb, s);
         const float r = recip_step(__fmul_rn(e4m3_value(e), s));
         uint32_t pk[2] = {0u, 0u};
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            const float y0 = __fmul_rn(alpha, __uint_as_float(v[16 * h + 2 * t]));
-            const float y1 = __fmul_rn(alpha, __uint_as_float(v[16 * h + 2 * t + 1]));
-            pk[t >> 2] |= e2m1x2(__fmul_rn(y0, r), __fmul_rn(y1, r)) << (8 * (t & 3));
-        }
+        for (int t = 0; t < 8; ++t)
+            pk[t >> 2] |= e2m1x2(__fmul_rn(y[16 * h + 2 * t], r), __fmul_rn(y[16 * h + 2 * t + 1], r))
+                          << (8 * (t & 3));
         const int64_t j = j0 + 16 * h;
         *reinterpret_cast<uint2 *>(p.yq_codes + i * (n / 2) + j / 2) = make_uint2(pk[0], pk[1]);
         const int64_t blk = j / 16, r7 = i & 127;
@@ -390,6 +391,30 @@ __device__ __forceinline__ float store_chunk_q(const Params &p, const uint32_t (
         m = fmaxf(m, amb);
     }
     return m;
+}
+
+// The 32 values y of row i from column j0 as BF16 or FP32 with 16-byte
+// stores (the host guarantees the alignment these modes need).
+__device__ __forceinline__ void store_vals(const Params &p, const float (&y)[32], int64_t i, int64_t j0)
+{
+    if (p.out_dtype == NVFP4_OUT_BF16) {
+        uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + i * p.ld_i + j0);
+#pragma unroll
+        for (int c = 0; c < 32; c += 8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                __nv_bfloat162 h = __floats2bfloat162_rn(y[c + 2 * q], y[c + 2 * q + 1]);
+                w[q] = *reinterpret_cast<uint32_t *>(&h);
+            }
+            o[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    } else {
+        float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + i * p.ld_i + j0);
+#pragma unroll
+        for (int c = 0; c < 32; c += 4)
+            o[c / 4] = make_float4(y[c], y[c + 1], y[c + 2], y[c + 3]);
+    }
 }
 
 template <int BN, bool GROUPED>
@@ -796,6 +821,83 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
             }
             tc_fence_after();
             constexpr int NCH = C::EPI_COLS / 32;
+            if (GROUPED && p.epi != EPI_PLAIN) {
+                const int64_t i = t.row0 + row_in_tile;
+                const bool row_ok = i < t.row_end;
+                const float alpha = a_s * p.b_second[t.expert];
+                const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
+                float m = 0.0f;
+                if (p.epi == EPI_SWIGLU) {
+                    // BN == 256: the stacked weights interleave 128-row gate
+                    // and up blocks, so accumulator columns 0..127 are the
+                    // gate and 128..255 the up products of the intermediate
+                    // columns tile_n * 128 + 0..127; this warp forms 64 of them
+                    const int h0 = (ew >> 2) * (BN / 4);
+                    const float s = p.out_q ? *p.yq_scale : 0.0f;
+#pragma unroll 1
+                    for (int c = 0; c < BN / 128; ++c) {
+                        uint32_t g[32], u[32];
+                        tc_ld_32x32b_x32(tb + h0 + 32 * c, g);
+                        tc_ld_32x32b_x32(tb + BN / 2 + h0 + 32 * c, u);
+                        tc_wait_ld();
+                        float y[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const float gv = __fmul_rn(alpha, __uint_as_float(g[e]));
+                            const float uv = __fmul_rn(alpha, __uint_as_float(u[e]));
+                            y[e] = __fmul_rn(__fdiv_rn(gv, 1.0f + expf(-gv)), uv); // SiLU(g) * u
+                        }
+                        const int64_t j = (int64_t)t.tile_n * (BN / 2) + h0 + 32 * c;
+                        if (row_ok) {
+                            if (p.out_q)
+                                m = fmaxf(m, encode_store_q(p, y, i, j, s));
+                            else
+                                store_vals(p, y, i, j);
+                        }
+                    }
+                } else {
+                    // gate-weighted combine: row i's products, times its
+                    // routing weight, added to its token's output row
+                    // (rows whose token index is out of range add nothing)
+                    const int64_t tok = row_ok ? (int64_t)p.comb_idx[i] : -1;
+                    const bool add = tok >= 0 && tok < p.comb_rows;
+                    const float gw = add ? p.comb_w[i] : 0.0f;
+                    const int64_t j_base = (int64_t)t.tile_n * BN + cbase;
+#pragma unroll 1
+                    for (int c = 0; c < NCH; ++c) {
+                        uint32_t v1[32];
+                        tc_ld_32x32b_x32(tb + cbase + 32 * c, v1);
+                        tc_wait_ld();
+                        if (add) {
+                            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + tok * p.ld_i +
+                                                                     j_base + 32 * c);
+#pragma unroll
+                            for (int e = 0; e < 32; e += 4)
+                                atomicAdd(dst + e / 4,
+                                          make_float4(gw * (alpha * __uint_as_float(v1[e])),
+                                                      gw * (alpha * __uint_as_float(v1[e + 1])),
+                                                      gw * (alpha * __uint_as_float(v1[e + 2])),
+                                                      gw * (alpha * __uint_as_float(v1[e + 3]))));
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&acc_empty[acc]);
+                if (++acc == C::ACC_BUFS) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+                if (p.out_q && p.yq_amax != nullptr) {
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+                        m = fmaxf(m, __shfl_xor_sync(FULLMASK, m, o));
+                    if (lane == 0)
+                        atomicMax(p.yq_amax, __float_as_uint(m));
+                }
+                continue;
+            }
             if (!GROUPED && p.out_q) {
                 // NVFP4 output (whole tiles only; N is a multiple of 64): one
                 // 32-column chunk at a time straight from TMEM, the
@@ -814,7 +916,11 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                     const int64_t j = j_base + c * 32;
                     if (j < p.b_rows) {
                         if (i < p.a_rows) {
-                            m = fmaxf(m, store_chunk_q(p, v1, i, j, alpha, s));
+                            float y[32];
+#pragma unroll
+                            for (int u = 0; u < 32; ++u)
+                                y[u] = __fmul_rn(alpha, __uint_as_float(v1[u]));
+                            m = fmaxf(m, encode_store_q(p, y, i, j, s));
                         } else {
                             // padding rows of the last M tile: zero scales,
                             // as the quantisers leave them
@@ -1127,6 +1233,7 @@ cudaError_t launch_w4a4_dense(const DenseGemmArgs &g, cudaStream_t stream)
     p.yq_scales = g.yq_scales;
     p.yq_scale = g.yq_scale;
     p.yq_amax = g.yq_amax;
+    p.yq_n = g.b_rows;
     p.slots = g.slots;
     p.flags = g.flags;
     p.slot_stride = g.a_rows * bn;
@@ -1178,6 +1285,16 @@ cudaError_t launch_w4a4_grouped(const GroupedGemmArgs &g, cudaStream_t stream)
     const int esz = g.out_dtype == NVFP4_OUT_BF16 ? 2 : 4;
     p.vec_ok = ((g.ldy * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(g.out) % 16) == 0) ? 1 : 0;
     p.b_row_tiles = (int)ceil_div(g.E * g.N, 128);
+    p.epi = g.epi;
+    p.comb_idx = g.comb_idx;
+    p.comb_w = g.comb_w;
+    p.comb_rows = g.comb_rows;
+    p.out_q = g.yq_codes != nullptr ? 1 : 0;
+    p.yq_codes = g.yq_codes;
+    p.yq_scales = g.yq_scales;
+    p.yq_scale = g.yq_scale;
+    p.yq_amax = g.yq_amax;
+    p.yq_n = g.N / 2; // SwiGLU output columns
     p.offsets = g.offsets;
     p.row_idx = g.row_idx;
     p.E = g.E;

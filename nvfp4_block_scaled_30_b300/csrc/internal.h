@@ -123,7 +123,21 @@ struct GroupedGemmArgs {
     int64_t total_rows;
     uint32_t *status;
     uint64_t timeout_ns;
+    // epilogue: EPI_PLAIN (out = alpha * acc), EPI_SWIGLU (N = 2I stacked
+    // rows per expert interleaving 128-row gate and up blocks; out, or the
+    // NVFP4 output yq_* when yq_codes is set, gets SiLU(gate) * up, [rows, I])
+    // or EPI_COMBINE (out FP32 [tokens][ldy]: row comb_idx[j] += comb_w[j] *
+    // alpha * acc of routed row j, atomically)
+    int epi;
+    const int32_t *comb_idx;
+    const float *comb_w;
+    int64_t comb_rows;       // tokens; rows with other token indices add nothing
+    uint8_t *yq_codes;
+    uint8_t *yq_scales;
+    const float *yq_scale;
+    uint32_t *yq_amax;
 };
+enum { EPI_PLAIN = 0, EPI_SWIGLU = 1, EPI_COMBINE = 2 };
 cudaError_t launch_w4a4_grouped(const GroupedGemmArgs &g, cudaStream_t stream);
 
 struct W4A8GemmArgs {

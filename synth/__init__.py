@@ -111,6 +111,22 @@ def moe_routing(T: int = 2048, E: int = 128, topk: int = 8, zipf_s: float = 1.1,
     return row_idx, offsets, counts, logits
 
 
+def moe_gate_weights(logits, row_idx, offsets, topk: int = 8) -> np.ndarray:
+    """Routing weight of every routed row (float32 [R]): the softmax of the
+    token's top-k router logits, renormalised over the k chosen experts, for
+    the (token row_idx[j], expert owning row j) pair."""
+    logits = np.asarray(logits, np.float64)
+    T, E = logits.shape
+    top = np.argsort(-logits, axis=1, kind="stable")[:, :topk]
+    sel = np.take_along_axis(logits, top, 1)
+    w = np.exp(sel - sel.max(axis=1, keepdims=True))
+    w /= w.sum(axis=1, keepdims=True)
+    table = np.zeros((T, E))
+    table[np.arange(T)[:, None], top] = w
+    expert = np.repeat(np.arange(E), np.diff(np.asarray(offsets, np.int64)))
+    return table[np.asarray(row_idx, np.int64), expert].astype(np.float32)
+
+
 def moe_routing_from_counts(counts, T: int, seed: int = SEED):
     """Routing lists for prescribed per-expert counts (e.g. forced-empty
     experts): expert e takes counts[e] distinct tokens drawn without

@@ -20,6 +20,16 @@ def untile_scales(tiled: np.ndarray, rows: int, K: int) -> np.ndarray:
     return np.ascontiguousarray(t.transpose(0, 3, 2, 1, 4)).reshape(-1, K // 16)[:rows]
 
 
+def interleave_gate_up(gate: np.ndarray, up: np.ndarray) -> np.ndarray:
+    """Per-expert gate and up row arrays [E, I, X] -> the stacked [E, 2I, X]
+    order of the SwiGLU up projection: 128-row gate and up blocks alternate
+    (rows 256b .. 256b+127 = gate rows 128b.., the next 128 = up rows 128b..)."""
+    E, I = gate.shape[:2]
+    g = gate.reshape(E, I // 128, 128, -1)
+    u = up.reshape(E, I // 128, 128, -1)
+    return np.concatenate([g, u], axis=2).reshape(E, 2 * I, -1)
+
+
 def bf16_half_ulp(y: np.ndarray) -> np.ndarray:
     """Half the BF16 spacing at |y| (the largest error of rounding y to BF16)."""
     a = np.abs(np.asarray(y, np.float64))

@@ -361,60 +361,46 @@ __device__ __forceinline__ void store_chunk(const Params &p, const uint32_t (&v)
     }
 }
 
-// NVFP4 store of the 32 consecutive outputs y of row i starting at column
-// j0 (two 16-element blocks): the block encode of the quantisers under the
-// given tensor scale s, 8 code bytes and one MMA-tiled scale byte per block,
-// into an output of p.yq_n columns.  Returns the largest |y|.
-__device__ __forceinline__ float encode_store_q(const Params &p, const float (&y)[32], int64_t i, int64_t j0,
+// NVFP4 store of 32 consecutive outputs y (binary32 bits in v) of one row
+// starting at column j0 (two 16-element blocks): the block encode of the
+// quantisers under the given tensor scale s, 8 code bytes at crow + j0/2 and
+// one scale byte per block in the row's MMA-tiled scale slots srow (see
+// q_row).  Returns the largest |y|.
+__device__ __forceinline__ float encode_store_q(const uint32_t (&v)[32], uint8_t *crow, uint8_t *srow, int j0,
                                                 float s)
 {
-    const int64_t n = p.yq_n; // a multiple of 64
     float m = 0.0f;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         float amb = 0.0f;
 #pragma unroll
         for (int t = 0; t < 16; ++t)
-            amb = fmaxf(amb, fabsf(y[16 * h + t]));
+            amb = fmaxf(amb, fabsf(__uint_as_float(v[16 * h + t])));
         const uint32_t e = block_scale_code(amb, s);
         const float r = recip_step(__fmul_rn(e4m3_value(e), s));
         uint32_t pk[2] = {0u, 0u};
 #pragma unroll
         for (int t = 0; t < 8; ++t)
-            pk[t >> 2] |= e2m1x2(__fmul_rn(y[16 * h + 2 * t], r), __fmul_rn(y[16 * h + 2 * t + 1], r))
+            pk[t >> 2] |= e2m1x2(__fmul_rn(__uint_as_float(v[16 * h + 2 * t]), r),
+                                 __fmul_rn(__uint_as_float(v[16 * h + 2 * t + 1]), r))
                           << (8 * (t & 3));
-        const int64_t j = j0 + 16 * h;
-        *reinterpret_cast<uint2 *>(p.yq_codes + i * (n / 2) + j / 2) = make_uint2(pk[0], pk[1]);
-        const int64_t blk = j / 16, r7 = i & 127;
-        p.yq_scales[((i >> 7) * (n / 64) + (blk >> 2)) * 512 + (r7 & 31) * 16 + (r7 >> 5) * 4 + (blk & 3)] =
-            (uint8_t)e;
+        const int j = j0 + 16 * h;
+        *reinterpret_cast<uint2 *>(crow + j / 2) = make_uint2(pk[0], pk[1]);
+        const int blk = j / 16;
+        srow[(blk >> 2) * 512 + (blk & 3)] = (uint8_t)e;
         m = fmaxf(m, amb);
     }
     return m;
 }
 
-// The 32 values y of row i from column j0 as BF16 or FP32 with 16-byte
-// stores (the host guarantees the alignment these modes need).
-__device__ __forceinline__ void store_vals(const Params &p, const float (&y)[32], int64_t i, int64_t j0)
+// Row i of an NVFP4 output of n columns: its code row and the base of its
+// scale slots in the MMA-tiled layout (byte (i % 32) * 16 + ((i % 128) / 32)
+// * 4 + b % 4 of atom (i / 128) * (n / 64) + b / 4 holds block b).
+__device__ __forceinline__ void q_row(const Params &p, int64_t i, uint8_t *&crow, uint8_t *&srow)
 {
-    if (p.out_dtype == NVFP4_OUT_BF16) {
-        uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + i * p.ld_i + j0);
-#pragma unroll
-        for (int c = 0; c < 32; c += 8) {
-            uint32_t w[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                __nv_bfloat162 h = __floats2bfloat162_rn(y[c + 2 * q], y[c + 2 * q + 1]);
-                w[q] = *reinterpret_cast<uint32_t *>(&h);
-            }
-            o[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-    } else {
-        float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + i * p.ld_i + j0);
-#pragma unroll
-        for (int c = 0; c < 32; c += 4)
-            o[c / 4] = make_float4(y[c], y[c + 1], y[c + 2], y[c + 3]);
-    }
+    const int64_t n = p.yq_n, r7 = i & 127;
+    crow = p.yq_codes + i * (n / 2);
+    srow = p.yq_scales + (i >> 7) * (n / 64) * 512 + (r7 & 31) * 16 + (r7 >> 5) * 4;
 }
 
 template <int BN, bool GROUPED>
@@ -821,139 +807,23 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
             }
             tc_fence_after();
             constexpr int NCH = C::EPI_COLS / 32;
-            if (GROUPED && p.epi != EPI_PLAIN) {
-                const int64_t i = t.row0 + row_in_tile;
-                const bool row_ok = i < t.row_end;
-                const float alpha = a_s * p.b_second[t.expert];
-                const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
-                float m = 0.0f;
-                if (p.epi == EPI_SWIGLU) {
-                    // BN == 256: the stacked weights interleave 128-row gate
-                    // and up blocks, so accumulator columns 0..127 are the
-                    // gate and 128..255 the up products of the intermediate
-                    // columns tile_n * 128 + 0..127; this warp forms 64 of them
-                    const int h0 = (ew >> 2) * (BN / 4);
-                    const float s = p.out_q ? *p.yq_scale : 0.0f;
-#pragma unroll 1
-                    for (int c = 0; c < BN / 128; ++c) {
-                        uint32_t g[32], u[32];
-                        tc_ld_32x32b_x32(tb + h0 + 32 * c, g);
-                        tc_ld_32x32b_x32(tb + BN / 2 + h0 + 32 * c, u);
-                        tc_wait_ld();
-                        float y[32];
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const float gv = __fmul_rn(alpha, __uint_as_float(g[e]));
-                            const float uv = __fmul_rn(alpha, __uint_as_float(u[e]));
-                            y[e] = __fmul_rn(__fdiv_rn(gv, 1.0f + expf(-gv)), uv); // SiLU(g) * u
-                        }
-                        const int64_t j = (int64_t)t.tile_n * (BN / 2) + h0 + 32 * c;
-                        if (row_ok) {
-                            if (p.out_q)
-                                m = fmaxf(m, encode_store_q(p, y, i, j, s));
-                            else
-                                store_vals(p, y, i, j);
-                        }
-                    }
-                } else {
-                    // gate-weighted combine: row i's products, times its
-                    // routing weight, added to its token's output row
-                    // (rows whose token index is out of range add nothing)
-                    const int64_t tok = row_ok ? (int64_t)p.comb_idx[i] : -1;
-                    const bool add = tok >= 0 && tok < p.comb_rows;
-                    const float gw = add ? p.comb_w[i] : 0.0f;
-                    const int64_t j_base = (int64_t)t.tile_n * BN + cbase;
-#pragma unroll 1
-                    for (int c = 0; c < NCH; ++c) {
-                        uint32_t v1[32];
-                        tc_ld_32x32b_x32(tb + cbase + 32 * c, v1);
-                        tc_wait_ld();
-                        if (add) {
-                            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + tok * p.ld_i +
-                                                                     j_base + 32 * c);
-#pragma unroll
-                            for (int e = 0; e < 32; e += 4)
-                                atomicAdd(dst + e / 4,
-                                          make_float4(gw * (alpha * __uint_as_float(v1[e])),
-                                                      gw * (alpha * __uint_as_float(v1[e + 1])),
-                                                      gw * (alpha * __uint_as_float(v1[e + 2])),
-                                                      gw * (alpha * __uint_as_float(v1[e + 3]))));
-                        }
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&acc_empty[acc]);
-                if (++acc == C::ACC_BUFS) {
-                    acc = 0;
-                    acc_phase ^= 1u;
-                }
-                if (p.out_q && p.yq_amax != nullptr) {
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1)
-                        m = fmaxf(m, __shfl_xor_sync(FULLMASK, m, o));
-                    if (lane == 0)
-                        atomicMax(p.yq_amax, __float_as_uint(m));
-                }
-                continue;
-            }
-            if (!GROUPED && p.out_q) {
-                // NVFP4 output (whole tiles only; N is a multiple of 64): one
-                // 32-column chunk at a time straight from TMEM, the
-                // accumulator goes back to the MMA warp after the last one
-                const int64_t i = (int64_t)t.tile_m * BM + row_in_tile;
-                const int64_t j_base = (int64_t)t.tile_n * BN + cbase;
-                const float alpha = a_s * p.b_second[0];
-                const float s = *p.yq_scale;
-                const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + cbase;
-                float m = 0.0f;
-#pragma unroll 1
-                for (int c = 0; c < NCH; ++c) {
-                    uint32_t v1[32];
-                    tc_ld_32x32b_x32(tbase + c * 32, v1);
-                    tc_wait_ld();
-                    const int64_t j = j_base + c * 32;
-                    if (j < p.b_rows) {
-                        if (i < p.a_rows) {
-                            float y[32];
-#pragma unroll
-                            for (int u = 0; u < 32; ++u)
-                                y[u] = __fmul_rn(alpha, __uint_as_float(v1[u]));
-                            m = fmaxf(m, encode_store_q(p, y, i, j, s));
-                        } else {
-                            // padding rows of the last M tile: zero scales,
-                            // as the quantisers leave them
-                            const int64_t r7 = i & 127, kb = p.b_rows / 64;
-                            uint8_t *sc = p.yq_scales + ((i >> 7) * kb + (j >> 6)) * 512 + (r7 & 31) * 16 +
-                                          (r7 >> 5) * 4 + ((j >> 4) & 3);
-                            sc[0] = 0;
-                            sc[1] = 0;
-                        }
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&acc_empty[acc]);
-                if (++acc == C::ACC_BUFS) {
-                    acc = 0;
-                    acc_phase ^= 1u;
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1)
-                    m = fmaxf(m, __shfl_xor_sync(FULLMASK, m, o));
-                if (p.yq_amax != nullptr && lane == 0)
-                    atomicMax(p.yq_amax, __float_as_uint(m)); // |y| >= 0: bit order = value order
-                continue;
-            }
             // the whole accumulator slice of this warp into registers, then
-            // the accumulator goes back to the MMA warp
+            // the accumulator goes back to the MMA warp (before any output
+            // work, so the next tile's MMAs overlap this epilogue)
             uint32_t v[NCH][32];
-            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + cbase;
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
+            // SwiGLU (BN == 256): the stacked weights interleave 128-row gate
+            // and up blocks, so accumulator columns 0..127 hold the gate and
+            // 128..255 the up products of the tile's 128 intermediate
+            // columns; this warp takes 64 of them: gate chunks first, then
+            // the matching up chunks
+            const bool swiglu = GROUPED && p.epi == EPI_SWIGLU;
+            const int h0 = (ew >> 2) * (BN / 4);
 #pragma unroll
-            for (int c = 0; c < NCH; ++c)
-                tc_ld_32x32b_x32(tbase + c * 32, v[c]);
+            for (int c = 0; c < NCH; ++c) {
+                const int col = swiglu ? (c >= NCH / 2 ? BN / 2 : 0) + h0 + 32 * (c % (NCH / 2)) : cbase + 32 * c;
+                tc_ld_32x32b_x32(tbase + col, v[c]);
+            }
             tc_wait_ld();
             tc_fence_before();
             __syncwarp();
@@ -974,6 +844,97 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
             }
             const int64_t j_base = (int64_t)t.tile_n * BN + cbase;
             const int64_t j_end = p.b_rows;
+            if (GROUPED && p.epi != EPI_PLAIN) {
+                float m = 0.0f;
+                if (p.epi == EPI_SWIGLU) {
+                    const float s = p.out_q ? *p.yq_scale : 0.0f;
+#pragma unroll
+                    for (int c = 0; c < NCH / 2; ++c) {
+                        // SiLU(g) * u into the gate chunk's registers
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const float gv = __fmul_rn(alpha, __uint_as_float(v[c][e]));
+                            const float uv = __fmul_rn(alpha, __uint_as_float(v[c + NCH / 2][e]));
+                            // fast exponential and division: their relative
+                            // error (~2^-21) is far inside the output
+                            // tolerance, and they keep this epilogue shorter
+                            // than the next tile's main loop
+                            v[c][e] = __float_as_uint(__fmul_rn(__fdividef(gv, 1.0f + __expf(-gv)), uv));
+                        }
+                        const int64_t j = (int64_t)t.tile_n * (BN / 2) + h0 + 32 * c;
+                        if (i < i_end) {
+                            if (p.out_q) {
+                                uint8_t *crow, *srow;
+                                q_row(p, i, crow, srow);
+                                m = fmaxf(m, encode_store_q(v[c], crow, srow, (int)j, s));
+                            } else
+                                store_chunk<BN>(p, v[c], i, j, 1.0f, i_end, p.yq_n);
+                        }
+                    }
+                } else {
+                    // gate-weighted combine: row i's products, times its
+                    // routing weight, added to its token's output row (rows
+                    // whose token index is out of range add nothing)
+                    const int64_t tok = i < i_end ? (int64_t)p.comb_idx[i] : -1;
+                    if (tok >= 0 && tok < p.comb_rows) {
+                        const float gw = p.comb_w[i];
+#pragma unroll
+                        for (int c = 0; c < NCH; ++c) {
+                            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + tok * p.ld_i +
+                                                                     j_base + 32 * c);
+#pragma unroll
+                            for (int e = 0; e < 32; e += 4)
+                                atomicAdd(dst + e / 4, make_float4(gw * (alpha * __uint_as_float(v[c][e])),
+                                                                   gw * (alpha * __uint_as_float(v[c][e + 1])),
+                                                                   gw * (alpha * __uint_as_float(v[c][e + 2])),
+                                                                   gw * (alpha * __uint_as_float(v[c][e + 3]))));
+                        }
+                    }
+                }
+                if (p.out_q && p.yq_amax != nullptr) {
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+                        m = fmaxf(m, __shfl_xor_sync(FULLMASK, m, o));
+                    if (lane == 0)
+                        atomicMax(p.yq_amax, __float_as_uint(m)); // |y| >= 0: bit order = value order
+                }
+                continue;
+            }
+            if (!GROUPED && p.out_q) {
+                // NVFP4 output (whole tiles only; N is a multiple of 64)
+                float m = 0.0f;
+                uint8_t *crow, *srow;
+                q_row(p, i, crow, srow);
+                if (i < i_end) {
+                    const float s = *p.yq_scale;
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) {
+                        if (j_base + c * 32 >= j_end)
+                            continue;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) // y = alpha * acc, as the FP32 output path forms it
+                            v[c][e] = __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[c][e])));
+                        m = fmaxf(m, encode_store_q(v[c], crow, srow, (int)(j_base + c * 32), s));
+                    }
+                } else {
+                    // padding rows of the last M tile (the tile's rows all
+                    // exist in the scale layout): zero scales, as the
+                    // quantisers leave them
+                    for (int c = 0; c < NCH; ++c) {
+                        const int j = (int)(j_base + c * 32);
+                        if (j < j_end) {
+                            srow[(j >> 6) * 512 + ((j >> 4) & 3)] = 0;
+                            srow[(j >> 6) * 512 + ((j >> 4) & 3) + 1] = 0;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    m = fmaxf(m, __shfl_xor_sync(FULLMASK, m, o));
+                if (p.yq_amax != nullptr && lane == 0)
+                    atomicMax(p.yq_amax, __float_as_uint(m)); // |y| >= 0: bit order = value order
+                continue;
+            }
             const bool partial = !GROUPED && p.streamk && !(t.kst0 == 0 && t.kst1 == p.kstages);
             if (partial && t.kst0 != 0) {
                 // contributor: this is the CTA's first tile and its range

@@ -276,6 +276,26 @@ def gemm_grouped_w4a4(a, row_idx, offsets, w_codes, w_scales, w_sg):
     return Y
 
 
+def gemm_grouped_w4a8(a_fp8, s_t, row_idx, offsets, w_codes, w_scales, w_sg):
+    """Grouped W4A8: the W4A8 contraction per expert over its routed rows
+    (the W4A8 path covers MoE operations as well as dense ones: "llama.cpp
+    Put Precision Policy Inside the Model", section "One model can need more
+    than one precision").  a_fp8 uint8 [T, K] with per-token scales s_t
+    float32 [T]; row_idx int32 [R] or None; offsets int64 [E+1]; weights as
+    for gemm_grouped_w4a4.  Returns float64 [R, N]:
+    Y[j] = s_t[row(j)] * s_w[e] * sum_k E4M3(a[row(j), k]) * w_e[n, k]."""
+    off = _c(offsets, np.int64)
+    wc, ws, wsg = _c(w_codes, np.uint8), _c(w_scales, np.uint8), _c(w_sg, np.float32)
+    T = int(off[-1])
+    Y = np.zeros((T, wc.shape[1]), np.float64)
+    for e in range(wc.shape[0]):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if hi > lo:
+            rows = np.arange(lo, hi) if row_idx is None else _c(row_idx, np.int32)[lo:hi].astype(np.int64)
+            Y[lo:hi] = gemm_w4a8(a_fp8, s_t, (wc[e], ws[e], wsg[e]), rows=rows)
+    return Y
+
+
 # ---- mixture-of-experts feed-forward around the grouped contraction ------------
 #
 # The pages name MoE models (Qwen3 MoE variants) and MoE operations on the

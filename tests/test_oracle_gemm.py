@@ -188,3 +188,29 @@ def test_grouped_equals_per_expert_dense(orc):
     # contiguous rows (no index list)
     Yc = orc.gemm_grouped_w4a4(a, None, np.array([0, 10, 10, 30, 31, 40]), wc, ws, wsg)
     np.testing.assert_array_equal(Yc[10:30], orc.gemm_w4a4(a, (wc[2], ws[2], wsg[2]), rows=np.arange(10, 30)))
+
+
+def test_grouped_w4a8_by_dequantised_matmul(orc):
+    # each expert's rows against numpy's float64 product of the decoded FP8
+    # rows (times their token scales) and the expert's dequantised weights
+    rng = np.random.default_rng(23)
+    T, K, N, E = 20, 64, 16, 4
+    a = rng.integers(0, 256, size=(T, K)).astype(np.uint8)
+    a[(a & 0x7F) == 0x7F] = 0  # no NaN codes
+    st = rng.uniform(0.01, 2, size=T).astype(np.float32)
+    counts = np.array([5, 0, 12, 3])
+    row_idx, offsets = synth.moe_routing_from_counts(counts, T)
+    wc = rng.integers(0, 256, size=(E, N, K // 2)).astype(np.uint8)
+    ws = rng.integers(0x20, 0x48, size=(E, N, K // 16)).astype(np.uint8)
+    wsg = np.array([0.5, 1.0, 0.25, 2.0], np.float32)
+    Y = orc.gemm_grouped_w4a8(a, st, row_idx, offsets, wc, ws, wsg)
+    ev = e4m3_values()
+    for e in range(E):
+        lo, hi = offsets[e], offsets[e + 1]
+        rows = row_idx[lo:hi]
+        ref = (ev[a[rows]] * st[rows, None].astype(np.float64)) @ orc.nvfp4_dequant(wc[e], ws[e], wsg[e]).T
+        np.testing.assert_allclose(Y[lo:hi], ref, rtol=1e-12, atol=1e-12 * max(np.abs(ref).max(initial=0), 1))
+    # contiguous rows: output row j reads activation row j
+    Yc = orc.gemm_grouped_w4a8(a, st, None, np.array([0, 4, 4, 19, 20]), wc, ws, wsg)
+    ref = (ev[a[4:19]] * st[4:19, None].astype(np.float64)) @ orc.nvfp4_dequant(wc[2], ws[2], wsg[2]).T
+    np.testing.assert_allclose(Yc[4:19], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())

@@ -113,7 +113,8 @@ typedef enum nvfp4_op {
     NVFP4_OP_QUANTIZE_FP8 = 1, /* M = rows, K */
     NVFP4_OP_GEMM = 2,         /* M, N, K; covers both routes and on-the-fly quantisation */
     NVFP4_OP_W4A8_GEMM = 3,    /* M, N, K */
-    NVFP4_OP_GROUPED_GEMM = 4  /* M = total routed rows, N, K, E experts */
+    NVFP4_OP_GROUPED_GEMM = 4, /* M = total routed rows, N, K, E experts */
+    NVFP4_OP_GROUPED_GEMM_X = 5 /* M = T activation rows (tokens), N, K, E; both routes */
 } nvfp4_op;
 
 /* ---- sizing and workspace ------------------------------------------------ */
@@ -231,14 +232,41 @@ nvfp4_status nvfp4_w4a8_gemm(const void *a_fp8, const float *s_t, const nvfp4_te
  *  y: [total_rows, N] with row stride ldy; rows past offsets[E] untouched.
  *  Y[j, n] = s_a * s_w[e] * sum_k a[row(j), k] * w[e*N + n, k].
  *  policy/sensitive: the layer's policy and sensitive flag as for nvfp4_gemm;
- *  only the W4A4 route is implemented here, so a request that resolves to
- *  W4A8 returns UNSUPPORTED.  Offsets are read on the device (no
+ *  `a` is NVFP4, so a request that resolves to W4A8 returns UNSUPPORTED
+ *  (nvfp4_grouped_gemm_x and nvfp4_grouped_w4a8_gemm take that route).  Offsets are read on the device (no
  *  host synchronisation); invalid offsets give unspecified rows. */
 nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor *a, const int32_t *row_idx,
                                 const int64_t *expert_offsets, int32_t E, const nvfp4_tensor *w,
                                 int64_t N, void *y, int64_t ldy, int32_t y_dtype,
                                 int64_t total_rows, int32_t policy, int32_t sensitive,
                                 void *ws, size_t ws_bytes, nvfp4_stream_t stream);
+
+/* Grouped W4A8 from pre-quantised FP8 activations (the W4A8 route of [LCP]
+ * covers MoE operations as well as dense ones):
+ *   Y[j, n] = s_t[row(j)] * s_w[e] * sum_k E4M3(a[row(j), k]) * w[e*N + n, k]
+ * with the row / offsets / expert conventions of nvfp4_grouped_gemm.
+ *  a_fp8: uint8 [T, K] E4M3 (16-byte aligned), s_t: float[T] per-token
+ *  scales (as nvfp4_quantize_fp8 writes them).  w: [E*N, K] TENSOR_FP32,
+ *  MMA_TILED, second = float[E]; N % 128 == 0, K % 64 == 0.
+ *  Routed rows whose activation index is out of range give zero rows.
+ *  Workspace: nvfp4_workspace_size(NVFP4_OP_GROUPED_GEMM, total_rows, N, K, E). */
+nvfp4_status nvfp4_grouped_w4a8_gemm(const void *a_fp8, const float *s_t, int64_t T,
+                                     const int32_t *row_idx, const int64_t *expert_offsets,
+                                     int32_t E, const nvfp4_tensor *w, int64_t N, void *y,
+                                     int64_t ldy, int32_t y_dtype, int64_t total_rows, void *ws,
+                                     size_t ws_bytes, nvfp4_stream_t stream);
+
+/* Grouped GEMM of BF16 activations x [T, K] (row stride ldx) under the
+ * precision policy: the route (nvfp4_policy_route(policy, sensitive))
+ * quantises x once into the workspace (NVFP4 per-tensor for W4A4, FP8
+ * per-token for W4A8) and runs nvfp4_grouped_gemm's or
+ * nvfp4_grouped_w4a8_gemm's contraction with the same conventions.
+ * Workspace: nvfp4_workspace_size(NVFP4_OP_GROUPED_GEMM_X, T, N, K, E). */
+nvfp4_status nvfp4_grouped_gemm_x(const void *x_bf16, int64_t ldx, int64_t T, const int32_t *row_idx,
+                                  const int64_t *expert_offsets, int32_t E, const nvfp4_tensor *w,
+                                  int64_t N, void *y, int64_t ldy, int32_t y_dtype,
+                                  int64_t total_rows, int32_t policy, int32_t sensitive, void *ws,
+                                  size_t ws_bytes, nvfp4_stream_t stream);
 
 /* ---- mixture-of-experts feed-forward: fused epilogues of the grouped GEMM ----
  * The pages run MoE models (Qwen3 MoE) through the NVFP4 path ([LCP], MoE

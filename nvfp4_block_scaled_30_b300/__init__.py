@@ -26,13 +26,13 @@ POLICY_AUTO, POLICY_Q4, POLICY_Q8 = 0, 1, 2
 SCALE_TENSOR_FP32, SCALE_MACRO_FP16 = 0, 1
 LAYOUT_ROW_MAJOR, LAYOUT_MMA_TILED = 0, 1
 OUT_BF16, OUT_FP32 = 0, 1
-OP_QUANTIZE, OP_QUANTIZE_FP8, OP_GEMM, OP_W4A8_GEMM, OP_GROUPED_GEMM = range(5)
+OP_QUANTIZE, OP_QUANTIZE_FP8, OP_GEMM, OP_W4A8_GEMM, OP_GROUPED_GEMM, OP_GROUPED_GEMM_X = range(6)
 
 EXPORTED = ["nvfp4_scale_bytes", "nvfp4_workspace_size", "nvfp4_workspace_init", "nvfp4_device_status",
             "nvfp4_policy_route", "nvfp4_quantize", "nvfp4_quantize_fp8", "nvfp4_gemm", "nvfp4_w4a8_gemm",
             "nvfp4_grouped_gemm", "nvfp4_probe_convert", "nvfp4_sm_count", "nvfp4_version",
             "nvfp4_gemm_w4a4_noalloc", "nvfp4_gemm_nvfp4_out", "nvfp4_moe_up_swiglu",
-            "nvfp4_moe_down_combine"]
+            "nvfp4_moe_down_combine", "nvfp4_grouped_w4a8_gemm", "nvfp4_grouped_gemm_x"]
 
 
 class NVFP4Error(RuntimeError):
@@ -75,6 +75,10 @@ def lib():
             "nvfp4_probe_convert": (_I32, [_VP, _I64, _VP, _VP, _VP]),
             "nvfp4_gemm_w4a4_noalloc": (_I32, [_PT, _PT, _VP, _I64, _I32, _VP]),
             "nvfp4_gemm_nvfp4_out": (_I32, [_VP, _I64, _PT, _PT, _PT, _VP, _I64, _VP, _SZ, _VP]),
+            "nvfp4_grouped_w4a8_gemm": (_I32, [_VP, _VP, _I64, _VP, _VP, _I32, _PT, _I64, _VP, _I64, _I32, _I64,
+                                               _VP, _SZ, _VP]),
+            "nvfp4_grouped_gemm_x": (_I32, [_VP, _I64, _I64, _VP, _VP, _I32, _PT, _I64, _VP, _I64, _I32, _I64,
+                                            _I32, _I32, _VP, _SZ, _VP]),
             "nvfp4_moe_up_swiglu": (_I32, [_PT, _VP, _VP, _I32, _PT, _I64, _VP, _I64, _I32, _PT, _VP, _I64,
                                            _VP, _SZ, _VP]),
             "nvfp4_moe_down_combine": (_I32, [_PT, _VP, _I32, _PT, _I64, _VP, _VP, _VP, _I64, _I64, _I64,
@@ -315,6 +319,46 @@ def probe_convert(v: torch.Tensor, stream=None):
 
 def version() -> str:
     return lib().nvfp4_version().decode()
+
+
+def grouped_w4a8_gemm(a_fp8: torch.Tensor, s_t: torch.Tensor, offsets: torch.Tensor, w: NVFP4Tensor, N: int,
+                      total_rows: int, row_idx: Optional[torch.Tensor] = None, out_dtype: int = OUT_BF16,
+                      y: Optional[torch.Tensor] = None, ws: Optional[Workspace] = None,
+                      stream=None) -> torch.Tensor:
+    """nvfp4_grouped_w4a8_gemm: grouped W4A8 of FP8 activations [T, K] with
+    per-token scales s_t [T]."""
+    assert offsets.dtype == torch.int64 and (row_idx is None or row_idx.dtype == torch.int32)
+    E = offsets.numel() - 1
+    y = _out(y, total_rows, N, out_dtype, a_fp8.device)
+    if total_rows == 0:
+        return y
+    ws = _ws(ws, workspace_size(OP_GROUPED_GEMM, total_rows, N, w.K, E), a_fp8.device)
+    wd = w.desc()
+    _check(lib().nvfp4_grouped_w4a8_gemm(_ptr(a_fp8), _ptr(s_t), a_fp8.shape[0], _ptr(row_idx), _ptr(offsets), E,
+                                         ctypes.byref(wd), N, _ptr(y), y.stride(0), out_dtype, total_rows, ws.ptr,
+                                         ws.nbytes, _stream(stream)), "nvfp4_grouped_w4a8_gemm")
+    return y
+
+
+def grouped_gemm_x(x: torch.Tensor, offsets: torch.Tensor, w: NVFP4Tensor, N: int, total_rows: int,
+                   row_idx: Optional[torch.Tensor] = None, out_dtype: int = OUT_BF16, policy: int = POLICY_AUTO,
+                   sensitive: int = 0, y: Optional[torch.Tensor] = None, ws: Optional[Workspace] = None,
+                   stream=None) -> torch.Tensor:
+    """nvfp4_grouped_gemm_x: grouped GEMM of BF16 activations under the
+    precision policy (W4A4 or W4A8 route)."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    assert offsets.dtype == torch.int64 and (row_idx is None or row_idx.dtype == torch.int32)
+    E = offsets.numel() - 1
+    y = _out(y, total_rows, N, out_dtype, x.device)
+    if total_rows == 0:
+        return y
+    ws = _ws(ws, workspace_size(OP_GROUPED_GEMM_X, x.shape[0], N, w.K, E), x.device)
+    wd = w.desc()
+    _check(lib().nvfp4_grouped_gemm_x(_ptr(x), x.stride(0), x.shape[0], _ptr(row_idx), _ptr(offsets), E,
+                                      ctypes.byref(wd), N, _ptr(y), y.stride(0), out_dtype, total_rows, policy,
+                                      int(bool(sensitive)), ws.ptr, ws.nbytes, _stream(stream)),
+           "nvfp4_grouped_gemm_x")
+    return y
 
 
 def moe_up_swiglu(a: NVFP4Tensor, offsets: torch.Tensor, w_gate_up: NVFP4Tensor, I: int, total_rows: int,

@@ -88,7 +88,7 @@ static WsLayout ws_layout(int op, int64_t M, int64_t N, int64_t K)
         return o;
     };
     L.amax = take(WS_AMAX_BYTES);
-    if (op == NVFP4_OP_GEMM) {
+    if (op == NVFP4_OP_GEMM || op == NVFP4_OP_GROUPED_GEMM_X) {
         const int64_t mpad = ceil_div(M, 128) * 128;
         const int64_t kpad = ceil_div(K, 64) * 64;
         L.a_codes = take((size_t)(M * (K / 2)));
@@ -247,7 +247,7 @@ nvfp4_status nvfp4_workspace_size(int32_t op, int64_t M, int64_t N, int64_t K, i
 {
     if (!bytes || M < 0 || N < 0 || K < 0 || E < 0 || M > MAX_DIM || N > MAX_DIM || K > MAX_DIM)
         return NVFP4_ERR_INVALID_ARG;
-    if (op < NVFP4_OP_QUANTIZE || op > NVFP4_OP_GROUPED_GEMM)
+    if (op < NVFP4_OP_QUANTIZE || op > NVFP4_OP_GROUPED_GEMM_X)
         return NVFP4_ERR_INVALID_ARG;
     *bytes = ws_layout(op, M, N, K).total;
     return NVFP4_OK;
@@ -586,6 +586,132 @@ nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor *a, const int32_t *row_idx, c
     g.ldy = ldy;
     g.out_dtype = y_dtype;
     return from_cuda(launch_w4a4_grouped(g, (cudaStream_t)stream));
+}
+
+// Checks of the grouped W4A8 operands; fills the argument block.
+static nvfp4_status grouped_w4a8_args(const void *a_fp8, const float *s_t, int64_t T, const int32_t *row_idx,
+                                      const int64_t *expert_offsets, int32_t E, const nvfp4_tensor *w, int64_t N,
+                                      void *y, int64_t ldy, int32_t y_dtype, int64_t total_rows, W4A8GemmArgs &g)
+{
+    nvfp4_status st = check_tensor(w, true);
+    if (st != NVFP4_OK)
+        return st;
+    if (w->mode != NVFP4_SCALE_TENSOR_FP32)
+        return NVFP4_ERR_UNSUPPORTED;
+    if (E <= 0 || E > 1024 || !expert_offsets || !aligned(expert_offsets, 8))
+        return NVFP4_ERR_INVALID_ARG;
+    if (N <= 0 || N % 128 != 0)
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (w->rows != (int64_t)E * N)
+        return NVFP4_ERR_INVALID_ARG;
+    if (T < 0 || T > MAX_DIM || total_rows < 0 || total_rows > MAX_DIM)
+        return NVFP4_ERR_INVALID_ARG;
+    if (T > 0 && (!a_fp8 || !aligned(a_fp8, 16) || !s_t || !aligned(s_t, 4)))
+        return NVFP4_ERR_INVALID_ARG;
+    if ((row_idx == nullptr && total_rows > T) || (row_idx != nullptr && !aligned(row_idx, 4)))
+        return NVFP4_ERR_INVALID_ARG;
+    if ((st = check_out(y, ldy, y_dtype, N)) != NVFP4_OK)
+        return st;
+    g = W4A8GemmArgs{};
+    g.a_fp8 = static_cast<const uint8_t *>(a_fp8);
+    g.s_t = s_t;
+    g.M = T;
+    g.w_codes = static_cast<const uint8_t *>(w->codes);
+    g.w_scales = static_cast<const uint8_t *>(w->scales);
+    g.w_second = static_cast<const float *>(w->second);
+    g.N = N;
+    g.K = w->K;
+    g.out = y;
+    g.ldy = ldy;
+    g.out_dtype = y_dtype;
+    g.timeout_ns = DEFAULT_TIMEOUT_NS;
+    g.E = E;
+    g.offsets = expert_offsets;
+    g.row_idx = row_idx;
+    g.total_rows = total_rows;
+    return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_grouped_w4a8_gemm(const void *a_fp8, const float *s_t, int64_t T, const int32_t *row_idx,
+                                     const int64_t *expert_offsets, int32_t E, const nvfp4_tensor *w, int64_t N,
+                                     void *y, int64_t ldy, int32_t y_dtype, int64_t total_rows, void *ws,
+                                     size_t ws_bytes, nvfp4_stream_t stream)
+{
+    W4A8GemmArgs g;
+    nvfp4_status st =
+        grouped_w4a8_args(a_fp8, s_t, T, row_idx, expert_offsets, E, w, N, y, ldy, y_dtype, total_rows, g);
+    if (st != NVFP4_OK)
+        return st;
+    if ((st = check_ws(ws, ws_bytes, ws_layout(NVFP4_OP_GROUPED_GEMM, total_rows, N, w->K).total)) != NVFP4_OK)
+        return st;
+    if (total_rows == 0 || T == 0)
+        return NVFP4_OK;
+    g.status = status_word(ws);
+    return from_cuda(launch_w4a8(g, (cudaStream_t)stream));
+}
+
+nvfp4_status nvfp4_grouped_gemm_x(const void *x_bf16, int64_t ldx, int64_t T, const int32_t *row_idx,
+                                  const int64_t *expert_offsets, int32_t E, const nvfp4_tensor *w, int64_t N,
+                                  void *y, int64_t ldy, int32_t y_dtype, int64_t total_rows, int32_t policy,
+                                  int32_t sensitive, void *ws, size_t ws_bytes, nvfp4_stream_t stream)
+{
+    const int32_t route = nvfp4_policy_route(policy, sensitive);
+    if (route < 0 || !w)
+        return NVFP4_ERR_INVALID_ARG;
+    const int64_t K = w->K;
+    if (T < 0 || T > MAX_DIM || ldx < K || ldx % 8 != 0 || (T > 0 && (!x_bf16 || !aligned(x_bf16, 16))))
+        return NVFP4_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(NVFP4_OP_GROUPED_GEMM_X, T, N, K);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (route == 8) {
+        uint8_t *a8 = ws_at(ws, L.a_fp8);
+        float *st_ = reinterpret_cast<float *>(ws_at(ws, L.a_st));
+        W4A8GemmArgs g;
+        nvfp4_status st =
+            grouped_w4a8_args(a8, st_, T, row_idx, expert_offsets, E, w, N, y, ldy, y_dtype, total_rows, g);
+        if (st != NVFP4_OK)
+            return st;
+        if ((st = check_ws(ws, ws_bytes, L.total)) != NVFP4_OK)
+            return st;
+        if (total_rows == 0 || T == 0)
+            return NVFP4_OK;
+        g.status = status_word(ws);
+        if (launch_fp8_quantize(static_cast<const uint16_t *>(x_bf16), T, K, ldx, a8, st_, status_word(ws), s) !=
+            cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        return from_cuda(launch_w4a8(g, s));
+    }
+    // W4A4: the NVFP4 activations live in the workspace
+    nvfp4_tensor a{};
+    a.codes = ws_at(ws, L.a_codes);
+    a.scales = ws_at(ws, L.a_scales);
+    a.second = ws_at(ws, L.a_second);
+    a.rows = T;
+    a.K = K;
+    a.mode = NVFP4_SCALE_TENSOR_FP32;
+    a.layout = NVFP4_LAYOUT_MMA_TILED;
+    if (!ws || !aligned(ws, 256))
+        return NVFP4_ERR_WORKSPACE;
+    GroupedGemmArgs g;
+    nvfp4_status st = grouped_args(&a, row_idx, expert_offsets, E, w, N, total_rows, ws, ws_bytes, g);
+    if (st != NVFP4_OK)
+        return st;
+    if ((st = check_out(y, ldy, y_dtype, N)) != NVFP4_OK)
+        return st;
+    if ((st = check_ws(ws, ws_bytes, L.total)) != NVFP4_OK)
+        return st;
+    if (total_rows == 0 || T == 0)
+        return NVFP4_OK;
+    g.out = y;
+    g.ldy = ldy;
+    g.out_dtype = y_dtype;
+    cudaError_t e = launch_nvfp4_quantize(static_cast<const uint16_t *>(x_bf16), T, K, ldx,
+                                          static_cast<uint8_t *>(a.codes), static_cast<uint8_t *>(a.scales), a.second,
+                                          NVFP4_SCALE_TENSOR_FP32, NVFP4_LAYOUT_MMA_TILED,
+                                          reinterpret_cast<uint32_t *>(ws_at(ws, L.amax)), status_word(ws), s, false);
+    if (e != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    return from_cuda(launch_w4a4_grouped(g, s));
 }
 
 nvfp4_status nvfp4_moe_up_swiglu(const nvfp4_tensor *a, const int32_t *row_idx, const int64_t *expert_offsets,

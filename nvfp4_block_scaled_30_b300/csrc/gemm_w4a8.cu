@@ -23,6 +23,11 @@
 //               thread t expands half of A row t % 128 and W row t
 //   warps 10..17 epilogue: TMEM -> registers 32 columns at a time,
 //               * s_t[m] * s_w, BF16/FP32 store
+// The grouped (mixture-of-experts) variant runs the same pipeline over the
+// experts' routed rows: work items are (expert, 128-row block of its rows,
+// N tile); gathered token rows are copied into the raw ring with 16-byte
+// cp.async by all producer lanes (contiguous rows by TMA), each row takes
+// its token's scale and the expert's weight scale.
 #include <algorithm>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -53,10 +58,11 @@ constexpr int CONV_A = BM * 128;            // FP16 rows of 128 bytes
 constexpr int CONV_B = BN * 128;
 constexpr int CONV_BYTES = CONV_A + CONV_B;
 constexpr int TMEM_COLS = 512;
+constexpr int MAX_EXPERTS = 1024;
 static_assert(CONV_WARPS * 32 == 2 * BM && CONV_WARPS * 32 == BN, "converter thread mapping");
 constexpr int SMEM_BYTES = CONV_STAGES * CONV_BYTES + RAW_STAGES * RAW_BYTES + 256 + 1024;
 static_assert(RAW_BYTES % 1024 == 0 && CONV_BYTES % 1024 == 0, "alignment");
-static_assert(SMEM_BYTES <= 232448, "shared memory");
+static_assert(SMEM_BYTES + 4 * (MAX_EXPERTS + 2) <= 232448, "shared memory");
 static_assert(ACC_BUFS * BN <= TMEM_COLS, "TMEM");
 
 struct Params {
@@ -70,9 +76,29 @@ struct Params {
     int32_t m_tiles, n_tiles, ksteps, k64_total, out_dtype, vec_ok, w_groups;
     uint32_t *status;
     uint64_t timeout_ns;
+    // grouped mode: N is per expert, W holds E * N rows
+    const uint8_t *a_fp8;     // gathered rows are copied from here
+    int64_t K;
+    const int64_t *offsets;
+    const int32_t *row_idx;   // null: routed row j reads activation row j
+    int32_t E;
+    int64_t total_rows;
 };
 
-__device__ __forceinline__ void decode(const Params &p, int item, int &tm, int &tn)
+struct Item {
+    int tn, expert;
+    int64_t row0, row_end;    // first output row of the tile, end of its rows
+};
+
+// Expert e's routed rows [lo, hi), offsets clamped to [0, total_rows] and
+// made non-decreasing.
+__device__ __forceinline__ void expert_rows(const Params &p, int e, int64_t &lo, int64_t &hi)
+{
+    lo = min(max(p.offsets[e], (int64_t)0), p.total_rows);
+    hi = min(max(p.offsets[e + 1], lo), p.total_rows);
+}
+
+__device__ __forceinline__ void decode_dense(const Params &p, int item, int &tm, int &tn)
 {
     constexpr int G = 8;
     const int band = G * p.n_tiles;
@@ -82,6 +108,39 @@ __device__ __forceinline__ void decode(const Params &p, int item, int &tm, int &
     const int r = item - bid * band;
     tm = first + r % gs;
     tn = r / gs;
+}
+
+// prefix[e] = 128-row blocks of experts 0..e-1 (grouped); items are the
+// expert's blocks, N tiles outermost within an expert.
+template <bool GROUPED>
+__device__ __forceinline__ void decode(const Params &p, const int *prefix, int item, Item &it)
+{
+    if (!GROUPED) {
+        int tm;
+        decode_dense(p, item, tm, it.tn);
+        it.expert = 0;
+        it.row0 = (int64_t)tm * BM;
+        it.row_end = p.M;
+        return;
+    }
+    const int blk = item / p.n_tiles;
+    int lo = 0, hi = p.E;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= blk)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    const int e = lo;
+    const int mt_e = prefix[e + 1] - prefix[e];
+    const int local = item - prefix[e] * p.n_tiles;
+    it.expert = e;
+    it.tn = local / mt_e;
+    int64_t r_lo, r_hi;
+    expert_rows(p, e, r_lo, r_hi);
+    it.row0 = r_lo + (int64_t)(local - it.tn * mt_e) * BM;
+    it.row_end = r_hi;
 }
 
 __device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t two_bytes)
@@ -110,6 +169,7 @@ __device__ __forceinline__ void timeout(const Params &p, volatile int *abort_fla
     atomicOr(p.status, ST_TIMEOUT);
 }
 
+template <bool GROUPED>
 __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant__ Params p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -125,12 +185,16 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
     uint64_t *drain = acc_empty + ACC_BUFS;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    __shared__ int prefix[GROUPED ? MAX_EXPERTS + 1 : 1];
+    __shared__ int total_s;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr unsigned FULLMASK = 0xFFFFFFFFu;
+    const bool indexed = GROUPED && p.row_idx != nullptr;
     if (threadIdx.x == 0) {
         for (int s = 0; s < RAW_STAGES; ++s) {
-            mbar_init(&raw_full[s], 1);
+            // gathered rows: one more arrival per producer lane (its cp.async)
+            mbar_init(&raw_full[s], indexed ? 33 : 1);
             mbar_init(&raw_empty[s], CONV_WARPS);
         }
         for (int s = 0; s < CONV_STAGES; ++s) {
@@ -149,11 +213,45 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
         tmem_alloc(tmem_slot, TMEM_COLS);
         tmem_relinquish();
     }
+    if (GROUPED) {
+        if (warp == 2) {
+            // 128-row blocks per expert, prefix-summed by one warp: lane l
+            // owns a contiguous run of experts, a shuffle scan joins the runs
+            const int per = (p.E + 31) / 32;
+            const int e0 = min(lane * per, p.E), e1 = min(e0 + per, p.E);
+            int run = 0;
+            for (int e = e0; e < e1; ++e) {
+                int64_t lo, hi;
+                expert_rows(p, e, lo, hi);
+                run += (int)((hi - lo + BM - 1) / BM);
+            }
+            int incl = run;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(FULLMASK, incl, o);
+                if (lane >= o)
+                    incl += v;
+            }
+            int acc = incl - run;
+            if (lane == 0)
+                prefix[0] = 0;
+            for (int e = e0; e < e1; ++e) {
+                int64_t lo, hi;
+                expert_rows(p, e, lo, hi);
+                acc += (int)((hi - lo + BM - 1) / BM);
+                prefix[e + 1] = acc;
+            }
+            if (lane == 31)
+                total_s = incl * p.n_tiles;
+        }
+    } else if (threadIdx.x == 0) {
+        total_s = p.m_tiles * p.n_tiles;
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int total = p.m_tiles * p.n_tiles;
+    const int total = total_s;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -161,9 +259,23 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
         uint32_t ph = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-            int tm, tn;
-            decode(p, item, tm, tn);
-            const int g0 = tn * NG; // first 128-row scale group of the W tile
+            Item it;
+            decode<GROUPED>(p, prefix, item, it);
+            const int64_t w_row0 = (int64_t)it.expert * p.N + (int64_t)it.tn * BN;
+            const int g0 = (int)(w_row0 / 128); // first 128-row scale group of the W tile
+            // gathered rows: source rows of this lane's 4 tile rows (row 0,
+            // zero-filled, past the expert or for out-of-range indices)
+            int64_t src[4] = {0, 0, 0, 0};
+            bool live[4] = {false, false, false, false};
+            if (indexed) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int64_t g = it.row0 + lane + 32 * q;
+                    const int r = g < it.row_end ? p.row_idx[g] : -1;
+                    live[q] = r >= 0 && r < p.M;
+                    src[q] = live[q] ? r : 0;
+                }
+            }
             int ng = 0;
 #pragma unroll
             for (int h = 0; h < NG; ++h)
@@ -178,17 +290,30 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
                 }
                 uint8_t *r = raw + st * RAW_BYTES;
                 if (lane == 0)
-                    mbar_arrive_expect_tx(&raw_full[st], RAW_A + RAW_W + ng * 512);
+                    mbar_arrive_expect_tx(&raw_full[st], (indexed ? 0 : RAW_A) + RAW_W + ng * 512);
                 __syncwarp();
                 // op 0: A, 1: W codes, 2..2+NG-1: W scale atoms; lanes 8r.. serve steps r, r+4, ...
                 const int op = lane - 8 * (issued & 3);
-                if (op == 0)
-                    tma_load_2d(r, &p.tmap_a, ks * KSTEP, tm * BM, &raw_full[st]);
+                if (op == 0 && !indexed)
+                    tma_load_2d(r, &p.tmap_a, ks * KSTEP, (int)it.row0, &raw_full[st]);
                 else if (op == 1)
-                    tma_load_2d(r + RAW_A, &p.tmap_w, ks * (KSTEP / 2), tn * BN, &raw_full[st]);
+                    tma_load_2d(r + RAW_A, &p.tmap_w, ks * (KSTEP / 2), (int)w_row0, &raw_full[st]);
                 else if (op >= 2 && op < 2 + NG && g0 + op - 2 < p.w_groups)
                     bulk_load(r + RAW_A + RAW_W + (op - 2) * 512,
                               p.w_scales + ((size_t)(g0 + op - 2) * p.k64_total + ks) * 512, 512, &raw_full[st]);
+                if (indexed) {
+                    // gathered FP8 rows: 64 bytes per row and step, plain
+                    // row-major like the TMA box; every lane's copies
+                    // complete the stage's barrier on their own
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint8_t *srow = p.a_fp8 + src[q] * p.K + (int64_t)ks * KSTEP;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            cp_async_16(r + (lane + 32 * q) * KSTEP + 16 * c, srow + 16 * c, live[q] ? 16u : 0u);
+                    }
+                    cp_async_arrive_noinc(&raw_full[st]);
+                }
                 ++issued;
                 if (++st == RAW_STAGES) {
                     st = 0;
@@ -339,10 +464,10 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
         const int row = q * 32 + lane;
         int acc = 0;
         uint32_t aph = 0;
-        const float sw = *p.w_second;
         for (int item = blockIdx.x; item < total; item += gridDim.x) {
-            int tm, tn;
-            decode(p, item, tm, tn);
+            Item it;
+            decode<GROUPED>(p, prefix, item, it);
+            const int tn = it.tn;
             const bool got = mbar_wait(&acc_full[acc], aph, p.timeout_ns, abort_flag);
             if (!__all_sync(FULLMASK, got)) {
                 if (lane == 0)
@@ -350,14 +475,20 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
                 break;
             }
             tc_fence_after();
-            const int64_t i = (int64_t)tm * BM + row;
-            const float alpha = i < p.M ? p.s_t[i] * sw : 0.0f;
+            const int64_t i = it.row0 + row;
+            const bool row_ok = i < it.row_end;
+            int64_t tok = i;
+            if (indexed && row_ok) {
+                const int r = p.row_idx[i];
+                tok = (r >= 0 && r < p.M) ? r : -1;
+            }
+            const float alpha = (row_ok && tok >= 0) ? p.s_t[tok] * p.w_second[it.expert] : 0.0f;
             const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
             for (int c0 = chalf * (BN / 2); c0 < (chalf + 1) * (BN / 2); c0 += 32) {
                 uint32_t v[32];
                 tc_ld_32x32b_x32(tb + c0, v);
                 tc_wait_ld();
-                if (i < p.M) {
+                if (row_ok) {
                     const int64_t j0 = (int64_t)tn * BN + c0;
                     if (p.vec_ok && j0 + 32 <= p.N) {
                         if (p.out_dtype == NVFP4_OUT_BF16) {
@@ -416,12 +547,14 @@ cudaError_t launch_w4a8(const W4A8GemmArgs &g, cudaStream_t stream)
 {
     if (g.K % KSTEP != 0)
         return cudaErrorInvalidValue;
+    const bool grouped = g.E > 0;
+    const int64_t w_rows = grouped ? (int64_t)g.E * g.N : g.N;
     Params p{};
     CUresult r = make_tmap_2d_u8(&p.tmap_a, g.a_fp8, (uint64_t)g.K, (uint64_t)g.M, (uint64_t)g.K, KSTEP, BM, false);
     if (r != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    r = make_tmap_2d_u8(&p.tmap_w, g.w_codes, (uint64_t)(g.K / 2), (uint64_t)g.N, (uint64_t)(g.K / 2), KSTEP / 2, BN,
-                        false);
+    r = make_tmap_2d_u8(&p.tmap_w, g.w_codes, (uint64_t)(g.K / 2), (uint64_t)w_rows, (uint64_t)(g.K / 2), KSTEP / 2,
+                        BN, false);
     if (r != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     p.w_scales = g.w_scales;
@@ -435,18 +568,27 @@ cudaError_t launch_w4a8(const W4A8GemmArgs &g, cudaStream_t stream)
     p.n_tiles = (int)ceil_div(g.N, BN);
     p.ksteps = (int)(g.K / KSTEP);
     p.k64_total = (int)(g.K / 64);
-    p.w_groups = (int)ceil_div(g.N, 128);
+    p.w_groups = (int)ceil_div(w_rows, 128);
     p.out_dtype = g.out_dtype;
     const int esz = g.out_dtype == NVFP4_OUT_BF16 ? 2 : 4;
     p.vec_ok = ((g.ldy * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(g.out) % 16) == 0) ? 1 : 0;
     p.status = g.status;
     p.timeout_ns = g.timeout_ns;
-    cudaError_t e = cudaFuncSetAttribute(w4a8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    p.a_fp8 = g.a_fp8;
+    p.K = g.K;
+    p.offsets = g.offsets;
+    p.row_idx = g.row_idx;
+    p.E = g.E;
+    p.total_rows = g.total_rows;
+    auto kern = grouped ? w4a8_kernel<true> : w4a8_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess)
         return e;
-    const int total = p.m_tiles * p.n_tiles;
-    const int grid = std::max(1, std::min(total, device_sm_count()));
-    w4a8_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(p);
+    // grouped: an upper bound of the items (every expert's rows in 128-row
+    // blocks, plus one partial block per expert); the kernel counts them
+    const int64_t items = grouped ? (ceil_div(g.total_rows, BM) + g.E) * p.n_tiles : (int64_t)p.m_tiles * p.n_tiles;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(items, device_sm_count()));
+    kern<<<grid, THREADS, SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -144,15 +144,22 @@ struct W4A8GemmArgs {
     const uint8_t *a_fp8;    // [M][K]
     const float *s_t;        // [M]
     int64_t M;
-    const uint8_t *w_codes;  // [N][K/2]
+    const uint8_t *w_codes;  // [N][K/2] ([E*N][K/2] grouped)
     const uint8_t *w_scales; // tiled
-    const float *w_second;
+    const float *w_second;   // [1] ([E] grouped)
     int64_t N, K;
     void *out;
     int64_t ldy;
     int out_dtype;
     uint32_t *status;
     uint64_t timeout_ns;
+    // grouped (E > 0): N per expert (% 128 == 0); expert e owns output rows
+    // offsets[e] .. offsets[e+1]-1, routed row j reads activation row
+    // row_idx[j] (or j when row_idx is null)
+    int E;
+    const int64_t *offsets;
+    const int32_t *row_idx;
+    int64_t total_rows;
 };
 cudaError_t launch_w4a8(const W4A8GemmArgs &g, cudaStream_t stream);
 

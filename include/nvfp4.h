@@ -356,6 +356,20 @@ nvfp4_status nvfp4_gemm_w4a4_noalloc(const nvfp4_tensor *a_q, const nvfp4_tensor
 nvfp4_status nvfp4_probe_convert(const float *in, int64_t n, uint8_t *out_e2m1, uint8_t *out_e4m3,
                                  nvfp4_stream_t stream);
 
+/* Test-only failure injection for the device-side failure detection: runs the
+ * W4A4 GEMM of pre-quantised a_q (TENSOR_FP32, MMA_TILED) and w on a shape
+ * that uses stream-K, with CTA `skip_cta` never raising its ready flag, and
+ * every bounded wait limited to timeout_ns (1 .. 1e10).  If skip_cta's range
+ * starts inside a tile, that tile's owner gives up waiting after timeout_ns,
+ * sets TIMEOUT in the workspace status word and exits cleanly (no fault, no
+ * hang; the context stays usable); that tile of y is then unspecified.
+ * Afterwards call nvfp4_workspace_init: the abandoned flags stay raised.
+ * Returns UNSUPPORTED_SHAPE for a shape that does not run stream-K. */
+nvfp4_status nvfp4_diag_streamk_skip_flag(const nvfp4_tensor *a_q, const nvfp4_tensor *w, void *y,
+                                          int64_t ldy, int32_t y_dtype, int32_t skip_cta,
+                                          uint64_t timeout_ns, void *ws, size_t ws_bytes,
+                                          nvfp4_stream_t stream);
+
 /* Number of streaming multiprocessors of the current device (0 on error). */
 int32_t nvfp4_sm_count(void);
 

@@ -32,7 +32,8 @@ EXPORTED = ["nvfp4_scale_bytes", "nvfp4_workspace_size", "nvfp4_workspace_init",
             "nvfp4_policy_route", "nvfp4_quantize", "nvfp4_quantize_fp8", "nvfp4_gemm", "nvfp4_w4a8_gemm",
             "nvfp4_grouped_gemm", "nvfp4_probe_convert", "nvfp4_sm_count", "nvfp4_version",
             "nvfp4_gemm_w4a4_noalloc", "nvfp4_gemm_nvfp4_out", "nvfp4_moe_up_swiglu",
-            "nvfp4_moe_down_combine", "nvfp4_grouped_w4a8_gemm", "nvfp4_grouped_gemm_x"]
+            "nvfp4_moe_down_combine", "nvfp4_grouped_w4a8_gemm", "nvfp4_grouped_gemm_x",
+            "nvfp4_diag_streamk_skip_flag"]
 
 
 class NVFP4Error(RuntimeError):
@@ -73,6 +74,8 @@ def lib():
             "nvfp4_grouped_gemm": (_I32, [_PT, _VP, _VP, _I32, _PT, _I64, _VP, _I64, _I32, _I64, _I32, _I32,
                                           _VP, _SZ, _VP]),
             "nvfp4_probe_convert": (_I32, [_VP, _I64, _VP, _VP, _VP]),
+            "nvfp4_diag_streamk_skip_flag": (_I32, [_PT, _PT, _VP, _I64, _I32, _I32, ctypes.c_uint64, _VP, _SZ,
+                                                    _VP]),
             "nvfp4_gemm_w4a4_noalloc": (_I32, [_PT, _PT, _VP, _I64, _I32, _VP]),
             "nvfp4_gemm_nvfp4_out": (_I32, [_VP, _I64, _PT, _PT, _PT, _VP, _I64, _VP, _SZ, _VP]),
             "nvfp4_grouped_w4a8_gemm": (_I32, [_VP, _VP, _I64, _VP, _VP, _I32, _PT, _I64, _VP, _I64, _I32, _I64,

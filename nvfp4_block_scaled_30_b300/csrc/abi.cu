@@ -157,7 +157,8 @@ static nvfp4_status from_cuda(cudaError_t e)
 static nvfp4_status run_w4a4_dense(const uint8_t *a_codes, const uint8_t *a_scales, const float *a_second,
                                    int64_t M, const nvfp4_tensor *w, void *y, int64_t ldy, int y_dtype, void *ws,
                                    const WsLayout &L, bool after_quantiser, cudaStream_t stream,
-                                   const nvfp4_tensor *yq = nullptr, float *y_amax = nullptr)
+                                   const nvfp4_tensor *yq = nullptr, float *y_amax = nullptr,
+                                   int diag_skip_flag = -1, uint64_t timeout_ns = DEFAULT_TIMEOUT_NS)
 {
     const int64_t N = w->rows, K = w->K;
     DenseGemmArgs g{};
@@ -171,7 +172,8 @@ static nvfp4_status run_w4a4_dense(const uint8_t *a_codes, const uint8_t *a_scal
     g.b_rows = N;
     g.K = K;
     g.status = status_word(ws);
-    g.timeout_ns = DEFAULT_TIMEOUT_NS;
+    g.timeout_ns = timeout_ns;
+    g.diag_skip_flag = diag_skip_flag;
     g.out = y;
     g.out_dtype = y_dtype;
     g.ld_i = ldy;
@@ -788,6 +790,32 @@ nvfp4_status nvfp4_moe_down_combine(const nvfp4_tensor *h, const int64_t *expert
     g.comb_w = gate_w;
     g.comb_rows = T;
     return from_cuda(launch_w4a4_grouped(g, (cudaStream_t)stream));
+}
+
+nvfp4_status nvfp4_diag_streamk_skip_flag(const nvfp4_tensor *a_q, const nvfp4_tensor *w, void *y, int64_t ldy,
+                                          int32_t y_dtype, int32_t skip_cta, uint64_t timeout_ns, void *ws,
+                                          size_t ws_bytes, nvfp4_stream_t stream)
+{
+    nvfp4_status st = check_tensor(w, true);
+    if (st != NVFP4_OK)
+        return st;
+    if ((st = check_tensor(a_q, true)) != NVFP4_OK)
+        return st;
+    if (w->mode != NVFP4_SCALE_TENSOR_FP32 || a_q->mode != NVFP4_SCALE_TENSOR_FP32 || a_q->K != w->K)
+        return NVFP4_ERR_INVALID_ARG;
+    const int64_t M = a_q->rows, N = w->rows, K = w->K;
+    if ((st = check_out(y, ldy, y_dtype, N)) != NVFP4_OK)
+        return st;
+    if (skip_cta < 0 || timeout_ns == 0 || timeout_ns > 10000000000ull)
+        return NVFP4_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(NVFP4_OP_GEMM, M, N, K);
+    if ((st = check_ws(ws, ws_bytes, L.total)) != NVFP4_OK)
+        return st;
+    if (L.sk_slots == 0)
+        return NVFP4_ERR_UNSUPPORTED_SHAPE; // the shape does not run stream-K
+    return run_w4a4_dense(static_cast<const uint8_t *>(a_q->codes), static_cast<const uint8_t *>(a_q->scales),
+                          static_cast<const float *>(a_q->second), M, w, y, ldy, y_dtype, ws, L, false,
+                          (cudaStream_t)stream, nullptr, nullptr, skip_cta, timeout_ns);
 }
 
 nvfp4_status nvfp4_probe_convert(const float *in, int64_t n, uint8_t *out_e2m1, uint8_t *out_e4m3,

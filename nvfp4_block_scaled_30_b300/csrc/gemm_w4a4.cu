@@ -101,6 +101,7 @@ struct Params {
     int32_t b_row_tiles;    // 128-row scale atoms available in B (total)
     int32_t a_box_rows;     // rows of A one stage loads (128, or M rounded up to 16 when M < 128)
     int32_t b_early;        // issue the first stages' B copies before waiting for the previous grid
+    int32_t diag_skip_flag; // stream-K: the CTA that does not raise its ready flag (-1: none)
     // NVFP4 output (the next layer's quantiser fused into the epilogue):
     // codes [a_rows][b_rows/2], MMA-tiled scales, under the given tensor
     // scale; the largest |Y| is max-reduced into yq_amax when it is set
@@ -950,7 +951,9 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                                                __uint_as_float(v[c][u + 2]), __uint_as_float(v[c][u + 3])));
                 }
                 epi_bar_sync();
-                if (threadIdx.x == 32 * EPI_FIRST_WARP) {
+                // (diag_skip_flag: a test names one CTA that never raises its
+                // flag, so the owner's bounded wait runs out)
+                if (threadIdx.x == 32 * EPI_FIRST_WARP && (int)blockIdx.x != p.diag_skip_flag) {
                     __threadfence();
                     st_release_gpu(p.flags + blockIdx.x, 1u);
                 }
@@ -1189,6 +1192,7 @@ cudaError_t launch_w4a4_dense(const DenseGemmArgs &g, cudaStream_t stream)
     p.b_rows = g.b_rows;
     p.out_dtype = g.out_dtype;
     p.b_early = g.b_early ? 1 : 0;
+    p.diag_skip_flag = g.diag_skip_flag;
     p.out_q = g.yq_codes != nullptr ? 1 : 0;
     p.yq_codes = g.yq_codes;
     p.yq_scales = g.yq_scales;
@@ -1246,6 +1250,7 @@ cudaError_t launch_w4a4_grouped(const GroupedGemmArgs &g, cudaStream_t stream)
     const int esz = g.out_dtype == NVFP4_OUT_BF16 ? 2 : 4;
     p.vec_ok = ((g.ldy * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(g.out) % 16) == 0) ? 1 : 0;
     p.b_row_tiles = (int)ceil_div(g.E * g.N, 128);
+    p.diag_skip_flag = -1;
     p.epi = g.epi;
     p.comb_idx = g.comb_idx;
     p.comb_w = g.comb_w;

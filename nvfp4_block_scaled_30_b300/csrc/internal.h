@@ -82,6 +82,8 @@ struct DenseGemmArgs {
     // the previous grid in the stream is this call's activation quantiser:
     // the first stages' weight copies may start before waiting for it
     bool b_early;
+    // test-only: stream-K CTA that skips raising its ready flag (-1: none)
+    int diag_skip_flag = -1;
     // NVFP4 output instead of out (whole tiles only, b_rows % 64 == 0):
     // codes [a_rows][b_rows/2], MMA-tiled scales, encoded under the device
     // tensor scale *yq_scale; the largest |Y| (float bits) is max-reduced

@@ -342,6 +342,260 @@ __global__ void __launch_bounds__(QT) nvfp4_encode_kernel(const uint16_t *__rest
         zero_pad_scales(scales, rows, rows_pad, K, (int64_t)blockIdx.x * QT + threadIdx.x, (int64_t)gridDim.x * QT);
 }
 
+// ---- staged streaming passes (contiguous x) ----------------------------------
+// x (ldx == K) is one flat run of 16-element blocks cut into units of SU_BLOCKS
+// blocks (SU_BYTES bytes).  One producer thread brings each unit into a
+// SU_STAGES-deep shared-memory ring with a single bulk copy carrying an L2
+// hint (pass 1 asks L2 to keep x, pass 2 marks its last use); 8 consumer
+// warps work from the ring, so the bytes in flight per SM are the ring's,
+// independent of the consumers' arithmetic.
+constexpr int SU_CONSUMERS = 256;
+constexpr int SU_BPT = 2;                          // blocks per consumer thread and unit
+constexpr int SU_BLOCKS = SU_CONSUMERS * SU_BPT;   // 512 blocks
+constexpr int SU_BYTES = SU_BLOCKS * 32;           // 16 KB
+constexpr int SU_THREADS = SU_CONSUMERS + 32;      // + the producer warp
+// pass 1 streams x from HBM: a deep ring, 3 CTAs per SM; pass 2 normally
+// finds x in L2 and is arithmetic-heavy: a short ring and 6 CTAs per SM
+constexpr int SU_STAGES_1 = 4, SU_CTAS_1 = 3;
+constexpr int SU_STAGES_2 = 2, SU_CTAS_2 = 6;
+constexpr int su_smem(int stages) { return stages * SU_BYTES + 2 * stages * 8 + 16; }
+
+__device__ __forceinline__ void bulk_load_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                               uint64_t policy)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, "
+                 "[%3], %4;" ::"r"(smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+                 : "memory");
+}
+
+template <bool KEEP>
+__device__ __forceinline__ uint64_t l2_policy()
+{
+    uint64_t pol;
+    if (KEEP)
+        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    else
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Named barrier 1 over the consumer warps only.
+__device__ __forceinline__ void consumers_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(SU_CONSUMERS) : "memory");
+}
+
+__device__ __forceinline__ uint32_t consumers_max(uint32_t v, uint32_t *red)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = max(v, __shfl_xor_sync(FULL, v, o));
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = v;
+    consumers_sync();
+    uint32_t r = 0;
+#pragma unroll
+    for (int i = 0; i < SU_CONSUMERS / 32; ++i)
+        r = max(r, red[i]);
+    consumers_sync();
+    return r;
+}
+
+// The block scale code of a block whose |x| maximum has BF16 magnitude bits
+// mb, from a per-CTA table: for amax = (1 + i/128) * 2^k the quantisers'
+// u = RN(RN(amax / 6) / s) equals U[i] * 2^k with U[i] = RN(RN((1 + i/128)
+// / 6) / s) whenever RN(amax / 6) and u are normal binary32 numbers (round to
+// nearest commutes with exact power-of-two scaling), and any u below the
+// normal range gives code 0 either way, as an overflow gives 448 either way.
+// So when s lies in [2^-100, 2^100] (U normal) and amax >= 2^-123 (amax / 6
+// normal) the code is e4m3(U[i] * 2^k), bit-identical to block_scale_code;
+// other blocks take block_scale_code itself.
+__device__ __forceinline__ uint32_t scale_code_tab(uint32_t mb, float sg, bool fast, const float *tab_u)
+{
+    const uint32_t eb = mb >> 7;
+    if (fast && eb >= 4u)
+        return e4m3(__fmul_rn(tab_u[mb & 127u], __uint_as_float(eb << 23)));
+    return block_scale_code(__uint_as_float(mb << 16), sg);
+}
+
+// PASS 1: per-CTA maximum of |x| magnitude bits into partial[blockIdx.x] and
+// the non-finite flag.  PASS 2: tensor scale from the partial maxima, then
+// the block encode of every block (and zero scales for the tiled padding
+// rows when zero_pad).  Units go to CTAs round robin.
+template <int PASS, bool TILED, int SU_STAGES>
+__global__ void __launch_bounds__(SU_THREADS) stream_quant_kernel(const uint16_t *__restrict__ x, int64_t rows,
+                                                                  int64_t rows_pad, int64_t K,
+                                                                  uint8_t *__restrict__ codes,
+                                                                  uint8_t *__restrict__ scales,
+                                                                  float *__restrict__ sg_out,
+                                                                  uint32_t *__restrict__ partial, int n_partial,
+                                                                  int zero_pad, uint32_t *__restrict__ status,
+                                                                  uint64_t timeout_ns)
+{
+    extern __shared__ __align__(128) uint8_t sq[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(sq + SU_STAGES * SU_BYTES);
+    uint64_t *empty = full + SU_STAGES;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + SU_STAGES);
+    __shared__ uint32_t red[SU_CONSUMERS / 32];
+    __shared__ float tab_u[PASS == 2 ? 128 : 1]; // scale_code_tab's U
+    __shared__ float tab_r[PASS == 2 ? 128 : 1]; // reciprocal step of every scale code
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < SU_STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], SU_CONSUMERS / 32);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // a programmatic dependent: wait for the previous grid before touching
+    // memory it may use (pass 2: the partial maxima of pass 1)
+    pdl_wait();
+    pdl_trigger();
+    const int64_t bpr = K / 16;
+    const int64_t total = rows * bpr;
+    const int64_t units = (total + SU_BLOCKS - 1) / SU_BLOCKS;
+
+    if (warp == SU_CONSUMERS / 32) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            const uint64_t pol = l2_policy<PASS == 1>();
+            int s = 0, issued = 0;
+            uint32_t ph = 0;
+            for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+                if (!mbar_wait(&empty[s], ph ^ 1u, timeout_ns, abort_flag)) {
+                    *abort_flag = 1;
+                    atomicOr(status, ST_TIMEOUT);
+                    break;
+                }
+                const int64_t nb = min((int64_t)SU_BLOCKS, total - u * SU_BLOCKS);
+                mbar_arrive_expect_tx(&full[s], (uint32_t)(nb * 32));
+                bulk_load_hint(sq + s * SU_BYTES, x + u * SU_BLOCKS * 16, (uint32_t)(nb * 32), &full[s], pol);
+                ++issued;
+                if (++s == SU_STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            // every copy issued lands before the CTA exits
+            for (int q = 0; q < min(issued, SU_STAGES); ++q) {
+                if (--s < 0) {
+                    s = SU_STAGES - 1;
+                    ph ^= 1u;
+                }
+                mbar_wait(&full[s], ph, timeout_ns, nullptr);
+            }
+        }
+        return;
+    }
+
+    // -------------------------------------------------------------- consumers
+    const int t = threadIdx.x;
+    float sg = 0.0f;
+    bool fast = false;
+    if (PASS == 2) {
+        uint32_t m = 0;
+        for (int i = t; i < n_partial; i += SU_CONSUMERS)
+            m = max(m, partial[i]);
+        const float amax = __uint_as_float(consumers_max(m, red) << 16);
+        sg = __fdiv_rn(amax, 2688.0f);
+        if (blockIdx.x == 0 && t == 0)
+            *sg_out = sg;
+        fast = sg >= 0x1p-100f && sg <= 0x1p100f;
+        if (t < 128) {
+            if (fast)
+                tab_u[t] = __fdiv_rn(__fdiv_rn(1.0f + (float)t * 0.0078125f, 6.0f), sg);
+            // codes 0x00..0x7E are all a non-negative saturating conversion gives
+            tab_r[t] = recip_step(__fmul_rn(e4m3_value(t < 127 ? (uint32_t)t : 0u), sg));
+        }
+        consumers_sync();
+    }
+    // block b = u * SU_BLOCKS + k * SU_CONSUMERS + t of unit u, k < SU_BPT:
+    // (row, block-in-row) cursors advanced by the round-robin unit step
+    Cursor cur[SU_BPT];
+#pragma unroll
+    for (int k = 0; k < SU_BPT; ++k) {
+        const int64_t b0 = (int64_t)blockIdx.x * SU_BLOCKS + k * SU_CONSUMERS + t;
+        cur[k] = Cursor{b0 / bpr, b0 % bpr};
+    }
+    const int64_t step = (int64_t)gridDim.x * SU_BLOCKS;
+    const int64_t qi = step / bpr, ri = step % bpr;
+    uint32_t m2 = 0;
+    int s = 0;
+    uint32_t ph = 0;
+    for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+        const bool got = mbar_wait(&full[s], ph, timeout_ns, abort_flag);
+        if (!__all_sync(FULL, got)) {
+            if (lane == 0) {
+                *abort_flag = 1;
+                atomicOr(status, ST_TIMEOUT);
+            }
+            break;
+        }
+        const uint8_t *src = sq + s * SU_BYTES;
+#pragma unroll
+        for (int k = 0; k < SU_BPT; ++k) {
+            const int slot = k * SU_CONSUMERS + t;
+            if (u * SU_BLOCKS + slot < total) {
+                const uint4 a = *reinterpret_cast<const uint4 *>(src + slot * 32);
+                const uint4 b = *reinterpret_cast<const uint4 *>(src + slot * 32 + 16);
+                const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                if (PASS == 1) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        m2 = __vmaxu2(m2, w[i] & 0x7FFF7FFFu);
+                } else {
+                    uint32_t mb2 = 0;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        mb2 = __vmaxu2(mb2, w[i] & 0x7FFF7FFFu);
+                    const uint32_t e = scale_code_tab(max(mb2 & 0xFFFFu, mb2 >> 16), sg, fast, tab_u);
+                    const float r = tab_r[e];
+                    uint32_t pk[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t pw = 0;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint32_t ww = w[4 * h + i];
+                            float q0, q1;
+                            mul2_rn(__uint_as_float(ww << 16), __uint_as_float(ww & 0xFFFF0000u), r, q0, q1);
+                            pw |= e2m1x2(q0, q1) << (8 * i);
+                        }
+                        pk[h] = pw;
+                    }
+                    // codes are contiguous: block b's 8 bytes sit at 8 b
+                    const int64_t b = u * SU_BLOCKS + slot;
+                    *reinterpret_cast<uint2 *>(codes + b * 8) = make_uint2(pk[0], pk[1]);
+                    scales[TILED ? scale_offset(cur[k].row, cur[k].j, K, true) : (size_t)b] = (uint8_t)e;
+                }
+            }
+            cursor_advance(cur[k], qi, ri, bpr);
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&empty[s]);
+        if (++s == SU_STAGES) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+    if (PASS == 1) {
+        const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+        const bool bad = __any_sync(FULL, m >= 0x7F80u);
+        const uint32_t bm = consumers_max(m, red);
+        if (t == 0)
+            partial[blockIdx.x] = bm;
+        if (bad && lane == 0)
+            atomicOr(status, ST_NONFINITE);
+    } else if (TILED && zero_pad) {
+        zero_pad_scales(scales, rows, rows_pad, K, (int64_t)blockIdx.x * SU_CONSUMERS + t,
+                        (int64_t)gridDim.x * SU_CONSUMERS);
+    }
+}
+
 // Small activations (decode): one kernel on one thread-block cluster of FC
 // CTAs.  Each thread holds up to FQ chunks of x in registers (a warp stops at
 // its last real chunk); every CTA pushes its absolute maximum into all CTAs'
@@ -584,9 +838,29 @@ cudaError_t launch_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K, in
         return cudaLaunchKernelEx(&cfg, nvfp4_encode_small_kernel<false>, x, rows, rows_pad, K, ldx, codes, scales, sg,
                                   status, zp);
     }
-    if (mode == NVFP4_SCALE_TENSOR_FP32) {
-        // flat passes: enough CTAs for one sweep of QU loads per thread, at
-        // most a few waves
+    if (mode == NVFP4_SCALE_TENSOR_FP32 && ldx == K) {
+        // contiguous x: the staged streaming passes, 3 CTAs per SM
+        const int64_t units = ceil_div(std::max<int64_t>(rows * (K / 16), 1), (int64_t)SU_BLOCKS);
+        const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(units, std::min(AMAX_MAX_CTAS, sms * SU_CTAS_1)));
+        const uint64_t tmo = 2000000000ull;
+        float *sg = static_cast<float *>(second);
+        const int grid2 = (int)std::max<int64_t>(1, std::min<int64_t>(units, (int64_t)sms * SU_CTAS_2));
+        auto k1 = stream_quant_kernel<1, false, SU_STAGES_1>;
+        auto k2 = tiled ? stream_quant_kernel<2, true, SU_STAGES_2> : stream_quant_kernel<2, false, SU_STAGES_2>;
+        cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, su_smem(SU_STAGES_1));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, su_smem(SU_STAGES_2));
+        if (e == cudaSuccess)
+            e = launch_pdl(k1, grid, SU_THREADS, su_smem(SU_STAGES_1), stream, x, rows, rows_pad, K, codes, scales,
+                           sg, amax_partial, 0, zp, status, tmo);
+        if (e == cudaSuccess)
+            e = launch_pdl(k2, grid2, SU_THREADS, su_smem(SU_STAGES_2), stream, x, rows, rows_pad, K, codes, scales,
+                           sg, amax_partial, grid, zp, status, tmo);
+        if (e != cudaSuccess)
+            return e;
+    } else if (mode == NVFP4_SCALE_TENSOR_FP32) {
+        // strided x: flat passes with register loads; enough CTAs for one
+        // sweep of QU loads per thread, at most a few waves
         const int64_t blocks1 = std::max<int64_t>(rows * (K / 16), 1);
         const int64_t per_cta = (int64_t)QT * QU;
         const int grid1 = (int)std::min<int64_t>(ceil_div(blocks1, per_cta), std::min(AMAX_MAX_CTAS, sms * 4));

@@ -191,3 +191,31 @@ def test_two_pass_alignment_fallback_bit_exact(offset, pitch):
     from helpers import untile_scales
     np.testing.assert_array_equal(untile_scales(host(t.scales), 128, K)[:M], os_)
     assert host(t.second)[0] == og
+
+
+def _every_magnitude_tensor(top_bits, seed):
+    """[64, 8192] BF16 (two-pass, contiguous: the staged path) whose 32768
+    16-element blocks take every positive BF16 magnitude pattern 0x0001 ..
+    top_bits as their maximum in turn (random sign and position), the other
+    15 elements random magnitudes not above it; the tensor maximum is
+    top_bits, which fixes the tensor scale."""
+    rng = np.random.default_rng(seed)
+    nb = 64 * 8192 // 16
+    pats = (np.arange(nb) % top_bits + 1).astype(np.uint32)
+    other = (rng.random((nb, 16)) * (pats[:, None] + 1)).astype(np.uint32)
+    other = np.minimum(other, pats[:, None])
+    other[np.arange(nb), rng.integers(0, 16, nb)] = pats
+    sign = rng.integers(0, 2, (nb, 16)).astype(np.uint32) << 15
+    return (other | sign).astype(np.uint16).reshape(64, 8192)
+
+
+# The staged encode pass takes block scales from a per-CTA table when the
+# tensor scale lies in [2^-100, 2^100] and the block maximum is at least
+# 2^-123, and the direct division otherwise: every block magnitude up to
+# the tensor maximum, with tensor maxima whose scale is inside the range
+# (1.0: s = 2^-11.4), just inside and just outside either end
+# (s = 2^-99.93, 2^-100.07, 2^99.95, 2^100.07) and far above it (2^116.6).
+@pytest.mark.parametrize("top", [0x3F80, 0x1330, 0x1320, 0x7720, 0x7730, 0x7F7F])
+def test_staged_path_every_block_magnitude(top):
+    assert_same(_every_magnitude_tensor(top, top))
+    assert_same(_every_magnitude_tensor(top, top + 1), layout=nv.LAYOUT_ROW_MAJOR)

@@ -60,13 +60,19 @@ constexpr int EPI_FIRST_WARP = 3;
 constexpr int THREADS = 32 * (EPI_FIRST_WARP + EPI_WARPS);
 constexpr int MAX_EXPERTS = 1024;
 
-template <int BN>
+// AR: activation rows one stage holds.  128 in general; 16 for the decode
+// shapes (M <= 16), whose stages then take 14 KB less shared memory, which
+// buys a deeper ring (more weight bytes in flight per SM).  The MMA still
+// reads 128 rows; rows past the 16 loaded ones read whatever follows in
+// shared memory and only feed output rows that are never stored.
+template <int BN, int AR = BM>
 struct Cfg {
     static_assert(BN == 128 || BN == 256, "N tile");
+    static_assert(AR == BM || AR == 16, "activation rows per stage");
     static constexpr int NB = BN / 128;                 // 128-row scale groups per B tile
-    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int STAGES = AR == BM ? (BN == 256 ? 4 : 6) : (BN == 256 ? 5 : 8);
     static constexpr int ACC_BUFS = BN == 256 ? 1 : 2;
-    static constexpr int A_BYTES = BM * STAGE_K_BYTES;
+    static constexpr int A_BYTES = AR * STAGE_K_BYTES;
     static constexpr int B_BYTES = BN * STAGE_K_BYTES;
     static constexpr int SFA_BYTES = 4 * 512;           // compact atoms as loaded
     static constexpr int SFB_BYTES = NB * 4 * 512;
@@ -404,10 +410,10 @@ __device__ __forceinline__ void q_row(const Params &p, int64_t i, uint8_t *&crow
     srow = p.yq_scales + (i >> 7) * (n / 64) * 512 + (r7 & 31) * 16 + (r7 >> 5) * 4;
 }
 
-template <int BN, bool GROUPED>
+template <int BN, bool GROUPED, int AR>
 __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant__ Params p)
 {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, AR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE_BYTES);
@@ -1086,11 +1092,11 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
     }
 }
 
-template <int BN, bool GROUPED>
+template <int BN, bool GROUPED, int AR = BM>
 cudaError_t launch(const Params &p, int grid_units, cudaStream_t stream)
 {
-    using C = Cfg<BN>;
-    auto kern = w4a4_kernel<BN, GROUPED>;
+    using C = Cfg<BN, AR>;
+    auto kern = w4a4_kernel<BN, GROUPED, AR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess)
         return e;
@@ -1105,6 +1111,9 @@ cudaError_t dispatch(int bn, bool grouped, const Params &p, int grid_units, cuda
 {
     if (grouped)
         return bn == 256 ? launch<256, true>(p, grid_units, stream) : launch<128, true>(p, grid_units, stream);
+    if (p.a_box_rows <= 16)
+        return bn == 256 ? launch<256, false, 16>(p, grid_units, stream)
+                         : launch<128, false, 16>(p, grid_units, stream);
     return bn == 256 ? launch<256, false>(p, grid_units, stream) : launch<128, false>(p, grid_units, stream);
 }
 

@@ -45,8 +45,8 @@ FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6400.0, 1800.0
 # DRAM bytes (read + write) per launch of the roofline kernel, from one ncu
 # capture of the current kernel (profiles/ holds the capture and command);
 # None until a capture of the current kernel exists.
-TRAFFIC = {"decode": 135.61e6,    # w4a4_kernel<256,false>, 8x28672x8192: 132.31 MB read + 3.30 MB written
-           "prefill": 345.66e6}   # w4a4_kernel<256,false>, 4096x28672x8192: 151.97 MB read + 193.69 MB written
+TRAFFIC = {"decode": 136.20e6,    # w4a4_kernel<256,false,16>, 8x28672x8192: 132.32 MB read + 3.88 MB written
+           "prefill": None}       # w4a4_kernel<256,false>: changed since its counters were taken
 
 
 def peaks():

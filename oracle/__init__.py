@@ -348,6 +348,79 @@ def moe_down_combine(h, offsets, w_codes, w_scales, w_sg, token_idx, gate_w, T, 
     return y
 
 
+# ---- NVFP4 KV cache and decode attention ---------------------------------------
+#
+# "The FP4 Inflection" (section "What does this mean for model serving
+# engines?") stores the KV cache in FP4 and names paged attention as the
+# consumer; the TensorRT-LLM page's engine-build listing pages the KV cache in
+# blocks of 64 tokens; "AdaLLM Breakthrough" pairs a low-precision KV cache
+# with its own decode kernel.  None prints the cache encoding or the attention
+# formula.  Readings taken: every cached key and value vector of one KV head
+# (head_dim D elements) is encoded by the same block encoder as the
+# activations -- 16-element blocks along D, E4M3 block scales, under a static
+# FP32 tensor scale per cache tensor fixed beforehand (as for the fused
+# output quantiser) -- and decode attention is the standard scaled dot-product
+# attention of one query token over the sequence's cached tokens, with the
+# query heads of a group sharing one KV head.
+
+def bf16_to_f32(bits):
+    """Exact binary32 values of BF16 bit patterns (a format conversion)."""
+    b = np.ascontiguousarray(bits, np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32)
+
+
+def kv_encode(x_bf16, s):
+    """KV-cache encode of BF16 vectors [n, D] under the static tensor scale s:
+    the given-scale block encode of their exact binary32 values.
+    Returns (codes uint8 [n, D/2], scales uint8 [n, D/16])."""
+    return nvfp4_encode_f32_scaled(bf16_to_f32(x_bf16), s)
+
+
+def kv_gather(codes_pages, scales_pages, s, block_table_row, n_tokens, head):
+    """Dequantised FP64 vectors [n_tokens, D] of one sequence and KV head from
+    paged storage: token t lives in page block_table_row[t // P] at slot
+    t % P (P = tokens per page); codes_pages [pages, H_kv, P, D/2]."""
+    P = codes_pages.shape[2]
+    rows_c, rows_s = [], []
+    for t in range(n_tokens):
+        pg = int(block_table_row[t // P])
+        rows_c.append(codes_pages[pg, head, t % P])
+        rows_s.append(scales_pages[pg, head, t % P])
+    if not rows_c:
+        return np.zeros((0, codes_pages.shape[3] * 2))
+    return nvfp4_dequant(np.stack(rows_c), np.stack(rows_s), s)
+
+
+def decode_attention(q, k_cache, v_cache, s_k, s_v, block_table, ctx_lens, sm_scale):
+    """One decode step of scaled dot-product attention over an NVFP4 paged KV
+    cache, in FP64.
+
+    q: float [B, H, D] (the BF16 queries' exact values); k_cache / v_cache:
+    (codes [pages, H_kv, P, D/2], scales [pages, H_kv, P, D/16]); block_table
+    int [B, max_pages]; ctx_lens int [B]; query head h reads KV head
+    h // (H / H_kv).  Returns o [B, H, D]:
+    o[b, h] = sum_t softmax_t(sm_scale * q[b, h] . k_t) v_t over the
+    ctx_lens[b] cached tokens (o = 0 for an empty context)."""
+    q = np.asarray(q, np.float64)
+    B, H, D = q.shape
+    H_kv = k_cache[0].shape[1]
+    G = H // H_kv
+    o = np.zeros((B, H, D))
+    for b in range(B):
+        n = int(ctx_lens[b])
+        if n == 0:
+            continue
+        for hk in range(H_kv):
+            K = kv_gather(k_cache[0], k_cache[1], s_k, block_table[b], n, hk)
+            V = kv_gather(v_cache[0], v_cache[1], s_v, block_table[b], n, hk)
+            for g in range(G):
+                h = hk * G + g
+                sc = sm_scale * (K @ q[b, h])
+                w = np.exp(sc - sc.max())
+                o[b, h] = (w / w.sum()) @ V
+    return o
+
+
 def threads():
     """OpenMP threads the oracle's parallel loops use."""
     return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))

@@ -25,6 +25,7 @@ bounded sample of the same workload on this machine's host cores.
 """
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -421,6 +422,51 @@ def workload_moe_ffn(c, steps, warmup):
             "tflops": flops / (ms * 1e-3) / 1e12, "device_status": work.status()}
 
 
+def workload_kv_decode(c, steps, warmup, B=16, H=64, H_kv=8, ctx=4096):
+    """Decode attention over an NVFP4 paged KV cache (Llama-3-70B-class
+    grouping: 64 query heads over 8 KV heads, head_dim 128), 16 sequences of
+    4096 cached tokens each, plus the append of each sequence's new token:
+    the step reads the whole cache once.  Cache bytes are synthetic (random
+    codes, scale bytes in a normal range); pages shuffled across the pool."""
+    t, nv = c.torch, c.nv
+    P, D = nv.KV_PAGE, nv.KV_HEAD_DIM
+    pages_per = ctx // P + 1
+    n_pages = B * pages_per
+    g = t.Generator(device=c.dev)
+    g.manual_seed(0)
+    ks = t.tensor([8.0 / 2688], device=c.dev)
+    vs = t.tensor([4.0 / 2688], device=c.dev)
+    cache = nv.KvCache.empty(n_pages, H_kv, ks, vs, device=c.dev)
+    for buf in (cache.k_codes, cache.v_codes):
+        buf.copy_(t.randint(0, 256, buf.shape, dtype=t.uint8, device=c.dev, generator=g))
+    for buf in (cache.k_scales, cache.v_scales):
+        buf.copy_(t.randint(0x28, 0x48, buf.shape, dtype=t.uint8, device=c.dev, generator=g))
+    perm = t.randperm(n_pages, device=c.dev, generator=g).to(t.int32)
+    table = perm.view(B, pages_per).contiguous()
+    ctx_lens = t.full((B,), ctx, dtype=t.int32, device=c.dev)
+    pos = t.full((B,), ctx, dtype=t.int32, device=c.dev)
+    q = t.randn((B, H, D), device=c.dev, generator=g).to(t.bfloat16)
+    k_new = t.randn((B, H_kv, D), device=c.dev, generator=g).to(t.bfloat16)
+    v_new = t.randn((B, H_kv, D), device=c.dev, generator=g).to(t.bfloat16)
+    out = t.empty((B, H, D), dtype=t.bfloat16, device=c.dev)
+    work = nv.Workspace(nv.workspace_size(nv.OP_KV_DECODE, B, H, ctx + 1, H_kv))
+    sm = 1.0 / math.sqrt(D)
+    ctx1 = t.full((B,), ctx + 1, dtype=t.int32, device=c.dev)
+
+    def step(i):
+        nv.kv_append(cache, k_new, v_new, pos, table)
+        nv.kv_decode_attention(cache, q, ctx1, table, ctx + 1, sm, out=out, ws=work)
+
+    def attn_only(i):
+        nv.kv_decode_attention(cache, q, ctx_lens, table, ctx, sm, out=out, ws=work)
+
+    ms = c.time(step, steps, warmup)
+    ams = c.time(attn_only, steps, warmup)
+    cache_bytes = B * H_kv * ctx * 2 * (D // 2 + D // 16)
+    return {"ms": ms, "attn_ms": ams, "bytes": cache_bytes, "value": cache_bytes / (ms * 1e-3) / 1e9,
+            "attn_gbs": cache_bytes / (ams * 1e-3) / 1e9, "device_status": work.status()}
+
+
 # ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
 def oracle_decode_sample(M=8, n_rows=2048, reps=1):
     """The oracle's decode step (encode X, dequantise-and-contract in FP64)
@@ -555,6 +601,11 @@ def main():
                                               "routes": q["routes"]}
         fq = workload_fused_stack(c, min(es, 20), 2)
         extras["policy_stack_q4_fused"] = {"value": fq["value"], "unit": "TFLOP/s", "ms": fq["ms"]}
+        kd = workload_kv_decode(c, min(es, 50), 3)
+        extras["kv_decode_attention"] = {"value": kd["value"], "unit": "GB/s", "ms": kd["ms"],
+                                         "frac_hbm": kd["value"] / hbm, "attn_gbs": kd["attn_gbs"],
+                                         "attn_frac_hbm": kd["attn_gbs"] / hbm,
+                                         "config": "16 seqs x 4096 tokens, 64 q heads / 8 kv heads, d 128"}
         mf = workload_moe_ffn(c, min(es, 50), 2)
         extras["moe_ffn_fused"] = {"value": mf["value"], "unit": "GB/s", "ms": mf["ms"], "tflops": mf["tflops"],
                                    "frac_hbm": mf["value"] / hbm}

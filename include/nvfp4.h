@@ -114,7 +114,8 @@ typedef enum nvfp4_op {
     NVFP4_OP_GEMM = 2,         /* M, N, K; covers both routes and on-the-fly quantisation */
     NVFP4_OP_W4A8_GEMM = 3,    /* M, N, K */
     NVFP4_OP_GROUPED_GEMM = 4, /* M = total routed rows, N, K, E experts */
-    NVFP4_OP_GROUPED_GEMM_X = 5 /* M = T activation rows (tokens), N, K, E; both routes */
+    NVFP4_OP_GROUPED_GEMM_X = 5, /* M = T activation rows (tokens), N, K, E; both routes */
+    NVFP4_OP_KV_DECODE = 6       /* M = sequences, N = query heads, K = max context, E = KV heads */
 } nvfp4_op;
 
 /* ---- sizing and workspace ------------------------------------------------ */
@@ -317,6 +318,65 @@ nvfp4_status nvfp4_moe_down_combine(const nvfp4_tensor *h, const int64_t *expert
                                     const int32_t *token_idx, const float *gate_w, float *y,
                                     int64_t ldy, int64_t T, int64_t total_rows, void *ws,
                                     size_t ws_bytes, nvfp4_stream_t stream);
+
+/* ---- NVFP4 paged KV cache and decode attention -------------------------------
+ * "The FP4 Inflection" (serving-engine section) keeps the KV cache in FP4 with
+ * paged attention as its consumer; the [TRT] engine build pages it in blocks
+ * of 64 tokens; [ADA] pairs a low-precision cache with its own decode kernel.
+ * Readings: every cached key / value head vector (head_dim 128) is encoded by
+ * the activation block encoder ([TRT] item 2: 16 elements along head_dim, E4M3
+ * block scales) under a static FP32 tensor scale per cache tensor fixed
+ * beforehand (calibration), and decode attention is scaled dot-product
+ * attention of one query token over its sequence's cached tokens, query head
+ * h reading KV head h / (num_heads / num_kv_heads).
+ *
+ * Cache layout, per page (64 token slots) and KV head; all device memory
+ * owned by the caller, pages of one sequence listed in its block-table row:
+ *   k_codes  uint8 [num_pages][num_kv_heads][64][64]   token-major, element
+ *            2j of a token in the low nibble of byte j
+ *   k_scales E4M3  [num_pages][num_kv_heads][64][8]
+ *   v_codes  uint8 [num_pages][num_kv_heads][128][32]  dim-major: byte j of
+ *            row d holds tokens 2j (low nibble) and 2j+1 of dimension d
+ *   v_scales E4M3  [num_pages][num_kv_heads][8][64]     block b of token t
+ *   k_scale, v_scale: device float[1] tensor scales.
+ * A page belongs to one sequence; slots past a sequence's length may hold
+ * anything (the attention ignores them). */
+typedef struct nvfp4_kv_cache {
+    void *k_codes;
+    void *k_scales;
+    void *v_codes;
+    void *v_scales;
+    const float *k_scale;
+    const float *v_scale;
+    int32_t num_pages;
+    int32_t num_kv_heads;
+    int32_t head_dim;    /* 128 */
+    int32_t page_tokens; /* 64 */
+} nvfp4_kv_cache;
+
+/* Encodes one new token per sequence into the cache: k_bf16 / v_bf16 BF16
+ * [B][num_kv_heads][128]; sequence b's token goes to slot positions[b] % 64 of
+ * page block_table[b * max_pages + positions[b] / 64].  Sequences whose
+ * position or page is out of range are skipped.  Two sequences must not write
+ * the same page in one call. */
+nvfp4_status nvfp4_kv_append(const nvfp4_kv_cache *kv, const void *k_bf16, const void *v_bf16,
+                             const int32_t *positions, const int32_t *block_table, int32_t max_pages,
+                             int32_t B, nvfp4_stream_t stream);
+
+/* One decode step of attention: q BF16 [B][num_heads][128]; sequence b
+ * attends to its first min(ctx_lens[b], max_ctx) cached tokens;
+ * out[b][h] = sum_t softmax_t(sm_scale * q[b][h] . k_t) v_t with the cached
+ * keys and values decoded (E2M1 x E4M3 x tensor scale), BF16 or FP32
+ * [B][num_heads][128]; an empty context gives zeros.  num_heads is a multiple
+ * of num_kv_heads with at most 16 query heads per KV head.  Long contexts
+ * are split across CTAs and merged in a second kernel.
+ * Workspace: nvfp4_workspace_size(NVFP4_OP_KV_DECODE, B, num_heads, max_ctx,
+ * num_kv_heads). */
+nvfp4_status nvfp4_kv_decode_attention(const nvfp4_kv_cache *kv, const void *q_bf16, int32_t num_heads,
+                                       const int32_t *ctx_lens, const int32_t *block_table,
+                                       int32_t max_pages, int32_t B, int32_t max_ctx, float sm_scale,
+                                       void *out, int32_t out_dtype, void *ws, size_t ws_bytes,
+                                       nvfp4_stream_t stream);
 
 /* ---- no-allocation variant --------------------------------------------------- */
 

@@ -26,14 +26,14 @@ POLICY_AUTO, POLICY_Q4, POLICY_Q8 = 0, 1, 2
 SCALE_TENSOR_FP32, SCALE_MACRO_FP16 = 0, 1
 LAYOUT_ROW_MAJOR, LAYOUT_MMA_TILED = 0, 1
 OUT_BF16, OUT_FP32 = 0, 1
-OP_QUANTIZE, OP_QUANTIZE_FP8, OP_GEMM, OP_W4A8_GEMM, OP_GROUPED_GEMM, OP_GROUPED_GEMM_X = range(6)
+OP_QUANTIZE, OP_QUANTIZE_FP8, OP_GEMM, OP_W4A8_GEMM, OP_GROUPED_GEMM, OP_GROUPED_GEMM_X, OP_KV_DECODE = range(7)
 
 EXPORTED = ["nvfp4_scale_bytes", "nvfp4_workspace_size", "nvfp4_workspace_init", "nvfp4_device_status",
             "nvfp4_policy_route", "nvfp4_quantize", "nvfp4_quantize_fp8", "nvfp4_gemm", "nvfp4_w4a8_gemm",
             "nvfp4_grouped_gemm", "nvfp4_probe_convert", "nvfp4_sm_count", "nvfp4_version",
             "nvfp4_gemm_w4a4_noalloc", "nvfp4_gemm_nvfp4_out", "nvfp4_moe_up_swiglu",
             "nvfp4_moe_down_combine", "nvfp4_grouped_w4a8_gemm", "nvfp4_grouped_gemm_x",
-            "nvfp4_diag_streamk_skip_flag"]
+            "nvfp4_diag_streamk_skip_flag", "nvfp4_kv_append", "nvfp4_kv_decode_attention"]
 
 
 class NVFP4Error(RuntimeError):
@@ -46,6 +46,13 @@ class TensorDesc(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("second", ctypes.c_void_p),
                 ("rows", ctypes.c_int64), ("K", ctypes.c_int64), ("mode", ctypes.c_int32),
                 ("layout", ctypes.c_int32)]
+
+
+class KvCacheDesc(ctypes.Structure):
+    _fields_ = [("k_codes", ctypes.c_void_p), ("k_scales", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
+                ("v_scales", ctypes.c_void_p), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("num_pages", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("page_tokens", ctypes.c_int32)]
 
 
 _LIB = None
@@ -82,6 +89,9 @@ def lib():
                                                _VP, _SZ, _VP]),
             "nvfp4_grouped_gemm_x": (_I32, [_VP, _I64, _I64, _VP, _VP, _I32, _PT, _I64, _VP, _I64, _I32, _I64,
                                             _I32, _I32, _VP, _SZ, _VP]),
+            "nvfp4_kv_append": (_I32, [ctypes.POINTER(KvCacheDesc), _VP, _VP, _VP, _VP, _I32, _I32, _VP]),
+            "nvfp4_kv_decode_attention": (_I32, [ctypes.POINTER(KvCacheDesc), _VP, _I32, _VP, _VP, _I32, _I32,
+                                                 _I32, ctypes.c_float, _VP, _I32, _VP, _SZ, _VP]),
             "nvfp4_moe_up_swiglu": (_I32, [_PT, _VP, _VP, _I32, _PT, _I64, _VP, _I64, _I32, _PT, _VP, _I64,
                                            _VP, _SZ, _VP]),
             "nvfp4_moe_down_combine": (_I32, [_PT, _VP, _I32, _PT, _I64, _VP, _VP, _VP, _I64, _I64, _I64,
@@ -412,3 +422,69 @@ def moe_down_combine(h: NVFP4Tensor, offsets: torch.Tensor, w_down: NVFP4Tensor,
                                         _ptr(token_idx), _ptr(gate_w), _ptr(y), y.stride(0), y.shape[0], R,
                                         ws.ptr, ws.nbytes, _stream(stream)), "nvfp4_moe_down_combine")
     return y
+
+
+# ---- NVFP4 paged KV cache --------------------------------------------------------------
+
+KV_PAGE = 64
+KV_HEAD_DIM = 128
+
+
+@dataclasses.dataclass
+class KvCache:
+    """Device NVFP4 paged KV cache (layouts in include/nvfp4.h): per page and
+    KV head, K codes [64][64], K scales [64][8], V codes [128][32] (dim-major),
+    V scales [8][64]; static tensor scales k_scale / v_scale (float32 [1])."""
+    k_codes: torch.Tensor
+    k_scales: torch.Tensor
+    v_codes: torch.Tensor
+    v_scales: torch.Tensor
+    k_scale: torch.Tensor
+    v_scale: torch.Tensor
+    num_pages: int
+    num_kv_heads: int
+
+    @staticmethod
+    def empty(num_pages: int, num_kv_heads: int, k_scale: torch.Tensor, v_scale: torch.Tensor,
+              device="cuda") -> "KvCache":
+        P, D = KV_PAGE, KV_HEAD_DIM
+        z = lambda *shape: torch.zeros(shape, dtype=torch.uint8, device=device)
+        return KvCache(z(num_pages, num_kv_heads, P, D // 2), z(num_pages, num_kv_heads, P, D // 16),
+                       z(num_pages, num_kv_heads, D, P // 2), z(num_pages, num_kv_heads, D // 16, P),
+                       k_scale, v_scale, num_pages, num_kv_heads)
+
+    def desc(self) -> KvCacheDesc:
+        return KvCacheDesc(self.k_codes.data_ptr(), self.k_scales.data_ptr(), self.v_codes.data_ptr(),
+                           self.v_scales.data_ptr(), self.k_scale.data_ptr(), self.v_scale.data_ptr(),
+                           self.num_pages, self.num_kv_heads, KV_HEAD_DIM, KV_PAGE)
+
+
+def kv_append(cache: KvCache, k_new: torch.Tensor, v_new: torch.Tensor, positions: torch.Tensor,
+              block_table: torch.Tensor, stream=None):
+    """nvfp4_kv_append: one new token per sequence (BF16 [B][H_kv][128])."""
+    assert k_new.dtype == torch.bfloat16 and v_new.dtype == torch.bfloat16 and k_new.is_contiguous()
+    assert positions.dtype == torch.int32 and block_table.dtype == torch.int32 and block_table.is_contiguous()
+    B = k_new.shape[0]
+    d = cache.desc()
+    _check(lib().nvfp4_kv_append(ctypes.byref(d), _ptr(k_new), _ptr(v_new.contiguous()), _ptr(positions),
+                                 _ptr(block_table), block_table.shape[1], B, _stream(stream)), "nvfp4_kv_append")
+
+
+def kv_decode_attention(cache: KvCache, q: torch.Tensor, ctx_lens: torch.Tensor, block_table: torch.Tensor,
+                        max_ctx: int, sm_scale: float, out_dtype: int = OUT_BF16,
+                        out: Optional[torch.Tensor] = None, ws: Optional[Workspace] = None,
+                        stream=None) -> torch.Tensor:
+    """nvfp4_kv_decode_attention: q BF16 [B][H][128] -> out [B][H][128]."""
+    assert q.dtype == torch.bfloat16 and q.is_contiguous() and q.shape[2] == KV_HEAD_DIM
+    assert ctx_lens.dtype == torch.int32 and block_table.dtype == torch.int32 and block_table.is_contiguous()
+    B, H, D = q.shape
+    if out is None:
+        out = torch.empty((B, H, D), dtype=torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32,
+                          device=q.device)
+    ws = _ws(ws, workspace_size(OP_KV_DECODE, B, H, max_ctx, cache.num_kv_heads), q.device)
+    d = cache.desc()
+    _check(lib().nvfp4_kv_decode_attention(ctypes.byref(d), _ptr(q), H, _ptr(ctx_lens), _ptr(block_table),
+                                           block_table.shape[1], B, max_ctx, float(sm_scale), _ptr(out),
+                                           out_dtype, ws.ptr, ws.nbytes, _stream(stream)),
+           "nvfp4_kv_decode_attention")
+    return out

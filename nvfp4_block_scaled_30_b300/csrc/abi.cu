@@ -73,12 +73,13 @@ struct WsLayout {
     size_t a_st = 0;
     size_t sk_slots = 0;  // stream-K FP32 partial tiles, one per CTA
     size_t sk_flags = 0;  // stream-K ready flags, one per CTA, kept zero between calls
+    size_t kv_partial = 0; // decode attention: per-split partial outputs
     size_t total = 0;
 };
 
 static constexpr int64_t SPLITK_MAX_M = 128;
 
-static WsLayout ws_layout(int op, int64_t M, int64_t N, int64_t K)
+static WsLayout ws_layout(int op, int64_t M, int64_t N, int64_t K, int64_t E = 0)
 {
     WsLayout L;
     size_t off = WS_HEADER;
@@ -96,6 +97,14 @@ static WsLayout ws_layout(int op, int64_t M, int64_t N, int64_t K)
         L.a_second = take(std::max<size_t>(16, (size_t)(M * (K / 256) * 2)));
         L.a_fp8 = take((size_t)(M * K));
         L.a_st = take((size_t)(M * 4));
+    }
+    if (op == NVFP4_OP_KV_DECODE) {
+        // M = sequences, N = query heads, K = max context, E = KV heads
+        int ns = 1, kps = 64;
+        kv_attn_splits(M, E, K, device_sm_count(), ns, kps);
+        const size_t pb = kv_attn_partial_bytes((int)M, (int)N, ns);
+        if (pb)
+            L.kv_partial = take(pb);
     }
     if (op == NVFP4_OP_GEMM && M <= SPLITK_MAX_M) {
         const StreamKPlan pl = w4a4_streamk_plan(M, N, K, device_sm_count());
@@ -249,9 +258,9 @@ nvfp4_status nvfp4_workspace_size(int32_t op, int64_t M, int64_t N, int64_t K, i
 {
     if (!bytes || M < 0 || N < 0 || K < 0 || E < 0 || M > MAX_DIM || N > MAX_DIM || K > MAX_DIM)
         return NVFP4_ERR_INVALID_ARG;
-    if (op < NVFP4_OP_QUANTIZE || op > NVFP4_OP_GROUPED_GEMM_X)
+    if (op < NVFP4_OP_QUANTIZE || op > NVFP4_OP_KV_DECODE)
         return NVFP4_ERR_INVALID_ARG;
-    *bytes = ws_layout(op, M, N, K).total;
+    *bytes = ws_layout(op, M, N, K, E).total;
     return NVFP4_OK;
 }
 
@@ -714,6 +723,102 @@ nvfp4_status nvfp4_grouped_gemm_x(const void *x_bf16, int64_t ldx, int64_t T, co
     if (e != cudaSuccess)
         return NVFP4_ERR_CUDA;
     return from_cuda(launch_w4a4_grouped(g, s));
+}
+
+static nvfp4_status check_kv(const nvfp4_kv_cache *kv)
+{
+    if (!kv || !kv->k_codes || !kv->k_scales || !kv->v_codes || !kv->v_scales || !kv->k_scale || !kv->v_scale)
+        return NVFP4_ERR_INVALID_ARG;
+    if (kv->head_dim != 128 || kv->page_tokens != 64)
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (kv->num_pages <= 0 || kv->num_kv_heads <= 0 || !aligned(kv->k_codes, 16) || !aligned(kv->k_scales, 16) ||
+        !aligned(kv->v_codes, 16) || !aligned(kv->v_scales, 16) || !aligned(kv->k_scale, 4) ||
+        !aligned(kv->v_scale, 4))
+        return NVFP4_ERR_INVALID_ARG;
+    return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_kv_append(const nvfp4_kv_cache *kv, const void *k_bf16, const void *v_bf16,
+                             const int32_t *positions, const int32_t *block_table, int32_t max_pages, int32_t B,
+                             nvfp4_stream_t stream)
+{
+    nvfp4_status st = check_kv(kv);
+    if (st != NVFP4_OK)
+        return st;
+    if (B < 0 || max_pages <= 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (B == 0)
+        return NVFP4_OK;
+    if (!k_bf16 || !v_bf16 || !positions || !block_table || !aligned(k_bf16, 2) || !aligned(v_bf16, 2) ||
+        !aligned(positions, 4) || !aligned(block_table, 4))
+        return NVFP4_ERR_INVALID_ARG;
+    KvAppendArgs a{};
+    a.k_new = static_cast<const uint16_t *>(k_bf16);
+    a.v_new = static_cast<const uint16_t *>(v_bf16);
+    a.positions = positions;
+    a.block_table = block_table;
+    a.B = B;
+    a.H_kv = kv->num_kv_heads;
+    a.max_pages = max_pages;
+    a.num_pages = kv->num_pages;
+    a.k_codes = static_cast<uint8_t *>(kv->k_codes);
+    a.k_scales = static_cast<uint8_t *>(kv->k_scales);
+    a.v_codes = static_cast<uint8_t *>(kv->v_codes);
+    a.v_scales = static_cast<uint8_t *>(kv->v_scales);
+    a.k_scale = kv->k_scale;
+    a.v_scale = kv->v_scale;
+    return from_cuda(launch_kv_append(a, (cudaStream_t)stream));
+}
+
+nvfp4_status nvfp4_kv_decode_attention(const nvfp4_kv_cache *kv, const void *q_bf16, int32_t num_heads,
+                                       const int32_t *ctx_lens, const int32_t *block_table, int32_t max_pages,
+                                       int32_t B, int32_t max_ctx, float sm_scale, void *out, int32_t out_dtype,
+                                       void *ws, size_t ws_bytes, nvfp4_stream_t stream)
+{
+    nvfp4_status st = check_kv(kv);
+    if (st != NVFP4_OK)
+        return st;
+    const int H_kv = kv->num_kv_heads;
+    if (B < 0 || max_pages <= 0 || max_ctx < 0 || num_heads <= 0 || num_heads % H_kv != 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (num_heads / H_kv > 16)
+        return NVFP4_ERR_UNSUPPORTED_SHAPE; // up to 16 query heads per KV head
+    if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32)
+        return NVFP4_ERR_INVALID_ARG;
+    if (!(sm_scale == sm_scale) || sm_scale < 0.0f || sm_scale > 1e30f)
+        return NVFP4_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(NVFP4_OP_KV_DECODE, B, num_heads, max_ctx, H_kv);
+    if ((st = check_ws(ws, ws_bytes, L.total)) != NVFP4_OK)
+        return st;
+    if (B == 0)
+        return NVFP4_OK;
+    if (!q_bf16 || !ctx_lens || !block_table || !out || !aligned(q_bf16, 2) || !aligned(ctx_lens, 4) ||
+        !aligned(block_table, 4) || !aligned(out, 4))
+        return NVFP4_ERR_INVALID_ARG;
+    KvAttnArgs a{};
+    a.q = static_cast<const uint16_t *>(q_bf16);
+    a.ctx_lens = ctx_lens;
+    a.block_table = block_table;
+    a.B = B;
+    a.H = num_heads;
+    a.H_kv = H_kv;
+    a.max_pages = max_pages;
+    a.num_pages = kv->num_pages;
+    a.max_ctx = max_ctx;
+    a.k_codes = static_cast<const uint8_t *>(kv->k_codes);
+    a.k_scales = static_cast<const uint8_t *>(kv->k_scales);
+    a.v_codes = static_cast<const uint8_t *>(kv->v_codes);
+    a.v_scales = static_cast<const uint8_t *>(kv->v_scales);
+    a.k_scale = kv->k_scale;
+    a.v_scale = kv->v_scale;
+    a.sm_scale = sm_scale;
+    kv_attn_splits(B, H_kv, max_ctx, device_sm_count(), a.n_splits, a.keys_per_split);
+    a.out = out;
+    a.out_dtype = out_dtype;
+    a.partial = L.kv_partial ? reinterpret_cast<float *>(ws_at(ws, L.kv_partial)) : nullptr;
+    a.status = status_word(ws);
+    a.timeout_ns = DEFAULT_TIMEOUT_NS;
+    return from_cuda(launch_kv_decode(a, (cudaStream_t)stream));
 }
 
 nvfp4_status nvfp4_moe_up_swiglu(const nvfp4_tensor *a, const int32_t *row_idx, const int64_t *expert_offsets,

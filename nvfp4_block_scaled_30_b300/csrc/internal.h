@@ -165,6 +165,39 @@ struct W4A8GemmArgs {
 };
 cudaError_t launch_w4a8(const W4A8GemmArgs &g, cudaStream_t stream);
 
+// ---- NVFP4 paged KV cache (kv_attention.cu) -----------------------------------------
+// head_dim 128, 64 tokens per page; layouts in include/nvfp4.h (nvfp4_kv_cache)
+struct KvAppendArgs {
+    const uint16_t *k_new, *v_new; // BF16 [B][H_kv][128]
+    const int32_t *positions;      // [B] slot of the new token in its sequence
+    const int32_t *block_table;    // [B][max_pages]
+    int B, H_kv, max_pages, num_pages;
+    uint8_t *k_codes, *k_scales, *v_codes, *v_scales;
+    const float *k_scale, *v_scale;
+};
+cudaError_t launch_kv_append(const KvAppendArgs &a, cudaStream_t stream);
+
+struct KvAttnArgs {
+    const uint16_t *q;             // BF16 [B][H][128]
+    const int32_t *ctx_lens;       // [B]
+    const int32_t *block_table;    // [B][max_pages]
+    int B, H, H_kv, max_pages, num_pages, max_ctx;
+    const uint8_t *k_codes, *k_scales, *v_codes, *v_scales;
+    const float *k_scale, *v_scale;
+    float sm_scale;
+    int keys_per_split, n_splits;  // keys_per_split % 64 == 0
+    void *out;                     // [B][H][128]
+    int out_dtype;
+    float *partial;                // [B][H][n_splits][130] when n_splits > 1
+    uint32_t *status;
+    uint64_t timeout_ns;
+};
+size_t kv_attn_partial_bytes(int B, int H, int n_splits);
+// Context splits of one decode-attention call: one wave of 3 CTAs per SM,
+// at least 256 keys (one page per warp) per split.
+void kv_attn_splits(int64_t B, int64_t H_kv, int64_t max_ctx, int sms, int &n_splits, int &keys_per_split);
+cudaError_t launch_kv_decode(const KvAttnArgs &a, cudaStream_t stream);
+
 struct MacroGemmArgs {
     const uint8_t *a_codes;
     const uint8_t *a_scales;  // tiled

@@ -1,0 +1,512 @@
+// NVFP4 paged KV cache: append of one token per sequence and decode attention.
+//
+// "The FP4 Inflection: Rethinking AI Inference Architecture" (section "What
+// does this mean for model serving engines?") stores the KV cache in FP4 and
+// names paged attention as its consumer; the engine-build listing of "NVIDIA
+// Ships TensorRT-LLM 0.16" pages the cache in blocks of 64 tokens.  Cached key
+// and value head vectors use the activation block encoder (16 elements along
+// head_dim, E4M3 block scales) under a static FP32 tensor scale per cache
+// tensor; attention is scaled dot-product attention of one query token over
+// the cached tokens, the query heads of a group sharing one KV head.
+//
+// Page layout (head_dim D = 128, 64 tokens per page, per page and KV head):
+//   K codes  [64 tokens][64 bytes]   (token-major, element 2j in the low nibble)
+//   K scales [64 tokens][8]
+//   V codes  [128 dims][32 bytes]    (dim-major: byte j of row d holds tokens
+//                                     2j (low nibble) and 2j+1 of dim d)
+//   V scales [8 blocks][64 tokens]
+// so that every tensor-core operand fragment of the attention comes straight
+// from code bytes: K rows feed the B operand of S = Q K^T, V rows (dims)
+// feed the B operand of O = P V, both through ldmatrix.
+//
+// Decode attention, one CTA per (sequence, KV head, split of the context),
+// 4 warps; each warp streams its own pages (4 bulk copies per page into a
+// 2-stage per-warp ring) and runs mma.sync m16n8k16 (FP16 operands, FP32
+// accumulation): this contraction has M = the group's query heads (<= 16),
+// far below the 64/128 rows of a tcgen05 MMA, and the kernel is bound by
+// reading the cache, not by tensor throughput.  Online softmax in FP32 (base
+// 2); warps merge through shared memory; splits merge in a second kernel.
+#include <algorithm>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace nv4 {
+
+namespace {
+
+constexpr int KV_D = 128;           // head_dim
+constexpr int KV_P = 64;            // tokens per page
+constexpr int KC_BYTES = KV_P * KV_D / 2;   // 4096
+constexpr int KS_BYTES = KV_P * KV_D / 16;  // 512
+constexpr int PAGE_BYTES = 2 * (KC_BYTES + KS_BYTES);
+constexpr int ATT_WARPS = 4;
+constexpr int ATT_STAGES = 2;
+
+__device__ __forceinline__ uint32_t h2_e2m1x2(uint32_t byte)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(r) : "r"(byte));
+    return r;
+}
+
+// f16x2 of two E4M3 bytes (lo in bits 0..7, hi in bits 8..15).
+__device__ __forceinline__ uint32_t h2_e4m3x2(uint32_t two)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)two));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b)
+{
+    __half2 r = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
+{
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ void ldsm_x4(const void *row_addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(row_addr)));
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                 "{%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ---- append ------------------------------------------------------------------------
+// One thread per 16-element block of one new key or value vector.
+__global__ void kv_append_kernel(KvAppendArgs a)
+{
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int nblk = KV_D / 16;
+    const int64_t total = (int64_t)a.B * a.H_kv * 2 * nblk;
+    if (tid >= total)
+        return;
+    const int blk = (int)(tid % nblk);
+    const int which = (int)((tid / nblk) % 2); // 0 key, 1 value
+    const int hk = (int)((tid / (2 * nblk)) % a.H_kv);
+    const int b = (int)(tid / (2 * nblk * a.H_kv));
+    const int pos = a.positions[b];
+    if (pos < 0 || pos / KV_P >= a.max_pages)
+        return;
+    const int page = a.block_table[(int64_t)b * a.max_pages + pos / KV_P];
+    if (page < 0 || page >= a.num_pages)
+        return;
+    const int slot = pos % KV_P;
+    const uint16_t *src = (which ? a.v_new : a.k_new) + ((int64_t)b * a.H_kv + hk) * KV_D + blk * 16;
+    float x[16];
+    float amb = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        x[i] = __uint_as_float((uint32_t)src[i] << 16);
+        amb = fmaxf(amb, fabsf(x[i]));
+    }
+    const float s = *(which ? a.v_scale : a.k_scale);
+    const uint32_t e = block_scale_code(amb, s);
+    const float r = recip_step(__fmul_rn(e4m3_value(e), s));
+    const int64_t ph = (int64_t)page * a.H_kv + hk;
+    if (!which) {
+        uint32_t pk[2] = {0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            pk[i >> 2] |= e2m1x2(__fmul_rn(x[2 * i], r), __fmul_rn(x[2 * i + 1], r)) << (8 * (i & 3));
+        *reinterpret_cast<uint2 *>(a.k_codes + ph * KC_BYTES + slot * (KV_D / 2) + blk * 8) = make_uint2(pk[0], pk[1]);
+        a.k_scales[ph * KS_BYTES + slot * (KV_D / 16) + blk] = (uint8_t)e;
+    } else {
+        uint8_t *vc = a.v_codes + ph * KC_BYTES;
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+            const uint32_t two = e2m1x2(__fmul_rn(x[i], r), __fmul_rn(x[i + 1], r));
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t c = (two >> (4 * h)) & 15u;
+                uint8_t *p = vc + (blk * 16 + i + h) * (KV_P / 2) + slot / 2;
+                *p = (slot & 1) ? (uint8_t)((*p & 0x0Fu) | (c << 4)) : (uint8_t)((*p & 0xF0u) | c);
+            }
+        }
+        a.v_scales[ph * KS_BYTES + blk * KV_P + slot] = (uint8_t)e;
+    }
+}
+
+// ---- decode attention ------------------------------------------------------------------
+
+// The page ring is dead once every warp has left its loop, so the warps'
+// partial outputs reuse it for the merge (3 CTAs fit on an SM).
+struct AttMerge {
+    float o[ATT_WARPS][16][KV_D];
+    float m[ATT_WARPS][16];
+    float l[ATT_WARPS][16];
+};
+struct AttSmem {
+    union {
+        uint8_t page[ATT_WARPS][ATT_STAGES][PAGE_BYTES]; // per warp: K codes, K scales, V codes, V scales
+        AttMerge merge;
+    };
+    uint64_t full[ATT_WARPS][ATT_STAGES];
+};
+static_assert(sizeof(AttMerge) <= ATT_WARPS * ATT_STAGES * PAGE_BYTES, "merge buffer fits in the ring");
+
+// Key order inside a 32-key chunk: QK n-tile j (8 keys) column n holds key
+// 8 (n / 2) + (n % 2) + 2 j, so that the S fragment of n-tiles 0, 1 (2, 3)
+// is exactly the P operand of the first (second) 16-key step of O = P V,
+// whose k slots 2t, 2t+1, 2t+8, 2t+9 hold keys 8t .. 8t+3 (8t+4 .. 8t+7): the
+// keys of V code byte 4t .. 4t+1 (4t+2 .. 4t+3) that ldmatrix hands lane t.
+__device__ __forceinline__ int chunk_key(int j, int n) { return 8 * (n >> 1) + (n & 1) + 2 * j; }
+
+__global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_kernel(const KvAttnArgs a)
+{
+    extern __shared__ __align__(128) uint8_t att_raw[];
+    AttSmem &sm = *reinterpret_cast<AttSmem *>(att_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+    const int G = a.H / a.H_kv;
+    const int ctx = max(0, min(min(a.ctx_lens[b], a.max_ctx), a.max_pages * KV_P));
+    const int k_begin = split * a.keys_per_split;
+    const int k_end = min(ctx, k_begin + a.keys_per_split);
+    const int n_pages = k_end > k_begin ? (k_end - k_begin + KV_P - 1) / KV_P : 0;
+
+    if (lane == 0) {
+        for (int s = 0; s < ATT_STAGES; ++s)
+            mbar_init(&sm.full[warp][s], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    // query fragments (A operand of S = Q K^T): rows = the group's heads (row
+    // g and g + 8), k slots of 16-dim step 2c + u hold dims 32 c + 8 t + 4 u
+    // + {0, 1} (slots 2t, 2t+1) and + {2, 3} (slots 2t+8, 2t+9), matching
+    // the dims ldmatrix hands lane t from a 16-byte chunk of a key row.
+    // Scores in base 2: q is pre-multiplied by sm_scale * log2(e).
+    uint32_t qf[8][4];
+    {
+        const float qs = a.sm_scale * 1.4426950408889634f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int d0 = 32 * c + 8 * t + 4 * u;
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int head = g + 8 * rr;
+                    float v[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (head < G) {
+                        const uint16_t *q = a.q + ((int64_t)b * a.H + hk * G + head) * KV_D + d0;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            v[i] = __uint_as_float((uint32_t)q[i] << 16) * qs;
+                    }
+                    qf[2 * c + u][rr] = pack_h2(v[0], v[1]);
+                    qf[2 * c + u][2 + rr] = pack_h2(v[2], v[3]);
+                }
+            }
+    }
+    const float s_k = *a.k_scale, s_v = *a.v_scale;
+
+    float o[16][4];
+#pragma unroll
+    for (int n = 0; n < 16; ++n)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            o[n][i] = 0.0f;
+    float m_run[2] = {-INFINITY, -INFINITY}; // rows g, g + 8 (base-2 scores of unit K)
+    float l_run[2] = {0.0f, 0.0f};           // this lane's share of the row sums
+
+    // pages of this warp: p = warp, warp + 4, ... of the CTA's range
+    auto issue = [&](int p, int s) {
+        const int tok = k_begin + p * KV_P;
+        const int page = a.block_table[(int64_t)b * a.max_pages + tok / KV_P];
+        const int64_t ph = (int64_t)min(max(page, 0), a.num_pages - 1) * a.H_kv + hk;
+        uint8_t *dst = sm.page[warp][s];
+        mbar_arrive_expect_tx(&sm.full[warp][s], PAGE_BYTES);
+        bulk_load(dst, a.k_codes + ph * KC_BYTES, KC_BYTES, &sm.full[warp][s]);
+        bulk_load(dst + KC_BYTES, a.k_scales + ph * KS_BYTES, KS_BYTES, &sm.full[warp][s]);
+        bulk_load(dst + KC_BYTES + KS_BYTES, a.v_codes + ph * KC_BYTES, KC_BYTES, &sm.full[warp][s]);
+        bulk_load(dst + 2 * KC_BYTES + KS_BYTES, a.v_scales + ph * KS_BYTES, KS_BYTES, &sm.full[warp][s]);
+    };
+    if (lane == 0) {
+        for (int i = 0; i < ATT_STAGES && warp + i * ATT_WARPS < n_pages; ++i)
+            issue(warp + i * ATT_WARPS, i);
+    }
+    bool ok = true;
+    int it = 0;
+    for (int p = warp; p < n_pages; p += ATT_WARPS, ++it) {
+        const int s = it % ATT_STAGES;
+        const uint32_t par = (uint32_t)(it / ATT_STAGES) & 1u;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sm.full[warp][s], par, a.timeout_ns, nullptr))) {
+            if (lane == 0)
+                atomicOr(a.status, ST_TIMEOUT);
+            ok = false;
+            break;
+        }
+        const uint8_t *kc = sm.page[warp][s];
+        const uint8_t *ks = kc + KC_BYTES;
+        const uint8_t *vc = ks + KS_BYTES;
+        const uint8_t *vs = vc + KC_BYTES;
+        const int tok0 = k_begin + p * KV_P;
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) { // 32-key chunks of the page
+            const int key0 = 32 * h;
+            const int valid = min(32, k_end - (tok0 + key0)); // keys of this chunk in the context
+            if (valid <= 0)
+                break;
+            // ---- S = Q K^T over 32 keys: 4 n-tiles x 8 k-steps
+            float sc[4][4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                // lane (g, t) supplies key chunk_key(j, g): 4 x 16 bytes of its row
+                // (ldmatrix matrix i = dims 32 i .. 32 i + 31)
+                const int krow = key0 + chunk_key(j, lane & 7);
+                uint32_t kr[4];
+                ldsm_x4(kc + krow * (KV_D / 2) + 16 * (lane >> 3), kr);
+                const int myrow = key0 + chunk_key(j, g);
+                const uint2 sc8 = *reinterpret_cast<const uint2 *>(ks + myrow * (KV_D / 16));
+                const uint32_t sb[2] = {sc8.x, sc8.y}; // block scales of this lane's key, 8 bytes
+                sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.0f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    // dims 32 c + 8 t .. + 7 lie in block 2 c + t / 2
+                    const uint32_t e = (sb[c >> 1] >> (8 * (2 * (c & 1) + (t >> 1)))) & 0xFFu;
+                    const uint32_t e2 = h2_e4m3x2(e * 0x0101u);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const uint32_t b0 = hmul2u(h2_e2m1x2((kr[c] >> (16 * u)) & 0xFFu), e2);
+                        const uint32_t b1 = hmul2u(h2_e2m1x2((kr[c] >> (16 * u + 8)) & 0xFFu), e2);
+                        mma16816(sc[j], qf[2 * c + u], b0, b1);
+                    }
+                }
+            }
+            // ---- online softmax (base 2; scores already carry sm_scale * log2 e / s_k)
+            // key of sc[j][i]: chunk_key(j, 2t + (i & 1)); rows g (i < 2), g + 8
+            float cmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int key = chunk_key(j, 2 * t + (i & 1));
+                    float v = sc[j][i] * s_k;
+                    v = key < valid ? v : -INFINITY;
+                    sc[j][i] = v;
+                    cmax[i >> 1] = fmaxf(cmax[i >> 1], v);
+                }
+            float corr[2];
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                cmax[rr] = fmaxf(cmax[rr], __shfl_xor_sync(0xFFFFFFFFu, cmax[rr], 1));
+                cmax[rr] = fmaxf(cmax[rr], __shfl_xor_sync(0xFFFFFFFFu, cmax[rr], 2));
+                const float mn = fmaxf(m_run[rr], cmax[rr]);
+                corr[rr] = mn == -INFINITY ? 1.0f : exp2f(m_run[rr] - mn);
+                m_run[rr] = mn;
+                l_run[rr] *= corr[rr];
+            }
+#pragma unroll
+            for (int n = 0; n < 16; ++n) {
+                o[n][0] *= corr[0];
+                o[n][1] *= corr[0];
+                o[n][2] *= corr[1];
+                o[n][3] *= corr[1];
+            }
+            uint32_t pf[2][4]; // P fragments of the two 16-key steps
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float pv[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float mm = m_run[i >> 1];
+                    pv[i] = mm == -INFINITY ? 0.0f : exp2f(sc[j][i] - mm);
+                    l_run[i >> 1] += pv[i];
+                }
+                // n-tile j -> step j / 2; even j: k slots 2t, 2t+1; odd j: 2t+8, 2t+9
+                pf[j >> 1][(j & 1) * 2 + 0] = pack_h2(pv[0], pv[1]);
+                pf[j >> 1][(j & 1) * 2 + 1] = pack_h2(pv[2], pv[3]);
+            }
+            // ---- O += P V: 2 k-steps x 16 n-tiles (dims), V rows via ldmatrix
+            // keys 8t .. 8t+7 of this chunk are valid up to `valid`
+            const bool full_chunk = valid >= 32;
+            const int nv = min(8, max(0, valid - 8 * t));
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                // 4 n-tiles = 32 dims: lane supplies V row (dim) 32 q4 + lane
+                uint32_t vr[4];
+                ldsm_x4(vc + (32 * q4 + lane) * (KV_P / 2) + 16 * h, vr);
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb) {
+                    // n-tiles 2 hb, 2 hb + 1: dims 32 q4 + 16 hb + 0..15, scale block 2 q4 + hb;
+                    // scales of keys 8t .. 8t+7 as four f16x2 pairs
+                    const uint2 e8 = *reinterpret_cast<const uint2 *>(vs + (2 * q4 + hb) * KV_P + key0 + 8 * t);
+                    uint32_t e2[4];
+#pragma unroll
+                    for (int y = 0; y < 4; ++y)
+                        e2[y] = h2_e4m3x2(((y < 2 ? e8.x : e8.y) >> (16 * (y & 1))) & 0xFFFFu);
+#pragma unroll
+                    for (int n4 = 2 * hb; n4 < 2 * hb + 2; ++n4) {
+                        uint32_t bv[4];
+#pragma unroll
+                        for (int y = 0; y < 4; ++y) {          // byte y: keys 8t+2y, 8t+2y+1
+                            uint32_t val = hmul2u(h2_e2m1x2((vr[n4] >> (8 * y)) & 0xFFu), e2[y]);
+                            if (!full_chunk) {
+                                if (2 * y >= nv)
+                                    val = 0u;
+                                else if (2 * y + 1 >= nv)
+                                    val &= 0x0000FFFFu;
+                            }
+                            bv[y] = val;
+                        }
+                        mma16816(o[4 * q4 + n4], pf[0], bv[0], bv[1]);
+                        mma16816(o[4 * q4 + n4], pf[1], bv[2], bv[3]);
+                    }
+                }
+            }
+        }
+        // the stage is free again: this warp's next page goes into it
+        __syncwarp();
+        if (lane == 0 && p + ATT_STAGES * ATT_WARPS < n_pages) {
+            fence_proxy_async_smem();
+            issue(p + ATT_STAGES * ATT_WARPS, s);
+        }
+    }
+    // drain: every copy this warp issued lands before the CTA moves on
+    if (lane == 0 && !ok) {
+        const int mine = n_pages > warp ? (n_pages - warp + ATT_WARPS - 1) / ATT_WARPS : 0;
+        for (int i = it; i < mine && i < it + ATT_STAGES; ++i)
+            mbar_wait(&sm.full[warp][i % ATT_STAGES], (uint32_t)(i / ATT_STAGES) & 1u, a.timeout_ns, nullptr);
+    }
+
+    // ---- merge the warps: row sums over the 4 lanes of a group, then through
+    // shared memory (the page ring, now idle in every warp)
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        l_run[rr] += __shfl_xor_sync(0xFFFFFFFFu, l_run[rr], 1);
+        l_run[rr] += __shfl_xor_sync(0xFFFFFFFFu, l_run[rr], 2);
+    }
+    __syncthreads();
+    AttMerge &mg = sm.merge;
+    if (t == 0) {
+        mg.m[warp][g] = m_run[0];
+        mg.m[warp][g + 8] = m_run[1];
+        mg.l[warp][g] = l_run[0];
+        mg.l[warp][g + 8] = l_run[1];
+    }
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+        mg.o[warp][g][8 * n + 2 * t] = o[n][0];
+        mg.o[warp][g][8 * n + 2 * t + 1] = o[n][1];
+        mg.o[warp][g + 8][8 * n + 2 * t] = o[n][2];
+        mg.o[warp][g + 8][8 * n + 2 * t + 1] = o[n][3];
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < G * KV_D; idx += 32 * ATT_WARPS) {
+        const int head = idx / KV_D, d = idx % KV_D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < ATT_WARPS; ++w)
+            M = fmaxf(M, mg.m[w][head]);
+        float L = 0.0f, O = 0.0f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < ATT_WARPS; ++w) {
+                const float f = mg.m[w][head] == -INFINITY ? 0.0f : exp2f(mg.m[w][head] - M);
+                L += f * mg.l[w][head];
+                O += f * mg.o[w][head][d];
+            }
+        }
+        const int64_t hq = (int64_t)b * a.H + hk * G + head;
+        if (a.n_splits == 1) {
+            const float y = L > 0.0f ? O * s_v / L : 0.0f;
+            if (a.out_dtype == NVFP4_OUT_BF16)
+                static_cast<__nv_bfloat16 *>(a.out)[hq * KV_D + d] = __float2bfloat16_rn(y);
+            else
+                static_cast<float *>(a.out)[hq * KV_D + d] = y;
+        } else {
+            float *part = a.partial + (hq * a.n_splits + split) * (KV_D + 2);
+            part[d] = O;
+            if (d == 0) {
+                part[KV_D] = M;
+                part[KV_D + 1] = L;
+            }
+        }
+    }
+}
+
+// Merge of the splits: o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+__global__ void kv_combine_kernel(const KvAttnArgs a)
+{
+    const int64_t hq = blockIdx.x; // b * H + h
+    const int d = threadIdx.x;
+    const float *part = a.partial + hq * a.n_splits * (KV_D + 2);
+    float M = -INFINITY;
+    for (int s = 0; s < a.n_splits; ++s)
+        M = fmaxf(M, part[s * (KV_D + 2) + KV_D]);
+    float L = 0.0f, O = 0.0f;
+    if (M != -INFINITY)
+        for (int s = 0; s < a.n_splits; ++s) {
+            const float ms = part[s * (KV_D + 2) + KV_D];
+            const float f = ms == -INFINITY ? 0.0f : exp2f(ms - M);
+            L += f * part[s * (KV_D + 2) + KV_D + 1];
+            O += f * part[s * (KV_D + 2) + d];
+        }
+    const float y = L > 0.0f ? O * *a.v_scale / L : 0.0f;
+    if (a.out_dtype == NVFP4_OUT_BF16)
+        static_cast<__nv_bfloat16 *>(a.out)[hq * KV_D + d] = __float2bfloat16_rn(y);
+    else
+        static_cast<float *>(a.out)[hq * KV_D + d] = y;
+}
+
+} // namespace
+
+cudaError_t launch_kv_append(const KvAppendArgs &a, cudaStream_t stream)
+{
+    const int64_t threads = (int64_t)a.B * a.H_kv * 2 * (KV_D / 16);
+    if (threads == 0)
+        return cudaSuccess;
+    kv_append_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+void kv_attn_splits(int64_t B, int64_t H_kv, int64_t max_ctx, int sms, int &n_splits, int &keys_per_split)
+{
+    // as many splits as keep every (sequence, KV head) CTA of the grid in one
+    // wave of 3 CTAs per SM
+    const int64_t units = std::max<int64_t>(1, B * H_kv);
+    int64_t ns = std::max<int64_t>(1, 3 * (int64_t)sms / units);
+    ns = std::min<int64_t>(ns, std::max<int64_t>(1, (max_ctx + 255) / 256));
+    int64_t kps = (std::max<int64_t>(max_ctx, 1) + ns - 1) / ns;
+    kps = (kps + KV_P - 1) / KV_P * KV_P;
+    n_splits = (int)std::max<int64_t>(1, (max_ctx + kps - 1) / kps);
+    keys_per_split = (int)kps;
+}
+
+size_t kv_attn_partial_bytes(int B, int H, int n_splits)
+{
+    return n_splits > 1 ? (size_t)B * H * n_splits * (KV_D + 2) * sizeof(float) : 0;
+}
+
+cudaError_t launch_kv_decode(const KvAttnArgs &a, cudaStream_t stream)
+{
+    const size_t smem = sizeof(AttSmem);
+    cudaError_t e = cudaFuncSetAttribute(kv_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    dim3 grid((unsigned)a.n_splits, (unsigned)a.H_kv, (unsigned)a.B);
+    kv_decode_kernel<<<grid, 32 * ATT_WARPS, smem, stream>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess || a.n_splits == 1)
+        return e;
+    kv_combine_kernel<<<(unsigned)(a.B * a.H), KV_D, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+} // namespace nv4

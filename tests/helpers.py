@@ -30,6 +30,31 @@ def interleave_gate_up(gate: np.ndarray, up: np.ndarray) -> np.ndarray:
     return np.concatenate([g, u], axis=2).reshape(E, 2 * I, -1)
 
 
+def kv_v_pages(codes_nat: np.ndarray, scales_nat: np.ndarray):
+    """Value pages from the natural per-token layout (codes [..., 64 tokens,
+    64 bytes], scales [..., 64, 8]) to the cache's dim-major layout (codes
+    [..., 128 dims, 32 bytes]: byte j of row d = tokens 2j (low nibble),
+    2j+1; scales [..., 8 blocks, 64 tokens]).  A pure relayout."""
+    c = np.asarray(codes_nat, np.uint8)
+    nib = np.empty(c.shape[:-1] + (c.shape[-1] * 2,), np.uint8)
+    nib[..., 0::2] = c & 15
+    nib[..., 1::2] = c >> 4                          # [..., token, dim]
+    nt = np.swapaxes(nib, -1, -2)                    # [..., dim, token]
+    v = (nt[..., 0::2] | (nt[..., 1::2] << 4)).astype(np.uint8)
+    return np.ascontiguousarray(v), np.ascontiguousarray(np.swapaxes(np.asarray(scales_nat, np.uint8), -1, -2))
+
+
+def kv_v_pages_natural(codes_dm: np.ndarray, scales_bm: np.ndarray):
+    """Inverse of kv_v_pages."""
+    c = np.asarray(codes_dm, np.uint8)
+    nib = np.empty(c.shape[:-1] + (c.shape[-1] * 2,), np.uint8)
+    nib[..., 0::2] = c & 15
+    nib[..., 1::2] = c >> 4                          # [..., dim, token]
+    nt = np.swapaxes(nib, -1, -2)                    # [..., token, dim]
+    k = (nt[..., 0::2] | (nt[..., 1::2] << 4)).astype(np.uint8)
+    return np.ascontiguousarray(k), np.ascontiguousarray(np.swapaxes(np.asarray(scales_bm, np.uint8), -1, -2))
+
+
 def bf16_half_ulp(y: np.ndarray) -> np.ndarray:
     """Half the BF16 spacing at |y| (the largest error of rounding y to BF16)."""
     a = np.abs(np.asarray(y, np.float64))

@@ -47,7 +47,7 @@ FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6400.0, 1800.0
 # capture of the current kernel (profiles/ holds the capture and command);
 # None until a capture of the current kernel exists.
 TRAFFIC = {"decode": 136.20e6,    # w4a4_kernel<256,false,16>, 8x28672x8192: 132.32 MB read + 3.88 MB written
-           "prefill": None}       # w4a4_kernel<256,false>: changed since its counters were taken
+           "prefill": 344.14e6}   # w4a4_kernel<256,false>, 4096x28672x8192: 151.90 MB read + 192.24 MB written
 
 
 def peaks():

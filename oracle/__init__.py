@@ -376,6 +376,34 @@ def kv_encode(x_bf16, s):
     return nvfp4_encode_f32_scaled(bf16_to_f32(x_bf16), s)
 
 
+def kv_encode_fp8(x_bf16, s):
+    """FP8 KV-cache encode ("AdaLLM Breakthrough" keeps an FP8 key-value
+    cache; the per-token FP8 quantiser's rule under a static tensor scale s):
+    code = E4M3_rne_sat(x * r) in binary32, r = 1/s (0 when s = 0, at most
+    FLT_MAX).  Returns uint8 [n, D]."""
+    x = bf16_to_f32(x_bf16)
+    s = np.float32(s)
+    if s == 0:
+        r = np.float32(0)
+    else:
+        with np.errstate(over="ignore"):
+            r = np.float32(1) / s
+        r = np.minimum(r, np.float32(np.finfo(np.float32).max))
+    prod = (x * r).astype(np.float32)
+    return e4m3_encode_array(prod).reshape(x.shape)
+
+
+def kv_gather_fp8(codes_pages, s, block_table_row, n_tokens, head):
+    """Decoded FP64 vectors [n_tokens, D] of one sequence and KV head of an
+    FP8 cache (codes_pages [pages, H_kv, P, D]): E4M3 value times s."""
+    P = codes_pages.shape[2]
+    rows = [codes_pages[int(block_table_row[t // P]), head, t % P] for t in range(n_tokens)]
+    if not rows:
+        return np.zeros((0, codes_pages.shape[3]))
+    table = np.array([e4m3_value(c & 0x7F) * (-1.0 if c & 0x80 else 1.0) for c in range(256)])
+    return table[np.stack(rows)] * float(np.float32(s))
+
+
 def kv_gather(codes_pages, scales_pages, s, block_table_row, n_tokens, head):
     """Dequantised FP64 vectors [n_tokens, D] of one sequence and KV head from
     paged storage: token t lives in page block_table_row[t // P] at slot
@@ -391,19 +419,20 @@ def kv_gather(codes_pages, scales_pages, s, block_table_row, n_tokens, head):
     return nvfp4_dequant(np.stack(rows_c), np.stack(rows_s), s)
 
 
-def decode_attention(q, k_cache, v_cache, s_k, s_v, block_table, ctx_lens, sm_scale):
+def decode_attention(q, k_cache, v_cache, s_k, s_v, block_table, ctx_lens, sm_scale, fmt="nvfp4"):
     """One decode step of scaled dot-product attention over an NVFP4 paged KV
     cache, in FP64.
 
     q: float [B, H, D] (the BF16 queries' exact values); k_cache / v_cache:
     (codes [pages, H_kv, P, D/2], scales [pages, H_kv, P, D/16]); block_table
     int [B, max_pages]; ctx_lens int [B]; query head h reads KV head
-    h // (H / H_kv).  Returns o [B, H, D]:
+    h // (H / H_kv); fmt "fp8": k_cache / v_cache are E4M3 codes
+    [pages, H_kv, P, D] alone.  Returns o [B, H, D]:
     o[b, h] = sum_t softmax_t(sm_scale * q[b, h] . k_t) v_t over the
     ctx_lens[b] cached tokens (o = 0 for an empty context)."""
     q = np.asarray(q, np.float64)
     B, H, D = q.shape
-    H_kv = k_cache[0].shape[1]
+    H_kv = (k_cache if fmt == "fp8" else k_cache[0]).shape[1]
     G = H // H_kv
     o = np.zeros((B, H, D))
     for b in range(B):
@@ -411,8 +440,12 @@ def decode_attention(q, k_cache, v_cache, s_k, s_v, block_table, ctx_lens, sm_sc
         if n == 0:
             continue
         for hk in range(H_kv):
-            K = kv_gather(k_cache[0], k_cache[1], s_k, block_table[b], n, hk)
-            V = kv_gather(v_cache[0], v_cache[1], s_v, block_table[b], n, hk)
+            if fmt == "fp8":
+                K = kv_gather_fp8(k_cache, s_k, block_table[b], n, hk)
+                V = kv_gather_fp8(v_cache, s_v, block_table[b], n, hk)
+            else:
+                K = kv_gather(k_cache[0], k_cache[1], s_k, block_table[b], n, hk)
+                V = kv_gather(v_cache[0], v_cache[1], s_v, block_table[b], n, hk)
             for g in range(G):
                 h = hk * G + g
                 sc = sm_scale * (K @ q[b, h])

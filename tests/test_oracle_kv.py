@@ -137,3 +137,42 @@ def test_grouped_query_heads_share_a_kv_head(orc):
     # an empty context gives zeros
     z = orc.decode_attention(q, kc, vc, 0.01, 0.01, np.array(table), np.array([0]), 0.125)
     assert not z.any()
+
+
+def test_fp8_encode_matches_the_token_quantiser_and_torch(orc):
+    # one row at its own amax / 448 scale is exactly the per-token FP8 encode
+    x = synth.activations(9, 91, 1, 128, 0.02, 30.0)
+    a, st = orc.fp8_token_encode(x)
+    np.testing.assert_array_equal(orc.kv_encode_fp8(x, st[0]), a)
+    # in-range products round like torch's E4M3 cast (an independent library)
+    import torch
+    xs = synth.activations(9, 92, 16, 128, 0.0, 1.0)
+    s = np.float32(0.01)
+    c = orc.kv_encode_fp8(xs, s)
+    prod = (orc.bf16_to_f32(xs) * (np.float32(1) / s)).astype(np.float32)
+    assert np.abs(prod).max() < 448
+    ref = torch.from_numpy(prod).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(c, ref)
+    # saturation at +-448 and exact decoding of E4M3 multiples of s
+    big = synth.bf16_bits(np.array([[1e4, -1e4, 2.0, 0.0]], np.float32))
+    np.testing.assert_array_equal(orc.kv_encode_fp8(big, 1.0), [[0x7E, 0xFE, 0x40, 0x00]])
+
+
+def test_fp8_attention_matches_the_fp4_formula_on_decoded_values(orc):
+    # the same attention definition over FP8 codes: single token and a
+    # hand-built two-token case with exactly representable values
+    D = 16
+    K = synth.bf16_bits(np.array([[0.375] + [0.0] * 15, [0.75] + [0.0] * 15], np.float32))
+    V = synth.bf16_bits(np.array([[0, 0, 0, 0.375] + [0.0] * 12, [0, 0, 0, -0.375] + [0.0] * 12], np.float32))
+    s = 2.0 ** -6
+    kc = np.zeros((1, 1, P, D), np.uint8)
+    vc = np.zeros((1, 1, P, D), np.uint8)
+    kc[0, 0, :2] = orc.kv_encode_fp8(K, s)
+    vc[0, 0, :2] = orc.kv_encode_fp8(V, s)
+    q = np.zeros((1, 1, D))
+    q[0, 0, 0] = 1.5
+    o = orc.decode_attention(q, kc, vc, s, s, np.array([[0]]), np.array([2]), 0.5, fmt="fp8")
+    w1, w2 = math.exp(0.28125), math.exp(0.5625)
+    assert o[0, 0, 3] == pytest.approx(0.375 * (w1 - w2) / (w1 + w2), rel=1e-14)
+    o1 = orc.decode_attention(q, kc, vc, s, s, np.array([[0]]), np.array([1]), 0.5, fmt="fp8")
+    assert o1[0, 0, 3] == 0.375 and np.count_nonzero(o1) == 1

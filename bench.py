@@ -427,7 +427,7 @@ def workload_moe_ffn(c, steps, warmup):
             "tflops": flops / (ms * 1e-3) / 1e12, "device_status": work.status()}
 
 
-def workload_kv_decode(c, steps, warmup, B=16, H=64, H_kv=8, ctx=4096):
+def workload_kv_decode(c, steps, warmup, B=16, H=64, H_kv=8, ctx=4096, fmt=0):
     """Decode attention over an NVFP4 paged KV cache (Llama-3-70B-class
     grouping: 64 query heads over 8 KV heads, head_dim 128), 16 sequences of
     4096 cached tokens each, plus the append of each sequence's new token:
@@ -441,11 +441,16 @@ def workload_kv_decode(c, steps, warmup, B=16, H=64, H_kv=8, ctx=4096):
     g.manual_seed(0)
     ks = t.tensor([8.0 / 2688], device=c.dev)
     vs = t.tensor([4.0 / 2688], device=c.dev)
-    cache = nv.KvCache.empty(n_pages, H_kv, ks, vs, device=c.dev)
+    cache = nv.KvCache.empty(n_pages, H_kv, ks, vs, device=c.dev, fmt=fmt)
     for buf in (cache.k_codes, cache.v_codes):
-        buf.copy_(t.randint(0, 256, buf.shape, dtype=t.uint8, device=c.dev, generator=g))
-    for buf in (cache.k_scales, cache.v_scales):
-        buf.copy_(t.randint(0x28, 0x48, buf.shape, dtype=t.uint8, device=c.dev, generator=g))
+        if fmt == nv.KV_FP8:   # finite E4M3 codes with random signs
+            buf.copy_(t.randint(0, 0x70, buf.shape, dtype=t.uint8, device=c.dev, generator=g)
+                      | (t.randint(0, 2, buf.shape, dtype=t.uint8, device=c.dev, generator=g) << 7))
+        else:
+            buf.copy_(t.randint(0, 256, buf.shape, dtype=t.uint8, device=c.dev, generator=g))
+    if fmt != nv.KV_FP8:
+        for buf in (cache.k_scales, cache.v_scales):
+            buf.copy_(t.randint(0x28, 0x48, buf.shape, dtype=t.uint8, device=c.dev, generator=g))
     perm = t.randperm(n_pages, device=c.dev, generator=g).to(t.int32)
     table = perm.view(B, pages_per).contiguous()
     ctx_lens = t.full((B,), ctx, dtype=t.int32, device=c.dev)
@@ -467,7 +472,7 @@ def workload_kv_decode(c, steps, warmup, B=16, H=64, H_kv=8, ctx=4096):
 
     ms = c.time(step, steps, warmup)
     ams = c.time(attn_only, steps, warmup)
-    cache_bytes = B * H_kv * ctx * 2 * (D // 2 + D // 16)
+    cache_bytes = B * H_kv * ctx * 2 * (D if fmt == nv.KV_FP8 else D // 2 + D // 16)
     return {"ms": ms, "attn_ms": ams, "bytes": cache_bytes, "value": cache_bytes / (ms * 1e-3) / 1e9,
             "attn_gbs": cache_bytes / (ams * 1e-3) / 1e9, "device_status": work.status()}
 
@@ -611,6 +616,11 @@ def main():
                                          "frac_hbm": kd["value"] / hbm, "attn_gbs": kd["attn_gbs"],
                                          "attn_frac_hbm": kd["attn_gbs"] / hbm,
                                          "config": "16 seqs x 4096 tokens, 64 q heads / 8 kv heads, d 128"}
+        kd8 = workload_kv_decode(c, min(es, 50), 3, fmt=nv.KV_FP8)
+        extras["kv_decode_attention_fp8"] = {"value": kd8["value"], "unit": "GB/s", "ms": kd8["ms"],
+                                             "frac_hbm": kd8["value"] / hbm, "attn_gbs": kd8["attn_gbs"],
+                                             "attn_frac_hbm": kd8["attn_gbs"] / hbm,
+                                             "config": "FP8 cache, 16 seqs x 4096 tokens, 64/8 heads, d 128"}
         mf = workload_moe_ffn(c, min(es, 50), 2)
         extras["moe_ffn_fused"] = {"value": mf["value"], "unit": "GB/s", "ms": mf["ms"], "tflops": mf["tflops"],
                                    "frac_hbm": mf["value"] / hbm}

@@ -330,17 +330,31 @@ nvfp4_status nvfp4_moe_down_combine(const nvfp4_tensor *h, const int64_t *expert
  * attention of one query token over its sequence's cached tokens, query head
  * h reading KV head h / (num_heads / num_kv_heads).
  *
+ * An FP8 cache ([ADA]: a custom FP8 key-value cache) is the alternative
+ * format: every element E4M3(x * 1/s) in binary32 (the per-token FP8 rule
+ * under the static scale s), no block scales.
+ *
  * Cache layout, per page (64 token slots) and KV head; all device memory
- * owned by the caller, pages of one sequence listed in its block-table row:
+ * owned by the caller, pages of one sequence listed in its block-table row.
+ * NVFP4_KV_NVFP4:
  *   k_codes  uint8 [num_pages][num_kv_heads][64][64]   token-major, element
  *            2j of a token in the low nibble of byte j
  *   k_scales E4M3  [num_pages][num_kv_heads][64][8]
  *   v_codes  uint8 [num_pages][num_kv_heads][128][32]  dim-major: byte j of
  *            row d holds tokens 2j (low nibble) and 2j+1 of dimension d
  *   v_scales E4M3  [num_pages][num_kv_heads][8][64]     block b of token t
- *   k_scale, v_scale: device float[1] tensor scales.
+ * NVFP4_KV_FP8 (k_scales, v_scales unused, may be NULL):
+ *   k_codes  E4M3  [num_pages][num_kv_heads][64][128]  token-major
+ *   v_codes  E4M3  [num_pages][num_kv_heads][2][128][32] two 32-token
+ *            halves, dim-major: byte j of row d of half h = token 32h + j
+ * Both: k_scale, v_scale are device float[1] tensor scales.
  * A page belongs to one sequence; slots past a sequence's length may hold
  * anything (the attention ignores them). */
+typedef enum nvfp4_kv_format {
+    NVFP4_KV_NVFP4 = 0,
+    NVFP4_KV_FP8 = 1
+} nvfp4_kv_format;
+
 typedef struct nvfp4_kv_cache {
     void *k_codes;
     void *k_scales;
@@ -352,6 +366,7 @@ typedef struct nvfp4_kv_cache {
     int32_t num_kv_heads;
     int32_t head_dim;    /* 128 */
     int32_t page_tokens; /* 64 */
+    int32_t format;      /* nvfp4_kv_format */
 } nvfp4_kv_cache;
 
 /* Encodes one new token per sequence into the cache: k_bf16 / v_bf16 BF16
@@ -366,7 +381,8 @@ nvfp4_status nvfp4_kv_append(const nvfp4_kv_cache *kv, const void *k_bf16, const
 /* One decode step of attention: q BF16 [B][num_heads][128]; sequence b
  * attends to its first min(ctx_lens[b], max_ctx) cached tokens;
  * out[b][h] = sum_t softmax_t(sm_scale * q[b][h] . k_t) v_t with the cached
- * keys and values decoded (E2M1 x E4M3 x tensor scale), BF16 or FP32
+ * keys and values decoded (E2M1 x E4M3 x tensor scale, or E4M3 x tensor
+ * scale in the FP8 format), BF16 or FP32
  * [B][num_heads][128]; an empty context gives zeros.  num_heads is a multiple
  * of num_kv_heads with at most 16 query heads per KV head.  Long contexts
  * are split across CTAs and merged in a second kernel.

@@ -727,12 +727,15 @@ nvfp4_status nvfp4_grouped_gemm_x(const void *x_bf16, int64_t ldx, int64_t T, co
 
 static nvfp4_status check_kv(const nvfp4_kv_cache *kv)
 {
-    if (!kv || !kv->k_codes || !kv->k_scales || !kv->v_codes || !kv->v_scales || !kv->k_scale || !kv->v_scale)
+    if (!kv || (kv->format != NVFP4_KV_NVFP4 && kv->format != NVFP4_KV_FP8))
+        return NVFP4_ERR_INVALID_ARG;
+    const bool fp4 = kv->format == NVFP4_KV_NVFP4;
+    if (!kv->k_codes || !kv->v_codes || !kv->k_scale || !kv->v_scale || (fp4 && (!kv->k_scales || !kv->v_scales)))
         return NVFP4_ERR_INVALID_ARG;
     if (kv->head_dim != 128 || kv->page_tokens != 64)
         return NVFP4_ERR_UNSUPPORTED_SHAPE;
-    if (kv->num_pages <= 0 || kv->num_kv_heads <= 0 || !aligned(kv->k_codes, 16) || !aligned(kv->k_scales, 16) ||
-        !aligned(kv->v_codes, 16) || !aligned(kv->v_scales, 16) || !aligned(kv->k_scale, 4) ||
+    if (kv->num_pages <= 0 || kv->num_kv_heads <= 0 || !aligned(kv->k_codes, 16) || !aligned(kv->v_codes, 16) ||
+        (fp4 && (!aligned(kv->k_scales, 16) || !aligned(kv->v_scales, 16))) || !aligned(kv->k_scale, 4) ||
         !aligned(kv->v_scale, 4))
         return NVFP4_ERR_INVALID_ARG;
     return NVFP4_OK;
@@ -753,6 +756,7 @@ nvfp4_status nvfp4_kv_append(const nvfp4_kv_cache *kv, const void *k_bf16, const
         !aligned(positions, 4) || !aligned(block_table, 4))
         return NVFP4_ERR_INVALID_ARG;
     KvAppendArgs a{};
+    a.fmt = kv->format;
     a.k_new = static_cast<const uint16_t *>(k_bf16);
     a.v_new = static_cast<const uint16_t *>(v_bf16);
     a.positions = positions;
@@ -796,6 +800,7 @@ nvfp4_status nvfp4_kv_decode_attention(const nvfp4_kv_cache *kv, const void *q_b
         !aligned(block_table, 4) || !aligned(out, 4))
         return NVFP4_ERR_INVALID_ARG;
     KvAttnArgs a{};
+    a.fmt = kv->format;
     a.q = static_cast<const uint16_t *>(q_bf16);
     a.ctx_lens = ctx_lens;
     a.block_table = block_table;

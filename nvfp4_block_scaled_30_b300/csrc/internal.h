@@ -165,9 +165,11 @@ struct W4A8GemmArgs {
 };
 cudaError_t launch_w4a8(const W4A8GemmArgs &g, cudaStream_t stream);
 
-// ---- NVFP4 paged KV cache (kv_attention.cu) -----------------------------------------
+// ---- NVFP4 / FP8 paged KV cache (kv_attention.cu) ------------------------------------
 // head_dim 128, 64 tokens per page; layouts in include/nvfp4.h (nvfp4_kv_cache)
+enum { KV_FMT_NVFP4 = 0, KV_FMT_FP8 = 1 };
 struct KvAppendArgs {
+    int fmt;
     const uint16_t *k_new, *v_new; // BF16 [B][H_kv][128]
     const int32_t *positions;      // [B] slot of the new token in its sequence
     const int32_t *block_table;    // [B][max_pages]
@@ -178,6 +180,7 @@ struct KvAppendArgs {
 cudaError_t launch_kv_append(const KvAppendArgs &a, cudaStream_t stream);
 
 struct KvAttnArgs {
+    int fmt;
     const uint16_t *q;             // BF16 [B][H][128]
     const int32_t *ctx_lens;       // [B]
     const int32_t *block_table;    // [B][max_pages]

@@ -42,6 +42,8 @@ constexpr int KV_P = 64;            // tokens per page
 constexpr int KC_BYTES = KV_P * KV_D / 2;   // 4096
 constexpr int KS_BYTES = KV_P * KV_D / 16;  // 512
 constexpr int PAGE_BYTES = 2 * (KC_BYTES + KS_BYTES);
+constexpr int KC8_BYTES = KV_P * KV_D;              // FP8 codes of one page and head, 8192
+constexpr int HALF8_BYTES = KC8_BYTES / 2;          // one 32-token half (keys or values)
 constexpr int ATT_WARPS = 4;
 constexpr int ATT_STAGES = 2;
 
@@ -70,6 +72,15 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
 {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// 2^x (the approximate hardware exponential: relative error ~2^-22, far
+// inside the attention tolerance)
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ void ldsm_x4(const void *row_addr, uint32_t (&r)[4])
@@ -116,6 +127,30 @@ __global__ void kv_append_kernel(KvAppendArgs a)
         amb = fmaxf(amb, fabsf(x[i]));
     }
     const float s = *(which ? a.v_scale : a.k_scale);
+    if (a.fmt == KV_FMT_FP8) {
+        // E4M3(x * 1/s) per element; keys token-major [64][128], values in
+        // two 32-token halves, dim-major [2][128][32]
+        const float r8 = recip_step(s);
+        const int64_t ph8 = (int64_t)page * a.H_kv + hk;
+        uint32_t c[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            c[i] = e4m3(__fmul_rn(x[i], r8)) | (x[i] < 0.0f || (x[i] == 0.0f && signbit(x[i])) ? 0x80u : 0u);
+        if (!which) {
+            uint32_t wds[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                wds[q] = c[4 * q] | (c[4 * q + 1] << 8) | (c[4 * q + 2] << 16) | (c[4 * q + 3] << 24);
+            *reinterpret_cast<uint4 *>(a.k_codes + ph8 * KC8_BYTES + slot * KV_D + blk * 16) =
+                make_uint4(wds[0], wds[1], wds[2], wds[3]);
+        } else {
+            uint8_t *vc = a.v_codes + ph8 * KC8_BYTES + (slot / 32) * (KV_D * 32) + (slot % 32);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                vc[(blk * 16 + i) * 32] = (uint8_t)c[i];
+        }
+        return;
+    }
     const uint32_t e = block_scale_code(amb, s);
     const float r = recip_step(__fmul_rn(e4m3_value(e), s));
     const int64_t ph = (int64_t)page * a.H_kv + hk;
@@ -159,6 +194,129 @@ struct AttSmem {
     uint64_t full[ATT_WARPS][ATT_STAGES];
 };
 static_assert(sizeof(AttMerge) <= ATT_WARPS * ATT_STAGES * PAGE_BYTES, "merge buffer fits in the ring");
+
+// Merge of the 4 warps' running softmax states (row sums over the 4 lanes
+// of a group, then through shared memory: the page ring, idle in every warp
+// by now) and the store of the output, or of this split's partial.
+__device__ __forceinline__ void kv_merge_and_store(const KvAttnArgs &a, AttMerge &mg, const float (&o)[16][4],
+                                                   const float (&m_run)[2], float (&l_run)[2], int warp, int g,
+                                                   int t, int G, int b, int hk, int split, float s_v)
+{
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        l_run[rr] += __shfl_xor_sync(0xFFFFFFFFu, l_run[rr], 1);
+        l_run[rr] += __shfl_xor_sync(0xFFFFFFFFu, l_run[rr], 2);
+    }
+    __syncthreads();
+    if (t == 0) {
+        mg.m[warp][g] = m_run[0];
+        mg.m[warp][g + 8] = m_run[1];
+        mg.l[warp][g] = l_run[0];
+        mg.l[warp][g + 8] = l_run[1];
+    }
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+        mg.o[warp][g][8 * n + 2 * t] = o[n][0];
+        mg.o[warp][g][8 * n + 2 * t + 1] = o[n][1];
+        mg.o[warp][g + 8][8 * n + 2 * t] = o[n][2];
+        mg.o[warp][g + 8][8 * n + 2 * t + 1] = o[n][3];
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < G * KV_D; idx += 32 * ATT_WARPS) {
+        const int head = idx / KV_D, d = idx % KV_D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < ATT_WARPS; ++w)
+            M = fmaxf(M, mg.m[w][head]);
+        float L = 0.0f, O = 0.0f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < ATT_WARPS; ++w) {
+                const float f = mg.m[w][head] == -INFINITY ? 0.0f : ex2(mg.m[w][head] - M);
+                L += f * mg.l[w][head];
+                O += f * mg.o[w][head][d];
+            }
+        }
+        const int64_t hq = (int64_t)b * a.H + hk * G + head;
+        if (a.n_splits == 1) {
+            const float y = L > 0.0f ? O * s_v / L : 0.0f;
+            if (a.out_dtype == NVFP4_OUT_BF16)
+                static_cast<__nv_bfloat16 *>(a.out)[hq * KV_D + d] = __float2bfloat16_rn(y);
+            else
+                static_cast<float *>(a.out)[hq * KV_D + d] = y;
+        } else {
+            float *part = a.partial + (hq * a.n_splits + split) * (KV_D + 2);
+            part[d] = O;
+            if (d == 0) {
+                part[KV_D] = M;
+                part[KV_D + 1] = L;
+            }
+        }
+    }
+}
+
+// Online softmax update of one 32-key chunk's scores (base 2, already
+// scaled): masks keys past `valid` (a partial chunk only), rescales the
+// running state and the output accumulators (only when a row maximum grew),
+// returns the P fragments of the chunk's two 16-key steps.  Key of sc[j][i]
+// is key_of(j, 2t + (i & 1)); rows g (i < 2), g + 8 (i >= 2, skipped when the
+// group has at most 8 query heads: those rows are padding and get P = 0).
+template <typename KeyOf>
+__device__ __forceinline__ void kv_softmax_chunk(float (&sc)[4][4], int valid, int t, KeyOf key_of, bool hi_rows,
+                                                 float (&m_run)[2], float (&l_run)[2], float (&o)[16][4],
+                                                 uint32_t (&pf)[2][4])
+{
+    if (valid < 32) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                sc[j][i] = key_of(j, 2 * t + (i & 1)) < valid ? sc[j][i] : -INFINITY;
+    }
+    float cmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            cmax[i >> 1] = fmaxf(cmax[i >> 1], sc[j][i]);
+    const int nrows = hi_rows ? 2 : 1;
+    bool grew = false;
+    float corr[2] = {1.0f, 1.0f};
+    for (int rr = 0; rr < nrows; ++rr) {
+        cmax[rr] = fmaxf(cmax[rr], __shfl_xor_sync(0xFFFFFFFFu, cmax[rr], 1));
+        cmax[rr] = fmaxf(cmax[rr], __shfl_xor_sync(0xFFFFFFFFu, cmax[rr], 2));
+        if (cmax[rr] > m_run[rr]) {
+            corr[rr] = m_run[rr] == -INFINITY ? 0.0f : ex2(m_run[rr] - cmax[rr]);
+            m_run[rr] = cmax[rr];
+            l_run[rr] *= corr[rr];
+            grew = true;
+        }
+    }
+    if (__any_sync(0xFFFFFFFFu, grew)) {
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+            o[n][0] *= corr[0];
+            o[n][1] *= corr[0];
+            o[n][2] *= corr[1];
+            o[n][3] *= corr[1];
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float pv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (i >= 2 && !hi_rows)
+                continue;
+            const float mm = m_run[i >> 1];
+            pv[i] = mm == -INFINITY ? 0.0f : ex2(sc[j][i] - mm);
+            l_run[i >> 1] += pv[i];
+        }
+        // n-tile j -> step j / 2; even j: k slots 2t, 2t+1; odd j: 2t+8, 2t+9
+        pf[j >> 1][(j & 1) * 2 + 0] = pack_h2(pv[0], pv[1]);
+        pf[j >> 1][(j & 1) * 2 + 1] = pack_h2(pv[2], pv[3]);
+    }
+}
 
 // Key order inside a 32-key chunk: QK n-tile j (8 keys) column n holds key
 // 8 (n / 2) + (n % 2) + 2 j, so that the S fragment of n-tiles 0, 1 (2, 3)
@@ -227,21 +385,33 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_kernel(const KvAttnA
     float l_run[2] = {0.0f, 0.0f};           // this lane's share of the row sums
 
     // pages of this warp: p = warp, warp + 4, ... of the CTA's range
+    // page ids of this warp's first 32 pages, one per lane, read once
+    int my_pg = 0;
+    if (warp + ATT_WARPS * lane < n_pages)
+        my_pg = a.block_table[(int64_t)b * a.max_pages + k_begin / KV_P + warp + ATT_WARPS * lane];
+    // warp-collective: the page's four copies go out from lanes 0..3 (one
+    // thread's copies are served one after another)
     auto issue = [&](int p, int s) {
-        const int tok = k_begin + p * KV_P;
-        const int page = a.block_table[(int64_t)b * a.max_pages + tok / KV_P];
+        const int i = (p - warp) / ATT_WARPS;
+        int page = __shfl_sync(0xFFFFFFFFu, my_pg, i & 31);
+        if (i >= 32)
+            page = a.block_table[(int64_t)b * a.max_pages + (k_begin + p * KV_P) / KV_P];
         const int64_t ph = (int64_t)min(max(page, 0), a.num_pages - 1) * a.H_kv + hk;
         uint8_t *dst = sm.page[warp][s];
-        mbar_arrive_expect_tx(&sm.full[warp][s], PAGE_BYTES);
-        bulk_load(dst, a.k_codes + ph * KC_BYTES, KC_BYTES, &sm.full[warp][s]);
-        bulk_load(dst + KC_BYTES, a.k_scales + ph * KS_BYTES, KS_BYTES, &sm.full[warp][s]);
-        bulk_load(dst + KC_BYTES + KS_BYTES, a.v_codes + ph * KC_BYTES, KC_BYTES, &sm.full[warp][s]);
-        bulk_load(dst + 2 * KC_BYTES + KS_BYTES, a.v_scales + ph * KS_BYTES, KS_BYTES, &sm.full[warp][s]);
+        if (lane == 0)
+            mbar_arrive_expect_tx(&sm.full[warp][s], PAGE_BYTES);
+        __syncwarp();
+        if (lane == 0)
+            bulk_load(dst, a.k_codes + ph * KC_BYTES, KC_BYTES, &sm.full[warp][s]);
+        else if (lane == 1)
+            bulk_load(dst + KC_BYTES, a.k_scales + ph * KS_BYTES, KS_BYTES, &sm.full[warp][s]);
+        else if (lane == 2)
+            bulk_load(dst + KC_BYTES + KS_BYTES, a.v_codes + ph * KC_BYTES, KC_BYTES, &sm.full[warp][s]);
+        else if (lane == 3)
+            bulk_load(dst + 2 * KC_BYTES + KS_BYTES, a.v_scales + ph * KS_BYTES, KS_BYTES, &sm.full[warp][s]);
     };
-    if (lane == 0) {
-        for (int i = 0; i < ATT_STAGES && warp + i * ATT_WARPS < n_pages; ++i)
-            issue(warp + i * ATT_WARPS, i);
-    }
+    for (int i = 0; i < ATT_STAGES && warp + i * ATT_WARPS < n_pages; ++i)
+        issue(warp + i * ATT_WARPS, i);
     bool ok = true;
     int it = 0;
     for (int p = warp; p < n_pages; p += ATT_WARPS, ++it) {
@@ -290,50 +460,14 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_kernel(const KvAttnA
                     }
                 }
             }
-            // ---- online softmax (base 2; scores already carry sm_scale * log2 e / s_k)
-            // key of sc[j][i]: chunk_key(j, 2t + (i & 1)); rows g (i < 2), g + 8
-            float cmax[2] = {-INFINITY, -INFINITY};
+            // ---- online softmax (base 2: the queries carry sm_scale * log2 e)
 #pragma unroll
             for (int j = 0; j < 4; ++j)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int key = chunk_key(j, 2 * t + (i & 1));
-                    float v = sc[j][i] * s_k;
-                    v = key < valid ? v : -INFINITY;
-                    sc[j][i] = v;
-                    cmax[i >> 1] = fmaxf(cmax[i >> 1], v);
-                }
-            float corr[2];
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                cmax[rr] = fmaxf(cmax[rr], __shfl_xor_sync(0xFFFFFFFFu, cmax[rr], 1));
-                cmax[rr] = fmaxf(cmax[rr], __shfl_xor_sync(0xFFFFFFFFu, cmax[rr], 2));
-                const float mn = fmaxf(m_run[rr], cmax[rr]);
-                corr[rr] = mn == -INFINITY ? 1.0f : exp2f(m_run[rr] - mn);
-                m_run[rr] = mn;
-                l_run[rr] *= corr[rr];
-            }
-#pragma unroll
-            for (int n = 0; n < 16; ++n) {
-                o[n][0] *= corr[0];
-                o[n][1] *= corr[0];
-                o[n][2] *= corr[1];
-                o[n][3] *= corr[1];
-            }
+                for (int i = 0; i < 4; ++i)
+                    sc[j][i] *= s_k;
             uint32_t pf[2][4]; // P fragments of the two 16-key steps
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float pv[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float mm = m_run[i >> 1];
-                    pv[i] = mm == -INFINITY ? 0.0f : exp2f(sc[j][i] - mm);
-                    l_run[i >> 1] += pv[i];
-                }
-                // n-tile j -> step j / 2; even j: k slots 2t, 2t+1; odd j: 2t+8, 2t+9
-                pf[j >> 1][(j & 1) * 2 + 0] = pack_h2(pv[0], pv[1]);
-                pf[j >> 1][(j & 1) * 2 + 1] = pack_h2(pv[2], pv[3]);
-            }
+            kv_softmax_chunk(sc, valid, t, chunk_key, G > 8, m_run, l_run, o, pf);
             // ---- O += P V: 2 k-steps x 16 n-tiles (dims), V rows via ldmatrix
             // keys 8t .. 8t+7 of this chunk are valid up to `valid`
             const bool full_chunk = valid >= 32;
@@ -374,7 +508,7 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_kernel(const KvAttnA
         }
         // the stage is free again: this warp's next page goes into it
         __syncwarp();
-        if (lane == 0 && p + ATT_STAGES * ATT_WARPS < n_pages) {
+        if (p + ATT_STAGES * ATT_WARPS < n_pages) {
             fence_proxy_async_smem();
             issue(p + ATT_STAGES * ATT_WARPS, s);
         }
@@ -386,60 +520,161 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_kernel(const KvAttnA
             mbar_wait(&sm.full[warp][i % ATT_STAGES], (uint32_t)(i / ATT_STAGES) & 1u, a.timeout_ns, nullptr);
     }
 
-    // ---- merge the warps: row sums over the 4 lanes of a group, then through
-    // shared memory (the page ring, now idle in every warp)
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-        l_run[rr] += __shfl_xor_sync(0xFFFFFFFFu, l_run[rr], 1);
-        l_run[rr] += __shfl_xor_sync(0xFFFFFFFFu, l_run[rr], 2);
+    kv_merge_and_store(a, sm.merge, o, m_run, l_run, warp, g, t, G, b, hk, split, s_v);
+}
+
+// FP8 cache (E4M3 codes, one static scale per tensor): the same structure
+// with 32-token half pages as the unit (keys [32][128], values [128][32],
+// 4 KB each, contiguous in the FP8 layout).  A 16-byte ldmatrix row holds 16
+// FP8 elements, so lane t receives elements 4t .. 4t+3 of its row: for keys,
+// dims 16 kk + 4t + {0,1} / {2,3} fill k slots 2t, 2t+1 / 2t+8, 2t+9 of k-step
+// kk; for values, keys 16 s + 4t + ... of step s.  QK n-tile j column n holds
+// key chunk_key8(j, n), matching those P slots.  One conversion per two
+// elements, no per-element scale.
+__device__ __forceinline__ int chunk_key8(int j, int n) { return 16 * (j >> 1) + 4 * (n >> 1) + (n & 1) + 2 * (j & 1); }
+
+__global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_fp8_kernel(const KvAttnArgs a)
+{
+    extern __shared__ __align__(128) uint8_t att_raw[];
+    AttSmem &sm = *reinterpret_cast<AttSmem *>(att_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+    const int G = a.H / a.H_kv;
+    const int ctx = max(0, min(min(a.ctx_lens[b], a.max_ctx), a.max_pages * KV_P));
+    const int k_begin = split * a.keys_per_split;
+    const int k_end = min(ctx, k_begin + a.keys_per_split);
+    const int n_chunks = k_end > k_begin ? (k_end - k_begin + 31) / 32 : 0;
+
+    if (lane == 0) {
+        for (int s = 0; s < ATT_STAGES; ++s)
+            mbar_init(&sm.full[warp][s], 1);
+        fence_mbar_init();
     }
-    __syncthreads();
-    AttMerge &mg = sm.merge;
-    if (t == 0) {
-        mg.m[warp][g] = m_run[0];
-        mg.m[warp][g + 8] = m_run[1];
-        mg.l[warp][g] = l_run[0];
-        mg.l[warp][g + 8] = l_run[1];
+    __syncwarp();
+
+    uint32_t qf[8][4];
+    {
+        const float qs = a.sm_scale * 1.4426950408889634f;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int head = g + 8 * rr;
+                float v[4] = {0.f, 0.f, 0.f, 0.f};
+                if (head < G) {
+                    const uint16_t *q = a.q + ((int64_t)b * a.H + hk * G + head) * KV_D + 16 * kk + 4 * t;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        v[i] = __uint_as_float((uint32_t)q[i] << 16) * qs;
+                }
+                qf[kk][rr] = pack_h2(v[0], v[1]);
+                qf[kk][2 + rr] = pack_h2(v[2], v[3]);
+            }
     }
+    const float s_k = *a.k_scale, s_v = *a.v_scale;
+    float o[16][4];
 #pragma unroll
-    for (int n = 0; n < 16; ++n) {
-        mg.o[warp][g][8 * n + 2 * t] = o[n][0];
-        mg.o[warp][g][8 * n + 2 * t + 1] = o[n][1];
-        mg.o[warp][g + 8][8 * n + 2 * t] = o[n][2];
-        mg.o[warp][g + 8][8 * n + 2 * t + 1] = o[n][3];
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < G * KV_D; idx += 32 * ATT_WARPS) {
-        const int head = idx / KV_D, d = idx % KV_D;
-        float M = -INFINITY;
+    for (int n = 0; n < 16; ++n)
 #pragma unroll
-        for (int w = 0; w < ATT_WARPS; ++w)
-            M = fmaxf(M, mg.m[w][head]);
-        float L = 0.0f, O = 0.0f;
-        if (M != -INFINITY) {
+        for (int i = 0; i < 4; ++i)
+            o[n][i] = 0.0f;
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_run[2] = {0.0f, 0.0f};
+
+    // chunk c of this CTA's range: keys k_begin + 32 c .. + 31 = half
+    // ((k_begin / 32 + c) % 2) of page (k_begin / 64 + c / 2)
+    // page ids of this warp's first 32 chunks, one per lane, read once
+    int my_pg = 0;
+    if (warp + ATT_WARPS * lane < n_chunks)
+        my_pg = a.block_table[(int64_t)b * a.max_pages + (k_begin + 32 * (warp + ATT_WARPS * lane)) / KV_P];
+    // warp-collective: the two copies go out from lanes 0 and 1
+    auto issue = [&](int c, int s) {
+        const int i = (c - warp) / ATT_WARPS;
+        const int tok = k_begin + 32 * c;
+        int page = __shfl_sync(0xFFFFFFFFu, my_pg, i & 31);
+        if (i >= 32)
+            page = a.block_table[(int64_t)b * a.max_pages + tok / KV_P];
+        const int64_t ph = (int64_t)min(max(page, 0), a.num_pages - 1) * a.H_kv + hk;
+        const int half = (tok / 32) & 1;
+        uint8_t *dst = sm.page[warp][s];
+        if (lane == 0)
+            mbar_arrive_expect_tx(&sm.full[warp][s], 2 * HALF8_BYTES);
+        __syncwarp();
+        if (lane == 0)
+            bulk_load(dst, a.k_codes + ph * KC8_BYTES + half * HALF8_BYTES, HALF8_BYTES, &sm.full[warp][s]);
+        else if (lane == 1)
+            bulk_load(dst + HALF8_BYTES, a.v_codes + ph * KC8_BYTES + half * HALF8_BYTES, HALF8_BYTES,
+                      &sm.full[warp][s]);
+    };
+    for (int i = 0; i < ATT_STAGES && warp + i * ATT_WARPS < n_chunks; ++i)
+        issue(warp + i * ATT_WARPS, i);
+    bool ok = true;
+    int it = 0;
+    for (int c = warp; c < n_chunks; c += ATT_WARPS, ++it) {
+        const int s = it % ATT_STAGES;
+        const uint32_t par = (uint32_t)(it / ATT_STAGES) & 1u;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sm.full[warp][s], par, a.timeout_ns, nullptr))) {
+            if (lane == 0)
+                atomicOr(a.status, ST_TIMEOUT);
+            ok = false;
+            break;
+        }
+        const uint8_t *kc = sm.page[warp][s];      // [32 keys][128]
+        const uint8_t *vc = kc + HALF8_BYTES;      // [128 dims][32 keys]
+        const int valid = min(32, k_end - (k_begin + 32 * c));
+        // ---- S = Q K^T over 32 keys
+        float sc[4][4];
 #pragma unroll
-            for (int w = 0; w < ATT_WARPS; ++w) {
-                const float f = mg.m[w][head] == -INFINITY ? 0.0f : exp2f(mg.m[w][head] - M);
-                L += f * mg.l[w][head];
-                O += f * mg.o[w][head][d];
+        for (int j = 0; j < 4; ++j) {
+            const int krow = chunk_key8(j, lane & 7);
+            uint32_t kr[8];
+            ldsm_x4(kc + krow * KV_D + 16 * (lane >> 3), *reinterpret_cast<uint32_t(*)[4]>(&kr[0]));
+            ldsm_x4(kc + krow * KV_D + 64 + 16 * (lane >> 3), *reinterpret_cast<uint32_t(*)[4]>(&kr[4]));
+            sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.0f;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma16816(sc[j], qf[kk], h2_e4m3x2(kr[kk] & 0xFFFFu), h2_e4m3x2(kr[kk] >> 16));
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                sc[j][i] *= s_k;
+        uint32_t pf[2][4];
+        kv_softmax_chunk(sc, valid, t, chunk_key8, G > 8, m_run, l_run, o, pf);
+        // ---- O += P V
+        const bool full_chunk = valid >= 32;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+            for (int st = 0; st < 2; ++st) {
+                uint32_t vr[4];
+                ldsm_x4(vc + (32 * q4 + lane) * 32 + 16 * st, vr);
+                const int nv = min(4, max(0, valid - 16 * st - 4 * t)); // valid keys of this lane's 4
+#pragma unroll
+                for (int n4 = 0; n4 < 4; ++n4) {
+                    uint32_t b0 = h2_e4m3x2(vr[n4] & 0xFFFFu), b1 = h2_e4m3x2(vr[n4] >> 16);
+                    if (!full_chunk) {
+                        b0 = nv >= 2 ? b0 : (nv == 1 ? (b0 & 0x0000FFFFu) : 0u);
+                        b1 = nv >= 4 ? b1 : (nv == 3 ? (b1 & 0x0000FFFFu) : 0u);
+                    }
+                    mma16816(o[4 * q4 + n4], pf[st], b0, b1);
+                }
             }
         }
-        const int64_t hq = (int64_t)b * a.H + hk * G + head;
-        if (a.n_splits == 1) {
-            const float y = L > 0.0f ? O * s_v / L : 0.0f;
-            if (a.out_dtype == NVFP4_OUT_BF16)
-                static_cast<__nv_bfloat16 *>(a.out)[hq * KV_D + d] = __float2bfloat16_rn(y);
-            else
-                static_cast<float *>(a.out)[hq * KV_D + d] = y;
-        } else {
-            float *part = a.partial + (hq * a.n_splits + split) * (KV_D + 2);
-            part[d] = O;
-            if (d == 0) {
-                part[KV_D] = M;
-                part[KV_D + 1] = L;
-            }
+        __syncwarp();
+        if (c + ATT_STAGES * ATT_WARPS < n_chunks) {
+            fence_proxy_async_smem();
+            issue(c + ATT_STAGES * ATT_WARPS, s);
         }
     }
+    if (lane == 0 && !ok) {
+        const int mine = n_chunks > warp ? (n_chunks - warp + ATT_WARPS - 1) / ATT_WARPS : 0;
+        for (int i = it; i < mine && i < it + ATT_STAGES; ++i)
+            mbar_wait(&sm.full[warp][i % ATT_STAGES], (uint32_t)(i / ATT_STAGES) & 1u, a.timeout_ns, nullptr);
+    }
+    kv_merge_and_store(a, sm.merge, o, m_run, l_run, warp, g, t, G, b, hk, split, s_v);
 }
 
 // Merge of the splits: o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
@@ -501,8 +736,15 @@ cudaError_t launch_kv_decode(const KvAttnArgs &a, cudaStream_t stream)
     cudaError_t e = cudaFuncSetAttribute(kv_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
+    if (a.fmt == KV_FMT_FP8 &&
+        (e = cudaFuncSetAttribute(kv_decode_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+            cudaSuccess)
+        return e;
     dim3 grid((unsigned)a.n_splits, (unsigned)a.H_kv, (unsigned)a.B);
-    kv_decode_kernel<<<grid, 32 * ATT_WARPS, smem, stream>>>(a);
+    if (a.fmt == KV_FMT_FP8)
+        kv_decode_fp8_kernel<<<grid, 32 * ATT_WARPS, smem, stream>>>(a);
+    else
+        kv_decode_kernel<<<grid, 32 * ATT_WARPS, smem, stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess || a.n_splits == 1)
         return e;
     kv_combine_kernel<<<(unsigned)(a.B * a.H), KV_D, 0, stream>>>(a);

@@ -171,3 +171,94 @@ def test_append_then_attend():
     ref = oracle.decode_attention(oracle.bf16_to_f32(qb).astype(np.float64), k_nat, v_nat, s_k, s_v, table,
                                   np.array(ctx), 0.0884)
     check_attention(out, ref, v_nat, s_v, table, ctx, H_kv, G, False)
+
+
+# ---- FP8 cache ---------------------------------------------------------------------------
+
+def fp8_v_layout(v_nat):
+    """[..., 64 tokens, 128] -> the FP8 cache's value layout [..., 2, 128, 32]."""
+    v = np.asarray(v_nat, np.uint8)
+    sh = v.shape[:-2]
+    return np.ascontiguousarray(np.swapaxes(v.reshape(sh + (2, 32, D)), -1, -2))
+
+
+def build_cache_fp8(rng, ctx_lens, H_kv, s_k, s_v):
+    B = len(ctx_lens)
+    pages_per = [max(1, -(-n // P)) for n in ctx_lens]
+    n_pages = sum(pages_per) + 2
+    order = rng.permutation(n_pages)
+    table = np.zeros((B, max(pages_per)), np.int32)
+    k = rng.integers(0, 256, (n_pages, H_kv, P, D)).astype(np.uint8)     # stale bytes (NaN codes too)
+    v = rng.integers(0, 256, (n_pages, H_kv, P, D)).astype(np.uint8)
+    nxt = 0
+    for b, n in enumerate(ctx_lens):
+        for i in range(pages_per[b]):
+            table[b, i] = order[nxt]
+            nxt += 1
+        for hk in range(H_kv):
+            kc = oracle.kv_encode_fp8(synth.activations(9, 600 + 7 * b + hk, n, D, 0.02, 8.0), s_k)
+            vc = oracle.kv_encode_fp8(synth.activations(9, 700 + 7 * b + hk, n, D, 0.0, 1.0), s_v)
+            for tkn in range(n):
+                k[table[b, tkn // P], hk, tkn % P] = kc[tkn]
+                v[table[b, tkn // P], hk, tkn % P] = vc[tkn]
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    cache = nv.KvCache(dev(k), None, dev(fp8_v_layout(v)), None,
+                       torch.tensor([s_k], dtype=torch.float32, device="cuda"),
+                       torch.tensor([s_v], dtype=torch.float32, device="cuda"), n_pages, H_kv, nv.KV_FP8)
+    return cache, k, v, table
+
+
+@pytest.mark.parametrize("ctx_lens,H_kv,G,out_dtype", [
+    ([1, 31, 32, 33, 64, 65, 200, 0], 2, 8, nv.OUT_FP32),  # half-page and page boundaries, empty
+    ([3000, 17, 1100], 1, 8, nv.OUT_BF16),                 # several context splits
+    ([700, 96, 5], 2, 16, nv.OUT_FP32),
+])
+def test_fp8_decode_attention_against_oracle(ctx_lens, H_kv, G, out_dtype):
+    rng = np.random.default_rng(sum(ctx_lens) + 7 * G)
+    s_k, s_v = 8.0 / 448, 4.0 / 448
+    cache, k, v, table = build_cache_fp8(rng, ctx_lens, H_kv, s_k, s_v)
+    H, B = H_kv * G, len(ctx_lens)
+    qb = synth.activations(9, 800 + G, B * H, D, 0.0, 1.0).reshape(B, H, D)
+    q = torch.from_numpy(qb.view(np.int16)).cuda().view(torch.bfloat16)
+    sm = 1.0 / math.sqrt(D)
+    out = nv.kv_decode_attention(cache, q, torch.tensor(ctx_lens, dtype=torch.int32, device="cuda"),
+                                 torch.from_numpy(table).cuda(), max(ctx_lens), sm, out_dtype=out_dtype)
+    on = host(out.float()).astype(np.float64)
+    ref = oracle.decode_attention(oracle.bf16_to_f32(qb).astype(np.float64), k, v, s_k, s_v, table,
+                                  np.array(ctx_lens), sm, fmt="fp8")
+    for b in range(B):
+        n = ctx_lens[b]
+        for h in range(H):
+            if n == 0:
+                assert not on[b, h].any()
+                continue
+            V = oracle.kv_gather_fp8(v, s_v, table[b], n, h // G)
+            err = np.abs(on[b, h] - ref[b, h])
+            if out_dtype == nv.OUT_BF16:
+                err = np.maximum(err - bf16_half_ulp(ref[b, h]), 0.0)
+            assert err.max() <= 1e-3 * np.abs(V).max(), f"seq {b} head {h}"
+
+
+def test_fp8_append_bit_exact():
+    rng = np.random.default_rng(17)
+    H_kv, B, n_pages, max_pages = 2, 4, 10, 2
+    s_k, s_v = 6.0 / 448, 3.0 / 448
+    k0 = rng.integers(0, 256, (n_pages, H_kv, P, D)).astype(np.uint8)
+    v0 = rng.integers(0, 256, (n_pages, H_kv, 2, D, 32)).astype(np.uint8)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    cache = nv.KvCache(dev(k0), None, dev(v0), None, torch.tensor([s_k], device="cuda"),
+                       torch.tensor([s_v], device="cuda"), n_pages, H_kv, nv.KV_FP8)
+    table = rng.permutation(n_pages)[:B * max_pages].reshape(B, max_pages).astype(np.int32)
+    positions = np.array([0, 31, 32, 127], np.int32)
+    kb = synth.activations(9, 900, B * H_kv, D, 0.02, 8.0).reshape(B, H_kv, D)
+    vb = synth.activations(9, 901, B * H_kv, D, 0.0, 1.0).reshape(B, H_kv, D)
+    to_dev = lambda x: torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    nv.kv_append(cache, to_dev(kb), to_dev(vb), torch.from_numpy(positions).cuda(), torch.from_numpy(table).cuda())
+    ek, ev = k0.copy(), v0.copy()
+    for b in range(B):
+        pg, sl = table[b, positions[b] // P], positions[b] % P
+        for hk in range(H_kv):
+            ek[pg, hk, sl] = oracle.kv_encode_fp8(kb[b, hk:hk + 1], s_k)[0]
+            ev[pg, hk, sl // 32, :, sl % 32] = oracle.kv_encode_fp8(vb[b, hk:hk + 1], s_v)[0]
+    np.testing.assert_array_equal(host(cache.k_codes), ek)
+    np.testing.assert_array_equal(host(cache.v_codes), ev)

@@ -442,15 +442,14 @@ def workload_kv_decode(c, steps, warmup, B=16, H=64, H_kv=8, ctx=4096, fmt=0):
     ks = t.tensor([8.0 / 2688], device=c.dev)
     vs = t.tensor([4.0 / 2688], device=c.dev)
     cache = nv.KvCache.empty(n_pages, H_kv, ks, vs, device=c.dev, fmt=fmt)
-    for buf in (cache.k_codes, cache.v_codes):
-        if fmt == nv.KV_FP8:   # finite E4M3 codes with random signs
-            buf.copy_(t.randint(0, 0x70, buf.shape, dtype=t.uint8, device=c.dev, generator=g)
-                      | (t.randint(0, 2, buf.shape, dtype=t.uint8, device=c.dev, generator=g) << 7))
-        else:
-            buf.copy_(t.randint(0, 256, buf.shape, dtype=t.uint8, device=c.dev, generator=g))
-    if fmt != nv.KV_FP8:
-        for buf in (cache.k_scales, cache.v_scales):
-            buf.copy_(t.randint(0x28, 0x48, buf.shape, dtype=t.uint8, device=c.dev, generator=g))
+    pg = cache.pages
+    if fmt == nv.KV_FP8:   # finite E4M3 codes with random signs
+        pg.copy_(t.randint(0, 0x70, pg.shape, dtype=t.uint8, device=c.dev, generator=g)
+                 | (t.randint(0, 2, pg.shape, dtype=t.uint8, device=c.dev, generator=g) << 7))
+    else:                  # random codes, scale bytes in a normal range
+        pg.copy_(t.randint(0, 256, pg.shape, dtype=t.uint8, device=c.dev, generator=g))
+        for lo, hi in ((4096, 4608), (8704, 9216)):
+            pg[..., lo:hi] = t.randint(0x28, 0x48, pg[..., lo:hi].shape, dtype=t.uint8, device=c.dev, generator=g)
     perm = t.randperm(n_pages, device=c.dev, generator=g).to(t.int32)
     table = perm.view(B, pages_per).contiguous()
     ctx_lens = t.full((B,), ctx, dtype=t.int32, device=c.dev)

@@ -334,32 +334,30 @@ nvfp4_status nvfp4_moe_down_combine(const nvfp4_tensor *h, const int64_t *expert
  * format: every element E4M3(x * 1/s) in binary32 (the per-token FP8 rule
  * under the static scale s), no block scales.
  *
- * Cache layout, per page (64 token slots) and KV head; all device memory
- * owned by the caller, pages of one sequence listed in its block-table row.
- * NVFP4_KV_NVFP4:
- *   k_codes  uint8 [num_pages][num_kv_heads][64][64]   token-major, element
- *            2j of a token in the low nibble of byte j
- *   k_scales E4M3  [num_pages][num_kv_heads][64][8]
- *   v_codes  uint8 [num_pages][num_kv_heads][128][32]  dim-major: byte j of
- *            row d holds tokens 2j (low nibble) and 2j+1 of dimension d
- *   v_scales E4M3  [num_pages][num_kv_heads][8][64]     block b of token t
- * NVFP4_KV_FP8 (k_scales, v_scales unused, may be NULL):
- *   k_codes  E4M3  [num_pages][num_kv_heads][64][128]  token-major
- *   v_codes  E4M3  [num_pages][num_kv_heads][2][128][32] two 32-token
- *            halves, dim-major: byte j of row d of half h = token 32h + j
- * Both: k_scale, v_scale are device float[1] tensor scales.
- * A page belongs to one sequence; slots past a sequence's length may hold
- * anything (the attention ignores them). */
+ * Cache layout: `pages` is uint8 [num_pages][num_kv_heads][page block], one
+ * contiguous block per page (64 token slots) and KV head, owned by the
+ * caller; a sequence's pages are listed in its block-table row.
+ * NVFP4_KV_NVFP4, 9216-byte blocks:
+ *   [0, 4096)     key codes   [64 tokens][64]  token-major, element 2j of a
+ *                 token in the low nibble of byte j
+ *   [4096, 4608)  key scales  [64 tokens][8]   E4M3
+ *   [4608, 8704)  value codes [128 dims][32]   dim-major: byte j of row d
+ *                 holds tokens 2j (low nibble) and 2j+1 of dimension d
+ *   [8704, 9216)  value scales [8 blocks][64 tokens]
+ * NVFP4_KV_FP8, 16384-byte blocks, two 32-token halves of 8192 bytes:
+ *   [h*8192, h*8192 + 4096)     keys  [32 tokens][128] E4M3, token-major
+ *   [h*8192 + 4096, (h+1)*8192) values [128 dims][32 tokens] E4M3, dim-major
+ *   (token 32h + j of the page).
+ * Both: k_scale, v_scale are device float[1] tensor scales.  A page belongs
+ * to one sequence; slots past a sequence's length may hold anything (the
+ * attention ignores them). */
 typedef enum nvfp4_kv_format {
     NVFP4_KV_NVFP4 = 0,
     NVFP4_KV_FP8 = 1
 } nvfp4_kv_format;
 
 typedef struct nvfp4_kv_cache {
-    void *k_codes;
-    void *k_scales;
-    void *v_codes;
-    void *v_scales;
+    void *pages;
     const float *k_scale;
     const float *v_scale;
     int32_t num_pages;

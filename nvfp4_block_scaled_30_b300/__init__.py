@@ -49,8 +49,7 @@ class TensorDesc(ctypes.Structure):
 
 
 class KvCacheDesc(ctypes.Structure):
-    _fields_ = [("k_codes", ctypes.c_void_p), ("k_scales", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
-                ("v_scales", ctypes.c_void_p), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+    _fields_ = [("pages", ctypes.c_void_p), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
                 ("num_pages", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("page_tokens", ctypes.c_int32), ("format", ctypes.c_int32)]
 
@@ -431,38 +430,38 @@ KV_HEAD_DIM = 128
 KV_NVFP4, KV_FP8 = 0, 1
 
 
+KV_PAGE_BYTES = {KV_NVFP4: 9216, KV_FP8: 16384}
+
+
 @dataclasses.dataclass
 class KvCache:
-    """Device paged KV cache (layouts in include/nvfp4.h).  NVFP4: per page
-    and KV head, K codes [64][64], K scales [64][8], V codes [128][32]
-    (dim-major), V scales [8][64].  FP8: K codes [64][128], V codes
-    [2][128][32] (32-token halves, dim-major), no block scales.  Static
+    """Device paged KV cache (layouts in include/nvfp4.h): `pages` uint8
+    [num_pages, num_kv_heads, page block], one contiguous block per page and
+    KV head (NVFP4: key codes, key scales, value codes dim-major, value
+    scales; FP8: two 32-token halves of keys then dim-major values); static
     tensor scales k_scale / v_scale (float32 [1])."""
-    k_codes: torch.Tensor
-    k_scales: Optional[torch.Tensor]
-    v_codes: torch.Tensor
-    v_scales: Optional[torch.Tensor]
+    pages: torch.Tensor
     k_scale: torch.Tensor
     v_scale: torch.Tensor
-    num_pages: int
-    num_kv_heads: int
     fmt: int = KV_NVFP4
+
+    @property
+    def num_pages(self) -> int:
+        return self.pages.shape[0]
+
+    @property
+    def num_kv_heads(self) -> int:
+        return self.pages.shape[1]
 
     @staticmethod
     def empty(num_pages: int, num_kv_heads: int, k_scale: torch.Tensor, v_scale: torch.Tensor,
               device="cuda", fmt: int = KV_NVFP4) -> "KvCache":
-        P, D = KV_PAGE, KV_HEAD_DIM
-        z = lambda *shape: torch.zeros(shape, dtype=torch.uint8, device=device)
-        if fmt == KV_FP8:
-            return KvCache(z(num_pages, num_kv_heads, P, D), None, z(num_pages, num_kv_heads, 2, D, P // 2), None,
-                           k_scale, v_scale, num_pages, num_kv_heads, KV_FP8)
-        return KvCache(z(num_pages, num_kv_heads, P, D // 2), z(num_pages, num_kv_heads, P, D // 16),
-                       z(num_pages, num_kv_heads, D, P // 2), z(num_pages, num_kv_heads, D // 16, P),
-                       k_scale, v_scale, num_pages, num_kv_heads)
+        pages = torch.zeros((num_pages, num_kv_heads, KV_PAGE_BYTES[fmt]), dtype=torch.uint8, device=device)
+        return KvCache(pages, k_scale, v_scale, fmt)
 
     def desc(self) -> KvCacheDesc:
-        return KvCacheDesc(self.k_codes.data_ptr(), _ptr(self.k_scales), self.v_codes.data_ptr(),
-                           _ptr(self.v_scales), self.k_scale.data_ptr(), self.v_scale.data_ptr(),
+        assert self.pages.is_contiguous() and self.pages.shape[2] == KV_PAGE_BYTES[self.fmt]
+        return KvCacheDesc(self.pages.data_ptr(), self.k_scale.data_ptr(), self.v_scale.data_ptr(),
                            self.num_pages, self.num_kv_heads, KV_HEAD_DIM, KV_PAGE, self.fmt)
 
 

@@ -729,13 +729,11 @@ static nvfp4_status check_kv(const nvfp4_kv_cache *kv)
 {
     if (!kv || (kv->format != NVFP4_KV_NVFP4 && kv->format != NVFP4_KV_FP8))
         return NVFP4_ERR_INVALID_ARG;
-    const bool fp4 = kv->format == NVFP4_KV_NVFP4;
-    if (!kv->k_codes || !kv->v_codes || !kv->k_scale || !kv->v_scale || (fp4 && (!kv->k_scales || !kv->v_scales)))
+    if (!kv->pages || !kv->k_scale || !kv->v_scale)
         return NVFP4_ERR_INVALID_ARG;
     if (kv->head_dim != 128 || kv->page_tokens != 64)
         return NVFP4_ERR_UNSUPPORTED_SHAPE;
-    if (kv->num_pages <= 0 || kv->num_kv_heads <= 0 || !aligned(kv->k_codes, 16) || !aligned(kv->v_codes, 16) ||
-        (fp4 && (!aligned(kv->k_scales, 16) || !aligned(kv->v_scales, 16))) || !aligned(kv->k_scale, 4) ||
+    if (kv->num_pages <= 0 || kv->num_kv_heads <= 0 || !aligned(kv->pages, 16) || !aligned(kv->k_scale, 4) ||
         !aligned(kv->v_scale, 4))
         return NVFP4_ERR_INVALID_ARG;
     return NVFP4_OK;
@@ -765,10 +763,7 @@ nvfp4_status nvfp4_kv_append(const nvfp4_kv_cache *kv, const void *k_bf16, const
     a.H_kv = kv->num_kv_heads;
     a.max_pages = max_pages;
     a.num_pages = kv->num_pages;
-    a.k_codes = static_cast<uint8_t *>(kv->k_codes);
-    a.k_scales = static_cast<uint8_t *>(kv->k_scales);
-    a.v_codes = static_cast<uint8_t *>(kv->v_codes);
-    a.v_scales = static_cast<uint8_t *>(kv->v_scales);
+    a.pages = static_cast<uint8_t *>(kv->pages);
     a.k_scale = kv->k_scale;
     a.v_scale = kv->v_scale;
     return from_cuda(launch_kv_append(a, (cudaStream_t)stream));
@@ -810,10 +805,7 @@ nvfp4_status nvfp4_kv_decode_attention(const nvfp4_kv_cache *kv, const void *q_b
     a.max_pages = max_pages;
     a.num_pages = kv->num_pages;
     a.max_ctx = max_ctx;
-    a.k_codes = static_cast<const uint8_t *>(kv->k_codes);
-    a.k_scales = static_cast<const uint8_t *>(kv->k_scales);
-    a.v_codes = static_cast<const uint8_t *>(kv->v_codes);
-    a.v_scales = static_cast<const uint8_t *>(kv->v_scales);
+    a.pages = static_cast<const uint8_t *>(kv->pages);
     a.k_scale = kv->k_scale;
     a.v_scale = kv->v_scale;
     a.sm_scale = sm_scale;

@@ -174,7 +174,7 @@ struct KvAppendArgs {
     const int32_t *positions;      // [B] slot of the new token in its sequence
     const int32_t *block_table;    // [B][max_pages]
     int B, H_kv, max_pages, num_pages;
-    uint8_t *k_codes, *k_scales, *v_codes, *v_scales;
+    uint8_t *pages;                // [num_pages][H_kv][page block]
     const float *k_scale, *v_scale;
 };
 cudaError_t launch_kv_append(const KvAppendArgs &a, cudaStream_t stream);
@@ -185,7 +185,7 @@ struct KvAttnArgs {
     const int32_t *ctx_lens;       // [B]
     const int32_t *block_table;    // [B][max_pages]
     int B, H, H_kv, max_pages, num_pages, max_ctx;
-    const uint8_t *k_codes, *k_scales, *v_codes, *v_scales;
+    const uint8_t *pages;          // [num_pages][H_kv][page block]
     const float *k_scale, *v_scale;
     float sm_scale;
     int keys_per_split, n_splits;  // keys_per_split % 64 == 0

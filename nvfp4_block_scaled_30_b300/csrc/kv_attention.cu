@@ -9,12 +9,17 @@
 // tensor; attention is scaled dot-product attention of one query token over
 // the cached tokens, the query heads of a group sharing one KV head.
 //
-// Page layout (head_dim D = 128, 64 tokens per page, per page and KV head):
-//   K codes  [64 tokens][64 bytes]   (token-major, element 2j in the low nibble)
-//   K scales [64 tokens][8]
-//   V codes  [128 dims][32 bytes]    (dim-major: byte j of row d holds tokens
-//                                     2j (low nibble) and 2j+1 of dim d)
-//   V scales [8 blocks][64 tokens]
+// Page block layout (head_dim D = 128, 64 tokens per page), one contiguous
+// 9216-byte block per page and KV head, read with ONE bulk copy (measured
+// on B300: an SM serves its bulk copies at a roughly fixed cost per copy
+// for copies this small, so the copy count, not the bytes, bounded the
+// first version that fetched the four parts separately):
+//   [0, 4096)     K codes  [64 tokens][64 bytes] (token-major, element 2j in
+//                 the low nibble)
+//   [4096, 4608)  K scales [64 tokens][8]
+//   [4608, 8704)  V codes  [128 dims][32 bytes]  (dim-major: byte j of row d
+//                 holds tokens 2j (low nibble) and 2j+1 of dim d)
+//   [8704, 9216)  V scales [8 blocks][64 tokens]
 // so that every tensor-core operand fragment of the attention comes straight
 // from code bytes: K rows feed the B operand of S = Q K^T, V rows (dims)
 // feed the B operand of O = P V, both through ldmatrix.
@@ -44,6 +49,8 @@ constexpr int KS_BYTES = KV_P * KV_D / 16;  // 512
 constexpr int PAGE_BYTES = 2 * (KC_BYTES + KS_BYTES);
 constexpr int KC8_BYTES = KV_P * KV_D;              // FP8 codes of one page and head, 8192
 constexpr int HALF8_BYTES = KC8_BYTES / 2;          // one 32-token half (keys or values)
+constexpr int PAGE8_BYTES = 2 * KC8_BYTES;          // FP8 page block: [2 halves][K 4096 | V 4096]
+constexpr int KS_OFF = KC_BYTES, VC_OFF = KC_BYTES + KS_BYTES, VS_OFF = 2 * KC_BYTES + KS_BYTES;
 constexpr int ATT_WARPS = 4;
 constexpr int ATT_STAGES = 2;
 
@@ -131,7 +138,7 @@ __global__ void kv_append_kernel(KvAppendArgs a)
         // E4M3(x * 1/s) per element; keys token-major [64][128], values in
         // two 32-token halves, dim-major [2][128][32]
         const float r8 = recip_step(s);
-        const int64_t ph8 = (int64_t)page * a.H_kv + hk;
+        uint8_t *blk8 = a.pages + ((int64_t)page * a.H_kv + hk) * PAGE8_BYTES + (slot / 32) * (2 * HALF8_BYTES);
         uint32_t c[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
@@ -141,10 +148,10 @@ __global__ void kv_append_kernel(KvAppendArgs a)
 #pragma unroll
             for (int q = 0; q < 4; ++q)
                 wds[q] = c[4 * q] | (c[4 * q + 1] << 8) | (c[4 * q + 2] << 16) | (c[4 * q + 3] << 24);
-            *reinterpret_cast<uint4 *>(a.k_codes + ph8 * KC8_BYTES + slot * KV_D + blk * 16) =
+            *reinterpret_cast<uint4 *>(blk8 + (slot % 32) * KV_D + blk * 16) =
                 make_uint4(wds[0], wds[1], wds[2], wds[3]);
         } else {
-            uint8_t *vc = a.v_codes + ph8 * KC8_BYTES + (slot / 32) * (KV_D * 32) + (slot % 32);
+            uint8_t *vc = blk8 + HALF8_BYTES + (slot % 32);
 #pragma unroll
             for (int i = 0; i < 16; ++i)
                 vc[(blk * 16 + i) * 32] = (uint8_t)c[i];
@@ -153,16 +160,16 @@ __global__ void kv_append_kernel(KvAppendArgs a)
     }
     const uint32_t e = block_scale_code(amb, s);
     const float r = recip_step(__fmul_rn(e4m3_value(e), s));
-    const int64_t ph = (int64_t)page * a.H_kv + hk;
+    uint8_t *pb = a.pages + ((int64_t)page * a.H_kv + hk) * PAGE_BYTES;
     if (!which) {
         uint32_t pk[2] = {0u, 0u};
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             pk[i >> 2] |= e2m1x2(__fmul_rn(x[2 * i], r), __fmul_rn(x[2 * i + 1], r)) << (8 * (i & 3));
-        *reinterpret_cast<uint2 *>(a.k_codes + ph * KC_BYTES + slot * (KV_D / 2) + blk * 8) = make_uint2(pk[0], pk[1]);
-        a.k_scales[ph * KS_BYTES + slot * (KV_D / 16) + blk] = (uint8_t)e;
+        *reinterpret_cast<uint2 *>(pb + slot * (KV_D / 2) + blk * 8) = make_uint2(pk[0], pk[1]);
+        pb[KS_OFF + slot * (KV_D / 16) + blk] = (uint8_t)e;
     } else {
-        uint8_t *vc = a.v_codes + ph * KC_BYTES;
+        uint8_t *vc = pb + VC_OFF;
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
             const uint32_t two = e2m1x2(__fmul_rn(x[i], r), __fmul_rn(x[i + 1], r));
@@ -173,7 +180,7 @@ __global__ void kv_append_kernel(KvAppendArgs a)
                 *p = (slot & 1) ? (uint8_t)((*p & 0x0Fu) | (c << 4)) : (uint8_t)((*p & 0xF0u) | c);
             }
         }
-        a.v_scales[ph * KS_BYTES + blk * KV_P + slot] = (uint8_t)e;
+        pb[VS_OFF + blk * KV_P + slot] = (uint8_t)e;
     }
 }
 
@@ -198,7 +205,10 @@ static_assert(sizeof(AttMerge) <= ATT_WARPS * ATT_STAGES * PAGE_BYTES, "merge bu
 // Merge of the 4 warps' running softmax states (row sums over the 4 lanes
 // of a group, then through shared memory: the page ring, idle in every warp
 // by now) and the store of the output, or of this split's partial.
-__device__ __forceinline__ void kv_merge_and_store(const KvAttnArgs &a, AttMerge &mg, const float (&o)[16][4],
+// The output accumulators hold O^T: o[mt][nt][i] is dimension 16 mt + g +
+// 8 (i >> 1) of head 8 nt + 2t + (i & 1).
+template <int NT>
+__device__ __forceinline__ void kv_merge_and_store(const KvAttnArgs &a, AttMerge &mg, const float (&o)[8][NT][4],
                                                    const float (&m_run)[2], float (&l_run)[2], int warp, int g,
                                                    int t, int G, int b, int hk, int split, float s_v)
 {
@@ -215,12 +225,12 @@ __device__ __forceinline__ void kv_merge_and_store(const KvAttnArgs &a, AttMerge
         mg.l[warp][g + 8] = l_run[1];
     }
 #pragma unroll
-    for (int n = 0; n < 16; ++n) {
-        mg.o[warp][g][8 * n + 2 * t] = o[n][0];
-        mg.o[warp][g][8 * n + 2 * t + 1] = o[n][1];
-        mg.o[warp][g + 8][8 * n + 2 * t] = o[n][2];
-        mg.o[warp][g + 8][8 * n + 2 * t + 1] = o[n][3];
-    }
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                mg.o[warp][8 * nt + 2 * t + (i & 1)][16 * mt + g + 8 * (i >> 1)] = o[mt][nt][i];
     __syncthreads();
     for (int idx = threadIdx.x; idx < G * KV_D; idx += 32 * ATT_WARPS) {
         const int head = idx / KV_D, d = idx % KV_D;
@@ -256,14 +266,17 @@ __device__ __forceinline__ void kv_merge_and_store(const KvAttnArgs &a, AttMerge
 }
 
 // Online softmax update of one 32-key chunk's scores (base 2, already
-// scaled): masks keys past `valid` (a partial chunk only), rescales the
-// running state and the output accumulators (only when a row maximum grew),
-// returns the P fragments of the chunk's two 16-key steps.  Key of sc[j][i]
-// is key_of(j, 2t + (i & 1)); rows g (i < 2), g + 8 (i >= 2, skipped when the
-// group has at most 8 query heads: those rows are padding and get P = 0).
+// scaled): masks keys past `valid` (a partial chunk only), updates the running
+// maxima and sums, and returns the P fragments of the chunk's two 16-key
+// steps and whether any row maximum grew (warp-uniform), with the factors
+// corr[] (rows g, g + 8) by which that row's accumulated output must be
+// scaled.  Key of sc[j][i] is key_of(j, 2t + (i & 1)); rows g (i < 2), g + 8
+// (i >= 2, skipped when the group has at most 8 query heads: those rows are
+// padding and get P = 0).  P of 16-key step s, n-tile (heads) nt: the B
+// operand pair (pf[s][nt], pf[s][2 + nt]) of O^T += V^T P^T.
 template <typename KeyOf>
-__device__ __forceinline__ void kv_softmax_chunk(float (&sc)[4][4], int valid, int t, KeyOf key_of, bool hi_rows,
-                                                 float (&m_run)[2], float (&l_run)[2], float (&o)[16][4],
+__device__ __forceinline__ bool kv_softmax_chunk(float (&sc)[4][4], int valid, int t, KeyOf key_of, bool hi_rows,
+                                                 float (&m_run)[2], float (&l_run)[2], float (&corr)[2],
                                                  uint32_t (&pf)[2][4])
 {
     if (valid < 32) {
@@ -281,7 +294,7 @@ __device__ __forceinline__ void kv_softmax_chunk(float (&sc)[4][4], int valid, i
             cmax[i >> 1] = fmaxf(cmax[i >> 1], sc[j][i]);
     const int nrows = hi_rows ? 2 : 1;
     bool grew = false;
-    float corr[2] = {1.0f, 1.0f};
+    corr[0] = corr[1] = 1.0f;
     for (int rr = 0; rr < nrows; ++rr) {
         cmax[rr] = fmaxf(cmax[rr], __shfl_xor_sync(0xFFFFFFFFu, cmax[rr], 1));
         cmax[rr] = fmaxf(cmax[rr], __shfl_xor_sync(0xFFFFFFFFu, cmax[rr], 2));
@@ -290,15 +303,6 @@ __device__ __forceinline__ void kv_softmax_chunk(float (&sc)[4][4], int valid, i
             m_run[rr] = cmax[rr];
             l_run[rr] *= corr[rr];
             grew = true;
-        }
-    }
-    if (__any_sync(0xFFFFFFFFu, grew)) {
-#pragma unroll
-        for (int n = 0; n < 16; ++n) {
-            o[n][0] *= corr[0];
-            o[n][1] *= corr[0];
-            o[n][2] *= corr[1];
-            o[n][3] *= corr[1];
         }
     }
 #pragma unroll
@@ -316,6 +320,26 @@ __device__ __forceinline__ void kv_softmax_chunk(float (&sc)[4][4], int valid, i
         pf[j >> 1][(j & 1) * 2 + 0] = pack_h2(pv[0], pv[1]);
         pf[j >> 1][(j & 1) * 2 + 1] = pack_h2(pv[2], pv[3]);
     }
+    return __any_sync(0xFFFFFFFFu, grew);
+}
+
+// Rescale of the O^T accumulators by the factors of their heads (column
+// 2t, 2t+1 of n-tile nt = head rows held by lanes 4 (2t) and 4 (2t+1)).
+template <int NT>
+__device__ __forceinline__ void kv_rescale(float (&o)[8][NT][4], const float (&corr)[2], int t)
+{
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const float c0 = __shfl_sync(0xFFFFFFFFu, corr[nt], 8 * t);
+        const float c1 = __shfl_sync(0xFFFFFFFFu, corr[nt], 8 * t + 4);
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            o[mt][nt][0] *= c0;
+            o[mt][nt][1] *= c1;
+            o[mt][nt][2] *= c0;
+            o[mt][nt][3] *= c1;
+        }
+    }
 }
 
 // Key order inside a 32-key chunk: QK n-tile j (8 keys) column n holds key
@@ -325,6 +349,7 @@ __device__ __forceinline__ void kv_softmax_chunk(float (&sc)[4][4], int valid, i
 // keys of V code byte 4t .. 4t+1 (4t+2 .. 4t+3) that ldmatrix hands lane t.
 __device__ __forceinline__ int chunk_key(int j, int n) { return 8 * (n >> 1) + (n & 1) + 2 * j; }
 
+template <int NT>
 __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_kernel(const KvAttnArgs a)
 {
     extern __shared__ __align__(128) uint8_t att_raw[];
@@ -375,12 +400,15 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_kernel(const KvAttnA
     }
     const float s_k = *a.k_scale, s_v = *a.v_scale;
 
-    float o[16][4];
+    // O^T accumulators: 8 m-tiles of 16 dimensions x NT n-tiles of 8 heads
+    float o[8][NT][4];
 #pragma unroll
-    for (int n = 0; n < 16; ++n)
+    for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            o[n][i] = 0.0f;
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                o[mt][nt][i] = 0.0f;
     float m_run[2] = {-INFINITY, -INFINITY}; // rows g, g + 8 (base-2 scores of unit K)
     float l_run[2] = {0.0f, 0.0f};           // this lane's share of the row sums
 
@@ -389,26 +417,17 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_kernel(const KvAttnA
     int my_pg = 0;
     if (warp + ATT_WARPS * lane < n_pages)
         my_pg = a.block_table[(int64_t)b * a.max_pages + k_begin / KV_P + warp + ATT_WARPS * lane];
-    // warp-collective: the page's four copies go out from lanes 0..3 (one
-    // thread's copies are served one after another)
+    // warp-collective (the page id comes from a shuffle); one copy per page
     auto issue = [&](int p, int s) {
         const int i = (p - warp) / ATT_WARPS;
         int page = __shfl_sync(0xFFFFFFFFu, my_pg, i & 31);
         if (i >= 32)
             page = a.block_table[(int64_t)b * a.max_pages + (k_begin + p * KV_P) / KV_P];
         const int64_t ph = (int64_t)min(max(page, 0), a.num_pages - 1) * a.H_kv + hk;
-        uint8_t *dst = sm.page[warp][s];
-        if (lane == 0)
+        if (lane == 0) {
             mbar_arrive_expect_tx(&sm.full[warp][s], PAGE_BYTES);
-        __syncwarp();
-        if (lane == 0)
-            bulk_load(dst, a.k_codes + ph * KC_BYTES, KC_BYTES, &sm.full[warp][s]);
-        else if (lane == 1)
-            bulk_load(dst + KC_BYTES, a.k_scales + ph * KS_BYTES, KS_BYTES, &sm.full[warp][s]);
-        else if (lane == 2)
-            bulk_load(dst + KC_BYTES + KS_BYTES, a.v_codes + ph * KC_BYTES, KC_BYTES, &sm.full[warp][s]);
-        else if (lane == 3)
-            bulk_load(dst + 2 * KC_BYTES + KS_BYTES, a.v_scales + ph * KS_BYTES, KS_BYTES, &sm.full[warp][s]);
+            bulk_load(sm.page[warp][s], a.pages + ph * PAGE_BYTES, PAGE_BYTES, &sm.full[warp][s]);
+        }
     };
     for (int i = 0; i < ATT_STAGES && warp + i * ATT_WARPS < n_pages; ++i)
         issue(warp + i * ATT_WARPS, i);
@@ -467,41 +486,48 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_kernel(const KvAttnA
                 for (int i = 0; i < 4; ++i)
                     sc[j][i] *= s_k;
             uint32_t pf[2][4]; // P fragments of the two 16-key steps
-            kv_softmax_chunk(sc, valid, t, chunk_key, G > 8, m_run, l_run, o, pf);
-            // ---- O += P V: 2 k-steps x 16 n-tiles (dims), V rows via ldmatrix
-            // keys 8t .. 8t+7 of this chunk are valid up to `valid`
+            float corr[2];
+            if (kv_softmax_chunk(sc, valid, t, chunk_key, NT == 2, m_run, l_run, corr, pf))
+                kv_rescale<NT>(o, corr, t);
+            // ---- O^T += V^T P^T: A = value rows (8 m-tiles of 16 dims), B = P^T
+            // (N = the group's heads: no padding rows); keys 8t .. 8t+7 of
+            // this chunk are valid up to `valid`
             const bool full_chunk = valid >= 32;
             const int nv = min(8, max(0, valid - 8 * t));
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                // 4 n-tiles = 32 dims: lane supplies V row (dim) 32 q4 + lane
+            for (int mp = 0; mp < 4; ++mp) {
+                // matrix i: value rows (dims) 32 mp + 8 i + 0..7; lane l supplies dim 32 mp + l
                 uint32_t vr[4];
-                ldsm_x4(vc + (32 * q4 + lane) * (KV_P / 2) + 16 * h, vr);
+                ldsm_x4(vc + (32 * mp + lane) * (KV_P / 2) + 16 * h, vr);
 #pragma unroll
-                for (int hb = 0; hb < 2; ++hb) {
-                    // n-tiles 2 hb, 2 hb + 1: dims 32 q4 + 16 hb + 0..15, scale block 2 q4 + hb;
-                    // scales of keys 8t .. 8t+7 as four f16x2 pairs
-                    const uint2 e8 = *reinterpret_cast<const uint2 *>(vs + (2 * q4 + hb) * KV_P + key0 + 8 * t);
+                for (int hm = 0; hm < 2; ++hm) {
+                    // m-tile mt: dims 16 mt + g (vr[2 hm]) and + g + 8 (vr[2 hm + 1]), scale block mt
+                    const int mt = 2 * mp + hm;
+                    const uint2 e8 = *reinterpret_cast<const uint2 *>(vs + mt * KV_P + key0 + 8 * t);
                     uint32_t e2[4];
 #pragma unroll
                     for (int y = 0; y < 4; ++y)
                         e2[y] = h2_e4m3x2(((y < 2 ? e8.x : e8.y) >> (16 * (y & 1))) & 0xFFFFu);
+                    uint32_t av[2][4];
 #pragma unroll
-                    for (int n4 = 2 * hb; n4 < 2 * hb + 2; ++n4) {
-                        uint32_t bv[4];
+                    for (int r2 = 0; r2 < 2; ++r2)
 #pragma unroll
                         for (int y = 0; y < 4; ++y) {          // byte y: keys 8t+2y, 8t+2y+1
-                            uint32_t val = hmul2u(h2_e2m1x2((vr[n4] >> (8 * y)) & 0xFFu), e2[y]);
+                            uint32_t val = hmul2u(h2_e2m1x2((vr[2 * hm + r2] >> (8 * y)) & 0xFFu), e2[y]);
                             if (!full_chunk) {
                                 if (2 * y >= nv)
                                     val = 0u;
                                 else if (2 * y + 1 >= nv)
                                     val &= 0x0000FFFFu;
                             }
-                            bv[y] = val;
+                            av[r2][y] = val;
                         }
-                        mma16816(o[4 * q4 + n4], pf[0], bv[0], bv[1]);
-                        mma16816(o[4 * q4 + n4], pf[1], bv[2], bv[3]);
+#pragma unroll
+                    for (int st = 0; st < 2; ++st) {
+                        const uint32_t afr[4] = {av[0][2 * st], av[1][2 * st], av[0][2 * st + 1], av[1][2 * st + 1]};
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            mma16816(o[mt][nt], afr, pf[st][nt], pf[st][2 + nt]);
                     }
                 }
             }
@@ -524,8 +550,8 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_kernel(const KvAttnA
 }
 
 // FP8 cache (E4M3 codes, one static scale per tensor): the same structure
-// with 32-token half pages as the unit (keys [32][128], values [128][32],
-// 4 KB each, contiguous in the FP8 layout).  A 16-byte ldmatrix row holds 16
+// with 32-token half pages as the unit (keys [32][128] then values
+// [128][32], 8 KB contiguous in the FP8 page block, one bulk copy).  A 16-byte ldmatrix row holds 16
 // FP8 elements, so lane t receives elements 4t .. 4t+3 of its row: for keys,
 // dims 16 kk + 4t + {0,1} / {2,3} fill k slots 2t, 2t+1 / 2t+8, 2t+9 of k-step
 // kk; for values, keys 16 s + 4t + ... of step s.  QK n-tile j column n holds
@@ -533,6 +559,7 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_kernel(const KvAttnA
 // elements, no per-element scale.
 __device__ __forceinline__ int chunk_key8(int j, int n) { return 16 * (j >> 1) + 4 * (n >> 1) + (n & 1) + 2 * (j & 1); }
 
+template <int NT>
 __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_fp8_kernel(const KvAttnArgs a)
 {
     extern __shared__ __align__(128) uint8_t att_raw[];
@@ -573,12 +600,15 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_fp8_kernel(const KvA
             }
     }
     const float s_k = *a.k_scale, s_v = *a.v_scale;
-    float o[16][4];
+    // O^T accumulators: 8 m-tiles of 16 dimensions x NT n-tiles of 8 heads
+    float o[8][NT][4];
 #pragma unroll
-    for (int n = 0; n < 16; ++n)
+    for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            o[n][i] = 0.0f;
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                o[mt][nt][i] = 0.0f;
     float m_run[2] = {-INFINITY, -INFINITY};
     float l_run[2] = {0.0f, 0.0f};
 
@@ -588,7 +618,7 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_fp8_kernel(const KvA
     int my_pg = 0;
     if (warp + ATT_WARPS * lane < n_chunks)
         my_pg = a.block_table[(int64_t)b * a.max_pages + (k_begin + 32 * (warp + ATT_WARPS * lane)) / KV_P];
-    // warp-collective: the two copies go out from lanes 0 and 1
+    // warp-collective (the page id comes from a shuffle); one copy per half page
     auto issue = [&](int c, int s) {
         const int i = (c - warp) / ATT_WARPS;
         const int tok = k_begin + 32 * c;
@@ -597,15 +627,11 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_fp8_kernel(const KvA
             page = a.block_table[(int64_t)b * a.max_pages + tok / KV_P];
         const int64_t ph = (int64_t)min(max(page, 0), a.num_pages - 1) * a.H_kv + hk;
         const int half = (tok / 32) & 1;
-        uint8_t *dst = sm.page[warp][s];
-        if (lane == 0)
+        if (lane == 0) {
             mbar_arrive_expect_tx(&sm.full[warp][s], 2 * HALF8_BYTES);
-        __syncwarp();
-        if (lane == 0)
-            bulk_load(dst, a.k_codes + ph * KC8_BYTES + half * HALF8_BYTES, HALF8_BYTES, &sm.full[warp][s]);
-        else if (lane == 1)
-            bulk_load(dst + HALF8_BYTES, a.v_codes + ph * KC8_BYTES + half * HALF8_BYTES, HALF8_BYTES,
+            bulk_load(sm.page[warp][s], a.pages + ph * PAGE8_BYTES + half * (2 * HALF8_BYTES), 2 * HALF8_BYTES,
                       &sm.full[warp][s]);
+        }
     };
     for (int i = 0; i < ATT_STAGES && warp + i * ATT_WARPS < n_chunks; ++i)
         issue(warp + i * ATT_WARPS, i);
@@ -642,25 +668,32 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_fp8_kernel(const KvA
             for (int i = 0; i < 4; ++i)
                 sc[j][i] *= s_k;
         uint32_t pf[2][4];
-        kv_softmax_chunk(sc, valid, t, chunk_key8, G > 8, m_run, l_run, o, pf);
-        // ---- O += P V
+        float corr[2];
+        if (kv_softmax_chunk(sc, valid, t, chunk_key8, NT == 2, m_run, l_run, corr, pf))
+            kv_rescale<NT>(o, corr, t);
+        // ---- O^T += V^T P^T: A = value rows (8 m-tiles of 16 dims), B = P^T
         const bool full_chunk = valid >= 32;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int mt = 0; mt < 8; ++mt) {
+            // matrix i: dims 16 mt + 8 (i & 1) + 0..7, keys 16 (i >> 1) .. + 15
+            uint32_t vr[4];
+            ldsm_x4(vc + (16 * mt + 8 * ((lane >> 3) & 1) + (lane & 7)) * 32 + 16 * (lane >> 4), vr);
 #pragma unroll
             for (int st = 0; st < 2; ++st) {
-                uint32_t vr[4];
-                ldsm_x4(vc + (32 * q4 + lane) * 32 + 16 * st, vr);
-                const int nv = min(4, max(0, valid - 16 * st - 4 * t)); // valid keys of this lane's 4
+                // rows g (vr[2 st]) and g + 8 (vr[2 st + 1]): keys 16 st + 4t + {0,1} / {2,3}
+                uint32_t afr[4] = {h2_e4m3x2(vr[2 * st] & 0xFFFFu), h2_e4m3x2(vr[2 * st + 1] & 0xFFFFu),
+                                   h2_e4m3x2(vr[2 * st] >> 16), h2_e4m3x2(vr[2 * st + 1] >> 16)};
+                if (!full_chunk) {
+                    const int nv = min(4, max(0, valid - 16 * st - 4 * t));
 #pragma unroll
-                for (int n4 = 0; n4 < 4; ++n4) {
-                    uint32_t b0 = h2_e4m3x2(vr[n4] & 0xFFFFu), b1 = h2_e4m3x2(vr[n4] >> 16);
-                    if (!full_chunk) {
-                        b0 = nv >= 2 ? b0 : (nv == 1 ? (b0 & 0x0000FFFFu) : 0u);
-                        b1 = nv >= 4 ? b1 : (nv == 3 ? (b1 & 0x0000FFFFu) : 0u);
+                    for (int r2 = 0; r2 < 2; ++r2) {
+                        afr[r2] = nv >= 2 ? afr[r2] : (nv == 1 ? (afr[r2] & 0x0000FFFFu) : 0u);
+                        afr[2 + r2] = nv >= 4 ? afr[2 + r2] : (nv == 3 ? (afr[2 + r2] & 0x0000FFFFu) : 0u);
                     }
-                    mma16816(o[4 * q4 + n4], pf[st], b0, b1);
                 }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    mma16816(o[mt][nt], afr, pf[st][nt], pf[st][2 + nt]);
             }
         }
         __syncwarp();
@@ -733,18 +766,15 @@ size_t kv_attn_partial_bytes(int B, int H, int n_splits)
 cudaError_t launch_kv_decode(const KvAttnArgs &a, cudaStream_t stream)
 {
     const size_t smem = sizeof(AttSmem);
-    cudaError_t e = cudaFuncSetAttribute(kv_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess)
-        return e;
-    if (a.fmt == KV_FMT_FP8 &&
-        (e = cudaFuncSetAttribute(kv_decode_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-            cudaSuccess)
+    cudaError_t e;
+    // one n-tile of 8 heads when a group has at most 8 query heads, else two
+    const bool two = a.H / a.H_kv > 8;
+    auto kern = a.fmt == KV_FMT_FP8 ? (two ? kv_decode_fp8_kernel<2> : kv_decode_fp8_kernel<1>)
+                                    : (two ? kv_decode_kernel<2> : kv_decode_kernel<1>);
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
         return e;
     dim3 grid((unsigned)a.n_splits, (unsigned)a.H_kv, (unsigned)a.B);
-    if (a.fmt == KV_FMT_FP8)
-        kv_decode_fp8_kernel<<<grid, 32 * ATT_WARPS, smem, stream>>>(a);
-    else
-        kv_decode_kernel<<<grid, 32 * ATT_WARPS, smem, stream>>>(a);
+    kern<<<grid, 32 * ATT_WARPS, smem, stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess || a.n_splits == 1)
         return e;
     kv_combine_kernel<<<(unsigned)(a.B * a.H), KV_D, 0, stream>>>(a);

@@ -55,6 +55,51 @@ def kv_v_pages_natural(codes_dm: np.ndarray, scales_bm: np.ndarray):
     return np.ascontiguousarray(k), np.ascontiguousarray(np.swapaxes(np.asarray(scales_bm, np.uint8), -1, -2))
 
 
+def kv_pack_nvfp4(k_c, k_s, v_c_nat, v_s_nat):
+    """Natural per-token NVFP4 cache arrays ([..., 64, 64] codes, [..., 64, 8]
+    scales, for keys and values) -> the cache's page blocks [..., 9216]: key
+    codes, key scales, value codes (dim-major), value scales (block-major)."""
+    vdm, vsbm = kv_v_pages(v_c_nat, v_s_nat)
+    lead = np.asarray(k_c).shape[:-2]
+    parts = [np.asarray(k_c, np.uint8), np.asarray(k_s, np.uint8), vdm, vsbm]
+    return np.ascontiguousarray(np.concatenate([x.reshape(lead + (-1,)) for x in parts], axis=-1))
+
+
+def kv_unpack_nvfp4(blocks):
+    """Inverse of kv_pack_nvfp4: (k_c, k_s, v_c natural, v_s natural)."""
+    b = np.asarray(blocks, np.uint8)
+    lead = b.shape[:-1]
+    k_c = b[..., :4096].reshape(lead + (64, 64))
+    k_s = b[..., 4096:4608].reshape(lead + (64, 8))
+    v_c, v_s = kv_v_pages_natural(b[..., 4608:8704].reshape(lead + (128, 32)),
+                                  b[..., 8704:9216].reshape(lead + (8, 64)))
+    return np.ascontiguousarray(k_c), np.ascontiguousarray(k_s), v_c, v_s
+
+
+def kv_pack_fp8(k, v_nat):
+    """Natural FP8 cache arrays ([..., 64 tokens, 128]) -> page blocks
+    [..., 16384]: per 32-token half, keys [32][128] then values [128][32]."""
+    k, v = np.asarray(k, np.uint8), np.asarray(v_nat, np.uint8)
+    lead = k.shape[:-2]
+    halves = []
+    for h in range(2):
+        halves.append(k[..., 32 * h:32 * h + 32, :].reshape(lead + (-1,)))
+        halves.append(np.swapaxes(v[..., 32 * h:32 * h + 32, :], -1, -2).reshape(lead + (-1,)))
+    return np.ascontiguousarray(np.concatenate(halves, axis=-1))
+
+
+def kv_unpack_fp8(blocks):
+    """Inverse of kv_pack_fp8: (keys, values) natural [..., 64, 128]."""
+    b = np.asarray(blocks, np.uint8)
+    lead = b.shape[:-1]
+    ks, vs = [], []
+    for h in range(2):
+        base = 8192 * h
+        ks.append(b[..., base:base + 4096].reshape(lead + (32, 128)))
+        vs.append(np.swapaxes(b[..., base + 4096:base + 8192].reshape(lead + (128, 32)), -1, -2))
+    return np.ascontiguousarray(np.concatenate(ks, axis=-2)), np.ascontiguousarray(np.concatenate(vs, axis=-2))
+
+
 def bf16_half_ulp(y: np.ndarray) -> np.ndarray:
     """Half the BF16 spacing at |y| (the largest error of rounding y to BF16)."""
     a = np.abs(np.asarray(y, np.float64))

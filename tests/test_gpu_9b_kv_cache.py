@@ -18,7 +18,7 @@ import torch
 import oracle
 import synth
 from gpu_common import host, nv
-from helpers import bf16_half_ulp, kv_v_pages, kv_v_pages_natural
+from helpers import bf16_half_ulp, kv_pack_fp8, kv_pack_nvfp4, kv_unpack_fp8, kv_unpack_nvfp4
 
 pytestmark = pytest.mark.gpu
 
@@ -53,11 +53,9 @@ def build_cache(rng, ctx_lens, H_kv, s_k, s_v, spare_pages=3, shuffle=True):
                 pg = table[b, tkn // P]
                 k_c[pg, hk, tkn % P], k_s[pg, hk, tkn % P] = kc[tkn], ks[tkn]
                 v_c[pg, hk, tkn % P], v_s[pg, hk, tkn % P] = vc[tkn], vs[tkn]
-    vdm, vsbm = kv_v_pages(v_c, v_s)
-    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-    cache = nv.KvCache(dev(k_c), dev(k_s), dev(vdm), dev(vsbm),
+    cache = nv.KvCache(torch.from_numpy(kv_pack_nvfp4(k_c, k_s, v_c, v_s)).cuda(),
                        torch.tensor([s_k], dtype=torch.float32, device="cuda"),
-                       torch.tensor([s_v], dtype=torch.float32, device="cuda"), n_pages, H_kv)
+                       torch.tensor([s_v], dtype=torch.float32, device="cuda"))
     return cache, (k_c, k_s), (v_c, v_s), table, max_pages
 
 
@@ -106,23 +104,17 @@ def test_append_bytes_bit_exact_and_neighbours_untouched():
     H_kv, B = 3, 5
     s_k, s_v = 6.0 / 2688, 3.0 / 2688
     n_pages, max_pages = 16, 3
-    k_c0 = rng.integers(0, 256, (n_pages, H_kv, P, D // 2)).astype(np.uint8)
-    k_s0 = rng.integers(0, 256, (n_pages, H_kv, P, D // 16)).astype(np.uint8)
-    v_c0 = rng.integers(0, 256, (n_pages, H_kv, D, P // 2)).astype(np.uint8)
-    v_s0 = rng.integers(0, 256, (n_pages, H_kv, D // 16, P)).astype(np.uint8)
-    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-    cache = nv.KvCache(dev(k_c0), dev(k_s0), dev(v_c0), dev(v_s0),
-                       torch.tensor([s_k], device="cuda"), torch.tensor([s_v], device="cuda"), n_pages, H_kv)
+    blocks0 = rng.integers(0, 256, (n_pages, H_kv, 9216)).astype(np.uint8)
+    cache = nv.KvCache(torch.from_numpy(blocks0.copy()).cuda(), torch.tensor([s_k], device="cuda"),
+                       torch.tensor([s_v], device="cuda"))
     table = rng.permutation(n_pages)[:B * max_pages].reshape(B, max_pages).astype(np.int32)
     positions = np.array([0, 1, 63, 64, 130], np.int32)     # first, odd, last slot, next page, page 3
     kb = synth.activations(9, 400, B * H_kv, D, 0.02, 8.0).reshape(B, H_kv, D)
     vb = synth.activations(9, 401, B * H_kv, D, 0.0, 1.0).reshape(B, H_kv, D)
     to_dev = lambda x: torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
     nv.kv_append(cache, to_dev(kb), to_dev(vb), torch.from_numpy(positions).cuda(), torch.from_numpy(table).cuda())
-    k_c, k_s = host(cache.k_codes), host(cache.k_scales)
-    v_c, v_s = kv_v_pages_natural(host(cache.v_codes), host(cache.v_scales))
-    ek_c, ek_s = k_c0.copy(), k_s0.copy()
-    ev_c, ev_s = kv_v_pages_natural(v_c0, v_s0)
+    k_c, k_s, v_c, v_s = kv_unpack_nvfp4(host(cache.pages))
+    ek_c, ek_s, ev_c, ev_s = [x.copy() for x in kv_unpack_nvfp4(blocks0)]
     for b in range(B):
         pg, sl = table[b, positions[b] // P], positions[b] % P
         for hk in range(H_kv):
@@ -153,8 +145,8 @@ def test_append_then_attend():
     for tkn in range(n):
         nv.kv_append(cache, to_dev(kb[tkn]), to_dev(vb[tkn]), torch.full((B,), tkn, dtype=torch.int32,
                                                                           device="cuda"), tdev)
-    k_nat = (host(cache.k_codes), host(cache.k_scales))
-    v_nat = kv_v_pages_natural(host(cache.v_codes), host(cache.v_scales))
+    k_c, k_s, v_c, v_s = kv_unpack_nvfp4(host(cache.pages))
+    k_nat, v_nat = (k_c, k_s), (v_c, v_s)
     for b in range(B):
         for hk in range(H_kv):
             c, sc = oracle.kv_encode(kb[:, b, hk], s_k)
@@ -175,13 +167,6 @@ def test_append_then_attend():
 
 # ---- FP8 cache ---------------------------------------------------------------------------
 
-def fp8_v_layout(v_nat):
-    """[..., 64 tokens, 128] -> the FP8 cache's value layout [..., 2, 128, 32]."""
-    v = np.asarray(v_nat, np.uint8)
-    sh = v.shape[:-2]
-    return np.ascontiguousarray(np.swapaxes(v.reshape(sh + (2, 32, D)), -1, -2))
-
-
 def build_cache_fp8(rng, ctx_lens, H_kv, s_k, s_v):
     B = len(ctx_lens)
     pages_per = [max(1, -(-n // P)) for n in ctx_lens]
@@ -201,10 +186,9 @@ def build_cache_fp8(rng, ctx_lens, H_kv, s_k, s_v):
             for tkn in range(n):
                 k[table[b, tkn // P], hk, tkn % P] = kc[tkn]
                 v[table[b, tkn // P], hk, tkn % P] = vc[tkn]
-    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-    cache = nv.KvCache(dev(k), None, dev(fp8_v_layout(v)), None,
+    cache = nv.KvCache(torch.from_numpy(kv_pack_fp8(k, v)).cuda(),
                        torch.tensor([s_k], dtype=torch.float32, device="cuda"),
-                       torch.tensor([s_v], dtype=torch.float32, device="cuda"), n_pages, H_kv, nv.KV_FP8)
+                       torch.tensor([s_v], dtype=torch.float32, device="cuda"), nv.KV_FP8)
     return cache, k, v, table
 
 
@@ -243,22 +227,21 @@ def test_fp8_append_bit_exact():
     rng = np.random.default_rng(17)
     H_kv, B, n_pages, max_pages = 2, 4, 10, 2
     s_k, s_v = 6.0 / 448, 3.0 / 448
-    k0 = rng.integers(0, 256, (n_pages, H_kv, P, D)).astype(np.uint8)
-    v0 = rng.integers(0, 256, (n_pages, H_kv, 2, D, 32)).astype(np.uint8)
-    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-    cache = nv.KvCache(dev(k0), None, dev(v0), None, torch.tensor([s_k], device="cuda"),
-                       torch.tensor([s_v], device="cuda"), n_pages, H_kv, nv.KV_FP8)
+    blocks0 = rng.integers(0, 256, (n_pages, H_kv, 16384)).astype(np.uint8)
+    cache = nv.KvCache(torch.from_numpy(blocks0.copy()).cuda(), torch.tensor([s_k], device="cuda"),
+                       torch.tensor([s_v], device="cuda"), nv.KV_FP8)
     table = rng.permutation(n_pages)[:B * max_pages].reshape(B, max_pages).astype(np.int32)
     positions = np.array([0, 31, 32, 127], np.int32)
     kb = synth.activations(9, 900, B * H_kv, D, 0.02, 8.0).reshape(B, H_kv, D)
     vb = synth.activations(9, 901, B * H_kv, D, 0.0, 1.0).reshape(B, H_kv, D)
     to_dev = lambda x: torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
     nv.kv_append(cache, to_dev(kb), to_dev(vb), torch.from_numpy(positions).cuda(), torch.from_numpy(table).cuda())
-    ek, ev = k0.copy(), v0.copy()
+    ek, ev = kv_unpack_fp8(blocks0)
     for b in range(B):
         pg, sl = table[b, positions[b] // P], positions[b] % P
         for hk in range(H_kv):
             ek[pg, hk, sl] = oracle.kv_encode_fp8(kb[b, hk:hk + 1], s_k)[0]
-            ev[pg, hk, sl // 32, :, sl % 32] = oracle.kv_encode_fp8(vb[b, hk:hk + 1], s_v)[0]
-    np.testing.assert_array_equal(host(cache.k_codes), ek)
-    np.testing.assert_array_equal(host(cache.v_codes), ev)
+            ev[pg, hk, sl] = oracle.kv_encode_fp8(vb[b, hk:hk + 1], s_v)[0]
+    gk, gv = kv_unpack_fp8(host(cache.pages))
+    np.testing.assert_array_equal(gk, ek)
+    np.testing.assert_array_equal(gv, ev)

@@ -448,7 +448,7 @@ def workload_kv_decode(c, steps, warmup, B=16, H=64, H_kv=8, ctx=4096, fmt=0):
                  | (t.randint(0, 2, pg.shape, dtype=t.uint8, device=c.dev, generator=g) << 7))
     else:                  # random codes, scale bytes in a normal range
         pg.copy_(t.randint(0, 256, pg.shape, dtype=t.uint8, device=c.dev, generator=g))
-        for lo, hi in ((4096, 4608), (8704, 9216)):
+        for lo, hi in ((2048, 2304), (4352, 4608), (6656, 6912), (8960, 9216)):
             pg[..., lo:hi] = t.randint(0x28, 0x48, pg[..., lo:hi].shape, dtype=t.uint8, device=c.dev, generator=g)
     perm = t.randperm(n_pages, device=c.dev, generator=g).to(t.int32)
     table = perm.view(B, pages_per).contiguous()

@@ -337,13 +337,14 @@ nvfp4_status nvfp4_moe_down_combine(const nvfp4_tensor *h, const int64_t *expert
  * Cache layout: `pages` is uint8 [num_pages][num_kv_heads][page block], one
  * contiguous block per page (64 token slots) and KV head, owned by the
  * caller; a sequence's pages are listed in its block-table row.
- * NVFP4_KV_NVFP4, 9216-byte blocks:
- *   [0, 4096)     key codes   [64 tokens][64]  token-major, element 2j of a
+ * NVFP4_KV_NVFP4, 9216-byte blocks, two 32-token halves of 4608 bytes
+ * (half h at byte 4608 h holds tokens 32h .. 32h + 31 of the page):
+ *   [0, 2048)     key codes   [32 tokens][64]  token-major, element 2j of a
  *                 token in the low nibble of byte j
- *   [4096, 4608)  key scales  [64 tokens][8]   E4M3
- *   [4608, 8704)  value codes [128 dims][32]   dim-major: byte j of row d
+ *   [2048, 2304)  key scales  [32 tokens][8]   E4M3
+ *   [2304, 4352)  value codes [128 dims][16]   dim-major: byte j of row d
  *                 holds tokens 2j (low nibble) and 2j+1 of dimension d
- *   [8704, 9216)  value scales [8 blocks][64 tokens]
+ *   [4352, 4608)  value scales [8 blocks][32 tokens]
  * NVFP4_KV_FP8, 16384-byte blocks, two 32-token halves of 8192 bytes:
  *   [h*8192, h*8192 + 4096)     keys  [32 tokens][128] E4M3, token-major
  *   [h*8192 + 4096, (h+1)*8192) values [128 dims][32 tokens] E4M3, dim-major

@@ -101,7 +101,8 @@ static WsLayout ws_layout(int op, int64_t M, int64_t N, int64_t K, int64_t E = 0
     if (op == NVFP4_OP_KV_DECODE) {
         // M = sequences, N = query heads, K = max context, E = KV heads
         int ns = 1, kps = 64;
-        kv_attn_splits(M, E, K, device_sm_count(), ns, kps);
+        // sized for the format with the most splits
+        kv_attn_splits(M, E, K, device_sm_count(), kv_ctas_per_sm(KV_FMT_NVFP4, E > 0 ? N / E : N), ns, kps);
         const size_t pb = kv_attn_partial_bytes((int)M, (int)N, ns);
         if (pb)
             L.kv_partial = take(pb);
@@ -809,7 +810,8 @@ nvfp4_status nvfp4_kv_decode_attention(const nvfp4_kv_cache *kv, const void *q_b
     a.k_scale = kv->k_scale;
     a.v_scale = kv->v_scale;
     a.sm_scale = sm_scale;
-    kv_attn_splits(B, H_kv, max_ctx, device_sm_count(), a.n_splits, a.keys_per_split);
+    kv_attn_splits(B, H_kv, max_ctx, device_sm_count(), kv_ctas_per_sm(a.fmt, num_heads / H_kv), a.n_splits,
+                   a.keys_per_split);
     a.out = out;
     a.out_dtype = out_dtype;
     a.partial = L.kv_partial ? reinterpret_cast<float *>(ws_at(ws, L.kv_partial)) : nullptr;

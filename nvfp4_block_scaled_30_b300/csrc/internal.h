@@ -196,9 +196,12 @@ struct KvAttnArgs {
     uint64_t timeout_ns;
 };
 size_t kv_attn_partial_bytes(int B, int H, int n_splits);
-// Context splits of one decode-attention call: one wave of 3 CTAs per SM,
-// at least 256 keys (one page per warp) per split.
-void kv_attn_splits(int64_t B, int64_t H_kv, int64_t max_ctx, int sms, int &n_splits, int &keys_per_split);
+// Context splits of one decode-attention call: one wave of ctas_per_sm CTAs
+// per SM, at least 256 keys per split.  kv_ctas_per_sm: the attention
+// kernel's occupancy for a cache format and query heads per KV head.
+int kv_ctas_per_sm(int fmt, int64_t group);
+void kv_attn_splits(int64_t B, int64_t H_kv, int64_t max_ctx, int sms, int ctas_per_sm, int &n_splits,
+                    int &keys_per_split);
 cudaError_t launch_kv_decode(const KvAttnArgs &a, cudaStream_t stream);
 
 struct MacroGemmArgs {

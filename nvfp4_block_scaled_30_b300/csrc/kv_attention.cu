@@ -9,28 +9,31 @@
 // tensor; attention is scaled dot-product attention of one query token over
 // the cached tokens, the query heads of a group sharing one KV head.
 //
-// Page block layout (head_dim D = 128, 64 tokens per page), one contiguous
-// 9216-byte block per page and KV head, read with ONE bulk copy (measured
-// on B300: an SM serves its bulk copies at a roughly fixed cost per copy
-// for copies this small, so the copy count, not the bytes, bounded the
-// first version that fetched the four parts separately):
-//   [0, 4096)     K codes  [64 tokens][64 bytes] (token-major, element 2j in
+// Page block layout (head_dim D = 128, 64 tokens per page): one contiguous
+// 9216-byte block per page and KV head, made of two 4608-byte halves of 32
+// tokens each; half h (at byte 4608 h) holds, for its tokens:
+//   [0, 2048)     K codes  [32 tokens][64 bytes] (token-major, element 2j in
 //                 the low nibble)
-//   [4096, 4608)  K scales [64 tokens][8]
-//   [4608, 8704)  V codes  [128 dims][32 bytes]  (dim-major: byte j of row d
+//   [2048, 2304)  K scales [32 tokens][8]
+//   [2304, 4352)  V codes  [128 dims][16 bytes]  (dim-major: byte j of row d
 //                 holds tokens 2j (low nibble) and 2j+1 of dim d)
-//   [8704, 9216)  V scales [8 blocks][64 tokens]
+//   [4352, 4608)  V scales [8 blocks][32 tokens]
 // so that every tensor-core operand fragment of the attention comes straight
-// from code bytes: K rows feed the B operand of S = Q K^T, V rows (dims)
-// feed the B operand of O = P V, both through ldmatrix.
+// from code bytes (K rows feed the B operand of S = Q K^T, V rows (dims) the
+// A operand of O^T = V^T P^T, both through ldmatrix), and a half page, the
+// unit the attention streams, is ONE bulk copy (measured on B300: an SM
+// serves bulk copies this small at a roughly fixed cost per copy).
 //
 // Decode attention, one CTA per (sequence, KV head, split of the context),
-// 4 warps; each warp streams its own pages (4 bulk copies per page into a
-// 2-stage per-warp ring) and runs mma.sync m16n8k16 (FP16 operands, FP32
-// accumulation): this contraction has M = the group's query heads (<= 16),
-// far below the 64/128 rows of a tcgen05 MMA, and the kernel is bound by
-// reading the cache, not by tensor throughput.  Online softmax in FP32 (base
-// 2); warps merge through shared memory; splits merge in a second kernel.
+// 4 warps; each warp streams its own half pages through a 2-stage per-warp
+// ring of 4.5 KB units, small enough for 4 CTAs (16 warps) per SM: the
+// kernel is bound by instruction latency at this occupancy, not by tensor
+// or memory throughput.  Products by mma.sync m16n8k16 (FP16 operands, FP32
+// accumulation): S = Q K^T with the group's query heads (<= 16) as M, then
+// O^T = V^T P^T with 16 value dimensions as M and the heads as N; these
+// contractions have 8-16 rows on one side, far below the 64/128 rows of a
+// tcgen05 MMA.  Online softmax in FP32 (base 2); warps merge through shared
+// memory; splits merge in a second kernel.
 #include <algorithm>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -44,13 +47,15 @@ namespace {
 
 constexpr int KV_D = 128;           // head_dim
 constexpr int KV_P = 64;            // tokens per page
-constexpr int KC_BYTES = KV_P * KV_D / 2;   // 4096
-constexpr int KS_BYTES = KV_P * KV_D / 16;  // 512
-constexpr int PAGE_BYTES = 2 * (KC_BYTES + KS_BYTES);
+constexpr int KV_H = KV_P / 2;      // tokens per half page, the unit of the attention
+constexpr int KS4_OFF = KV_H * KV_D / 2;              // 2048: K scales of a half page
+constexpr int VC4_OFF = KS4_OFF + KV_H * KV_D / 16;   // 2304: V codes
+constexpr int VS4_OFF = VC4_OFF + KV_H * KV_D / 2;    // 4352: V scales
+constexpr int HALF4_BYTES = VS4_OFF + KV_H * KV_D / 16; // 4608
+constexpr int PAGE_BYTES = 2 * HALF4_BYTES;           // 9216
 constexpr int KC8_BYTES = KV_P * KV_D;              // FP8 codes of one page and head, 8192
 constexpr int HALF8_BYTES = KC8_BYTES / 2;          // one 32-token half (keys or values)
 constexpr int PAGE8_BYTES = 2 * KC8_BYTES;          // FP8 page block: [2 halves][K 4096 | V 4096]
-constexpr int KS_OFF = KC_BYTES, VC_OFF = KC_BYTES + KS_BYTES, VS_OFF = 2 * KC_BYTES + KS_BYTES;
 constexpr int ATT_WARPS = 4;
 constexpr int ATT_STAGES = 2;
 
@@ -99,7 +104,7 @@ __device__ __forceinline__ void ldsm_x4(const void *row_addr, uint32_t (&r)[4])
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
 {
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
                  "{%8, %9}, {%0, %1, %2, %3};"
                  : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
@@ -160,47 +165,52 @@ __global__ void kv_append_kernel(KvAppendArgs a)
     }
     const uint32_t e = block_scale_code(amb, s);
     const float r = recip_step(__fmul_rn(e4m3_value(e), s));
-    uint8_t *pb = a.pages + ((int64_t)page * a.H_kv + hk) * PAGE_BYTES;
+    // the half page of this slot, and the slot's token within it
+    uint8_t *pb = a.pages + ((int64_t)page * a.H_kv + hk) * PAGE_BYTES + (slot / KV_H) * HALF4_BYTES;
+    const int sl = slot % KV_H;
     if (!which) {
         uint32_t pk[2] = {0u, 0u};
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             pk[i >> 2] |= e2m1x2(__fmul_rn(x[2 * i], r), __fmul_rn(x[2 * i + 1], r)) << (8 * (i & 3));
-        *reinterpret_cast<uint2 *>(pb + slot * (KV_D / 2) + blk * 8) = make_uint2(pk[0], pk[1]);
-        pb[KS_OFF + slot * (KV_D / 16) + blk] = (uint8_t)e;
+        *reinterpret_cast<uint2 *>(pb + sl * (KV_D / 2) + blk * 8) = make_uint2(pk[0], pk[1]);
+        pb[KS4_OFF + sl * (KV_D / 16) + blk] = (uint8_t)e;
     } else {
-        uint8_t *vc = pb + VC_OFF;
+        uint8_t *vc = pb + VC4_OFF;
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
             const uint32_t two = e2m1x2(__fmul_rn(x[i], r), __fmul_rn(x[i + 1], r));
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const uint32_t c = (two >> (4 * h)) & 15u;
-                uint8_t *p = vc + (blk * 16 + i + h) * (KV_P / 2) + slot / 2;
-                *p = (slot & 1) ? (uint8_t)((*p & 0x0Fu) | (c << 4)) : (uint8_t)((*p & 0xF0u) | c);
+                uint8_t *p = vc + (blk * 16 + i + h) * (KV_H / 2) + sl / 2;
+                *p = (sl & 1) ? (uint8_t)((*p & 0x0Fu) | (c << 4)) : (uint8_t)((*p & 0xF0u) | c);
             }
         }
-        pb[VS_OFF + blk * KV_P + slot] = (uint8_t)e;
+        pb[VS4_OFF + blk * KV_H + sl] = (uint8_t)e;
     }
 }
 
 // ---- decode attention ------------------------------------------------------------------
 
-// The page ring is dead once every warp has left its loop, so the warps'
-// partial outputs reuse it for the merge (3 CTAs fit on an SM).
+// The unit ring is dead once every warp has left its loop, so the warps'
+// partial outputs reuse it for the merge.
 struct AttMerge {
     float o[ATT_WARPS][16][KV_D];
     float m[ATT_WARPS][16];
     float l[ATT_WARPS][16];
 };
+template <int UNIT>
 struct AttSmem {
     union {
-        uint8_t page[ATT_WARPS][ATT_STAGES][PAGE_BYTES]; // per warp: K codes, K scales, V codes, V scales
+        uint8_t unit[ATT_WARPS][ATT_STAGES][UNIT]; // per warp: the half pages in flight
         AttMerge merge;
     };
     uint64_t full[ATT_WARPS][ATT_STAGES];
 };
-static_assert(sizeof(AttMerge) <= ATT_WARPS * ATT_STAGES * PAGE_BYTES, "merge buffer fits in the ring");
+static_assert(sizeof(AttMerge) <= ATT_WARPS * ATT_STAGES * HALF4_BYTES, "merge buffer fits in the ring");
+using AttSmem4 = AttSmem<HALF4_BYTES>;
+using AttSmem8 = AttSmem<2 * HALF8_BYTES>;
 
 // Merge of the 4 warps' running softmax states (row sums over the 4 lanes
 // of a group, then through shared memory: the page ring, idle in every warp
@@ -349,11 +359,13 @@ __device__ __forceinline__ void kv_rescale(float (&o)[8][NT][4], const float (&c
 // keys of V code byte 4t .. 4t+1 (4t+2 .. 4t+3) that ldmatrix hands lane t.
 __device__ __forceinline__ int chunk_key(int j, int n) { return 8 * (n >> 1) + (n & 1) + 2 * j; }
 
+// Occupancy: at most 128 registers a thread for one n-tile, so that 4 CTAs
+// fit on an SM (the ring takes 36 KB of shared memory per CTA); 3 for two.
 template <int NT>
-__global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_kernel(const KvAttnArgs a)
+__global__ void __launch_bounds__(32 * ATT_WARPS, NT == 1 ? 4 : 3) kv_decode_kernel(const KvAttnArgs a)
 {
     extern __shared__ __align__(128) uint8_t att_raw[];
-    AttSmem &sm = *reinterpret_cast<AttSmem *>(att_raw);
+    AttSmem4 &sm = *reinterpret_cast<AttSmem4 *>(att_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
@@ -361,7 +373,7 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_kernel(const KvAttnA
     const int ctx = max(0, min(min(a.ctx_lens[b], a.max_ctx), a.max_pages * KV_P));
     const int k_begin = split * a.keys_per_split;
     const int k_end = min(ctx, k_begin + a.keys_per_split);
-    const int n_pages = k_end > k_begin ? (k_end - k_begin + KV_P - 1) / KV_P : 0;
+    const int n_chunks = k_end > k_begin ? (k_end - k_begin + KV_H - 1) / KV_H : 0;
 
     if (lane == 0) {
         for (int s = 0; s < ATT_STAGES; ++s)
@@ -412,28 +424,32 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_kernel(const KvAttnA
     float m_run[2] = {-INFINITY, -INFINITY}; // rows g, g + 8 (base-2 scores of unit K)
     float l_run[2] = {0.0f, 0.0f};           // this lane's share of the row sums
 
-    // pages of this warp: p = warp, warp + 4, ... of the CTA's range
-    // page ids of this warp's first 32 pages, one per lane, read once
+    // chunk c of this CTA's range: keys k_begin + 32 c .. + 31 = half
+    // ((k_begin / 32 + c) % 2) of page (k_begin + 32 c) / 64; chunks of this
+    // warp: c = warp, warp + 4, ...; page ids of its first 32, one per lane
     int my_pg = 0;
-    if (warp + ATT_WARPS * lane < n_pages)
-        my_pg = a.block_table[(int64_t)b * a.max_pages + k_begin / KV_P + warp + ATT_WARPS * lane];
-    // warp-collective (the page id comes from a shuffle); one copy per page
-    auto issue = [&](int p, int s) {
-        const int i = (p - warp) / ATT_WARPS;
+    if (warp + ATT_WARPS * lane < n_chunks)
+        my_pg = a.block_table[(int64_t)b * a.max_pages + (k_begin + KV_H * (warp + ATT_WARPS * lane)) / KV_P];
+    // warp-collective (the page id comes from a shuffle); one copy per half page
+    auto issue = [&](int c, int s) {
+        const int i = (c - warp) / ATT_WARPS;
+        const int tok = k_begin + KV_H * c;
         int page = __shfl_sync(0xFFFFFFFFu, my_pg, i & 31);
         if (i >= 32)
-            page = a.block_table[(int64_t)b * a.max_pages + (k_begin + p * KV_P) / KV_P];
+            page = a.block_table[(int64_t)b * a.max_pages + tok / KV_P];
         const int64_t ph = (int64_t)min(max(page, 0), a.num_pages - 1) * a.H_kv + hk;
+        const int half = (tok / KV_H) & 1;
         if (lane == 0) {
-            mbar_arrive_expect_tx(&sm.full[warp][s], PAGE_BYTES);
-            bulk_load(sm.page[warp][s], a.pages + ph * PAGE_BYTES, PAGE_BYTES, &sm.full[warp][s]);
+            mbar_arrive_expect_tx(&sm.full[warp][s], HALF4_BYTES);
+            bulk_load(sm.unit[warp][s], a.pages + ph * PAGE_BYTES + half * HALF4_BYTES, HALF4_BYTES,
+                      &sm.full[warp][s]);
         }
     };
-    for (int i = 0; i < ATT_STAGES && warp + i * ATT_WARPS < n_pages; ++i)
+    for (int i = 0; i < ATT_STAGES && warp + i * ATT_WARPS < n_chunks; ++i)
         issue(warp + i * ATT_WARPS, i);
     bool ok = true;
     int it = 0;
-    for (int p = warp; p < n_pages; p += ATT_WARPS, ++it) {
+    for (int c = warp; c < n_chunks; c += ATT_WARPS, ++it) {
         const int s = it % ATT_STAGES;
         const uint32_t par = (uint32_t)(it / ATT_STAGES) & 1u;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sm.full[warp][s], par, a.timeout_ns, nullptr))) {
@@ -442,27 +458,22 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_kernel(const KvAttnA
             ok = false;
             break;
         }
-        const uint8_t *kc = sm.page[warp][s];
-        const uint8_t *ks = kc + KC_BYTES;
-        const uint8_t *vc = ks + KS_BYTES;
-        const uint8_t *vs = vc + KC_BYTES;
-        const int tok0 = k_begin + p * KV_P;
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) { // 32-key chunks of the page
-            const int key0 = 32 * h;
-            const int valid = min(32, k_end - (tok0 + key0)); // keys of this chunk in the context
-            if (valid <= 0)
-                break;
+        const uint8_t *kc = sm.unit[warp][s];
+        const uint8_t *ks = kc + KS4_OFF;
+        const uint8_t *vc = kc + VC4_OFF;
+        const uint8_t *vs = kc + VS4_OFF;
+        const int valid = min(KV_H, k_end - (k_begin + KV_H * c)); // keys of this chunk in the context
+        {
             // ---- S = Q K^T over 32 keys: 4 n-tiles x 8 k-steps
             float sc[4][4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 // lane (g, t) supplies key chunk_key(j, g): 4 x 16 bytes of its row
                 // (ldmatrix matrix i = dims 32 i .. 32 i + 31)
-                const int krow = key0 + chunk_key(j, lane & 7);
+                const int krow = chunk_key(j, lane & 7);
                 uint32_t kr[4];
                 ldsm_x4(kc + krow * (KV_D / 2) + 16 * (lane >> 3), kr);
-                const int myrow = key0 + chunk_key(j, g);
+                const int myrow = chunk_key(j, g);
                 const uint2 sc8 = *reinterpret_cast<const uint2 *>(ks + myrow * (KV_D / 16));
                 const uint32_t sb[2] = {sc8.x, sc8.y}; // block scales of this lane's key, 8 bytes
                 sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.0f;
@@ -498,12 +509,12 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_kernel(const KvAttnA
             for (int mp = 0; mp < 4; ++mp) {
                 // matrix i: value rows (dims) 32 mp + 8 i + 0..7; lane l supplies dim 32 mp + l
                 uint32_t vr[4];
-                ldsm_x4(vc + (32 * mp + lane) * (KV_P / 2) + 16 * h, vr);
+                ldsm_x4(vc + (32 * mp + lane) * (KV_H / 2), vr);
 #pragma unroll
                 for (int hm = 0; hm < 2; ++hm) {
                     // m-tile mt: dims 16 mt + g (vr[2 hm]) and + g + 8 (vr[2 hm + 1]), scale block mt
                     const int mt = 2 * mp + hm;
-                    const uint2 e8 = *reinterpret_cast<const uint2 *>(vs + mt * KV_P + key0 + 8 * t);
+                    const uint2 e8 = *reinterpret_cast<const uint2 *>(vs + mt * KV_H + 8 * t);
                     uint32_t e2[4];
 #pragma unroll
                     for (int y = 0; y < 4; ++y)
@@ -532,16 +543,16 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_kernel(const KvAttnA
                 }
             }
         }
-        // the stage is free again: this warp's next page goes into it
+        // the stage is free again: this warp's next half page goes into it
         __syncwarp();
-        if (p + ATT_STAGES * ATT_WARPS < n_pages) {
+        if (c + ATT_STAGES * ATT_WARPS < n_chunks) {
             fence_proxy_async_smem();
-            issue(p + ATT_STAGES * ATT_WARPS, s);
+            issue(c + ATT_STAGES * ATT_WARPS, s);
         }
     }
     // drain: every copy this warp issued lands before the CTA moves on
     if (lane == 0 && !ok) {
-        const int mine = n_pages > warp ? (n_pages - warp + ATT_WARPS - 1) / ATT_WARPS : 0;
+        const int mine = n_chunks > warp ? (n_chunks - warp + ATT_WARPS - 1) / ATT_WARPS : 0;
         for (int i = it; i < mine && i < it + ATT_STAGES; ++i)
             mbar_wait(&sm.full[warp][i % ATT_STAGES], (uint32_t)(i / ATT_STAGES) & 1u, a.timeout_ns, nullptr);
     }
@@ -563,7 +574,7 @@ template <int NT>
 __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_fp8_kernel(const KvAttnArgs a)
 {
     extern __shared__ __align__(128) uint8_t att_raw[];
-    AttSmem &sm = *reinterpret_cast<AttSmem *>(att_raw);
+    AttSmem8 &sm = *reinterpret_cast<AttSmem8 *>(att_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
@@ -629,7 +640,7 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_fp8_kernel(const KvA
         const int half = (tok / 32) & 1;
         if (lane == 0) {
             mbar_arrive_expect_tx(&sm.full[warp][s], 2 * HALF8_BYTES);
-            bulk_load(sm.page[warp][s], a.pages + ph * PAGE8_BYTES + half * (2 * HALF8_BYTES), 2 * HALF8_BYTES,
+            bulk_load(sm.unit[warp][s], a.pages + ph * PAGE8_BYTES + half * (2 * HALF8_BYTES), 2 * HALF8_BYTES,
                       &sm.full[warp][s]);
         }
     };
@@ -646,7 +657,7 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_fp8_kernel(const KvA
             ok = false;
             break;
         }
-        const uint8_t *kc = sm.page[warp][s];      // [32 keys][128]
+        const uint8_t *kc = sm.unit[warp][s];      // [32 keys][128]
         const uint8_t *vc = kc + HALF8_BYTES;      // [128 dims][32 keys]
         const int valid = min(32, k_end - (k_begin + 32 * c));
         // ---- S = Q K^T over 32 keys
@@ -745,12 +756,20 @@ cudaError_t launch_kv_append(const KvAppendArgs &a, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-void kv_attn_splits(int64_t B, int64_t H_kv, int64_t max_ctx, int sms, int &n_splits, int &keys_per_split)
+int kv_ctas_per_sm(int fmt, int64_t group)
+{
+    // NVFP4, one n-tile: 36 KB of ring and <= 128 registers a thread; FP8
+    // (64 KB of ring) and two n-tiles (more registers): 3
+    return fmt == KV_FMT_NVFP4 && group <= 8 ? 4 : 3;
+}
+
+void kv_attn_splits(int64_t B, int64_t H_kv, int64_t max_ctx, int sms, int ctas_per_sm, int &n_splits,
+                    int &keys_per_split)
 {
     // as many splits as keep every (sequence, KV head) CTA of the grid in one
-    // wave of 3 CTAs per SM
+    // wave of ctas_per_sm CTAs per SM
     const int64_t units = std::max<int64_t>(1, B * H_kv);
-    int64_t ns = std::max<int64_t>(1, 3 * (int64_t)sms / units);
+    int64_t ns = std::max<int64_t>(1, (int64_t)ctas_per_sm * sms / units);
     ns = std::min<int64_t>(ns, std::max<int64_t>(1, (max_ctx + 255) / 256));
     int64_t kps = (std::max<int64_t>(max_ctx, 1) + ns - 1) / ns;
     kps = (kps + KV_P - 1) / KV_P * KV_P;
@@ -765,7 +784,7 @@ size_t kv_attn_partial_bytes(int B, int H, int n_splits)
 
 cudaError_t launch_kv_decode(const KvAttnArgs &a, cudaStream_t stream)
 {
-    const size_t smem = sizeof(AttSmem);
+    const size_t smem = a.fmt == KV_FMT_FP8 ? sizeof(AttSmem8) : sizeof(AttSmem4);
     cudaError_t e;
     // one n-tile of 8 heads when a group has at most 8 query heads, else two
     const bool two = a.H / a.H_kv > 8;

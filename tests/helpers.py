@@ -57,11 +57,15 @@ def kv_v_pages_natural(codes_dm: np.ndarray, scales_bm: np.ndarray):
 
 def kv_pack_nvfp4(k_c, k_s, v_c_nat, v_s_nat):
     """Natural per-token NVFP4 cache arrays ([..., 64, 64] codes, [..., 64, 8]
-    scales, for keys and values) -> the cache's page blocks [..., 9216]: key
-    codes, key scales, value codes (dim-major), value scales (block-major)."""
-    vdm, vsbm = kv_v_pages(v_c_nat, v_s_nat)
+    scales, for keys and values) -> the cache's page blocks [..., 9216]: per
+    32-token half, key codes [32][64], key scales [32][8], value codes
+    dim-major [128][16], value scales block-major [8][32]."""
     lead = np.asarray(k_c).shape[:-2]
-    parts = [np.asarray(k_c, np.uint8), np.asarray(k_s, np.uint8), vdm, vsbm]
+    parts = []
+    for h in range(2):
+        sl = slice(32 * h, 32 * h + 32)
+        vdm, vsbm = kv_v_pages(np.asarray(v_c_nat)[..., sl, :], np.asarray(v_s_nat)[..., sl, :])
+        parts += [np.asarray(k_c, np.uint8)[..., sl, :], np.asarray(k_s, np.uint8)[..., sl, :], vdm, vsbm]
     return np.ascontiguousarray(np.concatenate([x.reshape(lead + (-1,)) for x in parts], axis=-1))
 
 
@@ -69,11 +73,16 @@ def kv_unpack_nvfp4(blocks):
     """Inverse of kv_pack_nvfp4: (k_c, k_s, v_c natural, v_s natural)."""
     b = np.asarray(blocks, np.uint8)
     lead = b.shape[:-1]
-    k_c = b[..., :4096].reshape(lead + (64, 64))
-    k_s = b[..., 4096:4608].reshape(lead + (64, 8))
-    v_c, v_s = kv_v_pages_natural(b[..., 4608:8704].reshape(lead + (128, 32)),
-                                  b[..., 8704:9216].reshape(lead + (8, 64)))
-    return np.ascontiguousarray(k_c), np.ascontiguousarray(k_s), v_c, v_s
+    out = [[], [], [], []]
+    for h in range(2):
+        o = 4608 * h
+        out[0].append(b[..., o:o + 2048].reshape(lead + (32, 64)))
+        out[1].append(b[..., o + 2048:o + 2304].reshape(lead + (32, 8)))
+        v_c, v_s = kv_v_pages_natural(b[..., o + 2304:o + 4352].reshape(lead + (128, 16)),
+                                      b[..., o + 4352:o + 4608].reshape(lead + (8, 32)))
+        out[2].append(v_c)
+        out[3].append(v_s)
+    return tuple(np.ascontiguousarray(np.concatenate(x, axis=-2)) for x in out)
 
 
 def kv_pack_fp8(k, v_nat):

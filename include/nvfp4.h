@@ -339,16 +339,23 @@ nvfp4_status nvfp4_moe_down_combine(const nvfp4_tensor *h, const int64_t *expert
  * caller; a sequence's pages are listed in its block-table row.
  * NVFP4_KV_NVFP4, 9216-byte blocks, two 32-token halves of 4608 bytes
  * (half h at byte 4608 h holds tokens 32h .. 32h + 31 of the page):
- *   [0, 2048)     key codes   [32 tokens][64]  token-major, element 2j of a
- *                 token in the low nibble of byte j
- *   [2048, 2304)  key scales  [32 tokens][8]   E4M3
+ *   [0, 2048)     key codes   [4 dim chunks][32 key slots][16]: chunk q
+ *                 holds dims 32q .. 32q + 31, element 2j in the low nibble
+ *                 of byte j; token k of the half sits in key slot
+ *                 8*((k>>1)&3) + 2*(k>>3) + (k&1)
+ *   [2048, 2304)  key scales  [32 key slots][8] E4M3
  *   [2304, 4352)  value codes [128 dims][16]   dim-major: byte j of row d
  *                 holds tokens 2j (low nibble) and 2j+1 of dimension d
  *   [4352, 4608)  value scales [8 blocks][32 tokens]
- * NVFP4_KV_FP8, 16384-byte blocks, two 32-token halves of 8192 bytes:
- *   [h*8192, h*8192 + 4096)     keys  [32 tokens][128] E4M3, token-major
- *   [h*8192 + 4096, (h+1)*8192) values [128 dims][32 tokens] E4M3, dim-major
- *   (token 32h + j of the page).
+ * NVFP4_KV_FP8, 16384-byte blocks, two 32-token halves of 8192 bytes
+ * (half h at byte 8192 h holds tokens 32h .. 32h + 31 of the page):
+ *   [0, 4096)     keys   [8 dim chunks][32 key slots][16] E4M3: chunk q holds
+ *                 dims 16q .. 16q + 15; token k of the half sits in key slot
+ *                 (k&16) | ((k&2)<<2) | ((k>>1)&6) | (k&1)
+ *   [4096, 8192)  values [2 token groups][128 dims][16] E4M3: byte j of row
+ *                 d of group u holds token 16u + j of dimension d.
+ * (The key slot orders put the 8 keys the attention reads together in 8
+ * consecutive 16-byte rows.)
  * Both: k_scale, v_scale are device float[1] tensor scales.  A page belongs
  * to one sequence; slots past a sequence's length may hold anything (the
  * attention ignores them). */

@@ -12,17 +12,19 @@
 // Page block layout (head_dim D = 128, 64 tokens per page): one contiguous
 // 9216-byte block per page and KV head, made of two 4608-byte halves of 32
 // tokens each; half h (at byte 4608 h) holds, for its tokens:
-//   [0, 2048)     K codes  [32 tokens][64 bytes] (token-major, element 2j in
-//                 the low nibble)
-//   [2048, 2304)  K scales [32 tokens][8]
+//   [0, 2048)     K codes  [4 dim chunks][32 key slots][16 bytes] (chunk q:
+//                 dims 32 q .. 32 q + 31, element 2j in the low nibble of
+//                 byte j); key slot kpos4(token) holds the token
+//   [2048, 2304)  K scales [32 key slots][8]
 //   [2304, 4352)  V codes  [128 dims][16 bytes]  (dim-major: byte j of row d
 //                 holds tokens 2j (low nibble) and 2j+1 of dim d)
 //   [4352, 4608)  V scales [8 blocks][32 tokens]
 // so that every tensor-core operand fragment of the attention comes straight
 // from code bytes (K rows feed the B operand of S = Q K^T, V rows (dims) the
-// A operand of O^T = V^T P^T, both through ldmatrix), and a half page, the
-// unit the attention streams, is ONE bulk copy (measured on B300: an SM
-// serves bulk copies this small at a roughly fixed cost per copy).
+// A operand of O^T = V^T P^T, both through ldmatrix, each 8x16-byte matrix
+// one contiguous 128 bytes: no bank conflicts), and a half page, the unit
+// the attention streams, is ONE bulk copy (measured on B300: an SM serves
+// bulk copies this small at a roughly fixed cost per copy).
 //
 // Decode attention, one CTA per (sequence, KV head, split of the context),
 // 4 warps; each warp streams its own half pages through a 2-stage per-warp
@@ -58,6 +60,14 @@ constexpr int HALF8_BYTES = KC8_BYTES / 2;          // one 32-token half (keys o
 constexpr int PAGE8_BYTES = 2 * KC8_BYTES;          // FP8 page block: [2 halves][K 4096 | V 4096]
 constexpr int ATT_WARPS = 4;
 constexpr int ATT_STAGES = 2;
+
+// Key slot of token k (0..31) of a half page.  The attention reads the keys
+// of one score n-tile (8 keys, chunk_key / chunk_key8 below) as 8
+// consecutive 16-byte rows: n-tile j column n sits in slot 8 j + n.  NVFP4:
+// the 2-bit fields k[4:3] and k[2:1] trade places; FP8: k[1] moves to bit 3
+// and k[3:2] to bits 2:1.
+__host__ __device__ __forceinline__ int kpos4(int k) { return 8 * ((k >> 1) & 3) + 2 * (k >> 3) + (k & 1); }
+__host__ __device__ __forceinline__ int kpos8(int k) { return (k & 16) | ((k & 2) << 2) | ((k >> 1) & 6) | (k & 1); }
 
 __device__ __forceinline__ uint32_t h2_e2m1x2(uint32_t byte)
 {
@@ -140,8 +150,8 @@ __global__ void kv_append_kernel(KvAppendArgs a)
     }
     const float s = *(which ? a.v_scale : a.k_scale);
     if (a.fmt == KV_FMT_FP8) {
-        // E4M3(x * 1/s) per element; keys token-major [64][128], values in
-        // two 32-token halves, dim-major [2][128][32]
+        // E4M3(x * 1/s) per element; per 32-token half, keys [8 dim chunks]
+        // [32 key slots][16], values [2 token groups][128 dims][16]
         const float r8 = recip_step(s);
         uint8_t *blk8 = a.pages + ((int64_t)page * a.H_kv + hk) * PAGE8_BYTES + (slot / 32) * (2 * HALF8_BYTES);
         uint32_t c[16];
@@ -153,13 +163,14 @@ __global__ void kv_append_kernel(KvAppendArgs a)
 #pragma unroll
             for (int q = 0; q < 4; ++q)
                 wds[q] = c[4 * q] | (c[4 * q + 1] << 8) | (c[4 * q + 2] << 16) | (c[4 * q + 3] << 24);
-            *reinterpret_cast<uint4 *>(blk8 + (slot % 32) * KV_D + blk * 16) =
+            *reinterpret_cast<uint4 *>(blk8 + (blk * 32 + kpos8(slot % 32)) * 16) =
                 make_uint4(wds[0], wds[1], wds[2], wds[3]);
         } else {
-            uint8_t *vc = blk8 + HALF8_BYTES + (slot % 32);
+            const int sl = slot % 32;
+            uint8_t *vc = blk8 + HALF8_BYTES + (sl >> 4) * (KV_D * 16) + (sl & 15);
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-                vc[(blk * 16 + i) * 32] = (uint8_t)c[i];
+                vc[(blk * 16 + i) * 16] = (uint8_t)c[i];
         }
         return;
     }
@@ -173,8 +184,9 @@ __global__ void kv_append_kernel(KvAppendArgs a)
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             pk[i >> 2] |= e2m1x2(__fmul_rn(x[2 * i], r), __fmul_rn(x[2 * i + 1], r)) << (8 * (i & 3));
-        *reinterpret_cast<uint2 *>(pb + sl * (KV_D / 2) + blk * 8) = make_uint2(pk[0], pk[1]);
-        pb[KS4_OFF + sl * (KV_D / 16) + blk] = (uint8_t)e;
+        const int kp = kpos4(sl);
+        *reinterpret_cast<uint2 *>(pb + ((blk >> 1) * KV_H + kp) * 16 + (blk & 1) * 8) = make_uint2(pk[0], pk[1]);
+        pb[KS4_OFF + kp * (KV_D / 16) + blk] = (uint8_t)e;
     } else {
         uint8_t *vc = pb + VC4_OFF;
 #pragma unroll
@@ -354,9 +366,10 @@ __device__ __forceinline__ void kv_rescale(float (&o)[8][NT][4], const float (&c
 
 // Key order inside a 32-key chunk: QK n-tile j (8 keys) column n holds key
 // 8 (n / 2) + (n % 2) + 2 j, so that the S fragment of n-tiles 0, 1 (2, 3)
-// is exactly the P operand of the first (second) 16-key step of O = P V,
-// whose k slots 2t, 2t+1, 2t+8, 2t+9 hold keys 8t .. 8t+3 (8t+4 .. 8t+7): the
-// keys of V code byte 4t .. 4t+1 (4t+2 .. 4t+3) that ldmatrix hands lane t.
+// is exactly the P^T operand (B) of the first (second) 16-key step of
+// O^T = V^T P^T, whose k slots 2t, 2t+1, 2t+8, 2t+9 hold keys 8t .. 8t+3
+// (8t+4 .. 8t+7): the keys of V code byte 4t .. 4t+1 (4t+2 .. 4t+3) that
+// ldmatrix hands lane t.  That key sits in slot kpos4 = 8 j + n.
 __device__ __forceinline__ int chunk_key(int j, int n) { return 8 * (n >> 1) + (n & 1) + 2 * j; }
 
 // Occupancy: at most 128 registers a thread for one n-tile, so that 4 CTAs
@@ -468,13 +481,12 @@ __global__ void __launch_bounds__(32 * ATT_WARPS, NT == 1 ? 4 : 3) kv_decode_ker
             float sc[4][4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                // lane (g, t) supplies key chunk_key(j, g): 4 x 16 bytes of its row
-                // (ldmatrix matrix i = dims 32 i .. 32 i + 31)
-                const int krow = chunk_key(j, lane & 7);
+                // ldmatrix matrix i = dims 32 i .. 32 i + 31 of the n-tile's
+                // 8 keys (slots 8 j .. 8 j + 7); lane (g, t) receives key
+                // chunk_key(j, g), dims 32 i + 8 t .. + 7
                 uint32_t kr[4];
-                ldsm_x4(kc + krow * (KV_D / 2) + 16 * (lane >> 3), kr);
-                const int myrow = chunk_key(j, g);
-                const uint2 sc8 = *reinterpret_cast<const uint2 *>(ks + myrow * (KV_D / 16));
+                ldsm_x4(kc + ((lane >> 3) * KV_H + 8 * j + (lane & 7)) * 16, kr);
+                const uint2 sc8 = *reinterpret_cast<const uint2 *>(ks + (8 * j + g) * (KV_D / 16));
                 const uint32_t sb[2] = {sc8.x, sc8.y}; // block scales of this lane's key, 8 bytes
                 sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.0f;
 #pragma unroll
@@ -561,13 +573,14 @@ __global__ void __launch_bounds__(32 * ATT_WARPS, NT == 1 ? 4 : 3) kv_decode_ker
 }
 
 // FP8 cache (E4M3 codes, one static scale per tensor): the same structure
-// with 32-token half pages as the unit (keys [32][128] then values
-// [128][32], 8 KB contiguous in the FP8 page block, one bulk copy).  A 16-byte ldmatrix row holds 16
-// FP8 elements, so lane t receives elements 4t .. 4t+3 of its row: for keys,
+// with 32-token half pages as the unit (keys [8 dim chunks][32 key slots]
+// [16] then values [2 token groups][128 dims][16], 8 KB contiguous in the
+// FP8 page block, one bulk copy).  A 16-byte ldmatrix row holds 16 FP8
+// elements, so lane t receives elements 4t .. 4t+3 of its row: for keys,
 // dims 16 kk + 4t + {0,1} / {2,3} fill k slots 2t, 2t+1 / 2t+8, 2t+9 of k-step
 // kk; for values, keys 16 s + 4t + ... of step s.  QK n-tile j column n holds
-// key chunk_key8(j, n), matching those P slots.  One conversion per two
-// elements, no per-element scale.
+// key chunk_key8(j, n) (slot kpos8 = 8 j + n), matching those P slots.  One
+// conversion per two elements, no per-element scale.
 __device__ __forceinline__ int chunk_key8(int j, int n) { return 16 * (j >> 1) + 4 * (n >> 1) + (n & 1) + 2 * (j & 1); }
 
 template <int NT>
@@ -657,17 +670,18 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_fp8_kernel(const KvA
             ok = false;
             break;
         }
-        const uint8_t *kc = sm.unit[warp][s];      // [32 keys][128]
-        const uint8_t *vc = kc + HALF8_BYTES;      // [128 dims][32 keys]
+        const uint8_t *kc = sm.unit[warp][s];      // [8 dim chunks][32 key slots][16]
+        const uint8_t *vc = kc + HALF8_BYTES;      // [2 token groups][128 dims][16]
         const int valid = min(32, k_end - (k_begin + 32 * c));
         // ---- S = Q K^T over 32 keys
         float sc[4][4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int krow = chunk_key8(j, lane & 7);
+            // matrix i of the two loads: dim chunk i (4 + i) of slots 8 j .. 8 j + 7
+            const uint8_t *krow = kc + ((lane >> 3) * 32 + 8 * j + (lane & 7)) * 16;
             uint32_t kr[8];
-            ldsm_x4(kc + krow * KV_D + 16 * (lane >> 3), *reinterpret_cast<uint32_t(*)[4]>(&kr[0]));
-            ldsm_x4(kc + krow * KV_D + 64 + 16 * (lane >> 3), *reinterpret_cast<uint32_t(*)[4]>(&kr[4]));
+            ldsm_x4(krow, *reinterpret_cast<uint32_t(*)[4]>(&kr[0]));
+            ldsm_x4(krow + 4 * 32 * 16, *reinterpret_cast<uint32_t(*)[4]>(&kr[4]));
             sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.0f;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
@@ -688,7 +702,7 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_fp8_kernel(const KvA
         for (int mt = 0; mt < 8; ++mt) {
             // matrix i: dims 16 mt + 8 (i & 1) + 0..7, keys 16 (i >> 1) .. + 15
             uint32_t vr[4];
-            ldsm_x4(vc + (16 * mt + 8 * ((lane >> 3) & 1) + (lane & 7)) * 32 + 16 * (lane >> 4), vr);
+            ldsm_x4(vc + ((lane >> 4) * KV_D + 16 * mt + 8 * ((lane >> 3) & 1) + (lane & 7)) * 16, vr);
 #pragma unroll
             for (int st = 0; st < 2; ++st) {
                 // rows g (vr[2 st]) and g + 8 (vr[2 st + 1]): keys 16 st + 4t + {0,1} / {2,3}

@@ -55,17 +55,37 @@ def kv_v_pages_natural(codes_dm: np.ndarray, scales_bm: np.ndarray):
     return np.ascontiguousarray(k), np.ascontiguousarray(np.swapaxes(np.asarray(scales_bm, np.uint8), -1, -2))
 
 
+def _kv_slots(fp8: bool) -> np.ndarray:
+    """slot -> token of a 32-token half page's keys: the attention reads the
+    8 keys of one score n-tile as 8 consecutive slots.  NVFP4 swaps the bit
+    fields token[4:3] and token[2:1]; FP8 moves token bit 1 to bit 3 and
+    token bits 3:2 to bits 2:1."""
+    k = np.arange(32)
+    if fp8:
+        pos = (k & 16) | ((k & 2) << 2) | ((k >> 1) & 6) | (k & 1)
+    else:
+        pos = 8 * ((k >> 1) & 3) + 2 * (k >> 3) + (k & 1)
+    tok = np.empty(32, np.int64)
+    tok[pos] = k
+    return tok
+
+
 def kv_pack_nvfp4(k_c, k_s, v_c_nat, v_s_nat):
     """Natural per-token NVFP4 cache arrays ([..., 64, 64] codes, [..., 64, 8]
     scales, for keys and values) -> the cache's page blocks [..., 9216]: per
-    32-token half, key codes [32][64], key scales [32][8], value codes
-    dim-major [128][16], value scales block-major [8][32]."""
+    32-token half, key codes [4 dim chunks][32 key slots][16], key scales
+    [32 key slots][8], value codes dim-major [128][16], value scales
+    block-major [8][32]."""
     lead = np.asarray(k_c).shape[:-2]
+    tok = _kv_slots(False)
     parts = []
     for h in range(2):
         sl = slice(32 * h, 32 * h + 32)
+        kc = np.asarray(k_c, np.uint8)[..., sl, :][..., tok, :]                  # [..., slot, 64]
+        kc = np.swapaxes(kc.reshape(lead + (32, 4, 16)), -3, -2)                # [..., chunk, slot, 16]
+        ks = np.asarray(k_s, np.uint8)[..., sl, :][..., tok, :]
         vdm, vsbm = kv_v_pages(np.asarray(v_c_nat)[..., sl, :], np.asarray(v_s_nat)[..., sl, :])
-        parts += [np.asarray(k_c, np.uint8)[..., sl, :], np.asarray(k_s, np.uint8)[..., sl, :], vdm, vsbm]
+        parts += [kc, ks, vdm, vsbm]
     return np.ascontiguousarray(np.concatenate([x.reshape(lead + (-1,)) for x in parts], axis=-1))
 
 
@@ -73,11 +93,17 @@ def kv_unpack_nvfp4(blocks):
     """Inverse of kv_pack_nvfp4: (k_c, k_s, v_c natural, v_s natural)."""
     b = np.asarray(blocks, np.uint8)
     lead = b.shape[:-1]
+    tok = _kv_slots(False)
     out = [[], [], [], []]
     for h in range(2):
         o = 4608 * h
-        out[0].append(b[..., o:o + 2048].reshape(lead + (32, 64)))
-        out[1].append(b[..., o + 2048:o + 2304].reshape(lead + (32, 8)))
+        kc = np.swapaxes(b[..., o:o + 2048].reshape(lead + (4, 32, 16)), -3, -2).reshape(lead + (32, 64))
+        ks = b[..., o + 2048:o + 2304].reshape(lead + (32, 8))
+        kn, sn = np.empty_like(kc), np.empty_like(ks)
+        kn[..., tok, :] = kc
+        sn[..., tok, :] = ks
+        out[0].append(kn)
+        out[1].append(sn)
         v_c, v_s = kv_v_pages_natural(b[..., o + 2304:o + 4352].reshape(lead + (128, 16)),
                                       b[..., o + 4352:o + 4608].reshape(lead + (8, 32)))
         out[2].append(v_c)
@@ -87,13 +113,18 @@ def kv_unpack_nvfp4(blocks):
 
 def kv_pack_fp8(k, v_nat):
     """Natural FP8 cache arrays ([..., 64 tokens, 128]) -> page blocks
-    [..., 16384]: per 32-token half, keys [32][128] then values [128][32]."""
+    [..., 16384]: per 32-token half, keys [8 dim chunks][32 key slots][16]
+    then values [2 token groups][128 dims][16] (byte j of group u = token
+    16 u + j)."""
     k, v = np.asarray(k, np.uint8), np.asarray(v_nat, np.uint8)
     lead = k.shape[:-2]
+    tok = _kv_slots(True)
     halves = []
     for h in range(2):
-        halves.append(k[..., 32 * h:32 * h + 32, :].reshape(lead + (-1,)))
-        halves.append(np.swapaxes(v[..., 32 * h:32 * h + 32, :], -1, -2).reshape(lead + (-1,)))
+        kh = k[..., 32 * h:32 * h + 32, :][..., tok, :]                           # [..., slot, 128]
+        halves.append(np.swapaxes(kh.reshape(lead + (32, 8, 16)), -3, -2).reshape(lead + (-1,)))
+        vh = v[..., 32 * h:32 * h + 32, :].reshape(lead + (2, 16, 128))          # [..., group, token, dim]
+        halves.append(np.swapaxes(vh, -1, -2).reshape(lead + (-1,)))
     return np.ascontiguousarray(np.concatenate(halves, axis=-1))
 
 
@@ -101,11 +132,16 @@ def kv_unpack_fp8(blocks):
     """Inverse of kv_pack_fp8: (keys, values) natural [..., 64, 128]."""
     b = np.asarray(blocks, np.uint8)
     lead = b.shape[:-1]
+    tok = _kv_slots(True)
     ks, vs = [], []
     for h in range(2):
         base = 8192 * h
-        ks.append(b[..., base:base + 4096].reshape(lead + (32, 128)))
-        vs.append(np.swapaxes(b[..., base + 4096:base + 8192].reshape(lead + (128, 32)), -1, -2))
+        kh = np.swapaxes(b[..., base:base + 4096].reshape(lead + (8, 32, 16)), -3, -2).reshape(lead + (32, 128))
+        kn = np.empty_like(kh)
+        kn[..., tok, :] = kh
+        ks.append(kn)
+        vh = b[..., base + 4096:base + 8192].reshape(lead + (2, 128, 16))
+        vs.append(np.swapaxes(vh, -1, -2).reshape(lead + (32, 128)))
     return np.ascontiguousarray(np.concatenate(ks, axis=-2)), np.ascontiguousarray(np.concatenate(vs, axis=-2))
 
 

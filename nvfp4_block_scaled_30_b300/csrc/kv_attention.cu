@@ -28,9 +28,9 @@
 //
 // Decode attention, one CTA per (sequence, KV head, split of the context),
 // 4 warps; each warp streams its own half pages through a 2-stage per-warp
-// ring of 4.5 KB units, small enough for 4 CTAs (16 warps) per SM: the
-// kernel is bound by instruction latency at this occupancy, not by tensor
-// or memory throughput.  Products by mma.sync m16n8k16 (FP16 operands, FP32
+// ring (4.5 KB units for NVFP4, small enough for 4 CTAs = 16 warps per SM;
+// 8 KB units for FP8, 3 CTAs): the kernels are bound by instruction latency
+// at these occupancies, not by tensor or memory throughput.  Products by mma.sync m16n8k16 (FP16 operands, FP32
 // accumulation): S = Q K^T with the group's query heads (<= 16) as M, then
 // O^T = V^T P^T with 16 value dimensions as M and the heads as N; these
 // contractions have 8-16 rows on one side, far below the 64/128 rows of a

@@ -240,18 +240,23 @@ def workload_decode(c, M, steps, warmup, rot=4, with_e2e=False, peaks_=None):
     return res
 
 
-def workload_prefill(c, N, steps, warmup, rot=2):
+def workload_prefill(c, N, steps, warmup, rot=2, x_rot=3):
+    """Prefill GEMM (X [4096, 8192] x W [N, 8192]^T) with its activation
+    quantiser.  Weights rotate over `rot` copies and activations over
+    `x_rot` copies (3 x 67 MB), so no step finds its inputs in the 126 MB L2
+    from an earlier step."""
     t, nv = c.torch, c.nv
     M, K = 4096, 8192
     W = c.quantized_weights(synth.weights(3, 1, N, K), copies=rot)
-    x = c.bf16(synth.activations(3, 0, M, K, 0.005, 100.0))
+    x0 = synth.activations(3, 0, M, K, 0.005, 100.0)
+    xs = [c.bf16(x0) for _ in range(x_rot)]
     y = t.empty((M, N), dtype=t.bfloat16, device=c.dev)
     work = nv.Workspace(nv.workspace_size(nv.OP_GEMM, M, N, K))
-    a_q = nv.quantize(x, ws=work)
+    a_q = nv.quantize(xs[0], ws=work)
     flops = 2.0 * M * N * K
 
     def step(i):
-        nv.gemm(W[i % rot], x=x, y=y, ws=work)
+        nv.gemm(W[i % rot], x=xs[i % x_rot], y=y, ws=work)
 
     def gemm_only(i):
         nv.gemm(W[i % rot], a_q=a_q, y=y, ws=work)
@@ -261,11 +266,11 @@ def workload_prefill(c, N, steps, warmup, rot=2):
     qbytes = M * K * 2 + nvfp4_bytes(M, K)
 
     def quant_only(i):
-        nv.quantize(x, out=a_q, ws=work)
+        nv.quantize(xs[i % x_rot], out=a_q, ws=work)
 
     qms = c.time(quant_only, steps, warmup)
     st = work.status()
-    del W
+    del W, xs
     return {"ms": ms, "gemm_ms": gms, "flops": flops, "value": flops / (ms * 1e-3) / 1e12, "launches_per_step": 3,
             "gemm_tflops": flops / (gms * 1e-3) / 1e12, "quant_ms": qms, "quant_bytes": qbytes,
             "quant_gbs": qbytes / (qms * 1e-3) / 1e9, "device_status": st}
@@ -427,12 +432,14 @@ def workload_moe_ffn(c, steps, warmup):
             "tflops": flops / (ms * 1e-3) / 1e12, "device_status": work.status()}
 
 
-def workload_kv_decode(c, steps, warmup, B=16, H=64, H_kv=8, ctx=4096, fmt=0):
+def workload_kv_decode(c, steps, warmup, B=16, H=64, H_kv=8, ctx=4096, fmt=0, copies=3):
     """Decode attention over an NVFP4 paged KV cache (Llama-3-70B-class
     grouping: 64 query heads over 8 KV heads, head_dim 128), 16 sequences of
     4096 cached tokens each, plus the append of each sequence's new token:
     the step reads the whole cache once.  Cache bytes are synthetic (random
-    codes, scale bytes in a normal range); pages shuffled across the pool."""
+    codes, scale bytes in a normal range); pages shuffled across the pool.
+    Steps rotate over `copies` caches (3 x 75 MB NVFP4, 3 x 134 MB FP8), so
+    no step finds its cache in the 126 MB L2 from an earlier step."""
     t, nv = c.torch, c.nv
     P, D = nv.KV_PAGE, nv.KV_HEAD_DIM
     pages_per = ctx // P + 1
@@ -450,6 +457,7 @@ def workload_kv_decode(c, steps, warmup, B=16, H=64, H_kv=8, ctx=4096, fmt=0):
         pg.copy_(t.randint(0, 256, pg.shape, dtype=t.uint8, device=c.dev, generator=g))
         for lo, hi in ((2048, 2304), (4352, 4608), (6656, 6912), (8960, 9216)):
             pg[..., lo:hi] = t.randint(0x28, 0x48, pg[..., lo:hi].shape, dtype=t.uint8, device=c.dev, generator=g)
+    caches = [cache] + [nv.KvCache(pg.clone(), ks, vs, fmt) for _ in range(copies - 1)]
     perm = t.randperm(n_pages, device=c.dev, generator=g).to(t.int32)
     table = perm.view(B, pages_per).contiguous()
     ctx_lens = t.full((B,), ctx, dtype=t.int32, device=c.dev)
@@ -463,11 +471,12 @@ def workload_kv_decode(c, steps, warmup, B=16, H=64, H_kv=8, ctx=4096, fmt=0):
     ctx1 = t.full((B,), ctx + 1, dtype=t.int32, device=c.dev)
 
     def step(i):
-        nv.kv_append(cache, k_new, v_new, pos, table)
-        nv.kv_decode_attention(cache, q, ctx1, table, ctx + 1, sm, out=out, ws=work)
+        kv = caches[i % copies]
+        nv.kv_append(kv, k_new, v_new, pos, table)
+        nv.kv_decode_attention(kv, q, ctx1, table, ctx + 1, sm, out=out, ws=work)
 
     def attn_only(i):
-        nv.kv_decode_attention(cache, q, ctx_lens, table, ctx, sm, out=out, ws=work)
+        nv.kv_decode_attention(caches[i % copies], q, ctx_lens, table, ctx, sm, out=out, ws=work)
 
     ms = c.time(step, steps, warmup)
     ams = c.time(attn_only, steps, warmup)

@@ -355,9 +355,11 @@ constexpr int SU_BLOCKS = SU_CONSUMERS * SU_BPT;   // 512 blocks
 constexpr int SU_BYTES = SU_BLOCKS * 32;           // 16 KB
 constexpr int SU_THREADS = SU_CONSUMERS + 32;      // + the producer warp
 // pass 1 streams x from HBM: a deep ring, 3 CTAs per SM; pass 2 normally
-// finds x in L2 and is arithmetic-heavy: a short ring and 6 CTAs per SM
+// finds x in L2 and is arithmetic-heavy: a short ring, and one wave of the
+// 4 CTAs per SM its registers allow (measured: a grid of 6 per SM ran as
+// 1.5 waves and was 2 % slower; capping registers for 5 per SM, 8 % slower)
 constexpr int SU_STAGES_1 = 4, SU_CTAS_1 = 3;
-constexpr int SU_STAGES_2 = 2, SU_CTAS_2 = 6;
+constexpr int SU_STAGES_2 = 2, SU_CTAS_2 = 4;
 constexpr int su_smem(int stages) { return stages * SU_BYTES + 2 * stages * 8 + 16; }
 
 __device__ __forceinline__ void bulk_load_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar,

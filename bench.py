@@ -655,7 +655,7 @@ def main():
                 "traffic": TRAFFIC.get("prefill"), "kernel": "w4a4_kernel<256,false>",
                 "peak_source": f"{peak_src} bf16_tflops x {NOMINAL_FP4_OVER_BF16:g} (nominal FP4/BF16)"}
         cfg = {"workload": "prefill_proj: X[4096,8192], W NVFP4[28672,8192]", "global_batch": 4096,
-               "l2": "inputs larger than L2 (X 67 MB + 2 rotating W copies of 132 MB)"}
+               "l2": "inputs larger than L2 (3 rotating X copies of 67 MB + 2 rotating W copies of 132 MB)"}
     elif args.workload == "policy":
         roof = None
         cfg = {"workload": "policy_stack AUTO: 8 x [2048,4096]x[4096,4096]^T, 2 W4A8 layers", "global_batch": 2048}

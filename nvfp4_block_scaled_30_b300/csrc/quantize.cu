@@ -841,7 +841,7 @@ cudaError_t launch_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K, in
                                   status, zp);
     }
     if (mode == NVFP4_SCALE_TENSOR_FP32 && ldx == K) {
-        // contiguous x: the staged streaming passes, 3 CTAs per SM
+        // contiguous x: the staged streaming passes (3 and 4 CTAs per SM)
         const int64_t units = ceil_div(std::max<int64_t>(rows * (K / 16), 1), (int64_t)SU_BLOCKS);
         const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(units, std::min(AMAX_MAX_CTAS, sms * SU_CTAS_1)));
         const uint64_t tmo = 2000000000ull;

@@ -390,8 +390,9 @@ nvfp4_status nvfp4_kv_append(const nvfp4_kv_cache *kv, const void *k_bf16, const
  * keys and values decoded (E2M1 x E4M3 x tensor scale, or E4M3 x tensor
  * scale in the FP8 format), BF16 or FP32
  * [B][num_heads][128]; an empty context gives zeros.  num_heads is a multiple
- * of num_kv_heads with at most 16 query heads per KV head.  Long contexts
- * are split across CTAs and merged in a second kernel.
+ * of num_kv_heads with at most 16 query heads per KV head, and B and
+ * num_kv_heads are at most 65535 (else NVFP4_ERR_UNSUPPORTED_SHAPE).  Long
+ * contexts are split across CTAs and merged in a second kernel.
  * Workspace: nvfp4_workspace_size(NVFP4_OP_KV_DECODE, B, num_heads, max_ctx,
  * num_kv_heads). */
 nvfp4_status nvfp4_kv_decode_attention(const nvfp4_kv_cache *kv, const void *q_bf16, int32_t num_heads,

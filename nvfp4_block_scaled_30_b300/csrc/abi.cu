@@ -781,8 +781,8 @@ nvfp4_status nvfp4_kv_decode_attention(const nvfp4_kv_cache *kv, const void *q_b
     const int H_kv = kv->num_kv_heads;
     if (B < 0 || max_pages <= 0 || max_ctx < 0 || num_heads <= 0 || num_heads % H_kv != 0)
         return NVFP4_ERR_INVALID_ARG;
-    if (num_heads / H_kv > 16)
-        return NVFP4_ERR_UNSUPPORTED_SHAPE; // up to 16 query heads per KV head
+    if (num_heads / H_kv > 16 || B > 65535 || H_kv > 65535)
+        return NVFP4_ERR_UNSUPPORTED_SHAPE; // up to 16 query heads per KV head; grid y = KV heads, z = sequences
     if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32)
         return NVFP4_ERR_INVALID_ARG;
     if (!(sm_scale == sm_scale) || sm_scale < 0.0f || sm_scale > 1e30f)

@@ -120,3 +120,33 @@ def test_argument_errors_fail_before_any_launch(nv):
     # fp8 quantiser shape check
     assert L.nvfp4_quantize_fp8(0x1000, 4, 40, 40, 0x2000, 0x3000, ws, big, None) == nv.ERR_UNSUPPORTED_SHAPE
     assert L.nvfp4_workspace_size(9, 1, 1, 1, 0, ctypes.byref(ctypes.c_size_t())) == nv.ERR_INVALID_ARG
+
+
+def test_kv_argument_errors_fail_before_any_launch(nv):
+    L = nv.lib()
+    ws, big = ctypes.c_void_p(0x40000), 1 << 30
+
+    def cache(**kw):
+        d = dict(pages=0x100000, k_scale=0x2000, v_scale=0x2004, num_pages=64, num_kv_heads=8, head_dim=128,
+                 page_tokens=64, format=nv.KV_NVFP4)
+        d.update(kw)
+        return nv.KvCacheDesc(d["pages"], d["k_scale"], d["v_scale"], d["num_pages"], d["num_kv_heads"],
+                              d["head_dim"], d["page_tokens"], d["format"])
+
+    def attn(c, H=64, B=4, max_ctx=4096, out_dtype=0, sm_scale=0.088):
+        return L.nvfp4_kv_decode_attention(ctypes.byref(c), 0x3000, H, 0x4000, 0x5000, 65, B, max_ctx, sm_scale,
+                                           0x6000, out_dtype, ws, big, None)
+
+    assert attn(cache(format=7)) == nv.ERR_INVALID_ARG
+    assert attn(cache(head_dim=64)) == nv.ERR_UNSUPPORTED_SHAPE
+    assert attn(cache(pages=0x100008)) == nv.ERR_INVALID_ARG            # pages not 16-byte aligned
+    assert attn(cache(), H=60) == nv.ERR_INVALID_ARG                     # not a multiple of the KV heads
+    assert attn(cache(), H=8 * 17) == nv.ERR_UNSUPPORTED_SHAPE          # 17 query heads per KV head
+    assert attn(cache(), B=65536) == nv.ERR_UNSUPPORTED_SHAPE           # beyond the grid's z limit
+    assert attn(cache(num_kv_heads=65536), H=65536) == nv.ERR_UNSUPPORTED_SHAPE
+    assert attn(cache(), out_dtype=5) == nv.ERR_INVALID_ARG
+    assert attn(cache(), sm_scale=float("nan")) == nv.ERR_INVALID_ARG
+    assert L.nvfp4_kv_decode_attention(ctypes.byref(cache()), 0x3000, 64, 0x4000, 0x5000, 65, 4, 4096, 0.088,
+                                       0x6000, 0, ctypes.c_void_p(0x40000), 16, None) == nv.ERR_WORKSPACE
+    assert L.nvfp4_kv_append(ctypes.byref(cache()), 0x3000, 0x3100, 0x4000, 0x5000, 0, 4, None) == nv.ERR_INVALID_ARG
+    assert L.nvfp4_kv_append(None, 0x3000, 0x3100, 0x4000, 0x5000, 65, 4, None) == nv.ERR_INVALID_ARG

@@ -36,6 +36,13 @@ EXPORTED = ["nvfp4_scale_bytes", "nvfp4_workspace_size", "nvfp4_workspace_init",
             "nvfp4_diag_streamk_skip_flag", "nvfp4_kv_append", "nvfp4_kv_decode_attention"]
 
 
+def _require(ok: bool, what: str) -> None:
+    """Argument check of the bindings (kept under python -O, unlike assert):
+    a wrong dtype or layout must not reach the C ABI as a raw pointer."""
+    if not ok:
+        raise ValueError(what)
+
+
 class NVFP4Error(RuntimeError):
     def __init__(self, status: int, where: str):
         super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
@@ -199,7 +206,8 @@ def policy_route(policy: int, sensitive: int) -> int:
 def quantize(x: torch.Tensor, mode: int = SCALE_TENSOR_FP32, layout: int = LAYOUT_MMA_TILED,
              out: Optional[NVFP4Tensor] = None, ws: Optional[Workspace] = None, stream=None) -> NVFP4Tensor:
     """nvfp4_quantize of a BF16 [rows, K] tensor (row stride x.stride(0))."""
-    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    _require(x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1,
+             "quantize: x must be a 2-D BF16 tensor with unit column stride")
     rows, K = x.shape
     if out is None:
         out = empty_nvfp4(rows, K, mode, layout, x.device)
@@ -212,7 +220,8 @@ def quantize(x: torch.Tensor, mode: int = SCALE_TENSOR_FP32, layout: int = LAYOU
 
 def quantize_fp8(x: torch.Tensor, ws: Optional[Workspace] = None, stream=None):
     """nvfp4_quantize_fp8: returns (E4M3 bytes uint8 [rows, K], s_t float32 [rows])."""
-    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    _require(x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1,
+             "quantize_fp8: x must be a 2-D BF16 tensor with unit column stride")
     rows, K = x.shape
     a = torch.empty((rows, K), dtype=torch.uint8, device=x.device)
     st = torch.empty(rows, dtype=torch.float32, device=x.device)
@@ -226,7 +235,7 @@ def _out(y, M, N, out_dtype, device):
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32,
                         device=device)
-    assert y.stride(1) == 1
+    _require(y.stride(1) == 1, "output y must have unit column stride")
     return y
 
 
@@ -260,8 +269,10 @@ def gemm_nvfp4_out(w: NVFP4Tensor, s_y: torch.Tensor, x: Optional[torch.Tensor] 
     N, K = w.rows, w.K
     M = x.shape[0] if x is not None else a_q.rows
     device = w.codes.device
-    assert s_y.dtype == torch.float32 and s_y.numel() == 1 and s_y.device == device
-    assert y_amax is None or (y_amax.dtype == torch.float32 and y_amax.device == device)
+    _require(s_y.dtype == torch.float32 and s_y.numel() == 1 and s_y.device == device,
+             "gemm_nvfp4_out: s_y must be one FP32 value on the GEMM's device")
+    _require(y_amax is None or (y_amax.dtype == torch.float32 and y_amax.device == device),
+             "gemm_nvfp4_out: y_amax must be FP32 on the GEMM's device")
     if out is None:
         out = empty_nvfp4(M, N, SCALE_TENSOR_FP32, LAYOUT_MMA_TILED, device)
     out.second = s_y
@@ -295,7 +306,8 @@ def grouped_gemm(a: NVFP4Tensor, offsets: torch.Tensor, w: NVFP4Tensor, N: int, 
                  policy: int = POLICY_AUTO, sensitive: int = 0, y: Optional[torch.Tensor] = None,
                  ws: Optional[Workspace] = None, stream=None) -> torch.Tensor:
     """nvfp4_grouped_gemm over E = offsets.numel() - 1 experts stacked in w."""
-    assert offsets.dtype == torch.int64 and (row_idx is None or row_idx.dtype == torch.int32)
+    _require(offsets.dtype == torch.int64 and (row_idx is None or row_idx.dtype == torch.int32),
+             "grouped_gemm: offsets must be int64 and row_idx int32")
     E = offsets.numel() - 1
     y = _out(y, total_rows, N, out_dtype, a.codes.device)
     if total_rows == 0:
@@ -321,7 +333,7 @@ def gemm_w4a4_noalloc(a_q: NVFP4Tensor, w: NVFP4Tensor, y: torch.Tensor, out_dty
 
 def probe_convert(v: torch.Tensor, stream=None):
     """The kernels' own E2M1 / E4M3 conversions applied to float32 values."""
-    assert v.dtype == torch.float32 and v.is_contiguous()
+    _require(v.dtype == torch.float32 and v.is_contiguous(), "probe_convert: v must be a contiguous FP32 tensor")
     o2 = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
     o3 = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
     _check(lib().nvfp4_probe_convert(_ptr(v), v.numel(), _ptr(o2), _ptr(o3), _stream(stream)),
@@ -339,7 +351,8 @@ def grouped_w4a8_gemm(a_fp8: torch.Tensor, s_t: torch.Tensor, offsets: torch.Ten
                       stream=None) -> torch.Tensor:
     """nvfp4_grouped_w4a8_gemm: grouped W4A8 of FP8 activations [T, K] with
     per-token scales s_t [T]."""
-    assert offsets.dtype == torch.int64 and (row_idx is None or row_idx.dtype == torch.int32)
+    _require(offsets.dtype == torch.int64 and (row_idx is None or row_idx.dtype == torch.int32),
+             "grouped_w4a8_gemm: offsets must be int64 and row_idx int32")
     E = offsets.numel() - 1
     y = _out(y, total_rows, N, out_dtype, a_fp8.device)
     if total_rows == 0:
@@ -358,8 +371,10 @@ def grouped_gemm_x(x: torch.Tensor, offsets: torch.Tensor, w: NVFP4Tensor, N: in
                    stream=None) -> torch.Tensor:
     """nvfp4_grouped_gemm_x: grouped GEMM of BF16 activations under the
     precision policy (W4A4 or W4A8 route)."""
-    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
-    assert offsets.dtype == torch.int64 and (row_idx is None or row_idx.dtype == torch.int32)
+    _require(x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1,
+             "grouped_gemm_x: x must be a 2-D BF16 tensor with unit column stride")
+    _require(offsets.dtype == torch.int64 and (row_idx is None or row_idx.dtype == torch.int32),
+             "grouped_gemm_x: offsets must be int64 and row_idx int32")
     E = offsets.numel() - 1
     y = _out(y, total_rows, N, out_dtype, x.device)
     if total_rows == 0:
@@ -381,7 +396,8 @@ def moe_up_swiglu(a: NVFP4Tensor, offsets: torch.Tensor, w_gate_up: NVFP4Tensor,
     """nvfp4_moe_up_swiglu: SiLU(gate) * up of the routed rows.  With s_h
     (float32 [1] device tensor scale) the output is NVFP4 (returned as an
     NVFP4Tensor); otherwise a BF16/FP32 [total_rows, I] tensor."""
-    assert offsets.dtype == torch.int64 and (row_idx is None or row_idx.dtype == torch.int32)
+    _require(offsets.dtype == torch.int64 and (row_idx is None or row_idx.dtype == torch.int32),
+             "moe_up_swiglu: offsets must be int64 and row_idx int32")
     E = offsets.numel() - 1
     dev = a.codes.device
     hd = None
@@ -411,8 +427,9 @@ def moe_down_combine(h: NVFP4Tensor, offsets: torch.Tensor, w_down: NVFP4Tensor,
                      ws: Optional[Workspace] = None, stream=None) -> torch.Tensor:
     """nvfp4_moe_down_combine: y[token_idx[j]] += gate_w[j] * (h[j] W_e^T) into
     the FP32 [T, N] tensor y (which holds zeros or the residual)."""
-    assert offsets.dtype == torch.int64 and token_idx.dtype == torch.int32 and gate_w.dtype == torch.float32
-    assert y.dtype == torch.float32 and y.stride(1) == 1
+    _require(offsets.dtype == torch.int64 and token_idx.dtype == torch.int32 and gate_w.dtype == torch.float32,
+             "moe_down_combine: offsets must be int64, token_idx int32 and gate_w FP32")
+    _require(y.dtype == torch.float32 and y.stride(1) == 1, "moe_down_combine: y must be FP32 with unit column stride")
     E = offsets.numel() - 1
     R = h.rows
     ws = _ws(ws, workspace_size(OP_GROUPED_GEMM, R, N, h.K, E), h.codes.device)
@@ -460,7 +477,8 @@ class KvCache:
         return KvCache(pages, k_scale, v_scale, fmt)
 
     def desc(self) -> KvCacheDesc:
-        assert self.pages.is_contiguous() and self.pages.shape[2] == KV_PAGE_BYTES[self.fmt]
+        _require(self.pages.is_contiguous() and self.pages.shape[2] == KV_PAGE_BYTES[self.fmt],
+                 "desc: pages must be contiguous page blocks of the cache format's size")
         return KvCacheDesc(self.pages.data_ptr(), self.k_scale.data_ptr(), self.v_scale.data_ptr(),
                            self.num_pages, self.num_kv_heads, KV_HEAD_DIM, KV_PAGE, self.fmt)
 
@@ -468,8 +486,10 @@ class KvCache:
 def kv_append(cache: KvCache, k_new: torch.Tensor, v_new: torch.Tensor, positions: torch.Tensor,
               block_table: torch.Tensor, stream=None):
     """nvfp4_kv_append: one new token per sequence (BF16 [B][H_kv][128])."""
-    assert k_new.dtype == torch.bfloat16 and v_new.dtype == torch.bfloat16 and k_new.is_contiguous()
-    assert positions.dtype == torch.int32 and block_table.dtype == torch.int32 and block_table.is_contiguous()
+    _require(k_new.dtype == torch.bfloat16 and v_new.dtype == torch.bfloat16 and k_new.is_contiguous(),
+             "kv_append: k_new and v_new must be BF16, k_new contiguous")
+    _require(positions.dtype == torch.int32 and block_table.dtype == torch.int32 and block_table.is_contiguous(),
+             "kv_append: positions and block_table must be int32, block_table contiguous")
     B = k_new.shape[0]
     d = cache.desc()
     _check(lib().nvfp4_kv_append(ctypes.byref(d), _ptr(k_new), _ptr(v_new.contiguous()), _ptr(positions),
@@ -481,8 +501,10 @@ def kv_decode_attention(cache: KvCache, q: torch.Tensor, ctx_lens: torch.Tensor,
                         out: Optional[torch.Tensor] = None, ws: Optional[Workspace] = None,
                         stream=None) -> torch.Tensor:
     """nvfp4_kv_decode_attention: q BF16 [B][H][128] -> out [B][H][128]."""
-    assert q.dtype == torch.bfloat16 and q.is_contiguous() and q.shape[2] == KV_HEAD_DIM
-    assert ctx_lens.dtype == torch.int32 and block_table.dtype == torch.int32 and block_table.is_contiguous()
+    _require(q.dtype == torch.bfloat16 and q.is_contiguous() and q.shape[2] == KV_HEAD_DIM,
+             "kv_decode_attention: q must be contiguous BF16 [B][H][128]")
+    _require(ctx_lens.dtype == torch.int32 and block_table.dtype == torch.int32 and block_table.is_contiguous(),
+             "kv_decode_attention: ctx_lens and block_table must be int32, block_table contiguous")
     B, H, D = q.shape
     if out is None:
         out = torch.empty((B, H, D), dtype=torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32,

@@ -213,7 +213,10 @@ nvfp4_status nvfp4_gemm_nvfp4_out(const void *x_bf16, int64_t ldx, const nvfp4_t
                                   const nvfp4_tensor *w, nvfp4_tensor *y_q, float *y_amax, int64_t M,
                                   void *ws, size_t ws_bytes, nvfp4_stream_t stream);
 
-/* W4A8 contraction from pre-quantised FP8 activations:
+/* W4A8 contraction from pre-quantised FP8 activations, the route [LCP]
+ * ("One model can need more than one precision") gives tensors marked as
+ * sensitive, and the FP8 activations [TRT] ("Deployment Guidelines and
+ * Production Safeguards", item 2) keeps for sensitive layers:
  * Y[m, n] = s_t[m] * s_w * sum_k E4M3(a[m, k]) * E2M1(w[n, k]) * E4M3(ew[n, k/16]).
  * a_fp8 uint8 [M][K] dense, s_t float[M]; w TENSOR_FP32, MMA_TILED. */
 nvfp4_status nvfp4_w4a8_gemm(const void *a_fp8, const float *s_t, const nvfp4_tensor *w,
@@ -258,7 +261,9 @@ nvfp4_status nvfp4_grouped_w4a8_gemm(const void *a_fp8, const float *s_t, int64_
                                      size_t ws_bytes, nvfp4_stream_t stream);
 
 /* Grouped GEMM of BF16 activations x [T, K] (row stride ldx) under the
- * precision policy: the route (nvfp4_policy_route(policy, sensitive))
+ * precision policy ([LCP]: MoE operations on both routes; q4 / q8 / auto in
+ * "Local inference is becoming a policy engine"): the route
+ * (nvfp4_policy_route(policy, sensitive))
  * quantises x once into the workspace (NVFP4 per-tensor for W4A4, FP8
  * per-token for W4A8) and runs nvfp4_grouped_gemm's or
  * nvfp4_grouped_w4a8_gemm's contraction with the same conventions.

@@ -187,6 +187,35 @@ def nvfp4_bytes(rows, K):
     return rows * K // 2 + rows * K // 16
 
 
+def _e4m3_table():
+    """Value of every E4M3 byte (sign bit 7, exponent bits 6-3 with bias 7,
+    mantissa bits 2-0; exponent 0 is subnormal m * 2^-9; S.1111.111 is NaN)."""
+    v = np.empty(256)
+    for b in range(256):
+        e, m = (b >> 3) & 15, b & 7
+        mag = m * 2.0 ** -9 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7)
+        v[b] = np.nan if (b & 0x7F) == 0x7F else (-mag if b & 0x80 else mag)
+    return v
+
+
+E4M3_VALUES = _e4m3_table()
+
+
+def scale_stats(q):
+    """Scale statistics of an NVFP4 tensor (tensor-scale mode) for the bench
+    log: its FP32 tensor scale and the smallest and largest non-zero E4M3
+    block scale (zero bytes, including the tiled layout's padding rows, are
+    left out), plus the share of zero blocks among the tensor's real blocks."""
+    sb = q.scales.cpu().numpy().ravel()
+    nz = sb[sb != 0]
+    vals = E4M3_VALUES[nz]
+    blocks = q.rows * (q.K // 16)
+    return {"tensor_scale": float(q.second.cpu().reshape(-1)[0]),
+            "block_scale_min": float(vals.min()) if nz.size else 0.0,
+            "block_scale_max": float(vals.max()) if nz.size else 0.0,
+            "zero_block_frac": float(1.0 - nz.size / max(blocks, 1))}
+
+
 def workload_decode(c, M, steps, warmup, rot=4, with_e2e=False, peaks_=None):
     t, nv = c.torch, c.nv
     N, K = 28672, 8192
@@ -213,11 +242,13 @@ def workload_decode(c, M, steps, warmup, rot=4, with_e2e=False, peaks_=None):
     ms = c.time(step, steps, warmup)
     gms = c.time(gemm_only, steps, warmup)
     st = work.status()
+    stats = {"x": scale_stats(a_q), "w": scale_stats(W[0])}   # after the timed loops
     # the quantiser is one launch (one thread-block cluster) up to 32768
     # chunks of 8 values, two staged passes above that; then the GEMM
     launches = (1 if M * K // 8 <= 32768 else 2) + 1
     res = {"ms": ms, "gemm_ms": gms, "step_bytes": step_bytes, "gemm_bytes": gemm_bytes,
-           "value": step_bytes / (ms * 1e-3) / 1e9, "launches_per_step": launches, "device_status": st}
+           "value": step_bytes / (ms * 1e-3) / 1e9, "launches_per_step": launches, "device_status": st,
+           "scale_stats": stats}
     if with_e2e:
         hx = t.from_numpy(xb.view(np.int16)).pin_memory()
         hy = t.empty((M, N), dtype=t.int16).pin_memory()
@@ -296,7 +327,9 @@ def workload_policy(c, steps, warmup, policy):
     ms = c.time(step, steps, warmup)
     flops = 2.0 * M * N * K * L
     routes = [nv.policy_route(policy, int(f)) for f in flags]
+    layer_stats = [scale_stats(w) for w in Ws]   # after the timed loop
     return {"ms": ms, "flops": flops, "value": flops / (ms * 1e-3) / 1e12, "routes": routes,
+            "w_scale_stats": layer_stats,
             "launches_per_step": sum(3 if r == 4 else 2 for r in routes), "device_status": work.status()}
 
 
@@ -622,6 +655,8 @@ def main():
             q = workload_policy(c, min(es, 20), 2, pol)
             extras[f"policy_stack_{name}"] = {"value": q["value"], "unit": "TFLOP/s", "ms": q["ms"],
                                               "routes": q["routes"]}
+            if name == "auto":   # the stack's weights are the same for every policy
+                extras["policy_stack_auto"]["layer_w_scale_stats"] = q["w_scale_stats"]
         fq = workload_fused_stack(c, min(es, 20), 2)
         extras["policy_stack_q4_fused"] = {"value": fq["value"], "unit": "TFLOP/s", "ms": fq["ms"]}
         kd = workload_kv_decode(c, min(es, 50), 3)
@@ -681,6 +716,8 @@ def main():
             line["cpu_baseline"] = cpu
         if "e2e" in r:
             line["e2e"] = r["e2e"]
+        if "scale_stats" in r:
+            line["scale_stats"] = r["scale_stats"]
         if extras:
             line["workloads"] = extras
         print(json.dumps(line))

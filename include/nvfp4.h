@@ -461,6 +461,15 @@ nvfp4_status nvfp4_diag_streamk_skip_flag(const nvfp4_tensor *a_q, const nvfp4_t
 /* Number of streaming multiprocessors of the current device (0 on error). */
 int32_t nvfp4_sm_count(void);
 
+/* How the W4A4 route of nvfp4_gemm (tensor-scale mode) spreads the work for
+ * M activation rows, N weight rows and depth K: NVFP4_PATH_WHOLE_TILES (each
+ * persistent CTA takes whole 128-row output tiles) or NVFP4_PATH_STREAMK
+ * (M <= 128 with too few N tiles to fill the SMs: the K stages are spread over
+ * the SMs and partial tiles meet in the workspace).  -1 for sizes nvfp4_gemm
+ * rejects.  Host-side query; launches nothing. */
+enum { NVFP4_PATH_WHOLE_TILES = 1, NVFP4_PATH_STREAMK = 2 };
+int32_t nvfp4_gemm_kernel_path(int64_t M, int64_t N, int64_t K);
+
 /* Library version string. */
 const char *nvfp4_version(void);
 

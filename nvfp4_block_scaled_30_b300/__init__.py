@@ -33,7 +33,8 @@ EXPORTED = ["nvfp4_scale_bytes", "nvfp4_workspace_size", "nvfp4_workspace_init",
             "nvfp4_grouped_gemm", "nvfp4_probe_convert", "nvfp4_sm_count", "nvfp4_version",
             "nvfp4_gemm_w4a4_noalloc", "nvfp4_gemm_nvfp4_out", "nvfp4_moe_up_swiglu",
             "nvfp4_moe_down_combine", "nvfp4_grouped_w4a8_gemm", "nvfp4_grouped_gemm_x",
-            "nvfp4_diag_streamk_skip_flag", "nvfp4_kv_append", "nvfp4_kv_decode_attention"]
+            "nvfp4_diag_streamk_skip_flag", "nvfp4_kv_append", "nvfp4_kv_decode_attention",
+            "nvfp4_gemm_kernel_path"]
 
 
 def _require(ok: bool, what: str) -> None:
@@ -103,6 +104,7 @@ def lib():
             "nvfp4_moe_down_combine": (_I32, [_PT, _VP, _I32, _PT, _I64, _VP, _VP, _VP, _I64, _I64, _I64,
                                               _VP, _SZ, _VP]),
             "nvfp4_sm_count": (_I32, []),
+            "nvfp4_gemm_kernel_path": (_I32, [_I64, _I64, _I64]),
             "nvfp4_version": (ctypes.c_char_p, []),
         }
         for name, (res, args) in sig.items():
@@ -198,6 +200,14 @@ def empty_nvfp4(rows: int, K: int, mode: int = SCALE_TENSOR_FP32, layout: int = 
 
 
 # ---- the hot path ----------------------------------------------------------------------
+
+PATH_WHOLE_TILES, PATH_STREAMK = 1, 2
+
+
+def gemm_kernel_path(M: int, N: int, K: int) -> int:
+    """nvfp4_gemm_kernel_path: whole tiles or stream-K for the W4A4 shape."""
+    return lib().nvfp4_gemm_kernel_path(M, N, K)
+
 
 def policy_route(policy: int, sensitive: int) -> int:
     return lib().nvfp4_policy_route(policy, int(bool(sensitive)))

@@ -226,6 +226,14 @@ int32_t nvfp4_sm_count(void)
     return n;
 }
 
+int32_t nvfp4_gemm_kernel_path(int64_t M, int64_t N, int64_t K)
+{
+    if (M <= 0 || N <= 0 || K <= 0 || M > MAX_DIM || N > MAX_DIM || K > MAX_DIM || K % 64 != 0)
+        return -1;
+    const WsLayout L = ws_layout(NVFP4_OP_GEMM, M, N, K);
+    return L.sk_slots != 0 ? NVFP4_PATH_STREAMK : NVFP4_PATH_WHOLE_TILES;
+}
+
 int32_t nvfp4_policy_route(int32_t policy, int32_t sensitive)
 {
     switch (policy) {

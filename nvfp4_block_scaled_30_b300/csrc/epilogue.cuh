@@ -1,0 +1,117 @@
+// Output stores shared by the W4A4 GEMM epilogues: 32 consecutive
+// accumulator columns of one row as BF16/FP32 (alpha-scaled), and the NVFP4
+// encode of such a run (the fused next-layer quantiser).
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace nv4 {
+
+// Where element (i, j) of the output goes: out[i * ld_i + j * ld_j]; vec_ok
+// when ld_j == 1 and 16-byte vector stores of a row are aligned.
+struct OutDesc {
+    void *out;
+    int64_t ld_i, ld_j;
+    int32_t out_dtype, vec_ok;
+};
+
+// Row i, columns j0 .. j0 + 31 (bits of the FP32 accumulator in v) times
+// alpha; rows >= i_end and columns >= j_end are not stored.
+__device__ __forceinline__ void store_chunk32(const OutDesc &o, const uint32_t (&v)[32], int64_t i, int64_t j0,
+                                              float alpha, int64_t i_end, int64_t j_end)
+{
+    if (i >= i_end)
+        return;
+    if (o.ld_j == 1 && o.vec_ok && j0 + 32 <= j_end) {
+        if (o.out_dtype == NVFP4_OUT_BF16) {
+            uint4 *d = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(o.out) + i * o.ld_i + j0);
+#pragma unroll
+            for (int c = 0; c < 32; c += 8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    __nv_bfloat162 h = __floats2bfloat162_rn(alpha * __uint_as_float(v[c + 2 * q]),
+                                                             alpha * __uint_as_float(v[c + 2 * q + 1]));
+                    w[q] = *reinterpret_cast<uint32_t *>(&h);
+                }
+                d[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        } else {
+            float4 *d = reinterpret_cast<float4 *>(static_cast<float *>(o.out) + i * o.ld_i + j0);
+#pragma unroll
+            for (int c = 0; c < 32; c += 4)
+                d[c / 4] = make_float4(alpha * __uint_as_float(v[c]), alpha * __uint_as_float(v[c + 1]),
+                                       alpha * __uint_as_float(v[c + 2]), alpha * __uint_as_float(v[c + 3]));
+        }
+        return;
+    }
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+        const int64_t j = j0 + c;
+        if (j < j_end) {
+            const float y = alpha * __uint_as_float(v[c]);
+            const int64_t off = i * o.ld_i + j * o.ld_j;
+            if (o.out_dtype == NVFP4_OUT_BF16)
+                static_cast<__nv_bfloat16 *>(o.out)[off] = __float2bfloat16_rn(y);
+            else
+                static_cast<float *>(o.out)[off] = y;
+        }
+    }
+}
+
+// NVFP4 store of 32 consecutive outputs y (binary32 bits in v) of one row
+// starting at column j0 (two 16-element blocks): the block encode of the
+// quantisers under the given tensor scale s, 8 code bytes at crow + j0/2 and
+// one scale byte per block in the row's MMA-tiled scale slots srow (see
+// q_row_addr).  Returns the largest |y|.
+__device__ __forceinline__ float encode_store_q(const uint32_t (&v)[32], uint8_t *crow, uint8_t *srow, int j0,
+                                                float s)
+{
+    float m = 0.0f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        float amb = 0.0f;
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+            amb = fmaxf(amb, fabsf(__uint_as_float(v[16 * h + t])));
+        const uint32_t e = block_scale_code(amb, s);
+        const float r = recip_step(__fmul_rn(e4m3_value(e), s));
+        uint32_t pk[2] = {0u, 0u};
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+            pk[t >> 2] |= e2m1x2(__fmul_rn(__uint_as_float(v[16 * h + 2 * t]), r),
+                                 __fmul_rn(__uint_as_float(v[16 * h + 2 * t + 1]), r))
+                          << (8 * (t & 3));
+        const int j = j0 + 16 * h;
+        *reinterpret_cast<uint2 *>(crow + j / 2) = make_uint2(pk[0], pk[1]);
+        const int blk = j / 16;
+        srow[(blk >> 2) * 512 + (blk & 3)] = (uint8_t)e;
+        m = fmaxf(m, amb);
+    }
+    return m;
+}
+
+// Row i of an NVFP4 output of n columns (codes [rows][n/2], MMA-tiled
+// scales): its code row and the base of its scale slots (byte (i % 32) * 16
+// + ((i % 128) / 32) * 4 + b % 4 of atom (i / 128) * (n / 64) + b / 4 holds
+// block b).
+__device__ __forceinline__ void q_row_addr(int64_t i, int64_t n, uint8_t *codes, uint8_t *scales, uint8_t *&crow,
+                                           uint8_t *&srow)
+{
+    const int64_t r7 = i & 127;
+    crow = codes + i * (n / 2);
+    srow = scales + (i >> 7) * (n / 64) * 512 + (r7 & 31) * 16 + (r7 >> 5) * 4;
+}
+
+// Zero scale bytes of 32 columns from j in a padding row's scale slots (rows
+// of the last 128-row tile past the real rows, as the quantisers leave them).
+__device__ __forceinline__ void zero_pad_scales32(uint8_t *srow, int j)
+{
+    srow[(j >> 6) * 512 + ((j >> 4) & 3)] = 0;
+    srow[(j >> 6) * 512 + ((j >> 4) & 3) + 1] = 0;
+}
+
+} // namespace nv4

@@ -46,6 +46,7 @@
 #include <algorithm>
 #include <cuda_bf16.h>
 
+#include "epilogue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -325,89 +326,15 @@ __device__ __forceinline__ bool wait_flag(const uint32_t *f, uint64_t timeout_ns
     return true;
 }
 
-template <int BN>
-__device__ __forceinline__ void store_chunk(const Params &p, const uint32_t (&v)[32], int64_t i, int64_t j0,
-                                            float alpha, int64_t i_end, int64_t j_end)
+__device__ __forceinline__ OutDesc out_desc(const Params &p)
 {
-    if (i >= i_end)
-        return;
-    if (p.ld_j == 1 && p.vec_ok && j0 + 32 <= j_end) {
-        if (p.out_dtype == NVFP4_OUT_BF16) {
-            uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + i * p.ld_i + j0);
-#pragma unroll
-            for (int c = 0; c < 32; c += 8) {
-                uint32_t w[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    __nv_bfloat162 h = __floats2bfloat162_rn(alpha * __uint_as_float(v[c + 2 * q]),
-                                                             alpha * __uint_as_float(v[c + 2 * q + 1]));
-                    w[q] = *reinterpret_cast<uint32_t *>(&h);
-                }
-                o[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-        } else {
-            float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + i * p.ld_i + j0);
-#pragma unroll
-            for (int c = 0; c < 32; c += 4)
-                o[c / 4] = make_float4(alpha * __uint_as_float(v[c]), alpha * __uint_as_float(v[c + 1]),
-                                       alpha * __uint_as_float(v[c + 2]), alpha * __uint_as_float(v[c + 3]));
-        }
-        return;
-    }
-#pragma unroll
-    for (int c = 0; c < 32; ++c) {
-        const int64_t j = j0 + c;
-        if (j < j_end) {
-            const float y = alpha * __uint_as_float(v[c]);
-            const int64_t off = i * p.ld_i + j * p.ld_j;
-            if (p.out_dtype == NVFP4_OUT_BF16)
-                static_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(y);
-            else
-                static_cast<float *>(p.out)[off] = y;
-        }
-    }
+    return OutDesc{p.out, p.ld_i, p.ld_j, p.out_dtype, p.vec_ok};
 }
 
-// NVFP4 store of 32 consecutive outputs y (binary32 bits in v) of one row
-// starting at column j0 (two 16-element blocks): the block encode of the
-// quantisers under the given tensor scale s, 8 code bytes at crow + j0/2 and
-// one scale byte per block in the row's MMA-tiled scale slots srow (see
-// q_row).  Returns the largest |y|.
-__device__ __forceinline__ float encode_store_q(const uint32_t (&v)[32], uint8_t *crow, uint8_t *srow, int j0,
-                                                float s)
-{
-    float m = 0.0f;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        float amb = 0.0f;
-#pragma unroll
-        for (int t = 0; t < 16; ++t)
-            amb = fmaxf(amb, fabsf(__uint_as_float(v[16 * h + t])));
-        const uint32_t e = block_scale_code(amb, s);
-        const float r = recip_step(__fmul_rn(e4m3_value(e), s));
-        uint32_t pk[2] = {0u, 0u};
-#pragma unroll
-        for (int t = 0; t < 8; ++t)
-            pk[t >> 2] |= e2m1x2(__fmul_rn(__uint_as_float(v[16 * h + 2 * t]), r),
-                                 __fmul_rn(__uint_as_float(v[16 * h + 2 * t + 1]), r))
-                          << (8 * (t & 3));
-        const int j = j0 + 16 * h;
-        *reinterpret_cast<uint2 *>(crow + j / 2) = make_uint2(pk[0], pk[1]);
-        const int blk = j / 16;
-        srow[(blk >> 2) * 512 + (blk & 3)] = (uint8_t)e;
-        m = fmaxf(m, amb);
-    }
-    return m;
-}
-
-// Row i of an NVFP4 output of n columns: its code row and the base of its
-// scale slots in the MMA-tiled layout (byte (i % 32) * 16 + ((i % 128) / 32)
-// * 4 + b % 4 of atom (i / 128) * (n / 64) + b / 4 holds block b).
+// Row i of the NVFP4 output: its code row and the base of its scale slots.
 __device__ __forceinline__ void q_row(const Params &p, int64_t i, uint8_t *&crow, uint8_t *&srow)
 {
-    const int64_t n = p.yq_n, r7 = i & 127;
-    crow = p.yq_codes + i * (n / 2);
-    srow = p.yq_scales + (i >> 7) * (n / 64) * 512 + (r7 & 31) * 16 + (r7 >> 5) * 4;
+    q_row_addr(i, p.yq_n, p.yq_codes, p.yq_scales, crow, srow);
 }
 
 template <int BN, bool GROUPED, int AR>
@@ -875,7 +802,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                                 q_row(p, i, crow, srow);
                                 m = fmaxf(m, encode_store_q(v[c], crow, srow, (int)j, s));
                             } else
-                                store_chunk<BN>(p, v[c], i, j, 1.0f, i_end, p.yq_n);
+                                store_chunk32(out_desc(p), v[c], i, j, 1.0f, i_end, p.yq_n);
                         }
                     }
                 } else {
@@ -929,10 +856,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                     // quantisers leave them
                     for (int c = 0; c < NCH; ++c) {
                         const int j = (int)(j_base + c * 32);
-                        if (j < j_end) {
-                            srow[(j >> 6) * 512 + ((j >> 4) & 3)] = 0;
-                            srow[(j >> 6) * 512 + ((j >> 4) & 3) + 1] = 0;
-                        }
+                        if (j < j_end)
+                            zero_pad_scales32(srow, j);
                     }
                 }
 #pragma unroll
@@ -1080,7 +1005,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
             }
 #pragma unroll
             for (int c = 0; c < NCH; ++c)
-                store_chunk<BN>(p, v[c], i, j_base + c * 32, alpha, i_end, j_end);
+                store_chunk32(out_desc(p), v[c], i, j_base + c * 32, alpha, i_end, j_end);
         }
     }
 

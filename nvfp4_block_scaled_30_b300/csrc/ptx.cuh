@@ -419,3 +419,4 @@ __device__ __forceinline__ float recip_step(float d)
 }
 
 } // namespace nv4
+

@@ -1,11 +1,13 @@
 """W4A4 block-scaled GEMM on the tensor cores against the oracle.
 
 Exact cases (FP32 output; every partial sum is exactly representable):
-all 16x16 E2M1 code pairs, every non-negative E4M3 scale, one-hot rows.
+all 16x16 E2M1 code pairs, every non-negative E4M3 scale, one-hot rows, on
+one 128-row tile and across several M tiles, partial tiles and K stages.
 Tolerance cases: max_n |Y - Y_ref| <= 1e-3 * ||Y_ref[m, :]||_2 per row
 against the FP64 oracle, on configuration 1 in full, the decode shapes
 (M = 1, 8, 16 against the 28672 x 8192 weights) in full, the prefill shapes
-on sampled rows, and ragged shapes that exercise M/N/K tails and split-K."""
+on 256 seeded rows plus the first and last, and ragged shapes that exercise
+M/N/K tails, stream-K and many-tile shapes."""
 import numpy as np
 import pytest
 import torch
@@ -52,20 +54,62 @@ def test_all_code_pairs_exact(M):
     np.testing.assert_array_equal(Y, ref)
 
 
-def test_every_e4m3_scale_exact():
+@pytest.mark.parametrize("M,N", [(384, 16), (256, 300), (513, 272)])
+def test_all_code_pairs_exact_many_tiles(M, N):
+    # several 128-row tiles, K = 256 (one stage): A row i has code (i + k) % 16
+    # at every k, W row j code (j + 3k) % 16, unit scales; each output is a
+    # sum of 256 products of E2M1 values, exact in FP32.  The shapes leave
+    # partial tiles in M and N.
+    K = 256
+    assert nv.gemm_kernel_path(M, N, K) == nv.PATH_WHOLE_TILES
+    k = np.arange(K)
+    ca = ((np.arange(M)[:, None] + k[None, :]) % 16).astype(np.uint8)
+    cw = ((np.arange(N)[:, None] + 3 * k[None, :]) % 16).astype(np.uint8)
+    sa = np.full((M, K // 16), ONE, np.uint8)
+    sw = np.full((N, K // 16), ONE, np.uint8)
+    a = nvfp4_device(pack(ca), sa, 1.0, M, K)
+    w = nvfp4_device(pack(cw), sw, 1.0, N, K)
+    Y = gemm_q(a, w)
+    ref = oracle.gemm_w4a4((pack(ca), sa, 1.0), (pack(cw), sw, 1.0))
+    np.testing.assert_array_equal(Y, ref)
+
+
+@pytest.mark.parametrize("M,K", [(128, 64), (256, 256), (300, 1024)])
+def test_every_e4m3_scale_exact(M, K):
     # only block 1 (k = 16..31) of the weights is non-zero, so every output is
-    # one scaled block sum: E4M3(m % 127) * E4M3(n) * sum_k a*w, exact in FP32
+    # one scaled block sum: E4M3(m % 127) * E4M3(n) * sum_k a*w, exact in FP32.
+    # M = 128 is one tile, the others several (the block sits in the first
+    # stage; K = 1024 adds stages of zeros).
     rng = np.random.default_rng(21)
-    K = 64
-    ca = rng.integers(0, 16, size=(128, K)).astype(np.uint8)
+    ca = rng.integers(0, 16, size=(M, K)).astype(np.uint8)
     cw = np.zeros((127, K), np.uint8)
     cw[:, 16:32] = rng.integers(0, 16, size=(127, 16))
-    sa = np.full((128, 4), ONE, np.uint8)
-    sw = np.full((127, 4), ONE, np.uint8)
+    sa = np.full((M, K // 16), ONE, np.uint8)
+    sw = np.full((127, K // 16), ONE, np.uint8)
     sw[:, 1] = np.arange(127)
-    sa[:, 1] = (np.arange(128) % 127).astype(np.uint8)
-    a = nvfp4_device(pack(ca), sa, 1.0, 128, K)
+    sa[:, 1] = (np.arange(M) % 127).astype(np.uint8)
+    a = nvfp4_device(pack(ca), sa, 1.0, M, K)
     w = nvfp4_device(pack(cw), sw, 1.0, 127, K)
+    Y = gemm_q(a, w)
+    ref = oracle.gemm_w4a4((pack(ca), sa, 1.0), (pack(cw), sw, 1.0))
+    np.testing.assert_array_equal(Y, ref)
+
+
+def test_every_e4m3_scale_exact_b_groups():
+    # B scales across tiles: 512 weight rows (two 256-row tiles, four 128-row
+    # scale groups) each carrying a different E4M3 scale in block 5 of the
+    # second stage (k = 336..351), and every activation scale there
+    rng = np.random.default_rng(23)
+    M, N, K = 256, 512, 512
+    ca = rng.integers(0, 16, size=(M, K)).astype(np.uint8)
+    cw = np.zeros((N, K), np.uint8)
+    cw[:, 336:352] = rng.integers(0, 16, size=(N, 16))
+    sa = np.full((M, K // 16), ONE, np.uint8)
+    sw = np.full((N, K // 16), ONE, np.uint8)
+    sw[:, 21] = (np.arange(N) % 127).astype(np.uint8)
+    sa[:, 21] = ((np.arange(M) * 7) % 127).astype(np.uint8)
+    a = nvfp4_device(pack(ca), sa, 1.0, M, K)
+    w = nvfp4_device(pack(cw), sw, 1.0, N, K)
     Y = gemm_q(a, w)
     ref = oracle.gemm_w4a4((pack(ca), sa, 1.0), (pack(cw), sw, 1.0))
     np.testing.assert_array_equal(Y, ref)
@@ -132,15 +176,18 @@ def test_decode_full(w_28672, M):
 
 @pytest.mark.parametrize("N", [8192, 28672])
 def test_prefill_sampled_rows(w_28672, N):
+    # configuration 3 in the launch configuration the bench times (whole
+    # tiles, BF16 output); 256 seeded rows plus the first and last
     if N == 28672:
         w, wq = w_28672
     else:
         wb = synth.weights(3, 1, 8192, 8192)
         w, wc, ws, wg = quantize_pinned(wb)
         wq = (wc, ws, wg[0])
+    assert nv.gemm_kernel_path(4096, N, 8192) == nv.PATH_WHOLE_TILES
     xb = synth.activations(3, 0, 4096, 8192, 0.005, 100.0)
     y = y_np(nv.gemm(w, x=dev_bf16(xb)))
-    rows = np.concatenate([[0, 4095], np.random.default_rng(N).choice(np.arange(1, 4095), 14, replace=False)])
+    rows = np.concatenate([[0, 4095], np.random.default_rng(N).choice(np.arange(1, 4095), 256, replace=False)])
     ref = oracle.gemm_w4a4(oracle.nvfp4_encode(xb), wq, rows=rows)
     _check(y[rows], ref, f"prefill N={N}")
 
@@ -153,6 +200,24 @@ def test_ragged_shapes(M, N, K, out_dtype):
     wb = synth.weights(9, 11, N, K)
     w, wc, ws, wg = quantize_pinned(wb)
     y = nv.gemm(w, x=dev_bf16(xb), out_dtype=out_dtype)
+    ref = oracle.gemm_w4a4(oracle.nvfp4_encode(xb), (wc, ws, wg[0]))
+    _check(y_np(y), ref, f"{M}x{N}x{K}", out_dtype == nv.OUT_BF16)
+
+
+# Many-tile shapes: a last M tile of 1 or 44 rows (257, 300), partial N tiles
+# and scale groups (N = 130, 384, 1000), one and many stages, more tiles
+# than SMs (1024 x 4864: 8 x 19 tiles)
+@pytest.mark.parametrize("M,N,K", [(257, 256, 256), (300, 130, 512), (384, 384, 768), (1000, 1000, 1024),
+                                   (640, 2560, 2304), (1024, 4864, 1024)])
+@pytest.mark.parametrize("out_dtype", [nv.OUT_BF16, nv.OUT_FP32])
+def test_many_tile_shapes(M, N, K, out_dtype):
+    assert nv.gemm_kernel_path(M, N, K) == nv.PATH_WHOLE_TILES
+    xb = synth.activations(9, 12, M, K, 0.01, 50.0)
+    wb = synth.weights(9, 13, N, K)
+    w, wc, ws, wg = quantize_pinned(wb)
+    work = nv.Workspace(nv.workspace_size(nv.OP_GEMM, M, N, K))
+    y = nv.gemm(w, x=dev_bf16(xb), out_dtype=out_dtype, ws=work)
+    assert work.status() == nv.OK
     ref = oracle.gemm_w4a4(oracle.nvfp4_encode(xb), (wc, ws, wg[0]))
     _check(y_np(y), ref, f"{M}x{N}x{K}", out_dtype == nv.OUT_BF16)
 

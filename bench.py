@@ -543,6 +543,111 @@ def oracle_decode_step(setup, reps=1):
     return nbytes / dt / 1e9, dt, nbytes
 
 
+def _median_time(fn, reps):
+    ts = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        fn()
+        ts.append(time.perf_counter() - t0)
+    return float(np.median(ts))
+
+
+def cpu_baseline_plan():
+    """The oracle timed on this host, per configuration: the encoder on each
+    configuration's full tensors (all cores, and one thread on the
+    activations), and the FP64 dequantise-and-contract step in full for
+    configurations 1 and 2 (M = 1, 8, 16), on 256 seeded rows plus the first
+    and last for configuration 3 (N = 8192), on 256 seeded rows of one layer
+    for configuration 4 and on the first 16 experts of configuration 5's up
+    projection (the last two labelled as samples, with the full-problem time
+    extrapolated).  Medians of repeats; about 20-30 s in all.  Returns
+    (headline dict: the configuration-2 M = 8 decode step, per-config dict)."""
+    import oracle
+    cores = os.cpu_count() or 1
+    oracle.set_threads(cores)
+    out = {}
+
+    def enc_entry(bits, reps=3, single=False):
+        n = bits.size
+        nbytes = n * 2 + n // 2 + n // 16
+        t = _median_time(lambda: oracle.nvfp4_encode(bits), reps)
+        e = {"elements": int(n), "s": t, "melem_per_s": n / t / 1e6, "gbs": nbytes / t / 1e9, "threads": cores}
+        if single:
+            oracle.set_threads(1)
+            t1 = _median_time(lambda: oracle.nvfp4_encode(bits), 1)
+            oracle.set_threads(cores)
+            e.update({"s_1thread": t1, "melem_per_s_1thread": n / t1 / 1e6})
+        return e
+
+    def gemm_entry(aq, wq, M, N, K, rows=None, reps=1, scale_to=None):
+        nr = M if rows is None else len(rows)
+        t = _median_time(lambda: oracle.gemm_w4a4(aq, wq, rows=rows), reps)
+        flop = 2.0 * nr * N * K
+        e = {"rows": int(nr), "s": t, "gflops_f64": flop / t / 1e9}
+        if scale_to is not None:
+            e["full_problem_s_extrapolated"] = t * scale_to
+        return e
+
+    # configuration 1
+    x1, w1 = synth.activations(1, 0, 128, 512, 0.01, 50.0), synth.weights(1, 1, 256, 512)
+    a1, q1 = oracle.nvfp4_encode(x1), oracle.nvfp4_encode(w1)
+    out["c1"] = {"encode_x": enc_entry(x1, single=True), "encode_w": enc_entry(w1),
+                 "gemm": gemm_entry(a1, q1, 128, 256, 512, reps=3)}
+    # configuration 2 (decode): full W, M = 1, 8, 16
+    K = 8192
+    w2 = synth.weights(2, 1, 28672, K)
+    c2 = {"encode_w": enc_entry(w2, reps=1)}
+    q2 = oracle.nvfp4_encode(w2)
+    del w2
+    head = None
+    for M in (1, 8, 16):
+        xb = synth.activations(2, 0, M, K, 0.005, 100.0)
+        c2[f"encode_x_m{M}"] = enc_entry(xb, single=True)
+        aq = oracle.nvfp4_encode(xb)
+        g = gemm_entry(aq, q2, M, 28672, K, reps=3 if M == 8 else 1)
+        nbytes = nvfp4_bytes(28672, K) + M * K * 2 + 2 * nvfp4_bytes(M, K) + M * 28672 * 2
+        g["step_gbs"] = nbytes / (g["s"] + c2[f"encode_x_m{M}"]["s"]) / 1e9
+        c2[f"gemm_m{M}"] = g
+        if M == 8:
+            head = {"value": g["step_gbs"], "unit": "GB/s", "cores": cores, "kind": "oracle",
+                    "sample": "configuration 2 decode step in full (encode X [8,8192], FP64 contraction with "
+                              "all 28672 weight rows), median of 3"}
+    out["c2"] = c2
+    del q2
+    # configuration 3 (prefill): encoder on X, contraction on 258 rows against N = 8192
+    x3 = synth.activations(3, 0, 4096, K, 0.005, 100.0)
+    w3 = synth.weights(3, 1, 8192, K)
+    rows = np.concatenate([[0, 4095], np.random.default_rng(8192).choice(np.arange(1, 4095), 256, replace=False)])
+    a3, q3 = oracle.nvfp4_encode(x3), oracle.nvfp4_encode(w3)
+    out["c3"] = {"encode_x": enc_entry(x3, reps=1, single=True), "encode_w": enc_entry(w3, reps=1),
+                 "gemm_n8192_sampled": gemm_entry(a3, q3, 4096, 8192, K, rows=rows, scale_to=4096 / len(rows))}
+    del x3, w3, a3, q3
+    # configuration 4: one layer, 256 seeded rows
+    x4, w4 = synth.activations(4, 0, 2048, 4096, 0.01, 50.0), synth.weights(4, 1, 4096, 4096)
+    a4, q4 = oracle.nvfp4_encode(x4), oracle.nvfp4_encode(w4)
+    r4 = np.random.default_rng(4).choice(2048, 256, replace=False)
+    out["c4"] = {"encode_x": enc_entry(x4, single=True), "encode_w": enc_entry(w4),
+                 "gemm_layer_sampled": gemm_entry(a4, q4, 2048, 4096, 4096, rows=r4, scale_to=2048 / 256)}
+    del x4, w4, a4, q4
+    # configuration 5: up projection, experts 0..15 of the default routing
+    idx, offs, _, _ = synth.moe_routing()
+    c5 = synth.CONFIGS[5]
+    xm = synth.activations(5, 0, 2048, 2048, c5["outlier_frac"], c5["outlier_factor"])
+    wup = synth.weights(5, 1, 16 * 768, 2048)
+    out["c5_encode_w_up_16_experts"] = enc_entry(wup, reps=1)
+    am = oracle.nvfp4_encode(xm)
+    qc, qs, qg = oracle.nvfp4_encode(wup)
+    E16 = 16
+    sub_off = offs[:E16 + 1] - offs[0]
+    sub_idx = idx[offs[0]:offs[E16]]
+    t = _median_time(lambda: oracle.gemm_grouped_w4a4(am, sub_idx, sub_off, qc.reshape(E16, 768, 1024),
+                                                      qs.reshape(E16, 768, 128), np.full(E16, qg, np.float32)), 1)
+    routed = int(sub_off[-1])
+    out["c5_up_16_experts"] = {"routed_rows": routed, "s": t, "gflops_f64": 2.0 * routed * 768 * 2048 / t / 1e9,
+                               "full_problem_s_extrapolated": t * float(offs[-1] - offs[0]) / max(routed, 1)}
+    return head, out
+
+
 def cpu_cores():
     try:
         import oracle
@@ -567,7 +672,7 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     hbm, bf16, bf16_sus, peak_src = peaks()
-    fp4_peak = bf16 * NOMINAL_FP4_OVER_BF16
+    fp4_nominal = bf16 * NOMINAL_FP4_OVER_BF16
     metric = "NVFP4 W4A4 GEMM TFLOPS & % dense FP4 peak (prefill); GB/s & % HBM (decode)"
 
     if args.impl == "reference":
@@ -594,6 +699,12 @@ def main():
         print(json.dumps(line))
         return 0
 
+    # the oracle's baseline runs first, before any GPU work, on rank 0 alone
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu, per_config = cpu_baseline_plan()
+        cpu["per_config"] = per_config
+
     import torch
     import nvfp4_block_scaled_30_b300 as nv
     nv.lib()
@@ -609,6 +720,21 @@ def main():
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.4)
+    # dense FP4 tensor-core rate of this GPU (the prefill roofline's peak):
+    # the MMA issue-rate kernel, one CTA per SM, operands resident on chip
+    fp4_iters = 400000      # ~0.1 s per launch, long enough for the clock samples
+    nv.fp4_mma_rate(200)
+    t_fp4 = time.time()
+    runs = [nv.fp4_mma_rate(fp4_iters) for _ in range(3)]
+    fp4_clocks = sampler.summary(t_fp4, time.time())
+    fp4_flop_clk_sm, fp4_ms, n_sm = max(runs, key=lambda r: r[0] / r[1] if r[1] > 0 else 0)
+    fp4_ms = min(r[1] for r in runs)
+    fp4_peak = fp4_iters * 4 * nv.FP4_MMA_FLOP * n_sm / (fp4_ms * 1e-3) / 1e12
+    fp4_info = {"tflops_measured": fp4_peak, "flop_per_clock_per_sm": fp4_flop_clk_sm, "sms": n_sm,
+                "sm_mhz_median": fp4_clocks.get("sm_mhz"),
+                "tflops_at_max_clock": fp4_flop_clk_sm * n_sm * 2032e6 / 1e12,
+                "tflops_nominal_ratio_of_bf16": fp4_nominal,
+                "how": f"{fp4_iters} x 4 tcgen05.mma kind::mxf4nvf4 M=128 N=256 K=64 per SM, CUDA events"}
 
     def barrier():
         if dist is not None:
@@ -650,6 +776,7 @@ def main():
                 extras[f"prefill_n{N}"] = {"value": p["value"], "unit": "TFLOP/s", "ms": p["ms"],
                                            "gemm_tflops": p["gemm_tflops"],
                                            "gemm_frac_fp4": p["gemm_tflops"] / fp4_peak,
+                                           "gemm_frac_fp4_nominal": p["gemm_tflops"] / fp4_nominal,
                                            "quant_gbs": p["quant_gbs"], "quant_frac_hbm": p["quant_gbs"] / hbm}
         for pol, name in ((nv.POLICY_AUTO, "auto"), (nv.POLICY_Q4, "q4"), (nv.POLICY_Q8, "q8")):
             q = workload_policy(c, min(es, 20), 2, pol)
@@ -676,12 +803,6 @@ def main():
         extras["moe_grouped"] = {"value": mo["value"], "unit": "GB/s", "ms": mo["ms"], "tflops": mo["tflops"],
                                  "frac_hbm": mo["value"] / hbm, "counts": [mo["counts_min"], mo["counts_max"]]}
 
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, dt, nb = oracle_decode_step(oracle_decode_setup(), reps=20)
-        cpu = {"value": v, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
-               "sample": "20 decode steps (encode X, FP64 contraction) on 2048 of 28672 weight rows"}
-
     if args.workload == "decode":
         ach = r["gemm_bytes"] / (r["gemm_ms"] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
@@ -693,7 +814,8 @@ def main():
         ach = r["gemm_tflops"]
         roof = {"bound": "tensor", "achieved": ach, "peak": fp4_peak, "unit": "TFLOP/s", "frac": ach / fp4_peak,
                 "traffic": TRAFFIC.get("prefill"), "kernel": "w4a4_kernel<256,false>",
-                "peak_source": f"{peak_src} bf16_tflops x {NOMINAL_FP4_OVER_BF16:g} (nominal FP4/BF16)"}
+                "peak_source": "measured in this run: tcgen05 mxf4nvf4 issue-rate kernel (fp4_peak)",
+                "frac_of_nominal": ach / fp4_nominal}
         cfg = {"workload": "prefill_proj: X[4096,8192], W NVFP4[28672,8192]", "global_batch": 4096,
                "l2": "inputs larger than L2 (3 rotating X copies of 67 MB + 2 rotating W copies of 132 MB)"}
     elif args.workload == "policy":
@@ -720,6 +842,7 @@ def main():
             line["scale_stats"] = r["scale_stats"]
         if extras:
             line["workloads"] = extras
+        line["fp4_peak"] = fp4_info
         print(json.dumps(line))
     sampler.stop()
     if dist is not None:

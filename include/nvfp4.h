@@ -428,12 +428,22 @@ nvfp4_status nvfp4_kv_decode_attention(const nvfp4_kv_cache *kv, const void *q_b
  *  - Every call shares the one array and zeroes the part it uses on `stream`
  *    before the kernel runs; calls that overlap on the GPU (other streams,
  *    other threads) race on it and must be serialised by the caller.
- *  - Device-side status (a bounded wait that ran out) is kept in that array
- *    and not reported; use nvfp4_gemm with a workspace to read it.
+ *  - Device-side status (a bounded wait that ran out, leaving part of y
+ *    unspecified) is kept in that array: read it with
+ *    nvfp4_gemm_w4a4_noalloc_status before the next call clears it.
  *  y: [M, N] with row stride ldy, y_dtype BF16 or FP32, 16-byte aligned.
- *  Other errors as nvfp4_gemm. */
+ *  The tensors are checked as nvfp4_gemm checks them (same error codes);
+ *  NVFP4_SCALE_MACRO_FP16 tensors give NVFP4_ERR_UNSUPPORTED. */
 nvfp4_status nvfp4_gemm_w4a4_noalloc(const nvfp4_tensor *a_q, const nvfp4_tensor *w, void *y, int64_t ldy,
                                      int32_t y_dtype, nvfp4_stream_t stream);
+
+/* Device status of the most recent nvfp4_gemm_w4a4_noalloc call(s) on the
+ * current device: waits for `stream`'s earlier work, then writes NVFP4_OK,
+ * NVFP4_ERR_TIMEOUT (a bounded wait ran out; part of y is unspecified) or
+ * NVFP4_ERR_NONFINITE_INPUT to *device_status (host memory) and clears the
+ * word.  Allocates nothing.  Like the calls themselves, it shares the
+ * library's scratch array: calls on other streams race with it. */
+nvfp4_status nvfp4_gemm_w4a4_noalloc_status(nvfp4_stream_t stream, int32_t *device_status);
 
 /* ---- diagnostics ----------------------------------------------------------- */
 
@@ -443,6 +453,20 @@ nvfp4_status nvfp4_gemm_w4a4_noalloc(const nvfp4_tensor *a_q, const nvfp4_tensor
  * Used to check the device conversions exhaustively against the oracle. */
 nvfp4_status nvfp4_probe_convert(const float *in, int64_t n, uint8_t *out_e2m1, uint8_t *out_e4m3,
                                  nvfp4_stream_t stream);
+
+/* Dense FP4 tensor-core rate of this GPU, the denominator of the W4A4 GEMM
+ * roofline ("NVIDIA Ships TensorRT-LLM 0.16: Native FP4 Quantization for
+ * Blackwell B200", section "The Mathematical Breakthrough of Microscopic FP4
+ * Scaling", item 3: the tensor cores take FP4 codes and their micro-scales).
+ * Launches one CTA per SM; each issues `iters` x 4 back-to-back block-scaled
+ * MMAs (kind::mxf4nvf4, M = 128, N = 256, K = 64: 4194304 FLOP each) on
+ * operands held in shared memory and TMEM, so nothing but the tensor core
+ * limits it, and writes its cycle count (clock64) to cycles[cta] (device
+ * memory, nvfp4_sm_count() entries, 8-byte aligned; ~0 if its bounded wait
+ * ran out).  FLOP per cycle and SM = iters * 4 * 4194304 / cycles; time the
+ * launch with events on `stream` for FLOP/s at the clock it ran at.
+ * iters in 1 .. 2^24.  Asynchronous; the caller owns `cycles`. */
+nvfp4_status nvfp4_diag_fp4_mma_rate(int32_t iters, uint64_t *cycles, nvfp4_stream_t stream);
 
 /* Test-only failure injection for the device-side failure detection: runs the
  * W4A4 GEMM of pre-quantised a_q (TENSOR_FP32, MMA_TILED) and w on a shape

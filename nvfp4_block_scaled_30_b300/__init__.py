@@ -34,7 +34,7 @@ EXPORTED = ["nvfp4_scale_bytes", "nvfp4_workspace_size", "nvfp4_workspace_init",
             "nvfp4_gemm_w4a4_noalloc", "nvfp4_gemm_nvfp4_out", "nvfp4_moe_up_swiglu",
             "nvfp4_moe_down_combine", "nvfp4_grouped_w4a8_gemm", "nvfp4_grouped_gemm_x",
             "nvfp4_diag_streamk_skip_flag", "nvfp4_kv_append", "nvfp4_kv_decode_attention",
-            "nvfp4_gemm_kernel_path"]
+            "nvfp4_gemm_kernel_path", "nvfp4_diag_fp4_mma_rate", "nvfp4_gemm_w4a4_noalloc_status"]
 
 
 def _require(ok: bool, what: str) -> None:
@@ -91,6 +91,7 @@ def lib():
             "nvfp4_diag_streamk_skip_flag": (_I32, [_PT, _PT, _VP, _I64, _I32, _I32, ctypes.c_uint64, _VP, _SZ,
                                                     _VP]),
             "nvfp4_gemm_w4a4_noalloc": (_I32, [_PT, _PT, _VP, _I64, _I32, _VP]),
+            "nvfp4_gemm_w4a4_noalloc_status": (_I32, [_VP, ctypes.POINTER(_I32)]),
             "nvfp4_gemm_nvfp4_out": (_I32, [_VP, _I64, _PT, _PT, _PT, _VP, _I64, _VP, _SZ, _VP]),
             "nvfp4_grouped_w4a8_gemm": (_I32, [_VP, _VP, _I64, _VP, _VP, _I32, _PT, _I64, _VP, _I64, _I32, _I64,
                                                _VP, _SZ, _VP]),
@@ -105,6 +106,7 @@ def lib():
                                               _VP, _SZ, _VP]),
             "nvfp4_sm_count": (_I32, []),
             "nvfp4_gemm_kernel_path": (_I32, [_I64, _I64, _I64]),
+            "nvfp4_diag_fp4_mma_rate": (_I32, [_I32, _VP, _VP]),
             "nvfp4_version": (ctypes.c_char_p, []),
         }
         for name, (res, args) in sig.items():
@@ -209,6 +211,33 @@ def gemm_kernel_path(M: int, N: int, K: int) -> int:
     return lib().nvfp4_gemm_kernel_path(M, N, K)
 
 
+def sm_count() -> int:
+    """nvfp4_sm_count: streaming multiprocessors of the current device."""
+    return lib().nvfp4_sm_count()
+
+
+FP4_MMA_FLOP = 2 * 128 * 256 * 64  # one kind::mxf4nvf4 M=128 N=256 K=64 instruction
+
+
+def fp4_mma_rate(iters: int = 20000, stream=None):
+    """nvfp4_diag_fp4_mma_rate: returns (FLOP per cycle and SM, elapsed ms of the
+    launch, SM count).  The rate is the slowest CTA's; ms is CUDA-event time
+    on the launching stream."""
+    n = sm_count()
+    cyc = torch.zeros(n, dtype=torch.int64, device="cuda")
+    s = stream if stream is not None else torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    _check(lib().nvfp4_diag_fp4_mma_rate(iters, cyc.data_ptr(), s.cuda_stream), "nvfp4_diag_fp4_mma_rate")
+    e1.record(s)
+    e1.synchronize()
+    c = cyc.cpu()
+    worst = int(c.max()) if int(c.min()) >= 0 else -1  # ~0 (a wait that ran out) reads as -1
+    if worst <= 0:
+        raise NVFP4Error(ERR_TIMEOUT, "nvfp4_diag_fp4_mma_rate: a CTA's wait ran out")
+    return iters * 4 * FP4_MMA_FLOP / worst, e0.elapsed_time(e1), n
+
+
 def policy_route(policy: int, sensitive: int) -> int:
     return lib().nvfp4_policy_route(policy, int(bool(sensitive)))
 
@@ -242,9 +271,17 @@ def quantize_fp8(x: torch.Tensor, ws: Optional[Workspace] = None, stream=None):
 
 
 def _out(y, M, N, out_dtype, device):
+    """The output tensor of a [M, N] product: allocated when y is None, else
+    checked before any pointer reaches the C ABI (a wrong dtype or shape would
+    make the kernel write past the buffer): a 2-D CUDA tensor of out_dtype,
+    at least [M, N], unit column stride."""
+    _require(out_dtype in (OUT_BF16, OUT_FP32), "out_dtype must be OUT_BF16 or OUT_FP32")
+    dt = torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32
     if y is None:
-        y = torch.empty((M, N), dtype=torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32,
-                        device=device)
+        return torch.empty((M, N), dtype=dt, device=device)
+    _require(y.is_cuda and y.dim() == 2, "output y must be a 2-D CUDA tensor")
+    _require(y.dtype == dt, f"output y must be {dt} for out_dtype {out_dtype}")
+    _require(y.shape[0] >= M and y.shape[1] >= N, f"output y {tuple(y.shape)} is smaller than [{M}, {N}]")
     _require(y.stride(1) == 1, "output y must have unit column stride")
     return y
 
@@ -335,10 +372,20 @@ def gemm_w4a4_noalloc(a_q: NVFP4Tensor, w: NVFP4Tensor, y: torch.Tensor, out_dty
     """nvfp4_gemm_w4a4_noalloc: the W4A4 product for callers that cannot
     allocate; takes no workspace (its scratch is a fixed array inside the
     library, shared by all calls).  y must be provided by the caller."""
+    _require(y is not None, "gemm_w4a4_noalloc: y must be provided by the caller")
+    y = _out(y, a_q.rows, w.rows, out_dtype, None)
     ad, wd = a_q.desc(), w.desc()
     _check(lib().nvfp4_gemm_w4a4_noalloc(ctypes.byref(ad), ctypes.byref(wd), _ptr(y), y.stride(0), out_dtype,
                                          _stream(stream)), "nvfp4_gemm_w4a4_noalloc")
     return y
+
+
+def noalloc_status(stream=None) -> int:
+    """nvfp4_gemm_w4a4_noalloc_status: OK, ERR_TIMEOUT or ERR_NONFINITE_INPUT
+    for the most recent no-allocation calls (waits for the stream; clears)."""
+    out = _I32(0)
+    _check(lib().nvfp4_gemm_w4a4_noalloc_status(_stream(stream), ctypes.byref(out)), "nvfp4_gemm_w4a4_noalloc_status")
+    return out.value
 
 
 def probe_convert(v: torch.Tensor, stream=None):

@@ -131,7 +131,7 @@ static nvfp4_status check_ws(void *ws, size_t ws_bytes, size_t need)
     return NVFP4_OK;
 }
 
-static nvfp4_status check_tensor(const nvfp4_tensor *t, bool need_tiled)
+nvfp4_status check_tensor(const nvfp4_tensor *t, bool need_tiled)
 {
     if (!t || !t->second || (t->rows > 0 && (!t->codes || !t->scales)))
         return NVFP4_ERR_INVALID_ARG;
@@ -928,6 +928,13 @@ nvfp4_status nvfp4_diag_streamk_skip_flag(const nvfp4_tensor *a_q, const nvfp4_t
     return run_w4a4_dense(static_cast<const uint8_t *>(a_q->codes), static_cast<const uint8_t *>(a_q->scales),
                           static_cast<const float *>(a_q->second), M, w, y, ldy, y_dtype, ws, L, false,
                           (cudaStream_t)stream, nullptr, nullptr, skip_cta, timeout_ns);
+}
+
+nvfp4_status nvfp4_diag_fp4_mma_rate(int32_t iters, uint64_t *cycles, nvfp4_stream_t stream)
+{
+    if (iters < 1 || iters > (1 << 24) || !cycles || !aligned(cycles, 8))
+        return NVFP4_ERR_INVALID_ARG;
+    return from_cuda(launch_fp4_mma_rate(iters, cycles, (cudaStream_t)stream));
 }
 
 nvfp4_status nvfp4_probe_convert(const float *in, int64_t n, uint8_t *out_e2m1, uint8_t *out_e4m3,

@@ -22,6 +22,12 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 int device_sm_count();
 
+// Argument checks of an nvfp4_tensor shared by the entry points (null or
+// misaligned pointers, enums, sizes: NVFP4_ERR_INVALID_ARG; K not a multiple
+// of 16, of 64 for the MMA-tiled layout or of 256 in macro mode:
+// NVFP4_ERR_UNSUPPORTED_SHAPE); need_tiled requires the MMA-tiled layout.
+nvfp4_status check_tensor(const nvfp4_tensor *t, bool need_tiled);
+
 // Launch with programmatic stream serialisation: the grid may start while
 // the previous grid in the stream is still running.  Every kernel launched
 // this way executes griddepcontrol.wait before it touches memory that the
@@ -52,6 +58,7 @@ cudaError_t launch_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K, in
                                   uint32_t *status, cudaStream_t stream, bool zero_pad = true);
 cudaError_t launch_fp8_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx, uint8_t *a, float *s_t,
                                 uint32_t *status, cudaStream_t stream);
+cudaError_t launch_fp4_mma_rate(int iters, uint64_t *cycles, cudaStream_t stream);
 cudaError_t launch_probe_convert(const float *in, int64_t n, uint8_t *o2, uint8_t *o3, cudaStream_t stream);
 cudaError_t launch_finalize_bf16(const float *acc, int64_t rows, int64_t cols, int64_t ld_acc, uint16_t *y,
                                  int64_t ldy, cudaStream_t stream);

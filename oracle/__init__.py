@@ -5,7 +5,7 @@ bench.py's CPU-baseline / reference legs may import this package.  It shares
 no code with the CUDA path (nvfp4_block_scaled_30_b300), and neither imports
 the other.  Every function follows a passage of the pages named in
 nvfp4_oracle.c; the readings taken where the pages are silent are listed
-there and in DESIGN.md.
+there.
 
 Layouts: activations/weights are BF16 bit patterns (uint16) [rows, K];
 codes are uint8 [rows, K/2] with the even element in the low nibble; scales
@@ -454,6 +454,21 @@ def decode_attention(q, k_cache, v_cache, s_k, s_v, block_table, ctx_lens, sm_sc
     return o
 
 
+_THREADS = None
+
+
 def threads():
     """OpenMP threads the oracle's parallel loops use."""
+    if _THREADS is not None:
+        return _THREADS
     return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
+def set_threads(n):
+    """Threads of the oracle's parallel loops from now on (timing only)."""
+    global _THREADS
+    L = lib()
+    L.orc_set_threads.restype = None
+    L.orc_set_threads.argtypes = [ctypes.c_int]
+    L.orc_set_threads(int(n))
+    _THREADS = int(n)

@@ -18,7 +18,7 @@
  *        Than W4A4", section "One model can need more than one precision"
  *        (W4A8 route for marked tensors, dense and mixture-of-experts).
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *  - E2M1 magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6}; the FP8 micro-scale is E4M3;
  *    the default second level is one FP32 tensor scale amax / (6 * 448).
  *  - Rounding is to the nearest representable value, ties to the even code,
@@ -44,6 +44,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define ORC_OK 0
 #define ORC_ERR_ARG 1
@@ -560,4 +563,16 @@ void orc_gemm_grouped_w4a4(const uint8_t *a_codes, const uint8_t *a_scales, floa
         free(arow);
         free(wdec);
     }
+}
+
+/* OpenMP threads of the parallel loops (timing only: results do not depend
+ * on it, every loop writes disjoint outputs). */
+void orc_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
 }

@@ -51,15 +51,6 @@ cudaError_t scratch_address(void **out)
     return cudaSuccess;
 }
 
-bool valid_tensor(const nvfp4_tensor *t)
-{
-    auto al = [](const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; };
-    return t && t->second && t->rows >= 0 && t->K > 0 && t->K % 64 == 0 &&
-           t->mode == NVFP4_SCALE_TENSOR_FP32 && t->layout == NVFP4_LAYOUT_MMA_TILED &&
-           (t->rows == 0 || (t->codes && t->scales && al(t->codes, 16) && al(t->scales, 16))) &&
-           al(t->second, 4);
-}
-
 } // namespace
 
 } // namespace nv4
@@ -69,13 +60,18 @@ using namespace nv4;
 extern "C" nvfp4_status nvfp4_gemm_w4a4_noalloc(const nvfp4_tensor *a_q, const nvfp4_tensor *w, void *y,
                                                  int64_t ldy, int32_t y_dtype, nvfp4_stream_t stream)
 {
-    if (!valid_tensor(a_q) || !valid_tensor(w) || a_q->K != w->K)
+    nvfp4_status st = check_tensor(a_q, true);
+    if (st == NVFP4_OK)
+        st = check_tensor(w, true);
+    if (st != NVFP4_OK)
+        return st;
+    if (a_q->mode != NVFP4_SCALE_TENSOR_FP32 || w->mode != NVFP4_SCALE_TENSOR_FP32)
+        return NVFP4_ERR_UNSUPPORTED;
+    if (a_q->K != w->K)
         return NVFP4_ERR_INVALID_ARG;
     if (y_dtype != NVFP4_OUT_BF16 && y_dtype != NVFP4_OUT_FP32)
         return NVFP4_ERR_INVALID_ARG;
     const int64_t M = a_q->rows, N = w->rows, K = w->K;
-    if (M > ((int64_t)1 << 30) || N > ((int64_t)1 << 30))
-        return NVFP4_ERR_INVALID_ARG;
     if (M == 0 || N == 0)
         return NVFP4_OK;
     if (!y || (reinterpret_cast<uintptr_t>(y) % 16) != 0 || ldy < N)
@@ -127,4 +123,25 @@ extern "C" nvfp4_status nvfp4_gemm_w4a4_noalloc(const nvfp4_tensor *a_q, const n
     if (e == cudaSuccess)
         return NVFP4_OK;
     return e == cudaErrorNotSupported ? NVFP4_ERR_UNSUPPORTED : NVFP4_ERR_CUDA;
+}
+
+extern "C" nvfp4_status nvfp4_gemm_w4a4_noalloc_status(nvfp4_stream_t stream, int32_t *device_status)
+{
+    if (!device_status)
+        return NVFP4_ERR_INVALID_ARG;
+    void *scratch = nullptr;
+    if (scratch_address(&scratch) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t word = 0;
+    // the copy into pageable host memory returns once the stream's earlier
+    // work (the calls being asked about) has finished
+    if (cudaMemcpyAsync(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    if (cudaMemsetAsync(scratch, 0, sizeof(word), s) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    *device_status = (word & ST_NONFINITE) ? NVFP4_ERR_NONFINITE_INPUT : (word & ST_TIMEOUT) ? NVFP4_ERR_TIMEOUT
+                                                                                           : NVFP4_OK;
+    return NVFP4_OK;
 }

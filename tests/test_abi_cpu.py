@@ -150,3 +150,12 @@ def test_kv_argument_errors_fail_before_any_launch(nv):
                                        0x6000, 0, ctypes.c_void_p(0x40000), 16, None) == nv.ERR_WORKSPACE
     assert L.nvfp4_kv_append(ctypes.byref(cache()), 0x3000, 0x3100, 0x4000, 0x5000, 0, 4, None) == nv.ERR_INVALID_ARG
     assert L.nvfp4_kv_append(None, 0x3000, 0x3100, 0x4000, 0x5000, 65, 4, None) == nv.ERR_INVALID_ARG
+
+
+def test_output_checks_reject_before_launch(nv):
+    # the bindings check an output tensor before its pointer reaches the C ABI
+    import torch
+    with pytest.raises(ValueError):
+        nv._out(torch.empty((8, 16)), 8, 16, nv.OUT_BF16, None)       # not on a GPU
+    with pytest.raises(ValueError):
+        nv._out(None, 8, 16, 7, None)                                 # no such output type

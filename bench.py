@@ -307,6 +307,32 @@ def workload_prefill(c, N, steps, warmup, rot=2, x_rot=3):
             "quant_gbs": qbytes / (qms * 1e-3) / 1e9, "device_status": st}
 
 
+def workload_prefill_macro(c, N, steps, warmup, rot=2):
+    """The FP16 macro-scale GEMM (one FP16 scale per 256 elements of each row
+    replacing the tensor scale) at the prefill shape X [4096, 8192] x W
+    [N, 8192]^T on pre-quantised macro-mode activations; weights rotate over
+    `rot` copies."""
+    t, nv = c.torch, c.nv
+    M, K = 4096, 8192
+    wb = synth.weights(3, 1, N, K)
+    W = []
+    for _ in range(rot):
+        W.append(nv.quantize(c.bf16(wb), mode=nv.SCALE_MACRO_FP16))
+    del wb
+    a_q = nv.quantize(c.bf16(synth.activations(3, 0, M, K, 0.005, 100.0)), mode=nv.SCALE_MACRO_FP16)
+    y = t.empty((M, N), dtype=t.bfloat16, device=c.dev)
+    work = nv.Workspace(nv.workspace_size(nv.OP_GEMM, M, N, K))
+
+    def gemm_only(i):
+        nv.gemm(W[i % rot], a_q=a_q, y=y, ws=work)
+
+    gms = c.time(gemm_only, steps, warmup)
+    st = work.status()
+    del W
+    flops = 2.0 * M * N * K
+    return {"gemm_ms": gms, "gemm_tflops": flops / (gms * 1e-3) / 1e12, "device_status": st}
+
+
 def workload_policy(c, steps, warmup, policy):
     t, nv = c.torch, c.nv
     cfg = synth.CONFIGS[4]
@@ -778,6 +804,11 @@ def main():
                                            "gemm_frac_fp4": p["gemm_tflops"] / fp4_peak,
                                            "gemm_frac_fp4_nominal": p["gemm_tflops"] / fp4_nominal,
                                            "quant_gbs": p["quant_gbs"], "quant_frac_hbm": p["quant_gbs"] / hbm}
+        pm = workload_prefill_macro(c, 8192, min(es, 50), args.warmup)
+        extras["prefill_macro_n8192"] = {"gemm_tflops": pm["gemm_tflops"], "gemm_ms": pm["gemm_ms"],
+                                         "gemm_frac_fp4": pm["gemm_tflops"] / fp4_peak,
+                                         "device_status": pm["device_status"],
+                                         "config": "FP16 macro-scale GEMM X[4096,8192] x W[8192,8192]^T"}
         for pol, name in ((nv.POLICY_AUTO, "auto"), (nv.POLICY_Q4, "q4"), (nv.POLICY_Q8, "q8")):
             q = workload_policy(c, min(es, 20), 2, pol)
             extras[f"policy_stack_{name}"] = {"value": q["value"], "unit": "TFLOP/s", "ms": q["ms"],

@@ -146,6 +146,19 @@ def bf16_value(b):
 
 # ---- encoders -----------------------------------------------------------------
 
+def bf16_round(y):
+    """BF16 bits (uint16) of a layer output: y rounded to the nearest binary32
+    value, then to BF16 with round-to-nearest-even on the 16 dropped bits (the
+    output format of the W4A4 / W4A8 layers; finite inputs).  Used between
+    the layers of the chained policy stack."""
+    f = np.asarray(y, np.float64).astype(np.float32)
+    if not np.isfinite(f).all():
+        raise OracleError("bf16_round: non-finite value")
+    b = f.view(np.uint32).astype(np.uint64)
+    r = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+    return r.astype(np.uint16)
+
+
 def nvfp4_encode(x_bf16):
     """Per-tensor NVFP4 encode of a BF16-bit array [R, K].
 

@@ -156,3 +156,16 @@ def test_encode_preserves_sign_of_zero_results(orc, fmt):
     neg = 0x8 if fmt == "e2m1" else 0x80
     tiny = 0.2 if fmt == "e2m1" else 1e-4
     assert enc(-tiny) == neg and enc(tiny) == 0 and enc(-0.0) == neg and enc(0.0) == 0
+
+
+def test_bf16_round_matches_torch_cast(orc):
+    # the oracle's bf16_round against torch's float32 -> bfloat16 cast (round to
+    # nearest even): random values across many binades, exact ties (the
+    # dropped half exactly 0x8000 with even and odd kept bits) and signed zero
+    rng = np.random.default_rng(7)
+    v = (rng.standard_normal(20000) * np.exp2(rng.integers(-60, 60, 20000))).astype(np.float32)
+    ties = (np.arange(512, dtype=np.uint32) << 16 | 0x8000).view(np.float32)
+    v = np.concatenate([v, ties, -ties, np.array([0.0, -0.0], np.float32)])
+    got = orc.bf16_round(v.astype(np.float64))
+    want = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(got, want)

@@ -494,6 +494,39 @@ int32_t nvfp4_sm_count(void);
 enum { NVFP4_PATH_WHOLE_TILES = 1, NVFP4_PATH_STREAMK = 2 };
 int32_t nvfp4_gemm_kernel_path(int64_t M, int64_t N, int64_t K);
 
+/* Bounds-checked build.  libnvfp4_checked.so is the same library compiled
+ * with NVFP4_CHECK_BOUNDS: before each access its kernels test that shared
+ * memory destinations and operands lie in the CTA's dynamic shared memory
+ * (bulk and tensor copies aligned, tensor-map x a multiple of 16 bytes),
+ * TMEM column ranges within the 512 columns, and global loads and stores
+ * within the byte range the call's arguments grant each tensor (its rows
+ * and leading dimension in the layout this header documents).  A failed test
+ * skips its access and is counted; the first failure of each translation unit
+ * keeps its site (file and line), the offending value and its limit.
+ * Outputs of a call with a failed test are unspecified (the call's bounded
+ * waits may also record TIMEOUT for copies that were skipped).
+ *
+ * nvfp4_diag_bounds_checked: 1 in the checked build, 0 in the normal one.
+ * nvfp4_diag_bounds_record: synchronises the device, then writes the total
+ * number of failed tests since the last clear to *failures and, when there is
+ * one, the first recorded failure's site ("unit.cu:line", or
+ * "unit.cu via ptx.cuh:line" for a test inside a shared wrapper) to `where`
+ * (NUL-terminated, at most where_len bytes; may be null) and its value and
+ * limit to *value and *limit (may be null); clear != 0 resets the records.
+ * Returns NVFP4_ERR_UNSUPPORTED in the normal build.
+ *
+ * nvfp4_diag_bounds_selftest: stores the byte 1 to every offset of
+ * [0, span_bytes + 64) of the device buffer buf (buf_bytes >= span_bytes +
+ * 64, so every store is inside buf) from a kernel that tests each store
+ * against a span of span_bytes (1 .. 2^30): the checked build skips and
+ * counts the last 64 stores, the normal build makes them all.  Asynchronous
+ * on `stream`; the caller owns buf. */
+int32_t nvfp4_diag_bounds_checked(void);
+nvfp4_status nvfp4_diag_bounds_record(uint64_t *failures, char *where, int32_t where_len, uint64_t *value,
+                                      uint64_t *limit, int32_t clear);
+nvfp4_status nvfp4_diag_bounds_selftest(uint8_t *buf, uint64_t buf_bytes, uint64_t span_bytes,
+                                        nvfp4_stream_t stream);
+
 /* Library version string. */
 const char *nvfp4_version(void);
 

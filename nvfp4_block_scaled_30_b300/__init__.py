@@ -14,7 +14,13 @@ from typing import Optional
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libnvfp4.so")
+# NVFP4_LIB=checked loads the bounds-checked build (libnvfp4_checked.so:
+# every kernel access tested first, failures recorded; see bounds_record)
+LIB_VARIANT = os.environ.get("NVFP4_LIB", "")
+if LIB_VARIANT not in ("", "checked"):
+    raise RuntimeError(f"NVFP4_LIB={LIB_VARIANT!r}: expected unset or 'checked'")
+LIB_NAME = "libnvfp4_checked.so" if LIB_VARIANT == "checked" else "libnvfp4.so"
+LIB_PATH = os.path.join(_HERE, LIB_NAME)
 
 # ---- enums (include/nvfp4.h) -----------------------------------------------------
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_NONFINITE_INPUT, ERR_TIMEOUT, ERR_CUDA, \
@@ -34,7 +40,8 @@ EXPORTED = ["nvfp4_scale_bytes", "nvfp4_workspace_size", "nvfp4_workspace_init",
             "nvfp4_gemm_w4a4_noalloc", "nvfp4_gemm_nvfp4_out", "nvfp4_moe_up_swiglu",
             "nvfp4_moe_down_combine", "nvfp4_grouped_w4a8_gemm", "nvfp4_grouped_gemm_x",
             "nvfp4_diag_streamk_skip_flag", "nvfp4_kv_append", "nvfp4_kv_decode_attention",
-            "nvfp4_gemm_kernel_path", "nvfp4_diag_fp4_mma_rate", "nvfp4_gemm_w4a4_noalloc_status"]
+            "nvfp4_gemm_kernel_path", "nvfp4_diag_fp4_mma_rate", "nvfp4_gemm_w4a4_noalloc_status",
+            "nvfp4_diag_bounds_checked", "nvfp4_diag_bounds_record", "nvfp4_diag_bounds_selftest"]
 
 
 def _require(ok: bool, what: str) -> None:
@@ -68,12 +75,14 @@ _PT = ctypes.POINTER(TensorDesc)
 
 
 def lib():
-    """Load libnvfp4.so (raises if it has not been built)."""
+    """Load libnvfp4.so, or libnvfp4_checked.so under NVFP4_LIB=checked
+    (raises if it has not been built)."""
     global _LIB
     if _LIB is None:
         if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"libnvfp4.so not built ({LIB_PATH}); run "
-                               "python -m nvfp4_block_scaled_30_b300.build")
+            flag = " --checked" if LIB_VARIANT == "checked" else ""
+            raise RuntimeError(f"{LIB_NAME} not built ({LIB_PATH}); run "
+                               f"python -m nvfp4_block_scaled_30_b300.build{flag}")
         L = ctypes.CDLL(LIB_PATH)
         sig = {
             "nvfp4_scale_bytes": (_I32, [_I64, _I64, _I32, ctypes.POINTER(_SZ)]),
@@ -107,6 +116,11 @@ def lib():
             "nvfp4_sm_count": (_I32, []),
             "nvfp4_gemm_kernel_path": (_I32, [_I64, _I64, _I64]),
             "nvfp4_diag_fp4_mma_rate": (_I32, [_I32, _VP, _VP]),
+            "nvfp4_diag_bounds_checked": (_I32, []),
+            "nvfp4_diag_bounds_record": (_I32, [ctypes.POINTER(ctypes.c_uint64), ctypes.c_char_p, _I32,
+                                                ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64),
+                                                _I32]),
+            "nvfp4_diag_bounds_selftest": (_I32, [_VP, ctypes.c_uint64, ctypes.c_uint64, _VP]),
             "nvfp4_version": (ctypes.c_char_p, []),
         }
         for name, (res, args) in sig.items():
@@ -386,6 +400,31 @@ def noalloc_status(stream=None) -> int:
     out = _I32(0)
     _check(lib().nvfp4_gemm_w4a4_noalloc_status(_stream(stream), ctypes.byref(out)), "nvfp4_gemm_w4a4_noalloc_status")
     return out.value
+
+
+def bounds_checked() -> bool:
+    """Whether the loaded library is the bounds-checked build."""
+    return bool(lib().nvfp4_diag_bounds_checked())
+
+
+def bounds_record(clear: bool = True):
+    """Bounds-checked build: (failures, where, value, limit) of the failed
+    address tests since the last clear (synchronises the device); where is
+    "unit.cu:line" of the first one, or "" when there was none."""
+    n, v, lim = ctypes.c_uint64(0), ctypes.c_uint64(0), ctypes.c_uint64(0)
+    buf = ctypes.create_string_buffer(128)
+    _check(lib().nvfp4_diag_bounds_record(ctypes.byref(n), buf, len(buf), ctypes.byref(v), ctypes.byref(lim),
+                                          1 if clear else 0), "nvfp4_diag_bounds_record")
+    return n.value, buf.value.decode(), v.value, lim.value
+
+
+def bounds_selftest(buf: torch.Tensor, span_bytes: int, stream=None) -> None:
+    """nvfp4_diag_bounds_selftest on a uint8 CUDA tensor of at least
+    span_bytes + 64 bytes."""
+    _require(buf.dtype == torch.uint8 and buf.is_cuda and buf.is_contiguous(),
+             "bounds_selftest: buf must be a contiguous uint8 CUDA tensor")
+    _check(lib().nvfp4_diag_bounds_selftest(_ptr(buf), buf.numel(), span_bytes, _stream(stream)),
+           "nvfp4_diag_bounds_selftest")
 
 
 def probe_convert(v: torch.Tensor, stream=None):

@@ -5,6 +5,7 @@
 // "AdaLLM Breakthrough: First NVFP4-Only Inference Engine for RTX 4090
 // Unveiled").
 #include <algorithm>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <cudaTypedefs.h>
@@ -206,6 +207,30 @@ static nvfp4_status run_w4a4_dense(const uint8_t *a_codes, const uint8_t *a_scal
     }
     (void)N;
     return from_cuda(launch_w4a4_dense(g, stream));
+}
+
+// Records of the bounds-checked build, one per translation unit with
+// kernels (registered by their static initialisers; constant-initialised
+// here, so registration order does not matter).
+#ifdef NVFP4_CHECK_BOUNDS
+constexpr bool kCheckBounds = true;
+#else
+constexpr bool kCheckBounds = false;
+#endif
+namespace {
+struct BoundsUnit {
+    const void *symbol;
+    const char *unit;
+};
+constexpr int MAX_BOUNDS_UNITS = 32;
+BoundsUnit g_bounds_units[MAX_BOUNDS_UNITS];
+int g_bounds_n = 0;
+} // namespace
+
+void register_bounds_record(const void *symbol, const char *unit)
+{
+    if (g_bounds_n < MAX_BOUNDS_UNITS)
+        g_bounds_units[g_bounds_n++] = BoundsUnit{symbol, unit};
 }
 
 } // namespace nv4
@@ -935,6 +960,59 @@ nvfp4_status nvfp4_diag_fp4_mma_rate(int32_t iters, uint64_t *cycles, nvfp4_stre
     if (iters < 1 || iters > (1 << 24) || !cycles || !aligned(cycles, 8))
         return NVFP4_ERR_INVALID_ARG;
     return from_cuda(launch_fp4_mma_rate(iters, cycles, (cudaStream_t)stream));
+}
+
+int32_t nvfp4_diag_bounds_checked(void) { return kCheckBounds ? 1 : 0; }
+
+nvfp4_status nvfp4_diag_bounds_selftest(uint8_t *buf, uint64_t buf_bytes, uint64_t span_bytes, nvfp4_stream_t stream)
+{
+    if (!buf || span_bytes == 0 || span_bytes > (uint64_t(1) << 30) || buf_bytes < span_bytes + 64)
+        return NVFP4_ERR_INVALID_ARG;
+    return from_cuda(launch_bounds_selftest(buf, span_bytes, (cudaStream_t)stream));
+}
+
+nvfp4_status nvfp4_diag_bounds_record(uint64_t *failures, char *where, int32_t where_len, uint64_t *value,
+                                      uint64_t *limit, int32_t clear)
+{
+    if (!kCheckBounds)
+        return NVFP4_ERR_UNSUPPORTED;
+    if (!failures || where_len < 0 || (where_len > 0 && !where))
+        return NVFP4_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    uint64_t total = 0;
+    bool have = false;
+    for (int u = 0; u < g_bounds_n; ++u) {
+        unsigned long long rec[4];
+        if (cudaMemcpyFromSymbol(rec, g_bounds_units[u].symbol, sizeof(rec)) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        total += rec[0];
+        if (rec[0] != 0 && !have) {
+            have = true;
+            if (value)
+                *value = rec[2];
+            if (limit)
+                *limit = rec[3];
+            if (where && where_len > 0) {
+                const char *name = g_bounds_units[u].unit;
+                const char *slash = std::strrchr(name, '/');
+                name = slash ? slash + 1 : name;
+                static const char *const shared_files[] = {"", " via ptx.cuh", " via epilogue.cuh"};
+                const unsigned file = (unsigned)(rec[1] >> 16);
+                std::snprintf(where, (size_t)where_len, "%s%s:%u", name, file < 3 ? shared_files[file] : " via ?",
+                              (unsigned)(rec[1] & 0xFFFFu));
+            }
+        }
+        if (clear) {
+            const unsigned long long zero[4] = {0, 0, 0, 0};
+            if (cudaMemcpyToSymbol(g_bounds_units[u].symbol, zero, sizeof(zero)) != cudaSuccess)
+                return NVFP4_ERR_CUDA;
+        }
+    }
+    *failures = total;
+    if (!have && where && where_len > 0)
+        where[0] = '\0';
+    return NVFP4_OK;
 }
 
 nvfp4_status nvfp4_probe_convert(const float *in, int64_t n, uint8_t *out_e2m1, uint8_t *out_e4m3,

@@ -11,11 +11,18 @@
 namespace nv4 {
 
 // Where element (i, j) of the output goes: out[i * ld_i + j * ld_j]; vec_ok
-// when ld_j == 1 and 16-byte vector stores of a row are aligned.
+// when ld_j == 1 and 16-byte vector stores of a row are aligned; span: the
+// output's bytes (tested in the bounds-checked build).
 struct OutDesc {
     void *out;
     int64_t ld_i, ld_j;
     int32_t out_dtype, vec_ok;
+    Span span;
+};
+
+// Spans of an NVFP4 output's codes and tiled scales.
+struct QSpans {
+    Span codes, scales;
 };
 
 // Row i, columns j0 .. j0 + 31 (bits of the FP32 accumulator in v) times
@@ -28,6 +35,8 @@ __device__ __forceinline__ void store_chunk32(const OutDesc &o, const uint32_t (
     if (o.ld_j == 1 && o.vec_ok && j0 + 32 <= j_end) {
         if (o.out_dtype == NVFP4_OUT_BF16) {
             uint4 *d = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(o.out) + i * o.ld_i + j0);
+            if (!in_span(NV4_SITE(2), o.span, d, 64))
+                return;
 #pragma unroll
             for (int c = 0; c < 32; c += 8) {
                 uint32_t w[4];
@@ -41,6 +50,8 @@ __device__ __forceinline__ void store_chunk32(const OutDesc &o, const uint32_t (
             }
         } else {
             float4 *d = reinterpret_cast<float4 *>(static_cast<float *>(o.out) + i * o.ld_i + j0);
+            if (!in_span(NV4_SITE(2), o.span, d, 128))
+                return;
 #pragma unroll
             for (int c = 0; c < 32; c += 4)
                 d[c / 4] = make_float4(alpha * __uint_as_float(v[c]), alpha * __uint_as_float(v[c + 1]),
@@ -54,10 +65,12 @@ __device__ __forceinline__ void store_chunk32(const OutDesc &o, const uint32_t (
         if (j < j_end) {
             const float y = alpha * __uint_as_float(v[c]);
             const int64_t off = i * o.ld_i + j * o.ld_j;
-            if (o.out_dtype == NVFP4_OUT_BF16)
-                static_cast<__nv_bfloat16 *>(o.out)[off] = __float2bfloat16_rn(y);
-            else
+            if (o.out_dtype == NVFP4_OUT_BF16) {
+                if (in_span(NV4_SITE(2), o.span, static_cast<__nv_bfloat16 *>(o.out) + off, 2))
+                    static_cast<__nv_bfloat16 *>(o.out)[off] = __float2bfloat16_rn(y);
+            } else if (in_span(NV4_SITE(2), o.span, static_cast<float *>(o.out) + off, 4)) {
                 static_cast<float *>(o.out)[off] = y;
+            }
         }
     }
 }
@@ -68,7 +81,7 @@ __device__ __forceinline__ void store_chunk32(const OutDesc &o, const uint32_t (
 // one scale byte per block in the row's MMA-tiled scale slots srow (see
 // q_row_addr).  Returns the largest |y|.
 __device__ __forceinline__ float encode_store_q(const uint32_t (&v)[32], uint8_t *crow, uint8_t *srow, int j0,
-                                                float s)
+                                                float s, const QSpans &qs)
 {
     float m = 0.0f;
 #pragma unroll
@@ -86,9 +99,11 @@ __device__ __forceinline__ float encode_store_q(const uint32_t (&v)[32], uint8_t
                                  __fmul_rn(__uint_as_float(v[16 * h + 2 * t + 1]), r))
                           << (8 * (t & 3));
         const int j = j0 + 16 * h;
-        *reinterpret_cast<uint2 *>(crow + j / 2) = make_uint2(pk[0], pk[1]);
+        if (in_span(NV4_SITE(2), qs.codes, crow + j / 2, 8))
+            *reinterpret_cast<uint2 *>(crow + j / 2) = make_uint2(pk[0], pk[1]);
         const int blk = j / 16;
-        srow[(blk >> 2) * 512 + (blk & 3)] = (uint8_t)e;
+        if (in_span(NV4_SITE(2), qs.scales, srow + (blk >> 2) * 512 + (blk & 3), 1))
+            srow[(blk >> 2) * 512 + (blk & 3)] = (uint8_t)e;
         m = fmaxf(m, amb);
     }
     return m;
@@ -108,10 +123,13 @@ __device__ __forceinline__ void q_row_addr(int64_t i, int64_t n, uint8_t *codes,
 
 // Zero scale bytes of 32 columns from j in a padding row's scale slots (rows
 // of the last 128-row tile past the real rows, as the quantisers leave them).
-__device__ __forceinline__ void zero_pad_scales32(uint8_t *srow, int j)
+__device__ __forceinline__ void zero_pad_scales32(uint8_t *srow, int j, const QSpans &qs)
 {
-    srow[(j >> 6) * 512 + ((j >> 4) & 3)] = 0;
-    srow[(j >> 6) * 512 + ((j >> 4) & 3) + 1] = 0;
+    uint8_t *b = srow + (j >> 6) * 512 + ((j >> 4) & 3);
+    if (in_span(NV4_SITE(2), qs.scales, b, 2)) {
+        b[0] = 0;
+        b[1] = 0;
+    }
 }
 
 } // namespace nv4

@@ -59,6 +59,9 @@ struct Params {
     int32_t m_tiles, n_tiles, k64, groups, out_dtype, vec_ok;
     uint32_t *status;
     uint64_t timeout_ns;
+    // the bytes the call's arguments grant each tensor (tested before each
+    // plain access in the bounds-checked build)
+    Span sp_sfa, sp_sfb, sp_a_macro, sp_w_macro, sp_out;
 };
 
 __device__ __forceinline__ void tile_of(const Params &p, int item, int &tm, int &tn)
@@ -133,11 +136,14 @@ __global__ void __launch_bounds__(THREADS, 1) macro_kernel(const __grid_constant
                     uint8_t *sA = smem + st * STAGE_BYTES;
                     uint8_t *sB = sA + A_BYTES;
                     mbar_arrive_expect_tx(&full[st], A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES);
-                    tma_load_2d(sA, &p.tmap_a, g * STAGE_K_BYTES, tm * BM, &full[st]);
-                    tma_load_2d(sB, &p.tmap_b, g * STAGE_K_BYTES, tn * BN, &full[st]);
-                    bulk_load(sB + B_BYTES, p.sfa + ((size_t)tm * p.k64 + 4 * g) * 512, SFA_BYTES, &full[st]);
-                    bulk_load(sB + B_BYTES + SFA_BYTES, p.sfb + ((size_t)tn * p.k64 + 4 * g) * 512, SFB_BYTES,
-                              &full[st]);
+                    tma_load_2d(sA, &p.tmap_a, g * STAGE_K_BYTES, tm * BM, &full[st], A_BYTES);
+                    tma_load_2d(sB, &p.tmap_b, g * STAGE_K_BYTES, tn * BN, &full[st], B_BYTES);
+                    const uint8_t *sfa_src = p.sfa + ((size_t)tm * p.k64 + 4 * g) * 512;
+                    const uint8_t *sfb_src = p.sfb + ((size_t)tn * p.k64 + 4 * g) * 512;
+                    if (in_span(NV4_SITE(0), p.sp_sfa, sfa_src, SFA_BYTES))
+                        bulk_load(sB + B_BYTES, sfa_src, SFA_BYTES, &full[st]);
+                    if (in_span(NV4_SITE(0), p.sp_sfb, sfb_src, SFB_BYTES))
+                        bulk_load(sB + B_BYTES + SFA_BYTES, sfb_src, SFB_BYTES, &full[st]);
                     ++issued;
                     if (++st == STAGES) {
                         st = 0;
@@ -231,7 +237,9 @@ __global__ void __launch_bounds__(THREADS, 1) macro_kernel(const __grid_constant
                     break;
                 }
                 tc_fence_after();
-                const float sa = i < p.M ? __half2float(__ushort_as_half(p.a_macro[i * p.groups + g])) : 0.0f;
+                const float sa = i < p.M && in_span(NV4_SITE(0), p.sp_a_macro, p.a_macro + i * p.groups + g, 2)
+                                     ? __half2float(__ushort_as_half(p.a_macro[i * p.groups + g]))
+                                     : 0.0f;
                 const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + pb * BN + half * 64;
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
@@ -248,8 +256,9 @@ __global__ void __launch_bounds__(THREADS, 1) macro_kernel(const __grid_constant
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
                         const int64_t j = j0 + h2 * 32 + c;
-                        const float sw =
-                            j < p.N ? __half2float(__ushort_as_half(__ldg(p.w_macro + j * p.groups + g))) : 0.0f;
+                        const float sw = j < p.N && in_span(NV4_SITE(0), p.sp_w_macro, p.w_macro + j * p.groups + g, 2)
+                                             ? __half2float(__ushort_as_half(__ldg(p.w_macro + j * p.groups + g)))
+                                             : 0.0f;
                         acc[h2 * 32 + c] = fmaf(sa * sw, __uint_as_float(v[c]), acc[h2 * 32 + c]);
                     }
                 }
@@ -266,6 +275,8 @@ __global__ void __launch_bounds__(THREADS, 1) macro_kernel(const __grid_constant
                         uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + i * p.ldy + j0);
 #pragma unroll
                         for (int c = 0; c < 64; c += 8) {
+                            if (!in_span(NV4_SITE(0), p.sp_out, o + c / 8, 16))
+                                continue;
                             uint32_t w[4];
 #pragma unroll
                             for (int z = 0; z < 4; ++z) {
@@ -278,16 +289,20 @@ __global__ void __launch_bounds__(THREADS, 1) macro_kernel(const __grid_constant
                         float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + i * p.ldy + j0);
 #pragma unroll
                         for (int c = 0; c < 64; c += 4)
-                            o[c / 4] = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+                            if (in_span(NV4_SITE(0), p.sp_out, o + c / 4, 16))
+                                o[c / 4] = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
                     }
                 } else {
 #pragma unroll
                     for (int c = 0; c < 64; ++c) {
                         if (j0 + c < p.N) {
-                            if (p.out_dtype == NVFP4_OUT_BF16)
-                                static_cast<__nv_bfloat16 *>(p.out)[i * p.ldy + j0 + c] = __float2bfloat16_rn(acc[c]);
-                            else
-                                static_cast<float *>(p.out)[i * p.ldy + j0 + c] = acc[c];
+                            const int64_t off = i * p.ldy + j0 + c;
+                            if (p.out_dtype == NVFP4_OUT_BF16) {
+                                if (in_span(NV4_SITE(0), p.sp_out, static_cast<__nv_bfloat16 *>(p.out) + off, 2))
+                                    static_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(acc[c]);
+                            } else if (in_span(NV4_SITE(0), p.sp_out, static_cast<float *>(p.out) + off, 4)) {
+                                static_cast<float *>(p.out)[off] = acc[c];
+                            }
                         }
                     }
                 }
@@ -335,6 +350,11 @@ cudaError_t launch_w4a4_macro(const MacroGemmArgs &g, cudaStream_t stream)
     p.vec_ok = ((g.ldy * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(g.out) % 16) == 0) ? 1 : 0;
     p.status = g.status;
     p.timeout_ns = g.timeout_ns;
+    p.sp_sfa = span_of(g.a_scales, tiled_scale_bytes(g.M, g.K));
+    p.sp_sfb = span_of(g.w_scales, tiled_scale_bytes(g.N, g.K));
+    p.sp_a_macro = span_of(g.a_macro, 2u * (uint64_t)g.M * (uint64_t)p.groups);
+    p.sp_w_macro = span_of(g.w_macro, 2u * (uint64_t)g.N * (uint64_t)p.groups);
+    p.sp_out = span_of(g.out, matrix_bytes(g.M, g.N, g.ldy, esz));
     cudaError_t e = cudaFuncSetAttribute(macro_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess)
         return e;

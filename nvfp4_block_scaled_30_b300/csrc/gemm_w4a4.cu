@@ -129,6 +129,10 @@ struct Params {
     int64_t total_rows;      // rows of the index list / output (offsets are clamped to it)
     uint32_t *status;
     uint64_t timeout_ns;
+    // the bytes the call's arguments grant each tensor (tested before each
+    // plain access in the bounds-checked build)
+    Span sp_a_codes, sp_sfa, sp_sfb, sp_b_second, sp_out, sp_slots, sp_flags, sp_yq_codes, sp_yq_scales;
+    Span sp_comb_idx, sp_comb_w, sp_offsets, sp_row_idx;
 };
 
 struct Tile {
@@ -162,6 +166,10 @@ __device__ __forceinline__ void decode_dense(const Params &p, int tile, Tile &t)
 // memory outside the index list or the output.
 __device__ __forceinline__ void expert_rows(const Params &p, int e, int64_t &lo, int64_t &hi)
 {
+    if (!in_span(NV4_SITE(0), p.sp_offsets, p.offsets + e, 16)) {
+        lo = hi = 0;
+        return;
+    }
     lo = min(max(p.offsets[e], (int64_t)0), p.total_rows);
     hi = min(max(p.offsets[e + 1], lo), p.total_rows);
 }
@@ -267,7 +275,13 @@ __device__ __forceinline__ void tile_rows(const Params &p, bool indexed, const T
     for (int q = 0; q < 4; ++q) {
         const int64_t g = t.row0 + lane + 32 * q;
         row_ok[q] = g < t.row_end;
-        int r = row_ok[q] ? (indexed ? p.row_idx[g] : (int)g) : 0;
+        int r = 0;
+        if (row_ok[q]) {
+            if (!indexed)
+                r = (int)g;
+            else if (in_span(NV4_SITE(0), p.sp_row_idx, p.row_idx + g, 4))
+                r = p.row_idx[g];
+        }
         if (r < 0 || r >= p.a_rows)
             r = 0;
         src_row[q] = r;
@@ -328,7 +342,12 @@ __device__ __forceinline__ bool wait_flag(const uint32_t *f, uint64_t timeout_ns
 
 __device__ __forceinline__ OutDesc out_desc(const Params &p)
 {
-    return OutDesc{p.out, p.ld_i, p.ld_j, p.out_dtype, p.vec_ok};
+    return OutDesc{p.out, p.ld_i, p.ld_j, p.out_dtype, p.vec_ok, p.sp_out};
+}
+
+__device__ __forceinline__ QSpans q_spans(const Params &p)
+{
+    return QSpans{p.sp_yq_codes, p.sp_yq_scales};
 }
 
 // Row i of the NVFP4 output: its code row and the base of its scale slots.
@@ -465,12 +484,14 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
             if ((op == 1 && part_b) || (op == 0 && !indexed && part_a)) {
                 const int arow = GROUPED ? (int)tt.row0 : tt.tile_m * BM;
                 tma_load_2d(op == 0 ? sA : sB, op == 0 ? &p.tmap_a : &p.tmap_b, kb * STAGE_K_BYTES,
-                            op == 0 ? arow : brow0, &full[st]);
+                            op == 0 ? arow : brow0, &full[st],
+                            op == 0 ? (uint32_t)p.a_box_rows * STAGE_K_BYTES : (uint32_t)C::B_BYTES);
             } else if ((op == 2 && !GROUPED && part_a) ||
                        (op >= 3 && op < 3 + C::NB && bt0 + op - 3 < p.b_row_tiles && part_b)) {
                 const uint8_t *src = op == 2 ? p.sfa + ((size_t)tt.tile_m * p.k64 + 4 * kb) * 512
                                              : p.sfb + ((size_t)(bt0 + op - 3) * p.k64 + 4 * kb) * 512;
-                bulk_load(op == 2 ? sSFA : sSFB + (op - 3) * 2048, src, nk * 512, &sf_full[st]);
+                if (in_span(NV4_SITE(0), op == 2 ? p.sp_sfa : p.sp_sfb, src, nk * 512))
+                    bulk_load(op == 2 ? sSFA : sSFB + (op - 3) * 2048, src, nk * 512, &sf_full[st]);
             }
         };
         // Before waiting for the previous grid (programmatic dependent
@@ -537,7 +558,9 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                             const uint8_t *src = p.a_codes + (size_t)src_row[q] * row_bytes + kb * STAGE_K_BYTES;
 #pragma unroll
                             for (int c = 0; c < 8; ++c) {
-                                const int n = row_ok[q] ? max(0, min(16, kbytes - c * 16)) : 0;
+                                int n = row_ok[q] ? max(0, min(16, kbytes - c * 16)) : 0;
+                                if (n && !in_span(NV4_SITE(0), p.sp_a_codes, src + c * 16, n))
+                                    n = 0;
                                 cp_async_16(sA + r * STAGE_K_BYTES + ((c ^ (r & 7)) << 4), n ? src + c * 16 : src, n);
                             }
                         }
@@ -552,7 +575,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                             ((size_t)(r >> 7) * p.k64 + 4 * kb) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
-                            const bool live = row_ok[q] && kk < nk;
+                            const bool live = row_ok[q] && kk < nk &&
+                                              in_span(NV4_SITE(0), p.sp_sfa, p.sfa + base + kk * 512, 4);
                             cp_async_4(sSFA + kk * 512 + lane * 16 + q * 4, p.sfa + (live ? base + kk * 512 : 0),
                                        live ? 4u : 0u);
                         }
@@ -767,7 +791,9 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                 acc = 0;
                 acc_phase ^= 1u;
             }
-            const float alpha = a_s * p.b_second[GROUPED ? t.expert : 0];
+            const int b_idx = GROUPED ? t.expert : 0;
+            const float alpha =
+                a_s * (in_span(NV4_SITE(0), p.sp_b_second, p.b_second + b_idx, 4) ? p.b_second[b_idx] : 0.0f);
             int64_t i, i_end;
             if (GROUPED) {
                 i = t.row0 + row_in_tile;
@@ -800,7 +826,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                             if (p.out_q) {
                                 uint8_t *crow, *srow;
                                 q_row(p, i, crow, srow);
-                                m = fmaxf(m, encode_store_q(v[c], crow, srow, (int)j, s));
+                                m = fmaxf(m, encode_store_q(v[c], crow, srow, (int)j, s, q_spans(p)));
                             } else
                                 store_chunk32(out_desc(p), v[c], i, j, 1.0f, i_end, p.yq_n);
                         }
@@ -809,13 +835,17 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                     // gate-weighted combine: row i's products, times its
                     // routing weight, added to its token's output row (rows
                     // whose token index is out of range add nothing)
-                    const int64_t tok = i < i_end ? (int64_t)p.comb_idx[i] : -1;
+                    const bool row_in = i < i_end && in_span(NV4_SITE(0), p.sp_comb_idx, p.comb_idx + i, 4) &&
+                                        in_span(NV4_SITE(0), p.sp_comb_w, p.comb_w + i, 4);
+                    const int64_t tok = row_in ? (int64_t)p.comb_idx[i] : -1;
                     if (tok >= 0 && tok < p.comb_rows) {
                         const float gw = p.comb_w[i];
 #pragma unroll
                         for (int c = 0; c < NCH; ++c) {
                             float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + tok * p.ld_i +
                                                                      j_base + 32 * c);
+                            if (!in_span(NV4_SITE(0), p.sp_out, dst, 128))
+                                continue;
 #pragma unroll
                             for (int e = 0; e < 32; e += 4)
                                 atomicAdd(dst + e / 4, make_float4(gw * (alpha * __uint_as_float(v[c][e])),
@@ -848,7 +878,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
 #pragma unroll
                         for (int e = 0; e < 32; ++e) // y = alpha * acc, as the FP32 output path forms it
                             v[c][e] = __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[c][e])));
-                        m = fmaxf(m, encode_store_q(v[c], crow, srow, (int)(j_base + c * 32), s));
+                        m = fmaxf(m, encode_store_q(v[c], crow, srow, (int)(j_base + c * 32), s, q_spans(p)));
                     }
                 } else {
                     // padding rows of the last M tile (the tile's rows all
@@ -857,7 +887,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                     for (int c = 0; c < NCH; ++c) {
                         const int j = (int)(j_base + c * 32);
                         if (j < j_end)
-                            zero_pad_scales32(srow, j);
+                            zero_pad_scales32(srow, j, q_spans(p));
                     }
                 }
 #pragma unroll
@@ -877,14 +907,16 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                     for (int c = 0; c < NCH; ++c)
 #pragma unroll
                         for (int u = 0; u < 32; u += 4)
-                            __stcg(reinterpret_cast<float4 *>(slot + c * 32 + u),
+                            if (in_span(NV4_SITE(0), p.sp_slots, slot + c * 32 + u, 16))
+                                __stcg(reinterpret_cast<float4 *>(slot + c * 32 + u),
                                    make_float4(__uint_as_float(v[c][u]), __uint_as_float(v[c][u + 1]),
                                                __uint_as_float(v[c][u + 2]), __uint_as_float(v[c][u + 3])));
                 }
                 epi_bar_sync();
                 // (diag_skip_flag: a test names one CTA that never raises its
                 // flag, so the owner's bounded wait runs out)
-                if (threadIdx.x == 32 * EPI_FIRST_WARP && (int)blockIdx.x != p.diag_skip_flag) {
+                if (threadIdx.x == 32 * EPI_FIRST_WARP && (int)blockIdx.x != p.diag_skip_flag &&
+                    in_span(NV4_SITE(0), p.sp_flags, p.flags + blockIdx.x, 4)) {
                     __threadfence();
                     st_release_gpu(p.flags + blockIdx.x, 1u);
                 }
@@ -907,7 +939,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                     for (int c = 0; c < NCH; ++c)
 #pragma unroll
                         for (int u = 0; u < 32; u += 4)
-                            *reinterpret_cast<float4 *>(tile_s + row_in_tile * RS + cbase + c * 32 + u) =
+                            if (in_dyn_smem(NV4_SITE(0), smem_u32(tile_s + row_in_tile * RS + cbase + c * 32 + u), 16))
+                                *reinterpret_cast<float4 *>(tile_s + row_in_tile * RS + cbase + c * 32 + u) =
                                 make_float4(__uint_as_float(v[c][u]), __uint_as_float(v[c][u + 1]),
                                             __uint_as_float(v[c][u + 2]), __uint_as_float(v[c][u + 3]));
                 }
@@ -920,7 +953,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                 bool got = true;
                 if (threadIdx.x == 32 * EPI_FIRST_WARP)
                     for (int c = 1; c <= n_contrib && got; ++c)
-                        got = wait_flag(p.flags + blockIdx.x + c, p.timeout_ns, abort_flag);
+                        got = in_span(NV4_SITE(0), p.sp_flags, p.flags + blockIdx.x + c, 4) &&
+                              wait_flag(p.flags + blockIdx.x + c, p.timeout_ns, abort_flag);
                 if (!epi_bar_all(got)) {
                     if (threadIdx.x == 32 * EPI_FIRST_WARP)
                         record_timeout(p, abort_flag);
@@ -941,8 +975,9 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                     for (int u = 0; u < UB; ++u) {
                         const int e4 = base + u * STEP;
                         const int r = e4 / BN, cc = e4 - r * BN;
-                        acc4[u] = e4 < total4 ? *reinterpret_cast<const float4 *>(tile_s + r * RS + cc)
-                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+                        acc4[u] = e4 < total4 && in_dyn_smem(NV4_SITE(0), smem_u32(tile_s + r * RS + cc), 16)
+                                      ? *reinterpret_cast<const float4 *>(tile_s + r * RS + cc)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
                     for (int c = 1; c <= n_contrib; ++c) {
                         const float *slot = p.slots + (size_t)(blockIdx.x + c) * p.slot_stride;
@@ -950,8 +985,9 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
 #pragma unroll
                         for (int u = 0; u < UB; ++u) {
                             const int e4 = base + u * STEP;
-                            w4[u] = e4 < total4 ? __ldcg(reinterpret_cast<const float4 *>(slot + e4))
-                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+                            w4[u] = e4 < total4 && in_span(NV4_SITE(0), p.sp_slots, slot + e4, 16)
+                                        ? __ldcg(reinterpret_cast<const float4 *>(slot + e4))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
                         }
 #pragma unroll
                         for (int u = 0; u < UB; ++u) {
@@ -976,21 +1012,25 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                                 __nv_bfloat162 h1 = __floats2bfloat162_rn(y4[2], y4[3]);
                                 const uint2 w2 = make_uint2(*reinterpret_cast<uint32_t *>(&h0),
                                                             *reinterpret_cast<uint32_t *>(&h1));
-                                *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.out) + row * p.ld_i + c0 +
-                                                           cc) = w2;
+                                __nv_bfloat16 *d = static_cast<__nv_bfloat16 *>(p.out) + row * p.ld_i + c0 + cc;
+                                if (in_span(NV4_SITE(0), p.sp_out, d, 8))
+                                    *reinterpret_cast<uint2 *>(d) = w2;
                             } else {
-                                *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + row * p.ld_i + c0 + cc) =
-                                    make_float4(y4[0], y4[1], y4[2], y4[3]);
+                                float *d = static_cast<float *>(p.out) + row * p.ld_i + c0 + cc;
+                                if (in_span(NV4_SITE(0), p.sp_out, d, 16))
+                                    *reinterpret_cast<float4 *>(d) = make_float4(y4[0], y4[1], y4[2], y4[3]);
                             }
                         } else {
 #pragma unroll
                             for (int q4 = 0; q4 < 4; ++q4) {
                                 if (cc + q4 < cols) {
                                     const int64_t off = row * p.ld_i + (c0 + cc + q4) * p.ld_j;
-                                    if (p.out_dtype == NVFP4_OUT_BF16)
-                                        static_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(y4[q4]);
-                                    else
+                                    if (p.out_dtype == NVFP4_OUT_BF16) {
+                                        if (in_span(NV4_SITE(0), p.sp_out, static_cast<__nv_bfloat16 *>(p.out) + off, 2))
+                                            static_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(y4[q4]);
+                                    } else if (in_span(NV4_SITE(0), p.sp_out, static_cast<float *>(p.out) + off, 4)) {
                                         static_cast<float *>(p.out)[off] = y4[q4];
+                                    }
                                 }
                             }
                         }
@@ -1000,7 +1040,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                 epi_bar_sync();
                 if (threadIdx.x == 32 * EPI_FIRST_WARP)
                     for (int c = 1; c <= n_contrib; ++c)
-                        p.flags[blockIdx.x + c] = 0u;
+                        if (in_span(NV4_SITE(0), p.sp_flags, p.flags + blockIdx.x + c, 4))
+                            p.flags[blockIdx.x + c] = 0u;
                 continue;
             }
 #pragma unroll
@@ -1147,6 +1188,19 @@ cudaError_t launch_w4a4_dense(const DenseGemmArgs &g, cudaStream_t stream)
     const int tiles = p.m_tiles * p.n_tiles;
     // stream-K: one CTA per SM over all (tile, stage) units
     const int grid_units = g.streamk ? (int)std::min<int64_t>((int64_t)tiles * kstages, sms) : tiles;
+    p.sp_a_codes = span_of(g.a_codes, (uint64_t)g.a_rows * (uint64_t)(g.K / 2));
+    p.sp_sfa = span_of(g.a_scales, tiled_scale_bytes(g.a_rows, g.K));
+    p.sp_sfb = span_of(g.b_scales, tiled_scale_bytes(g.b_rows, g.K));
+    p.sp_b_second = span_of(g.b_second, 4);
+    p.sp_out = span_of(g.out, g.a_rows > 0 && g.b_rows > 0
+                                  ? (uint64_t)((g.a_rows - 1) * g.ld_i + (g.b_rows - 1) * g.ld_j + 1) * esz
+                                  : 0u);
+    if (g.streamk) {
+        p.sp_slots = span_of(g.slots, (uint64_t)grid_units * (uint64_t)p.slot_stride * 4u);
+        p.sp_flags = span_of(g.flags, (uint64_t)grid_units * 4u);
+    }
+    p.sp_yq_codes = span_of(g.yq_codes, (uint64_t)g.a_rows * (uint64_t)(g.b_rows / 2));
+    p.sp_yq_scales = span_of(g.yq_scales, tiled_scale_bytes(g.a_rows, g.b_rows));
     return dispatch(bn, false, p, grid_units, stream);
 }
 
@@ -1201,6 +1255,19 @@ cudaError_t launch_w4a4_grouped(const GroupedGemmArgs &g, cudaStream_t stream)
     p.total_rows = g.total_rows;
     p.status = g.status;
     p.timeout_ns = g.timeout_ns;
+    p.sp_a_codes = span_of(g.a_codes, (uint64_t)g.a_rows * (uint64_t)(g.K / 2));
+    p.sp_sfa = span_of(g.a_scales, tiled_scale_bytes(g.a_rows, g.K));
+    p.sp_sfb = span_of(g.w_scales, tiled_scale_bytes(g.E * g.N, g.K));
+    p.sp_b_second = span_of(g.w_second, 4u * (uint64_t)g.E);
+    const int64_t out_cols = g.epi == EPI_SWIGLU ? g.N / 2 : g.N;
+    const int64_t out_rows = g.epi == EPI_COMBINE ? g.comb_rows : g.total_rows;
+    p.sp_out = span_of(g.out, matrix_bytes(out_rows, out_cols, g.ldy, g.epi == EPI_COMBINE ? 4 : esz));
+    p.sp_yq_codes = span_of(g.yq_codes, (uint64_t)g.total_rows * (uint64_t)(g.N / 4));
+    p.sp_yq_scales = span_of(g.yq_scales, tiled_scale_bytes(g.total_rows, g.N / 2));
+    p.sp_comb_idx = span_of(g.comb_idx, 4u * (uint64_t)g.total_rows);
+    p.sp_comb_w = span_of(g.comb_w, 4u * (uint64_t)g.total_rows);
+    p.sp_offsets = span_of(g.offsets, 8u * (uint64_t)(g.E + 1));
+    p.sp_row_idx = span_of(g.row_idx, 4u * (uint64_t)g.total_rows);
     // upper bound of items: every expert's rows in tiles of 128, plus one partial tile per expert
     const int64_t max_tiles = ceil_div(g.total_rows, BM) + g.E;
     const int total = (int)std::min<int64_t>(max_tiles * p.n_tiles, 1 << 30);

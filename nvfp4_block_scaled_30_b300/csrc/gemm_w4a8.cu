@@ -83,6 +83,9 @@ struct Params {
     const int32_t *row_idx;   // null: routed row j reads activation row j
     int32_t E;
     int64_t total_rows;
+    // the bytes the call's arguments grant each tensor (tested before each
+    // plain access in the bounds-checked build)
+    Span sp_w_scales, sp_s_t, sp_w_second, sp_out, sp_a_fp8, sp_offsets, sp_row_idx;
 };
 
 struct Item {
@@ -94,6 +97,10 @@ struct Item {
 // made non-decreasing.
 __device__ __forceinline__ void expert_rows(const Params &p, int e, int64_t &lo, int64_t &hi)
 {
+    if (!in_span(NV4_SITE(0), p.sp_offsets, p.offsets + e, 16)) {
+        lo = hi = 0;
+        return;
+    }
     lo = min(max(p.offsets[e], (int64_t)0), p.total_rows);
     hi = min(max(p.offsets[e + 1], lo), p.total_rows);
 }
@@ -271,7 +278,9 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int64_t g = it.row0 + lane + 32 * q;
-                    const int r = g < it.row_end ? p.row_idx[g] : -1;
+                    const int r = g < it.row_end && in_span(NV4_SITE(0), p.sp_row_idx, p.row_idx + g, 4)
+                                      ? p.row_idx[g]
+                                      : -1;
                     live[q] = r >= 0 && r < p.M;
                     src[q] = live[q] ? r : 0;
                 }
@@ -295,10 +304,12 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
                 // op 0: A, 1: W codes, 2..2+NG-1: W scale atoms; lanes 8r.. serve steps r, r+4, ...
                 const int op = lane - 8 * (issued & 3);
                 if (op == 0 && !indexed)
-                    tma_load_2d(r, &p.tmap_a, ks * KSTEP, (int)it.row0, &raw_full[st]);
+                    tma_load_2d(r, &p.tmap_a, ks * KSTEP, (int)it.row0, &raw_full[st], RAW_A);
                 else if (op == 1)
-                    tma_load_2d(r + RAW_A, &p.tmap_w, ks * (KSTEP / 2), (int)w_row0, &raw_full[st]);
-                else if (op >= 2 && op < 2 + NG && g0 + op - 2 < p.w_groups)
+                    tma_load_2d(r + RAW_A, &p.tmap_w, ks * (KSTEP / 2), (int)w_row0, &raw_full[st], RAW_W);
+                else if (op >= 2 && op < 2 + NG && g0 + op - 2 < p.w_groups &&
+                         in_span(NV4_SITE(0), p.sp_w_scales,
+                                 p.w_scales + ((size_t)(g0 + op - 2) * p.k64_total + ks) * 512, 512))
                     bulk_load(r + RAW_A + RAW_W + (op - 2) * 512,
                               p.w_scales + ((size_t)(g0 + op - 2) * p.k64_total + ks) * 512, 512, &raw_full[st]);
                 if (indexed) {
@@ -309,8 +320,10 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
                     for (int q = 0; q < 4; ++q) {
                         const uint8_t *srow = p.a_fp8 + src[q] * p.K + (int64_t)ks * KSTEP;
 #pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            cp_async_16(r + (lane + 32 * q) * KSTEP + 16 * c, srow + 16 * c, live[q] ? 16u : 0u);
+                        for (int c = 0; c < 4; ++c) {
+                            const bool in = live[q] && in_span(NV4_SITE(0), p.sp_a_fp8, srow + 16 * c, 16);
+                            cp_async_16(r + (lane + 32 * q) * KSTEP + 16 * c, srow + 16 * c, in ? 16u : 0u);
+                        }
                     }
                     cp_async_arrive_noinc(&raw_full[st]);
                 }
@@ -479,10 +492,12 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
             const bool row_ok = i < it.row_end;
             int64_t tok = i;
             if (indexed && row_ok) {
-                const int r = p.row_idx[i];
+                const int r = in_span(NV4_SITE(0), p.sp_row_idx, p.row_idx + i, 4) ? p.row_idx[i] : -1;
                 tok = (r >= 0 && r < p.M) ? r : -1;
             }
-            const float alpha = (row_ok && tok >= 0) ? p.s_t[tok] * p.w_second[it.expert] : 0.0f;
+            const bool scales_in = row_ok && tok >= 0 && in_span(NV4_SITE(0), p.sp_s_t, p.s_t + tok, 4) &&
+                                   in_span(NV4_SITE(0), p.sp_w_second, p.w_second + it.expert, 4);
+            const float alpha = scales_in ? p.s_t[tok] * p.w_second[it.expert] : 0.0f;
             const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
             for (int c0 = chalf * (BN / 2); c0 < (chalf + 1) * (BN / 2); c0 += 32) {
                 uint32_t v[32];
@@ -493,6 +508,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
                     if (p.vec_ok && j0 + 32 <= p.N) {
                         if (p.out_dtype == NVFP4_OUT_BF16) {
                             uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + i * p.ldy + j0);
+                            if (!in_span(NV4_SITE(0), p.sp_out, o, 64))
+                                continue;
 #pragma unroll
                             for (int c = 0; c < 32; c += 8) {
                                 uint32_t w[4];
@@ -506,6 +523,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
                             }
                         } else {
                             float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + i * p.ldy + j0);
+                            if (!in_span(NV4_SITE(0), p.sp_out, o, 128))
+                                continue;
 #pragma unroll
                             for (int c = 0; c < 32; c += 4)
                                 o[c / 4] = make_float4(alpha * __uint_as_float(v[c]), alpha * __uint_as_float(v[c + 1]),
@@ -514,10 +533,13 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
                     } else {
                         for (int c = 0; c < 32 && j0 + c < p.N; ++c) {
                             const float y = alpha * __uint_as_float(v[c]);
-                            if (p.out_dtype == NVFP4_OUT_BF16)
-                                static_cast<__nv_bfloat16 *>(p.out)[i * p.ldy + j0 + c] = __float2bfloat16_rn(y);
-                            else
-                                static_cast<float *>(p.out)[i * p.ldy + j0 + c] = y;
+                            const int64_t off = i * p.ldy + j0 + c;
+                            if (p.out_dtype == NVFP4_OUT_BF16) {
+                                if (in_span(NV4_SITE(0), p.sp_out, static_cast<__nv_bfloat16 *>(p.out) + off, 2))
+                                    static_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(y);
+                            } else if (in_span(NV4_SITE(0), p.sp_out, static_cast<float *>(p.out) + off, 4)) {
+                                static_cast<float *>(p.out)[off] = y;
+                            }
                         }
                     }
                 }
@@ -580,6 +602,13 @@ cudaError_t launch_w4a8(const W4A8GemmArgs &g, cudaStream_t stream)
     p.row_idx = g.row_idx;
     p.E = g.E;
     p.total_rows = g.total_rows;
+    p.sp_w_scales = span_of(g.w_scales, tiled_scale_bytes(w_rows, g.K));
+    p.sp_s_t = span_of(g.s_t, 4u * (uint64_t)g.M);
+    p.sp_w_second = span_of(g.w_second, 4u * (uint64_t)(grouped ? g.E : 1));
+    p.sp_out = span_of(g.out, matrix_bytes(grouped ? g.total_rows : g.M, g.N, g.ldy, esz));
+    p.sp_a_fp8 = span_of(g.a_fp8, (uint64_t)g.M * (uint64_t)g.K);
+    p.sp_offsets = span_of(g.offsets, 8u * (uint64_t)(g.E + 1));
+    p.sp_row_idx = span_of(g.row_idx, 4u * (uint64_t)g.total_rows);
     auto kern = grouped ? w4a8_kernel<true> : w4a8_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess)

@@ -19,8 +19,34 @@ constexpr size_t WS_AMAX_BYTES = AMAX_MAX_CTAS * sizeof(uint32_t);
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+// Bytes of the MMA-tiled scale layout of rows x cols elements (atoms of 128
+// rows x 64 columns, 512 bytes each).
+inline uint64_t tiled_scale_bytes(int64_t rows, int64_t cols)
+{
+    return rows > 0 ? (uint64_t)ceil_div(rows, 128) * (uint64_t)(cols / 64) * 512u : 0u;
+}
+// Bytes of a rows x cols matrix of esz-byte elements with row pitch ld
+// (elements), the last row ending at its last element.
+inline uint64_t matrix_bytes(int64_t rows, int64_t cols, int64_t ld, int64_t esz)
+{
+    return rows > 0 && cols > 0 ? (uint64_t)((rows - 1) * ld + cols) * (uint64_t)esz : 0u;
+}
 
 int device_sm_count();
+
+// A byte range [lo, lo + bytes) of global memory that a call's arguments
+// grant a tensor (the bounds-checked build tests accesses against it).
+struct Span {
+    uint64_t lo = 0, bytes = 0;
+};
+
+__host__ __device__ __forceinline__ Span span_of(const void *p, uint64_t bytes)
+{
+    Span s;
+    s.lo = reinterpret_cast<uint64_t>(p);
+    s.bytes = p ? bytes : 0;
+    return s;
+}
 
 // Argument checks of an nvfp4_tensor shared by the entry points (null or
 // misaligned pointers, enums, sizes: NVFP4_ERR_INVALID_ARG; K not a multiple
@@ -59,6 +85,7 @@ cudaError_t launch_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K, in
 cudaError_t launch_fp8_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx, uint8_t *a, float *s_t,
                                 uint32_t *status, cudaStream_t stream);
 cudaError_t launch_fp4_mma_rate(int iters, uint64_t *cycles, cudaStream_t stream);
+cudaError_t launch_bounds_selftest(uint8_t *buf, uint64_t span_bytes, cudaStream_t stream);
 cudaError_t launch_probe_convert(const float *in, int64_t n, uint8_t *o2, uint8_t *o3, cudaStream_t stream);
 cudaError_t launch_finalize_bf16(const float *acc, int64_t rows, int64_t cols, int64_t ld_acc, uint16_t *y,
                                  int64_t ldy, cudaStream_t stream);
@@ -183,6 +210,7 @@ struct KvAppendArgs {
     int B, H_kv, max_pages, num_pages;
     uint8_t *pages;                // [num_pages][H_kv][page block]
     const float *k_scale, *v_scale;
+    Span sp_k_new, sp_v_new, sp_positions, sp_block_table, sp_pages, sp_k_scale, sp_v_scale; // set by the launch
 };
 cudaError_t launch_kv_append(const KvAppendArgs &a, cudaStream_t stream);
 
@@ -201,6 +229,7 @@ struct KvAttnArgs {
     float *partial;                // [B][H][n_splits][130] when n_splits > 1
     uint32_t *status;
     uint64_t timeout_ns;
+    Span sp_q, sp_ctx_lens, sp_block_table, sp_pages, sp_k_scale, sp_v_scale, sp_out, sp_partial; // set by the launch
 };
 size_t kv_attn_partial_bytes(int B, int H, int n_splits);
 // Context splits of one decode-attention call: one wave of ctas_per_sm CTAs

@@ -133,14 +133,21 @@ __global__ void kv_append_kernel(KvAppendArgs a)
     const int which = (int)((tid / nblk) % 2); // 0 key, 1 value
     const int hk = (int)((tid / (2 * nblk)) % a.H_kv);
     const int b = (int)(tid / (2 * nblk * a.H_kv));
+    if (!in_span(NV4_SITE(0), a.sp_positions, a.positions + b, 4))
+        return;
     const int pos = a.positions[b];
     if (pos < 0 || pos / KV_P >= a.max_pages)
+        return;
+    if (!in_span(NV4_SITE(0), a.sp_block_table, a.block_table + (int64_t)b * a.max_pages + pos / KV_P, 4))
         return;
     const int page = a.block_table[(int64_t)b * a.max_pages + pos / KV_P];
     if (page < 0 || page >= a.num_pages)
         return;
     const int slot = pos % KV_P;
     const uint16_t *src = (which ? a.v_new : a.k_new) + ((int64_t)b * a.H_kv + hk) * KV_D + blk * 16;
+    if (!in_span(NV4_SITE(0), which ? a.sp_v_new : a.sp_k_new, src, 32) ||
+        !in_span(NV4_SITE(0), which ? a.sp_v_scale : a.sp_k_scale, which ? a.v_scale : a.k_scale, 4))
+        return;
     float x[16];
     float amb = 0.0f;
 #pragma unroll
@@ -163,14 +170,16 @@ __global__ void kv_append_kernel(KvAppendArgs a)
 #pragma unroll
             for (int q = 0; q < 4; ++q)
                 wds[q] = c[4 * q] | (c[4 * q + 1] << 8) | (c[4 * q + 2] << 16) | (c[4 * q + 3] << 24);
-            *reinterpret_cast<uint4 *>(blk8 + (blk * 32 + kpos8(slot % 32)) * 16) =
-                make_uint4(wds[0], wds[1], wds[2], wds[3]);
+            uint8_t *dk = blk8 + (blk * 32 + kpos8(slot % 32)) * 16;
+            if (in_span(NV4_SITE(0), a.sp_pages, dk, 16))
+                *reinterpret_cast<uint4 *>(dk) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
         } else {
             const int sl = slot % 32;
             uint8_t *vc = blk8 + HALF8_BYTES + (sl >> 4) * (KV_D * 16) + (sl & 15);
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-                vc[(blk * 16 + i) * 16] = (uint8_t)c[i];
+                if (in_span(NV4_SITE(0), a.sp_pages, vc + (blk * 16 + i) * 16, 1))
+                    vc[(blk * 16 + i) * 16] = (uint8_t)c[i];
         }
         return;
     }
@@ -185,8 +194,11 @@ __global__ void kv_append_kernel(KvAppendArgs a)
         for (int i = 0; i < 8; ++i)
             pk[i >> 2] |= e2m1x2(__fmul_rn(x[2 * i], r), __fmul_rn(x[2 * i + 1], r)) << (8 * (i & 3));
         const int kp = kpos4(sl);
-        *reinterpret_cast<uint2 *>(pb + ((blk >> 1) * KV_H + kp) * 16 + (blk & 1) * 8) = make_uint2(pk[0], pk[1]);
-        pb[KS4_OFF + kp * (KV_D / 16) + blk] = (uint8_t)e;
+        uint8_t *dk = pb + ((blk >> 1) * KV_H + kp) * 16 + (blk & 1) * 8;
+        if (in_span(NV4_SITE(0), a.sp_pages, dk, 8))
+            *reinterpret_cast<uint2 *>(dk) = make_uint2(pk[0], pk[1]);
+        if (in_span(NV4_SITE(0), a.sp_pages, pb + KS4_OFF + kp * (KV_D / 16) + blk, 1))
+            pb[KS4_OFF + kp * (KV_D / 16) + blk] = (uint8_t)e;
     } else {
         uint8_t *vc = pb + VC4_OFF;
 #pragma unroll
@@ -196,10 +208,13 @@ __global__ void kv_append_kernel(KvAppendArgs a)
             for (int h = 0; h < 2; ++h) {
                 const uint32_t c = (two >> (4 * h)) & 15u;
                 uint8_t *p = vc + (blk * 16 + i + h) * (KV_H / 2) + sl / 2;
+                if (!in_span(NV4_SITE(0), a.sp_pages, p, 1))
+                    continue;
                 *p = (sl & 1) ? (uint8_t)((*p & 0x0Fu) | (c << 4)) : (uint8_t)((*p & 0xF0u) | c);
             }
         }
-        pb[VS4_OFF + blk * KV_H + sl] = (uint8_t)e;
+        if (in_span(NV4_SITE(0), a.sp_pages, pb + VS4_OFF + blk * KV_H + sl, 1))
+            pb[VS4_OFF + blk * KV_H + sl] = (uint8_t)e;
     }
 }
 
@@ -272,16 +287,20 @@ __device__ __forceinline__ void kv_merge_and_store(const KvAttnArgs &a, AttMerge
         const int64_t hq = (int64_t)b * a.H + hk * G + head;
         if (a.n_splits == 1) {
             const float y = L > 0.0f ? O * s_v / L : 0.0f;
-            if (a.out_dtype == NVFP4_OUT_BF16)
-                static_cast<__nv_bfloat16 *>(a.out)[hq * KV_D + d] = __float2bfloat16_rn(y);
-            else
+            if (a.out_dtype == NVFP4_OUT_BF16) {
+                if (in_span(NV4_SITE(0), a.sp_out, static_cast<__nv_bfloat16 *>(a.out) + hq * KV_D + d, 2))
+                    static_cast<__nv_bfloat16 *>(a.out)[hq * KV_D + d] = __float2bfloat16_rn(y);
+            } else if (in_span(NV4_SITE(0), a.sp_out, static_cast<float *>(a.out) + hq * KV_D + d, 4)) {
                 static_cast<float *>(a.out)[hq * KV_D + d] = y;
+            }
         } else {
             float *part = a.partial + (hq * a.n_splits + split) * (KV_D + 2);
-            part[d] = O;
-            if (d == 0) {
-                part[KV_D] = M;
-                part[KV_D + 1] = L;
+            if (in_span(NV4_SITE(0), a.sp_partial, part, (KV_D + 2) * 4)) {
+                part[d] = O;
+                if (d == 0) {
+                    part[KV_D] = M;
+                    part[KV_D + 1] = L;
+                }
             }
         }
     }
@@ -383,7 +402,8 @@ __global__ void __launch_bounds__(32 * ATT_WARPS, NT == 1 ? 4 : 3) kv_decode_ker
     const int g = lane >> 2, t = lane & 3;
     const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const int G = a.H / a.H_kv;
-    const int ctx = max(0, min(min(a.ctx_lens[b], a.max_ctx), a.max_pages * KV_P));
+    const int ctx_b = in_span(NV4_SITE(0), a.sp_ctx_lens, a.ctx_lens + b, 4) ? a.ctx_lens[b] : 0;
+    const int ctx = max(0, min(min(ctx_b, a.max_ctx), a.max_pages * KV_P));
     const int k_begin = split * a.keys_per_split;
     const int k_end = min(ctx, k_begin + a.keys_per_split);
     const int n_chunks = k_end > k_begin ? (k_end - k_begin + KV_H - 1) / KV_H : 0;
@@ -414,16 +434,19 @@ __global__ void __launch_bounds__(32 * ATT_WARPS, NT == 1 ? 4 : 3) kv_decode_ker
                     float v[4] = {0.f, 0.f, 0.f, 0.f};
                     if (head < G) {
                         const uint16_t *q = a.q + ((int64_t)b * a.H + hk * G + head) * KV_D + d0;
+                        if (in_span(NV4_SITE(0), a.sp_q, q, 8)) {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            v[i] = __uint_as_float((uint32_t)q[i] << 16) * qs;
+                            for (int i = 0; i < 4; ++i)
+                                v[i] = __uint_as_float((uint32_t)q[i] << 16) * qs;
+                        }
                     }
                     qf[2 * c + u][rr] = pack_h2(v[0], v[1]);
                     qf[2 * c + u][2 + rr] = pack_h2(v[2], v[3]);
                 }
             }
     }
-    const float s_k = *a.k_scale, s_v = *a.v_scale;
+    const float s_k = in_span(NV4_SITE(0), a.sp_k_scale, a.k_scale, 4) ? *a.k_scale : 0.0f;
+    const float s_v = in_span(NV4_SITE(0), a.sp_v_scale, a.v_scale, 4) ? *a.v_scale : 0.0f;
 
     // O^T accumulators: 8 m-tiles of 16 dimensions x NT n-tiles of 8 heads
     float o[8][NT][4];
@@ -442,20 +465,26 @@ __global__ void __launch_bounds__(32 * ATT_WARPS, NT == 1 ? 4 : 3) kv_decode_ker
     // warp: c = warp, warp + 4, ...; page ids of its first 32, one per lane
     int my_pg = 0;
     if (warp + ATT_WARPS * lane < n_chunks)
-        my_pg = a.block_table[(int64_t)b * a.max_pages + (k_begin + KV_H * (warp + ATT_WARPS * lane)) / KV_P];
+    {
+        const int32_t *bt = a.block_table + (int64_t)b * a.max_pages + (k_begin + KV_H * (warp + ATT_WARPS * lane)) / KV_P;
+        my_pg = in_span(NV4_SITE(0), a.sp_block_table, bt, 4) ? *bt : 0;
+    }
     // warp-collective (the page id comes from a shuffle); one copy per half page
     auto issue = [&](int c, int s) {
         const int i = (c - warp) / ATT_WARPS;
         const int tok = k_begin + KV_H * c;
         int page = __shfl_sync(0xFFFFFFFFu, my_pg, i & 31);
         if (i >= 32)
-            page = a.block_table[(int64_t)b * a.max_pages + tok / KV_P];
+            page = in_span(NV4_SITE(0), a.sp_block_table, a.block_table + (int64_t)b * a.max_pages + tok / KV_P, 4)
+                       ? a.block_table[(int64_t)b * a.max_pages + tok / KV_P]
+                       : 0;
         const int64_t ph = (int64_t)min(max(page, 0), a.num_pages - 1) * a.H_kv + hk;
         const int half = (tok / KV_H) & 1;
         if (lane == 0) {
             mbar_arrive_expect_tx(&sm.full[warp][s], HALF4_BYTES);
-            bulk_load(sm.unit[warp][s], a.pages + ph * PAGE_BYTES + half * HALF4_BYTES, HALF4_BYTES,
-                      &sm.full[warp][s]);
+            if (in_span(NV4_SITE(0), a.sp_pages, a.pages + ph * PAGE_BYTES + half * HALF4_BYTES, HALF4_BYTES))
+                bulk_load(sm.unit[warp][s], a.pages + ph * PAGE_BYTES + half * HALF4_BYTES, HALF4_BYTES,
+                          &sm.full[warp][s]);
         }
     };
     for (int i = 0; i < ATT_STAGES && warp + i * ATT_WARPS < n_chunks; ++i)
@@ -592,7 +621,8 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_fp8_kernel(const KvA
     const int g = lane >> 2, t = lane & 3;
     const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const int G = a.H / a.H_kv;
-    const int ctx = max(0, min(min(a.ctx_lens[b], a.max_ctx), a.max_pages * KV_P));
+    const int ctx_b = in_span(NV4_SITE(0), a.sp_ctx_lens, a.ctx_lens + b, 4) ? a.ctx_lens[b] : 0;
+    const int ctx = max(0, min(min(ctx_b, a.max_ctx), a.max_pages * KV_P));
     const int k_begin = split * a.keys_per_split;
     const int k_end = min(ctx, k_begin + a.keys_per_split);
     const int n_chunks = k_end > k_begin ? (k_end - k_begin + 31) / 32 : 0;
@@ -615,15 +645,18 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_fp8_kernel(const KvA
                 float v[4] = {0.f, 0.f, 0.f, 0.f};
                 if (head < G) {
                     const uint16_t *q = a.q + ((int64_t)b * a.H + hk * G + head) * KV_D + 16 * kk + 4 * t;
+                    if (in_span(NV4_SITE(0), a.sp_q, q, 8)) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        v[i] = __uint_as_float((uint32_t)q[i] << 16) * qs;
+                        for (int i = 0; i < 4; ++i)
+                            v[i] = __uint_as_float((uint32_t)q[i] << 16) * qs;
+                    }
                 }
                 qf[kk][rr] = pack_h2(v[0], v[1]);
                 qf[kk][2 + rr] = pack_h2(v[2], v[3]);
             }
     }
-    const float s_k = *a.k_scale, s_v = *a.v_scale;
+    const float s_k = in_span(NV4_SITE(0), a.sp_k_scale, a.k_scale, 4) ? *a.k_scale : 0.0f;
+    const float s_v = in_span(NV4_SITE(0), a.sp_v_scale, a.v_scale, 4) ? *a.v_scale : 0.0f;
     // O^T accumulators: 8 m-tiles of 16 dimensions x NT n-tiles of 8 heads
     float o[8][NT][4];
 #pragma unroll
@@ -641,20 +674,27 @@ __global__ void __launch_bounds__(32 * ATT_WARPS) kv_decode_fp8_kernel(const KvA
     // page ids of this warp's first 32 chunks, one per lane, read once
     int my_pg = 0;
     if (warp + ATT_WARPS * lane < n_chunks)
-        my_pg = a.block_table[(int64_t)b * a.max_pages + (k_begin + 32 * (warp + ATT_WARPS * lane)) / KV_P];
+    {
+        const int32_t *bt = a.block_table + (int64_t)b * a.max_pages + (k_begin + 32 * (warp + ATT_WARPS * lane)) / KV_P;
+        my_pg = in_span(NV4_SITE(0), a.sp_block_table, bt, 4) ? *bt : 0;
+    }
     // warp-collective (the page id comes from a shuffle); one copy per half page
     auto issue = [&](int c, int s) {
         const int i = (c - warp) / ATT_WARPS;
         const int tok = k_begin + 32 * c;
         int page = __shfl_sync(0xFFFFFFFFu, my_pg, i & 31);
         if (i >= 32)
-            page = a.block_table[(int64_t)b * a.max_pages + tok / KV_P];
+            page = in_span(NV4_SITE(0), a.sp_block_table, a.block_table + (int64_t)b * a.max_pages + tok / KV_P, 4)
+                       ? a.block_table[(int64_t)b * a.max_pages + tok / KV_P]
+                       : 0;
         const int64_t ph = (int64_t)min(max(page, 0), a.num_pages - 1) * a.H_kv + hk;
         const int half = (tok / 32) & 1;
         if (lane == 0) {
             mbar_arrive_expect_tx(&sm.full[warp][s], 2 * HALF8_BYTES);
-            bulk_load(sm.unit[warp][s], a.pages + ph * PAGE8_BYTES + half * (2 * HALF8_BYTES), 2 * HALF8_BYTES,
-                      &sm.full[warp][s]);
+            if (in_span(NV4_SITE(0), a.sp_pages, a.pages + ph * PAGE8_BYTES + half * (2 * HALF8_BYTES),
+                        2 * HALF8_BYTES))
+                bulk_load(sm.unit[warp][s], a.pages + ph * PAGE8_BYTES + half * (2 * HALF8_BYTES), 2 * HALF8_BYTES,
+                          &sm.full[warp][s]);
         }
     };
     for (int i = 0; i < ATT_STAGES && warp + i * ATT_WARPS < n_chunks; ++i)
@@ -741,6 +781,9 @@ __global__ void kv_combine_kernel(const KvAttnArgs a)
     const int64_t hq = blockIdx.x; // b * H + h
     const int d = threadIdx.x;
     const float *part = a.partial + hq * a.n_splits * (KV_D + 2);
+    if (!in_span(NV4_SITE(0), a.sp_partial, part, (uint64_t)a.n_splits * (KV_D + 2) * 4) ||
+        !in_span(NV4_SITE(0), a.sp_v_scale, a.v_scale, 4))
+        return;
     float M = -INFINITY;
     for (int s = 0; s < a.n_splits; ++s)
         M = fmaxf(M, part[s * (KV_D + 2) + KV_D]);
@@ -753,19 +796,30 @@ __global__ void kv_combine_kernel(const KvAttnArgs a)
             O += f * part[s * (KV_D + 2) + d];
         }
     const float y = L > 0.0f ? O * *a.v_scale / L : 0.0f;
-    if (a.out_dtype == NVFP4_OUT_BF16)
-        static_cast<__nv_bfloat16 *>(a.out)[hq * KV_D + d] = __float2bfloat16_rn(y);
-    else
+    if (a.out_dtype == NVFP4_OUT_BF16) {
+        if (in_span(NV4_SITE(0), a.sp_out, static_cast<__nv_bfloat16 *>(a.out) + hq * KV_D + d, 2))
+            static_cast<__nv_bfloat16 *>(a.out)[hq * KV_D + d] = __float2bfloat16_rn(y);
+    } else if (in_span(NV4_SITE(0), a.sp_out, static_cast<float *>(a.out) + hq * KV_D + d, 4)) {
         static_cast<float *>(a.out)[hq * KV_D + d] = y;
+    }
 }
 
 } // namespace
 
-cudaError_t launch_kv_append(const KvAppendArgs &a, cudaStream_t stream)
+cudaError_t launch_kv_append(const KvAppendArgs &args, cudaStream_t stream)
 {
-    const int64_t threads = (int64_t)a.B * a.H_kv * 2 * (KV_D / 16);
+    const int64_t threads = (int64_t)args.B * args.H_kv * 2 * (KV_D / 16);
     if (threads == 0)
         return cudaSuccess;
+    KvAppendArgs a = args;
+    const uint64_t page_bytes = a.fmt == KV_FMT_FP8 ? PAGE8_BYTES : PAGE_BYTES;
+    a.sp_k_new = span_of(a.k_new, 2u * (uint64_t)a.B * a.H_kv * KV_D);
+    a.sp_v_new = span_of(a.v_new, 2u * (uint64_t)a.B * a.H_kv * KV_D);
+    a.sp_positions = span_of(a.positions, 4u * (uint64_t)a.B);
+    a.sp_block_table = span_of(a.block_table, 4u * (uint64_t)a.B * a.max_pages);
+    a.sp_pages = span_of(a.pages, page_bytes * (uint64_t)a.num_pages * a.H_kv);
+    a.sp_k_scale = span_of(a.k_scale, 4);
+    a.sp_v_scale = span_of(a.v_scale, 4);
     kv_append_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(a);
     return cudaGetLastError();
 }
@@ -796,8 +850,18 @@ size_t kv_attn_partial_bytes(int B, int H, int n_splits)
     return n_splits > 1 ? (size_t)B * H * n_splits * (KV_D + 2) * sizeof(float) : 0;
 }
 
-cudaError_t launch_kv_decode(const KvAttnArgs &a, cudaStream_t stream)
+cudaError_t launch_kv_decode(const KvAttnArgs &args, cudaStream_t stream)
 {
+    KvAttnArgs a = args;
+    const uint64_t page_bytes = a.fmt == KV_FMT_FP8 ? PAGE8_BYTES : PAGE_BYTES;
+    a.sp_q = span_of(a.q, 2u * (uint64_t)a.B * a.H * KV_D);
+    a.sp_ctx_lens = span_of(a.ctx_lens, 4u * (uint64_t)a.B);
+    a.sp_block_table = span_of(a.block_table, 4u * (uint64_t)a.B * a.max_pages);
+    a.sp_pages = span_of(a.pages, page_bytes * (uint64_t)a.num_pages * a.H_kv);
+    a.sp_k_scale = span_of(a.k_scale, 4);
+    a.sp_v_scale = span_of(a.v_scale, 4);
+    a.sp_out = span_of(a.out, (a.out_dtype == NVFP4_OUT_BF16 ? 2u : 4u) * (uint64_t)a.B * a.H * KV_D);
+    a.sp_partial = span_of(a.partial, kv_attn_partial_bytes(a.B, a.H, a.n_splits));
     const size_t smem = a.fmt == KV_FMT_FP8 ? sizeof(AttSmem8) : sizeof(AttSmem4);
     cudaError_t e;
     // one n-tile of 8 heads when a group has at most 8 query heads, else two

@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda.h>
 
+#include "bounds.cuh"
+
 namespace nv4 {
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -87,6 +89,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
 // are filled with zeros.
 __device__ __forceinline__ void cp_async_16(void *dst, const void *src, uint32_t src_bytes)
 {
+    if (!(in_dyn_smem(NV4_SITE(1), smem_u32(dst), 16) && aligned_to(NV4_SITE(1), smem_u32(dst), 16) &&
+          in_bounds(NV4_SITE(1), src_bytes, 17)))
+        return;
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
                  : "memory");
 }
@@ -94,6 +99,9 @@ __device__ __forceinline__ void cp_async_16(void *dst, const void *src, uint32_t
 // 4-byte cp.async (src_bytes 0 or 4; 0 zero-fills the destination).
 __device__ __forceinline__ void cp_async_4(void *dst, const void *src, uint32_t src_bytes)
 {
+    if (!(in_dyn_smem(NV4_SITE(1), smem_u32(dst), 4) && aligned_to(NV4_SITE(1), smem_u32(dst), 4) &&
+          in_bounds(NV4_SITE(1), src_bytes, 5)))
+        return;
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
                  : "memory");
 }
@@ -112,9 +120,15 @@ __device__ __forceinline__ void cp_async_wait_all()
 
 // ---- TMA / bulk copies ----------------------------------------------------------
 
+// 2-D tiled copy of the box at (x, y) of a byte-element tensor map; box_bytes
+// is the box's size in shared memory (checked in the bounds-checked build,
+// with x a multiple of 16 and dst 128-byte aligned).
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int32_t x, int32_t y,
-                                            uint64_t *bar)
+                                            uint64_t *bar, uint32_t box_bytes)
 {
+    if (!(in_dyn_smem(NV4_SITE(1), smem_u32(dst), box_bytes) && aligned_to(NV4_SITE(1), smem_u32(dst), 128) &&
+          aligned_to(NV4_SITE(1), (uint32_t)x, 16)))
+        return;
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
@@ -203,6 +217,9 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes
 // 1-D bulk copy global -> shared; both addresses 16-byte aligned, bytes % 16 == 0.
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
 {
+    if (!(in_dyn_smem(NV4_SITE(1), smem_u32(dst), bytes) && aligned_to(NV4_SITE(1), smem_u32(dst), 16) &&
+          aligned_to(NV4_SITE(1), reinterpret_cast<uint64_t>(src), 16) && aligned_to(NV4_SITE(1), bytes, 16)))
+        return;
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      smem_u32(dst)),
                  "l"(src), "r"(bytes), "r"(smem_u32(bar))
@@ -244,11 +261,34 @@ __device__ __forceinline__ void tc_fence_after()
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// Bounds-checked build: the TMEM columns [col, col + n) of taddr lie within
+// the 512 columns, and the operand tiles that the descriptors address (128
+// rows of A, N rows of B, 128 bytes each, from the 1024-byte aligned tile
+// base) lie in dynamic shared memory.
+__device__ __forceinline__ bool tmem_cols_ok(uint32_t site, uint32_t taddr, uint32_t n)
+{
+    return in_bounds(site, (taddr & 0xFFFFu) + n - 1, 512) && in_bounds(site, taddr >> 16, 128);
+}
+
+__device__ __forceinline__ bool mma_operands_ok(uint32_t site, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                uint32_t idesc)
+{
+    if (!kCheckBounds)
+        return true;
+    const uint32_t n = ((idesc >> 17) & 0x3Fu) << 3;
+    const uint32_t a0 = ((uint32_t)(adesc & 0x3FFFu) << 4) & ~1023u;
+    const uint32_t b0 = ((uint32_t)(bdesc & 0x3FFFu) << 4) & ~1023u;
+    return tmem_cols_ok(site, d_tmem, n) && in_dyn_smem(site, a0, 128 * 128) && in_dyn_smem(site, b0, n * 128);
+}
+
 // Single thread: D(tmem) (+)= A(smem) x B(smem)^T, block-scaled E2M1 x E2M1
 // with UE4M3 scales per 16 elements of K (K = 64 per instruction).
 __device__ __forceinline__ void mma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                              uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
 {
+    if (!(mma_operands_ok(NV4_SITE(1), d_tmem, adesc, bdesc, idesc) && tmem_cols_ok(NV4_SITE(1), sfa_tmem, 1) &&
+          tmem_cols_ok(NV4_SITE(1), sfb_tmem, 1)))
+        return;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %6, 0;\n\t"
@@ -263,6 +303,8 @@ __device__ __forceinline__ void mma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc, ui
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t accumulate)
 {
+    if (!mma_operands_ok(NV4_SITE(1), d_tmem, adesc, bdesc, idesc))
+        return;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
@@ -275,6 +317,9 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
 // 0..31 of 4 consecutive columns, replicated into all four lane quarters.
 __device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc)
 {
+    if (!(tmem_cols_ok(NV4_SITE(1), taddr, 4) &&
+          in_dyn_smem(NV4_SITE(1), (uint32_t)(sdesc & 0x3FFFu) << 4, 512)))
+        return;
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
@@ -290,6 +335,11 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar)
 // Whole warp: 32 consecutive fp32 columns of this warp's 32 TMEM lanes.
 __device__ __forceinline__ void tc_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32])
 {
+    if (!tmem_cols_ok(NV4_SITE(1), taddr, 32)) { // taddr is the same in every lane
+        for (int c = 0; c < 32; ++c)
+            r[c] = 0u;
+        return;
+    }
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
         "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
@@ -304,6 +354,11 @@ __device__ __forceinline__ void tc_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[3
 // Whole warp: 16 consecutive fp32 columns of this warp's 32 TMEM lanes.
 __device__ __forceinline__ void tc_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16])
 {
+    if (!tmem_cols_ok(NV4_SITE(1), taddr, 16)) {
+        for (int c = 0; c < 16; ++c)
+            r[c] = 0u;
+        return;
+    }
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
         "%15}, [%16];"

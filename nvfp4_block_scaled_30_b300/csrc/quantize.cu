@@ -34,6 +34,14 @@ namespace {
 constexpr int QT = 256; // threads per quantiser CTA
 constexpr unsigned FULL = 0xFFFFFFFFu;
 
+// The bytes a quantiser call's arguments grant each tensor (tested before
+// each plain access in the bounds-checked build): x, codes (FP8 values for
+// the per-token quantiser), scales (s_t), the second-level scale or macro
+// scales, and the partial maxima.
+struct QuantSpans {
+    Span x, codes, scales, second, partial;
+};
+
 __device__ __forceinline__ void bf16x8(const uint16_t *p, float (&f)[8])
 {
     uint4 v = __ldg(reinterpret_cast<const uint4 *>(p));
@@ -124,7 +132,7 @@ __device__ __forceinline__ void absmax_bits(const uint4 v, uint32_t &m, uint32_t
 // Zero scales of the tiled layout's padding rows rows..rows_pad: one 32-bit
 // word = one row's 4 scales of a 64-element chunk.
 __device__ __forceinline__ void zero_pad_scales(uint8_t *scales, int64_t rows, int64_t rows_pad, int64_t K,
-                                                int64_t first, int64_t stride)
+                                                int64_t first, int64_t stride, const QuantSpans &sp)
 {
     // fewer than 128 padding rows: 32-bit index arithmetic suffices
     const uint32_t k64 = (uint32_t)(K / 64);
@@ -134,7 +142,8 @@ __device__ __forceinline__ void zero_pad_scales(uint8_t *scales, int64_t rows, i
         const uint32_t q = (uint32_t)i / k64, c = (uint32_t)i - q * k64;
         const uint32_t r = (uint32_t)(rows & 127) + q;
         const size_t off = ((size_t)tile0 * k64 + c) * 512 + (r & 31) * 16 + (r >> 5) * 4;
-        *reinterpret_cast<uint32_t *>(scales + off) = 0u;
+        if (in_span(NV4_SITE(0), sp.scales, scales + off, 4))
+            *reinterpret_cast<uint32_t *>(scales + off) = 0u;
     }
 }
 
@@ -142,7 +151,7 @@ __device__ __forceinline__ void zero_pad_scales(uint8_t *scales, int64_t rows, i
 // codes and scale of chunk (row, j) of f under second-level scale sg.
 template <bool TILED>
 __device__ __forceinline__ void encode_chunk(const float (&f)[8], bool real, int64_t row, int64_t j, int64_t K,
-                                             float sg, uint8_t *codes, uint8_t *scales)
+                                             float sg, uint8_t *codes, uint8_t *scales, const QuantSpans &sp)
 {
     float am = 0.0f;
 #pragma unroll
@@ -152,8 +161,10 @@ __device__ __forceinline__ void encode_chunk(const float (&f)[8], bool real, int
     const uint32_t e = real ? block_scale_code(amb, sg) : 0u;
     const float r = recip_step(__fmul_rn(e4m3_value(e), sg));
     if (real) {
-        *reinterpret_cast<uint32_t *>(codes + row * (K / 2) + j * 4) = pack8(f, r);
-        if ((threadIdx.x & 1) == 0)
+        const uint32_t pk = pack8(f, r);
+        if (in_span(NV4_SITE(0), sp.codes, codes + row * (K / 2) + j * 4, 4))
+            *reinterpret_cast<uint32_t *>(codes + row * (K / 2) + j * 4) = pk;
+        if ((threadIdx.x & 1) == 0 && in_span(NV4_SITE(0), sp.scales, scales + scale_offset(row, j >> 1, K, TILED), 1))
             scales[scale_offset(row, j >> 1, K, TILED)] = (uint8_t)e;
     }
 }
@@ -179,7 +190,7 @@ __device__ __forceinline__ void mul2_rn(float a0, float a1, float r, float &p0, 
 // one 8-byte code store plus one scale byte.
 template <bool TILED>
 __device__ __forceinline__ void encode_block16(const uint32_t (&w)[8], int64_t row, int64_t blk, int64_t K, float sg,
-                                               uint8_t *codes, uint8_t *scales)
+                                               uint8_t *codes, uint8_t *scales, const QuantSpans &sp)
 {
     uint32_t m2 = 0;
 #pragma unroll
@@ -201,8 +212,10 @@ __device__ __forceinline__ void encode_block16(const uint32_t (&w)[8], int64_t r
         }
         pk[h] = p;
     }
-    *reinterpret_cast<uint2 *>(codes + row * (K / 2) + blk * 8) = make_uint2(pk[0], pk[1]);
-    scales[scale_offset(row, blk, K, TILED)] = (uint8_t)e;
+    if (in_span(NV4_SITE(0), sp.codes, codes + row * (K / 2) + blk * 8, 8))
+        *reinterpret_cast<uint2 *>(codes + row * (K / 2) + blk * 8) = make_uint2(pk[0], pk[1]);
+    if (in_span(NV4_SITE(0), sp.scales, scales + scale_offset(row, blk, K, TILED), 1))
+        scales[scale_offset(row, blk, K, TILED)] = (uint8_t)e;
 }
 
 // One 16-value block (32 bytes) of x.  With V8 the block is 32-byte aligned
@@ -239,7 +252,7 @@ __device__ __forceinline__ void load_block16(const uint16_t *p, uint32_t (&w)[8]
 template <bool V8>
 __global__ void __launch_bounds__(QT) amax_partial_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t K,
                                                           int64_t ldx, uint32_t *__restrict__ partial,
-                                                          uint32_t *__restrict__ status)
+                                                          uint32_t *__restrict__ status, const QuantSpans sp)
 {
     __shared__ uint32_t red[QT / 32];
     // launched as a programmatic dependent: wait for the previous grid (it
@@ -261,7 +274,7 @@ __global__ void __launch_bounds__(QT) amax_partial_kernel(const uint16_t *__rest
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 w[u][i] = 0u;
-            if (base + (int64_t)u * QT < total)
+            if (base + (int64_t)u * QT < total && in_span(NV4_SITE(0), sp.x, x + c.row * ldx + c.j * 16, 32))
                 load_block16<V8, true>(x + c.row * ldx + c.j * 16, w[u]);
             cursor_advance(c, qs, rs, bpr);
         }
@@ -276,7 +289,7 @@ __global__ void __launch_bounds__(QT) amax_partial_kernel(const uint16_t *__rest
     // a non-finite value has the largest magnitude bits (>= 0x7F80)
     bad = __any_sync(FULL, m >= 0x7F80u);
     uint32_t bm = block_max_u32(m, red);
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0 && in_span(NV4_SITE(0), sp.partial, partial + blockIdx.x, 4))
         partial[blockIdx.x] = bm;
     if (bad && (threadIdx.x & 31) == 0)
         atomicOr(status, ST_NONFINITE);
@@ -293,17 +306,18 @@ __global__ void __launch_bounds__(QT) nvfp4_encode_kernel(const uint16_t *__rest
                                                           uint8_t *__restrict__ codes, uint8_t *__restrict__ scales,
                                                           float *__restrict__ sg_out,
                                                           const uint32_t *__restrict__ partial, int n_partial,
-                                                          int zero_pad)
+                                                          int zero_pad, const QuantSpans sp)
 {
     __shared__ uint32_t red[QT / 32];
     pdl_wait(); // the partial maxima of pass 1
     pdl_trigger();
     uint32_t m = 0;
     for (int i = threadIdx.x; i < n_partial; i += QT)
-        m = max(m, partial[i]);
+        if (in_span(NV4_SITE(0), sp.partial, partial + i, 4))
+            m = max(m, partial[i]);
     const float amax = __uint_as_float(block_max_u32(m, red) << 16);
     const float sg = __fdiv_rn(amax, 2688.0f);
-    if (blockIdx.x == 0 && threadIdx.x == 0)
+    if (blockIdx.x == 0 && threadIdx.x == 0 && in_span(NV4_SITE(0), sp.second, sg_out, 4))
         *sg_out = sg;
 
     // one thread per 16-element block (two 16-byte loads), QB blocks in
@@ -327,19 +341,20 @@ __global__ void __launch_bounds__(QT) nvfp4_encode_kernel(const uint16_t *__rest
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 v[u][i] = 0u;
-            if (base + (int64_t)u * QT < total)
+            if (base + (int64_t)u * QT < total && in_span(NV4_SITE(0), sp.x, x + c[u].row * ldx + c[u].j * 16, 32))
                 load_block16<V8, false>(x + c[u].row * ldx + c[u].j * 16, v[u]);
         }
 #pragma unroll
         for (int u = 0; u < QB; ++u) {
             if (base + (int64_t)u * QT >= total)
                 continue;
-            encode_block16<TILED>(v[u], c[u].row, c[u].j, K, sg, codes, scales);
+            encode_block16<TILED>(v[u], c[u].row, c[u].j, K, sg, codes, scales, sp);
         }
         cursor_advance(cur, qi, ri, bpr);
     }
     if (TILED && zero_pad)
-        zero_pad_scales(scales, rows, rows_pad, K, (int64_t)blockIdx.x * QT + threadIdx.x, (int64_t)gridDim.x * QT);
+        zero_pad_scales(scales, rows, rows_pad, K, (int64_t)blockIdx.x * QT + threadIdx.x, (int64_t)gridDim.x * QT,
+                        sp);
 }
 
 // ---- staged streaming passes (contiguous x) ----------------------------------
@@ -365,6 +380,9 @@ constexpr int su_smem(int stages) { return stages * SU_BYTES + 2 * stages * 8 + 
 __device__ __forceinline__ void bulk_load_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
                                                uint64_t policy)
 {
+    if (!(in_dyn_smem(NV4_SITE(0), smem_u32(dst), bytes) && aligned_to(NV4_SITE(0), smem_u32(dst), 16) &&
+          aligned_to(NV4_SITE(0), reinterpret_cast<uint64_t>(src), 16) && aligned_to(NV4_SITE(0), bytes, 16)))
+        return;
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, "
                  "[%3], %4;" ::"r"(smem_u32(dst)),
                  "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
@@ -433,7 +451,7 @@ __global__ void __launch_bounds__(SU_THREADS) stream_quant_kernel(const uint16_t
                                                                   float *__restrict__ sg_out,
                                                                   uint32_t *__restrict__ partial, int n_partial,
                                                                   int zero_pad, uint32_t *__restrict__ status,
-                                                                  uint64_t timeout_ns)
+                                                                  uint64_t timeout_ns, const QuantSpans sp)
 {
     extern __shared__ __align__(128) uint8_t sq[];
     uint64_t *full = reinterpret_cast<uint64_t *>(sq + SU_STAGES * SU_BYTES);
@@ -474,7 +492,8 @@ __global__ void __launch_bounds__(SU_THREADS) stream_quant_kernel(const uint16_t
                 }
                 const int64_t nb = min((int64_t)SU_BLOCKS, total - u * SU_BLOCKS);
                 mbar_arrive_expect_tx(&full[s], (uint32_t)(nb * 32));
-                bulk_load_hint(sq + s * SU_BYTES, x + u * SU_BLOCKS * 16, (uint32_t)(nb * 32), &full[s], pol);
+                if (in_span(NV4_SITE(0), sp.x, x + u * SU_BLOCKS * 16, (uint64_t)(nb * 32)))
+                    bulk_load_hint(sq + s * SU_BYTES, x + u * SU_BLOCKS * 16, (uint32_t)(nb * 32), &full[s], pol);
                 ++issued;
                 if (++s == SU_STAGES) {
                     s = 0;
@@ -500,10 +519,11 @@ __global__ void __launch_bounds__(SU_THREADS) stream_quant_kernel(const uint16_t
     if (PASS == 2) {
         uint32_t m = 0;
         for (int i = t; i < n_partial; i += SU_CONSUMERS)
-            m = max(m, partial[i]);
+            if (in_span(NV4_SITE(0), sp.partial, partial + i, 4))
+                m = max(m, partial[i]);
         const float amax = __uint_as_float(consumers_max(m, red) << 16);
         sg = __fdiv_rn(amax, 2688.0f);
-        if (blockIdx.x == 0 && t == 0)
+        if (blockIdx.x == 0 && t == 0 && in_span(NV4_SITE(0), sp.second, sg_out, 4))
             *sg_out = sg;
         fast = sg >= 0x1p-100f && sg <= 0x1p100f;
         if (t < 128) {
@@ -570,8 +590,11 @@ __global__ void __launch_bounds__(SU_THREADS) stream_quant_kernel(const uint16_t
                     }
                     // codes are contiguous: block b's 8 bytes sit at 8 b
                     const int64_t b = u * SU_BLOCKS + slot;
-                    *reinterpret_cast<uint2 *>(codes + b * 8) = make_uint2(pk[0], pk[1]);
-                    scales[TILED ? scale_offset(cur[k].row, cur[k].j, K, true) : (size_t)b] = (uint8_t)e;
+                    if (in_span(NV4_SITE(0), sp.codes, codes + b * 8, 8))
+                        *reinterpret_cast<uint2 *>(codes + b * 8) = make_uint2(pk[0], pk[1]);
+                    const size_t so = TILED ? scale_offset(cur[k].row, cur[k].j, K, true) : (size_t)b;
+                    if (in_span(NV4_SITE(0), sp.scales, scales + so, 1))
+                        scales[so] = (uint8_t)e;
                 }
             }
             cursor_advance(cur[k], qi, ri, bpr);
@@ -588,13 +611,13 @@ __global__ void __launch_bounds__(SU_THREADS) stream_quant_kernel(const uint16_t
         const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
         const bool bad = __any_sync(FULL, m >= 0x7F80u);
         const uint32_t bm = consumers_max(m, red);
-        if (t == 0)
+        if (t == 0 && in_span(NV4_SITE(0), sp.partial, partial + blockIdx.x, 4))
             partial[blockIdx.x] = bm;
         if (bad && lane == 0)
             atomicOr(status, ST_NONFINITE);
     } else if (TILED && zero_pad) {
         zero_pad_scales(scales, rows, rows_pad, K, (int64_t)blockIdx.x * SU_CONSUMERS + t,
-                        (int64_t)gridDim.x * SU_CONSUMERS);
+                        (int64_t)gridDim.x * SU_CONSUMERS, sp);
     }
 }
 
@@ -614,7 +637,8 @@ __global__ void __launch_bounds__(FT) nvfp4_encode_small_kernel(const uint16_t *
                                                                 uint8_t *__restrict__ codes,
                                                                 uint8_t *__restrict__ scales,
                                                                 float *__restrict__ sg_out,
-                                                                uint32_t *__restrict__ status, int zero_pad)
+                                                                uint32_t *__restrict__ status, int zero_pad,
+                                                                const QuantSpans sp)
 {
     __shared__ uint32_t red[FT / 32];
     __shared__ uint32_t cta_max[FC];
@@ -637,7 +661,8 @@ __global__ void __launch_bounds__(FT) nvfp4_encode_small_kernel(const uint16_t *
         const int idx = first + k * STEP;
         if (idx < total) {
             const int row = idx / cpr, j = idx - row * cpr;
-            v[k] = __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)row * ldx + j * 8));
+            if (in_span(NV4_SITE(0), sp.x, x + (int64_t)row * ldx + j * 8, 16))
+                v[k] = __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)row * ldx + j * 8));
         }
     }
 #pragma unroll
@@ -667,7 +692,7 @@ __global__ void __launch_bounds__(FT) nvfp4_encode_small_kernel(const uint16_t *
         g = max(g, cta_max[c]);
     const float amax = __uint_as_float(g << 16);
     const float sg = __fdiv_rn(amax, 2688.0f);
-    if (rank == 0 && threadIdx.x == 0)
+    if (rank == 0 && threadIdx.x == 0 && in_span(NV4_SITE(0), sp.second, sg_out, 4))
         *sg_out = sg;
 #pragma unroll
     for (int k = 0; k < FQ; ++k) {
@@ -678,10 +703,10 @@ __global__ void __launch_bounds__(FT) nvfp4_encode_small_kernel(const uint16_t *
         const int row = real ? idx / cpr : 0, j = real ? idx - row * cpr : 0;
         float f[8];
         bf16x8_of(v[k], f);
-        encode_chunk<TILED>(f, real, row, j, K, sg, codes, scales);
+        encode_chunk<TILED>(f, real, row, j, K, sg, codes, scales, sp);
     }
     if (TILED && zero_pad)
-        zero_pad_scales(scales, rows, rows_pad, K, first, STEP);
+        zero_pad_scales(scales, rows, rows_pad, K, first, STEP, sp);
 }
 
 // Macro mode: one warp covers 32 chunks = 256 elements = one macro group (K is
@@ -692,7 +717,7 @@ __global__ void __launch_bounds__(QT) nvfp4_encode_macro_kernel(const uint16_t *
                                                                 uint8_t *__restrict__ codes,
                                                                 uint8_t *__restrict__ scales,
                                                                 uint16_t *__restrict__ macro,
-                                                                uint32_t *__restrict__ status)
+                                                                uint32_t *__restrict__ status, const QuantSpans sp)
 {
     const int64_t cpr = K / 8;
     uint32_t bad = 0;
@@ -703,7 +728,7 @@ __global__ void __launch_bounds__(QT) nvfp4_encode_macro_kernel(const uint16_t *
             const bool valid = j < cpr;
             const bool real = valid && real_row;
             float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            if (real) {
+            if (real && in_span(NV4_SITE(0), sp.x, x + row * ldx + j * 8, 16)) {
                 bf16x8(x + row * ldx + j * 8, f);
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
@@ -725,11 +750,14 @@ __global__ void __launch_bounds__(QT) nvfp4_encode_macro_kernel(const uint16_t *
             const uint32_t e = real ? block_scale_code(amb, S) : 0u;
             const float r = recip_step(__fmul_rn(e4m3_value(e), S));
             if (real) {
-                *reinterpret_cast<uint32_t *>(codes + row * (K / 2) + j * 4) = pack8(f, r);
-                if ((threadIdx.x & 31) == 0)
+                const uint32_t pk = pack8(f, r);
+                if (in_span(NV4_SITE(0), sp.codes, codes + row * (K / 2) + j * 4, 4))
+                    *reinterpret_cast<uint32_t *>(codes + row * (K / 2) + j * 4) = pk;
+                if ((threadIdx.x & 31) == 0 && in_span(NV4_SITE(0), sp.second, macro + row * (K / 256) + (j >> 5), 2))
                     macro[row * (K / 256) + (j >> 5)] = __half_as_ushort(h);
             }
-            if (valid && (threadIdx.x & 1) == 0)
+            if (valid && (threadIdx.x & 1) == 0 &&
+                in_span(NV4_SITE(0), sp.scales, scales + scale_offset(row, j >> 1, K, TILED), 1))
                 scales[scale_offset(row, j >> 1, K, TILED)] = (uint8_t)e;
         }
     }
@@ -746,7 +774,8 @@ __device__ __forceinline__ uint32_t e4m3_signed(float v)
 // pass 2 (re-reading the row from L1/L2) encodes 8 elements per thread.
 __global__ void __launch_bounds__(QT) fp8_token_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t K,
                                                        int64_t ldx, uint8_t *__restrict__ a,
-                                                       float *__restrict__ s_t, uint32_t *__restrict__ status)
+                                                       float *__restrict__ s_t, uint32_t *__restrict__ status,
+                                                       const QuantSpans sp)
 {
     __shared__ uint32_t red[QT / 32];
     const int64_t cpr = K / 8;
@@ -754,7 +783,8 @@ __global__ void __launch_bounds__(QT) fp8_token_kernel(const uint16_t *__restric
         const uint16_t *xr = x + row * ldx;
         uint32_t m = 0, bad = 0;
         for (int64_t j = threadIdx.x; j < cpr; j += QT) {
-            uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr + j * 8));
+            const uint4 v = in_span(NV4_SITE(0), sp.x, xr + j * 8, 16) ? __ldg(reinterpret_cast<const uint4 *>(xr + j * 8))
+                                                                       : make_uint4(0u, 0u, 0u, 0u);
             uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -768,26 +798,31 @@ __global__ void __launch_bounds__(QT) fp8_token_kernel(const uint16_t *__restric
         const float amax = __uint_as_float(block_max_u32(m, red) << 16);
         const float s = __fdiv_rn(amax, 448.0f);
         const float r = recip_step(s);
-        if (threadIdx.x == 0)
+        if (threadIdx.x == 0 && in_span(NV4_SITE(0), sp.scales, s_t + row, 4))
             s_t[row] = s;
         for (int64_t j = threadIdx.x; j < cpr; j += QT) {
-            float f[8];
-            bf16x8(xr + j * 8, f);
+            float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            if (in_span(NV4_SITE(0), sp.x, xr + j * 8, 16))
+                bf16x8(xr + j * 8, f);
             uint32_t lo = 0, hi = 0;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 lo |= e4m3_signed(__fmul_rn(f[i], r)) << (8 * i);
                 hi |= e4m3_signed(__fmul_rn(f[4 + i], r)) << (8 * i);
             }
-            *reinterpret_cast<uint2 *>(a + row * K + j * 8) = make_uint2(lo, hi);
+            if (in_span(NV4_SITE(0), sp.codes, a + row * K + j * 8, 8))
+                *reinterpret_cast<uint2 *>(a + row * K + j * 8) = make_uint2(lo, hi);
         }
     }
 }
 
 __global__ void probe_convert_kernel(const float *__restrict__ in, int64_t n, uint8_t *__restrict__ o2,
-                                     uint8_t *__restrict__ o3)
+                                     uint8_t *__restrict__ o3, const QuantSpans sp)
 {
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        if (!(in_span(NV4_SITE(0), sp.x, in + i, 4) && in_span(NV4_SITE(0), sp.codes, o2 + i, 1) &&
+              in_span(NV4_SITE(0), sp.scales, o3 + i, 1)))
+            continue;
         const float v = in[i];
         o2[i] = (uint8_t)(e2m1x2(v, 0.0f) & 0xFu);
         o3[i] = (uint8_t)e4m3_signed(v);
@@ -796,12 +831,13 @@ __global__ void probe_convert_kernel(const float *__restrict__ in, int64_t n, ui
 
 // Split-K epilogue for BF16 outputs: y = bf16_rn(acc).
 __global__ void finalize_bf16_kernel(const float *__restrict__ acc, int64_t rows, int64_t cols, int64_t ld_acc,
-                                     uint16_t *__restrict__ y, int64_t ldy)
+                                     uint16_t *__restrict__ y, int64_t ldy, const QuantSpans sp)
 {
     const int64_t total = rows * cols;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = i / cols, c = i - r * cols;
-        y[r * ldy + c] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[r * ld_acc + c]));
+        if (in_span(NV4_SITE(0), sp.x, acc + r * ld_acc + c, 4) && in_span(NV4_SITE(0), sp.codes, y + r * ldy + c, 2))
+            y[r * ldy + c] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[r * ld_acc + c]));
     }
 }
 
@@ -814,6 +850,12 @@ cudaError_t launch_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K, in
     const int zp = zero_pad ? 1 : 0;
     const bool tiled = layout == NVFP4_LAYOUT_MMA_TILED;
     const int64_t rows_pad = tiled ? ceil_div(rows, 128) * 128 : rows;
+    QuantSpans sp;
+    sp.x = span_of(x, matrix_bytes(rows, K, ldx, 2));
+    sp.codes = span_of(codes, (uint64_t)rows * (uint64_t)(K / 2));
+    sp.scales = span_of(scales, tiled ? tiled_scale_bytes(rows, K) : (uint64_t)rows * (uint64_t)(K / 16));
+    sp.second = span_of(second, mode == NVFP4_SCALE_MACRO_FP16 ? 2u * (uint64_t)rows * (uint64_t)(K / 256) : 4u);
+    sp.partial = span_of(amax_partial, WS_AMAX_BYTES);
     const int sms = device_sm_count();
     if (rows_pad == 0)
         return cudaSuccess;
@@ -836,9 +878,9 @@ cudaError_t launch_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K, in
         float *sg = static_cast<float *>(second);
         if (tiled)
             return cudaLaunchKernelEx(&cfg, nvfp4_encode_small_kernel<true>, x, rows, rows_pad, K, ldx, codes, scales,
-                                      sg, status, zp);
+                                      sg, status, zp, sp);
         return cudaLaunchKernelEx(&cfg, nvfp4_encode_small_kernel<false>, x, rows, rows_pad, K, ldx, codes, scales, sg,
-                                  status, zp);
+                                  status, zp, sp);
     }
     if (mode == NVFP4_SCALE_TENSOR_FP32 && ldx == K) {
         // contiguous x: the staged streaming passes (3 and 4 CTAs per SM)
@@ -854,10 +896,10 @@ cudaError_t launch_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K, in
             e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, su_smem(SU_STAGES_2));
         if (e == cudaSuccess)
             e = launch_pdl(k1, grid, SU_THREADS, su_smem(SU_STAGES_1), stream, x, rows, rows_pad, K, codes, scales,
-                           sg, amax_partial, 0, zp, status, tmo);
+                           sg, amax_partial, 0, zp, status, tmo, sp);
         if (e == cudaSuccess)
             e = launch_pdl(k2, grid2, SU_THREADS, su_smem(SU_STAGES_2), stream, x, rows, rows_pad, K, codes, scales,
-                           sg, amax_partial, grid, zp, status, tmo);
+                           sg, amax_partial, grid, zp, status, tmo, sp);
         if (e != cudaSuccess)
             return e;
     } else if (mode == NVFP4_SCALE_TENSOR_FP32) {
@@ -874,32 +916,32 @@ cudaError_t launch_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K, in
         // 32-byte block loads when x and its row stride allow them
         const bool v8 = (reinterpret_cast<uintptr_t>(x) % 32) == 0 && (ldx % 16) == 0;
         cudaError_t e = v8 ? launch_pdl(amax_partial_kernel<true>, grid1, QT, 0, stream, x, rows, K, ldx,
-                                        amax_partial, status)
+                                        amax_partial, status, sp)
                            : launch_pdl(amax_partial_kernel<false>, grid1, QT, 0, stream, x, rows, K, ldx,
-                                        amax_partial, status);
+                                        amax_partial, status, sp);
         if (e != cudaSuccess)
             return e;
         float *sg = static_cast<float *>(second);
         const uint32_t *part = amax_partial;
         if (tiled)
             e = v8 ? launch_pdl(nvfp4_encode_kernel<true, true>, grid_e, QT, 0, stream, x, rows, rows_pad, K, ldx,
-                                codes, scales, sg, part, grid1, zp)
+                                codes, scales, sg, part, grid1, zp, sp)
                    : launch_pdl(nvfp4_encode_kernel<true, false>, grid_e, QT, 0, stream, x, rows, rows_pad, K, ldx,
-                                codes, scales, sg, part, grid1, zp);
+                                codes, scales, sg, part, grid1, zp, sp);
         else
             e = v8 ? launch_pdl(nvfp4_encode_kernel<false, true>, grid_e, QT, 0, stream, x, rows, rows_pad, K, ldx,
-                                codes, scales, sg, part, grid1, zp)
+                                codes, scales, sg, part, grid1, zp, sp)
                    : launch_pdl(nvfp4_encode_kernel<false, false>, grid_e, QT, 0, stream, x, rows, rows_pad, K, ldx,
-                                codes, scales, sg, part, grid1, zp);
+                                codes, scales, sg, part, grid1, zp, sp);
         if (e != cudaSuccess)
             return e;
     } else {
         if (tiled)
             nvfp4_encode_macro_kernel<true><<<grid2, QT, 0, stream>>>(x, rows, rows_pad, K, ldx, codes, scales,
-                                                                        static_cast<uint16_t *>(second), status);
+                                                                        static_cast<uint16_t *>(second), status, sp);
         else
             nvfp4_encode_macro_kernel<false><<<grid2, QT, 0, stream>>>(x, rows, rows_pad, K, ldx, codes, scales,
-                                                                         static_cast<uint16_t *>(second), status);
+                                                                         static_cast<uint16_t *>(second), status, sp);
     }
     return cudaGetLastError();
 }
@@ -910,7 +952,11 @@ cudaError_t launch_fp8_quantize(const uint16_t *x, int64_t rows, int64_t K, int6
     if (rows == 0)
         return cudaSuccess;
     const int grid = (int)std::min<int64_t>(rows, (int64_t)device_sm_count() * 8);
-    fp8_token_kernel<<<grid, QT, 0, stream>>>(x, rows, K, ldx, a, s_t, status);
+    QuantSpans sp;
+    sp.x = span_of(x, matrix_bytes(rows, K, ldx, 2));
+    sp.codes = span_of(a, (uint64_t)rows * (uint64_t)K);
+    sp.scales = span_of(s_t, 4u * (uint64_t)rows);
+    fp8_token_kernel<<<grid, QT, 0, stream>>>(x, rows, K, ldx, a, s_t, status, sp);
     return cudaGetLastError();
 }
 
@@ -919,7 +965,11 @@ cudaError_t launch_probe_convert(const float *in, int64_t n, uint8_t *o2, uint8_
     if (n == 0)
         return cudaSuccess;
     const int grid = (int)std::min<int64_t>(ceil_div(n, 256), (int64_t)device_sm_count() * 16);
-    probe_convert_kernel<<<grid, 256, 0, stream>>>(in, n, o2, o3);
+    QuantSpans sp;
+    sp.x = span_of(in, 4u * (uint64_t)n);
+    sp.codes = span_of(o2, (uint64_t)n);
+    sp.scales = span_of(o3, (uint64_t)n);
+    probe_convert_kernel<<<grid, 256, 0, stream>>>(in, n, o2, o3, sp);
     return cudaGetLastError();
 }
 
@@ -930,7 +980,10 @@ cudaError_t launch_finalize_bf16(const float *acc, int64_t rows, int64_t cols, i
     if (total == 0)
         return cudaSuccess;
     const int grid = (int)std::min<int64_t>(ceil_div(total, 256), (int64_t)device_sm_count() * 8);
-    finalize_bf16_kernel<<<grid, 256, 0, stream>>>(acc, rows, cols, ld_acc, y, ldy);
+    QuantSpans sp;
+    sp.x = span_of(acc, matrix_bytes(rows, cols, ld_acc, 4));
+    sp.codes = span_of(y, matrix_bytes(rows, cols, ldy, 2));
+    finalize_bf16_kernel<<<grid, 256, 0, stream>>>(acc, rows, cols, ld_acc, y, ldy, sp);
     return cudaGetLastError();
 }
 

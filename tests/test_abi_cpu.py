@@ -159,3 +159,23 @@ def test_output_checks_reject_before_launch(nv):
         nv._out(torch.empty((8, 16)), 8, 16, nv.OUT_BF16, None)       # not on a GPU
     with pytest.raises(ValueError):
         nv._out(None, 8, 16, 7, None)                                 # no such output type
+
+
+def test_checked_variant_loads_and_says_so(nv):
+    """The bounds-checked build exports the same functions and reports itself;
+    the normal build reports that it is not checked and refuses the record
+    query.  Host calls only."""
+    from nvfp4_block_scaled_30_b300 import build
+    path = build.build(checked=True)
+    C = ctypes.CDLL(path)
+    for n in header_functions():
+        assert hasattr(C, n), n
+    assert C.nvfp4_diag_bounds_checked() == 1
+    L = ctypes.CDLL(build.LIB)
+    assert L.nvfp4_diag_bounds_checked() == 0
+    n = ctypes.c_uint64(0)
+    assert L.nvfp4_diag_bounds_record(ctypes.byref(n), None, 0, None, None, 0) == nv.ERR_UNSUPPORTED
+    # argument checks of the self-test come before any launch
+    assert C.nvfp4_diag_bounds_selftest(None, ctypes.c_uint64(4160), ctypes.c_uint64(4096), None) == nv.ERR_INVALID_ARG
+    assert C.nvfp4_diag_bounds_selftest(ctypes.c_void_p(0x1000), ctypes.c_uint64(4100), ctypes.c_uint64(4096),
+                                        None) == nv.ERR_INVALID_ARG

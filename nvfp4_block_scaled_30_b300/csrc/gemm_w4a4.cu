@@ -11,7 +11,7 @@
 // Put Precision Policy Inside the Model. That Matters More Than W4A4",
 // section "One model can need more than one precision".
 //
-// Design (one CTA per SM, persistent, warp-specialised, 352 threads):
+// Design (one CTA per SM, persistent, warp-specialised, 384 threads):
 //   warp 0      producer: A/B code tiles by TMA (128-byte rows = 256 FP4,
 //               128-byte swizzle) and the compact 512-byte scale atoms by bulk
 //               copies, into a STAGES-deep ring; each copy of a stage is
@@ -36,6 +36,11 @@
 //               K stages (normally the last to finish it) adds the slots of
 //               the flagged contributors to its registers and stores the
 //               tile.
+//   warp 11     grouped only, gather warp: the activation rows of a work item
+//               (gathered through the routing indices) and their scale bytes
+//               by 16- and 4-byte cp.async into the stages the producer
+//               arms, so those many small copies do not hold up the
+//               producer's bulk copies.
 // The dense launch is a programmatic dependent launch: set-up, tensor-map
 // fetch and the first weight stages' L2 prefetch overlap the previous grid
 // (normally the activation quantiser); every access to memory the previous
@@ -58,7 +63,8 @@ constexpr int BM = 128;
 constexpr int STAGE_K_BYTES = 128; // per row and stage: 256 FP4 elements
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_FIRST_WARP = 3;
-constexpr int THREADS = 32 * (EPI_FIRST_WARP + EPI_WARPS);
+constexpr int GATHER_WARP = EPI_FIRST_WARP + EPI_WARPS; // grouped: activation row / scale gathers
+constexpr int THREADS = 32 * (GATHER_WARP + 1);
 constexpr int MAX_EXPERTS = 1024;
 
 // AR: activation rows one stage holds.  128 in general; 16 for the decode
@@ -86,7 +92,7 @@ struct Cfg {
     static constexpr int EPI_COLS = BN / 2;              // accumulator columns per epilogue warp
     static_assert(SF_BASE + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
     static_assert(STAGE_BYTES % 1024 == 0, "alignment");
-    static_assert(SMEM_BYTES + 4 * (MAX_EXPERTS + 2) <= 232448, "shared memory budget");
+    static_assert(SMEM_BYTES + 4 * (2 * MAX_EXPERTS + 3) <= 232448, "shared memory budget");
 };
 
 struct Params {
@@ -174,7 +180,10 @@ __device__ __forceinline__ void expert_rows(const Params &p, int e, int64_t &lo,
     hi = min(max(p.offsets[e + 1], lo), p.total_rows);
 }
 
-// Grouped: prefix[e] = number of 128-row tiles of experts 0..e-1.
+// Grouped: prefix[e] = number of 128-row tiles of experts 0..e-1, and from
+// prefix + MAX_EXPERTS + 1 on, elo[e] = offsets[e] clamped to [0,
+// total_rows] (e = 0..E), so expert e's rows are [elo[e], max(elo[e + 1],
+// elo[e])): expert_rows without a global load.
 __device__ __forceinline__ void decode_grouped(const Params &p, const int *prefix, int item, Tile &t)
 {
     const int tile_idx = item / p.n_tiles;
@@ -194,8 +203,8 @@ __device__ __forceinline__ void decode_grouped(const Params &p, const int *prefi
     t.tile_n = local / mt_e;
     const int mt = local - t.tile_n * mt_e;
     t.tile_m = mt;
-    int64_t r_lo, r_hi;
-    expert_rows(p, e, r_lo, r_hi);
+    const int *elo = prefix + MAX_EXPERTS + 1;
+    const int64_t r_lo = elo[e], r_hi = max(elo[e + 1], elo[e]);
     t.row0 = r_lo + (int64_t)mt * BM;
     t.row_end = r_hi;
     t.kst0 = 0;
@@ -266,22 +275,38 @@ __device__ __forceinline__ bool work_next_light(const Params &p, const int *pref
     return true;
 }
 
-// Grouped: source activation row of tile rows lane + 32q (row 0 for rows past
-// the expert or out-of-range indices, whose results are unspecified).
-__device__ __forceinline__ void tile_rows(const Params &p, bool indexed, const Tile &t, int lane, int (&src_row)[4],
-                                          bool (&row_ok)[4])
+// Grouped: source activation row of tile rows lane + 32q, in two steps so
+// the index loads of the next work item stay in flight while the current
+// one runs: tile_rows_load issues them (raw[q]: the index, or NO_ROW for
+// rows past the expert), tile_rows_use validates (row 0 for rows past the
+// expert or out-of-range indices, whose results are unspecified).
+constexpr int NO_ROW = -2147483647 - 1;
+__device__ __forceinline__ void tile_rows_load(const Params &p, bool indexed, const Tile &t, int lane,
+                                               int (&raw)[4])
 {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const int64_t g = t.row0 + lane + 32 * q;
-        row_ok[q] = g < t.row_end;
-        int r = 0;
-        if (row_ok[q]) {
+        int r = NO_ROW;
+        if (g < t.row_end) {
             if (!indexed)
                 r = (int)g;
             else if (in_span(NV4_SITE(0), p.sp_row_idx, p.row_idx + g, 4))
                 r = p.row_idx[g];
+            else
+                r = 0;
         }
+        raw[q] = r;
+    }
+}
+
+__device__ __forceinline__ void tile_rows_use(const Params &p, const int (&raw)[4], int (&src_row)[4],
+                                              bool (&row_ok)[4])
+{
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        row_ok[q] = raw[q] != NO_ROW;
+        int r = raw[q];
         if (r < 0 || r >= p.a_rows)
             r = 0;
         src_row[q] = r;
@@ -371,7 +396,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
     uint64_t *drain = acc_empty + C::ACC_BUFS;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    __shared__ int prefix[GROUPED ? MAX_EXPERTS + 1 : 1];
+    __shared__ int prefix[GROUPED ? 2 * (MAX_EXPERTS + 1) : 1];
     __shared__ int total_items_s;
 
     const int warp = threadIdx.x >> 5;
@@ -422,6 +447,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                     incl += v;
             }
             int acc = incl - run;
+            int *elo = prefix + MAX_EXPERTS + 1;
             if (lane == 0)
                 prefix[0] = 0;
             for (int e = e0; e < e1; ++e) {
@@ -429,9 +455,15 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                 expert_rows(p, e, lo, hi);
                 acc += (int)((hi - lo + BM - 1) / BM);
                 prefix[e + 1] = acc;
+                elo[e] = (int)lo; // < 2^31: total_rows is bounded by the host checks
             }
-            if (lane == 31)
+            if (lane == 31) {
                 total_items_s = incl * p.n_tiles;
+                // offsets[E] clamped to [0, total_rows], as expert_rows clamps it
+                elo[p.E] = (int)(in_span(NV4_SITE(0), p.sp_offsets, p.offsets + p.E, 8)
+                                     ? min(max(p.offsets[p.E], (int64_t)0), p.total_rows)
+                                     : 0);
+            }
         }
     } else if (threadIdx.x == 0) {
         total_items_s = p.m_tiles * p.n_tiles;
@@ -481,7 +513,12 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                 __syncwarp();
             }
             const int op = lane - 8 * (idx & 3);
-            if ((op == 1 && part_b) || (op == 0 && !indexed && part_a)) {
+            if (GROUPED && op == 1 && part_b) {
+                // the experts' weights are read once: evict them first, so
+                // the activation rows the gathers read again stay in L2
+                tma_load_2d_hint(sB, &p.tmap_b, kb * STAGE_K_BYTES, brow0, &full[st], (uint32_t)C::B_BYTES,
+                                 l2_policy_evict_first());
+            } else if ((op == 1 && part_b) || (op == 0 && !indexed && part_a)) {
                 const int arow = GROUPED ? (int)tt.row0 : tt.tile_m * BM;
                 tma_load_2d(op == 0 ? sA : sB, op == 0 ? &p.tmap_a : &p.tmap_b, kb * STAGE_K_BYTES,
                             op == 0 ? arow : brow0, &full[st],
@@ -514,23 +551,9 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                     issue(pt, kb, n_early, n_early, true, true, false);
         }
         pdl_wait();
-        // grouped items are decoded one ahead (expert offsets, then the row
-        // indices once the offsets have arrived) so their global loads
-        // overlap the current item's copies
-        Tile t_next;
-        bool have_next = work_next<GROUPED>(p, prefix, total_items, wi, t_next);
-        int src_row[4] = {0, 0, 0, 0}, next_row[4] = {0, 0, 0, 0};
-        bool row_ok[4] = {false, false, false, false}, next_ok[4] = {false, false, false, false};
-        if (GROUPED && have_next)
-            tile_rows(p, indexed, t_next, lane, next_row, next_ok);
-        while (ok && have_next) {
-            t = t_next;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                src_row[q] = next_row[q];
-                row_ok[q] = next_ok[q];
-            }
-            have_next = work_next<GROUPED>(p, prefix, total_items, wi, t_next);
+        // (grouped: the activation rows and scales are gathered by the
+        // gather warp; this warp issues the bulk copies only)
+        while (ok && work_next<GROUPED>(p, prefix, total_items, wi, t)) {
             for (int kb = t.kst0; kb < t.kst1; ++kb) {
                 const bool got = mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag);
                 if (!__all_sync(FULLMASK, got)) {
@@ -543,58 +566,12 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                 // their barriers armed and weight copies in flight
                 const bool early = issued < n_early;
                 issue(t, kb, stage, issued, !early, !early, true);
-                const int nk = min(4, p.k64 - 4 * kb);
-                uint8_t *sA = smem + stage * C::STAGE_BYTES;
-                uint8_t *sSFA = sA + C::A_BYTES + C::B_BYTES;
-                if (GROUPED) {
-                    if (indexed) {
-                        // gathered code rows: 16-byte cp.async with the 128-byte
-                        // swizzle (chunk c of row r lands in chunk c ^ (r & 7))
-                        const int row_bytes = p.k64 * 32;
-                        const int kbytes = min(STAGE_K_BYTES, row_bytes - kb * STAGE_K_BYTES);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int r = lane + 32 * q;
-                            const uint8_t *src = p.a_codes + (size_t)src_row[q] * row_bytes + kb * STAGE_K_BYTES;
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) {
-                                int n = row_ok[q] ? max(0, min(16, kbytes - c * 16)) : 0;
-                                if (n && !in_span(NV4_SITE(0), p.sp_a_codes, src + c * 16, n))
-                                    n = 0;
-                                cp_async_16(sA + r * STAGE_K_BYTES + ((c ^ (r & 7)) << 4), n ? src + c * 16 : src, n);
-                            }
-                        }
-                    }
-                    // activation scales of the tile's rows: 4 bytes per row and
-                    // 64-K chunk, gathered asynchronously (zero for rows past
-                    // the expert and chunks past K)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int r = src_row[q];
-                        const size_t base =
-                            ((size_t)(r >> 7) * p.k64 + 4 * kb) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4;
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const bool live = row_ok[q] && kk < nk &&
-                                              in_span(NV4_SITE(0), p.sp_sfa, p.sfa + base + kk * 512, 4);
-                            cp_async_4(sSFA + kk * 512 + lane * 16 + q * 4, p.sfa + (live ? base + kk * 512 : 0),
-                                       live ? 4u : 0u);
-                        }
-                    }
-                    // each lane's gathers complete the stage's barriers on
-                    // their own; the consumers fence before the tensor core reads
-                    cp_async_arrive_noinc(&sf_full[stage]);
-                    if (indexed)
-                        cp_async_arrive_noinc(&full[stage]);
-                }
                 ++issued;
                 if (++stage == C::STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
-            if (GROUPED && have_next)
-                tile_rows(p, indexed, t_next, lane, next_row, next_ok);
         }
         // every load is issued: the next grid in the stream may start its
         // set-up (it waits for this grid's completion before touching memory)
@@ -743,7 +720,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp < GATHER_WARP) {
         // ------------------------------------------------------------ epilogue
         const int ew = warp - EPI_FIRST_WARP;    // 0..7
         const int q = warp & 3;                  // the TMEM lane quarter this warp may access
@@ -1048,6 +1025,106 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
             for (int c = 0; c < NCH; ++c)
                 store_chunk32(out_desc(p), v[c], i, j_base + c * 32, alpha, i_end, j_end);
         }
+    } else if (GROUPED) {
+        // ------------------------------------------------------------ gather warp
+        // Grouped: the activation code rows (gathered) and the activation
+        // scales of each stage, by 16- and 4-byte cp.async into the stage
+        // the producer arms.  Many small copies per stage would otherwise
+        // hold up the producer's bulk copies; this warp waits for the same
+        // free slots and completes the stage's barriers with one arrival per
+        // lane.  Items are decoded one ahead: the expert offsets come from
+        // shared memory and the next item's row-index loads are issued when
+        // the current item starts, to be used only by the next item.
+        pdl_wait(); // the activations may come from the previous grid
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        WorkIter wi;
+        work_begin(p, total_items, wi);
+        Tile t, t_next;
+        bool have_next = work_next<GROUPED>(p, prefix, total_items, wi, t_next);
+        int src_row[4] = {0, 0, 0, 0}, next_raw[4] = {NO_ROW, NO_ROW, NO_ROW, NO_ROW};
+        bool row_ok[4] = {false, false, false, false};
+        if (have_next)
+            tile_rows_load(p, indexed, t_next, lane, next_raw);
+        while (ok && have_next) {
+            t = t_next;
+            tile_rows_use(p, next_raw, src_row, row_ok);
+            have_next = work_next<GROUPED>(p, prefix, total_items, wi, t_next);
+            if (have_next)
+                tile_rows_load(p, indexed, t_next, lane, next_raw);
+            for (int kb = t.kst0; kb < t.kst1; ++kb) {
+                const bool got = mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag);
+                if (!__all_sync(FULLMASK, got)) {
+                    if (lane == 0)
+                        record_timeout(p, abort_flag);
+                    ok = false;
+                    break;
+                }
+                const int nk = min(4, p.k64 - 4 * kb);
+                uint8_t *sA = smem + stage * C::STAGE_BYTES;
+                uint8_t *sSFA = sA + C::A_BYTES + C::B_BYTES;
+                if (GROUPED) {
+                    if (indexed) {
+                        // gathered code rows: 16-byte cp.async with the 128-byte
+                        // swizzle (chunk c of row r lands in chunk c ^ (r & 7)).
+                        // Eight lanes take the eight chunks of one row, so a
+                        // warp instruction covers four whole rows (four cache
+                        // lines, not 32); tile row r's source row is held by
+                        // lane r % 32 in src_row[r / 32] (-1: no row)
+                        const int row_bytes = p.k64 * 32;
+                        const int kbytes = min(STAGE_K_BYTES, row_bytes - kb * STAGE_K_BYTES);
+                        const int c = lane & 7;
+                        const int cbytes = max(0, min(16, kbytes - c * 16));
+                        const uint64_t keep = l2_policy_evict_last();
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int mine = row_ok[q] ? src_row[q] : -1;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const int r = 32 * q + 4 * j + (lane >> 3);
+                                const int srow = __shfl_sync(FULLMASK, mine, 4 * j + (lane >> 3));
+                                const uint8_t *src =
+                                    p.a_codes + (size_t)max(srow, 0) * row_bytes + kb * STAGE_K_BYTES + c * 16;
+                                int n = srow >= 0 ? cbytes : 0;
+                                if (n && !in_span(NV4_SITE(0), p.sp_a_codes, src, n))
+                                    n = 0;
+                                cp_async_16_hint(sA + r * STAGE_K_BYTES + ((c ^ (r & 7)) << 4), n ? src : p.a_codes, n,
+                                                 keep);
+                            }
+                        }
+                    }
+                    // activation scales of the tile's rows: 4 bytes per row and
+                    // 64-K chunk, gathered asynchronously (zero for rows past
+                    // the expert and chunks past K)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int r = src_row[q];
+                        const size_t base =
+                            ((size_t)(r >> 7) * p.k64 + 4 * kb) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const bool live = row_ok[q] && kk < nk &&
+                                              in_span(NV4_SITE(0), p.sp_sfa, p.sfa + base + kk * 512, 4);
+                            cp_async_4(sSFA + kk * 512 + lane * 16 + q * 4, p.sfa + (live ? base + kk * 512 : 0),
+                                       live ? 4u : 0u);
+                        }
+                    }
+                    // each lane's gathers complete the stage's barriers on
+                    // their own; the consumers fence before the tensor core reads
+                    cp_async_arrive_noinc(&sf_full[stage]);
+                    if (indexed)
+                        cp_async_arrive_noinc(&full[stage]);
+                }
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        // every gather of this warp lands before the CTA exits
+        cp_async_wait_all();
+        __syncwarp();
     }
 
     tc_fence_before();

@@ -96,6 +96,33 @@ __device__ __forceinline__ void cp_async_16(void *dst, const void *src, uint32_t
                  : "memory");
 }
 
+// L2 eviction-priority policies for the cache-hint forms below: data read
+// once (a weight stream) and data read again soon (gathered activations).
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// cp_async_16 with an L2 cache policy.
+__device__ __forceinline__ void cp_async_16_hint(void *dst, const void *src, uint32_t src_bytes, uint64_t policy)
+{
+    if (!(in_dyn_smem(NV4_SITE(1), smem_u32(dst), 16) && aligned_to(NV4_SITE(1), smem_u32(dst), 16) &&
+          in_bounds(NV4_SITE(1), src_bytes, 17)))
+        return;
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(src_bytes), "l"(policy)
+                 : "memory");
+}
+
 // 4-byte cp.async (src_bytes 0 or 4; 0 zero-fills the destination).
 __device__ __forceinline__ void cp_async_4(void *dst, const void *src, uint32_t src_bytes)
 {
@@ -133,6 +160,20 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// tma_load_2d with an L2 cache policy.
+__device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *map, int32_t x, int32_t y,
+                                                 uint64_t *bar, uint32_t box_bytes, uint64_t policy)
+{
+    if (!(in_dyn_smem(NV4_SITE(1), smem_u32(dst), box_bytes) && aligned_to(NV4_SITE(1), smem_u32(dst), 128) &&
+          aligned_to(NV4_SITE(1), (uint32_t)x, 16)))
+        return;
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
 
@@ -202,6 +243,8 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
 // L2 prefetch of one tile of a 2-D tensor map (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int32_t x, int32_t y)
 {
+    if (!aligned_to(NV4_SITE(1), (uint32_t)x, 16))
+        return;
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
                      reinterpret_cast<uint64_t>(map)),
                  "r"(x), "r"(y)
@@ -211,6 +254,8 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int32_t 
 // L2 prefetch of a contiguous range; address 16-byte aligned, bytes % 16 == 0.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
 {
+    if (!(aligned_to(NV4_SITE(1), reinterpret_cast<uint64_t>(src), 16) && aligned_to(NV4_SITE(1), bytes, 16)))
+        return;
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 

@@ -36,11 +36,16 @@
 //               K stages (normally the last to finish it) adds the slots of
 //               the flagged contributors to its registers and stores the
 //               tile.
-//   warp 11     grouped only, gather warp: the activation rows of a work item
-//               (gathered through the routing indices) and their scale bytes
-//               by 16- and 4-byte cp.async into the stages the producer
-//               arms, so those many small copies do not hold up the
-//               producer's bulk copies.
+//   warp 11     grouped with routing indices only, gather warp: the
+//               activation rows of a work item (gathered through the
+//               indices) and their scale bytes by 16- and 4-byte cp.async
+//               into the stages the producer arms, so those many small
+//               copies do not hold up the producer's bulk copies.
+//               Contiguous grouped rows need no gather: an expert's tiles
+//               start at the 128-row boundary at or below its first row,
+//               so they load like dense tiles (TMA codes, bulk-copied scale
+//               atoms) and the leading rows of the previous expert are
+//               computed but not stored.
 // The dense launch is a programmatic dependent launch: set-up, tensor-map
 // fetch and the first weight stages' L2 prefetch overlap the previous grid
 // (normally the activation quantiser); every access to memory the previous
@@ -145,6 +150,7 @@ struct Tile {
     int tile, tile_m, tile_n, kst0, kst1;
     int expert;            // grouped
     int64_t row0, row_end; // grouped: first output row of the tile, end of the expert's rows
+    int64_t row_lo;        // grouped: the expert's first row (rows below it are not stored)
 };
 
 // Tiles in bands of group_m M-tiles, M fastest inside a band, so CTAs running
@@ -165,6 +171,23 @@ __device__ __forceinline__ void decode_dense(const Params &p, int tile, Tile &t)
     t.expert = 0;
     t.row0 = 0;
     t.row_end = 0;
+    t.row_lo = 0;
+}
+
+// Grouped: first row of expert e's first tile.  Gathered rows start at the
+// expert's first row; contiguous rows start at the 128-row boundary at or
+// below it, so every tile lines up with the activations' 128-row scale
+// atoms and loads like a dense tile (the rows before the expert's first one
+// belong to the previous expert: computed, never stored).
+__device__ __forceinline__ int64_t expert_tile_base(const Params &p, int64_t lo)
+{
+    return p.row_idx == nullptr ? (lo & ~(int64_t)(BM - 1)) : lo;
+}
+
+// Grouped: number of 128-row tiles of expert e's rows [lo, hi).
+__device__ __forceinline__ int expert_tiles(const Params &p, int64_t lo, int64_t hi)
+{
+    return hi > lo ? (int)((hi - expert_tile_base(p, lo) + BM - 1) / BM) : 0;
 }
 
 // Expert e's output rows [lo, hi), with the device offsets clamped to
@@ -205,8 +228,9 @@ __device__ __forceinline__ void decode_grouped(const Params &p, const int *prefi
     t.tile_m = mt;
     const int *elo = prefix + MAX_EXPERTS + 1;
     const int64_t r_lo = elo[e], r_hi = max(elo[e + 1], elo[e]);
-    t.row0 = r_lo + (int64_t)mt * BM;
+    t.row0 = expert_tile_base(p, r_lo) + (int64_t)mt * BM;
     t.row_end = r_hi;
+    t.row_lo = r_lo;
     t.kst0 = 0;
     t.kst1 = p.kstages;
 }
@@ -410,7 +434,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
             // arrival per producer lane for gathered rows; scales likewise
             // (grouped: the activation scales are gathered by cp.async)
             mbar_init(&full[s], indexed ? 33 : 1);
-            mbar_init(&sf_full[s], GROUPED ? 33 : 1);
+            mbar_init(&sf_full[s], indexed ? 33 : 1);
             mbar_init(&empty[s], 1);
             mbar_init(&sf_ready[s], 1);
         }
@@ -437,7 +461,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
             for (int e = e0; e < e1; ++e) {
                 int64_t lo, hi;
                 expert_rows(p, e, lo, hi);
-                run += (int)((hi - lo + BM - 1) / BM);
+                run += expert_tiles(p, lo, hi);
             }
             int incl = run;
 #pragma unroll
@@ -453,7 +477,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
             for (int e = e0; e < e1; ++e) {
                 int64_t lo, hi;
                 expert_rows(p, e, lo, hi);
-                acc += (int)((hi - lo + BM - 1) / BM);
+                acc += expert_tiles(p, lo, hi);
                 prefix[e + 1] = acc;
                 elo[e] = (int)lo; // < 2^31: total_rows is bounded by the host checks
             }
@@ -505,7 +529,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                     nb_loaded += (bt0 + h < p.b_row_tiles) ? 1 : 0;
                 const uint32_t code_bytes =
                     C::B_BYTES + (indexed ? 0u : (uint32_t)p.a_box_rows * STAGE_K_BYTES);
-                const uint32_t sf_bytes = (nb_loaded + (GROUPED ? 0 : 1)) * nk * 512;
+                const uint32_t sf_bytes = (nb_loaded + (indexed ? 0 : 1)) * nk * 512;
                 if (lane == 0)
                     mbar_arrive_expect_tx(&full[st], code_bytes);
                 else if (lane == 1)
@@ -523,9 +547,10 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                 tma_load_2d(op == 0 ? sA : sB, op == 0 ? &p.tmap_a : &p.tmap_b, kb * STAGE_K_BYTES,
                             op == 0 ? arow : brow0, &full[st],
                             op == 0 ? (uint32_t)p.a_box_rows * STAGE_K_BYTES : (uint32_t)C::B_BYTES);
-            } else if ((op == 2 && !GROUPED && part_a) ||
+            } else if ((op == 2 && !indexed && part_a) ||
                        (op >= 3 && op < 3 + C::NB && bt0 + op - 3 < p.b_row_tiles && part_b)) {
-                const uint8_t *src = op == 2 ? p.sfa + ((size_t)tt.tile_m * p.k64 + 4 * kb) * 512
+                const int64_t a_atom_row = GROUPED ? tt.row0 / BM : tt.tile_m;
+                const uint8_t *src = op == 2 ? p.sfa + ((size_t)a_atom_row * p.k64 + 4 * kb) * 512
                                              : p.sfb + ((size_t)(bt0 + op - 3) * p.k64 + 4 * kb) * 512;
                 if (in_span(NV4_SITE(0), op == 2 ? p.sp_sfa : p.sp_sfb, src, nk * 512))
                     bulk_load(op == 2 ? sSFA : sSFB + (op - 3) * 2048, src, nk * 512, &sf_full[st]);
@@ -676,7 +701,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                     ok = false;
                     break;
                 }
-                if (GROUPED) // gathered activation scales were written by cp.async
+                if (indexed) // gathered activation scales were written by cp.async
                     fence_proxy_async_smem();
                 if (lane == 0) {
                     // atoms of B row groups past the weight rows hold stale
@@ -774,7 +799,9 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
             int64_t i, i_end;
             if (GROUPED) {
                 i = t.row0 + row_in_tile;
-                i_end = t.row_end;
+                // rows before the expert's first one (an aligned contiguous
+                // tile) are the previous expert's: not stored
+                i_end = i < t.row_lo ? i : t.row_end;
             } else {
                 i = (int64_t)t.tile_m * BM + row_in_tile;
                 i_end = p.a_rows;
@@ -1025,7 +1052,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
             for (int c = 0; c < NCH; ++c)
                 store_chunk32(out_desc(p), v[c], i, j_base + c * 32, alpha, i_end, j_end);
         }
-    } else if (GROUPED) {
+    } else if (GROUPED && indexed) {
         // ------------------------------------------------------------ gather warp
         // Grouped: the activation code rows (gathered) and the activation
         // scales of each stage, by 16- and 4-byte cp.async into the stage

@@ -99,6 +99,27 @@ def test_small_full_with_empty_experts(indexed):
     assert ok, worst
 
 
+@pytest.mark.parametrize("out_dtype", [nv.OUT_BF16, nv.OUT_FP32])
+def test_contiguous_expert_boundaries_every_row(out_dtype):
+    # contiguous rows tile from the 128-row boundary at or below each
+    # expert's first row; these boundaries fall at every kind of offset
+    # (inside a block, on a block edge, a 1-row expert, an empty one, an
+    # expert spanning three blocks), and every row is checked against its
+    # own expert's product, so a tile that stored the previous expert's
+    # leading rows would fail
+    E, N, K = 7, 256, 512
+    counts = np.array([1, 127, 129, 0, 255, 70, 128])
+    w, wc, ws, wg = stacked_weights(E, N, K, 4)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    total = int(offsets[-1])
+    xb = synth.activations(9, 31, total, K, 0.01, 50.0)
+    a, ac, as_, ag = quantize_pinned(xb)
+    y = nv.grouped_gemm(a, torch.from_numpy(offsets).cuda(), w, N, total, out_dtype=out_dtype)
+    ref = oracle.gemm_grouped_w4a4((ac, as_, ag[0]), None, offsets, wc, ws, wg)
+    ok, worst = row_tolerance_ok(y_np(y), ref, out_bf16=out_dtype == nv.OUT_BF16)
+    assert ok, worst
+
+
 def test_heavy_zipf_routing(up_weights):
     w, wc, ws, wg = up_weights
     row_idx, offsets, counts, _ = synth.moe_routing(literal=True)

@@ -689,7 +689,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["decode", "prefill", "policy", "moe"], default="decode")
+    ap.add_argument("--workload", choices=["decode", "prefill", "policy", "moe", "macro"], default="decode")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle leg (profiling runs)")
     args = ap.parse_args()
@@ -778,6 +778,10 @@ def main():
     elif args.workload == "policy":
         r = workload_policy(c, args.steps, args.warmup, nv.POLICY_AUTO)
         unit, value_rank = "TFLOP/s", r["value"]
+    elif args.workload == "macro":
+        r = workload_prefill_macro(c, 8192, args.steps, args.warmup)
+        r.update({"ms": r["gemm_ms"], "value": r["gemm_tflops"], "launches_per_step": 1})
+        unit, value_rank = "TFLOP/s", r["value"]
     else:
         r = workload_moe(c, args.steps, args.warmup)
         unit, value_rank = "GB/s", r["value"]
@@ -852,6 +856,12 @@ def main():
     elif args.workload == "policy":
         roof = None
         cfg = {"workload": "policy_stack AUTO: 8 x [2048,4096]x[4096,4096]^T, 2 W4A8 layers", "global_batch": 2048}
+    elif args.workload == "macro":
+        ach = r["gemm_tflops"]
+        roof = {"bound": "tensor", "achieved": ach, "peak": fp4_peak, "unit": "TFLOP/s", "frac": ach / fp4_peak,
+                "traffic": None, "kernel": "macro_kernel", "peak_source": "measured in this run (fp4_peak)"}
+        cfg = {"workload": "prefill_macro: X[4096,8192] x W[8192,8192]^T, FP16 macro-scales per 256",
+               "global_batch": 4096, "l2": "2 rotating weight copies"}
     else:
         roof = None
         cfg = {"workload": "moe_grouped: 2048 tokens, 128 experts top-8, up [768,2048] + down [2048,768]",

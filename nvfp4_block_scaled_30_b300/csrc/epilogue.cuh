@@ -92,12 +92,12 @@ __device__ __forceinline__ float encode_store_q(const uint32_t (&v)[32], uint8_t
             amb = fmaxf(amb, fabsf(__uint_as_float(v[16 * h + t])));
         const uint32_t e = block_scale_code(amb, s);
         const float r = recip_step(__fmul_rn(e4m3_value(e), s));
-        uint32_t pk[2] = {0u, 0u};
+        float q[16];
 #pragma unroll
-        for (int t = 0; t < 8; ++t)
-            pk[t >> 2] |= e2m1x2(__fmul_rn(__uint_as_float(v[16 * h + 2 * t]), r),
-                                 __fmul_rn(__uint_as_float(v[16 * h + 2 * t + 1]), r))
-                          << (8 * (t & 3));
+        for (int t = 0; t < 16; ++t)
+            q[t] = __fmul_rn(__uint_as_float(v[16 * h + t]), r);
+        const uint32_t pk[2] = {e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]),
+                                e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15])};
         const int j = j0 + 16 * h;
         if (in_span(NV4_SITE(2), qs.codes, crow + j / 2, 8))
             *reinterpret_cast<uint2 *>(crow + j / 2) = make_uint2(pk[0], pk[1]);

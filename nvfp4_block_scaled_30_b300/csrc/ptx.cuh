@@ -482,6 +482,25 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi)
     return b;
 }
 
+// Eight values' E2M1 codes packed into one word: byte i holds the codes of
+// q[2i] (low nibble) and q[2i+1] (high nibble), each byte as e2m1x2 forms it;
+// the four bytes are joined by one vector move instead of per-byte widening,
+// shifts and ORs.
+__device__ __forceinline__ uint32_t e2m1x8(float q0, float q1, float q2, float q3, float q4, float q5, float q6,
+                                           float q7)
+{
+    uint32_t w;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(w)
+        : "f"(q0), "f"(q1), "f"(q2), "f"(q3), "f"(q4), "f"(q5), "f"(q6), "f"(q7));
+    return w;
+}
+
 // E4M3 code of v (round to nearest even, saturating at +-448).
 __device__ __forceinline__ uint32_t e4m3(float v)
 {

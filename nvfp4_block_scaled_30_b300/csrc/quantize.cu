@@ -74,11 +74,8 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t *red)
 // 8 values times r -> 4 packed E2M1 bytes (element 0 in the lowest nibble).
 __device__ __forceinline__ uint32_t pack8(const float (&f)[8], float r)
 {
-    uint32_t p = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        p |= e2m1x2(__fmul_rn(f[2 * i], r), __fmul_rn(f[2 * i + 1], r)) << (8 * i);
-    return p;
+    return e2m1x8(__fmul_rn(f[0], r), __fmul_rn(f[1], r), __fmul_rn(f[2], r), __fmul_rn(f[3], r),
+                  __fmul_rn(f[4], r), __fmul_rn(f[5], r), __fmul_rn(f[6], r), __fmul_rn(f[7], r));
 }
 
 __device__ __forceinline__ size_t scale_offset(int64_t row, int64_t blk, int64_t K, bool tiled)
@@ -202,15 +199,13 @@ __device__ __forceinline__ void encode_block16(const uint32_t (&w)[8], int64_t r
     uint32_t pk[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        uint32_t p = 0;
+        float q[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint32_t ww = w[4 * h + i];
-            float q0, q1;
-            mul2_rn(__uint_as_float(ww << 16), __uint_as_float(ww & 0xFFFF0000u), r, q0, q1);
-            p |= e2m1x2(q0, q1) << (8 * i);
+            mul2_rn(__uint_as_float(ww << 16), __uint_as_float(ww & 0xFFFF0000u), r, q[2 * i], q[2 * i + 1]);
         }
-        pk[h] = p;
+        pk[h] = e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
     }
     if (in_span(NV4_SITE(0), sp.codes, codes + row * (K / 2) + blk * 8, 8))
         *reinterpret_cast<uint2 *>(codes + row * (K / 2) + blk * 8) = make_uint2(pk[0], pk[1]);
@@ -578,15 +573,14 @@ __global__ void __launch_bounds__(SU_THREADS) stream_quant_kernel(const uint16_t
                     uint32_t pk[2];
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        uint32_t pw = 0;
+                        float q[8];
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const uint32_t ww = w[4 * h + i];
-                            float q0, q1;
-                            mul2_rn(__uint_as_float(ww << 16), __uint_as_float(ww & 0xFFFF0000u), r, q0, q1);
-                            pw |= e2m1x2(q0, q1) << (8 * i);
+                            mul2_rn(__uint_as_float(ww << 16), __uint_as_float(ww & 0xFFFF0000u), r, q[2 * i],
+                                    q[2 * i + 1]);
                         }
-                        pk[h] = pw;
+                        pk[h] = e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
                     }
                     // codes are contiguous: block b's 8 bytes sit at 8 b
                     const int64_t b = u * SU_BLOCKS + slot;

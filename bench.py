@@ -242,6 +242,20 @@ def workload_decode(c, M, steps, warmup, rot=4, with_e2e=False, peaks_=None):
     ms = c.time(step, steps, warmup)
     gms = c.time(gemm_only, steps, warmup)
     st = work.status()
+    stream = None
+    if with_e2e:
+        # the copy engine's streaming rate on the same rotating weight codes,
+        # with the GEMM's boxes and nothing else (nvfp4_diag_tma_stream): at
+        # the decode kernel's grid (one CTA per 256-row tile) and at one CTA
+        # per SM; the ceiling the decode GEMM's HBM fraction meets in practice
+        status = t.zeros(1, dtype=t.int32, device=c.dev)
+        codes = [w.codes.view(t.uint8).reshape(N, K // 2) for w in W]
+        stream = {}
+        for grid in (N // 256, nv.sm_count()):
+            sms = c.time(lambda i, g=grid: nv.tma_stream(codes[i % rot], g, status), steps, warmup)
+            stream[f"gbs_grid{grid}"] = codes[0].numel() / (sms * 1e-3) / 1e9
+        stream["status"] = int(status.item())
+        stream["bytes"] = codes[0].numel()
     stats = {"x": scale_stats(a_q), "w": scale_stats(W[0])}   # after the timed loops
     # the quantiser is one launch (one thread-block cluster) up to 32768
     # chunks of 8 values, two staged passes above that; then the GEMM
@@ -249,6 +263,8 @@ def workload_decode(c, M, steps, warmup, rot=4, with_e2e=False, peaks_=None):
     res = {"ms": ms, "gemm_ms": gms, "step_bytes": step_bytes, "gemm_bytes": gemm_bytes,
            "value": step_bytes / (ms * 1e-3) / 1e9, "launches_per_step": launches, "device_status": st,
            "scale_stats": stats}
+    if stream is not None:
+        res["stream"] = stream
     if with_e2e:
         hx = t.from_numpy(xb.view(np.int16)).pin_memory()
         hy = t.empty((M, N), dtype=t.int16).pin_memory()
@@ -843,6 +859,11 @@ def main():
         roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
                 "traffic": TRAFFIC.get("decode"), "kernel": "w4a4_kernel<256,false> (112 CTAs, one 256-row weight tile each)",
                 "peak_source": f"{peak_src} hbm_gbs"}
+        if r.get("stream"):
+            best = max(v for k, v in r["stream"].items() if k.startswith("gbs_"))
+            roof["stream_ceiling"] = dict(r["stream"], frac_of_hbm=best / hbm, gemm_frac_of_stream=ach / best,
+                                          how="nvfp4_diag_tma_stream: the weight codes by the GEMM's TMA boxes, "
+                                              "6-stage ring, no compute")
         cfg = {"workload": "decode_mlp_up: X[8,8192] bf16 -> NVFP4, W NVFP4[28672,8192], Y bf16",
                "global_batch": 8, "l2": "4 rotating weight copies (528 MB > 126 MB L2)"}
     elif args.workload == "prefill":

@@ -468,6 +468,21 @@ nvfp4_status nvfp4_probe_convert(const float *in, int64_t n, uint8_t *out_e2m1, 
  * iters in 1 .. 2^24.  Asynchronous; the caller owns `cycles`. */
 nvfp4_status nvfp4_diag_fp4_mma_rate(int32_t iters, uint64_t *cycles, nvfp4_stream_t stream);
 
+/* Diagnostic: the copy engine's streaming rate as the W4A4 GEMM's weight
+ * operand sees it.  Streams the rows x row_bytes byte matrix w (device,
+ * 16-byte aligned, row-major; rows a multiple of 256 up to 2^31, row_bytes a
+ * multiple of 128 in 128 .. 2^20) into shared memory with the GEMM's weight
+ * boxes (128 bytes x 256 rows, 128-byte swizzle) through a 6-deep ring of
+ * 32 KB stages on `grid` CTAs (1 .. 4096, one warp each), each CTA taking an
+ * equal contiguous range of the boxes, and does nothing else with them.
+ * Time the launch with events on `stream`: rows x row_bytes bytes over that
+ * time is the streaming ceiling of the decode GEMM (whose weights arrive
+ * exactly so).  A bounded wait that runs out ORs NVFP4's timeout bit (2)
+ * into *status (a device word, 4-byte aligned, caller-owned).
+ * Asynchronous. */
+nvfp4_status nvfp4_diag_tma_stream(const uint8_t *w, int64_t rows, int64_t row_bytes, int32_t grid,
+                                   uint32_t *status, nvfp4_stream_t stream);
+
 /* Test-only failure injection for the device-side failure detection: runs the
  * W4A4 GEMM of pre-quantised a_q (TENSOR_FP32, MMA_TILED) and w on a shape
  * that uses stream-K, with CTA `skip_cta` never raising its ready flag, and

@@ -41,7 +41,8 @@ EXPORTED = ["nvfp4_scale_bytes", "nvfp4_workspace_size", "nvfp4_workspace_init",
             "nvfp4_moe_down_combine", "nvfp4_grouped_w4a8_gemm", "nvfp4_grouped_gemm_x",
             "nvfp4_diag_streamk_skip_flag", "nvfp4_kv_append", "nvfp4_kv_decode_attention",
             "nvfp4_gemm_kernel_path", "nvfp4_diag_fp4_mma_rate", "nvfp4_gemm_w4a4_noalloc_status",
-            "nvfp4_diag_bounds_checked", "nvfp4_diag_bounds_record", "nvfp4_diag_bounds_selftest"]
+            "nvfp4_diag_bounds_checked", "nvfp4_diag_bounds_record", "nvfp4_diag_bounds_selftest",
+            "nvfp4_diag_tma_stream"]
 
 
 def _require(ok: bool, what: str) -> None:
@@ -121,6 +122,7 @@ def lib():
                                                 ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64),
                                                 _I32]),
             "nvfp4_diag_bounds_selftest": (_I32, [_VP, ctypes.c_uint64, ctypes.c_uint64, _VP]),
+            "nvfp4_diag_tma_stream": (_I32, [_VP, _I64, _I64, _I32, _VP, _VP]),
             "nvfp4_version": (ctypes.c_char_p, []),
         }
         for name, (res, args) in sig.items():
@@ -400,6 +402,17 @@ def noalloc_status(stream=None) -> int:
     out = _I32(0)
     _check(lib().nvfp4_gemm_w4a4_noalloc_status(_stream(stream), ctypes.byref(out)), "nvfp4_gemm_w4a4_noalloc_status")
     return out.value
+
+
+def tma_stream(w: torch.Tensor, grid: int, status: torch.Tensor, stream=None) -> None:
+    """nvfp4_diag_tma_stream over a contiguous 2-D uint8 CUDA tensor (rows a
+    multiple of 256, row bytes a multiple of 128); status: an int32 CUDA word."""
+    _require(w.dtype == torch.uint8 and w.is_cuda and w.dim() == 2 and w.is_contiguous(),
+             "tma_stream: w must be a contiguous 2-D uint8 CUDA tensor")
+    _require(status.dtype == torch.int32 and status.is_cuda and status.numel() >= 1,
+             "tma_stream: status must be an int32 CUDA tensor")
+    _check(lib().nvfp4_diag_tma_stream(_ptr(w), w.shape[0], w.shape[1], grid, _ptr(status), _stream(stream)),
+           "nvfp4_diag_tma_stream")
 
 
 def bounds_checked() -> bool:

@@ -1015,6 +1015,16 @@ nvfp4_status nvfp4_diag_bounds_record(uint64_t *failures, char *where, int32_t w
     return NVFP4_OK;
 }
 
+nvfp4_status nvfp4_diag_tma_stream(const uint8_t *w, int64_t rows, int64_t row_bytes, int32_t grid, uint32_t *status,
+                                   nvfp4_stream_t stream)
+{
+    if (!w || !aligned(w, 16) || rows <= 0 || rows % 256 != 0 || rows > ((int64_t)1 << 31) || row_bytes < 128 ||
+        row_bytes % 128 != 0 || row_bytes > ((int64_t)1 << 20) || grid < 1 || grid > 4096 || !status ||
+        !aligned(status, 4))
+        return NVFP4_ERR_INVALID_ARG;
+    return from_cuda(launch_tma_stream(w, rows, row_bytes, grid, status, (cudaStream_t)stream));
+}
+
 nvfp4_status nvfp4_probe_convert(const float *in, int64_t n, uint8_t *out_e2m1, uint8_t *out_e4m3,
                                  nvfp4_stream_t stream)
 {

@@ -86,6 +86,8 @@ cudaError_t launch_fp8_quantize(const uint16_t *x, int64_t rows, int64_t K, int6
                                 uint32_t *status, cudaStream_t stream);
 cudaError_t launch_fp4_mma_rate(int iters, uint64_t *cycles, cudaStream_t stream);
 cudaError_t launch_bounds_selftest(uint8_t *buf, uint64_t span_bytes, cudaStream_t stream);
+cudaError_t launch_tma_stream(const uint8_t *w, int64_t rows, int64_t row_bytes, int grid, uint32_t *status,
+                              cudaStream_t stream);
 cudaError_t launch_probe_convert(const float *in, int64_t n, uint8_t *o2, uint8_t *o3, cudaStream_t stream);
 cudaError_t launch_finalize_bf16(const float *acc, int64_t rows, int64_t cols, int64_t ld_acc, uint16_t *y,
                                  int64_t ldy, cudaStream_t stream);

@@ -537,5 +537,45 @@ __device__ __forceinline__ float recip_step(float d)
     return d == 0.0f ? 0.0f : fminf(__frcp_rn(d), 3.402823466e+38f);
 }
 
+// Two IEEE round-to-nearest products at once (bit-identical to two
+// __fmul_rn).
+__device__ __forceinline__ void mul2_rn(float a0, float a1, float r, float &p0, float &p1)
+{
+    uint64_t a = (uint64_t)__float_as_uint(a0) | ((uint64_t)__float_as_uint(a1) << 32);
+    const uint64_t rr = (uint64_t)__float_as_uint(r) | ((uint64_t)__float_as_uint(r) << 32);
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(rr));
+    p0 = __uint_as_float((uint32_t)d);
+    p1 = __uint_as_float((uint32_t)(d >> 32));
+}
+
+// One 16-element block of BF16 values (8 words, element 2i in the low half
+// of word i) encoded under the tensor scale s by the quantisers' rule: the
+// block maximum from the magnitude bits (exact, equal to the float maximum
+// of finite values), the E4M3 scale code, the reciprocal step, and the 16
+// E2M1 codes packed into two words (element 2j in the low nibble of byte j).
+// Returns the scale code.
+__device__ __forceinline__ uint32_t encode_bf16_block(const uint32_t (&w)[8], float s, uint32_t (&pk)[2])
+{
+    uint32_t m2 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        m2 = __vmaxu2(m2, w[i] & 0x7FFF7FFFu);
+    const float amb = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
+    const uint32_t e = block_scale_code(amb, s);
+    const float r = recip_step(__fmul_rn(e4m3_value(e), s));
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        float q[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t ww = w[4 * h + i];
+            mul2_rn(__uint_as_float(ww << 16), __uint_as_float(ww & 0xFFFF0000u), r, q[2 * i], q[2 * i + 1]);
+        }
+        pk[h] = e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
+    }
+    return e;
+}
+
 } // namespace nv4
 

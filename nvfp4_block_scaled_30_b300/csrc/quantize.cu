@@ -169,18 +169,6 @@ __device__ __forceinline__ void encode_chunk(const float (&f)[8], bool real, int
 // Blocks in flight per thread in the two-pass encode.
 constexpr int QB = 2;
 
-// Two IEEE round-to-nearest products at once (bit-identical to two
-// __fmul_rn).
-__device__ __forceinline__ void mul2_rn(float a0, float a1, float r, float &p0, float &p1)
-{
-    uint64_t a = (uint64_t)__float_as_uint(a0) | ((uint64_t)__float_as_uint(a1) << 32);
-    const uint64_t rr = (uint64_t)__float_as_uint(r) | ((uint64_t)__float_as_uint(r) << 32);
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(rr));
-    p0 = __uint_as_float((uint32_t)d);
-    p1 = __uint_as_float((uint32_t)(d >> 32));
-}
-
 // One whole 16-element block (16 BF16 values in 8 words) by one thread: the
 // block maximum from the magnitude bits (exact, equal to the float maximum
 // of finite values), the same scale and code arithmetic as encode_chunk, and
@@ -189,24 +177,8 @@ template <bool TILED>
 __device__ __forceinline__ void encode_block16(const uint32_t (&w)[8], int64_t row, int64_t blk, int64_t K, float sg,
                                                uint8_t *codes, uint8_t *scales, const QuantSpans &sp)
 {
-    uint32_t m2 = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        m2 = __vmaxu2(m2, w[i] & 0x7FFF7FFFu);
-    const float amb = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
-    const uint32_t e = block_scale_code(amb, sg);
-    const float r = recip_step(__fmul_rn(e4m3_value(e), sg));
     uint32_t pk[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        float q[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t ww = w[4 * h + i];
-            mul2_rn(__uint_as_float(ww << 16), __uint_as_float(ww & 0xFFFF0000u), r, q[2 * i], q[2 * i + 1]);
-        }
-        pk[h] = e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
-    }
+    const uint32_t e = encode_bf16_block(w, sg, pk);
     if (in_span(NV4_SITE(0), sp.codes, codes + row * (K / 2) + blk * 8, 8))
         *reinterpret_cast<uint2 *>(codes + row * (K / 2) + blk * 8) = make_uint2(pk[0], pk[1]);
     if (in_span(NV4_SITE(0), sp.scales, scales + scale_offset(row, blk, K, TILED), 1))

@@ -21,6 +21,7 @@
 // single-launch path on one thread-block cluster (amax exchanged through
 // distributed shared memory); larger tensors take two streaming passes.
 #include <cfloat>
+#include <mutex>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -592,12 +593,13 @@ __global__ void __launch_bounds__(SU_THREADS) stream_quant_kernel(const uint16_t
 // its last real chunk); every CTA pushes its absolute maximum into all CTAs'
 // shared memory, one cluster barrier publishes them, and each CTA encodes
 // from its registers, so x is read once and there is no second launch.
-constexpr int FC = 8;    // CTAs per cluster
+// A cluster of 16 CTAs (a non-portable size; one chunk per thread at 8 x 8192)
+// measured 0.7-1.1 us faster per decode step than 8; 8 is kept for devices
+// that cannot hold a 16-CTA cluster.
 constexpr int FT = 512;  // threads per CTA
-constexpr int FQ = 8;    // chunks per thread
-constexpr int64_t FUSED_MAX_CHUNKS = (int64_t)FC * FT * FQ;
+constexpr int64_t FUSED_MAX_CHUNKS = 32768;
 
-template <bool TILED>
+template <bool TILED, int FC>
 __global__ void __launch_bounds__(FT) nvfp4_encode_small_kernel(const uint16_t *__restrict__ x, int64_t rows,
                                                                 int64_t rows_pad, int64_t K, int64_t ldx,
                                                                 uint8_t *__restrict__ codes,
@@ -606,6 +608,8 @@ __global__ void __launch_bounds__(FT) nvfp4_encode_small_kernel(const uint16_t *
                                                                 uint32_t *__restrict__ status, int zero_pad,
                                                                 const QuantSpans sp)
 {
+    constexpr int FQ = (int)(FUSED_MAX_CHUNKS / (FC * FT)); // chunks per thread
+    static_assert(FQ * FC * FT == FUSED_MAX_CHUNKS, "cluster shape");
     __shared__ uint32_t red[FT / 32];
     __shared__ uint32_t cta_max[FC];
     // this CTA is running: peers may write its shared memory once they have
@@ -807,6 +811,40 @@ __global__ void finalize_bf16_kernel(const float *__restrict__ acc, int64_t rows
     }
 }
 
+// Cluster size of the small-activation quantiser: 16 CTAs where the device
+// can hold such a cluster (decided once, by an occupancy query: no launch,
+// so it is also safe while a stream is being captured), else 8.
+int small_cluster_size()
+{
+    static std::once_flag once;
+    static int fc = 8;
+    std::call_once(once, [] {
+        if (cudaFuncSetAttribute(nvfp4_encode_small_kernel<true, 16>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                 1) != cudaSuccess ||
+            cudaFuncSetAttribute(nvfp4_encode_small_kernel<false, 16>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                 1) != cudaSuccess) {
+            cudaGetLastError();
+            return;
+        }
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(16);
+        cfg.blockDim = dim3(FT);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 16;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, nvfp4_encode_small_kernel<true, 16>, &cfg) == cudaSuccess &&
+            clusters > 0)
+            fc = 16;
+        cudaGetLastError();
+    });
+    return fc;
+}
+
 } // namespace
 
 cudaError_t launch_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx, uint8_t *codes,
@@ -828,13 +866,14 @@ cudaError_t launch_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K, in
     const int grid2 = (int)std::min<int64_t>(rows_pad, (int64_t)sms * 8);
     if (mode == NVFP4_SCALE_TENSOR_FP32 && rows * (K / 8) <= FUSED_MAX_CHUNKS) {
         // small activations: one cluster, one launch
+        const int fc = small_cluster_size();
         cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3(FC);
+        cfg.gridDim = dim3(fc);
         cfg.blockDim = dim3(FT);
         cfg.stream = stream;
         cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = FC;
+        attr[0].val.clusterDim.x = fc;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -842,11 +881,15 @@ cudaError_t launch_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K, in
         cfg.attrs = attr;
         cfg.numAttrs = 2;
         float *sg = static_cast<float *>(second);
-        if (tiled)
-            return cudaLaunchKernelEx(&cfg, nvfp4_encode_small_kernel<true>, x, rows, rows_pad, K, ldx, codes, scales,
-                                      sg, status, zp, sp);
-        return cudaLaunchKernelEx(&cfg, nvfp4_encode_small_kernel<false>, x, rows, rows_pad, K, ldx, codes, scales, sg,
-                                  status, zp, sp);
+        if (fc == 16)
+            return tiled ? cudaLaunchKernelEx(&cfg, nvfp4_encode_small_kernel<true, 16>, x, rows, rows_pad, K, ldx,
+                                              codes, scales, sg, status, zp, sp)
+                         : cudaLaunchKernelEx(&cfg, nvfp4_encode_small_kernel<false, 16>, x, rows, rows_pad, K, ldx,
+                                              codes, scales, sg, status, zp, sp);
+        return tiled ? cudaLaunchKernelEx(&cfg, nvfp4_encode_small_kernel<true, 8>, x, rows, rows_pad, K, ldx, codes,
+                                          scales, sg, status, zp, sp)
+                     : cudaLaunchKernelEx(&cfg, nvfp4_encode_small_kernel<false, 8>, x, rows, rows_pad, K, ldx, codes,
+                                          scales, sg, status, zp, sp);
     }
     if (mode == NVFP4_SCALE_TENSOR_FP32 && ldx == K) {
         // contiguous x: the staged streaming passes (3 and 4 CTAs per SM)

@@ -7,8 +7,11 @@
 //
 // Exactness: an E4M3 value and an E2M1 x E4M3 product (at most 6 significant
 // bits, magnitudes 2^-10 .. 2688) are both exact in FP16, so converter warps
-// expand both operands to FP16 in shared memory and tcgen05.mma kind::f16
-// (FP16 x FP16 -> FP32) contracts them; no requantisation of the weights.
+// expand both operands to FP16 and tcgen05.mma kind::f16 (FP16 x FP16 ->
+// FP32) contracts them; no requantisation of the weights.  The activations
+// go to TMEM (the MMA's A operand may come from there) and only the weights
+// through shared memory: the kernel is bound by shared-memory traffic, and
+// the FP16 activations would be a third of it.
 // The block-scaled FP8 MMA kinds use power-of-two scales per 32 elements and
 // cannot carry the weights' E4M3 scales per 16 elements exactly.
 //
@@ -17,10 +20,13 @@
 //               and the W scale atoms per 64-element K step (raw ring); each
 //               copy of a step from its own lane (one thread's copies are
 //               served one after another, different threads' in parallel)
-//   warp 1      TMEM alloc (two 256-column accumulators); lane 0 issues
-//               4 x tcgen05.mma kind::f16 (M 128, N 256, K 16) per step
-//   warps 2..9  converters: raw ring -> FP16 tiles (128-byte swizzled rows);
-//               thread t expands half of A row t % 128 and W row t
+//   warp 1      TMEM alloc (one 256-column accumulator, then the FP16 A
+//               stages); lane 0 issues 4 x tcgen05.mma kind::f16 (M 128,
+//               N 256, K 16, A from TMEM) per step
+//   warps 2..9  converters: raw ring -> FP16.  Warp w expands its TMEM lane
+//               quarter's 32 A rows, K half (w - 2) / 4, into the step's TMEM
+//               A stage (tcgen05.st, 16 columns per lane); thread t expands
+//               W row t into a 128-byte swizzled shared-memory row
 //   warps 10..17 epilogue: TMEM -> registers 32 columns at a time,
 //               * s_t[m] * s_w, BF16/FP32 store
 // The grouped (mixture-of-experts) variant runs the same pipeline over the
@@ -44,8 +50,8 @@ constexpr int BN = 256;
 constexpr int NG = BN / 128;    // 128-row scale groups per W tile
 constexpr int KSTEP = 64;       // K elements per pipeline step
 constexpr int RAW_STAGES = 4;
-constexpr int CONV_STAGES = 3;
-constexpr int ACC_BUFS = 2;
+constexpr int CONV_STAGES = 4;
+constexpr int ACC_BUFS = 1;
 constexpr int CONV_WARPS = 8;
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_FIRST_WARP = 2 + CONV_WARPS;
@@ -54,16 +60,17 @@ constexpr int RAW_A = BM * KSTEP;           // 8192 B of FP8
 constexpr int RAW_W = BN * KSTEP / 2;       // 8192 B of FP4 codes
 constexpr int RAW_S = NG * 512;             // scale atoms
 constexpr int RAW_BYTES = RAW_A + RAW_W + RAW_S;
-constexpr int CONV_A = BM * 128;            // FP16 rows of 128 bytes
-constexpr int CONV_B = BN * 128;
-constexpr int CONV_BYTES = CONV_A + CONV_B;
+constexpr int CONV_B = BN * 128;            // FP16 W rows of 128 bytes
+constexpr int CONV_BYTES = CONV_B;
 constexpr int TMEM_COLS = 512;
+constexpr int A_COLS = KSTEP / 2;           // TMEM columns of one FP16 A stage (2 per column)
+constexpr int A_BASE = ACC_BUFS * BN;       // first A stage column
 constexpr int MAX_EXPERTS = 1024;
 static_assert(CONV_WARPS * 32 == 2 * BM && CONV_WARPS * 32 == BN, "converter thread mapping");
 constexpr int SMEM_BYTES = CONV_STAGES * CONV_BYTES + RAW_STAGES * RAW_BYTES + 256 + 1024;
 static_assert(RAW_BYTES % 1024 == 0 && CONV_BYTES % 1024 == 0, "alignment");
 static_assert(SMEM_BYTES + 4 * (MAX_EXPERTS + 2) <= 232448, "shared memory");
-static_assert(ACC_BUFS * BN <= TMEM_COLS, "TMEM");
+static_assert(A_BASE + CONV_STAGES * A_COLS <= TMEM_COLS, "TMEM");
 
 struct Params {
     CUtensorMap tmap_a; // FP8 [M][K]
@@ -367,12 +374,11 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
                         break;
                     }
                     tc_fence_after();
-                    const uint8_t *cA = conv + cs * CONV_BYTES;
-                    const uint64_t ad = sdesc_sw128(smem_u32(cA));
-                    const uint64_t bd = sdesc_sw128(smem_u32(cA + CONV_A));
+                    const uint64_t bd = sdesc_sw128(smem_u32(conv + cs * CONV_BYTES));
+                    const uint32_t ta = tmem + A_BASE + cs * A_COLS;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) { // 16 FP16 = 32 bytes per MMA
-                        mma_f16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, accumulate);
+                    for (int kk = 0; kk < 4; ++kk) { // 16 FP16 per MMA: 8 A columns, 32 B bytes
+                        mma_f16_ta(d, ta + 8 * kk, bd + (uint64_t)(kk * 2), idesc, accumulate);
                         accumulate = 1;
                     }
                     tc_commit(&conv_empty[cs]);
@@ -410,26 +416,25 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
                     break;
                 }
                 const uint8_t *r = raw + rs * RAW_BYTES;
-                uint8_t *cA = conv + cs * CONV_BYTES;
-                uint8_t *cB = cA + CONV_A;
-                // A row ar, half ah: 32 FP8 -> 32 FP16 = chunks 4 ah .. 4 ah + 3 (swizzled)
+                uint8_t *cB = conv + cs * CONV_BYTES;
+                // A rows of this warp's TMEM lane quarter, K half ah: 32 FP8
+                // -> 32 FP16 = 16 columns of the step's A stage in TMEM
                 {
-                    const int ar = t & (BM - 1), ah = t >> 7;
+                    const int quarter = warp & 3, ah = (warp - 2) >> 2;
+                    const int ar = quarter * 32 + lane;
                     const uint4 *src = reinterpret_cast<const uint4 *>(r + ar * KSTEP + ah * 32);
+                    uint32_t o[16];
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const uint4 v = src[h]; // 16 FP8 -> 2 output chunks
+                        const uint4 v = src[h]; // 16 FP8 -> 8 columns
                         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                        uint32_t o[8];
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            o[2 * q] = f16x2_from_e4m3x2(w[q] & 0xFFFFu);
-                            o[2 * q + 1] = f16x2_from_e4m3x2(w[q] >> 16);
+                            o[8 * h + 2 * q] = f16x2_from_e4m3x2(w[q] & 0xFFFFu);
+                            o[8 * h + 2 * q + 1] = f16x2_from_e4m3x2(w[q] >> 16);
                         }
-                        const int c0 = 4 * ah + 2 * h, c1 = c0 + 1;
-                        *reinterpret_cast<uint4 *>(cA + ar * 128 + ((c0 ^ (ar & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-                        *reinterpret_cast<uint4 *>(cA + ar * 128 + ((c1 ^ (ar & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
                     }
+                    tc_st_32x32b_x16(tmem + ((uint32_t)(quarter * 32) << 16) + A_BASE + cs * A_COLS + 16 * ah, o);
                 }
                 // W row t: 32 code bytes (64 E2M1) x 4 E4M3 scales -> 64 FP16
                 {
@@ -452,7 +457,11 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
                         *reinterpret_cast<uint4 *>(cB + t * 128 + ((c1 ^ (t & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
                     }
                 }
+                // A (TMEM stores) and W (shared memory) reach the tensor core
+                // before this warp's arrival
+                tc_wait_st();
                 fence_proxy_async_smem();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&conv_full[cs]);

@@ -358,6 +358,46 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
         : "memory");
 }
 
+// Single thread: D(tmem) (+)= A(tmem) x B(smem)^T, kind::f16 with the A
+// operand in TMEM (M = 128 rows in lanes 0..127, each 32-bit column holding
+// two consecutive K elements, K = 16 per instruction: 8 columns from a_tmem).
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate)
+{
+    if (kCheckBounds) {
+        const uint32_t n = ((idesc >> 17) & 0x3Fu) << 3;
+        const uint32_t b0 = ((uint32_t)(bdesc & 0x3FFFu) << 4) & ~1023u;
+        if (!(tmem_cols_ok(NV4_SITE(1), d_tmem, n) && tmem_cols_ok(NV4_SITE(1), a_tmem, 8) &&
+              aligned_to(NV4_SITE(1), a_tmem & 0xFFFFu, 8) && in_dyn_smem(NV4_SITE(1), b0, n * 128)))
+            return;
+    }
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Whole warp: 16 consecutive 32-bit columns into this warp's 32 TMEM lanes
+// (one row of 16 words per lane); taddr's column a multiple of 16.
+__device__ __forceinline__ void tc_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16])
+{
+    if (!(tmem_cols_ok(NV4_SITE(1), taddr, 16) && aligned_to(NV4_SITE(1), taddr & 0xFFFFu, 16)))
+        return; // taddr is the same in every lane
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+                 "%13, %14, %15, %16};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+                 "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+                 : "memory");
+}
+
+// Whole warp: every tcgen05.st of this thread has completed.
+__device__ __forceinline__ void tc_wait_st()
+{
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Single thread: copy 32 rows x 16 bytes from shared memory into TMEM lanes
 // 0..31 of 4 consecutive columns, replicated into all four lane quarters.
 __device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc)

@@ -48,8 +48,9 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-CUresult make_tmap_2d_u8(CUtensorMap *map, const void *base, uint64_t inner_bytes, uint64_t rows,
-                         uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128)
+CUresult make_tmap_2d_u8_swizzle(CUtensorMap *map, const void *base, uint64_t inner_bytes, uint64_t rows,
+                                 uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows,
+                                 CUtensorMapSwizzle swizzle)
 {
     auto fn = encode_fn();
     if (!fn)
@@ -59,8 +60,15 @@ CUresult make_tmap_2d_u8(CUtensorMap *map, const void *base, uint64_t inner_byte
     cuuint32_t box[2] = {box_inner, box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+CUresult make_tmap_2d_u8(CUtensorMap *map, const void *base, uint64_t inner_bytes, uint64_t rows,
+                         uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128)
+{
+    return make_tmap_2d_u8_swizzle(map, base, inner_bytes, rows, row_pitch_bytes, box_inner, box_rows,
+                                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // ---- workspace layout ------------------------------------------------------------

@@ -25,8 +25,9 @@
 //               N 256, K 16, A from TMEM) per step
 //   warps 2..9  converters: raw ring -> FP16.  Warp w expands its TMEM lane
 //               quarter's 32 A rows, K half (w - 2) / 4, into the step's TMEM
-//               A stage (tcgen05.st, 16 columns per lane); thread t expands
-//               W row t into a 128-byte swizzled shared-memory row
+//               A stage (tcgen05.st, 16 columns per lane); threads 2i, 2i+1
+//               expand the halves of W rows i and 128 + i into 128-byte
+//               swizzled shared-memory rows (no bank conflicts)
 //   warps 10..17 epilogue: TMEM -> registers 32 columns at a time,
 //               * s_t[m] * s_w, BF16/FP32 store
 // The grouped (mixture-of-experts) variant runs the same pipeline over the
@@ -329,7 +330,9 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
                             const bool in = live[q] && in_span(NV4_SITE(0), p.sp_a_fp8, srow + 16 * c, 16);
-                            cp_async_16(r + (lane + 32 * q) * KSTEP + 16 * c, srow + 16 * c, in ? 16u : 0u);
+                            // the TMA's 64-byte swizzle, applied by hand
+                            const int row = lane + 32 * q;
+                            cp_async_16(r + row * KSTEP + ((c ^ ((row >> 1) & 3)) << 4), srow + 16 * c, in ? 16u : 0u);
                         }
                     }
                     cp_async_arrive_noinc(&raw_full[st]);
@@ -422,11 +425,12 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
                 {
                     const int quarter = warp & 3, ah = (warp - 2) >> 2;
                     const int ar = quarter * 32 + lane;
-                    const uint4 *src = reinterpret_cast<const uint4 *>(r + ar * KSTEP + ah * 32);
                     uint32_t o[16];
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const uint4 v = src[h]; // 16 FP8 -> 8 columns
+                        // chunk 2 ah + h of the row, 64-byte swizzled
+                        const uint4 v = *reinterpret_cast<const uint4 *>(
+                            r + ar * KSTEP + (((2 * ah + h) ^ ((ar >> 1) & 3)) << 4)); // 16 FP8 -> 8 columns
                         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
@@ -436,25 +440,33 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
                     }
                     tc_st_32x32b_x16(tmem + ((uint32_t)(quarter * 32) << 16) + A_BASE + cs * A_COLS + 16 * ah, o);
                 }
-                // W row t: 32 code bytes (64 E2M1) x 4 E4M3 scales -> 64 FP16
-                {
-                    const uint8_t *wr = r + RAW_A + t * (KSTEP / 2);
-                    const uint32_t sc = *reinterpret_cast<const uint32_t *>(
-                        r + RAW_A + RAW_W + (t >> 7) * 512 + (t & 31) * 16 + ((t & 127) >> 5) * 4);
+                // W: two threads per row, each half a row (16 code bytes = two
+                // 16-element blocks) x their E4M3 scales -> 32 FP16, rows
+                // t / 2 and 128 + t / 2.  Eight threads of a load cover four
+                // whole 32-byte rows, and their stores land in eight
+                // different 16-byte chunk positions: no bank conflicts
 #pragma unroll
-                    for (int b = 0; b < 4; ++b) { // 16-element block b uses scale byte b
+                for (int pass = 0; pass < 2; ++pass) {
+                    const int wrow = pass * 128 + (t >> 1), hw = t & 1;
+                    const uint4 v = *reinterpret_cast<const uint4 *>(r + RAW_A + wrow * (KSTEP / 2) + hw * 16);
+                    const uint32_t sc = *reinterpret_cast<const uint32_t *>(
+                        r + RAW_A + RAW_W + (wrow >> 7) * 512 + (wrow & 31) * 16 + ((wrow & 127) >> 5) * 4);
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int bb = 0; bb < 2; ++bb) { // 16-element block b = 2 hw + bb uses scale byte b
+                        const int b = 2 * hw + bb;
                         const uint32_t s2 = f16x2_from_e4m3x2(((sc >> (8 * b)) & 0xFFu) * 0x0101u);
-                        const uint2 v = *reinterpret_cast<const uint2 *>(wr + b * 8);
-                        const uint32_t w[2] = {v.x, v.y};
                         uint32_t o[8];
 #pragma unroll
                         for (int q = 0; q < 2; ++q)
 #pragma unroll
                             for (int y = 0; y < 4; ++y)
-                                o[4 * q + y] = hmul2_u32(f16x2_from_e2m1x2((w[q] >> (8 * y)) & 0xFFu), s2);
+                                o[4 * q + y] = hmul2_u32(f16x2_from_e2m1x2((w4[2 * bb + q] >> (8 * y)) & 0xFFu), s2);
                         const int c0 = 2 * b, c1 = 2 * b + 1;
-                        *reinterpret_cast<uint4 *>(cB + t * 128 + ((c0 ^ (t & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-                        *reinterpret_cast<uint4 *>(cB + t * 128 + ((c1 ^ (t & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+                        *reinterpret_cast<uint4 *>(cB + wrow * 128 + ((c0 ^ (wrow & 7)) << 4)) =
+                            make_uint4(o[0], o[1], o[2], o[3]);
+                        *reinterpret_cast<uint4 *>(cB + wrow * 128 + ((c1 ^ (wrow & 7)) << 4)) =
+                            make_uint4(o[4], o[5], o[6], o[7]);
                     }
                 }
                 // A (TMEM stores) and W (shared memory) reach the tensor core
@@ -581,7 +593,11 @@ cudaError_t launch_w4a8(const W4A8GemmArgs &g, cudaStream_t stream)
     const bool grouped = g.E > 0;
     const int64_t w_rows = grouped ? (int64_t)g.E * g.N : g.N;
     Params p{};
-    CUresult r = make_tmap_2d_u8(&p.tmap_a, g.a_fp8, (uint64_t)g.K, (uint64_t)g.M, (uint64_t)g.K, KSTEP, BM, false);
+    // the raw FP8 A tile with the 64-byte swizzle: 16-byte chunk c of row r
+    // lands at chunk c ^ ((r / 2) % 4), so the converters' per-row reads hit
+    // every bank once
+    CUresult r = make_tmap_2d_u8_swizzle(&p.tmap_a, g.a_fp8, (uint64_t)g.K, (uint64_t)g.M, (uint64_t)g.K, KSTEP, BM,
+                                         CU_TENSOR_MAP_SWIZZLE_64B);
     if (r != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     r = make_tmap_2d_u8(&p.tmap_w, g.w_codes, (uint64_t)(g.K / 2), (uint64_t)w_rows, (uint64_t)(g.K / 2), KSTEP / 2,

@@ -262,6 +262,9 @@ cudaError_t launch_w4a4_macro(const MacroGemmArgs &g, cudaStream_t stream);
 // Tensor-map creation through the driver entry point (no libcuda link).
 CUresult make_tmap_2d_u8(CUtensorMap *map, const void *base, uint64_t inner_bytes, uint64_t rows,
                          uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128);
+CUresult make_tmap_2d_u8_swizzle(CUtensorMap *map, const void *base, uint64_t inner_bytes, uint64_t rows,
+                                 uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows,
+                                 CUtensorMapSwizzle swizzle);
 
 
 } // namespace nv4

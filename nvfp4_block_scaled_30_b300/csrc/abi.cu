@@ -86,8 +86,6 @@ struct WsLayout {
     size_t total = 0;
 };
 
-static constexpr int64_t SPLITK_MAX_M = 128;
-
 static WsLayout ws_layout(int op, int64_t M, int64_t N, int64_t K, int64_t E = 0)
 {
     WsLayout L;
@@ -116,7 +114,7 @@ static WsLayout ws_layout(int op, int64_t M, int64_t N, int64_t K, int64_t E = 0
         if (pb)
             L.kv_partial = take(pb);
     }
-    if (op == NVFP4_OP_GEMM && M <= SPLITK_MAX_M) {
+    if (op == NVFP4_OP_GEMM) {
         const StreamKPlan pl = w4a4_streamk_plan(M, N, K, device_sm_count());
         if (pl.used) {
             L.sk_slots = take(pl.slot_bytes);

@@ -11,14 +11,27 @@
 namespace nv4 {
 
 // Where element (i, j) of the output goes: out[i * ld_i + j * ld_j]; vec_ok
-// when ld_j == 1 and 16-byte vector stores of a row are aligned; span: the
-// output's bytes (tested in the bounds-checked build).
+// 1 when ld_j == 1 and 16-byte vector stores of a row are aligned, 2 when
+// 32-byte ones are too; span: the output's bytes (tested in the
+// bounds-checked build).
 struct OutDesc {
     void *out;
     int64_t ld_i, ld_j;
     int32_t out_dtype, vec_ok;
     Span span;
 };
+
+// Host: OutDesc.vec_ok of an output at `out` with strides (ld_i, ld_j) in
+// elements of esz bytes.
+inline int32_t out_vec_level(const void *out, int64_t ld_i, int64_t ld_j, int esz)
+{
+    if (ld_j != 1)
+        return 0;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(out);
+    if ((ld_i * esz) % 32 == 0 && a % 32 == 0)
+        return 2;
+    return ((ld_i * esz) % 16 == 0 && a % 16 == 0) ? 1 : 0;
+}
 
 // Spans of an NVFP4 output's codes and tiled scales.
 struct QSpans {
@@ -73,6 +86,106 @@ __device__ __forceinline__ void store_chunk32(const OutDesc &o, const uint32_t (
             }
         }
     }
+}
+
+// 256-bit global store (sm_100 and later): one whole 32-byte sector.
+__device__ __forceinline__ void st_global_v8(void *ptr, const uint32_t (&r)[8])
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
+// One warp's rows r0 .. r0 + 31 (lane l holds row r0 + l), a run of 64
+// bytes per row in w (two 32-byte pieces of 8 words), stored so that each
+// store instruction writes whole runs of 16 rows.  Lane l stores piece l % 2
+// of row 16 s + l / 2 in instruction s; in exchange round a the lanes holding
+// rows of instruction s = a ^ (l % 2) send, each source lane the piece its
+// receiver stores, so every round moves 32 distinct words per word index (a
+// transpose by shuffles, no shared memory).  Rows outside [i_lo, i_hi) are
+// not stored; row i's run starts at base + i * row_bytes.  Every lane of the
+// warp calls this.
+__device__ __forceinline__ void store_rows64(const uint32_t (&w)[16], uint8_t *base, int64_t row_bytes, int64_t r0,
+                                             int64_t i_lo, int64_t i_hi, const Span &span, int lane)
+{
+    const int piece = lane & 1;  // the piece this lane stores
+    const int rsub = lane >> 1;  // its row within an instruction's 16 rows
+    const int s_own = lane >> 4; // the instruction this lane's own row goes out in
+    uint32_t o[2][8];
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+        const int src = 16 * (a ^ piece) + rsub;
+        const bool give1 = (s_own ^ a) != 0; // the receiver stores piece 1
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t got = __shfl_sync(0xFFFFFFFFu, give1 ? w[8 + k] : w[k], src);
+            if ((a ^ piece) == 0)
+                o[0][k] = got;
+            else
+                o[1][k] = got;
+        }
+    }
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+        const int64_t i = r0 + 16 * s + rsub;
+        uint8_t *d = base + i * row_bytes + 32 * piece;
+        if (i >= i_lo && i < i_hi && in_span(NV4_SITE(2), span, d, 32))
+            st_global_v8(d, o[s]);
+    }
+}
+
+// The BF16 words of 32 consecutive columns of one row: accumulator bits v
+// times alpha, two columns per word.
+__device__ __forceinline__ void pack_bf16x32(const uint32_t (&v)[32], float alpha, uint32_t (&w)[16])
+{
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        __nv_bfloat162 h =
+            __floats2bfloat162_rn(alpha * __uint_as_float(v[2 * q]), alpha * __uint_as_float(v[2 * q + 1]));
+        w[q] = *reinterpret_cast<uint32_t *>(&h);
+    }
+}
+
+// Whether one warp's rows can go out through store_rows64 for the run of 32
+// columns at j0: 32-byte aligned rows (vec_ok == 2), unit column stride and
+// the whole run inside the output (warp-uniform).
+__device__ __forceinline__ bool rows64_ok(const OutDesc &o, int64_t j0, int64_t j_end)
+{
+    return o.ld_j == 1 && o.vec_ok == 2 && j0 + 32 <= j_end;
+}
+
+// Rows r0 .. r0 + 31 of one warp (lane l: row r0 + l, accumulator bits of
+// columns j0 .. j0 + 31 in v) times alpha (each lane its own), rows outside
+// [i_lo, i_hi) and columns >= j_end not stored: by store_rows64 (BF16 as one
+// 64-byte run per row, FP32 as two) when rows64_ok, else row by row through
+// store_chunk32.  Every lane calls this.
+__device__ __forceinline__ void store_chunk32_warp(const OutDesc &o, const uint32_t (&v)[32], int64_t r0,
+                                                   int64_t i_lo, int64_t i_hi, int64_t j0, float alpha,
+                                                   int64_t j_end, int lane)
+{
+    if (r0 >= i_hi || r0 + 32 <= i_lo) // no row of this warp is stored (warp-uniform)
+        return;
+    if (rows64_ok(o, j0, j_end)) {
+        if (o.out_dtype == NVFP4_OUT_BF16) {
+            uint32_t w[16];
+            pack_bf16x32(v, alpha, w);
+            store_rows64(w, reinterpret_cast<uint8_t *>(static_cast<__nv_bfloat16 *>(o.out) + j0), o.ld_i * 2, r0,
+                         i_lo, i_hi, o.span, lane);
+        } else {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t w[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    w[q] = __float_as_uint(alpha * __uint_as_float(v[16 * h + q]));
+                store_rows64(w, reinterpret_cast<uint8_t *>(static_cast<float *>(o.out) + j0 + 16 * h), o.ld_i * 4,
+                             r0, i_lo, i_hi, o.span, lane);
+            }
+        }
+        return;
+    }
+    const int64_t i = r0 + lane;
+    store_chunk32(o, v, i, j0, alpha, i >= i_lo ? i_hi : i, j_end);
 }
 
 // NVFP4 store of 32 consecutive outputs y (binary32 bits in v) of one row

@@ -21,6 +21,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "epilogue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -317,6 +318,7 @@ __global__ void __launch_bounds__(THREADS, 1) macro_kernel(const __grid_constant
         const int half = (warp - EPI_FIRST_WARP) >> 2;
         const int row = q * 32 + lane;
         const int et = threadIdx.x - 32 * EPI_FIRST_WARP; // 0 .. 32 * EPI_WARPS - 1
+        const OutDesc out_desc{p.out, p.ldy, 1, p.out_dtype, p.vec_ok, p.sp_out};
         int pb = 0;
         uint32_t pph = 0;
         bool ok = true;
@@ -416,43 +418,14 @@ __global__ void __launch_bounds__(THREADS, 1) macro_kernel(const __grid_constant
             ok = epi_bar_all(ok);
             if (!ok)
                 break;
-            if (i < p.M) {
-                if (p.vec_ok && j0 + 64 <= p.N) {
-                    if (p.out_dtype == NVFP4_OUT_BF16) {
-                        uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + i * p.ldy + j0);
+            // the warp's 32 rows together (32-byte stores of whole row runs)
 #pragma unroll
-                        for (int c = 0; c < 64; c += 8) {
-                            if (!in_span(NV4_SITE(0), p.sp_out, o + c / 8, 16))
-                                continue;
-                            uint32_t w[4];
+            for (int h = 0; h < 2; ++h) {
+                uint32_t v[32];
 #pragma unroll
-                            for (int z = 0; z < 4; ++z) {
-                                __nv_bfloat162 h = __floats2bfloat162_rn(acc[c + 2 * z], acc[c + 2 * z + 1]);
-                                w[z] = *reinterpret_cast<uint32_t *>(&h);
-                            }
-                            o[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
-                        }
-                    } else {
-                        float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + i * p.ldy + j0);
-#pragma unroll
-                        for (int c = 0; c < 64; c += 4)
-                            if (in_span(NV4_SITE(0), p.sp_out, o + c / 4, 16))
-                                o[c / 4] = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) {
-                        if (j0 + c < p.N) {
-                            const int64_t off = i * p.ldy + j0 + c;
-                            if (p.out_dtype == NVFP4_OUT_BF16) {
-                                if (in_span(NV4_SITE(0), p.sp_out, static_cast<__nv_bfloat16 *>(p.out) + off, 2))
-                                    static_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(acc[c]);
-                            } else if (in_span(NV4_SITE(0), p.sp_out, static_cast<float *>(p.out) + off, 4)) {
-                                static_cast<float *>(p.out)[off] = acc[c];
-                            }
-                        }
-                    }
-                }
+                for (int k = 0; k < 32; ++k)
+                    v[k] = __float_as_uint(acc[32 * h + k]);
+                store_chunk32_warp(out_desc, v, i - lane, 0, p.M, j0 + 32 * h, 1.0f, p.N, lane);
             }
         }
     }
@@ -494,7 +467,7 @@ cudaError_t launch_w4a4_macro(const MacroGemmArgs &g, cudaStream_t stream)
     p.groups = (int)(g.K / 256);
     p.out_dtype = g.out_dtype;
     const int esz = g.out_dtype == NVFP4_OUT_BF16 ? 2 : 4;
-    p.vec_ok = ((g.ldy * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(g.out) % 16) == 0) ? 1 : 0;
+    p.vec_ok = out_vec_level(g.out, g.ldy, 1, esz);
     p.status = g.status;
     p.timeout_ns = g.timeout_ns;
     p.sp_sfa = span_of(g.a_scales, tiled_scale_bytes(g.M, g.K));

@@ -913,8 +913,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                         for (int u = 0; u < 32; u += 4)
                             if (in_span(NV4_SITE(0), p.sp_slots, slot + c * 32 + u, 16))
                                 __stcg(reinterpret_cast<float4 *>(slot + c * 32 + u),
-                                   make_float4(__uint_as_float(v[c][u]), __uint_as_float(v[c][u + 1]),
-                                               __uint_as_float(v[c][u + 2]), __uint_as_float(v[c][u + 3])));
+                                       make_float4(__uint_as_float(v[c][u]), __uint_as_float(v[c][u + 1]),
+                                                   __uint_as_float(v[c][u + 2]), __uint_as_float(v[c][u + 3])));
                 }
                 epi_bar_sync();
                 // (diag_skip_flag: a test names one CTA that never raises its
@@ -965,12 +965,14 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                     break;
                 }
                 const int et = threadIdx.x - 32 * EPI_FIRST_WARP;
-                const int rows = (int)(i_end < BM ? i_end : BM); // one M-tile: rows 0..a_rows-1
+                const int64_t r0 = (int64_t)t.tile_m * BM; // dense: i_end = a_rows
+                const int rows = (int)(i_end - r0 < BM ? i_end - r0 : BM);
                 const int64_t c0 = (int64_t)t.tile_n * BN;
                 const int cols = (int)(j_end - c0 < BN ? j_end - c0 : BN);
                 // 4 consecutive columns per thread and position; UB positions
-                // per round with all their slot loads in flight together
-                constexpr int UB = 8;
+                // per round, the slot loads of CB contributors in flight
+                // together (the partials are added in contributor order)
+                constexpr int UB = 4, CB = 4;
                 constexpr int STEP = 4 * 32 * EPI_WARPS;
                 const int total4 = rows * BN;
                 for (int base = et * 4; base < total4; base += UB * STEP) {
@@ -983,23 +985,31 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                                       ? *reinterpret_cast<const float4 *>(tile_s + r * RS + cc)
                                       : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
-                    for (int c = 1; c <= n_contrib; ++c) {
-                        const float *slot = p.slots + (size_t)(blockIdx.x + c) * p.slot_stride;
-                        float4 w4[UB];
+                    for (int c0 = 1; c0 <= n_contrib; c0 += CB) {
+                        float4 w4[CB][UB];
 #pragma unroll
-                        for (int u = 0; u < UB; ++u) {
-                            const int e4 = base + u * STEP;
-                            w4[u] = e4 < total4 && in_span(NV4_SITE(0), p.sp_slots, slot + e4, 16)
-                                        ? __ldcg(reinterpret_cast<const float4 *>(slot + e4))
-                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int b = 0; b < CB; ++b) {
+                            const float *slot = p.slots + (size_t)(blockIdx.x + c0 + b) * p.slot_stride;
+#pragma unroll
+                            for (int u = 0; u < UB; ++u) {
+                                const int e4 = base + u * STEP;
+                                w4[b][u] = c0 + b <= n_contrib && e4 < total4 &&
+                                                   in_span(NV4_SITE(0), p.sp_slots, slot + e4, 16)
+                                               ? __ldcg(reinterpret_cast<const float4 *>(slot + e4))
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
                         }
 #pragma unroll
-                        for (int u = 0; u < UB; ++u) {
-                            acc4[u].x += w4[u].x;
-                            acc4[u].y += w4[u].y;
-                            acc4[u].z += w4[u].z;
-                            acc4[u].w += w4[u].w;
-                        }
+                        for (int b = 0; b < CB; ++b)
+#pragma unroll
+                            for (int u = 0; u < UB; ++u) {
+                                if (c0 + b > n_contrib)
+                                    continue;
+                                acc4[u].x += w4[b][u].x;
+                                acc4[u].y += w4[b][u].y;
+                                acc4[u].z += w4[b][u].z;
+                                acc4[u].w += w4[b][u].w;
+                            }
                     }
 #pragma unroll
                     for (int u = 0; u < UB; ++u) {
@@ -1009,7 +1019,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                         const int r = e4 / BN, cc = e4 - r * BN;
                         const float y4[4] = {alpha * acc4[u].x, alpha * acc4[u].y, alpha * acc4[u].z,
                                              alpha * acc4[u].w};
-                        const int64_t row = r;
+                        const int64_t row = r0 + r;
                         if (p.vec_ok && cc + 4 <= cols) {
                             if (p.out_dtype == NVFP4_OUT_BF16) {
                                 __nv_bfloat162 h0 = __floats2bfloat162_rn(y4[0], y4[1]);
@@ -1048,9 +1058,27 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                             p.flags[blockIdx.x + c] = 0u;
                 continue;
             }
+            const int64_t r0 = i - lane; // the warp's first row
+            const int64_t i_lo = GROUPED ? t.row_lo : 0, i_hi = GROUPED ? t.row_end : p.a_rows;
+            if (p.out_dtype == NVFP4_OUT_BF16 && rows64_ok(out_desc(p), j_base, j_end - 32 * (NCH - 1))) {
+                // BF16 with 32-byte aligned rows: the whole slice packed first
+                // (half the registers), then the warp's 32 rows together as
+                // whole 64-byte runs
+                if (r0 < i_hi && r0 + 32 > i_lo) {
+                    uint32_t w[NCH][16];
 #pragma unroll
-            for (int c = 0; c < NCH; ++c)
-                store_chunk32(out_desc(p), v[c], i, j_base + c * 32, alpha, i_end, j_end);
+                    for (int c = 0; c < NCH; ++c)
+                        pack_bf16x32(v[c], alpha, w[c]);
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c)
+                        store_rows64(w[c], reinterpret_cast<uint8_t *>(static_cast<__nv_bfloat16 *>(p.out) + j_base + c * 32),
+                                     p.ld_i * 2, r0, i_lo, i_hi, p.sp_out, lane);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < NCH; ++c)
+                    store_chunk32(out_desc(p), v[c], i, j_base + c * 32, alpha, i < i_lo ? i : i_hi, j_end);
+            }
         }
     } else if (GROUPED && indexed) {
         // ------------------------------------------------------------ gather warp
@@ -1212,22 +1240,27 @@ int w4a4_dense_bn(int64_t b_rows)
 StreamKPlan w4a4_streamk_plan(int64_t M, int64_t N, int64_t K, int sms)
 {
     StreamKPlan pl;
-    if (M <= 0 || M > BM || N <= 0 || K <= 0 || sms <= 0)
+    if (M <= 0 || N <= 0 || K <= 0 || sms <= 0)
         return pl;
     const int bn = w4a4_dense_bn(N);
-    const int64_t tiles = ceil_div(N, bn);
+    const int64_t tiles = ceil_div(M, BM) * ceil_div(N, bn);
     const int64_t kstages = ceil_div(ceil_div(K, 64), 4);
     // M <= 128 is bound by streaming the weights.  Measured on B300 (M = 8 to
     // 128, K = 8192): 112 whole tiles of N = 28672 already keep HBM busy and
     // beat stream-K at every M (its partial reduction only adds a tail),
     // while 16 tiles (N = 4096) leave most SMs idle and stream-K is 1.5x
-    // faster.  So stream-K only when the tiles cover under 60% of the SMs
-    // and there is enough K to share.
-    if (!(tiles * 10 < 6 * (int64_t)sms && tiles * kstages >= 2 * (int64_t)sms))
+    // faster.  So stream-K only when the tiles cover under 60% of the SMs and
+    // there is enough K to share.  Several M tiles (compute-bound) run whole
+    // tiles: measured on [2048, 4096] x [4096, 4096] (256 tiles, 1.73 waves),
+    // stream-K took 41 us against 33 us for whole tiles of the wider [2048,
+    // 4352] x [4096, 4352] (272 tiles), its FP32 partial tiles (128 KB per
+    // CTA) moving through L2 at ~30-60 GB/s per SM, far more than the part
+    // of a wave it saves.
+    if (M > BM || !(tiles * 10 < 6 * (int64_t)sms && tiles * kstages >= 2 * (int64_t)sms))
         return pl;
     pl.used = true;
     pl.grid = (int)std::min<int64_t>(tiles * kstages, sms);
-    pl.slot_bytes = align_up((size_t)pl.grid * (size_t)M * (size_t)bn * 4, 256);
+    pl.slot_bytes = align_up((size_t)pl.grid * (size_t)std::min<int64_t>(M, BM) * (size_t)bn * 4, 256);
     pl.flag_bytes = align_up((size_t)pl.grid * 4, 256);
     return pl;
 }
@@ -1280,9 +1313,9 @@ cudaError_t launch_w4a4_dense(const DenseGemmArgs &g, cudaStream_t stream)
     p.yq_n = g.b_rows;
     p.slots = g.slots;
     p.flags = g.flags;
-    p.slot_stride = g.a_rows * bn;
+    p.slot_stride = std::min<int64_t>(g.a_rows, BM) * bn; // rows of one M tile
     const int esz = g.out_dtype == NVFP4_OUT_BF16 ? 2 : 4;
-    p.vec_ok = (g.ld_j == 1 && (g.ld_i * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(g.out) % 16) == 0) ? 1 : 0;
+    p.vec_ok = out_vec_level(g.out, g.ld_i, g.ld_j, esz);
     p.b_row_tiles = (int)ceil_div(g.b_rows, 128);
     p.offsets = nullptr;
     p.row_idx = nullptr;
@@ -1340,7 +1373,7 @@ cudaError_t launch_w4a4_grouped(const GroupedGemmArgs &g, cudaStream_t stream)
     p.b_rows = g.N;
     p.out_dtype = g.out_dtype;
     const int esz = g.out_dtype == NVFP4_OUT_BF16 ? 2 : 4;
-    p.vec_ok = ((g.ldy * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(g.out) % 16) == 0) ? 1 : 0;
+    p.vec_ok = out_vec_level(g.out, g.ldy, 1, esz);
     p.b_row_tiles = (int)ceil_div(g.E * g.N, 128);
     p.diag_skip_flag = -1;
     p.epi = g.epi;

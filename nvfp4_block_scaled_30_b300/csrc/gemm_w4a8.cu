@@ -39,6 +39,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "epilogue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -495,6 +496,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                     // the TMEM lane quarter this warp may access
         const int chalf = (warp - EPI_FIRST_WARP) >> 2; // which 128 accumulator columns
+        const OutDesc out_desc{p.out, p.ldy, 1, p.out_dtype, p.vec_ok, p.sp_out};
         const int row = q * 32 + lane;
         int acc = 0;
         uint32_t aph = 0;
@@ -524,46 +526,10 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_kernel(const __grid_constant_
                 uint32_t v[32];
                 tc_ld_32x32b_x32(tb + c0, v);
                 tc_wait_ld();
-                if (row_ok) {
-                    const int64_t j0 = (int64_t)tn * BN + c0;
-                    if (p.vec_ok && j0 + 32 <= p.N) {
-                        if (p.out_dtype == NVFP4_OUT_BF16) {
-                            uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + i * p.ldy + j0);
-                            if (!in_span(NV4_SITE(0), p.sp_out, o, 64))
-                                continue;
-#pragma unroll
-                            for (int c = 0; c < 32; c += 8) {
-                                uint32_t w[4];
-#pragma unroll
-                                for (int z = 0; z < 4; ++z) {
-                                    __nv_bfloat162 h = __floats2bfloat162_rn(alpha * __uint_as_float(v[c + 2 * z]),
-                                                                             alpha * __uint_as_float(v[c + 2 * z + 1]));
-                                    w[z] = *reinterpret_cast<uint32_t *>(&h);
-                                }
-                                o[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
-                            }
-                        } else {
-                            float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + i * p.ldy + j0);
-                            if (!in_span(NV4_SITE(0), p.sp_out, o, 128))
-                                continue;
-#pragma unroll
-                            for (int c = 0; c < 32; c += 4)
-                                o[c / 4] = make_float4(alpha * __uint_as_float(v[c]), alpha * __uint_as_float(v[c + 1]),
-                                                       alpha * __uint_as_float(v[c + 2]), alpha * __uint_as_float(v[c + 3]));
-                        }
-                    } else {
-                        for (int c = 0; c < 32 && j0 + c < p.N; ++c) {
-                            const float y = alpha * __uint_as_float(v[c]);
-                            const int64_t off = i * p.ldy + j0 + c;
-                            if (p.out_dtype == NVFP4_OUT_BF16) {
-                                if (in_span(NV4_SITE(0), p.sp_out, static_cast<__nv_bfloat16 *>(p.out) + off, 2))
-                                    static_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(y);
-                            } else if (in_span(NV4_SITE(0), p.sp_out, static_cast<float *>(p.out) + off, 4)) {
-                                static_cast<float *>(p.out)[off] = y;
-                            }
-                        }
-                    }
-                }
+                // the warp's 32 rows together (32-byte stores of whole row
+                // runs; each lane scales its own row by its alpha)
+                store_chunk32_warp(out_desc, v, it.row0 + q * 32, it.row0, it.row_end, (int64_t)tn * BN + c0,
+                                   alpha, p.N, lane);
             }
             tc_fence_before();
             __syncwarp();
@@ -618,7 +584,7 @@ cudaError_t launch_w4a8(const W4A8GemmArgs &g, cudaStream_t stream)
     p.w_groups = (int)ceil_div(w_rows, 128);
     p.out_dtype = g.out_dtype;
     const int esz = g.out_dtype == NVFP4_OUT_BF16 ? 2 : 4;
-    p.vec_ok = ((g.ldy * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(g.out) % 16) == 0) ? 1 : 0;
+    p.vec_ok = out_vec_level(g.out, g.ldy, 1, esz);
     p.status = g.status;
     p.timeout_ns = g.timeout_ns;
     p.a_fp8 = g.a_fp8;

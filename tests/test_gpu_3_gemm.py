@@ -222,6 +222,32 @@ def test_many_tile_shapes(M, N, K, out_dtype):
     _check(y_np(y), ref, f"{M}x{N}x{K}", out_dtype == nv.OUT_BF16)
 
 
+# The epilogue stores whole 32-byte row runs when every row of the output
+# starts 32-byte aligned, 16-byte vectors when only 16-byte alignment holds
+# and single elements otherwise: row strides and column offsets that give
+# each level, for both output types, with the bytes around y untouched.
+@pytest.mark.parametrize("out_dtype", [nv.OUT_BF16, nv.OUT_FP32])
+# (row length N + extra elements, first column col0)
+@pytest.mark.parametrize("extra,col0", [(0, 0), (8, 0), (16, 8), (32, 16), (3, 0)])
+def test_output_alignment_levels(out_dtype, extra, col0):
+    M, N, K = 300, 512, 512
+    xb = synth.activations(9, 46, M, K, 0.01, 50.0)
+    wb = synth.weights(9, 47, N, K)
+    w, wc, ws, wg = quantize_pinned(wb)
+    tdt = torch.bfloat16 if out_dtype == nv.OUT_BF16 else torch.float32
+    big = torch.full((M, N + extra), 7.0, dtype=tdt, device="cuda")
+    nv.gemm(w, x=dev_bf16(xb), y=big[:, col0:col0 + N], out_dtype=out_dtype)
+    full = y_np(big)
+    ref = oracle.gemm_w4a4(oracle.nvfp4_encode(xb), (wc, ws, wg[0]))
+    _check(full[:, col0:col0 + N], ref, f"ld +{extra}, col {col0}", out_dtype == nv.OUT_BF16)
+    assert (full[:, :col0] == 7.0).all() and (full[:, col0 + N:] == 7.0).all()
+    if out_dtype == nv.OUT_BF16 and extra >= 4:
+        # an output that does not start 16-byte aligned is refused
+        with pytest.raises(nv.NVFP4Error) as e:
+            nv.gemm(w, x=dev_bf16(xb), y=big[:, 4:4 + N], out_dtype=out_dtype)
+        assert e.value.status == nv.ERR_INVALID_ARG
+
+
 def test_output_row_stride_and_empty():
     xb, wb = _layer(1, 40, 256, 512)
     w, wc, ws, wg = quantize_pinned(wb)

@@ -280,11 +280,78 @@ def workload_decode(c, M, steps, warmup, rot=4, with_e2e=False, peaks_=None):
         # CUDA graph, copies included, as a serving loop would replay them
         ems = min(c.time(e2e, steps, warmup, graph=False) for _ in range(3))
         gms_e2e = c.time(e2e, steps, warmup, graph=True)
-        res["e2e"] = {"value": step_bytes / (ems * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ems,
-                      "value_graph": step_bytes / (gms_e2e * 1e-3) / 1e9, "ms_per_step_graph": gms_e2e,
+        pms = e2e_pipelined(c, W, rot, hx, M, N, K, work, steps, warmup)
+        res["e2e"] = {"value": step_bytes / (pms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": pms,
+                      "how": "pipelined: step i's input copy, step i-1's GEMM and step i-2's result copy "
+                             "in flight together (copy-in, compute and copy-out streams, double-buffered "
+                             "device X and Y, ordered by events), captured into one CUDA graph",
+                      "value_serial_python": step_bytes / (ems * 1e-3) / 1e9, "ms_per_step_serial_python": ems,
+                      "value_serial_graph": step_bytes / (gms_e2e * 1e-3) / 1e9,
+                      "ms_per_step_serial_graph": gms_e2e,
                       "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": M * N * 2}
     del W
     return res
+
+
+def e2e_pipelined(c, W, rot, hx, M, N, K, work, steps, warmup):
+    """End to end with the copies overlapped across steps, as a serving loop
+    runs them: every step still copies its input from pinned host memory and
+    its result back, but step i's input copy, the GEMM of step i - 1 and the
+    result copy of step i - 2 run together on three streams.  Device X and Y
+    are double-buffered; events order each buffer's reuse (the copy into
+    X[b] waits for the GEMM that read it two steps before, the GEMM into
+    Y[b] for the copy-out that read it).  The whole loop is captured into
+    one CUDA graph; ms per step of one timed replay."""
+    t, nv = c.torch, c.nv
+    xd = [t.empty((M, K), dtype=t.int16, device=c.dev) for _ in range(2)]
+    yd = [t.empty((M, N), dtype=t.bfloat16, device=c.dev) for _ in range(2)]
+    hy = [t.empty((M, N), dtype=t.int16).pin_memory() for _ in range(2)]
+    s_in, s_out = t.cuda.Stream(), t.cuda.Stream()
+
+    def body(n, base):
+        main = t.cuda.current_stream()
+        fork = t.cuda.Event()
+        fork.record(main)
+        s_in.wait_event(fork)
+        s_out.wait_event(fork)
+        done_cmp, done_out = [None, None], [None, None]
+        last_in = last_out = None
+        for i in range(n):
+            b = i % 2
+            with t.cuda.stream(s_in):
+                if done_cmp[b] is not None:
+                    s_in.wait_event(done_cmp[b])
+                xd[b].copy_(hx, non_blocking=True)
+                last_in = t.cuda.Event()
+                last_in.record(s_in)
+            main.wait_event(last_in)
+            if done_out[b] is not None:
+                main.wait_event(done_out[b])
+            nv.gemm(W[(base + i) % rot], x=xd[b].view(t.bfloat16), y=yd[b], ws=work)
+            done_cmp[b] = t.cuda.Event()
+            done_cmp[b].record(main)
+            with t.cuda.stream(s_out):
+                s_out.wait_event(done_cmp[b])
+                hy[b].copy_(yd[b].view(t.int16), non_blocking=True)
+                done_out[b] = t.cuda.Event()
+                done_out[b].record(s_out)
+                last_out = done_out[b]
+        main.wait_event(last_in)   # join both side streams
+        main.wait_event(last_out)
+
+    body(warmup, 0)
+    t.cuda.synchronize()
+    g = t.cuda.CUDAGraph()
+    with t.cuda.graph(g, capture_error_mode="relaxed"):
+        body(steps, warmup)
+    g.replay()  # one untimed replay
+    t.cuda.synchronize()
+    s, e = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+    s.record()
+    g.replay()
+    e.record()
+    t.cuda.synchronize()
+    return s.elapsed_time(e) / steps
 
 
 def workload_prefill(c, N, steps, warmup, rot=2, x_rot=3):

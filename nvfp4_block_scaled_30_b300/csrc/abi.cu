@@ -624,7 +624,7 @@ nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor *a, const int32_t *row_idx, c
     if (route < 0)
         return NVFP4_ERR_INVALID_ARG;
     if (route == 8)
-        return NVFP4_ERR_UNSUPPORTED; // grouped W4A8 is not implemented
+        return NVFP4_ERR_UNSUPPORTED; // W4A8 needs FP8 activations: nvfp4_grouped_gemm_x / _w4a8_gemm
     GroupedGemmArgs g;
     nvfp4_status st = grouped_args(a, row_idx, expert_offsets, E, w, N, total_rows, ws, ws_bytes, g);
     if (st != NVFP4_OK)

@@ -42,7 +42,9 @@ def test_macro_gemm_against_oracle(M, N, K, out_dtype):
 def test_macro_prefill_sampled_rows():
     xb, w, wq = _macro_case(4096, 8192, 8192, seed=62)
     y = y_np(nv.gemm(w, x=dev_bf16(xb)))
-    rows = np.array([0, 1, 777, 2048, 4095])
+    # the first and last rows plus 256 seeded ones, as for the tensor-scale
+    # prefill
+    rows = np.concatenate([[0, 4095], np.random.default_rng(62).choice(np.arange(1, 4095), 256, replace=False)])
     ref = oracle.gemm_w4a4_macro(oracle.nvfp4_encode_macro(xb), wq, rows=rows)
     ok, worst = row_tolerance_ok(y[rows], ref, out_bf16=True)
     assert ok, worst

@@ -64,6 +64,21 @@ CUresult make_tmap_2d_u8_swizzle(CUtensorMap *map, const void *base, uint64_t in
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+CUresult make_tmap_scale_atoms(CUtensorMap *map, const void *scales, uint64_t groups, uint64_t k64,
+                               uint32_t box_k64, uint32_t box_groups)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return CUDA_ERROR_NOT_FOUND;
+    cuuint64_t dims[4] = {128, 4, k64, groups};
+    cuuint64_t strides[3] = {128, 512, k64 * 512};
+    cuuint32_t box[4] = {128, 4, box_k64, box_groups};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(scales), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 CUresult make_tmap_2d_u8(CUtensorMap *map, const void *base, uint64_t inner_bytes, uint64_t rows,
                          uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128)
 {

@@ -103,6 +103,7 @@ struct Cfg {
 struct Params {
     CUtensorMap tmap_a;  // MMA operand A codes [a_rows][K/2]
     CUtensorMap tmap_b;  // MMA operand B codes
+    CUtensorMap tmap_sfb; // B's scale atoms, [groups][k64][4][128 B]: one box per stage
     const uint8_t *a_codes; // indexed grouped rows are copied from here with cp.async
     const uint8_t *sfa;  // tiled scales of A (row-padded to 128)
     const uint8_t *sfb;  // tiled scales of B
@@ -523,13 +524,11 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
             const int brow0 = GROUPED ? tt.expert * (int)p.b_rows + tt.tile_n * BN : tt.tile_n * BN;
             const int bt0 = brow0 / 128;
             if (expect) {
-                int nb_loaded = 0;
-#pragma unroll
-                for (int h = 0; h < C::NB; ++h)
-                    nb_loaded += (bt0 + h < p.b_row_tiles) ? 1 : 0;
                 const uint32_t code_bytes =
                     C::B_BYTES + (indexed ? 0u : (uint32_t)p.a_box_rows * STAGE_K_BYTES);
-                const uint32_t sf_bytes = (nb_loaded + (indexed ? 0 : 1)) * nk * 512;
+                // A's atoms of the stage's K blocks; B's box is always whole
+                // (atoms past K or past the weight rows read as zero)
+                const uint32_t sf_bytes = (indexed ? 0u : (uint32_t)nk * 512u) + (uint32_t)C::SFB_BYTES;
                 if (lane == 0)
                     mbar_arrive_expect_tx(&full[st], code_bytes);
                 else if (lane == 1)
@@ -547,13 +546,14 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                 tma_load_2d(op == 0 ? sA : sB, op == 0 ? &p.tmap_a : &p.tmap_b, kb * STAGE_K_BYTES,
                             op == 0 ? arow : brow0, &full[st],
                             op == 0 ? (uint32_t)p.a_box_rows * STAGE_K_BYTES : (uint32_t)C::B_BYTES);
-            } else if ((op == 2 && !indexed && part_a) ||
-                       (op >= 3 && op < 3 + C::NB && bt0 + op - 3 < p.b_row_tiles && part_b)) {
+            } else if (op == 2 && !indexed && part_a) {
                 const int64_t a_atom_row = GROUPED ? tt.row0 / BM : tt.tile_m;
-                const uint8_t *src = op == 2 ? p.sfa + ((size_t)a_atom_row * p.k64 + 4 * kb) * 512
-                                             : p.sfb + ((size_t)(bt0 + op - 3) * p.k64 + 4 * kb) * 512;
-                if (in_span(NV4_SITE(0), op == 2 ? p.sp_sfa : p.sp_sfb, src, nk * 512))
-                    bulk_load(op == 2 ? sSFA : sSFB + (op - 3) * 2048, src, nk * 512, &sf_full[st]);
+                const uint8_t *src = p.sfa + ((size_t)a_atom_row * p.k64 + 4 * kb) * 512;
+                if (in_span(NV4_SITE(0), p.sp_sfa, src, nk * 512))
+                    bulk_load(sSFA, src, nk * 512, &sf_full[st]);
+            } else if (op == 3 && part_b) {
+                // both 128-row groups' atoms of the stage in one copy
+                tma_load_4d(sSFB, &p.tmap_sfb, 0, 0, 4 * kb, bt0, &sf_full[st], (uint32_t)C::SFB_BYTES);
             }
         };
         // Before waiting for the previous grid (programmatic dependent
@@ -565,6 +565,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
         if (lane == 0) {
             prefetch_tmap(&p.tmap_a);
             prefetch_tmap(&p.tmap_b);
+            prefetch_tmap(&p.tmap_sfb);
         }
         int n_early = 0;
         if (!GROUPED && p.b_early) {
@@ -704,7 +705,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a4_kernel(const __grid_constant_
                 if (indexed) // gathered activation scales were written by cp.async
                     fence_proxy_async_smem();
                 if (lane == 0) {
-                    // atoms of B row groups past the weight rows hold stale
+                    // atoms of B row groups past the weight rows read as zero
                     // bytes; they only feed output columns that are never stored
                     const int nk = min(4, p.k64 - 4 * kb);
                     const uint8_t *sSFA = smem + stage * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
@@ -1292,6 +1293,10 @@ cudaError_t launch_w4a4_dense(const DenseGemmArgs &g, cudaStream_t stream)
                         STAGE_K_BYTES, (uint32_t)bn, true);
     if (r != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
+    r = make_tmap_scale_atoms(&p.tmap_sfb, g.b_scales, (uint64_t)ceil_div(g.b_rows, 128), (uint64_t)k64, 4,
+                              (uint32_t)(bn / 128));
+    if (r != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
     p.a_codes = g.a_codes;
     p.sfa = g.a_scales;
     p.sfb = g.b_scales;
@@ -1359,6 +1364,10 @@ cudaError_t launch_w4a4_grouped(const GroupedGemmArgs &g, cudaStream_t stream)
         return cudaErrorInvalidValue;
     r = make_tmap_2d_u8(&p.tmap_b, g.w_codes, (uint64_t)(g.K / 2), (uint64_t)(g.E * g.N), (uint64_t)(g.K / 2),
                         STAGE_K_BYTES, (uint32_t)bn, true);
+    if (r != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    r = make_tmap_scale_atoms(&p.tmap_sfb, g.w_scales, (uint64_t)ceil_div(g.E * g.N, 128), (uint64_t)k64, 4,
+                              (uint32_t)(bn / 128));
     if (r != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     p.a_codes = g.a_codes;

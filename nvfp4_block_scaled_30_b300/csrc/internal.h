@@ -265,6 +265,11 @@ CUresult make_tmap_2d_u8(CUtensorMap *map, const void *base, uint64_t inner_byte
 CUresult make_tmap_2d_u8_swizzle(CUtensorMap *map, const void *base, uint64_t inner_bytes, uint64_t rows,
                                  uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows,
                                  CUtensorMapSwizzle swizzle);
+// The MMA-tiled scale atoms of a [groups x 128 rows][k64 x 64] tensor viewed
+// as a 4-D tensor [groups][k64][4][128 bytes]: one box of box_k64 atoms of
+// box_groups consecutive row groups lands as [group][atom][512 bytes].
+CUresult make_tmap_scale_atoms(CUtensorMap *map, const void *scales, uint64_t groups, uint64_t k64,
+                               uint32_t box_k64, uint32_t box_groups);
 
 
 } // namespace nv4

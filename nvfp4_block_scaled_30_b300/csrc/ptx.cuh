@@ -163,6 +163,21 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// 4-D tiled TMA load (coordinates innermost first); x must be a multiple of
+// 16 bytes.
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int32_t x, int32_t y, int32_t z,
+                                            int32_t w, uint64_t *bar, uint32_t box_bytes)
+{
+    if (!(in_dyn_smem(NV4_SITE(1), smem_u32(dst), box_bytes) && aligned_to(NV4_SITE(1), smem_u32(dst), 128) &&
+          aligned_to(NV4_SITE(1), (uint32_t)x, 16)))
+        return;
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // tma_load_2d with an L2 cache policy.
 __device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *map, int32_t x, int32_t y,
                                                  uint64_t *bar, uint32_t box_bytes, uint64_t policy)

@@ -46,8 +46,8 @@ FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6400.0, 1800.0
 # DRAM bytes (read + write) per launch of the roofline kernel, from one ncu
 # capture of the current kernel (profiles/ holds the capture and command);
 # None until a capture of the current kernel exists.
-TRAFFIC = {"decode": 135.79e6,    # w4a4_kernel<256,false,16>, 8x28672x8192: 132.32 MB read + 3.47 MB written
-           "prefill": 352.69e6}   # w4a4_kernel<256,false>, 4096x28672x8192: 151.32 MB read + 201.36 MB written
+TRAFFIC = {"decode": 135.40e6,    # w4a4_kernel<256,false,16>, 8x28672x8192: 132.32 MB read + 3.08 MB written
+           "prefill": None}       # w4a4_kernel<256,false>: counters not yet retaken since the one-copy scale fetch
 
 
 def peaks():

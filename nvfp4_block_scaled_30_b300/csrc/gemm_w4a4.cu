@@ -13,10 +13,11 @@
 //
 // Design (one CTA per SM, persistent, warp-specialised, 384 threads):
 //   warp 0      producer: A/B code tiles by TMA (128-byte rows = 256 FP4,
-//               128-byte swizzle) and the compact 512-byte scale atoms by bulk
-//               copies, into a STAGES-deep ring; each copy of a stage is
-//               issued by its own lane (one thread's copies are served in
-//               order, different threads' copies in parallel).
+//               128-byte swizzle), A's compact 512-byte scale atoms by a bulk
+//               copy and B's (the stage's atoms of both 128-row groups) by
+//               one 4-D TMA copy, into a STAGES-deep ring; each copy of a
+//               stage is issued by its own lane (one thread's copies are
+//               served in order, different threads' copies in parallel).
 //   warp 1      allocates TMEM; lane 0 issues tcgen05.mma kind::mxf4nvf4
 //               (M = 128, N = BN, K = 64; 4 per stage) and tcgen05.commit.
 //   warp 2      scale warp: moves each stage's compact scale atoms from the
@@ -30,12 +31,14 @@
 //               engine, limits a stage.
 //   warps 3-10  epilogue: tcgen05.ld of the FP32 accumulator into registers,
 //               release of the accumulator, then alpha scale and BF16/FP32
-//               stores.  Stream-K partial tiles: a CTA whose range starts
-//               inside a tile parks its FP32 partial in its own workspace
-//               slot and raises its flag; the CTA holding the tile's first
-//               K stages (normally the last to finish it) adds the slots of
-//               the flagged contributors to its registers and stores the
-//               tile.
+//               stores (with 32-byte aligned rows, whole 64-byte row runs:
+//               each warp exchanges its 32 rows' words by shuffles so every
+//               256-bit store covers 16 rows).  Stream-K partial tiles: a
+//               CTA whose range starts inside a tile parks its FP32 partial
+//               in its own workspace slot and raises its flag; the CTA
+//               holding the tile's first K stages (its last work item)
+//               parks its accumulator in the idle ring, adds the flagged
+//               contributors' slots and stores the tile.
 //   warp 11     grouped with routing indices only, gather warp: the
 //               activation rows of a work item (gathered through the
 //               indices) and their scale bytes by 16- and 4-byte cp.async
